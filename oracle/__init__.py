@@ -1,0 +1,124 @@
+"""Greedy IoU NMS oracle (TEST INFRASTRUCTURE ONLY).
+
+A plain, slow, single-threaded CPU implementation of greedy hard NMS, written
+in C (``nms_oracle.c``) and loaded with ctypes.  Only ``tests/``,
+``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline / reference leg may
+import this package.  It shares no code with ``greedy_iou_nms_gb300``.
+
+Every function restates the method as the pages define it; see the header of
+``nms_oracle.c`` for the citations and the readings taken where the pages are
+silent.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "nms_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "liboracle.so")
+
+# -ffp-contract=off: gcc contracts a*b+c into an FMA by default on aarch64,
+# which would change the binary32 rounding of the canonical IoU.
+CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library with gcc (idempotent)."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        f32p = ctypes.POINTER(ctypes.c_float)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        u64p = ctypes.POINTER(ctypes.c_uint64)
+        lib.oracle_iou.argtypes = [f32p, f32p]
+        lib.oracle_iou.restype = ctypes.c_float
+        lib.oracle_nms.argtypes = [f32p, f32p, ctypes.c_int64, i32p, i64p, ctypes.c_int32,
+                                   ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_int32,
+                                   i64p, i64p]
+        lib.oracle_nms.restype = ctypes.c_int64
+        lib.oracle_score_order.argtypes = [f32p, i64p, ctypes.c_int64]
+        lib.oracle_score_order.restype = None
+        lib.oracle_mask.argtypes = [f32p, ctypes.c_int64, ctypes.c_float, u64p]
+        lib.oracle_mask.restype = None
+        _lib = lib
+    return _lib
+
+
+def _ptr(a, ctype):
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def iou(a, b) -> np.float32:
+    """Canonical binary32 IoU of two xyxy boxes."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    b = np.ascontiguousarray(b, dtype=np.float32)
+    return np.float32(_load().oracle_iou(_ptr(a, ctypes.c_float), _ptr(b, ctypes.c_float)))
+
+
+def score_order(scores) -> np.ndarray:
+    """Greedy visiting order: stable descending score, NaN last."""
+    s = np.ascontiguousarray(scores, dtype=np.float32)
+    idx = np.arange(s.shape[0], dtype=np.int64)
+    _load().oracle_score_order(_ptr(s, ctypes.c_float), _ptr(idx, ctypes.c_int64), s.shape[0])
+    return idx
+
+
+def nms(boxes, scores, iou_thr, *, class_ids=None, batch_offsets=None, score_thr=None,
+        max_out=0):
+    """Greedy NMS.  Returns (keep, counts) exactly as the library lays them out:
+    image b's kept indices sit at keep[b*max_out] (max_out > 0) or at
+    keep[batch_offsets[b]] (no cap); counts[b] is their number.  For a single
+    image, keep[:counts[0]] is the answer."""
+    bx = np.ascontiguousarray(boxes, dtype=np.float32).reshape(-1, 4)
+    sc = np.ascontiguousarray(scores, dtype=np.float32).reshape(-1)
+    n = sc.shape[0]
+    assert bx.shape[0] == n
+    cls = None if class_ids is None else np.ascontiguousarray(class_ids, dtype=np.int32)
+    off = None if batch_offsets is None else np.ascontiguousarray(batch_offsets, dtype=np.int64)
+    batch = 1 if off is None else off.shape[0] - 1
+    cap = batch * max_out if max_out > 0 else n
+    keep = np.full(max(cap, 1), -1, dtype=np.int64)
+    counts = np.zeros(batch, dtype=np.int64)
+    total = _load().oracle_nms(
+        _ptr(bx, ctypes.c_float), _ptr(sc, ctypes.c_float), n,
+        None if cls is None else _ptr(cls, ctypes.c_int32),
+        None if off is None else _ptr(off, ctypes.c_int64), batch,
+        float(np.float32(iou_thr)), 0 if score_thr is None else 1,
+        float(np.float32(score_thr if score_thr is not None else 0.0)), int(max_out),
+        _ptr(keep, ctypes.c_int64), _ptr(counts, ctypes.c_int64))
+    if total < 0:
+        raise ValueError("oracle_nms: invalid arguments")
+    return keep[:cap], counts
+
+
+def nms_single(boxes, scores, iou_thr, *, max_out=0, score_thr=None) -> np.ndarray:
+    """Single image, single class: the kept indices in score order."""
+    keep, counts = nms(boxes, scores, iou_thr, max_out=max_out, score_thr=score_thr)
+    return keep[: counts[0]].copy()
+
+
+def mask(boxes_sorted, iou_thr) -> np.ndarray:
+    """Row-major [n][ceil(n/64)] uint64 suppression bitmask of score-sorted boxes."""
+    bx = np.ascontiguousarray(boxes_sorted, dtype=np.float32).reshape(-1, 4)
+    n = bx.shape[0]
+    W = (n + 63) // 64
+    m = np.zeros((n, max(W, 1)), dtype=np.uint64)
+    _load().oracle_mask(_ptr(bx, ctypes.c_float), n, float(np.float32(iou_thr)),
+                        _ptr(m, ctypes.c_uint64))
+    return m[:, :W]

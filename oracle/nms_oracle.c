@@ -1,0 +1,165 @@
+/*
+ * Greedy IoU NMS oracle: TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT PATH.
+ *
+ * Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline / reference
+ * leg may load, call or run this code.  It shares no code, header, table or
+ * helper with the CUDA library in greedy_iou_nms_gb300/csrc; the two never
+ * import each other.
+ *
+ * What it computes is the plain definition of greedy hard NMS, written out as
+ * a slow loop with no bitmask, no tiling and no reordering:
+ *
+ *   "NMS CUDA代码学习" (leetCUDA 14-nms), intro and section 算法与数据流:
+ *     boxes are visited from the highest score to the lowest (stable sort, so
+ *     equal scores keep input order); a box is dropped when it overlaps an
+ *     already-kept box with IoU strictly greater than the threshold; the
+ *     survivors are returned as original input indices (section "host 侧:
+ *     zeros、映射回原索引、返回类型": int64 indices, in score order).
+ *
+ *   "YOLOv5后处理GPU移植实战", section 2.2 稳定性增强方案: among equal scores the
+ *     lower index has priority, and suppression only happens between boxes of
+ *     the same class.
+ *
+ * Readings where the pages are silent (each one also listed in the design doc):
+ *   - IoU on continuous xyxy coordinates, no "+1"; every step in IEEE binary32
+ *     with round-to-nearest-even, in the fixed order of oracle_iou() below, no
+ *     fused multiply-add (this file must be built with -ffp-contract=off and
+ *     without -ffast-math), no flush-to-zero.  max/min are C fmaxf/fminf.
+ *   - The threshold is an fp32 value and the test is iou > thr (strict).
+ *   - Score order: descending; -0 equals +0; NaN scores go after every other
+ *     score (including -inf); ties (and NaNs among themselves) by lower index.
+ *   - Optional pre-filter keeps score > score_thr (strict; NaN fails).
+ *   - max_out caps the number of outputs per image (first max_out kept in score
+ *     order); max_out <= 0 means no cap.
+ *   - Batched class-aware mode: images are the ranges
+ *     [batch_offsets[b], batch_offsets[b+1]); within an image, boxes suppress
+ *     only boxes of the same class; the output of image b is written at
+ *     keep[b * max_out] when max_out > 0, else at keep[batch_offsets[b]], in
+ *     score order across classes, and counts[b] holds its length.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Canonical IoU of two xyxy boxes, in the fixed binary32 operation order. */
+float oracle_iou(const float* a, const float* b)
+{
+    float area_a = (a[2] - a[0]) * (a[3] - a[1]);
+    float area_b = (b[2] - b[0]) * (b[3] - b[1]);
+    float xx1 = fmaxf(a[0], b[0]);
+    float yy1 = fmaxf(a[1], b[1]);
+    float xx2 = fminf(a[2], b[2]);
+    float yy2 = fminf(a[3], b[3]);
+    float w = fmaxf(xx2 - xx1, 0.0f);
+    float h = fmaxf(yy2 - yy1, 0.0f);
+    float inter = w * h;
+    float uni = (area_a + area_b) - inter;
+    return inter / uni;
+}
+
+/* Score order used for sorting: returns <0 when candidate (sa, ia) comes
+ * before (sb, ib).  Descending score, NaN last, ties by lower index. */
+static int score_before(float sa, int64_t ia, float sb, int64_t ib)
+{
+    int na = isnan(sa), nb = isnan(sb);
+    if (na != nb) return na ? 1 : -1;
+    if (!na) {
+        if (sa > sb) return -1;
+        if (sa < sb) return 1;
+    }
+    if (ia < ib) return -1;
+    if (ia > ib) return 1;
+    return 0;
+}
+
+static const float* g_scores; /* comparator context (single-threaded oracle) */
+
+static int cmp_index(const void* pa, const void* pb)
+{
+    int64_t ia = *(const int64_t*)pa, ib = *(const int64_t*)pb;
+    return score_before(g_scores[ia], ia, g_scores[ib], ib);
+}
+
+/* Sort idx[0..m) into greedy visiting order (stable descending score). */
+void oracle_score_order(const float* scores, int64_t* idx, int64_t m)
+{
+    g_scores = scores;
+    qsort(idx, (size_t)m, sizeof(int64_t), cmp_index);
+}
+
+/*
+ * Greedy NMS over one image [lo, hi) of the input.
+ * Writes kept original indices (score order) to out, returns their number.
+ * order/kept are caller-provided scratch of at least hi-lo entries.
+ */
+static int64_t greedy_image(const float* boxes, const float* scores, const int32_t* class_ids,
+                            int64_t lo, int64_t hi, float iou_thr, int use_score_thr,
+                            float score_thr, int32_t max_out, int64_t* order, int64_t* out)
+{
+    int64_t m = 0;
+    for (int64_t i = lo; i < hi; ++i)
+        if (!use_score_thr || scores[i] > score_thr) order[m++] = i;
+    oracle_score_order(scores, order, m);
+
+    int64_t nkept = 0;
+    for (int64_t p = 0; p < m; ++p) {
+        int64_t i = order[p];
+        int suppressed = 0;
+        for (int64_t q = 0; q < nkept && !suppressed; ++q) {
+            int64_t k = out[q];
+            if (class_ids && class_ids[k] != class_ids[i]) continue;
+            if (oracle_iou(boxes + 4 * k, boxes + 4 * i) > iou_thr) suppressed = 1;
+        }
+        if (suppressed) continue;
+        out[nkept++] = i;
+        if (max_out > 0 && nkept == max_out) break;
+    }
+    return nkept;
+}
+
+/*
+ * Full oracle entry.  boxes: [n][4] xyxy fp32; scores: [n]; class_ids: [n] or
+ * NULL (one class); batch_offsets: [batch+1] or NULL (one image, batch must be
+ * 1).  keep must hold batch*max_out entries when max_out > 0, else n.
+ * counts: [batch].  Returns the total number of kept boxes, or -1 on bad input.
+ */
+int64_t oracle_nms(const float* boxes, const float* scores, int64_t n,
+                   const int32_t* class_ids, const int64_t* batch_offsets, int32_t batch,
+                   float iou_thr, int use_score_thr, float score_thr, int32_t max_out,
+                   int64_t* keep, int64_t* counts)
+{
+    if (n < 0 || batch < 1) return -1;
+    if (!batch_offsets && batch != 1) return -1;
+    int64_t* order = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    if (!order) return -1;
+    int64_t total = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        int64_t lo = batch_offsets ? batch_offsets[b] : 0;
+        int64_t hi = batch_offsets ? batch_offsets[b + 1] : n;
+        if (lo < 0 || hi < lo || hi > n) { free(order); return -1; }
+        int64_t base = (max_out > 0) ? (int64_t)b * max_out : lo;
+        counts[b] = greedy_image(boxes, scores, class_ids, lo, hi, iou_thr, use_score_thr,
+                                 score_thr, max_out, order, keep + base);
+        total += counts[b];
+    }
+    free(order);
+    return total;
+}
+
+/*
+ * Suppression bitmask of boxes that are already in score order, as the pages
+ * define it ("NMS CUDA代码学习", section Phase 1): bit (j mod 64) of word
+ * j/64 in row i is set iff j > i and IoU(i, j) > thr.  Row-major [n][W]
+ * uint64 words, W = ceil(n/64), every word written (zero where no bit).
+ * Used only by tests that check the library's mask entry point.
+ */
+void oracle_mask(const float* boxes_sorted, int64_t n, float iou_thr, uint64_t* mask)
+{
+    int64_t W = (n + 63) / 64;
+    memset(mask, 0, sizeof(uint64_t) * (size_t)(n * W));
+    for (int64_t i = 0; i < n; ++i)
+        for (int64_t j = i + 1; j < n; ++j)
+            if (oracle_iou(boxes_sorted + 4 * i, boxes_sorted + 4 * j) > iou_thr)
+                mask[i * W + j / 64] |= (uint64_t)1 << (j % 64);
+}

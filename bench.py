@@ -1,0 +1,428 @@
+#!/usr/bin/env python3
+"""Benchmark of greedy IoU NMS on GB300: one JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gbnms|reference]
+                    [--workload single_n8192] [--no-cpu-baseline]
+
+A step is one nms_run call (the whole hot path: sort + gather, IoU mask,
+resolve + map back) over the headline workload: N=8192 boxes, 300 clusters in
+1280x1280, jitter N(0,15), w,h ~ U(8,200), scores Beta(2,5), IoU threshold
+0.5.  Inputs are resident in HBM when the timed region starts; L2 is flushed
+(a 256 MiB write) before every timed step, outside the timed events.
+`value` is boxes/s over all ranks (weak scaling: each rank runs its own copy).
+`e2e` is the same metric through nms_run with the host buffers: the pinned
+host->device copy of boxes and scores and the device->host read of the keep
+list and count are inside the timed region.
+
+--impl reference times the CPU oracle (plain C greedy NMS, one thread) on the
+same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from greedy_iou_nms_gb300 import workloads as W  # noqa: E402
+
+METRIC = "NMS µs/call & boxes/s at N=8192; IoU Gpairs/s and mask GB/s vs roofline"
+UNIT = "boxes/s"
+# FP32 operations of one canonical IoU test (4 min/max, 2 sub, 2 clamp, 1 mul,
+# 1 add, 1 sub, 1 div, 1 compare): the algorithmic work per pair.
+OPS_PER_PAIR = 13
+SMS = 152
+FP32_LANES_PER_SM = 128
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "sm_max_mhz": 2070.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_oracle_run(wl, budget_s: float):
+    """Time the oracle (as it stands, one thread) on full copies of the workload
+    until about budget_s seconds have passed.  Returns (boxes/s, reps, seconds)."""
+    import oracle
+    oracle.build()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.nms(wl.boxes, wl.scores, wl.iou_thr, class_ids=wl.class_ids,
+                   batch_offsets=wl.batch_offsets, score_thr=wl.score_thr, max_out=wl.max_out)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s:
+            break
+    return wl.n * reps / dt, reps, dt
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    wl = W.make(args.workload, 0)
+    per_step, reps_total = [], 0
+    # Each timed step is one full oracle NMS of the workload (a bounded sample:
+    # the whole --warmup/--steps run stays within a few minutes).
+    for _ in range(args.warmup):
+        cpu_oracle_run(wl, 0.0)
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        cpu_oracle_run(wl, 0.0)
+        per_step.append(time.perf_counter() - t0)
+        reps_total += 1
+    ms = 1000 * statistics.mean(per_step)
+    value = wl.n / (ms / 1000)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "n": wl.n, "iou_thr": wl.iou_thr},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{reps_total} full runs of {wl.name} (one per step)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def _algorithmic_resolve_bytes(wl):
+    """Mask bytes the resolve must read: for every kept row i, its words from
+    floor(i/64) to the end of the row (the triangle part to the right), plus
+    the diagonal word of every other row."""
+    import oracle
+    keep = oracle.nms_single(wl.boxes, wl.scores, wl.iou_thr, max_out=wl.max_out)
+    order = oracle.score_order(wl.scores)
+    pos = np.empty(wl.n, np.int64)
+    pos[order] = np.arange(wl.n)
+    kp = pos[keep]
+    Wn = (wl.n + 63) // 64
+    row_words = (Wn - kp // 64).sum()
+    return int(8 * (row_words + wl.n)), len(keep)
+
+
+def run_gbnms(args):
+    import torch
+    import greedy_iou_nms_gb300 as g
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    g.build()
+    g.load()
+
+    wl = W.make(args.workload, 0)
+    if wl.class_ids is not None or wl.batch_offsets is not None:
+        raise SystemExit("bench.py times the single-image path; use a single_* or stress_* workload")
+    n = wl.n
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    boxes = torch.from_numpy(wl.boxes).to(dev)
+    scores = torch.from_numpy(wl.scores).to(dev)
+    cap = g.keep_capacity(n, None, wl.max_out)
+    keep = torch.empty(max(cap, 1), dtype=torch.int64, device=dev)
+    counts = torch.empty(1, dtype=torch.int64, device=dev)
+    status = torch.empty(1, dtype=torch.int32, device=dev)
+    ws = g.Workspace(n, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    score_thr = -math.inf if wl.score_thr is None else wl.score_thr
+
+    def step():
+        st = g.nms_run(boxes.data_ptr(), scores.data_ptr(), n, 0, 0, 0, 0, wl.iou_thr, score_thr,
+                       wl.max_out, keep.data_ptr(), cap, counts.data_ptr(), status.data_ptr(),
+                       ws.ptr, ws.bytes, sp)
+        if st != g.NMS_OK:
+            raise g.NmsError(st, "nms_run")
+
+    for _ in range(max(args.warmup, 3)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    got = keep[: int(counts.item())].cpu().numpy()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for e0, e1 in evs:
+        flush.fill_(1)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    total_ms = sum(step_ms)
+    clocks = sampler.stop()
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * n * args.steps / (total_ms / 1000)
+
+    # ---- per-kernel durations: the same mask and resolve kernels launched
+    # alone through their entry points, on the same stream, L2 flushed before
+    # each launch.
+    order = np.argsort(-wl.scores.astype(np.float64), kind="stable")  # input prep only
+    bs = torch.from_numpy(np.ascontiguousarray(wl.boxes[order])).to(dev)
+    ldw = g.nms_mask_row_words(n)
+    mask = torch.zeros((n, ldw), dtype=torch.int64, device=dev)
+    kp = torch.empty(max(cap, 1), dtype=torch.int64, device=dev)
+    kc = torch.empty(1, dtype=torch.int64, device=dev)
+
+    def time_launch(fn, reps):
+        ts = []
+        for _ in range(reps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ts)
+
+    def mask_launch():
+        assert g.nms_iou_mask(bs.data_ptr(), n, wl.iou_thr, mask.data_ptr(), mask.numel(), sp) == 0
+
+    def resolve_launch():
+        assert g.nms_resolve_mask(mask.data_ptr(), n, 0, wl.max_out, kp.data_ptr(), kc.data_ptr(),
+                                  ws.ptr, ws.bytes, sp) == 0
+
+    for _ in range(3):
+        mask_launch()
+        resolve_launch()
+    reps = max(args.steps, 10)
+    mask_ms = time_launch(mask_launch, reps)
+    resolve_ms = time_launch(resolve_launch, reps)
+
+    # ---- end to end through nms_run with host buffers
+    hb = torch.from_numpy(wl.boxes).pin_memory()
+    hs = torch.from_numpy(wl.scores).pin_memory()
+    hk = torch.empty(max(cap, 1), dtype=torch.int64).pin_memory()
+    hc = torch.empty(1, dtype=torch.int64).pin_memory()
+    db = torch.empty_like(boxes)
+    dsc = torch.empty_like(scores)
+
+    def e2e_step():
+        db.copy_(hb, non_blocking=True)
+        dsc.copy_(hs, non_blocking=True)
+        st = g.nms_run(db.data_ptr(), dsc.data_ptr(), n, 0, 0, 0, 0, wl.iou_thr, score_thr,
+                       wl.max_out, keep.data_ptr(), cap, counts.data_ptr(), status.data_ptr(),
+                       ws.ptr, ws.bytes, sp)
+        assert st == 0
+        hc.copy_(counts, non_blocking=True)
+        hk.copy_(keep, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_t = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_t.append(a.elapsed_time(b))
+    e2e_ms = statistics.mean(e2e_t)
+    h2d = hb.numel() * 4 + hs.numel() * 4
+    d2h = hk.numel() * 8 + hc.numel() * 8
+
+    if rank != 0:
+        return 0
+
+    import oracle
+    exp = oracle.nms_single(wl.boxes, wl.scores, wl.iou_thr, max_out=wl.max_out)
+    parity = bool(got.tolist() == exp.tolist())
+
+    peaks, peak_kind = _peaks()
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    alu_peak_tops = SMS * FP32_LANES_PER_SM * sm_max * 1e6 / 1e12
+    pairs = n * (n - 1) // 2
+    mask_tops = OPS_PER_PAIR * pairs / (mask_ms / 1000) / 1e12
+    Wn = (n + 63) // 64
+    mask_bytes = 8 * sum(Wn - i // 64 for i in range(0, n, 1))  # written triangle words
+    resolve_bytes, _ = _algorithmic_resolve_bytes(wl)
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    sort_ms = max(ms_per_step - mask_ms - resolve_ms, 0.0)
+    kernels = {"rank_sort_gather_ms_est": sort_ms, "iou_mask_ms": mask_ms,
+               "resolve_ms": resolve_ms}
+    dominant = max(("iou_mask", mask_ms), ("resolve", resolve_ms), key=lambda x: x[1])[0]
+    traffic = _ncu_traffic(dominant)
+    if dominant == "iou_mask":
+        roof = {"kernel": "iou_mask_kernel", "bound": "alu", "achieved": mask_tops,
+                "peak": alu_peak_tops, "unit": "TFLOP/s", "frac": mask_tops / alu_peak_tops,
+                "traffic": traffic,
+                "note": f"FP32 ops, {OPS_PER_PAIR}/pair x {pairs} pairs; peak = {SMS} SMs x "
+                        f"{FP32_LANES_PER_SM} lanes x {sm_max:.0f} MHz (max clock)"}
+    else:
+        ach = resolve_bytes / (resolve_ms / 1000) / 1e9
+        roof = {"kernel": "resolve_single_kernel", "bound": "hbm", "achieved": ach, "peak": hbm,
+                "unit": "GB/s", "frac": ach / hbm, "traffic": traffic,
+                "note": f"algorithmic mask bytes read {resolve_bytes}; peak {peak_kind}"}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, reps_cpu, secs = cpu_oracle_run(wl, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{reps_cpu} full runs of {wl.name} in {secs:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "n": n, "iou_thr": wl.iou_thr, "max_out": wl.max_out,
+                   "l2": "flushed (256 MiB write) before every timed step",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_call": 1000 * ms_per_step,
+        "gpairs_per_s": pairs / (ms_per_step / 1000) / 1e9,
+        "mask_gpairs_per_s": pairs / (mask_ms / 1000) / 1e9,
+        "mask_gbs": mask_bytes / (mask_ms / 1000) / 1e9,
+        "mask_hbm_frac": mask_bytes / (mask_ms / 1000) / 1e9 / hbm,
+        "kernels": kernels,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": n / (e2e_ms / 1000), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+        "parity_vs_oracle": parity,
+        "peaks": peak_kind,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+KERNEL_SOURCES = {"iou_mask": "k_mask.cu", "resolve": "k_resolve.cu"}
+
+
+def kernel_source_sha(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "greedy_iou_nms_gb300", "csrc")
+    for name in (KERNEL_SOURCES[kernel], "common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(kernel):
+    """DRAM bytes per launch of `kernel` (dram__bytes_read.sum + write.sum) from
+    the committed ncu summary, or None when absent or when the kernel source
+    changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d or d.get("src_sha") != kernel_source_sha(kernel):
+        return None
+    return d.get("bytes_per_launch")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gbnms", choices=["gbnms", "reference"])
+    ap.add_argument("--workload", default=W.HEADLINE)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gbnms(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,234 @@
+"""Greedy IoU NMS for GB300: thin Python binding of the libgbnms C ABI.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+only marshals arguments.  PyTorch provides device memory and the stream.  The
+raw entry points carry the same names as the C functions in include/gbnms.h
+(`nms_run`, `nms_workspace_size`, `nms_status_string`, `nms_iou_mask`,
+`nms_mask_row_words`) and take device pointers as integers.  `nms()` and
+`iou_mask()` are the tensor-level conveniences.
+
+There is no CPU fallback: if the shared library is missing or cannot load,
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_build", "libgbnms.so")
+
+NMS_OK = 0
+NMS_ERR_INVALID_ARG = 1
+NMS_ERR_WORKSPACE = 2
+NMS_ERR_CAPACITY = 3
+NMS_ERR_CUDA = 4
+NMS_ERR_TIMEOUT = 5
+NMS_MAX_SINGLE_N = 1 << 18
+
+EXPORTED = ("nms_status_string", "nms_workspace_size", "nms_run", "nms_mask_row_words",
+            "nms_iou_mask", "nms_resolve_mask")
+
+_lib = None
+
+
+class NmsError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {nms_status_string(code)} ({code})")
+
+
+def build(force: bool = False) -> str:
+    """Compile libgbnms.so in-tree (nvcc, sm_103a)."""
+    from . import _build
+    return _build.build(force=force)
+
+
+def load():
+    """Load libgbnms.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libgbnms.so not built at {LIB_PATH}: call greedy_iou_nms_gb300.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    lib.nms_status_string.argtypes = [ctypes.c_int]
+    lib.nms_status_string.restype = ctypes.c_char_p
+    lib.nms_workspace_size.argtypes = [i64, i32, i32, ctypes.POINTER(sz)]
+    lib.nms_workspace_size.restype = ctypes.c_int
+    lib.nms_run.argtypes = [vp, vp, i64, vp, i32, vp, i32, f32, f32, i32, vp, i64, vp, vp, vp, sz, vp]
+    lib.nms_run.restype = ctypes.c_int
+    lib.nms_mask_row_words.argtypes = [i64]
+    lib.nms_mask_row_words.restype = i64
+    lib.nms_iou_mask.argtypes = [vp, i64, f32, vp, i64, vp]
+    lib.nms_iou_mask.restype = ctypes.c_int
+    lib.nms_resolve_mask.argtypes = [vp, i64, vp, i32, vp, vp, vp, sz, vp]
+    lib.nms_resolve_mask.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+# ------------------------------------------------------------- raw C entries
+
+def nms_status_string(code: int) -> str:
+    return load().nms_status_string(int(code)).decode()
+
+
+def nms_workspace_size(n: int, batch: int = 0, num_classes: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    st = load().nms_workspace_size(int(n), int(batch), int(num_classes), ctypes.byref(out))
+    if st != NMS_OK:
+        raise NmsError(st, "nms_workspace_size")
+    return int(out.value)
+
+
+def nms_mask_row_words(n: int) -> int:
+    return int(load().nms_mask_row_words(int(n)))
+
+
+def nms_run(boxes: int, scores: int, n: int, class_ids: int, num_classes: int,
+            batch_offsets: int, batch: int, iou_thr: float, score_thr: float, max_out: int,
+            keep: int, keep_cap: int, counts: int, dev_status: int, workspace: int,
+            workspace_bytes: int, stream: int) -> int:
+    """The C entry point with device addresses as ints (0 = NULL).  Returns the status code."""
+    return load().nms_run(boxes or None, scores or None, int(n), class_ids or None,
+                          int(num_classes), batch_offsets or None, int(batch), float(iou_thr),
+                          float(score_thr), int(max_out), keep or None, int(keep_cap),
+                          counts or None, dev_status or None, workspace or None,
+                          int(workspace_bytes), stream or None)
+
+
+def nms_iou_mask(boxes_sorted: int, n: int, iou_thr: float, mask: int, mask_words: int,
+                 stream: int) -> int:
+    return load().nms_iou_mask(boxes_sorted or None, int(n), float(iou_thr), mask or None,
+                               int(mask_words), stream or None)
+
+
+def nms_resolve_mask(mask: int, n: int, perm: int, max_out: int, keep: int, count: int,
+                     workspace: int, workspace_bytes: int, stream: int) -> int:
+    return load().nms_resolve_mask(mask or None, int(n), perm or None, int(max_out), keep or None,
+                                   count or None, workspace or None, int(workspace_bytes),
+                                   stream or None)
+
+
+# ----------------------------------------------------------- tensor helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def keep_capacity(n: int, batch: Optional[int], max_out: int) -> int:
+    b = 1 if batch is None else batch
+    if max_out > 0:
+        return min(n, max_out) if batch is None else b * max_out
+    return n
+
+
+class Workspace:
+    """A reusable device workspace (a torch uint8 tensor) sized for nms_run."""
+
+    def __init__(self, n: int, batch: int = 0, num_classes: int = 0, device="cuda"):
+        torch = _torch()
+        self.bytes = nms_workspace_size(n, batch, num_classes)
+        self.tensor = torch.empty(max(self.bytes, 256), dtype=torch.uint8, device=device)
+
+    @property
+    def ptr(self) -> int:
+        return self.tensor.data_ptr()
+
+
+def nms(boxes, scores, iou_thr: float, *, class_ids=None, num_classes: Optional[int] = None,
+        batch_offsets=None, score_thr: Optional[float] = None, max_out: int = 0,
+        workspace: Optional[Workspace] = None, return_counts: bool = False):
+    """Greedy IoU NMS on CUDA tensors.
+
+    boxes [n,4] fp32 xyxy and scores [n] fp32 on one CUDA device; class_ids
+    int32 [n] (optional, with num_classes), batch_offsets int64 [B+1]
+    (optional).  Returns the int64 kept indices: for one image a 1-D tensor in
+    score order; with batch_offsets a list of per-image tensors.  With
+    return_counts=True also returns the device counts tensor.  Runs on the
+    current stream and synchronises it once to read the counts.
+    """
+    torch = _torch()
+    if not (boxes.is_cuda and scores.is_cuda):
+        raise ValueError("nms: boxes and scores must be CUDA tensors")
+    boxes = boxes.contiguous()
+    scores = scores.contiguous()
+    if boxes.dtype != torch.float32 or scores.dtype != torch.float32:
+        raise ValueError("nms: boxes and scores must be float32")
+    n = scores.shape[0]
+    if boxes.shape != (n, 4):
+        raise ValueError("nms: boxes must be [n, 4]")
+    dev = boxes.device
+    cls_ptr, C = 0, 0
+    if class_ids is not None:
+        class_ids = class_ids.to(device=dev, dtype=torch.int32).contiguous()
+        C = int(num_classes) if num_classes is not None else int(class_ids.max().item()) + 1 if n else 1
+        cls_ptr = class_ids.data_ptr()
+    off_ptr, B = 0, 0
+    if batch_offsets is not None:
+        batch_offsets = batch_offsets.to(device=dev, dtype=torch.int64).contiguous()
+        B = batch_offsets.shape[0] - 1
+        off_ptr = batch_offsets.data_ptr()
+    cap = keep_capacity(n, B if batch_offsets is not None else None, max_out)
+    keep = torch.empty(max(cap, 1), dtype=torch.int64, device=dev)
+    counts = torch.empty(max(B, 1), dtype=torch.int64, device=dev)
+    status = torch.empty(1, dtype=torch.int32, device=dev)
+    ws = workspace if workspace is not None else Workspace(n, B, C, device=dev)
+    st = nms_run(boxes.data_ptr() if n else 0, scores.data_ptr() if n else 0, n, cls_ptr, C,
+                 off_ptr, B, iou_thr, -math.inf if score_thr is None else score_thr, max_out,
+                 keep.data_ptr(), cap, counts.data_ptr(), status.data_ptr(), ws.ptr, ws.bytes,
+                 torch.cuda.current_stream(dev).cuda_stream)
+    if st != NMS_OK:
+        raise NmsError(st, "nms_run")
+    cnt = counts.cpu()
+    dst = int(status.item())
+    if dst != NMS_OK:
+        raise NmsError(dst, "nms_run (device)")
+    if batch_offsets is None:
+        out = keep[: int(cnt[0])]
+    else:
+        offs = batch_offsets.cpu()
+        out = []
+        for b in range(B):
+            base = b * max_out if max_out > 0 else int(offs[b])
+            out.append(keep[base: base + int(cnt[b])])
+    return (out, counts) if return_counts else out
+
+
+def iou_mask(boxes_sorted, iou_thr: float):
+    """Suppression bitmask of score-sorted boxes: int64 tensor [n, nms_mask_row_words(n)]
+    holding the uint64 words (bit j%64 of word j//64 of row i: j > i and IoU > thr).
+    Words left of each row's diagonal tile are zero here."""
+    torch = _torch()
+    boxes_sorted = boxes_sorted.contiguous()
+    n = boxes_sorted.shape[0]
+    ldw = nms_mask_row_words(n)
+    mask = torch.zeros((n, max(ldw, 1)), dtype=torch.int64, device=boxes_sorted.device)
+    st = nms_iou_mask(boxes_sorted.data_ptr() if n else 0, n, iou_thr, mask.data_ptr(),
+                      mask.numel(), torch.cuda.current_stream(boxes_sorted.device).cuda_stream)
+    if st != NMS_OK:
+        raise NmsError(st, "nms_iou_mask")
+    return mask[:, :ldw]
+
+
+def resolve_mask(mask, max_out: int = 0, perm=None, workspace: Optional[Workspace] = None):
+    """Kept sorted positions (or perm entries) of a mask in the iou_mask layout."""
+    torch = _torch()
+    n = mask.shape[0]
+    cap = min(n, max_out) if max_out > 0 else n
+    keep = torch.empty(max(cap, 1), dtype=torch.int64, device=mask.device)
+    count = torch.empty(1, dtype=torch.int64, device=mask.device)
+    if perm is not None:
+        perm = perm.to(device=mask.device, dtype=torch.int32).contiguous()
+    ws = workspace if workspace is not None else Workspace(n, device=mask.device)
+    st = nms_resolve_mask(mask.data_ptr() if n else 0, n, perm.data_ptr() if perm is not None else 0,
+                          max_out, keep.data_ptr(), count.data_ptr(), ws.ptr, ws.bytes,
+                          torch.cuda.current_stream(mask.device).cuda_stream)
+    if st != NMS_OK:
+        raise NmsError(st, "nms_resolve_mask")
+    return keep[: int(count.item())]

@@ -1,0 +1,286 @@
+// The C ABI of include/gbnms.h: argument checks, workspace layout and the
+// launch sequence of each path.  No host synchronisation, no allocation.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gbnms {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Region offsets inside the caller's workspace.
+struct Layout {
+    size_t off[16] = {};
+    size_t total = 0;
+    int k = 0;
+    size_t add(size_t bytes)
+    {
+        size_t o = total;
+        total = align_up(total + (bytes ? bytes : 1));
+        off[k++] = o;
+        return o;
+    }
+};
+
+struct SingleLayout {
+    int64_t ldw = 0;
+    int NB = 0;  // 64-bit words of the per-row chunk bitmap
+    size_t status, m_count, cand, perm, boxes_s, rowbits, band, mask, total;
+};
+
+SingleLayout single_layout(int64_t n)
+{
+    SingleLayout s;
+    const int64_t T = (n + 255) / 256;
+    s.ldw = 4 * T;
+    s.NB = static_cast<int>((T + 63) / 64 > 0 ? (T + 63) / 64 : 1);
+    Layout L;
+    s.status = L.add(4);
+    s.m_count = L.add(4);
+    s.cand = L.add(4 * static_cast<size_t>(n));
+    s.perm = L.add(4 * static_cast<size_t>(n));
+    s.boxes_s = L.add(16 * static_cast<size_t>(n));
+    s.rowbits = L.add(8 * static_cast<size_t>(n) * static_cast<size_t>(s.NB));
+    s.band = L.add(8 * static_cast<size_t>((n + 63) / 64) * (BAND_L + 1) * 64);
+    s.mask = L.add(8 * static_cast<size_t>(n) * static_cast<size_t>(s.ldw));
+    s.total = L.total;
+    return s;
+}
+
+struct BatchedLayout {
+    size_t status, ok, seg_cnt, seg_off, seg_of, slot, cand, kept_key, kept_cnt, sorted_key,
+        sorted_box, stage, total;
+};
+
+BatchedLayout batched_layout(int64_t n, int64_t S)
+{
+    BatchedLayout b;
+    Layout L;
+    const size_t N = static_cast<size_t>(n);
+    b.status = L.add(4);
+    b.ok = L.add(4);
+    b.seg_cnt = L.add(4 * static_cast<size_t>(S));
+    b.seg_off = L.add(4 * static_cast<size_t>(S + 1));
+    b.seg_of = L.add(4 * N);
+    b.slot = L.add(4 * N);
+    b.cand = L.add(4 * N);
+    b.kept_key = L.add(8 * N);
+    b.kept_cnt = L.add(4 * static_cast<size_t>(S));
+    b.sorted_key = L.add(8 * N);
+    b.sorted_box = L.add(16 * N);
+    b.stage = L.add(8 * N);
+    b.total = L.total;
+    return b;
+}
+
+float next_up(float x) { return std::nextafter(x, INFINITY); }
+float next_down(float x) { return std::nextafter(x, -INFINITY); }
+
+// Constants of the division-free test; the bounds are proved in common.cuh.
+ThrParams make_thr(float thr)
+{
+    ThrParams p{};
+    p.thr = thr;
+    const double t = thr;
+    p.fast_ok = (t >= 0x1p-20 && t <= 0x1p20) ? 1 : 0;
+    p.k_hi = 1.0f;
+    p.k_lo = 0.0f;
+    if (p.fast_ok) {
+        const double T2 = t * (1.0 + 0x1p-21), T1 = t * (1.0 - 0x1p-21);
+        const double k2 = T2 / (1.0 + T2) * (1.0 + 0x1p-22);
+        const double k1 = T1 / (1.0 + T1) * (1.0 - 0x1p-22);
+        float f2 = static_cast<float>(k2);
+        if (static_cast<double>(f2) < k2) f2 = next_up(f2);
+        float f1 = static_cast<float>(k1);
+        if (static_cast<double>(f1) > k1) f1 = next_down(f1);
+        p.k_hi = f2;
+        p.k_lo = f1;
+    }
+    return p;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+template <typename T>
+T* at(void* base, size_t off) { return reinterpret_cast<T*>(static_cast<char*>(base) + off); }
+
+nms_status cuda_status()
+{
+    return cudaGetLastError() == cudaSuccess ? NMS_OK : NMS_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gbnms
+
+using namespace gbnms;
+
+extern "C" const char* nms_status_string(nms_status s)
+{
+    switch (s) {
+        case NMS_OK: return "NMS_OK";
+        case NMS_ERR_INVALID_ARG: return "NMS_ERR_INVALID_ARG";
+        case NMS_ERR_WORKSPACE: return "NMS_ERR_WORKSPACE";
+        case NMS_ERR_CAPACITY: return "NMS_ERR_CAPACITY";
+        case NMS_ERR_CUDA: return "NMS_ERR_CUDA";
+        case NMS_ERR_TIMEOUT: return "NMS_ERR_TIMEOUT";
+    }
+    return "NMS_ERR_UNKNOWN";
+}
+
+extern "C" nms_status nms_workspace_size(int64_t n, int32_t batch, int32_t num_classes,
+                                         size_t* bytes)
+{
+    if (!bytes || n < 0 || n > INT32_MAX || batch < 0 || num_classes < 0) return NMS_ERR_INVALID_ARG;
+    if (batch == 0 && num_classes == 0) {
+        if (n > NMS_MAX_SINGLE_N) return NMS_ERR_CAPACITY;
+        *bytes = single_layout(n).total;
+        return NMS_OK;
+    }
+    const int64_t S = static_cast<int64_t>(batch > 0 ? batch : 1) * (num_classes > 0 ? num_classes : 1);
+    if (S > INT32_MAX / 2) return NMS_ERR_INVALID_ARG;
+    *bytes = batched_layout(n, S).total;
+    return NMS_OK;
+}
+
+extern "C" int64_t nms_mask_row_words(int64_t n)
+{
+    return n <= 0 ? 0 : 4 * ((n + 255) / 256);
+}
+
+extern "C" nms_status nms_run(const float* boxes, const float* scores, int64_t n,
+                              const int32_t* class_ids, int32_t num_classes,
+                              const int64_t* batch_offsets, int32_t batch, float iou_thr,
+                              float score_thr, int32_t max_out, int64_t* keep, int64_t keep_cap,
+                              int64_t* counts, int32_t* dev_status, void* workspace,
+                              size_t workspace_bytes, void* stream)
+{
+    if (n < 0 || n > INT32_MAX) return NMS_ERR_INVALID_ARG;
+    if (std::isnan(iou_thr) || std::isnan(score_thr)) return NMS_ERR_INVALID_ARG;
+    if (n > 0 && (!boxes || !scores || !aligned(boxes, 16))) return NMS_ERR_INVALID_ARG;
+    if (!keep || !counts) return NMS_ERR_INVALID_ARG;
+    if (class_ids && num_classes < 1) return NMS_ERR_INVALID_ARG;
+    if (batch_offsets && batch < 1) return NMS_ERR_INVALID_ARG;
+    if (keep_cap < 0) return NMS_ERR_INVALID_ARG;
+    const int B = batch_offsets ? batch : 1;
+    const int C = class_ids ? num_classes : 1;
+    const bool single = !class_ids && !batch_offsets;
+    int64_t need = max_out > 0 ? static_cast<int64_t>(B) * max_out : n;
+    if (single && max_out > 0) need = n < max_out ? n : max_out;
+    if (keep_cap < need) return NMS_ERR_CAPACITY;
+    if (single && n > NMS_MAX_SINGLE_N) return NMS_ERR_CAPACITY;
+    const int64_t S64 = static_cast<int64_t>(B) * C;
+    if (S64 > INT32_MAX / 2) return NMS_ERR_INVALID_ARG;
+    size_t need_ws = 0;
+    nms_status st0 = nms_workspace_size(n, batch_offsets ? batch : 0, class_ids ? num_classes : 0, &need_ws);
+    if (st0 != NMS_OK) return st0;
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < need_ws) return NMS_ERR_WORKSPACE;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();  // clear any stale error of this runtime
+    const bool use_thr = !(std::isinf(score_thr) && score_thr < 0);
+
+    if (single) {
+        const SingleLayout L = single_layout(n);
+        int32_t* status = dev_status ? dev_status : at<int32_t>(workspace, L.status);
+        if (n == 0) {
+            cudaMemsetAsync(counts, 0, sizeof(int64_t), st);
+            cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+            return cuda_status();
+        }
+        const ThrParams p = make_thr(iou_thr);
+        int* m_count = nullptr;
+        int* cand = nullptr;
+        if (use_thr) {
+            m_count = at<int>(workspace, L.m_count);
+            cand = at<int>(workspace, L.cand);
+            launch_prefilter(scores, static_cast<int>(n), score_thr, cand, m_count, st);
+        }
+        int* perm = at<int>(workspace, L.perm);
+        float4* boxes_s = at<float4>(workspace, L.boxes_s);
+        uint64_t* mask = at<uint64_t>(workspace, L.mask);
+        uint64_t* rowbits = at<uint64_t>(workspace, L.rowbits);
+        launch_rank_sort(scores, reinterpret_cast<const float4*>(boxes), cand, m_count,
+                         static_cast<int>(n), perm, boxes_s, status, rowbits, L.NB, st);
+        uint64_t* band = at<uint64_t>(workspace, L.band);
+        launch_iou_mask(boxes_s, m_count, static_cast<int>(n), p, mask, L.ldw, rowbits, L.NB, band, st);
+        launch_resolve_single(mask, L.ldw, rowbits, L.NB, band, m_count, static_cast<int>(n), perm,
+                              max_out, keep, counts, status, st);
+        return cuda_status();
+    }
+
+    const BatchedLayout L = batched_layout(n, S64);
+    BatchedArgs a{};
+    a.boxes = reinterpret_cast<const float4*>(boxes);
+    a.scores = scores;
+    a.cls = class_ids;
+    a.C = C;
+    a.off = batch_offsets;
+    a.batch = B;
+    a.n = static_cast<int>(n);
+    a.S = static_cast<int>(S64);
+    a.use_thr = use_thr ? 1 : 0;
+    a.score_thr = score_thr;
+    a.thr = iou_thr;
+    a.max_out = max_out;
+    a.seg_cnt = at<int>(workspace, L.seg_cnt);
+    a.seg_off = at<int>(workspace, L.seg_off);
+    a.seg_of = at<int>(workspace, L.seg_of);
+    a.slot = at<int>(workspace, L.slot);
+    a.cand = at<int>(workspace, L.cand);
+    a.ok = at<int>(workspace, L.ok);
+    a.kept_key = at<uint64_t>(workspace, L.kept_key);
+    a.kept_cnt = at<int>(workspace, L.kept_cnt);
+    a.sorted_key = at<uint64_t>(workspace, L.sorted_key);
+    a.sorted_box = at<float4>(workspace, L.sorted_box);
+    a.stage = at<uint64_t>(workspace, L.stage);
+    a.keep = keep;
+    a.counts = counts;
+    a.status = dev_status ? dev_status : at<int32_t>(workspace, L.status);
+    launch_batched(a, st);
+    return cuda_status();
+}
+
+extern "C" nms_status nms_iou_mask(const float* boxes_sorted, int64_t n, float iou_thr,
+                                   uint64_t* mask, int64_t mask_words, void* stream)
+{
+    if (n < 0 || std::isnan(iou_thr)) return NMS_ERR_INVALID_ARG;
+    if (n > NMS_MAX_SINGLE_N) return NMS_ERR_CAPACITY;
+    if (n == 0) return NMS_OK;
+    if (!boxes_sorted || !mask || !aligned(boxes_sorted, 16) || !aligned(mask, 16))
+        return NMS_ERR_INVALID_ARG;
+    const int64_t ldw = nms_mask_row_words(n);
+    if (mask_words < n * ldw) return NMS_ERR_CAPACITY;
+    cudaGetLastError();
+    launch_iou_mask(reinterpret_cast<const float4*>(boxes_sorted), nullptr, static_cast<int>(n),
+                    make_thr(iou_thr), mask, ldw, nullptr, 1, nullptr,
+                    static_cast<cudaStream_t>(stream));
+    return cuda_status();
+}
+
+extern "C" nms_status nms_resolve_mask(const uint64_t* mask, int64_t n, const int32_t* perm,
+                                       int32_t max_out, int64_t* keep, int64_t* count,
+                                       void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (n < 0) return NMS_ERR_INVALID_ARG;
+    if (n > NMS_MAX_SINGLE_N) return NMS_ERR_CAPACITY;
+    if (!count || (n > 0 && (!mask || !keep || !aligned(mask, 16)))) return NMS_ERR_INVALID_ARG;
+    const SingleLayout L = single_layout(n);
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < L.total) return NMS_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();
+    if (n == 0) {
+        cudaMemsetAsync(count, 0, sizeof(int64_t), st);
+        return cuda_status();
+    }
+    uint64_t* band = at<uint64_t>(workspace, L.band);
+    launch_band_from_mask(mask, L.ldw, static_cast<int>(n), band, st);
+    launch_resolve_single(mask, L.ldw, nullptr, 1, band, nullptr, static_cast<int>(n), perm, max_out,
+                          keep, count, nullptr, st);
+    return cuda_status();
+}

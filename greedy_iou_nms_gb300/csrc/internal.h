@@ -1,0 +1,58 @@
+// Host-side launchers shared between the translation units of the library.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gbnms {
+
+struct ThrParams;
+
+void launch_prefilter(const float* scores, int n, float score_thr, int* cand, int* m_count,
+                      cudaStream_t st);
+void launch_rank_sort(const float* scores, const float4* boxes, const int* cand, const int* m_dev,
+                      int m_bound, int* perm, float4* boxes_s, int32_t* status, uint64_t* rowbits,
+                      int NB, cudaStream_t st);
+int64_t mask_tiles(int64_t n);
+void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const ThrParams& p,
+                     uint64_t* mask, int64_t ldw, uint64_t* rowbits, int NB, uint64_t* band,
+                     cudaStream_t st);
+size_t resolve_smem_bytes(int m_bound, int NB);
+void launch_band_from_mask(const uint64_t* mask, int64_t ldw, int n, uint64_t* band, cudaStream_t st);
+void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* rowbits, int NB,
+                           const uint64_t* band, const int* m_dev, int m_bound, const int* perm,
+                           int max_out, int64_t* keep, int64_t* counts, int32_t* status,
+                           cudaStream_t st);
+
+struct BatchedArgs {
+    const float4* boxes;
+    const float* scores;
+    const int32_t* cls;
+    int C;
+    const int64_t* off;
+    int batch;
+    int n;
+    int S;
+    int use_thr;
+    float score_thr;
+    float thr;
+    int max_out;
+    int* seg_cnt;
+    int* seg_off;
+    int* seg_of;
+    int* slot;
+    int* cand;
+    int* ok;
+    uint64_t* kept_key;
+    int* kept_cnt;
+    uint64_t* sorted_key;
+    float4* sorted_box;
+    uint64_t* stage;
+    int64_t* keep;
+    int64_t* counts;
+    int32_t* status;
+};
+
+void launch_batched(const BatchedArgs& a, cudaStream_t st);
+
+}  // namespace gbnms

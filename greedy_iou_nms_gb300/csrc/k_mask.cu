@@ -1,0 +1,225 @@
+// Upper-triangular IoU suppression bitmask of score-sorted boxes.
+//
+// "NMS CUDA代码学习", section Phase 1: only j > i can be suppressed by i, one
+// IoU per pair, bit k of a word always means box (word base + k) so rows stay
+// aligned (the j_base rule), and 32 IoUs fold into one word write with no
+// atomics.  "nms_kernel.cu 파일 분석 -2", sections row_start/col_start and
+// 중복 비교 제거: a 2-D tiling where tiles below the diagonal do no work, and
+// the column tile is staged in shared memory.  "Fastest Matrix NMS in the West
+// (Part 2)", section "Optimization 1: tile the IoU matrix": coordinates loaded
+// once per tile and reused by every row.
+//
+// GB300 shape: a CTA computes a 256-row x 256-column tile.  Each lane holds two
+// row boxes in registers and walks the 256 staged column boxes (broadcast
+// shared-memory reads), so a row's four words of the tile (one 32-byte
+// sector) are built in registers and written with two 16-byte stores.  The
+// triangle of tiles is enumerated column by column.  Each row also records,
+// one bit per 256-column chunk, which of its chunks hold a set bit, and the
+// 64x64 blocks within BAND_L tiles of the diagonal are also written in column
+// view; the resolve uses the first to skip all-zero chunks and the second to
+// decide a tile with lane-local tests.  Pairs are decided by the
+// division-free test of common.cuh and, for the rare pair it leaves open and
+// for tiles holding a malformed box, by the exact binary32 division.
+#include "common.cuh"
+#include "internal.h"
+
+namespace gbnms {
+
+constexpr int MT = 256;         // tile edge (rows and columns)
+constexpr int M_WARPS = 4;      // 4 warps x 64 rows
+constexpr int M_THREADS = M_WARPS * 32;
+
+// Far-away zero-area box used to pad ragged tiles: overlaps nothing.
+__device__ __forceinline__ float4 pad_box() { return make_float4(3e38f, 3e38f, 3e38f, 3e38f); }
+
+// Linear index k of the tile triangle (column-major: column c holds rows
+// 0..c) -> (row tile a, column tile c).
+__device__ __forceinline__ void tri_coords(long long k, int& a, int& c)
+{
+    long long cc = static_cast<long long>((sqrt(8.0 * static_cast<double>(k) + 1.0) - 1.0) * 0.5);
+    while ((cc + 1) * (cc + 2) / 2 <= k) ++cc;
+    while (cc * (cc + 1) / 2 > k) --cc;
+    c = static_cast<int>(cc);
+    a = static_cast<int>(k - cc * (cc + 1) / 2);
+}
+
+template <bool FAST>
+__device__ __forceinline__ void tile_rows(const float4* __restrict__ cbox, const float* __restrict__ carea,
+                                          float4 r0, float ar0, float4 r1, float ar1,
+                                          const ThrParams& p, uint64_t (&w0)[4], uint64_t (&w1)[4],
+                                          bool& unsure)
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+            float4 c = cbox[q * 64 + k];
+            float ac = carea[q * 64 + k];
+            bool s0, s1;
+            if (FAST) {
+                s0 = suppress_fast(r0, ar0, c, ac, p, unsure);
+                s1 = suppress_fast(r1, ar1, c, ac, p, unsure);
+            } else {
+                s0 = suppress_exact(r0, ar0, c, ac, p.thr);
+                s1 = suppress_exact(r1, ar1, c, ac, p.thr);
+            }
+            lo0 |= static_cast<uint32_t>(s0) << k;
+            lo1 |= static_cast<uint32_t>(s1) << k;
+        }
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+            float4 c = cbox[q * 64 + 32 + k];
+            float ac = carea[q * 64 + 32 + k];
+            bool s0, s1;
+            if (FAST) {
+                s0 = suppress_fast(r0, ar0, c, ac, p, unsure);
+                s1 = suppress_fast(r1, ar1, c, ac, p, unsure);
+            } else {
+                s0 = suppress_exact(r0, ar0, c, ac, p.thr);
+                s1 = suppress_exact(r1, ar1, c, ac, p.thr);
+            }
+            hi0 |= static_cast<uint32_t>(s0) << k;
+            hi1 |= static_cast<uint32_t>(s1) << k;
+        }
+        w0[q] = (static_cast<uint64_t>(hi0) << 32) | lo0;
+        w1[q] = (static_cast<uint64_t>(hi1) << 32) | lo1;
+    }
+}
+
+// Keep only bits j with j > i and j < n of the four words at column base cb.
+__device__ __forceinline__ void clip_words(uint64_t (&w)[4], int i, int cb, int n)
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        int j0 = cb + 64 * q;
+        uint64_t keep = ~0ull;
+        int lo = i + 1 - j0;                    // first allowed bit
+        if (lo >= 64) keep = 0;
+        else if (lo > 0) keep &= ~0ull << lo;
+        int hi = n - j0;                        // bits >= hi are beyond n
+        if (hi <= 0) keep = 0;
+        else if (hi < 64) keep &= (1ull << hi) - 1ull;
+        w[q] &= keep;
+    }
+}
+
+__global__ void __launch_bounds__(M_THREADS)
+iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_dev, int m_bound,
+                ThrParams p, uint64_t* __restrict__ mask, int64_t ldw,
+                unsigned long long* __restrict__ rowbits, int NB, ulonglong2* __restrict__ band)
+{
+    __shared__ float4 cbox[MT];
+    __shared__ float carea[MT];
+
+    const int n = m_dev ? *m_dev : m_bound;
+    int a, c;
+    tri_coords(blockIdx.x, a, c);
+    const int T = (n + MT - 1) / MT;
+    if (c >= T) return;  // beyond the device-side count
+
+    const int cb = c * MT;
+    const int rbase = a * MT;
+    bool ok = true;
+    for (int t = threadIdx.x; t < MT; t += M_THREADS) {
+        int j = cb + t;
+        float4 b = j < n ? boxes_s[j] : pad_box();
+        float ar = j < n ? box_area(b) : 0.0f;
+        if (j < n) ok &= well_formed(b, ar);
+        cbox[t] = b;
+        carea[t] = ar;
+    }
+    const unsigned l = lane_id();
+    const int wp = threadIdx.x >> 5;
+    const int i0 = rbase + wp * 64 + l;
+    const int i1 = i0 + 32;
+    float4 r0 = i0 < n ? boxes_s[i0] : pad_box();
+    float4 r1 = i1 < n ? boxes_s[i1] : pad_box();
+    float ar0 = i0 < n ? box_area(r0) : 0.0f;
+    float ar1 = i1 < n ? box_area(r1) : 0.0f;
+    if (i0 < n) ok &= well_formed(r0, ar0);
+    if (i1 < n) ok &= well_formed(r1, ar1);
+    const bool fast = __syncthreads_and(ok) && p.fast_ok;
+
+    uint64_t w0[4], w1[4];
+    bool unsure = false;
+    if (fast) {
+        tile_rows<true>(cbox, carea, r0, ar0, r1, ar1, p, w0, w1, unsure);
+        if (__any_sync(FULL, unsure)) {
+            uint64_t e0[4], e1[4];
+            bool dummy = false;
+            if (unsure) {
+                tile_rows<false>(cbox, carea, r0, ar0, r1, ar1, p, e0, e1, dummy);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) { w0[q] = e0[q]; w1[q] = e1[q]; }
+            }
+        }
+    } else {
+        tile_rows<false>(cbox, carea, r0, ar0, r1, ar1, p, w0, w1, unsure);
+    }
+
+    if (a == c) {
+        clip_words(w0, i0, cb, n);
+        clip_words(w1, i1, cb, n);
+    } else {
+        clip_words(w0, -1, cb, n);
+        clip_words(w1, -1, cb, n);
+    }
+    // Column view of the blocks within BAND_L tiles of the diagonal (64-row
+    // tile R of this warp, 64-column tile C = 4c+q): transpose the block's
+    // final words with two ballots per column.  Lane l keeps columns l and
+    // l+32.
+    if (band) {
+        const int R = 4 * a + wp;
+        const int T64 = (n + 63) / 64;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int C = 4 * c + q;
+            const int d = C - R;
+            if (d < 0 || d > BAND_L || C >= T64) continue;  // warp-uniform
+            uint64_t colA = 0, colB = 0;
+#pragma unroll 4
+            for (int b = 0; b < 64; ++b) {
+                const uint64_t col = ballot64((w0[q] >> b) & 1ull, (w1[q] >> b) & 1ull);
+                if (b == static_cast<int>(l)) colA = col;
+                if (b == static_cast<int>(l) + 32) colB = col;
+            }
+            band[(static_cast<int64_t>(C) * (BAND_L + 1) + d) * 32 + l] = make_ulonglong2(colA, colB);
+        }
+    }
+    const int64_t wcol = static_cast<int64_t>(c) * 4;
+    if (i0 < n) {
+        uint64_t* dst = mask + static_cast<int64_t>(i0) * ldw + wcol;
+        reinterpret_cast<ulonglong2*>(dst)[0] = make_ulonglong2(w0[0], w0[1]);
+        reinterpret_cast<ulonglong2*>(dst)[1] = make_ulonglong2(w0[2], w0[3]);
+        if (rowbits && (w0[0] | w0[1] | w0[2] | w0[3]))
+            atomicOr(rowbits + static_cast<int64_t>(i0) * NB + (c >> 6), 1ull << (c & 63));
+    }
+    if (i1 < n) {
+        uint64_t* dst = mask + static_cast<int64_t>(i1) * ldw + wcol;
+        reinterpret_cast<ulonglong2*>(dst)[0] = make_ulonglong2(w1[0], w1[1]);
+        reinterpret_cast<ulonglong2*>(dst)[1] = make_ulonglong2(w1[2], w1[3]);
+        if (rowbits && (w1[0] | w1[1] | w1[2] | w1[3]))
+            atomicOr(rowbits + static_cast<int64_t>(i1) * NB + (c >> 6), 1ull << (c & 63));
+    }
+}
+
+int64_t mask_tiles(int64_t n)
+{
+    int64_t T = (n + MT - 1) / MT;
+    return T * (T + 1) / 2;
+}
+
+void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const ThrParams& p,
+                     uint64_t* mask, int64_t ldw, uint64_t* rowbits, int NB, uint64_t* band,
+                     cudaStream_t st)
+{
+    int64_t tiles = mask_tiles(m_bound);
+    if (tiles == 0) return;
+    iou_mask_kernel<<<static_cast<unsigned>(tiles), M_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, p,
+                                                                        mask, ldw,
+                                                                        reinterpret_cast<unsigned long long*>(rowbits), NB,
+                                                                        reinterpret_cast<ulonglong2*>(band));
+}
+
+}  // namespace gbnms

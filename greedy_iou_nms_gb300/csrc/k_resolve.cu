@@ -1,0 +1,509 @@
+// Sequential resolve of the suppression bitmask, in score order, with the map
+// back to input indices.
+//
+// "NMS CUDA代码学习", section Phase 2: one thread block walks the boxes from
+// the highest score down with the removed-bitmap in shared memory; a box not
+// yet removed is kept and its mask row is ORed into the bitmap, each decision
+// visible to the next.  Section "host 侧": the kept sorted positions are
+// mapped back through the sort permutation to int64 input indices.
+//
+// GB300 shape: one CTA, three roles, 64-box tiles.  Whether box b of tile t
+// is removed by a kept box depends on
+//   (a) the kept sets of tiles t-1 and t-2,       -> the resolver warp,
+//   (b) the kept sets of tiles t-3 .. t-BAND_L,   -> two helper warps,
+//   (c) the kept sets of tiles <= t-BAND_L-1,     -> worker warp groups.
+// (a) and (b) use the column views of the blocks (tile t-d, tile t) that the
+// mask kernel writes for d <= BAND_L: lane l ANDs its two boxes' columns with
+// the kept sets and one pair of ballots gives the removed word.  (c) ORs the
+// kept rows of the row-major mask into a shared removed-bitmap with shared
+// atomics, skipping the 256-column chunks the per-row chunk bitmap marks
+// all-zero.  Helpers fold (b) and (c) into one word per tile before the
+// resolver needs it, so the resolver's critical path is (a), the tile's own
+// decision (tile_greedy) and the hand-over of the kept set.
+//
+// The column-view windows arrive by lane-parallel cp.async copies into
+// shared-memory rings (bulk copies cost ~200 cycles of issue each on this SM,
+// too much for one small window per tile); every hand-over between roles is
+// an mbarrier, waiters off the critical path nap between attempts, and every
+// wait is bounded and gives up with NMS_ERR_TIMEOUT.  The resolver owns a scheduler partition: the warps that
+// share warp 0's partition (4, 8, ...) stay idle.  Kept sets go to shared
+// memory; the output list is written by the whole CTA after the walk.
+#include "common.cuh"
+#include "internal.h"
+
+namespace gbnms {
+
+constexpr int RV_L = BAND_L;               // tiles covered by the column-view band
+constexpr int RV_DR = 2;                   // distances the resolver covers itself
+constexpr int RV_RB = RV_DR + 1;           // blocks of a resolver window (d = 0..RV_DR)
+constexpr int RV_HB = RV_L - RV_DR;        // blocks of a helper window (d = RV_DR+1..RV_L)
+constexpr int RV_RP = 8;                   // resolver window prefetch distance (tiles)
+constexpr int RV_RR = RV_RP + 1;           // resolver window slots
+constexpr int RV_NH = 2;                   // helper warps (tiles alternate between them)
+constexpr int RV_HR = 4;                   // window slots per helper
+constexpr int RV_WARPS = 32;
+constexpr int RV_THREADS = RV_WARPS * 32;
+constexpr int RV_WPG = 3;                  // warps per worker group
+constexpr int RV_GT = RV_WPG * 32;
+constexpr int RV_G = 7;                    // worker groups
+constexpr int RV_KR = 32;                  // ring of per-tile hand-overs
+constexpr int RV_BATCH = 8;                // kept rows whose loads a worker lane issues together
+constexpr int RV_SERIAL = 12;              // conflicts resolved one by one before rounds
+constexpr long long RV_WAIT_LIMIT = 1ll << 24;  // wait attempts before giving up
+#ifndef GBNMS_RV_NAP_HELPER
+#define GBNMS_RV_NAP_HELPER 32
+#endif
+#ifndef GBNMS_RV_NAP_WORKER
+#define GBNMS_RV_NAP_WORKER 256
+#endif
+constexpr unsigned RV_NAP_HELPER = GBNMS_RV_NAP_HELPER;  // ns between wait attempts (helpers)
+constexpr unsigned RV_NAP_WORKER = GBNMS_RV_NAP_WORKER;  // ns between wait attempts (workers)
+
+static_assert(RV_KR >= RV_L + 1, "hand-over ring must outlive the band");
+static_assert(RV_DR + 1 <= RV_L, "helpers cover at least one distance");
+static_assert(RV_G <= 15 && RV_G * RV_WPG <= RV_WARPS - RV_WARPS / 4 - 1 - RV_NH, "worker warps");
+
+struct ResolveShared {
+    unsigned long long pub[RV_KR];     // kept set of tile t published (resolver)
+    unsigned long long ready[RV_KR];   // far removed word of tile t ready (helper)
+    unsigned long long done[RV_KR];    // kept rows of tile t applied (worker group)
+    uint64_t far[RV_KR];               // removed word of tile t from distances > RV_DR
+    int stop;
+    int ntiles;                        // tiles decided (the walk may stop early at max_out)
+};
+
+__device__ __forceinline__ int vload(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
+
+__device__ __forceinline__ unsigned smem_addr(const void* p)
+{
+    return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(unsigned long long* b, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(b)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive(unsigned long long* b)
+{
+    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(smem_addr(b))
+                 : "memory");
+}
+
+// One wait attempt for the phase with the given parity.
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* b, unsigned parity)
+{
+    unsigned ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of use `k` of barrier b; gives up (returns
+// false) after RV_WAIT_LIMIT attempts or when `stop` is raised.  try_wait may
+// return at once instead of suspending the warp, so waiters off the critical
+// path sleep `nap` ns between attempts to leave the issue slots to the warps
+// that work.
+__device__ __forceinline__ bool mbar_wait(unsigned long long* b, int k, const int* stop,
+                                          unsigned nap = 0)
+{
+    long long w = 0;
+    while (!mbar_try_wait(b, static_cast<unsigned>(k) & 1u)) {
+        if ((stop && vload(stop)) || ++w > RV_WAIT_LIMIT) return false;
+        if (nap) __nanosleep(nap);
+    }
+    return true;
+}
+
+// Lane-parallel copy of NB16 16-byte pieces per lane (a window of 32*NB16*16
+// bytes) from global to shared memory, as one cp.async group.
+template <int NB16>
+__device__ __forceinline__ void window_copy(uint64_t* dst, const uint64_t* src, unsigned l)
+{
+#pragma unroll
+    for (int q = 0; q < NB16; ++q) {
+        const int w = 2 * (q * 32 + static_cast<int>(l));
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst + w)), "l"(src + w)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+__device__ __forceinline__ void empty_group() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void wait_groups() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void group_bar(int g)
+{
+    asm volatile("bar.sync %0, %1;\n" ::"r"(g + 1), "n"(RV_GT));
+}
+
+// Barrier of one worker group that also ORs a predicate over the group.
+__device__ __forceinline__ bool group_bar_or(int g, bool v)
+{
+    unsigned r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
+        " bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(static_cast<unsigned>(v)), "r"(g + 1), "n"(RV_GT));
+    return r != 0;
+}
+
+// The greedy kept set of one tile.  Lane l holds ca = C[l], cb = C[l+32]
+// (column view of the diagonal block: bit k of C[b] set iff box k < b
+// suppresses box b) and `cand` the boxes no earlier kept box removed.  A
+// candidate with no candidate suppressor inside the tile is kept outright;
+// the others ("conflicts") are decided in ascending order, each against the
+// boxes kept so far, or by resolve_tile_col when there are many.
+__device__ __forceinline__ uint64_t tile_greedy(uint64_t cand, uint64_t ca, uint64_t cb)
+{
+    const unsigned l = lane_id();
+    const bool ia = (cand >> l) & 1ull, ib = (cand >> (l + 32)) & 1ull;
+    const uint64_t X = ballot64(ia && (ca & cand) != 0, ib && (cb & cand) != 0);
+    if (__popcll(X) > RV_SERIAL) return resolve_tile_col(cand, ca, cb);
+    uint64_t kept = cand & ~X;
+    uint64_t rest = X;
+    while (rest) {
+        const int b = __ffsll(static_cast<long long>(rest)) - 1;
+        rest &= rest - 1;
+        const uint64_t cbits = __shfl_sync(FULL, b < 32 ? ca : cb, b & 31);
+        if (!(cbits & kept)) kept |= 1ull << b;
+    }
+    return kept;
+}
+
+// Words of the shared removed-bitmap: the used words plus a 256-column chunk
+// of slack, rounded to a multiple of 4.
+__host__ __device__ __forceinline__ int resolve_bitmap_words(int m_bound)
+{
+    return ((m_bound + 63) / 64 + 4 + 3) & ~3;
+}
+
+struct ResolveLayout {
+    size_t removed, rwin, hwin, fl, wlist, kept, opre, total;  // offsets in 64-bit words / bytes
+};
+
+__host__ __device__ __forceinline__ ResolveLayout resolve_layout(int m_bound, int NB)
+{
+    ResolveLayout L;
+    const size_t tiles = static_cast<size_t>((m_bound + 63) / 64);
+    L.removed = 0;
+    L.rwin = L.removed + static_cast<size_t>(resolve_bitmap_words(m_bound));
+    L.hwin = L.rwin + static_cast<size_t>(RV_RR) * RV_RB * 64;
+    L.fl = L.hwin + static_cast<size_t>(RV_NH) * RV_HR * RV_HB * 64;
+    L.wlist = L.fl + static_cast<size_t>(RV_G) * 64 * NB;       // bytes [RV_G*RV_WPG][64]
+    L.kept = L.wlist + static_cast<size_t>(RV_G) * RV_WPG * 64 / 8;
+    L.opre = L.kept + tiles;                                     // int[tiles] after kept
+    L.total = 8 * L.opre + 4 * tiles;                            // bytes
+    return L;
+}
+
+__global__ void __launch_bounds__(RV_THREADS, 1)
+resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
+                      const uint64_t* __restrict__ rowbits, int NB,
+                      const uint64_t* __restrict__ band,
+                      const int* __restrict__ m_dev, int m_bound, const int* __restrict__ perm,
+                      int max_out, int64_t* __restrict__ keep, int64_t* __restrict__ counts,
+                      int32_t* status)
+{
+    extern __shared__ __align__(128) uint64_t smem[];
+    __shared__ ResolveShared S;
+
+    const int n = m_dev ? *m_dev : m_bound;
+    const int T = (n + 63) / 64;              // tiles
+    const int T256 = (n + 255) / 256;         // 256-column chunks
+    const ResolveLayout LY = resolve_layout(m_bound, NB);
+    uint64_t* removed = smem + LY.removed;
+    uint64_t* rwin = smem + LY.rwin;          // [RV_RR][RV_RB*64]
+    uint64_t* hwin = smem + LY.hwin;          // [RV_NH][RV_HR][RV_HB*64]
+    uint64_t* fl = smem + LY.fl;              // [RV_G][64][NB]
+    unsigned char* wlist = reinterpret_cast<unsigned char*>(smem + LY.wlist);  // per worker warp
+    uint64_t* kept = smem + LY.kept;          // [tiles]
+    int* opre = reinterpret_cast<int*>(smem + LY.opre);
+    constexpr int BW = (BAND_L + 1) * 64;     // words of one tile's band
+
+    const int Wpad = resolve_bitmap_words(m_bound);
+    for (int w = threadIdx.x; w < Wpad; w += blockDim.x) removed[w] = 0;
+    if (threadIdx.x < RV_KR) {
+        mbar_init(&S.pub[threadIdx.x], 1);
+        mbar_init(&S.ready[threadIdx.x], 1);
+        mbar_init(&S.done[threadIdx.x], 1);
+    }
+    if (threadIdx.x == 0) { S.stop = 0; S.ntiles = 0; }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    __syncthreads();
+
+    const unsigned l = lane_id();
+    const int warp = threadIdx.x >> 5;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ resolver
+        // Window of tile t lives in slot t % RV_RR; one cp.async group per tile
+        // (empty past the end), RV_RP groups in flight.
+        for (int t = 0; t < RV_RP; ++t) {
+            if (t < T) window_copy<RV_RB>(rwin + static_cast<size_t>(t % RV_RR) * RV_RB * 64,
+                                          band + static_cast<int64_t>(t) * BW, l);
+            else empty_group();
+        }
+        uint64_t K1 = 0, K2 = 0;  // kept sets of tiles t-1, t-2
+        int count = 0, t = 0;
+        bool timeout = false;
+        for (; t < T; ++t) {
+            wait_groups<RV_RP - 1>();
+            __syncwarp();
+            if (!mbar_wait(&S.ready[t % RV_KR], t / RV_KR, nullptr)) { timeout = true; break; }
+            const ulonglong2* wv =
+                reinterpret_cast<const ulonglong2*>(rwin + static_cast<size_t>(t % RV_RR) * RV_RB * 64);
+            const ulonglong2 dg = wv[l], b1 = wv[32 + l], b2 = wv[64 + l];
+            const uint64_t xa = (b1.x & K1) | (b2.x & K2);
+            const uint64_t xb = (b1.y & K1) | (b2.y & K2);
+            const uint64_t near = ballot64(xa != 0, xb != 0);
+            const int rem = n - t * 64;
+            const uint64_t valid = rem >= 64 ? ~0ull : ((1ull << rem) - 1ull);
+            const uint64_t cand = ~(S.far[t % RV_KR] | near) & valid;
+            uint64_t K = tile_greedy(cand, dg.x, dg.y);
+            const int nk = __popcll(K);
+            const bool last = max_out > 0 && count + nk >= max_out;
+            if (last) K = lowest_bits(K, max_out - count);
+            count += nk;
+            if (l == 0) {
+                kept[t] = K;
+                mbar_arrive(&S.pub[t % RV_KR]);  // release: kept[t] visible
+            }
+            if (last) { ++t; break; }
+            K2 = K1;
+            K1 = K;
+            // Refill the slot of tile t-1 (every lane is past it) with tile t+RV_RP.
+            const int tn = t + RV_RP;
+            if (tn < T) window_copy<RV_RB>(rwin + static_cast<size_t>(tn % RV_RR) * RV_RB * 64,
+                                           band + static_cast<int64_t>(tn) * BW, l);
+            else empty_group();
+        }
+        // No copy may land after the CTA exits.
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
+        if (l == 0) {
+            S.ntiles = t;
+            if (timeout && status) set_status(status, NMS_ERR_TIMEOUT);
+            __threadfence_block();
+            *reinterpret_cast<volatile int*>(&S.stop) = 1;
+        }
+    } else if (warp <= RV_NH) {
+        // ------------------------------------------------------------- helpers
+        const int h = warp - 1;
+        uint64_t* myw = hwin + static_cast<size_t>(h) * RV_HR * RV_HB * 64;
+        // Own tile i (tile h + RV_NH*i) lives in slot i % RV_HR; RV_HR-1 groups in flight.
+        for (int i = 0; i < RV_HR - 1; ++i) {
+            const int tt = h + RV_NH * i;
+            if (tt < T) window_copy<RV_HB>(myw + static_cast<size_t>(i % RV_HR) * RV_HB * 64,
+                                           band + static_cast<int64_t>(tt) * BW + RV_RB * 64, l);
+            else empty_group();
+        }
+        for (int i = 0; h + RV_NH * i < T; ++i) {
+            const int t = h + RV_NH * i;
+            {   // keep RV_HR-1 copies in flight: issue own tile i+RV_HR-1 into the slot freed by i-1
+                const int tn = h + RV_NH * (i + RV_HR - 1);
+                if (tn < T) window_copy<RV_HB>(myw + static_cast<size_t>((i + RV_HR - 1) % RV_HR) * RV_HB * 64,
+                                               band + static_cast<int64_t>(tn) * BW + RV_RB * 64, l);
+                else empty_group();
+            }
+            // Kept sets of tiles <= t-RV_DR-1, and the workers' part of word t:
+            // worker groups finish tiles out of order, so wait for every tile
+            // since this helper's previous tile (t-RV_NH): together with that
+            // tile's waits, all tiles <= t-RV_L-1 are applied.
+            if (t - RV_DR - 1 >= 0 &&
+                !mbar_wait(&S.pub[(t - RV_DR - 1) % RV_KR], (t - RV_DR - 1) / RV_KR, &S.stop, RV_NAP_HELPER))
+                break;
+            bool ok = true;
+            for (int f = max(t - RV_L - RV_NH, 0); ok && f <= t - RV_L - 1; ++f)
+                ok = mbar_wait(&S.done[f % RV_KR], f / RV_KR, &S.stop, RV_NAP_HELPER);
+            if (!ok) break;
+            wait_groups<RV_HR - 1>();
+            __syncwarp();
+            const ulonglong2* wv =
+                reinterpret_cast<const ulonglong2*>(myw + static_cast<size_t>(i % RV_HR) * RV_HB * 64);
+            uint64_t xa = 0, xb = 0;
+#pragma unroll
+            for (int d = RV_DR + 1; d <= RV_L; ++d) {
+                const uint64_t Kd = t - d >= 0 ? kept[t - d] : 0ull;
+                const ulonglong2 v = wv[(d - RV_DR - 1) * 32 + l];
+                xa |= v.x & Kd;
+                xb |= v.y & Kd;
+            }
+            const uint64_t word = removed[t] | ballot64(xa != 0, xb != 0);
+            if (l == 0) {
+                S.far[t % RV_KR] = word;
+                mbar_arrive(&S.ready[t % RV_KR]);
+            }
+            __syncwarp();
+        }
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
+    } else if ((warp & 3) != 0 && (warp - 1 - RV_NH - warp / 4) < RV_G * RV_WPG) {
+        // ------------------------------------------------------------- workers
+        const int wk = warp - 1 - RV_NH - warp / 4;  // index among worker warps
+        const int g = wk / RV_WPG;
+        const int wg = wk % RV_WPG;
+        const int gt = wg * 32 + static_cast<int>(l);
+        uint64_t* gfl = fl + static_cast<size_t>(g) * 64 * NB;
+        for (int r = g; r < T; r += RV_G) {
+            // Chunk bitmaps of the tile's 64 rows (independent of the decision).
+            if (rowbits) {
+                for (int q = gt; q < 64 * NB; q += RV_GT) {
+                    const int64_t i = static_cast<int64_t>(r) * 64 + q / NB;
+                    gfl[q] = i < n ? rowbits[i * NB + q % NB] : 0ull;
+                }
+            }
+            const bool stop = group_bar_or(g, !mbar_wait(&S.pub[r % RV_KR], r / RV_KR, &S.stop, RV_NAP_WORKER));
+            if (stop) break;
+            const uint64_t K = kept[r];
+            // Warp wg of the group takes the kept rows of rank wg, wg+RV_WPG, ...:
+            // a warp-parallel compaction writes them to the warp's row list.
+            unsigned char* rows = wlist + static_cast<size_t>(wk) * 64;
+            int nmine = 0;
+            {
+                const int nlo = __popc(static_cast<unsigned>(K));
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int b = static_cast<int>(l) + 32 * hh;
+                    const bool set = (K >> b) & 1ull;
+                    const int rank = __popcll(K & ((1ull << b) - 1ull));
+                    if (set && rank % RV_WPG == wg) rows[rank / RV_WPG] = static_cast<unsigned char>(b);
+                }
+                const int nk = nlo + __popc(static_cast<unsigned>(K >> 32));
+                nmine = nk > wg ? (nk - wg + RV_WPG - 1) / RV_WPG : 0;
+                __syncwarp();
+            }
+            const int c0 = (r + 1) >> 2;
+            for (int cq = c0 + static_cast<int>(l); nmine && cq < T256; cq += 32) {
+                uint64_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+                for (int j0 = 0; j0 < nmine; j0 += RV_BATCH) {
+                    // Up to RV_BATCH rows per round, all loads in flight together.
+                    int rb[RV_BATCH];
+#pragma unroll
+                    for (int u = 0; u < RV_BATCH; ++u) {
+                        const int b = j0 + u < nmine ? rows[j0 + u] : -1;
+                        rb[u] = (b >= 0 && (!rowbits || ((gfl[b * NB + (cq >> 6)] >> (cq & 63)) & 1ull)))
+                                    ? b : -1;
+                    }
+                    ulonglong2 x[RV_BATCH], y[RV_BATCH];
+#pragma unroll
+                    for (int u = 0; u < RV_BATCH; ++u) {
+                        x[u] = make_ulonglong2(0, 0);
+                        y[u] = make_ulonglong2(0, 0);
+                        if (rb[u] >= 0) {
+                            const ulonglong2* src = reinterpret_cast<const ulonglong2*>(
+                                mask + (static_cast<int64_t>(r) * 64 + rb[u]) * ldw + 4 * cq);
+                            x[u] = src[0];
+                            y[u] = src[1];
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < RV_BATCH; ++u) {
+                        a0 |= x[u].x; a1 |= x[u].y; a2 |= y[u].x; a3 |= y[u].y;
+                    }
+                }
+                unsigned long long* dst = reinterpret_cast<unsigned long long*>(removed + 4 * cq);
+                if (a0) atomicOr(dst + 0, a0);
+                if (a1) atomicOr(dst + 1, a1);
+                if (a2) atomicOr(dst + 2, a2);
+                if (a3) atomicOr(dst + 3, a3);
+            }
+            group_bar(g);
+            if (gt == 0) {
+                __threadfence_block();
+                mbar_arrive(&S.done[r % RV_KR]);
+            }
+        }
+    }
+    __syncthreads();
+    // Output: exclusive prefix of the kept counts over the decided tiles, then
+    // each warp writes whole tiles, mapping sorted positions through perm.
+    const int nt = S.ntiles;
+    if (warp == 0) {
+        int carry = 0;
+        for (int t0 = 0; t0 < nt; t0 += 32) {
+            const int t = t0 + static_cast<int>(l);
+            const int c = t < nt ? __popcll(kept[t]) : 0;
+            int x = c;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(FULL, x, d);
+                if (static_cast<int>(l) >= d) x += y;
+            }
+            if (t < nt) opre[t] = carry + x - c;
+            carry += __shfl_sync(FULL, x, 31);
+        }
+        if (l == 0) counts[0] = carry;
+    }
+    __syncthreads();
+    for (int t = warp; t < nt; t += RV_WARPS) {
+        const uint64_t K = kept[t];
+        const int p0 = opre[t];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int b = static_cast<int>(l) + 32 * hh;
+            if ((K >> b) & 1ull) {
+                const int pos = t * 64 + b;
+                keep[p0 + __popcll(K & ((1ull << b) - 1ull))] = perm ? perm[pos] : pos;
+            }
+        }
+    }
+}
+
+size_t resolve_smem_bytes(int m_bound, int NB) { return resolve_layout(m_bound, NB).total; }
+
+// Column view of the band blocks of a row-major mask: one warp per (column
+// tile C, distance d) transposes block (C-d, C) with two ballots per column.
+// Used when the caller brings its own mask (nms_resolve_mask).
+__global__ void band_from_mask_kernel(const uint64_t* __restrict__ mask, int64_t ldw, int n,
+                                      ulonglong2* __restrict__ band)
+{
+    const int T64 = (n + 63) / 64;
+    const int blk = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (blk >= T64 * (BAND_L + 1)) return;
+    const int C = blk / (BAND_L + 1), d = blk % (BAND_L + 1), R = C - d;
+    const unsigned l = lane_id();
+    uint64_t ra = 0, rb = 0;
+    if (R >= 0) {
+        const int64_t ia = static_cast<int64_t>(R) * 64 + l, ib = ia + 32;
+        if (ia < n) ra = mask[ia * ldw + C];
+        if (ib < n) rb = mask[ib * ldw + C];
+        if (d == 0) {  // only bits above the diagonal belong to the mask
+            ra &= (l + 1 < 64) ? (~0ull << (l + 1)) : 0ull;
+            rb &= (l + 33 < 64) ? (~0ull << (l + 33)) : 0ull;
+        }
+    }
+    uint64_t colA = 0, colB = 0;
+#pragma unroll 4
+    for (int b = 0; b < 64; ++b) {
+        const uint64_t col = ballot64((ra >> b) & 1ull, (rb >> b) & 1ull);
+        if (b == static_cast<int>(l)) colA = col;
+        if (b == static_cast<int>(l) + 32) colB = col;
+    }
+    band[static_cast<int64_t>(blk) * 32 + l] = make_ulonglong2(colA, colB);
+}
+
+void launch_band_from_mask(const uint64_t* mask, int64_t ldw, int n, uint64_t* band, cudaStream_t st)
+{
+    const int blocks = ((n + 63) / 64) * (BAND_L + 1);
+    if (blocks == 0) return;
+    band_from_mask_kernel<<<(blocks + 7) / 8, 256, 0, st>>>(mask, ldw, n,
+                                                            reinterpret_cast<ulonglong2*>(band));
+}
+
+void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* rowbits, int NB,
+                           const uint64_t* band, const int* m_dev, int m_bound, const int* perm,
+                           int max_out, int64_t* keep, int64_t* counts, int32_t* status,
+                           cudaStream_t st)
+{
+    const size_t smem = resolve_smem_bytes(m_bound, NB);
+    cudaFuncSetAttribute(resolve_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
+    resolve_single_kernel<<<1, RV_THREADS, smem, st>>>(mask, ldw, rowbits, NB, band, m_dev, m_bound,
+                                                       perm, max_out, keep, counts, status);
+}
+
+}  // namespace gbnms

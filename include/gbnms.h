@@ -1,0 +1,175 @@
+/*
+ * gbnms: greedy IoU non-maximum suppression on GB300 (sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only; no PyTorch or C++ types cross it.
+ * Every entry point returns an nms_status and never throws.  All device work
+ * is enqueued on the caller's CUDA stream (`stream` is a cudaStream_t passed
+ * as void*; NULL means the legacy default stream) and nms_run / nms_iou_mask
+ * never synchronise the host.  The library never allocates device memory:
+ * the caller owns every buffer, including the workspace.
+ *
+ * The operation (cited by page title and section):
+ *   "NMS CUDA代码学习" (leetCUDA 14-nms), intro and section 算法与数据流:
+ *     visit boxes from the highest score to the lowest (stable: equal scores
+ *     keep input order), keep a box unless an already-kept box overlaps it
+ *     with IoU strictly greater than the threshold, and return the survivors
+ *     as original input indices; section "host 侧": int64 indices, on the
+ *     input's device, in score order.
+ *   "YOLOv5后处理GPU移植实战", section 1.1 (a device-side count next to the
+ *     boxes), section 2.2 (equal scores: the lower index has priority;
+ *     suppression only within one class).
+ *
+ * Conventions fixed by this library where the pages are silent:
+ *   - boxes are xyxy fp32 [n][4], row-major, 16-byte aligned; scores fp32 [n].
+ *   - IoU = inter / ((area_a + area_b) - inter) with area = (x2-x1)*(y2-y1),
+ *     w = max(min(x2)-max(x1), 0), h likewise, every step one IEEE binary32
+ *     operation with round-to-nearest-even, no fused multiply-add, no
+ *     flush-to-zero; max/min return the non-NaN operand.  The test is
+ *     iou > iou_thr in binary32 (strict).
+ *   - score order: descending; -0 == +0; NaN after everything; ties (and NaNs
+ *     among themselves) by lower input index.
+ */
+#ifndef GBNMS_H
+#define GBNMS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nms_status {
+    NMS_OK = 0,
+    NMS_ERR_INVALID_ARG = 1, /* bad pointer, size, threshold, alignment, offsets or class id */
+    NMS_ERR_WORKSPACE = 2,   /* workspace NULL or smaller than nms_workspace_size() */
+    NMS_ERR_CAPACITY = 3,    /* keep_cap or mask capacity too small, or n beyond a limit */
+    NMS_ERR_CUDA = 4,        /* a CUDA launch or copy failed */
+    NMS_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (device status only) */
+} nms_status;
+
+/* Largest n of the single-image, single-class path (its mask is n*ceil(n/256)*32 bytes). */
+#define NMS_MAX_SINGLE_N (1 << 18)
+
+/* Human-readable name of a status code (static string; never NULL). */
+const char* nms_status_string(nms_status s);
+
+/*
+ * Workspace bytes nms_run needs for n boxes.
+ *   batch       = 0 when nms_run will get batch_offsets == NULL (one image),
+ *                 else the number of images (>= 1).
+ *   num_classes = 0 when nms_run will get class_ids == NULL (one class),
+ *                 else the number of classes (>= 1).
+ * The single-image single-class path (batch == 0 && num_classes == 0) holds
+ * the full suppression bitmask: about n*n/8 bytes.  The batched path needs
+ * O(n + batch*num_classes) bytes.  Pure host computation.
+ * Errors: NMS_ERR_INVALID_ARG (n < 0, negative batch/num_classes, bytes NULL),
+ *         NMS_ERR_CAPACITY (single path with n > NMS_MAX_SINGLE_N).
+ */
+nms_status nms_workspace_size(int64_t n, int32_t batch, int32_t num_classes, size_t* bytes);
+
+/*
+ * Greedy IoU NMS.
+ *
+ *   boxes          device fp32 [n][4] xyxy, 16-byte aligned.
+ *   scores         device fp32 [n].
+ *   n              number of boxes, 0 <= n < 2^31.
+ *   class_ids      device int32 [n] with values in [0, num_classes), or NULL
+ *                  (all boxes one class).  Boxes of different classes never
+ *                  suppress each other.
+ *   num_classes    >= 1 when class_ids != NULL; ignored otherwise.
+ *   batch_offsets  device int64 [batch+1], 0 = off[0] <= off[1] <= ... <=
+ *                  off[batch] = n: image b is boxes [off[b], off[b+1]).  NULL
+ *                  means one image.  Boxes of different images never suppress
+ *                  each other.
+ *   batch          >= 1 when batch_offsets != NULL; ignored otherwise.
+ *   iou_thr        fp32 IoU threshold (not NaN); a box is dropped when its IoU
+ *                  with a kept box of the same image and class is > iou_thr.
+ *   score_thr      pre-filter: only boxes with score > score_thr (strict; NaN
+ *                  scores fail) take part.  -INFINITY disables the pre-filter
+ *                  (then NaN and -inf scores take part and sort last).
+ *   max_out        at most max_out outputs per image (the first ones in score
+ *                  order); <= 0 means no cap.
+ *   keep           device int64 output.  Image b's kept indices (global input
+ *                  indices, descending score, ties by index, classes merged)
+ *                  are written at keep[b * max_out] when max_out > 0, else at
+ *                  keep[off[b]] (keep[0] for one image).
+ *   keep_cap       entries available at keep: must be >= batch*max_out
+ *                  (max_out > 0; min(n, max_out) for one image) or >= n.
+ *   counts         device int64 [max(batch,1)]: kept boxes per image.
+ *   dev_status     device int32 [1] or NULL.  Receives NMS_OK, or an error found
+ *                  on the device (invalid batch_offsets or class ids:
+ *                  NMS_ERR_INVALID_ARG; a bounded wait that gave up:
+ *                  NMS_ERR_TIMEOUT).  On a device error, keep/counts of the
+ *                  affected images are unspecified but all writes stay in
+ *                  bounds.
+ *   workspace      device scratch of >= nms_workspace_size(n, batch or 0,
+ *                  num_classes or 0) bytes, 256-byte aligned; contents on entry
+ *                  do not matter.  Reused freely between calls on one stream.
+ *   stream         cudaStream_t.
+ *
+ * Host-detected errors return before anything is enqueued.  Asynchronous:
+ * results are valid once the stream reaches the end of the call.
+ */
+nms_status nms_run(const float* boxes, const float* scores, int64_t n,
+                   const int32_t* class_ids, int32_t num_classes,
+                   const int64_t* batch_offsets, int32_t batch,
+                   float iou_thr, float score_thr, int32_t max_out,
+                   int64_t* keep, int64_t keep_cap, int64_t* counts,
+                   int32_t* dev_status,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Row stride, in 64-bit words, of the bitmask nms_iou_mask writes: 4*ceil(n/256). */
+int64_t nms_mask_row_words(int64_t n);
+
+/*
+ * The suppression bitmask of boxes already in score order
+ * ("NMS CUDA代码学习", section Phase 1: warp-per-box ballot and the aligned
+ * j_base rule): bit (j mod 64) of word j/64 of row i is set iff j > i, j < n
+ * and IoU(box i, box j) > iou_thr.  Bit k of a word always means box
+ * 64*word + k; in little-endian memory this equals the pages' 32-bit words.
+ *
+ *   boxes_sorted  device fp32 [n][4] xyxy, 16-byte aligned, highest score first.
+ *   mask          device uint64 [n][nms_mask_row_words(n)], row-major.  For row
+ *                 i, words w >= floor(i/64) are written (w < ceil(n/64) hold
+ *                 the bits above, the padding words up to the stride are 0);
+ *                 words below floor(i/64) are not part of the result.
+ *   mask_words    capacity of mask in words (>= n * nms_mask_row_words(n)).
+ * Errors: NMS_ERR_INVALID_ARG (NULL/unaligned pointers, n < 0, NaN threshold),
+ *         NMS_ERR_CAPACITY (n > NMS_MAX_SINGLE_N or mask_words too small),
+ *         NMS_ERR_CUDA.
+ */
+nms_status nms_iou_mask(const float* boxes_sorted, int64_t n, float iou_thr,
+                        uint64_t* mask, int64_t mask_words, void* stream);
+
+/*
+ * Sequential resolve of a suppression bitmask in score order
+ * ("NMS CUDA代码学习", section Phase 2: walk the boxes from the highest score
+ * down, keep a box whose bit is not yet set in the removed-bitmap and OR its
+ * mask row into the bitmap; section "host 侧": map kept positions back through
+ * the sort permutation).  One thread block; the walk stops at max_out.
+ *
+ *   mask     device uint64 [n][nms_mask_row_words(n)] in the nms_iou_mask
+ *            layout, 16-byte aligned.  Words w >= floor(i/64) of row i carry
+ *            the bits; words below may be read but never change the result.
+ *   perm     device int32 [n]: input index of each sorted position, or NULL
+ *            (the output is then the kept sorted positions themselves).
+ *   max_out  cap on the number of outputs; <= 0 means none.
+ *   keep     device int64 [min(n, max_out) or n]: kept entries in order.
+ *   count    device int64 [1]: number of kept entries.
+ *   workspace device scratch of >= nms_workspace_size(n, 0, 0) bytes,
+ *            256-byte aligned (the column view of the blocks near the
+ *            diagonal is rebuilt there from the mask).
+ * Errors: NMS_ERR_INVALID_ARG (NULL or unaligned pointers with n > 0, n < 0),
+ *         NMS_ERR_CAPACITY (n > NMS_MAX_SINGLE_N), NMS_ERR_WORKSPACE,
+ *         NMS_ERR_CUDA.
+ */
+nms_status nms_resolve_mask(const uint64_t* mask, int64_t n, const int32_t* perm,
+                            int32_t max_out, int64_t* keep, int64_t* count,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBNMS_H */

@@ -1,0 +1,115 @@
+"""The C-ABI library: builds, loads, exports what include/gbnms.h declares, and
+rejects bad arguments on the host before touching the device (no GPU needed)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import greedy_iou_nms_gb300 as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    g.build()
+    return g.load()
+
+
+def _declared():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(nms_\w+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared()
+    assert declared == set(g.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in ((0, "NMS_OK"), (1, "NMS_ERR_INVALID_ARG"), (2, "NMS_ERR_WORKSPACE"),
+                       (3, "NMS_ERR_CAPACITY"), (4, "NMS_ERR_CUDA"), (5, "NMS_ERR_TIMEOUT")):
+        assert g.nms_status_string(code) == name
+    assert g.nms_status_string(99) == "NMS_ERR_UNKNOWN"
+
+
+def test_workspace_size(lib):
+    # Single path holds the mask: n * 4*ceil(n/256) words.
+    for n in (0, 1, 255, 256, 257, 8192):
+        ws = g.nms_workspace_size(n)
+        assert ws >= 8 * n * g.nms_mask_row_words(n)
+    assert g.nms_workspace_size(1 << 18) > 0
+    with pytest.raises(g.NmsError) as e:
+        g.nms_workspace_size((1 << 18) + 1)
+    assert e.value.code == g.NMS_ERR_CAPACITY
+    # Batched path: linear in n.
+    b1 = g.nms_workspace_size(100000, 16, 80)
+    b2 = g.nms_workspace_size(200000, 16, 80)
+    assert b2 < 2.2 * b1
+    with pytest.raises(g.NmsError):
+        g.nms_workspace_size(-1)
+
+
+def test_mask_row_words(lib):
+    assert g.nms_mask_row_words(0) == 0
+    assert g.nms_mask_row_words(1) == 4
+    assert g.nms_mask_row_words(256) == 4
+    assert g.nms_mask_row_words(257) == 8
+
+
+FAKE = 1 << 20  # an aligned non-null address; never dereferenced on these paths
+
+
+def _run(**kw):
+    a = dict(boxes=FAKE, scores=FAKE, n=10, class_ids=0, num_classes=0, batch_offsets=0, batch=0,
+             iou_thr=0.5, score_thr=-math.inf, max_out=0, keep=FAKE, keep_cap=10, counts=FAKE,
+             dev_status=0, workspace=FAKE, workspace_bytes=0, stream=0)
+    a.update(kw)
+    return g.nms_run(**a)
+
+
+def test_host_validation(lib):
+    ws = g.nms_workspace_size(10)
+    assert _run(n=-1) == g.NMS_ERR_INVALID_ARG
+    assert _run(iou_thr=math.nan, workspace_bytes=ws) == g.NMS_ERR_INVALID_ARG
+    assert _run(score_thr=math.nan, workspace_bytes=ws) == g.NMS_ERR_INVALID_ARG
+    assert _run(boxes=0, workspace_bytes=ws) == g.NMS_ERR_INVALID_ARG
+    assert _run(boxes=FAKE + 4, workspace_bytes=ws) == g.NMS_ERR_INVALID_ARG  # not 16-B aligned
+    assert _run(keep=0, workspace_bytes=ws) == g.NMS_ERR_INVALID_ARG
+    assert _run(counts=0, workspace_bytes=ws) == g.NMS_ERR_INVALID_ARG
+    assert _run(class_ids=FAKE, num_classes=0, workspace_bytes=ws) == g.NMS_ERR_INVALID_ARG
+    assert _run(batch_offsets=FAKE, batch=0, workspace_bytes=ws) == g.NMS_ERR_INVALID_ARG
+    assert _run(keep_cap=9, workspace_bytes=ws) == g.NMS_ERR_CAPACITY
+    assert _run(workspace_bytes=ws - 1) == g.NMS_ERR_WORKSPACE
+    assert _run(workspace=0, workspace_bytes=ws) == g.NMS_ERR_WORKSPACE
+    assert _run(workspace=FAKE + 8, workspace_bytes=ws) == g.NMS_ERR_WORKSPACE
+    assert _run(n=(1 << 18) + 1, keep_cap=1 << 19, workspace_bytes=1 << 40) == g.NMS_ERR_CAPACITY
+    # batched capacity: batch * max_out
+    wsb = g.nms_workspace_size(10, 4, 3)
+    assert _run(class_ids=FAKE, num_classes=3, batch_offsets=FAKE, batch=4, max_out=5,
+                keep_cap=19, workspace_bytes=wsb) == g.NMS_ERR_CAPACITY
+
+
+def test_mask_entry_validation(lib):
+    assert g.nms_iou_mask(FAKE, -1, 0.5, FAKE, 0, 0) == g.NMS_ERR_INVALID_ARG
+    assert g.nms_iou_mask(FAKE, 10, math.nan, FAKE, 40, 0) == g.NMS_ERR_INVALID_ARG
+    assert g.nms_iou_mask(0, 10, 0.5, FAKE, 40, 0) == g.NMS_ERR_INVALID_ARG
+    assert g.nms_iou_mask(FAKE, 10, 0.5, FAKE, 39, 0) == g.NMS_ERR_CAPACITY
+    assert g.nms_iou_mask(FAKE, (1 << 18) + 1, 0.5, FAKE, 1 << 40, 0) == g.NMS_ERR_CAPACITY
+    assert g.nms_iou_mask(0, 0, 0.5, 0, 0, 0) == g.NMS_OK
+
+
+def test_no_cpu_fallback_when_library_missing(monkeypatch):
+    monkeypatch.setattr(g, "_lib", None)
+    monkeypatch.setattr(g, "LIB_PATH", "/nonexistent/libgbnms.so")
+    with pytest.raises(RuntimeError):
+        g.load()

@@ -29,7 +29,8 @@ NMS_ERR_TIMEOUT = 5
 NMS_MAX_SINGLE_N = 1 << 18
 
 EXPORTED = ("nms_status_string", "nms_workspace_size", "nms_run", "nms_mask_row_words",
-            "nms_iou_mask", "nms_resolve_mask")
+            "nms_iou_mask", "nms_resolve_mask", "nms_resolve_mask_noalloc")
+NMS_NOALLOC_MAX_N = 16384
 
 _lib = None
 
@@ -67,6 +68,8 @@ def load():
     lib.nms_iou_mask.restype = ctypes.c_int
     lib.nms_resolve_mask.argtypes = [vp, i64, vp, i32, vp, vp, vp, sz, vp]
     lib.nms_resolve_mask.restype = ctypes.c_int
+    lib.nms_resolve_mask_noalloc.argtypes = [vp, i64, vp, i32, vp, vp, vp]
+    lib.nms_resolve_mask_noalloc.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -112,6 +115,14 @@ def nms_resolve_mask(mask: int, n: int, perm: int, max_out: int, keep: int, coun
     return load().nms_resolve_mask(mask or None, int(n), perm or None, int(max_out), keep or None,
                                    count or None, workspace or None, int(workspace_bytes),
                                    stream or None)
+
+
+def nms_resolve_mask_noalloc(mask: int, n: int, perm: int, max_out: int, keep: int, count: int,
+                             stream: int) -> int:
+    """nms_resolve_mask with its scratch in a library-held device array (no
+    workspace, no allocation in the call); n <= NMS_NOALLOC_MAX_N."""
+    return load().nms_resolve_mask_noalloc(mask or None, int(n), perm or None, int(max_out),
+                                           keep or None, count or None, stream or None)
 
 
 # ----------------------------------------------------------- tensor helpers

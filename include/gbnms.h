@@ -168,6 +168,34 @@ nms_status nms_resolve_mask(const uint64_t* mask, int64_t n, const int32_t* perm
                             int32_t max_out, int64_t* keep, int64_t* count,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/* Largest n nms_resolve_mask_noalloc accepts. */
+#define NMS_NOALLOC_MAX_N 16384
+
+/*
+ * nms_resolve_mask without a workspace: the same resolve, with its scratch in
+ * a device array that the library holds for the life of the process.  The
+ * pages have no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory where they run NMS (a plugin whose host
+ * framework owns every allocation, a real-time loop whose memory is planned
+ * at start-up, a deployment that bans allocation after initialisation).
+ *
+ *   mask, perm, max_out, keep, count: as for nms_resolve_mask; n must be
+ *            <= NMS_NOALLOC_MAX_N (about 2.2 MB of scratch per GPU, held by
+ *            every GPU that loads the library until the process exits).
+ * The first call on a device looks up the scratch array's device address on
+ * that device (cudaGetSymbolAddress, with the device current); make that
+ * first call before any stream capture.  The call allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine.  All calls share the
+ * one array, so calls that may overlap on the GPU (other streams, other host
+ * threads, the same device) race on it and must be serialised by the caller;
+ * calls on one stream are ordered and safe.  Each call rewrites all the
+ * scratch it reads, so what an earlier call left behind never matters.
+ * Errors: NMS_ERR_INVALID_ARG (n < 0, NULL or unaligned pointers),
+ *         NMS_ERR_CAPACITY (n > NMS_NOALLOC_MAX_N), NMS_ERR_CUDA.
+ */
+nms_status nms_resolve_mask_noalloc(const uint64_t* mask, int64_t n, const int32_t* perm,
+                                    int32_t max_out, int64_t* keep, int64_t* count, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

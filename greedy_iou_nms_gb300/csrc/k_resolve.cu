@@ -9,46 +9,55 @@
 //
 // GB300 shape: one CTA, three roles, 64-box tiles.  Whether box b of tile t
 // is removed by a kept box depends on
-//   (a) the kept sets of tiles t-1 and t-2,       -> the resolver warp,
-//   (b) the kept sets of tiles t-3 .. t-BAND_L,   -> two helper warps,
-//   (c) the kept sets of tiles <= t-BAND_L-1,     -> worker warp groups.
+//   (a) the kept sets of tiles t-1 .. t-RV_DR,          -> the resolver warp,
+//   (b) the kept sets of tiles t-RV_DR-1 .. t-BAND_L,   -> helper warps,
+//   (c) the kept sets of tiles <= t-BAND_L-1,           -> worker warp groups.
 // (a) and (b) use the column views of the blocks (tile t-d, tile t) that the
 // mask kernel writes for d <= BAND_L: lane l ANDs its two boxes' columns with
 // the kept sets and one pair of ballots gives the removed word.  (c) ORs the
 // kept rows of the row-major mask into a shared removed-bitmap with shared
 // atomics, skipping the 256-column chunks the per-row chunk bitmap marks
-// all-zero.  Helpers fold (b) and (c) into one word per tile before the
-// resolver needs it, so the resolver's critical path is (a), the tile's own
-// decision (tile_greedy) and the hand-over of the kept set.
+// all-zero.
+//
+// A helper folds (b) and (c) into the tile's candidates and also decides the
+// tile on them (tile_greedy): a speculative kept set that ignores (a).  The
+// resolver then only tests (a): if no box of the speculative kept set is hit,
+// the speculation is the answer (boxes hit by (a) were not kept, and a box
+// that is not kept suppresses nothing); otherwise it re-decides the tile
+// without the boxes (a) removed.  Its critical path per tile is the (a) test
+// and the hand-over of the kept set.
 //
 // The column-view windows arrive by lane-parallel cp.async copies into
 // shared-memory rings (bulk copies cost ~200 cycles of issue each on this SM,
 // too much for one small window per tile); every hand-over between roles is
 // an mbarrier, waiters off the critical path nap between attempts, and every
-// wait is bounded and gives up with NMS_ERR_TIMEOUT.  The resolver owns a scheduler partition: the warps that
-// share warp 0's partition (4, 8, ...) stay idle.  Kept sets go to shared
-// memory; the output list is written by the whole CTA after the walk.
+// wait is bounded and gives up with NMS_ERR_TIMEOUT.  The resolver owns a
+// scheduler partition: the warps that share warp 0's partition (4, 8, ...)
+// stay idle.  Kept sets go to shared memory; the output list is written by
+// the whole CTA after the walk.
 #include "common.cuh"
 #include "internal.h"
 
 namespace gbnms {
 
 constexpr int RV_L = BAND_L;               // tiles covered by the column-view band
-constexpr int RV_DR = 2;                   // distances the resolver covers itself
+constexpr int RV_DR = 4;                   // distances the resolver tests itself
 constexpr int RV_RB = RV_DR + 1;           // blocks of a resolver window (d = 0..RV_DR)
-constexpr int RV_HB = RV_L - RV_DR;        // blocks of a helper window (d = RV_DR+1..RV_L)
+constexpr int RV_HB = RV_L - RV_DR;        // far blocks of a helper window (d = RV_DR+1..RV_L)
+constexpr int RV_HW = RV_HB + 1;           // blocks of a helper window: diagonal + far blocks
 constexpr int RV_RP = 8;                   // resolver window prefetch distance (tiles)
 constexpr int RV_RR = RV_RP + 1;           // resolver window slots
-constexpr int RV_NH = 2;                   // helper warps (tiles alternate between them)
-constexpr int RV_HR = 4;                   // window slots per helper
+constexpr int RV_NH = 4;                   // helper warps (tiles round-robin)
+constexpr int RV_HR = 3;                   // window slots per helper
 constexpr int RV_WARPS = 32;
 constexpr int RV_THREADS = RV_WARPS * 32;
-constexpr int RV_WPG = 3;                  // warps per worker group
+constexpr int RV_WPG = 2;                  // warps per worker group
 constexpr int RV_GT = RV_WPG * 32;
-constexpr int RV_G = 7;                    // worker groups
+constexpr int RV_G = 10;                   // worker groups at most (fewer when the bitmaps are wide)
+constexpr int RV_FL_BUDGET = 40 * 1024;    // shared bytes for the workers' chunk bitmaps
 constexpr int RV_KR = 32;                  // ring of per-tile hand-overs
 constexpr int RV_BATCH = 8;                // kept rows whose loads a worker lane issues together
-constexpr int RV_SERIAL = 12;              // conflicts resolved one by one before rounds
+constexpr int RV_SERIAL = 2;               // conflicts resolved one by one before rounds
 constexpr long long RV_WAIT_LIMIT = 1ll << 24;  // wait attempts before giving up
 #ifndef GBNMS_RV_NAP_HELPER
 #define GBNMS_RV_NAP_HELPER 32
@@ -59,15 +68,23 @@ constexpr long long RV_WAIT_LIMIT = 1ll << 24;  // wait attempts before giving u
 constexpr unsigned RV_NAP_HELPER = GBNMS_RV_NAP_HELPER;  // ns between wait attempts (helpers)
 constexpr unsigned RV_NAP_WORKER = GBNMS_RV_NAP_WORKER;  // ns between wait attempts (workers)
 
-static_assert(RV_KR >= RV_L + 1, "hand-over ring must outlive the band");
+static_assert(RV_KR >= RV_L + RV_NH, "hand-over ring must outlive the band and the helpers");
 static_assert(RV_DR + 1 <= RV_L, "helpers cover at least one distance");
-static_assert(RV_G <= 15 && RV_G * RV_WPG <= RV_WARPS - RV_WARPS / 4 - 1 - RV_NH, "worker warps");
+static_assert(RV_G <= 15 && RV_NH + RV_G * RV_WPG <= RV_WARPS - RV_WARPS / 4, "warp roles");
+
+// Worker groups that fit the chunk-bitmap budget for NB words per row.
+__host__ __device__ __forceinline__ int resolve_groups(int NB)
+{
+    const int g = RV_FL_BUDGET / (64 * 8 * (NB > 0 ? NB : 1));
+    return g < 1 ? 1 : (g > RV_G ? RV_G : g);
+}
 
 struct ResolveShared {
     unsigned long long pub[RV_KR];     // kept set of tile t published (resolver)
-    unsigned long long ready[RV_KR];   // far removed word of tile t ready (helper)
+    unsigned long long ready[RV_KR];   // speculation for tile t ready (helper)
     unsigned long long done[RV_KR];    // kept rows of tile t applied (worker group)
-    uint64_t far[RV_KR];               // removed word of tile t from distances > RV_DR
+    uint64_t cand[RV_KR];              // candidates of tile t without distances <= RV_DR
+    uint64_t spec[RV_KR];              // greedy kept set of those candidates
     int stop;
     int ntiles;                        // tiles decided (the walk may stop early at max_out)
 };
@@ -119,8 +136,8 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* b, int k, const in
     return true;
 }
 
-// Lane-parallel copy of NB16 16-byte pieces per lane (a window of 32*NB16*16
-// bytes) from global to shared memory, as one cp.async group.
+// Lane-parallel copy of NB16 16-byte pieces per lane (32*NB16*16 contiguous
+// bytes) from global to shared memory; commit_group() closes a window.
 template <int NB16>
 __device__ __forceinline__ void window_copy(uint64_t* dst, const uint64_t* src, unsigned l)
 {
@@ -130,9 +147,8 @@ __device__ __forceinline__ void window_copy(uint64_t* dst, const uint64_t* src, 
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst + w)), "l"(src + w)
                      : "memory");
     }
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
-__device__ __forceinline__ void empty_group() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void commit_group() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void wait_groups() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
@@ -194,8 +210,8 @@ __host__ __device__ __forceinline__ ResolveLayout resolve_layout(int m_bound, in
     L.removed = 0;
     L.rwin = L.removed + static_cast<size_t>(resolve_bitmap_words(m_bound));
     L.hwin = L.rwin + static_cast<size_t>(RV_RR) * RV_RB * 64;
-    L.fl = L.hwin + static_cast<size_t>(RV_NH) * RV_HR * RV_HB * 64;
-    L.wlist = L.fl + static_cast<size_t>(RV_G) * 64 * NB;       // bytes [RV_G*RV_WPG][64]
+    L.fl = L.hwin + static_cast<size_t>(RV_NH) * RV_HR * RV_HW * 64;
+    L.wlist = L.fl + static_cast<size_t>(resolve_groups(NB)) * 64 * NB;  // bytes [worker warps][64]
     L.kept = L.wlist + static_cast<size_t>(RV_G) * RV_WPG * 64 / 8;
     L.opre = L.kept + tiles;                                     // int[tiles] after kept
     L.total = 8 * L.opre + 4 * tiles;                            // bytes
@@ -217,10 +233,11 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
     const int T = (n + 63) / 64;              // tiles
     const int T256 = (n + 255) / 256;         // 256-column chunks
     const ResolveLayout LY = resolve_layout(m_bound, NB);
+    const int G = resolve_groups(NB);         // worker groups
     uint64_t* removed = smem + LY.removed;
     uint64_t* rwin = smem + LY.rwin;          // [RV_RR][RV_RB*64]
-    uint64_t* hwin = smem + LY.hwin;          // [RV_NH][RV_HR][RV_HB*64]
-    uint64_t* fl = smem + LY.fl;              // [RV_G][64][NB]
+    uint64_t* hwin = smem + LY.hwin;          // [RV_NH][RV_HR][RV_HW*64]
+    uint64_t* fl = smem + LY.fl;              // [G][64][NB]
     unsigned char* wlist = reinterpret_cast<unsigned char*>(smem + LY.wlist);  // per worker warp
     uint64_t* kept = smem + LY.kept;          // [tiles]
     int* opre = reinterpret_cast<int*>(smem + LY.opre);
@@ -240,16 +257,19 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
     const unsigned l = lane_id();
     const int warp = threadIdx.x >> 5;
 
+    const int role = (warp & 3) == 0 ? -1 : warp - 1 - warp / 4;  // index among non-idle warps
     if (warp == 0) {
         // ------------------------------------------------------------ resolver
-        // Window of tile t lives in slot t % RV_RR; one cp.async group per tile
-        // (empty past the end), RV_RP groups in flight.
+        // Window of tile t (blocks d = 0..RV_DR) lives in slot t % RV_RR; one
+        // cp.async group per tile (empty past the end), RV_RP in flight.
         for (int t = 0; t < RV_RP; ++t) {
             if (t < T) window_copy<RV_RB>(rwin + static_cast<size_t>(t % RV_RR) * RV_RB * 64,
                                           band + static_cast<int64_t>(t) * BW, l);
-            else empty_group();
+            commit_group();
         }
-        uint64_t K1 = 0, K2 = 0;  // kept sets of tiles t-1, t-2
+        uint64_t Kh[RV_DR + 1];  // Kh[d] = kept set of tile t-d (0 before the first tile)
+#pragma unroll
+        for (int d = 0; d <= RV_DR; ++d) Kh[d] = 0;
         int count = 0, t = 0;
         bool timeout = false;
         for (; t < T; ++t) {
@@ -258,14 +278,19 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
             if (!mbar_wait(&S.ready[t % RV_KR], t / RV_KR, nullptr)) { timeout = true; break; }
             const ulonglong2* wv =
                 reinterpret_cast<const ulonglong2*>(rwin + static_cast<size_t>(t % RV_RR) * RV_RB * 64);
-            const ulonglong2 dg = wv[l], b1 = wv[32 + l], b2 = wv[64 + l];
-            const uint64_t xa = (b1.x & K1) | (b2.x & K2);
-            const uint64_t xb = (b1.y & K1) | (b2.y & K2);
+            uint64_t xa = 0, xb = 0;
+#pragma unroll
+            for (int d = 1; d <= RV_DR; ++d) {
+                const ulonglong2 v = wv[d * 32 + l];
+                xa |= v.x & Kh[d];
+                xb |= v.y & Kh[d];
+            }
             const uint64_t near = ballot64(xa != 0, xb != 0);
-            const int rem = n - t * 64;
-            const uint64_t valid = rem >= 64 ? ~0ull : ((1ull << rem) - 1ull);
-            const uint64_t cand = ~(S.far[t % RV_KR] | near) & valid;
-            uint64_t K = tile_greedy(cand, dg.x, dg.y);
+            uint64_t K = S.spec[t % RV_KR];
+            if (K & near) {  // the speculation kept a box a recent tile removes: re-decide
+                const ulonglong2 dg = wv[l];
+                K = resolve_tile_col(S.cand[t % RV_KR] & ~near, dg.x, dg.y);
+            }
             const int nk = __popcll(K);
             const bool last = max_out > 0 && count + nk >= max_out;
             if (last) K = lowest_bits(K, max_out - count);
@@ -275,13 +300,14 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
                 mbar_arrive(&S.pub[t % RV_KR]);  // release: kept[t] visible
             }
             if (last) { ++t; break; }
-            K2 = K1;
-            K1 = K;
+#pragma unroll
+            for (int d = RV_DR; d > 1; --d) Kh[d] = Kh[d - 1];
+            Kh[1] = K;
             // Refill the slot of tile t-1 (every lane is past it) with tile t+RV_RP.
             const int tn = t + RV_RP;
             if (tn < T) window_copy<RV_RB>(rwin + static_cast<size_t>(tn % RV_RR) * RV_RB * 64,
                                            band + static_cast<int64_t>(tn) * BW, l);
-            else empty_group();
+            commit_group();
         }
         // No copy may land after the CTA exits.
         asm volatile("cp.async.wait_all;\n" ::: "memory");
@@ -291,25 +317,24 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
             __threadfence_block();
             *reinterpret_cast<volatile int*>(&S.stop) = 1;
         }
-    } else if (warp <= RV_NH) {
+    } else if (role >= 0 && role < RV_NH) {
         // ------------------------------------------------------------- helpers
-        const int h = warp - 1;
-        uint64_t* myw = hwin + static_cast<size_t>(h) * RV_HR * RV_HB * 64;
-        // Own tile i (tile h + RV_NH*i) lives in slot i % RV_HR; RV_HR-1 groups in flight.
-        for (int i = 0; i < RV_HR - 1; ++i) {
+        const int h = role;
+        uint64_t* myw = hwin + static_cast<size_t>(h) * RV_HR * RV_HW * 64;
+        auto fill = [&](int i) {  // own tile i: diagonal block + far blocks into slot i % RV_HR
             const int tt = h + RV_NH * i;
-            if (tt < T) window_copy<RV_HB>(myw + static_cast<size_t>(i % RV_HR) * RV_HB * 64,
-                                           band + static_cast<int64_t>(tt) * BW + RV_RB * 64, l);
-            else empty_group();
-        }
+            if (tt < T) {
+                uint64_t* dst = myw + static_cast<size_t>(i % RV_HR) * RV_HW * 64;
+                const uint64_t* src = band + static_cast<int64_t>(tt) * BW;
+                window_copy<1>(dst, src, l);
+                window_copy<RV_HB>(dst + 64, src + (RV_DR + 1) * 64, l);
+            }
+            commit_group();
+        };
+        for (int i = 0; i < RV_HR - 1; ++i) fill(i);
         for (int i = 0; h + RV_NH * i < T; ++i) {
             const int t = h + RV_NH * i;
-            {   // keep RV_HR-1 copies in flight: issue own tile i+RV_HR-1 into the slot freed by i-1
-                const int tn = h + RV_NH * (i + RV_HR - 1);
-                if (tn < T) window_copy<RV_HB>(myw + static_cast<size_t>((i + RV_HR - 1) % RV_HR) * RV_HB * 64,
-                                               band + static_cast<int64_t>(tn) * BW + RV_RB * 64, l);
-                else empty_group();
-            }
+            fill(i + RV_HR - 1);  // into the slot freed by own tile i-1
             // Kept sets of tiles <= t-RV_DR-1, and the workers' part of word t:
             // worker groups finish tiles out of order, so wait for every tile
             // since this helper's previous tile (t-RV_NH): together with that
@@ -324,31 +349,36 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
             wait_groups<RV_HR - 1>();
             __syncwarp();
             const ulonglong2* wv =
-                reinterpret_cast<const ulonglong2*>(myw + static_cast<size_t>(i % RV_HR) * RV_HB * 64);
+                reinterpret_cast<const ulonglong2*>(myw + static_cast<size_t>(i % RV_HR) * RV_HW * 64);
             uint64_t xa = 0, xb = 0;
 #pragma unroll
             for (int d = RV_DR + 1; d <= RV_L; ++d) {
                 const uint64_t Kd = t - d >= 0 ? kept[t - d] : 0ull;
-                const ulonglong2 v = wv[(d - RV_DR - 1) * 32 + l];
+                const ulonglong2 v = wv[(d - RV_DR) * 32 + l];
                 xa |= v.x & Kd;
                 xb |= v.y & Kd;
             }
-            const uint64_t word = removed[t] | ballot64(xa != 0, xb != 0);
+            const int rem = n - t * 64;
+            const uint64_t valid = rem >= 64 ? ~0ull : ((1ull << rem) - 1ull);
+            const uint64_t cand = ~(removed[t] | ballot64(xa != 0, xb != 0)) & valid;
+            const ulonglong2 dg = wv[l];
+            const uint64_t spec = tile_greedy(cand, dg.x, dg.y);
             if (l == 0) {
-                S.far[t % RV_KR] = word;
+                S.cand[t % RV_KR] = cand;
+                S.spec[t % RV_KR] = spec;
                 mbar_arrive(&S.ready[t % RV_KR]);
             }
             __syncwarp();
         }
         asm volatile("cp.async.wait_all;\n" ::: "memory");
-    } else if ((warp & 3) != 0 && (warp - 1 - RV_NH - warp / 4) < RV_G * RV_WPG) {
+    } else if (role >= RV_NH && (role - RV_NH) / RV_WPG < G) {
         // ------------------------------------------------------------- workers
-        const int wk = warp - 1 - RV_NH - warp / 4;  // index among worker warps
+        const int wk = role - RV_NH;  // index among worker warps
         const int g = wk / RV_WPG;
         const int wg = wk % RV_WPG;
         const int gt = wg * 32 + static_cast<int>(l);
         uint64_t* gfl = fl + static_cast<size_t>(g) * 64 * NB;
-        for (int r = g; r < T; r += RV_G) {
+        for (int r = g; r < T; r += G) {
             // Chunk bitmaps of the tile's 64 rows (independent of the decision).
             if (rowbits) {
                 for (int q = gt; q < 64 * NB; q += RV_GT) {

@@ -319,3 +319,16 @@ def test_resolve_long_chains():
         got = g.resolve_mask(g.iou_mask(torch.from_numpy(b).cuda(), thr)).cpu().numpy()
         assert got.tolist() == exp.tolist()
         assert _gpu_nms(b, s, thr).tolist() == exp.tolist()
+
+
+def test_largest_single_image():
+    """n = NMS_MAX_SINGLE_N (2^18): the widest chunk bitmaps and the largest
+    shared-memory layout of the resolve; dense clusters keep the oracle quick."""
+    n = g.NMS_MAX_SINGLE_N
+    rng = np.random.default_rng(77)
+    centres = rng.uniform(0, 4000, (800, 2))
+    c = centres[rng.integers(0, 800, n)] + rng.normal(0, 2, (n, 2))
+    wh = rng.uniform(20, 40, (n, 2))
+    b = np.concatenate([c - wh / 2, c + wh / 2], 1).astype(np.float32)
+    s = rng.uniform(0, 1, n).astype(np.float32)
+    _check_single(b, s, 0.5)

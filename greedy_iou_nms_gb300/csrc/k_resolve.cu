@@ -27,9 +27,11 @@
 // without the boxes (a) removed.  Its critical path per tile is the (a) test
 // and the hand-over of the kept set.
 //
-// The column-view windows arrive by lane-parallel cp.async copies into
-// shared-memory rings (bulk copies cost ~200 cycles of issue each on this SM,
-// too much for one small window per tile); every hand-over between roles is
+// The column-view windows arrive by lane-parallel cp.async copies (bulk
+// copies cost ~200 cycles of issue each on this SM, too much for one small
+// window per tile) into the helpers' shared-memory rings; the resolver reads
+// the blocks it needs from the helper's slot, so it issues no global memory
+// operation of its own.  Every hand-over between roles is
 // an mbarrier, waiters off the critical path nap between attempts, and every
 // wait is bounded and gives up with NMS_ERR_TIMEOUT.  The resolver owns a
 // scheduler partition: the warps that share warp 0's partition (4, 8, ...)
@@ -42,11 +44,7 @@ namespace gbnms {
 
 constexpr int RV_L = BAND_L;               // tiles covered by the column-view band
 constexpr int RV_DR = 4;                   // distances the resolver tests itself
-constexpr int RV_RB = RV_DR + 1;           // blocks of a resolver window (d = 0..RV_DR)
-constexpr int RV_HB = RV_L - RV_DR;        // far blocks of a helper window (d = RV_DR+1..RV_L)
-constexpr int RV_HW = RV_HB + 1;           // blocks of a helper window: diagonal + far blocks
-constexpr int RV_RP = 8;                   // resolver window prefetch distance (tiles)
-constexpr int RV_RR = RV_RP + 1;           // resolver window slots
+constexpr int RV_HW = RV_L + 1;            // blocks of a window: the whole band of one tile
 constexpr int RV_NH = 4;                   // helper warps (tiles round-robin)
 constexpr int RV_HR = 3;                   // window slots per helper
 constexpr int RV_WARPS = 32;
@@ -200,7 +198,7 @@ __host__ __device__ __forceinline__ int resolve_bitmap_words(int m_bound)
 }
 
 struct ResolveLayout {
-    size_t removed, rwin, hwin, fl, wlist, kept, opre, total;  // offsets in 64-bit words / bytes
+    size_t removed, hwin, fl, wlist, kept, opre, total;  // offsets in 64-bit words / bytes
 };
 
 __host__ __device__ __forceinline__ ResolveLayout resolve_layout(int m_bound, int NB)
@@ -208,8 +206,7 @@ __host__ __device__ __forceinline__ ResolveLayout resolve_layout(int m_bound, in
     ResolveLayout L;
     const size_t tiles = static_cast<size_t>((m_bound + 63) / 64);
     L.removed = 0;
-    L.rwin = L.removed + static_cast<size_t>(resolve_bitmap_words(m_bound));
-    L.hwin = L.rwin + static_cast<size_t>(RV_RR) * RV_RB * 64;
+    L.hwin = L.removed + static_cast<size_t>(resolve_bitmap_words(m_bound));
     L.fl = L.hwin + static_cast<size_t>(RV_NH) * RV_HR * RV_HW * 64;
     L.wlist = L.fl + static_cast<size_t>(resolve_groups(NB)) * 64 * NB;  // bytes [worker warps][64]
     L.kept = L.wlist + static_cast<size_t>(RV_G) * RV_WPG * 64 / 8;
@@ -235,7 +232,6 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
     const ResolveLayout LY = resolve_layout(m_bound, NB);
     const int G = resolve_groups(NB);         // worker groups
     uint64_t* removed = smem + LY.removed;
-    uint64_t* rwin = smem + LY.rwin;          // [RV_RR][RV_RB*64]
     uint64_t* hwin = smem + LY.hwin;          // [RV_NH][RV_HR][RV_HW*64]
     uint64_t* fl = smem + LY.fl;              // [G][64][NB]
     unsigned char* wlist = reinterpret_cast<unsigned char*>(smem + LY.wlist);  // per worker warp
@@ -260,24 +256,17 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
     const int role = (warp & 3) == 0 ? -1 : warp - 1 - warp / 4;  // index among non-idle warps
     if (warp == 0) {
         // ------------------------------------------------------------ resolver
-        // Window of tile t (blocks d = 0..RV_DR) lives in slot t % RV_RR; one
-        // cp.async group per tile (empty past the end), RV_RP in flight.
-        for (int t = 0; t < RV_RP; ++t) {
-            if (t < T) window_copy<RV_RB>(rwin + static_cast<size_t>(t % RV_RR) * RV_RB * 64,
-                                          band + static_cast<int64_t>(t) * BW, l);
-            commit_group();
-        }
         uint64_t Kh[RV_DR + 1];  // Kh[d] = kept set of tile t-d (0 before the first tile)
 #pragma unroll
         for (int d = 0; d <= RV_DR; ++d) Kh[d] = 0;
         int count = 0, t = 0;
         bool timeout = false;
         for (; t < T; ++t) {
-            wait_groups<RV_RP - 1>();
-            __syncwarp();
             if (!mbar_wait(&S.ready[t % RV_KR], t / RV_KR, nullptr)) { timeout = true; break; }
-            const ulonglong2* wv =
-                reinterpret_cast<const ulonglong2*>(rwin + static_cast<size_t>(t % RV_RR) * RV_RB * 64);
+            // The helper of tile t left the tile's band window in its slot.
+            const int hh = t % RV_NH, hi = t / RV_NH;
+            const ulonglong2* wv = reinterpret_cast<const ulonglong2*>(
+                hwin + (static_cast<size_t>(hh) * RV_HR + hi % RV_HR) * RV_HW * 64);
             uint64_t xa = 0, xb = 0;
 #pragma unroll
             for (int d = 1; d <= RV_DR; ++d) {
@@ -303,14 +292,7 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
 #pragma unroll
             for (int d = RV_DR; d > 1; --d) Kh[d] = Kh[d - 1];
             Kh[1] = K;
-            // Refill the slot of tile t-1 (every lane is past it) with tile t+RV_RP.
-            const int tn = t + RV_RP;
-            if (tn < T) window_copy<RV_RB>(rwin + static_cast<size_t>(tn % RV_RR) * RV_RB * 64,
-                                           band + static_cast<int64_t>(tn) * BW, l);
-            commit_group();
         }
-        // No copy may land after the CTA exits.
-        asm volatile("cp.async.wait_all;\n" ::: "memory");
         if (l == 0) {
             S.ntiles = t;
             if (timeout && status) set_status(status, NMS_ERR_TIMEOUT);
@@ -321,20 +303,21 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
         // ------------------------------------------------------------- helpers
         const int h = role;
         uint64_t* myw = hwin + static_cast<size_t>(h) * RV_HR * RV_HW * 64;
-        auto fill = [&](int i) {  // own tile i: diagonal block + far blocks into slot i % RV_HR
+        auto fill = [&](int i) {  // own tile i: its whole band window into slot i % RV_HR
             const int tt = h + RV_NH * i;
-            if (tt < T) {
-                uint64_t* dst = myw + static_cast<size_t>(i % RV_HR) * RV_HW * 64;
-                const uint64_t* src = band + static_cast<int64_t>(tt) * BW;
-                window_copy<1>(dst, src, l);
-                window_copy<RV_HB>(dst + 64, src + (RV_DR + 1) * 64, l);
-            }
+            if (tt < T)
+                window_copy<RV_HW>(myw + static_cast<size_t>(i % RV_HR) * RV_HW * 64,
+                                   band + static_cast<int64_t>(tt) * BW, l);
             commit_group();
         };
         for (int i = 0; i < RV_HR - 1; ++i) fill(i);
         for (int i = 0; h + RV_NH * i < T; ++i) {
             const int t = h + RV_NH * i;
-            fill(i + RV_HR - 1);  // into the slot freed by own tile i-1
+            // The slot of own tile i-1 (tile t-RV_NH) is free once the resolver
+            // has published that tile; refill it with own tile i+RV_HR-1.
+            if (i > 0 && !mbar_wait(&S.pub[(t - RV_NH) % RV_KR], (t - RV_NH) / RV_KR, &S.stop, RV_NAP_HELPER))
+                break;
+            fill(i + RV_HR - 1);
             // Kept sets of tiles <= t-RV_DR-1, and the workers' part of word t:
             // worker groups finish tiles out of order, so wait for every tile
             // since this helper's previous tile (t-RV_NH): together with that
@@ -354,7 +337,7 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
 #pragma unroll
             for (int d = RV_DR + 1; d <= RV_L; ++d) {
                 const uint64_t Kd = t - d >= 0 ? kept[t - d] : 0ull;
-                const ulonglong2 v = wv[(d - RV_DR) * 32 + l];
+                const ulonglong2 v = wv[d * 32 + l];
                 xa |= v.x & Kd;
                 xb |= v.y & Kd;
             }
@@ -407,7 +390,18 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
                 __syncwarp();
             }
             const int c0 = (r + 1) >> 2;
-            for (int cq = c0 + static_cast<int>(l); nmine && cq < T256; cq += 32) {
+            // Chunks any of the warp's rows has a bit in (all of them when the
+            // bitmaps are absent); lane l takes chunks 64q+l and 64q+l+32.
+            const int NQ = rowbits ? NB : (T256 + 63) / 64;
+            for (int q = 0; nmine && q < NQ; ++q) {
+              uint64_t un = ~0ull;
+              if (rowbits) {
+                  un = 0;
+                  for (int j = 0; j < nmine; ++j) un |= gfl[rows[j] * NB + q];
+              }
+              for (int hh = 0; hh < 2; ++hh) {
+                const int cq = 64 * q + static_cast<int>(l) + 32 * hh;
+                if (!((un >> (cq & 63)) & 1ull) || cq < c0 || cq >= T256) continue;
                 uint64_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
                 for (int j0 = 0; j0 < nmine; j0 += RV_BATCH) {
                     // Up to RV_BATCH rows per round, all loads in flight together.
@@ -440,6 +434,7 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
                 if (a1) atomicOr(dst + 1, a1);
                 if (a2) atomicOr(dst + 2, a2);
                 if (a3) atomicOr(dst + 3, a3);
+              }
             }
             group_bar(g);
             if (gt == 0) {

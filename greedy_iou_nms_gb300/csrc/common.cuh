@@ -80,36 +80,20 @@ __device__ __forceinline__ bool well_formed(float4 b, float area)
 
 // Threshold constants of the division-free test (computed on the host).
 //   With s = area_a + area_b and a = inter as binary32 values, for well-formed
-//   boxes and 2^-20 <= thr <= 2^20:
-//     a >  RN(k_hi * s)  implies  RN(a / RN(s - a)) >  thr   (suppress)
-//     a <= RN(k_lo * s)  implies  RN(a / RN(s - a)) <= thr   (keep)
+//   boxes and 2^-20 <= thr <= 2^20, and k*s the exact real product:
+//     a >  k_hi * s  implies  RN(a / RN(s - a)) >  thr   (suppress)
+//     a <= k_lo * s  implies  RN(a / RN(s - a)) <= thr   (keep)
 //   and any pair between the two bounds is decided by the exact division.
+//   Proof sketch: q = a/(s-a) and the two roundings put the canonical IoU in
+//   q(1 +- 2^-23); q > T2 = thr(1+2^-21) <=> a > s T2/(1+T2), and k_hi exceeds
+//   that ratio by a factor 1+2^-22 (likewise k_lo is below T1/(1+T1), T1 =
+//   thr(1-2^-21)), so the rounded IoU lands strictly on the proven side.
 struct ThrParams {
     float thr;     // the binary32 threshold
     float k_hi;    // >= (T2/(1+T2)) (1+2^-22), T2 = thr (1+2^-21)
     float k_lo;    // <= (T1/(1+T1)) (1-2^-22), T1 = thr (1-2^-21)
     int fast_ok;   // thr within [2^-20, 2^20]
 };
-
-// Per-pair test used by the mask kernels.  Returns the suppression bit of the
-// fast test; sets `unsure` when the pair lies in the band the fast test does
-// not decide.
-__device__ __forceinline__ bool suppress_fast(float4 a, float area_a, float4 b, float area_b,
-                                              const ThrParams& p, bool& unsure)
-{
-    float xx1 = fmaxf(a.x, b.x);
-    float yy1 = fmaxf(a.y, b.y);
-    float xx2 = fminf(a.z, b.z);
-    float yy2 = fminf(a.w, b.w);
-    float w = fmaxf(__fsub_rn(xx2, xx1), 0.0f);
-    float h = fmaxf(__fsub_rn(yy2, yy1), 0.0f);
-    float inter = __fmul_rn(w, h);
-    float s = __fadd_rn(area_a, area_b);
-    bool yes = inter > __fmul_rn(p.k_hi, s);
-    bool maybe = inter > __fmul_rn(p.k_lo, s);
-    unsure |= (yes != maybe);
-    return yes;
-}
 
 // ------------------------------------------------------------- warp helpers
 

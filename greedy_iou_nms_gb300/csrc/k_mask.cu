@@ -9,7 +9,7 @@
 // (Part 2)", section "Optimization 1: tile the IoU matrix": coordinates loaded
 // once per tile and reused by every row.
 //
-// GB300 shape: a CTA computes a 256-row x 256-column tile.  Each lane holds two
+// GB300 shape: a CTA computes a 128-row x 256-column tile.  Each lane holds two
 // row boxes in registers and walks the 256 staged column boxes (broadcast
 // shared-memory reads), so a row's four words of the tile (one 32-byte
 // sector) are built in registers and written with two 16-byte stores.  The
@@ -23,24 +23,70 @@
 #include "common.cuh"
 #include "internal.h"
 
+#ifndef GBNMS_MASK_WARPS
+#define GBNMS_MASK_WARPS 4
+#endif
+#ifndef GBNMS_MASK_UNROLL
+#define GBNMS_MASK_UNROLL 8
+#endif
+namespace gbnms {
+constexpr int kMaskUnroll = GBNMS_MASK_UNROLL;  // unroll of the 32-column inner loop
+}
+
 namespace gbnms {
 
-constexpr int MT = 256;         // tile edge (rows and columns)
-constexpr int M_WARPS = 4;      // 4 warps x 64 rows
+constexpr int MT = 256;         // tile width (columns)
+constexpr int M_WARPS = GBNMS_MASK_WARPS;  // warps of 64 rows per tile
+constexpr int MR = M_WARPS * 64;  // tile height (rows)
 constexpr int M_THREADS = M_WARPS * 32;
 
 // Far-away zero-area box used to pad ragged tiles: overlaps nothing.
 __device__ __forceinline__ float4 pad_box() { return make_float4(3e38f, 3e38f, 3e38f, 3e38f); }
 
-// Linear index k of the tile triangle (column-major: column c holds rows
-// 0..c) -> (row tile a, column tile c).
+// Linear index k of the tile triangle -> (row tile a, column tile c).  With
+// r = MT/MR row tiles per column tile, column tile c meets row tiles
+// a = 0 .. r(c+1)-1, so the tiles of columns before c number r c(c+1)/2;
+// enumeration is column by column.
 __device__ __forceinline__ void tri_coords(long long k, int& a, int& c)
 {
-    long long cc = static_cast<long long>((sqrt(8.0 * static_cast<double>(k) + 1.0) - 1.0) * 0.5);
-    while ((cc + 1) * (cc + 2) / 2 <= k) ++cc;
-    while (cc * (cc + 1) / 2 > k) --cc;
+    constexpr long long r = MT / MR;
+    long long cc = static_cast<long long>((sqrt(8.0 * static_cast<double>(k) / r + 1.0) - 1.0) * 0.5);
+    while (r * (cc + 1) * (cc + 2) / 2 <= k) ++cc;
+    while (r * cc * (cc + 1) / 2 > k) --cc;
     c = static_cast<int>(cc);
-    a = static_cast<int>(k - cc * (cc + 1) / 2);
+    a = static_cast<int>(k - r * cc * (cc + 1) / 2);
+}
+static_assert(MT == 2 * MR || MT == MR, "tri_coords handles column tiles one or two row tiles wide");
+
+// Sign bit of RN(k*s - a): set iff the exact k*s - a is negative, i.e.
+// a > k*s (the product inside a fused multiply-add is not rounded).
+__device__ __forceinline__ uint32_t sign_above(float k, float s, float a)
+{
+    return __float_as_uint(__fmaf_rn(k, s, -a));
+}
+
+// One 32-column half of the division-free test for one row: shifts the
+// decision bits into `yes` and the "not surely below" bits into `maybe`,
+// highest column first, so bit k ends up meaning column k.  For well-formed
+// boxes and the constants of ThrParams, a > k_hi*s proves suppression and
+// a <= k_lo*s proves no suppression (common.cuh); a pair with maybe and not
+// yes is left to the exact division.  The intersection is fmax(w,0)*h with h
+// unclamped: when h <= 0 the product is <= 0 and both tests say no, as the
+// canonical (clamped) intersection 0 would.
+__device__ __forceinline__ void half_fast(const float4* __restrict__ cb, const float* __restrict__ ca,
+                                          float4 r, float ar, float khi, float klo, uint32_t& yes,
+                                          uint32_t& maybe)
+{
+#pragma unroll kMaskUnroll
+    for (int k = 31; k >= 0; --k) {
+        const float4 c = cb[k];
+        const float w = fmaxf(__fsub_rn(fminf(r.z, c.z), fmaxf(r.x, c.x)), 0.0f);
+        const float h = __fsub_rn(fminf(r.w, c.w), fmaxf(r.y, c.y));
+        const float a = __fmul_rn(w, h);
+        const float s = __fadd_rn(ar, ca[k]);
+        yes = __funnelshift_l(sign_above(khi, s, a), yes, 1);
+        maybe = __funnelshift_l(sign_above(klo, s, a), maybe, 1);
+    }
 }
 
 template <bool FAST>
@@ -52,35 +98,28 @@ __device__ __forceinline__ void tile_rows(const float4* __restrict__ cbox, const
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         uint32_t lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
+        if (FAST) {
+            uint32_t ml0 = 0, mh0 = 0, ml1 = 0, mh1 = 0;
+            half_fast(cbox + q * 64, carea + q * 64, r0, ar0, p.k_hi, p.k_lo, lo0, ml0);
+            half_fast(cbox + q * 64, carea + q * 64, r1, ar1, p.k_hi, p.k_lo, lo1, ml1);
+            half_fast(cbox + q * 64 + 32, carea + q * 64 + 32, r0, ar0, p.k_hi, p.k_lo, hi0, mh0);
+            half_fast(cbox + q * 64 + 32, carea + q * 64 + 32, r1, ar1, p.k_hi, p.k_lo, hi1, mh1);
+            unsure |= ((ml0 & ~lo0) | (mh0 & ~hi0) | (ml1 & ~lo1) | (mh1 & ~hi1)) != 0;
+        } else {
 #pragma unroll 8
-        for (int k = 0; k < 32; ++k) {
-            float4 c = cbox[q * 64 + k];
-            float ac = carea[q * 64 + k];
-            bool s0, s1;
-            if (FAST) {
-                s0 = suppress_fast(r0, ar0, c, ac, p, unsure);
-                s1 = suppress_fast(r1, ar1, c, ac, p, unsure);
-            } else {
-                s0 = suppress_exact(r0, ar0, c, ac, p.thr);
-                s1 = suppress_exact(r1, ar1, c, ac, p.thr);
+            for (int k = 0; k < 32; ++k) {
+                const float4 c = cbox[q * 64 + k];
+                const float ac = carea[q * 64 + k];
+                lo0 |= static_cast<uint32_t>(suppress_exact(r0, ar0, c, ac, p.thr)) << k;
+                lo1 |= static_cast<uint32_t>(suppress_exact(r1, ar1, c, ac, p.thr)) << k;
             }
-            lo0 |= static_cast<uint32_t>(s0) << k;
-            lo1 |= static_cast<uint32_t>(s1) << k;
-        }
 #pragma unroll 8
-        for (int k = 0; k < 32; ++k) {
-            float4 c = cbox[q * 64 + 32 + k];
-            float ac = carea[q * 64 + 32 + k];
-            bool s0, s1;
-            if (FAST) {
-                s0 = suppress_fast(r0, ar0, c, ac, p, unsure);
-                s1 = suppress_fast(r1, ar1, c, ac, p, unsure);
-            } else {
-                s0 = suppress_exact(r0, ar0, c, ac, p.thr);
-                s1 = suppress_exact(r1, ar1, c, ac, p.thr);
+            for (int k = 0; k < 32; ++k) {
+                const float4 c = cbox[q * 64 + 32 + k];
+                const float ac = carea[q * 64 + 32 + k];
+                hi0 |= static_cast<uint32_t>(suppress_exact(r0, ar0, c, ac, p.thr)) << k;
+                hi1 |= static_cast<uint32_t>(suppress_exact(r1, ar1, c, ac, p.thr)) << k;
             }
-            hi0 |= static_cast<uint32_t>(s0) << k;
-            hi1 |= static_cast<uint32_t>(s1) << k;
         }
         w0[q] = (static_cast<uint64_t>(hi0) << 32) | lo0;
         w1[q] = (static_cast<uint64_t>(hi1) << 32) | lo1;
@@ -116,10 +155,10 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
     int a, c;
     tri_coords(blockIdx.x, a, c);
     const int T = (n + MT - 1) / MT;
-    if (c >= T) return;  // beyond the device-side count
+    if (c >= T || a * MR >= n) return;  // beyond the device-side count
 
     const int cb = c * MT;
-    const int rbase = a * MT;
+    const int rbase = a * MR;
     bool ok = true;
     for (int t = threadIdx.x; t < MT; t += M_THREADS) {
         int j = cb + t;
@@ -158,7 +197,7 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
         tile_rows<false>(cbox, carea, r0, ar0, r1, ar1, p, w0, w1, unsure);
     }
 
-    if (a == c) {
+    if (rbase + MR > cb) {  // the tile meets the diagonal
         clip_words(w0, i0, cb, n);
         clip_words(w1, i1, cb, n);
     } else {
@@ -170,7 +209,7 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
     // final words with two ballots per column.  Lane l keeps columns l and
     // l+32.
     if (band) {
-        const int R = 4 * a + wp;
+        const int R = rbase / 64 + wp;
         const int T64 = (n + 63) / 64;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -207,7 +246,7 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
 int64_t mask_tiles(int64_t n)
 {
     int64_t T = (n + MT - 1) / MT;
-    return T * (T + 1) / 2;
+    return (MT / MR) * T * (T + 1) / 2;
 }
 
 void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const ThrParams& p,

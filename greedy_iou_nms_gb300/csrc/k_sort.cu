@@ -30,19 +30,20 @@ __global__ void prefilter_kernel(const float* __restrict__ scores, int n, float 
     if (pass) cand[base + __popc(ballot & ((1u << l) - 1u))] = i;
 }
 
-// Rank sort.  Each CTA owns RS_I candidates (lanes l and l+32 of every warp)
-// and its RS_WARPS warps split the candidates j to compare against; a
-// candidate's sorted position is the number of candidates whose (score key,
-// index) is smaller.  The keys are unique, so the positions form a
-// permutation and the sort is stable by construction.
+// Rank sort.  A candidate's sorted position is the number of candidates whose
+// (score key, index) is smaller; the keys are unique, so the positions form a
+// permutation and the sort is stable by construction.  Each CTA ranks RS_I
+// candidates against all of them: lane l of a warp owns 4 consecutive
+// candidates (group l % 8) and takes every fourth 4-key group of the warp's
+// share (subset l / 8), so one 16-byte shared-memory load feeds 16 compares.
 //
 // Without a pre-filter the candidate list is the input in index order, so a
-// j before the CTA's block counts when key_j <= key_i and a j after it when
-// key_j < key_i: one 32-bit compare per pair, keys staged in shared memory
-// four per 16-byte load.  With a pre-filter the list order is arbitrary and
-// the 64-bit (key, index) compare is used.
+// j before candidate i counts when key_j <= key_i and a j after it when key_j
+// < key_i: one 32-bit compare per pair.  With a pre-filter the list order is
+// arbitrary and the 64-bit (key, index) compare is used.
 constexpr int RS_WARPS = 16;
-constexpr int RS_I = 64;         // candidates ranked per CTA
+constexpr int RS_I = 32;         // candidates ranked per CTA (8 lanes x 4)
+constexpr int RS_SUB = 4;        // key subsets per warp (lanes / 8)
 constexpr int RS_CHUNK = 4096;   // keys staged in shared memory per step
 
 __global__ void __launch_bounds__(RS_WARPS * 32)
@@ -52,7 +53,7 @@ rank_sort_kernel(const float* __restrict__ scores, const float4* __restrict__ bo
                  uint64_t* __restrict__ rowbits, int NB)
 {
     __shared__ __align__(16) uint64_t keys64[RS_CHUNK];   // u32 keys use the first half
-    __shared__ uint32_t part[RS_WARPS][RS_I];
+    __shared__ uint32_t part[RS_WARPS * RS_SUB][RS_I];
     uint32_t* keys32 = reinterpret_cast<uint32_t*>(keys64);
 
     const int m = m_dev ? *m_dev : m_bound;
@@ -69,46 +70,75 @@ rank_sort_kernel(const float* __restrict__ scores, const float4* __restrict__ bo
 
     const unsigned l = lane_id();
     const int w = threadIdx.x >> 5;
-    const int ia = i0 + l, ib = i0 + 32 + l;
-    const int xa = ia < m ? (cand ? cand[ia] : ia) : 0;
-    const int xb = ib < m ? (cand ? cand[ib] : ib) : 0;
-    uint32_t ca = 0, cb = 0;
+    const int ig = l & 7, js = l >> 3;
+    const int sub = w * RS_SUB + js;           // this lane's share of the keys
+    const int nsub = RS_WARPS * RS_SUB;
+    int iv[4];
+    uint32_t cnt[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) iv[u] = i0 + 4 * ig + u;
 
     if (!cand) {
-        const uint32_t ka = ia < m ? score_key(scores[xa]) : 0xffffffffu;
-        const uint32_t kb = ib < m ? score_key(scores[xb]) : 0xffffffffu;
+        uint32_t kk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) kk[u] = iv[u] < m ? score_key(scores[iv[u]]) : 0xffffffffu;
         for (int c0 = 0; c0 < m; c0 += RS_CHUNK) {
             const int cn = min(RS_CHUNK, m - c0);
             __syncthreads();
-            for (int t = threadIdx.x; t < cn; t += blockDim.x) keys32[t] = score_key(scores[c0 + t]);
+            // Four scores per 16-byte load when the chunk start is aligned (all
+            // loads of a thread in flight together); the ragged end pads with
+            // the largest key.
+            const bool vec = ((reinterpret_cast<uintptr_t>(scores + c0) & 15) == 0);
+            if (vec) {
+                const float4* s4 = reinterpret_cast<const float4*>(scores + c0);
+                const int n4 = cn >> 2;
+#pragma unroll 4
+                for (int t = threadIdx.x; t < n4; t += blockDim.x) {
+                    const float4 v = s4[t];
+                    reinterpret_cast<uint4*>(keys32)[t] =
+                        make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
+                }
+                for (int t = 4 * n4 + threadIdx.x; t < cn; t += blockDim.x) keys32[t] = score_key(scores[c0 + t]);
+            } else {
+#pragma unroll 4
+                for (int t = threadIdx.x; t < cn; t += blockDim.x) keys32[t] = score_key(scores[c0 + t]);
+            }
             for (int t = cn + threadIdx.x; t < ((cn + 3) & ~3); t += blockDim.x) keys32[t] = 0xffffffffu;
             __syncthreads();
             const uint4* k4 = reinterpret_cast<const uint4*>(keys32);
-            for (int q = w; 4 * q < cn; q += RS_WARPS) {
+            for (int q = sub; 4 * q < cn; q += nsub) {
                 const uint4 v = k4[q];
                 const int j = c0 + 4 * q;
                 if (j + 3 < i0) {               // all four before the block: ties count
-                    ca += (v.x <= ka) + (v.y <= ka) + (v.z <= ka) + (v.w <= ka);
-                    cb += (v.x <= kb) + (v.y <= kb) + (v.z <= kb) + (v.w <= kb);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        cnt[u] += (v.x <= kk[u]) + (v.y <= kk[u]) + (v.z <= kk[u]) + (v.w <= kk[u]);
                 } else if (j >= i0 + RS_I) {    // all after: strict
-                    ca += (v.x < ka) + (v.y < ka) + (v.z < ka) + (v.w < ka);
-                    cb += (v.x < kb) + (v.y < kb) + (v.z < kb) + (v.w < kb);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        cnt[u] += (v.x < kk[u]) + (v.y < kk[u]) + (v.z < kk[u]) + (v.w < kk[u]);
                 } else {
                     const uint32_t e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int jj = j + u;
+                    for (int x = 0; x < 4; ++x) {
+                        const int jj = j + x;
                         if (jj < m) {
-                            ca += (e[u] < ka) || (e[u] == ka && jj < ia);
-                            cb += (e[u] < kb) || (e[u] == kb && jj < ib);
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                cnt[u] += (e[x] < kk[u]) || (e[x] == kk[u] && jj < iv[u]);
                         }
                     }
                 }
             }
         }
     } else {
-        const uint64_t ka = ia < m ? order_key(scores[xa], xa) : ~0ull;
-        const uint64_t kb = ib < m ? order_key(scores[xb], xb) : ~0ull;
+        int xv[4];
+        uint64_t kk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            xv[u] = iv[u] < m ? cand[iv[u]] : 0;
+            kk[u] = iv[u] < m ? order_key(scores[xv[u]], xv[u]) : ~0ull;
+        }
         for (int c0 = 0; c0 < m; c0 += RS_CHUNK) {
             const int cn = min(RS_CHUNK, m - c0);
             __syncthreads();
@@ -117,24 +147,23 @@ rank_sort_kernel(const float* __restrict__ scores, const float4* __restrict__ bo
                 keys64[t] = order_key(scores[x], x);
             }
             __syncthreads();
-            for (int t = w; t < cn; t += RS_WARPS) {
+            for (int t = sub; t < cn; t += nsub) {
                 const uint64_t k = keys64[t];
-                ca += k < ka;
-                cb += k < kb;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) cnt[u] += k < kk[u];
             }
         }
     }
-    part[w][l] = ca;
-    part[w][l + 32] = cb;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) part[sub][4 * ig + u] = cnt[u];
     __syncthreads();
-    if (w < 2) {
-        const int e = w * 32 + l;
+    if (threadIdx.x < RS_I) {
+        const int e = threadIdx.x;
         const int i = i0 + e;
         if (i < m) {
             uint32_t r = 0;
-#pragma unroll
-            for (int q = 0; q < RS_WARPS; ++q) r += part[q][e];
-            const int x = e < 32 ? xa : xb;
+            for (int q = 0; q < nsub; ++q) r += part[q][e];
+            const int x = cand ? cand[i] : i;
             perm[r] = x;
             boxes_s[r] = boxes[x];
         }

@@ -176,6 +176,51 @@ def _algorithmic_resolve_bytes(wl):
     return int(8 * (row_words + wl.n)), len(keep)
 
 
+def time_workload(g, torch, wl, dev, flush, reps=30):
+    """Device time of one nms_run call on workload wl (inputs resident, L2
+    flushed before each call): median, p10 and p90 in microseconds."""
+    stream = torch.cuda.current_stream(dev)
+    batched = wl.class_ids is not None or wl.batch_offsets is not None
+    B = wl.batch if wl.batch_offsets is not None else 0
+    C = wl.num_classes if wl.class_ids is not None else 0
+    boxes = torch.from_numpy(wl.boxes).to(dev)
+    scores = torch.from_numpy(wl.scores).to(dev)
+    cls = torch.from_numpy(wl.class_ids).to(dev) if wl.class_ids is not None else None
+    off = torch.from_numpy(wl.batch_offsets).to(dev) if wl.batch_offsets is not None else None
+    cap = g.keep_capacity(wl.n, B if off is not None else None, wl.max_out)
+    keep = torch.empty(max(cap, 1), dtype=torch.int64, device=dev)
+    counts = torch.empty(max(B, 1), dtype=torch.int64, device=dev)
+    ws = g.Workspace(wl.n, B, C, device=dev)
+    score_thr = -math.inf if wl.score_thr is None else wl.score_thr
+
+    def call():
+        st = g.nms_run(boxes.data_ptr(), scores.data_ptr(), wl.n,
+                       cls.data_ptr() if cls is not None else 0, C,
+                       off.data_ptr() if off is not None else 0, B, wl.iou_thr, score_thr,
+                       wl.max_out, keep.data_ptr(), cap, counts.data_ptr(), 0, ws.ptr, ws.bytes,
+                       stream.cuda_stream)
+        if st != g.NMS_OK:
+            raise g.NmsError(st, "nms_run")
+
+    for _ in range(3):
+        call()
+    evs = []
+    for _ in range(reps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    us = sorted(1000 * a.elapsed_time(b) for a, b in evs)
+    q = lambda f: us[min(len(us) - 1, int(f * len(us)))]
+    med = statistics.median(us)
+    return {"us_median": med, "us_p10": q(0.1), "us_p90": q(0.9), "boxes_per_s": wl.n / (med / 1e6),
+            "gpairs_per_s": wl.pairs / (med / 1e6) / 1e9, "n": wl.n,
+            "kept": int(counts.sum().item()), "batched": batched}
+
+
 def run_gbnms(args):
     import torch
     import greedy_iou_nms_gb300 as g
@@ -348,6 +393,12 @@ def run_gbnms(args):
                 "unit": "GB/s", "frac": ach / hbm, "traffic": traffic,
                 "note": f"algorithmic mask bytes read {resolve_bytes}; peak {peak_kind}"}
 
+    per_config = None
+    if not args.no_configs:
+        per_config = {}
+        for name in W.CONFIGS:
+            per_config[name] = time_workload(g, torch, W.make(name, 0), dev, flush)
+
     cpu = None
     if not args.no_cpu_baseline:
         v, reps_cpu, secs = cpu_oracle_run(wl, args.cpu_seconds)
@@ -367,6 +418,7 @@ def run_gbnms(args):
         "mask_gbs": mask_bytes / (mask_ms / 1000) / 1e9,
         "mask_hbm_frac": mask_bytes / (mask_ms / 1000) / 1e9 / hbm,
         "kernels": kernels,
+        "per_config": per_config,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": n / (e2e_ms / 1000), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -417,6 +469,7 @@ def main():
     ap.add_argument("--impl", default="gbnms", choices=["gbnms", "reference"])
     ap.add_argument("--workload", default=W.HEADLINE)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config timing table")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.impl == "reference":

@@ -118,6 +118,35 @@ __device__ __forceinline__ uint64_t ballot64(bool lo, bool hi)
            (static_cast<uint64_t>(__ballot_sync(FULL, hi)) << 32);
 }
 
+// Transpose of a 64x64 bit matrix spread over a warp: lane l holds rows l
+// (a) and l+32 (b), bit c of a row meaning column c; afterwards lane l holds
+// columns l and l+32 the same way (bit r meaning row r).  Recursive block
+// swap: at step j the j x j blocks (rows with bit j clear, columns with bit j
+// set) and (rows with bit j set, columns with bit j clear) trade places.
+// j = 32 pairs a lane's own two rows; a smaller j pairs lane l with l ^ j.
+__device__ __forceinline__ void transpose64(uint64_t& a, uint64_t& b)
+{
+    const uint64_t t = ((a >> 32) ^ b) & 0x00000000ffffffffull;
+    b ^= t;
+    a ^= t << 32;
+    const unsigned l = lane_id();
+    constexpr uint64_t kMask[5] = {0x0000ffff0000ffffull, 0x00ff00ff00ff00ffull, 0x0f0f0f0f0f0f0f0full,
+                                   0x3333333333333333ull, 0x5555555555555555ull};
+#pragma unroll
+    for (int s = 0; s < 5; ++s) {
+        const int j = 16 >> s;
+        const uint64_t m = kMask[s];
+        const uint64_t pa = __shfl_xor_sync(FULL, a, j), pb = __shfl_xor_sync(FULL, b, j);
+        if (l & j) {  // second row of the pair: takes the first row's high block
+            a ^= ((pa >> j) ^ a) & m;
+            b ^= ((pb >> j) ^ b) & m;
+        } else {      // first row: takes the second row's low block
+            a ^= (((a >> j) ^ pa) & m) << j;
+            b ^= (((b >> j) ^ pb) & m) << j;
+        }
+    }
+}
+
 // Column-view tile resolve.  Lane l holds ca = C[l] and cb = C[l+32], where
 // bit k of C[b] is set iff box k (k < b) of the tile suppresses box b.
 // `cand` holds the tile's boxes no earlier kept box removed.  Each round, a

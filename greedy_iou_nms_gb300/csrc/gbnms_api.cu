@@ -3,11 +3,29 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "internal.h"
 
 namespace gbnms {
+
+void ensure_dynamic_smem(const void* kernel, size_t bytes)
+{
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, size_t> limit;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return;
+    std::lock_guard<std::mutex> lock(mu);
+    size_t& have = limit[{dev, kernel}];
+    if (bytes <= have) return;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) ==
+        cudaSuccess)
+        have = bytes;
+}
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -31,7 +49,9 @@ struct Layout {
 struct SingleLayout {
     int64_t ldw = 0;
     int NB = 0;  // 64-bit words of the per-row chunk bitmap
-    size_t status, m_count, cand, perm, boxes_s, rowbits, band, mask, total;
+    unsigned ecap = 0;  // pairs of the sparse list (0: no list, the walk resolves)
+    size_t status, m_count, ecount, cand, perm, boxes_s, keys, rowbits, band, edges, haspred, mask,
+        total;
 };
 
 SingleLayout single_layout(int64_t n)
@@ -41,13 +61,18 @@ SingleLayout single_layout(int64_t n)
     s.ldw = 4 * T;
     s.NB = static_cast<int>((T + 63) / 64 > 0 ? (T + 63) / 64 : 1);
     Layout L;
+    s.ecap = graph_edge_cap(static_cast<int>(n));
     s.status = L.add(4);
     s.m_count = L.add(4);
+    s.ecount = L.add(4);
     s.cand = L.add(4 * static_cast<size_t>(n));
     s.perm = L.add(4 * static_cast<size_t>(n));
     s.boxes_s = L.add(16 * static_cast<size_t>(n));
+    s.keys = L.add(sort_keys_bytes(static_cast<int>(n)));
     s.rowbits = L.add(8 * static_cast<size_t>(n) * static_cast<size_t>(s.NB));
     s.band = L.add(8 * static_cast<size_t>((n + 63) / 64) * (BAND_L + 1) * 64);
+    s.edges = L.add(4 * static_cast<size_t>(s.ecap));
+    s.haspred = L.add(s.ecap ? 8 * static_cast<size_t>((n + 63) / 64) : 0);
     s.mask = L.add(8 * static_cast<size_t>(n) * static_cast<size_t>(s.ldw));
     s.total = L.total;
     return s;
@@ -205,12 +230,17 @@ extern "C" nms_status nms_run(const float* boxes, const float* scores, int64_t n
         float4* boxes_s = at<float4>(workspace, L.boxes_s);
         uint64_t* mask = at<uint64_t>(workspace, L.mask);
         uint64_t* rowbits = at<uint64_t>(workspace, L.rowbits);
-        launch_rank_sort(scores, reinterpret_cast<const float4*>(boxes), cand, m_count,
-                         static_cast<int>(n), perm, boxes_s, status, rowbits, L.NB, st);
+        uint32_t* edges = L.ecap ? at<uint32_t>(workspace, L.edges) : nullptr;
+        unsigned* ecount = at<unsigned>(workspace, L.ecount);
+        uint64_t* haspred = L.ecap ? at<uint64_t>(workspace, L.haspred) : nullptr;
+        uint64_t* keys = sort_keys_bytes(static_cast<int>(n)) ? at<uint64_t>(workspace, L.keys) : nullptr;
+        launch_sort(scores, reinterpret_cast<const float4*>(boxes), cand, m_count, static_cast<int>(n),
+                    perm, boxes_s, keys, status, rowbits, L.NB, ecount, haspred, st);
         uint64_t* band = at<uint64_t>(workspace, L.band);
-        launch_iou_mask(boxes_s, m_count, static_cast<int>(n), p, mask, L.ldw, rowbits, L.NB, band, st);
-        launch_resolve_single(mask, L.ldw, rowbits, L.NB, band, m_count, static_cast<int>(n), perm,
-                              max_out, keep, counts, status, st);
+        launch_iou_mask(boxes_s, m_count, static_cast<int>(n), p, mask, L.ldw, rowbits, L.NB, band,
+                        edges, ecount, L.ecap, haspred, st);
+        launch_resolve_single(mask, L.ldw, rowbits, L.NB, band, edges, ecount, haspred, m_count,
+                              static_cast<int>(n), perm, max_out, keep, counts, status, st);
         return cuda_status();
     }
 
@@ -258,7 +288,7 @@ extern "C" nms_status nms_iou_mask(const float* boxes_sorted, int64_t n, float i
     if (mask_words < n * ldw) return NMS_ERR_CAPACITY;
     cudaGetLastError();
     launch_iou_mask(reinterpret_cast<const float4*>(boxes_sorted), nullptr, static_cast<int>(n),
-                    make_thr(iou_thr), mask, ldw, nullptr, 1, nullptr,
+                    make_thr(iou_thr), mask, ldw, nullptr, 1, nullptr, nullptr, nullptr, 0u, nullptr,
                     static_cast<cudaStream_t>(stream));
     return cuda_status();
 }
@@ -280,7 +310,7 @@ extern "C" nms_status nms_resolve_mask(const uint64_t* mask, int64_t n, const in
     }
     uint64_t* band = at<uint64_t>(workspace, L.band);
     launch_band_from_mask(mask, L.ldw, static_cast<int>(n), band, st);
-    launch_resolve_single(mask, L.ldw, nullptr, 1, band, nullptr, static_cast<int>(n), perm, max_out,
-                          keep, count, nullptr, st);
+    launch_resolve_single(mask, L.ldw, nullptr, 1, band, nullptr, nullptr, nullptr, nullptr,
+                          static_cast<int>(n), perm, max_out, keep, count, nullptr, st);
     return cuda_status();
 }

@@ -77,7 +77,7 @@ extern "C" nms_status nms_resolve_mask_noalloc(const uint64_t* mask, int64_t n, 
     // used and nothing needs clearing first.
     const int64_t ldw = nms_mask_row_words(n);
     launch_band_from_mask(mask, ldw, static_cast<int>(n), band, st);
-    launch_resolve_single(mask, ldw, nullptr, 1, band, nullptr, static_cast<int>(n), perm, max_out,
-                          keep, count, nullptr, st);
+    launch_resolve_single(mask, ldw, nullptr, 1, band, nullptr, nullptr, nullptr, nullptr,
+                          static_cast<int>(n), perm, max_out, keep, count, nullptr, st);
     return cudaGetLastError() == cudaSuccess ? NMS_OK : NMS_ERR_CUDA;
 }

@@ -8,19 +8,28 @@ namespace gbnms {
 
 struct ThrParams;
 
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device; the runtime is called only when the limit recorded for
+// that (device, kernel) is lower, so repeated launches pay nothing.
+void ensure_dynamic_smem(const void* kernel, size_t bytes);
+
 void launch_prefilter(const float* scores, int n, float score_thr, int* cand, int* m_count,
                       cudaStream_t st);
-void launch_rank_sort(const float* scores, const float4* boxes, const int* cand, const int* m_dev,
-                      int m_bound, int* perm, float4* boxes_s, int32_t* status, uint64_t* rowbits,
-                      int NB, cudaStream_t st);
+size_t sort_keys_bytes(int m_bound);
+void launch_sort(const float* scores, const float4* boxes, const int* cand, const int* m_dev,
+                 int m_bound, int* perm, float4* boxes_s, uint64_t* keys, int32_t* status,
+                 uint64_t* rowbits, int NB, unsigned* ecount, uint64_t* haspred, cudaStream_t st);
 int64_t mask_tiles(int64_t n);
 void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const ThrParams& p,
                      uint64_t* mask, int64_t ldw, uint64_t* rowbits, int NB, uint64_t* band,
+                     uint32_t* edges, unsigned* ecount, unsigned ecap, uint64_t* haspred,
                      cudaStream_t st);
 size_t resolve_smem_bytes(int m_bound, int NB);
+unsigned graph_edge_cap(int m_bound);
 void launch_band_from_mask(const uint64_t* mask, int64_t ldw, int n, uint64_t* band, cudaStream_t st);
 void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* rowbits, int NB,
-                           const uint64_t* band, const int* m_dev, int m_bound, const int* perm,
+                           const uint64_t* band, const uint32_t* edges, const unsigned* ecount,
+                           const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm,
                            int max_out, int64_t* keep, int64_t* counts, int32_t* status,
                            cudaStream_t st);
 

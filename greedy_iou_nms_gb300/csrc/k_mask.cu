@@ -17,7 +17,11 @@
 // one bit per 256-column chunk, which of its chunks hold a set bit, and the
 // 64x64 blocks within BAND_L tiles of the diagonal are also written in column
 // view; the resolve uses the first to skip all-zero chunks and the second to
-// decide a tile with lane-local tests.  Pairs are decided by the
+// decide a tile with lane-local tests.  When asked, every set bit is also
+// appended to a list of (row, column) pairs, the sparse form of the same
+// graph, as long as the list has room, and every column with a set bit is
+// marked in a bitmap of boxes that have an earlier neighbour.  Pairs are
+// decided by the
 // division-free test of common.cuh and, for the rare pair it leaves open and
 // for tiles holding a malformed box, by the exact binary32 division.
 #include "common.cuh"
@@ -143,10 +147,33 @@ __device__ __forceinline__ void clip_words(uint64_t (&w)[4], int i, int cb, int 
     }
 }
 
+// Append the set bits of row i's four words at column base cb as packed
+// (i << 16 | j) pairs.
+__device__ __forceinline__ uint32_t* emit_row(uint32_t* dst, const uint64_t (&w)[4], int i, int cb)
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint64_t x = w[q];
+        while (x) {
+            const int b = __ffsll(static_cast<long long>(x)) - 1;
+            x &= x - 1;
+            *dst++ = (static_cast<uint32_t>(i) << 16) | static_cast<uint32_t>(cb + 64 * q + b);
+        }
+    }
+    return dst;
+}
+
+__device__ __forceinline__ int popc4(const uint64_t (&w)[4])
+{
+    return __popcll(w[0]) + __popcll(w[1]) + __popcll(w[2]) + __popcll(w[3]);
+}
+
 __global__ void __launch_bounds__(M_THREADS)
 iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_dev, int m_bound,
                 ThrParams p, uint64_t* __restrict__ mask, int64_t ldw,
-                unsigned long long* __restrict__ rowbits, int NB, ulonglong2* __restrict__ band)
+                unsigned long long* __restrict__ rowbits, int NB, ulonglong2* __restrict__ band,
+                uint32_t* __restrict__ edges, unsigned* __restrict__ ecount, unsigned ecap,
+                unsigned long long* __restrict__ haspred)
 {
     __shared__ float4 cbox[MT];
     __shared__ float carea[MT];
@@ -205,9 +232,8 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
         clip_words(w1, -1, cb, n);
     }
     // Column view of the blocks within BAND_L tiles of the diagonal (64-row
-    // tile R of this warp, 64-column tile C = 4c+q): transpose the block's
-    // final words with two ballots per column.  Lane l keeps columns l and
-    // l+32.
+    // tile R of this warp, 64-column tile C = 4c+q): a warp transpose of the
+    // block's final words leaves columns l and l+32 in lane l.
     if (band) {
         const int R = rbase / 64 + wp;
         const int T64 = (n + 63) / 64;
@@ -216,13 +242,8 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
             const int C = 4 * c + q;
             const int d = C - R;
             if (d < 0 || d > BAND_L || C >= T64) continue;  // warp-uniform
-            uint64_t colA = 0, colB = 0;
-#pragma unroll 4
-            for (int b = 0; b < 64; ++b) {
-                const uint64_t col = ballot64((w0[q] >> b) & 1ull, (w1[q] >> b) & 1ull);
-                if (b == static_cast<int>(l)) colA = col;
-                if (b == static_cast<int>(l) + 32) colB = col;
-            }
+            uint64_t colA = w0[q], colB = w1[q];
+            transpose64(colA, colB);
             band[(static_cast<int64_t>(C) * (BAND_L + 1) + d) * 32 + l] = make_ulonglong2(colA, colB);
         }
     }
@@ -241,6 +262,42 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
         if (rowbits && (w1[0] | w1[1] | w1[2] | w1[3]))
             atomicOr(rowbits + static_cast<int64_t>(i1) * NB + (c >> 6), 1ull << (c & 63));
     }
+    // Boxes with at least one earlier box over the threshold: the OR of the
+    // warp's rows, one atomic per non-zero 64-column word.
+    if (haspred) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint64_t v = (i0 < n ? w0[q] : 0ull) | (i1 < n ? w1[q] : 0ull);
+            const unsigned lo = __reduce_or_sync(FULL, static_cast<unsigned>(v));
+            const unsigned hi = __reduce_or_sync(FULL, static_cast<unsigned>(v >> 32));
+            if (static_cast<int>(l) == q && (lo | hi))
+                atomicOr(haspred + (cb >> 6) + q, (static_cast<unsigned long long>(hi) << 32) | lo);
+        }
+    }
+    // Sparse form: one counter reservation per warp with any set bit; the
+    // pairs of a warp land contiguously, lane by lane.  Past the capacity the
+    // count still grows (it tells the resolve the list is incomplete) and
+    // nothing is written.
+    if (edges) {
+        const int cnt = (i0 < n ? popc4(w0) : 0) + (i1 < n ? popc4(w1) : 0);
+        int x = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(FULL, x, d);
+            if (static_cast<int>(l) >= d) x += y;
+        }
+        const int total = __shfl_sync(FULL, x, 31);
+        if (total) {
+            unsigned base = 0;
+            if (l == 31) base = atomicAdd(ecount, static_cast<unsigned>(total));
+            base = __shfl_sync(FULL, base, 31);
+            if (base <= ecap && static_cast<unsigned>(total) <= ecap - base) {
+                uint32_t* dst = edges + base + (x - cnt);
+                if (i0 < n) dst = emit_row(dst, w0, i0, cb);
+                if (i1 < n) emit_row(dst, w1, i1, cb);
+            }
+        }
+    }
 }
 
 int64_t mask_tiles(int64_t n)
@@ -251,6 +308,7 @@ int64_t mask_tiles(int64_t n)
 
 void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const ThrParams& p,
                      uint64_t* mask, int64_t ldw, uint64_t* rowbits, int NB, uint64_t* band,
+                     uint32_t* edges, unsigned* ecount, unsigned ecap, uint64_t* haspred,
                      cudaStream_t st)
 {
     int64_t tiles = mask_tiles(m_bound);
@@ -258,7 +316,9 @@ void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const
     iou_mask_kernel<<<static_cast<unsigned>(tiles), M_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, p,
                                                                         mask, ldw,
                                                                         reinterpret_cast<unsigned long long*>(rowbits), NB,
-                                                                        reinterpret_cast<ulonglong2*>(band));
+                                                                        reinterpret_cast<ulonglong2*>(band),
+                                                                        edges, ecount, ecap,
+                                                                        reinterpret_cast<unsigned long long*>(haspred));
 }
 
 }  // namespace gbnms

@@ -1,6 +1,21 @@
-// Sequential resolve of the suppression bitmask, in score order, with the map
-// back to input indices.
+// Resolve of the suppression graph in score order, with the map back to input
+// indices.
 //
+// Two ways to the same result, chosen on the device per call:
+//
+// Graph path (the sparse pair list fits in shared memory).  Greedy NMS
+// decides box j as soon as every earlier box that overlaps it beyond the
+// threshold is decided: j is removed when one of them is kept, and kept when
+// all of them are removed.  Deciding, in rounds, every box whose earlier
+// neighbours are all decided therefore gives exactly the greedy result
+// (induction over the score order), in as many rounds as the longest chain of
+// such dependencies.  For detector-like inputs that chain is a handful of
+// links even when the walk below would take thousands of steps.  One CTA
+// keeps the kept/removed bitmaps and the live pairs in shared memory; a round
+// is one pass over the pairs whose target is still open plus one word-wide
+// pass over the bitmaps.
+//
+// Walk (everything else, and a caller's own mask):
 // "NMS CUDA代码学习", section Phase 2: one thread block walks the boxes from
 // the highest score down with the removed-bitmap in shared memory; a box not
 // yet removed is kept and its mask row is ORed into the bitmap, each decision
@@ -37,6 +52,8 @@
 // scheduler partition: the warps that share warp 0's partition (4, 8, ...)
 // stay idle.  Kept sets go to shared memory; the output list is written by
 // the whole CTA after the walk.
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -215,10 +232,208 @@ __host__ __device__ __forceinline__ ResolveLayout resolve_layout(int m_bound, in
     return L;
 }
 
+// ---------------------------------------------------------------- graph path
+constexpr int GR_SMEM = 200 * 1024;   // shared bytes the graph path may take
+constexpr int GR_MAX_N = 65536;       // a pair packs two 16-bit sorted positions
+constexpr int GR_HEAD = 64;           // words: block-prefix scratch [0,32), copy barrier at 32
+constexpr int GR_COPY = 32 * 1024;    // bytes per bulk copy of the pair list
+
+// 32-bit bitmap words for m_bound boxes, rounded up to a multiple of 4 so the
+// pair list that follows starts 16-byte aligned.
+__host__ __device__ __forceinline__ int graph_words(int m_bound) { return ((m_bound + 31) / 32 + 3) & ~3; }
+
+unsigned graph_edge_cap(int m_bound)
+{
+    if (m_bound <= 0 || m_bound > GR_MAX_N) return 0;
+    const long long room = GR_SMEM - 4ll * (GR_HEAD + 4ll * graph_words(m_bound));
+    return room > 0 ? static_cast<unsigned>((room / 4) & ~3ll) : 0u;
+}
+
+size_t graph_smem_bytes(int m_bound)
+{
+    return 4 * (GR_HEAD + 4 * static_cast<size_t>(graph_words(m_bound))) +
+           4 * static_cast<size_t>(graph_edge_cap(m_bound));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* b, unsigned bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(b)), "r"(bytes)
+                 : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from global to shared memory,
+// completing on mbarrier b.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, unsigned long long* b)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(b))
+        : "memory");
+}
+
+// Rounds over the pair list gedges[0..E) of n sorted boxes (haspred: bit j
+// set iff box j has a pair).  Returns false, with nothing written, when the
+// rounds outnumber the walk's tiles plus 16 (a long chain of dependencies:
+// the walk is then the faster way).
+//
+// Shared layout (32-bit words): scratch and the copy barrier, then the
+// (kept, removed) bits of 32 boxes per uint2, then the (hit by a kept box,
+// blocked by an open box) bits per uint2, then the live pairs.  Thread t owns
+// the pairs at t, t + RV_THREADS, ... and compacts its own share in place.
+// A pair leaves the list once its source is decided; while the source is
+// open the target is open too (a box is decided only after all its sources).
+__device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedges, unsigned E,
+                              const uint32_t* __restrict__ haspred, int n, int NWp,
+                              const int* __restrict__ perm, int max_out, int64_t* __restrict__ keep,
+                              int64_t* __restrict__ counts, int32_t* status, uint32_t* sm)
+{
+    int* scratch = reinterpret_cast<int*>(sm);
+    unsigned long long* bar = reinterpret_cast<unsigned long long*>(sm + 32);
+    uint2* KR = reinterpret_cast<uint2*>(sm + GR_HEAD);
+    uint2* HB = KR + NWp;
+    uint32_t* Es = sm + GR_HEAD + 4 * NWp;
+    const int tid = threadIdx.x;
+    const unsigned l = lane_id();
+    const int warp = tid >> 5;
+    const int NW = (n + 31) / 32;
+
+    // Stage the list with bulk copies (the list is 16-byte aligned and padded
+    // to a multiple of 4 pairs) while the bitmaps are set up.
+    const unsigned bytes = 16u * ((E + 3) / 4);
+    const unsigned ncopy = (bytes + GR_COPY - 1) / GR_COPY;
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+    if (tid == 0 && bytes) mbar_expect_tx(bar, bytes);
+    __syncwarp();
+    if (warp == 0 && l < ncopy) {
+        const unsigned off = l * GR_COPY;
+        const unsigned len = min(static_cast<unsigned>(GR_COPY), bytes - off);
+        bulk_g2s(reinterpret_cast<char*>(Es) + off, reinterpret_cast<const char*>(gedges) + off, len, bar);
+    }
+    for (int w = tid; w < NW; w += RV_THREADS) {
+        KR[w] = make_uint2(0u, 0u);
+        HB[w] = make_uint2(0u, haspred[w]);  // before the first round every target is blocked
+    }
+    bool copied = true;
+    if (bytes) {
+        long long tries = 0;
+        while (!mbar_try_wait(bar, 0)) {
+            if (++tries > RV_WAIT_LIMIT) { copied = false; break; }
+            __nanosleep(64);
+        }
+    }
+    const bool all_copied = __syncthreads_and(copied);
+    if (tid == 0) asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(smem_addr(bar)) : "memory");
+    if (!all_copied) {
+        if (tid == 0) {
+            if (status) set_status(status, NMS_ERR_TIMEOUT);
+            counts[0] = 0;
+        }
+        return true;
+    }
+    int live = E > static_cast<unsigned>(tid) ? static_cast<int>((E - tid + RV_THREADS - 1) / RV_THREADS) : 0;
+    const int max_rounds = (n + 63) / 64 + 16;
+    for (int round = 0;; ++round) {
+        // Decide every open box: removed if a kept source hit it, kept if no
+        // open source blocked it.
+        bool more = false;
+        for (int w = tid; w < NW; w += RV_THREADS) {
+            const uint2 kr = KR[w];
+            const uint32_t valid = (w == NW - 1 && (n & 31)) ? (1u << (n & 31)) - 1u : ~0u;
+            const uint32_t open = ~(kr.x | kr.y) & valid;
+            if (open) {
+                const uint2 hb = HB[w];
+                KR[w] = make_uint2(kr.x | (open & ~hb.x & ~hb.y), kr.y | (open & hb.x));
+                HB[w] = make_uint2(0u, 0u);
+                more |= (open & ~hb.x & hb.y) != 0;
+            }
+        }
+        if (!__syncthreads_or(more)) break;
+        if (round == max_rounds) return false;
+        // One pass over the live pairs: a kept source hits its target, a
+        // removed source no longer matters, an open source blocks its target
+        // and the pair stays.
+        int nl = 0;
+        for (int k0 = 0; k0 < live; k0 += 4) {
+            uint32_t e[4];
+            uint2 ki[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) e[u] = k0 + u < live ? Es[tid + RV_THREADS * (k0 + u)] : 0xffffffffu;
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (e[u] != 0xffffffffu) ki[u] = KR[e[u] >> 21];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (e[u] == 0xffffffffu) continue;
+                const uint32_t j = e[u] & 0xffffu;
+                const uint32_t bi = 1u << ((e[u] >> 16) & 31);
+                if (ki[u].x & bi) {
+                    atomicOr(&HB[j >> 5].x, 1u << (j & 31));
+                } else if (!(ki[u].y & bi)) {
+                    atomicOr(&HB[j >> 5].y, 1u << (j & 31));
+                    Es[tid + RV_THREADS * nl++] = e[u];
+                }
+            }
+        }
+        live = nl;
+        __syncthreads();
+    }
+    // Output: warp w owns 32-box words [w*wpw, (w+1)*wpw); a block-wide
+    // prefix of the warps' kept counts places them, and within a word lane l
+    // writes box 32w+l, so loads of perm and stores of keep are coalesced.
+    const int wpw = (NW + 31) / 32;
+    const int w0 = min(warp * wpw, NW), w1 = min(w0 + wpw, NW);
+    int c = 0;
+    for (int w = w0 + static_cast<int>(l); w < w1; w += 32) c += __popc(KR[w].x);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) c += __shfl_xor_sync(FULL, c, d);
+    if (l == 0) scratch[warp] = c;
+    __syncthreads();
+    if (warp == 0) {
+        int v = scratch[l];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(FULL, v, d);
+            if (static_cast<int>(l) >= d) v += y;
+        }
+        scratch[l] = v;
+    }
+    __syncthreads();
+    const int total = scratch[31];
+    const int cap = max_out > 0 ? max_out : INT_MAX;
+    int base = warp ? scratch[warp - 1] : 0;
+    const uint32_t below = (1u << l) - 1u;
+    constexpr int OW = 8;  // words whose loads are in flight together
+    for (int wb = w0; wb < w1 && base < cap; wb += OW) {
+        uint32_t bits[OW];
+        int v[OW];
+#pragma unroll
+        for (int u = 0; u < OW; ++u) {
+            bits[u] = wb + u < w1 ? KR[wb + u].x : 0u;
+            const int j = 32 * (wb + u) + static_cast<int>(l);
+            v[u] = ((bits[u] >> l) & 1u) ? (perm ? perm[j] : j) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < OW; ++u) {
+            const int pos = base + __popc(bits[u] & below);
+            if (((bits[u] >> l) & 1u) && pos < cap) keep[pos] = v[u];
+            base += __popc(bits[u]);
+        }
+    }
+    if (tid == 0) counts[0] = total < cap ? total : cap;
+    return true;
+}
+
 __global__ void __launch_bounds__(RV_THREADS, 1)
 resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
                       const uint64_t* __restrict__ rowbits, int NB,
                       const uint64_t* __restrict__ band,
+                      const uint32_t* __restrict__ edges, const unsigned* __restrict__ ecount,
+                      unsigned ecap, const uint32_t* __restrict__ haspred,
                       const int* __restrict__ m_dev, int m_bound, const int* __restrict__ perm,
                       int max_out, int64_t* __restrict__ keep, int64_t* __restrict__ counts,
                       int32_t* status)
@@ -227,6 +442,13 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
     __shared__ ResolveShared S;
 
     const int n = m_dev ? *m_dev : m_bound;
+    if (edges) {
+        const unsigned E = *ecount;
+        if (E <= ecap && graph_resolve(edges, E, haspred, n, graph_words(m_bound), perm, max_out,
+                                       keep, counts, status, reinterpret_cast<uint32_t*>(smem)))
+            return;
+        __syncthreads();  // the walk reuses the shared memory
+    }
     const int T = (n + 63) / 64;              // tiles
     const int T256 = (n + 255) / 256;         // 256-column chunks
     const ResolveLayout LY = resolve_layout(m_bound, NB);
@@ -481,7 +703,7 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
 size_t resolve_smem_bytes(int m_bound, int NB) { return resolve_layout(m_bound, NB).total; }
 
 // Column view of the band blocks of a row-major mask: one warp per (column
-// tile C, distance d) transposes block (C-d, C) with two ballots per column.
+// tile C, distance d) transposes block (C-d, C).
 // Used when the caller brings its own mask (nms_resolve_mask).
 __global__ void band_from_mask_kernel(const uint64_t* __restrict__ mask, int64_t ldw, int n,
                                       ulonglong2* __restrict__ band)
@@ -501,14 +723,8 @@ __global__ void band_from_mask_kernel(const uint64_t* __restrict__ mask, int64_t
             rb &= (l + 33 < 64) ? (~0ull << (l + 33)) : 0ull;
         }
     }
-    uint64_t colA = 0, colB = 0;
-#pragma unroll 4
-    for (int b = 0; b < 64; ++b) {
-        const uint64_t col = ballot64((ra >> b) & 1ull, (rb >> b) & 1ull);
-        if (b == static_cast<int>(l)) colA = col;
-        if (b == static_cast<int>(l) + 32) colB = col;
-    }
-    band[static_cast<int64_t>(blk) * 32 + l] = make_ulonglong2(colA, colB);
+    transpose64(ra, rb);
+    band[static_cast<int64_t>(blk) * 32 + l] = make_ulonglong2(ra, rb);
 }
 
 void launch_band_from_mask(const uint64_t* mask, int64_t ldw, int n, uint64_t* band, cudaStream_t st)
@@ -520,15 +736,19 @@ void launch_band_from_mask(const uint64_t* mask, int64_t ldw, int n, uint64_t* b
 }
 
 void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* rowbits, int NB,
-                           const uint64_t* band, const int* m_dev, int m_bound, const int* perm,
+                           const uint64_t* band, const uint32_t* edges, const unsigned* ecount,
+                           const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm,
                            int max_out, int64_t* keep, int64_t* counts, int32_t* status,
                            cudaStream_t st)
 {
-    const size_t smem = resolve_smem_bytes(m_bound, NB);
-    cudaFuncSetAttribute(resolve_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
-    resolve_single_kernel<<<1, RV_THREADS, smem, st>>>(mask, ldw, rowbits, NB, band, m_dev, m_bound,
-                                                       perm, max_out, keep, counts, status);
+    size_t smem = resolve_smem_bytes(m_bound, NB);
+    const unsigned ecap = edges ? graph_edge_cap(m_bound) : 0u;
+    if (edges && graph_smem_bytes(m_bound) > smem) smem = graph_smem_bytes(m_bound);
+    ensure_dynamic_smem(reinterpret_cast<const void*>(resolve_single_kernel), smem);
+    resolve_single_kernel<<<1, RV_THREADS, smem, st>>>(mask, ldw, rowbits, NB, band, edges, ecount,
+                                                       ecap, reinterpret_cast<const uint32_t*>(haspred),
+                                                       m_dev, m_bound, perm, max_out, keep, counts,
+                                                       status);
 }
 
 }  // namespace gbnms

@@ -1,6 +1,6 @@
 // Single-image path, front end: optional score pre-filter (warp-aggregated
-// atomics) and the stable descending sort by rank counting, fused with the
-// gather of the sorted boxes.
+// atomics) and the stable descending sort, a merge sort of (score key, index)
+// keys, fused with the gather of the sorted boxes.
 //
 // "NMS CUDA代码学习", section 算法与数据流 step 1 (sort by descending score,
 // stable) and section "host 侧" (the sort permutation maps kept positions back
@@ -14,8 +14,8 @@
 namespace gbnms {
 
 // Pre-filter: candidates with score > score_thr, compacted with one atomic per
-// warp.  The order of the compacted list is not deterministic; the rank sort
-// below includes the input index in its key, so the result is.
+// warp.  The order of the compacted list is not deterministic; the sort below
+// includes the input index in its key, so the result is.
 __global__ void prefilter_kernel(const float* __restrict__ scores, int n, float score_thr,
                                  int* __restrict__ cand, int* __restrict__ m_count)
 {
@@ -30,143 +30,301 @@ __global__ void prefilter_kernel(const float* __restrict__ scores, int n, float 
     if (pass) cand[base + __popc(ballot & ((1u << l) - 1u))] = i;
 }
 
-// Rank sort.  A candidate's sorted position is the number of candidates whose
-// (score key, index) is smaller; the keys are unique, so the positions form a
-// permutation and the sort is stable by construction.  Each CTA ranks RS_I
-// candidates against all of them: lane l of a warp owns 4 consecutive
-// candidates (group l % 8) and takes every fourth 4-key group of the warp's
-// share (subset l / 8), so one 16-byte shared-memory load feeds 16 compares.
+// Sort on 64-bit (score key << 32 | input index) keys.  The keys are unique,
+// so any correct sort of them is the stable descending score order (ties by
+// lower index); 0xffff...ff pads and sorts after every real key.
 //
-// Without a pre-filter the candidate list is the input in index order, so a
-// j before candidate i counts when key_j <= key_i and a j after it when key_j
-// < key_i: one 32-bit compare per pair.  With a pre-filter the list order is
-// arbitrary and the 64-bit (key, index) compare is used.
-constexpr int RS_WARPS = 16;
-constexpr int RS_I = 32;         // candidates ranked per CTA (8 lanes x 4)
-constexpr int RS_SUB = 4;        // key subsets per warp (lanes / 8)
-constexpr int RS_CHUNK = 4096;   // keys staged in shared memory per step
+// Chunks of MS_CHUNK keys are sorted by bucketed ranking (below), every
+// chunk by many CTAs.  Larger inputs then merge pairs of sorted runs in
+// global memory, one launch per doubling: a CTA produces one MS_CHUNK tile of
+// the output, loads the two input ranges it covers (found by a 32-way
+// search) into shared memory, and each thread merges MS_P outputs after a
+// merge-path search for its first one.  Shared memory keeps one spare slot
+// per MS_P keys so that lanes MS_P keys apart do not share banks.  The last
+// step writes the permutation and the gathered boxes instead of keys.
+constexpr int MS_THREADS = 1024;
+constexpr int MS_P = 8;                        // keys per thread
+constexpr int MS_CHUNK = MS_THREADS * MS_P;    // keys per CTA
+constexpr uint64_t MS_PAD = ~0ull;
 
-__global__ void __launch_bounds__(RS_WARPS * 32)
-rank_sort_kernel(const float* __restrict__ scores, const float4* __restrict__ boxes,
-                 const int* __restrict__ cand, const int* __restrict__ m_dev, int m_bound,
-                 int* __restrict__ perm, float4* __restrict__ boxes_s, int32_t* status,
-                 uint64_t* __restrict__ rowbits, int NB)
+// Shared-memory slot of logical key i: one spare slot after every MS_P keys,
+// so the lanes of a warp, MS_P keys apart, hit different banks.
+__device__ __forceinline__ int sk(int i) { return i + i / MS_P; }
+constexpr int MS_SLOTS = MS_CHUNK + MS_CHUNK / MS_P;
+
+// Number of A elements among the first d outputs of merge(A, B) (A first on
+// ties), A = keys [a0, a0+na) and B = keys [b0, b0+nb) of the skewed buffer.
+__device__ __forceinline__ int merge_path(const uint64_t* buf, int a0, int na, int b0, int nb, int d)
 {
-    __shared__ __align__(16) uint64_t keys64[RS_CHUNK];   // u32 keys use the first half
-    __shared__ uint32_t part[RS_WARPS * RS_SUB][RS_I];
-    uint32_t* keys32 = reinterpret_cast<uint32_t*>(keys64);
+    int lo = max(0, d - nb), hi = min(d, na);
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (buf[sk(a0 + mid)] <= buf[sk(b0 + d - 1 - mid)]) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
 
+// MS_P outputs of merge(A, B) starting at output d, into out[].
+__device__ __forceinline__ void merge_p(const uint64_t* buf, int a0, int na, int b0, int nb, int d,
+                                        uint64_t (&out)[MS_P])
+{
+    int i = merge_path(buf, a0, na, b0, nb, d), j = d - i;
+    uint64_t a = i < na ? buf[sk(a0 + i)] : MS_PAD, b = j < nb ? buf[sk(b0 + j)] : MS_PAD;
+#pragma unroll
+    for (int u = 0; u < MS_P; ++u) {
+        const bool takeA = j >= nb || (i < na && a <= b);
+        out[u] = takeA ? a : b;
+        if (takeA) { ++i; a = i < na ? buf[sk(a0 + i)] : MS_PAD; }
+        else { ++j; b = j < nb ? buf[sk(b0 + j)] : MS_PAD; }
+    }
+}
+
+// Sorted position r holds key k: the permutation entry and the gathered box.
+__device__ __forceinline__ void emit_sorted(uint64_t k, int r, int m, const float4* __restrict__ boxes,
+                                            int* __restrict__ perm, float4* __restrict__ boxes_s)
+{
+    if (r < m) {
+        const int x = static_cast<int>(static_cast<uint32_t>(k));
+        perm[r] = x;
+        boxes_s[r] = boxes[x];
+    }
+}
+
+// Bucketed rank within a chunk of MS_CHUNK candidates (positions
+// [c*MS_CHUNK, ...), c = blockIdx.y).  A key's sorted position in its chunk
+// is the number of smaller keys.  Every CTA of the chunk histograms all of the
+// chunk's keys into BR_BUCKETS buckets, scatters them into bucket order in
+// shared memory (order inside a bucket does not matter) and then counts, for
+// each of its BR_CAND candidates, the smaller keys of its own bucket: the
+// work per CTA is linear in the chunk plus the candidates' bucket sizes.
+// The bucket of a key is its score key's place in the [lo, hi] range of the
+// chunk's finite scores, scaled by a fixed-point multiply (score keys beyond
+// the range, i.e. +inf, -inf and NaN, go to the end buckets); it is monotone
+// in the key, so buckets come in key order and equal scores share one.
+// With one chunk the kernel writes perm and boxes_s, otherwise the chunk's
+// sorted keys for the merge levels.  It also clears what the mask kernel
+// accumulates into: the status, the pair counter, the bitmap of boxes with an
+// earlier neighbour and the per-row chunk bitmaps of its candidates' rows.
+constexpr int BR_THREADS = 512;
+constexpr int BR_CAND = 128;                   // candidates ranked per CTA
+constexpr int BR_BUCKETS = 4096;
+constexpr int BR_KPT = MS_CHUNK / BR_THREADS;  // chunk keys per thread
+
+struct BucketMap {
+    uint32_t lo, hi;  // score-key range of the finite scores
+    uint64_t mul;     // floor((BR_BUCKETS-1) * 2^32 / (hi - lo + 1))
+    __device__ __forceinline__ int operator()(uint64_t key) const
+    {
+        const uint32_t k = static_cast<uint32_t>(key >> 32);
+        if (k < lo) return 0;
+        if (k > hi) return BR_BUCKETS - 1;
+        return static_cast<int>((static_cast<uint64_t>(k - lo) * mul) >> 32);
+    }
+};
+
+__global__ void __launch_bounds__(BR_THREADS)
+bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ boxes,
+                   const int* __restrict__ cand, const int* __restrict__ m_dev, int m_bound,
+                   uint64_t* __restrict__ keys_out, int* __restrict__ perm, float4* __restrict__ boxes_s,
+                   int32_t* status, uint64_t* __restrict__ rowbits, int NB, unsigned* __restrict__ ecount,
+                   uint64_t* __restrict__ haspred)
+{
+    extern __shared__ __align__(16) uint64_t list[];                 // MS_CHUNK keys, bucket order
+    int* start = reinterpret_cast<int*>(list + MS_CHUNK);            // [BR_BUCKETS + 1]
+    int* cur = start + BR_BUCKETS + 1;                               // [BR_BUCKETS]
+    __shared__ int wsum[BR_THREADS / 32];
+    __shared__ uint32_t wlo[BR_THREADS / 32], whi[BR_THREADS / 32];
+    __shared__ uint64_t ckey[BR_CAND];  // this CTA's candidates
+    __shared__ int crank[BR_CAND];
+    const int tid = threadIdx.x;
+    const int c0 = blockIdx.y * MS_CHUNK;
+    const int q0 = c0 + blockIdx.x * BR_CAND;  // this CTA's candidates [q0, q0 + BR_CAND)
+    if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) {
+        if (status) *status = 0;
+        if (ecount) *ecount = 0;
+    }
+    const int r1 = min(q0 + BR_CAND, m_bound);
+    if (haspred && (q0 & 63) == 0)
+        for (int w = q0 / 64 + tid; w < (r1 + 63) / 64; w += BR_THREADS) haspred[w] = 0;
+    if (rowbits)
+        for (int64_t q = static_cast<int64_t>(q0) * NB + tid; q < static_cast<int64_t>(r1) * NB; q += BR_THREADS)
+            rowbits[q] = 0;
     const int m = m_dev ? *m_dev : m_bound;
-    if (blockIdx.x == 0 && threadIdx.x == 0 && status) *status = 0;
-    const int i0 = blockIdx.x * RS_I;
-    // Clear the mask's per-row chunk bitmaps of rows [i0, i0+RS_I) for the
-    // mask kernel that follows.
-    if (rowbits) {
-        const int64_t q0 = static_cast<int64_t>(i0) * NB;
-        const int64_t q1 = static_cast<int64_t>(min(i0 + RS_I, m_bound)) * NB;
-        for (int64_t q = q0 + threadIdx.x; q < q1; q += blockDim.x) rowbits[q] = 0;
-    }
-    if (i0 >= m) return;
+    const int cn = min(MS_CHUNK, m - c0);     // keys of this chunk (may be <= 0)
+    const bool multi = gridDim.y > 1;
+    if (!multi && q0 >= m) return;
 
+    for (int b = tid; b < BR_BUCKETS; b += BR_THREADS) start[b] = 0;
+    if (tid < BR_CAND) {
+        const int p = q0 + tid;
+        uint64_t key = MS_PAD;
+        if (p < m && p < c0 + MS_CHUNK) {
+            const int xi = cand ? cand[p] : p;
+            key = order_key(scores[xi], static_cast<uint32_t>(xi));
+        }
+        ckey[tid] = key;
+    }
+    uint64_t k[BR_KPT];
+    uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+    for (int u = 0; u < BR_KPT; ++u) {
+        const int t = tid + u * BR_THREADS;
+        if (t < cn) {
+            const int x = cand ? cand[c0 + t] : c0 + t;
+            const float sc = scores[x];
+            k[u] = order_key(sc, static_cast<uint32_t>(x));
+            if (isfinite(sc)) {
+                lo = min(lo, static_cast<uint32_t>(k[u] >> 32));
+                hi = max(hi, static_cast<uint32_t>(k[u] >> 32));
+            }
+        } else {
+            k[u] = MS_PAD;
+        }
+    }
     const unsigned l = lane_id();
-    const int w = threadIdx.x >> 5;
-    const int ig = l & 7, js = l >> 3;
-    const int sub = w * RS_SUB + js;           // this lane's share of the keys
-    const int nsub = RS_WARPS * RS_SUB;
-    int iv[4];
-    uint32_t cnt[4] = {0, 0, 0, 0};
-#pragma unroll
-    for (int u = 0; u < 4; ++u) iv[u] = i0 + 4 * ig + u;
-
-    if (!cand) {
-        uint32_t kk[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) kk[u] = iv[u] < m ? score_key(scores[iv[u]]) : 0xffffffffu;
-        for (int c0 = 0; c0 < m; c0 += RS_CHUNK) {
-            const int cn = min(RS_CHUNK, m - c0);
-            __syncthreads();
-            // Four scores per 16-byte load when the chunk start is aligned (all
-            // loads of a thread in flight together); the ragged end pads with
-            // the largest key.
-            const bool vec = ((reinterpret_cast<uintptr_t>(scores + c0) & 15) == 0);
-            if (vec) {
-                const float4* s4 = reinterpret_cast<const float4*>(scores + c0);
-                const int n4 = cn >> 2;
-#pragma unroll 4
-                for (int t = threadIdx.x; t < n4; t += blockDim.x) {
-                    const float4 v = s4[t];
-                    reinterpret_cast<uint4*>(keys32)[t] =
-                        make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
-                }
-                for (int t = 4 * n4 + threadIdx.x; t < cn; t += blockDim.x) keys32[t] = score_key(scores[c0 + t]);
-            } else {
-#pragma unroll 4
-                for (int t = threadIdx.x; t < cn; t += blockDim.x) keys32[t] = score_key(scores[c0 + t]);
-            }
-            for (int t = cn + threadIdx.x; t < ((cn + 3) & ~3); t += blockDim.x) keys32[t] = 0xffffffffu;
-            __syncthreads();
-            const uint4* k4 = reinterpret_cast<const uint4*>(keys32);
-            for (int q = sub; 4 * q < cn; q += nsub) {
-                const uint4 v = k4[q];
-                const int j = c0 + 4 * q;
-                if (j + 3 < i0) {               // all four before the block: ties count
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        cnt[u] += (v.x <= kk[u]) + (v.y <= kk[u]) + (v.z <= kk[u]) + (v.w <= kk[u]);
-                } else if (j >= i0 + RS_I) {    // all after: strict
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        cnt[u] += (v.x < kk[u]) + (v.y < kk[u]) + (v.z < kk[u]) + (v.w < kk[u]);
-                } else {
-                    const uint32_t e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const int jj = j + x;
-                        if (jj < m) {
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                cnt[u] += (e[x] < kk[u]) || (e[x] == kk[u] && jj < iv[u]);
-                        }
-                    }
-                }
-            }
-        }
-    } else {
-        int xv[4];
-        uint64_t kk[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            xv[u] = iv[u] < m ? cand[iv[u]] : 0;
-            kk[u] = iv[u] < m ? order_key(scores[xv[u]], xv[u]) : ~0ull;
-        }
-        for (int c0 = 0; c0 < m; c0 += RS_CHUNK) {
-            const int cn = min(RS_CHUNK, m - c0);
-            __syncthreads();
-            for (int t = threadIdx.x; t < cn; t += blockDim.x) {
-                const int x = cand[c0 + t];
-                keys64[t] = order_key(scores[x], x);
-            }
-            __syncthreads();
-            for (int t = sub; t < cn; t += nsub) {
-                const uint64_t k = keys64[t];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) cnt[u] += k < kk[u];
-            }
-        }
+    lo = __reduce_min_sync(FULL, lo);
+    hi = __reduce_max_sync(FULL, hi);
+    if (l == 0) {
+        wlo[tid >> 5] = lo;
+        whi[tid >> 5] = hi;
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) part[sub][4 * ig + u] = cnt[u];
     __syncthreads();
-    if (threadIdx.x < RS_I) {
-        const int e = threadIdx.x;
-        const int i = i0 + e;
-        if (i < m) {
-            uint32_t r = 0;
-            for (int q = 0; q < nsub; ++q) r += part[q][e];
-            const int x = cand ? cand[i] : i;
-            perm[r] = x;
-            boxes_s[r] = boxes[x];
+    BucketMap bm;
+    bm.lo = 0xffffffffu;
+    bm.hi = 0u;
+    for (int w = 0; w < BR_THREADS / 32; ++w) {
+        bm.lo = min(bm.lo, wlo[w]);
+        bm.hi = max(bm.hi, whi[w]);
+    }
+    if (bm.lo > bm.hi) bm.lo = bm.hi = 0u;  // no finite score
+    bm.mul = (static_cast<uint64_t>(BR_BUCKETS - 1) << 32) / (static_cast<uint64_t>(bm.hi - bm.lo) + 1);
+#pragma unroll
+    for (int u = 0; u < BR_KPT; ++u)
+        if (k[u] != MS_PAD) atomicAdd(&start[bm(k[u])], 1);
+    __syncthreads();
+    // Exclusive prefix of the bucket counts: thread t owns buckets [8t, 8t+8).
+    constexpr int BPT = BR_BUCKETS / BR_THREADS;
+    int v[BPT], run = 0;
+#pragma unroll
+    for (int u = 0; u < BPT; ++u) {
+        v[u] = start[tid * BPT + u];
+        run += v[u];
+    }
+    int x = run;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, d);
+        if (static_cast<int>(l) >= d) x += y;
+    }
+    if (l == 31) wsum[tid >> 5] = x;
+    __syncthreads();
+    int before = x - run;
+    for (int w = 0; w < (tid >> 5); ++w) before += wsum[w];
+#pragma unroll
+    for (int u = 0; u < BPT; ++u) {
+        start[tid * BPT + u] = before;
+        cur[tid * BPT + u] = before;
+        before += v[u];
+    }
+    if (tid == BR_THREADS - 1) start[BR_BUCKETS] = before;
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < BR_KPT; ++u)
+        if (k[u] != MS_PAD) list[atomicAdd(&cur[bm(k[u])], 1)] = k[u];
+    __syncthreads();
+    // Rank: warp w takes candidates w, w + 16, ...; lanes split the bucket.
+    const int warp = tid >> 5;
+    for (int e = warp; e < BR_CAND; e += BR_THREADS / 32) {
+        const uint64_t key = ckey[e];
+        int r = q0 + e - c0;                   // pads keep their place at the end
+        if (key != MS_PAD) {
+            const int b = bm(key);
+            const int s0 = start[b], s1 = start[b + 1];
+            int c = 0;
+            for (int i = s0 + static_cast<int>(l); i < s1; i += 32) c += list[i] < key;
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) c += __shfl_xor_sync(FULL, c, d);
+            r = s0 + c;
         }
+        if (l == 0) crank[e] = r;
+    }
+    __syncthreads();
+    if (tid < BR_CAND && q0 + tid < c0 + MS_CHUNK) {
+        if (multi) keys_out[c0 + crank[tid]] = ckey[tid];
+        else emit_sorted(ckey[tid], crank[tid], m, boxes, perm, boxes_s);
+    }
+}
+
+// Warp-cooperative merge-path search in global memory: the number of A
+// elements among the first d outputs of merge(A[0..na), B[0..nb)).  Each step
+// probes 32 evenly spaced candidates and keeps the interval where the
+// predicate A[i] <= B[d-1-i] changes.
+__device__ __forceinline__ int merge_path_warp(const uint64_t* __restrict__ A, int na,
+                                               const uint64_t* __restrict__ B, int nb, int d)
+{
+    int lo = max(0, d - nb), hi = min(d, na);  // answer in [lo, hi]
+    const int l = static_cast<int>(lane_id());
+    while (hi - lo > 0) {
+        const int span = hi - lo;
+        const int step = (span + 31) / 32;
+        const int mid = lo + l * step;  // probe: is the answer > mid?
+        const bool beyond = mid < hi && A[mid] <= B[d - 1 - mid];
+        const unsigned ball = __ballot_sync(FULL, beyond);
+        // predicate is true for a prefix of probes; the answer lies after the
+        // last true probe and at or before the first false one
+        const int t = __popc(ball);
+        const int nlo = t ? lo + (t - 1) * step + 1 : lo;
+        const int nhi = t < 32 ? min(hi, lo + t * step) : hi;
+        lo = nlo;
+        hi = nhi;
+        if (step == 1) break;
+    }
+    return lo;
+}
+
+// One doubling of the global merge: pairs of sorted runs of `run` keys from
+// keys_in into keys_out (or, when `last`, into perm and boxes_s).  CTA b makes
+// output tile [b*MS_CHUNK, (b+1)*MS_CHUNK).
+__global__ void __launch_bounds__(MS_THREADS, 1)
+merge_level_kernel(const uint64_t* __restrict__ keys_in, uint64_t* __restrict__ keys_out, int run,
+                   int last, const int* __restrict__ m_dev, int m_bound,
+                   const float4* __restrict__ boxes, int* __restrict__ perm,
+                   float4* __restrict__ boxes_s)
+{
+    extern __shared__ __align__(16) uint64_t buf[];  // MS_CHUNK keys, A part then B part, skewed
+    __shared__ int split[2];
+    const int tid = threadIdx.x;
+    const int o0 = blockIdx.x * MS_CHUNK;
+    const int pb = o0 & ~(2 * run - 1);       // start of the merge pair
+    const uint64_t* A = keys_in + pb;
+    const uint64_t* B = A + run;
+    const int warp = tid >> 5;
+    if (warp < 2) {
+        const int d = o0 - pb + warp * MS_CHUNK;
+        const int i = merge_path_warp(A, run, B, run, d);
+        if (lane_id() == 0) split[warp] = i;
+    }
+    __syncthreads();
+    const int d0 = o0 - pb;
+    const int ia = split[0], ib = split[1];
+    const int ja = d0 - ia, jb = d0 + MS_CHUNK - ib;
+    const int na = ib - ia, nb = jb - ja;
+    for (int t = tid; t < na; t += MS_THREADS) buf[sk(t)] = A[ia + t];
+    for (int t = tid; t < nb; t += MS_THREADS) buf[sk(na + t)] = B[ja + t];
+    __syncthreads();
+    uint64_t k[MS_P];
+    merge_p(buf, 0, na, na, nb, tid * MS_P, k);
+    if (last) {
+        const int m = m_dev ? *m_dev : m_bound;
+#pragma unroll
+        for (int u = 0; u < MS_P; ++u) emit_sorted(k[u], o0 + tid * MS_P + u, m, boxes, perm, boxes_s);
+    } else {
+        uint4* dst = reinterpret_cast<uint4*>(keys_out + o0 + tid * MS_P);
+#pragma unroll
+        for (int u = 0; u < MS_P; u += 2)
+            dst[u / 2] = make_uint4(static_cast<uint32_t>(k[u]), static_cast<uint32_t>(k[u] >> 32),
+                                    static_cast<uint32_t>(k[u + 1]), static_cast<uint32_t>(k[u + 1] >> 32));
     }
 }
 
@@ -177,14 +335,44 @@ void launch_prefilter(const float* scores, int n, float score_thr, int* cand, in
     if (n > 0) prefilter_kernel<<<(n + 255) / 256, 256, 0, st>>>(scores, n, score_thr, cand, m_count);
 }
 
-void launch_rank_sort(const float* scores, const float4* boxes, const int* cand, const int* m_dev,
-                      int m_bound, int* perm, float4* boxes_s, int32_t* status, uint64_t* rowbits,
-                      int NB, cudaStream_t st)
+int sort_chunks(int m_bound)
 {
-    int grid = (m_bound + RS_I - 1) / RS_I;
-    if (grid < 1) grid = 1;
-    rank_sort_kernel<<<grid, RS_WARPS * 32, 0, st>>>(scores, boxes, cand, m_dev, m_bound, perm,
-                                                    boxes_s, status, rowbits, NB);
+    int c = (m_bound + MS_CHUNK - 1) / MS_CHUNK;
+    int p = 1;
+    while (p < c) p *= 2;
+    return m_bound > 0 ? p : 1;
+}
+
+size_t sort_keys_bytes(int m_bound)
+{
+    const int c = sort_chunks(m_bound);
+    return c > 1 ? 2 * sizeof(uint64_t) * static_cast<size_t>(c) * MS_CHUNK : 0;
+}
+
+void launch_sort(const float* scores, const float4* boxes, const int* cand, const int* m_dev,
+                 int m_bound, int* perm, float4* boxes_s, uint64_t* keys, int32_t* status,
+                 uint64_t* rowbits, int NB, unsigned* ecount, uint64_t* haspred, cudaStream_t st)
+{
+    const int chunks = sort_chunks(m_bound);
+    const int per_chunk = chunks > 1 ? MS_CHUNK / BR_CAND : (m_bound + BR_CAND - 1) / BR_CAND;
+    const size_t rank_smem = sizeof(uint64_t) * MS_CHUNK + sizeof(int) * (2 * BR_BUCKETS + 1);
+    ensure_dynamic_smem(reinterpret_cast<const void*>(bucket_rank_kernel), rank_smem);
+    const size_t half = static_cast<size_t>(chunks) * MS_CHUNK;
+    uint64_t* k0 = keys;
+    uint64_t* k1 = keys ? keys + half : nullptr;
+    bucket_rank_kernel<<<dim3(per_chunk > 0 ? per_chunk : 1, chunks), BR_THREADS, rank_smem, st>>>(
+        scores, boxes, cand, m_dev, m_bound, k0, perm, boxes_s, status, rowbits, NB, ecount, haspred);
+    if (chunks == 1) return;
+    const size_t smem = sizeof(uint64_t) * MS_SLOTS;
+    ensure_dynamic_smem(reinterpret_cast<const void*>(merge_level_kernel), smem);
+    for (int run = MS_CHUNK; run < chunks * MS_CHUNK; run *= 2) {
+        const bool last = 2 * run >= chunks * MS_CHUNK;
+        merge_level_kernel<<<chunks, MS_THREADS, smem, st>>>(k0, k1, run, last ? 1 : 0, m_dev, m_bound,
+                                                             boxes, perm, boxes_s);
+        uint64_t* t = k0;
+        k0 = k1;
+        k1 = t;
+    }
 }
 
 }  // namespace gbnms

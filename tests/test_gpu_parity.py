@@ -332,3 +332,28 @@ def test_largest_single_image():
     b = np.concatenate([c - wh / 2, c + wh / 2], 1).astype(np.float32)
     s = rng.uniform(0, 1, n).astype(np.float32)
     _check_single(b, s, 0.5)
+
+
+def _parallel_chains(n_chains, length, step=0.3):
+    """n_chains separate rows of unit boxes sliding by `step`; box k of every
+    chain is visited before box k+1 of any chain, so the dependencies form
+    n_chains chains of `length` links that all advance together."""
+    k = np.repeat(np.arange(length), n_chains)
+    c = np.tile(np.arange(n_chains), length)
+    x = (k * step).astype(np.float32)
+    y = (c * 10.0).astype(np.float32)
+    b = np.stack([x, y, x + 1.0, y + 1.0], 1).astype(np.float32)
+    s = (1.0 - np.arange(length * n_chains) / (length * n_chains)).astype(np.float32)
+    perm = np.random.default_rng(length).permutation(len(s))
+    return b[perm], s[perm]
+
+
+@pytest.mark.parametrize("n_chains,length", [(100, 60), (64, 200), (8, 700), (1, 40)])
+def test_dependency_chains_of_many_links(n_chains, length):
+    """Chains deep enough to take many rounds of the sparse-graph resolve (and
+    the longest ones past its round limit, where the walk takes over)."""
+    b, s = _parallel_chains(n_chains, length)
+    for thr in (0.5, 0.3):
+        _check_single(b, s, thr)
+    _check_single(b, s, 0.5, max_out=len(s) // 3)
+    _check_single(b, s, 0.5, score_thr=0.25)

@@ -161,19 +161,15 @@ def run_reference(args):
     return 0
 
 
-def _algorithmic_resolve_bytes(wl):
-    """Mask bytes the resolve must read: for every kept row i, its words from
-    floor(i/64) to the end of the row (the triangle part to the right), plus
-    the diagonal word of every other row."""
+def _graph_size(wl):
+    """Pairs over the threshold in the upper triangle of the sorted order and
+    the number of kept boxes, from the oracle."""
     import oracle
     keep = oracle.nms_single(wl.boxes, wl.scores, wl.iou_thr, max_out=wl.max_out)
     order = oracle.score_order(wl.scores)
-    pos = np.empty(wl.n, np.int64)
-    pos[order] = np.arange(wl.n)
-    kp = pos[keep]
-    Wn = (wl.n + 63) // 64
-    row_words = (Wn - kp // 64).sum()
-    return int(8 * (row_words + wl.n)), len(keep)
+    m = oracle.mask(np.ascontiguousarray(wl.boxes[order]), wl.iou_thr)
+    bits = int(np.unpackbits(m.view(np.uint8)).sum())
+    return bits, len(keep)
 
 
 def time_workload(g, torch, wl, dev, flush, reps=30):
@@ -288,41 +284,24 @@ def run_gbnms(args):
     ms_per_step = total_ms / args.steps
     value = world * n * args.steps / (total_ms / 1000)
 
-    # ---- per-kernel durations: the same mask and resolve kernels launched
-    # alone through their entry points, on the same stream, L2 flushed before
-    # each launch.
-    order = np.argsort(-wl.scores.astype(np.float64), kind="stable")  # input prep only
-    bs = torch.from_numpy(np.ascontiguousarray(wl.boxes[order])).to(dev)
-    ldw = g.nms_mask_row_words(n)
-    mask = torch.zeros((n, ldw), dtype=torch.int64, device=dev)
-    kp = torch.empty(max(cap, 1), dtype=torch.int64, device=dev)
-    kc = torch.empty(1, dtype=torch.int64, device=dev)
-
-    def time_launch(fn, reps):
-        ts = []
-        for _ in range(reps):
-            flush.fill_(1)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            ts.append((a, b))
+    # ---- per-stage durations of the same calls: nms_run_timed records CUDA
+    # events on the launching stream between the stages (L2 flushed before
+    # each call, as in the timed region).
+    stage_t = [[], [], []]
+    for _ in range(max(args.steps, 10)):
+        flush.fill_(1)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        for e in ev:
+            e.record(stream)  # creates the handle; nms_run_timed records it again
+        st = g.nms_run_timed(boxes.data_ptr(), scores.data_ptr(), n, 0, 0, 0, 0, wl.iou_thr,
+                             score_thr, wl.max_out, keep.data_ptr(), cap, counts.data_ptr(),
+                             status.data_ptr(), ws.ptr, ws.bytes, sp, ev)
+        if st != g.NMS_OK:
+            raise g.NmsError(st, "nms_run_timed")
         torch.cuda.synchronize()
-        return statistics.mean(a.elapsed_time(b) for a, b in ts)
-
-    def mask_launch():
-        assert g.nms_iou_mask(bs.data_ptr(), n, wl.iou_thr, mask.data_ptr(), mask.numel(), sp) == 0
-
-    def resolve_launch():
-        assert g.nms_resolve_mask(mask.data_ptr(), n, 0, wl.max_out, kp.data_ptr(), kc.data_ptr(),
-                                  ws.ptr, ws.bytes, sp) == 0
-
-    for _ in range(3):
-        mask_launch()
-        resolve_launch()
-    reps = max(args.steps, 10)
-    mask_ms = time_launch(mask_launch, reps)
-    resolve_ms = time_launch(resolve_launch, reps)
+        for k in range(3):
+            stage_t[k].append(ev[k].elapsed_time(ev[k + 1]))
+    sort_ms, mask_ms, resolve_ms = (statistics.median(t) for t in stage_t)
 
     # ---- end to end through nms_run with host buffers
     hb = torch.from_numpy(wl.boxes).pin_memory()
@@ -370,16 +349,21 @@ def run_gbnms(args):
     peaks, peak_kind = _peaks()
     sm_max = float(peaks.get("sm_max_mhz", 2070.0))
     alu_peak_tops = SMS * FP32_LANES_PER_SM * sm_max * 1e6 / 1e12
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
     pairs = n * (n - 1) // 2
     mask_tops = OPS_PER_PAIR * pairs / (mask_ms / 1000) / 1e12
     Wn = (n + 63) // 64
-    mask_bytes = 8 * sum(Wn - i // 64 for i in range(0, n, 1))  # written triangle words
-    resolve_bytes, _ = _algorithmic_resolve_bytes(wl)
-    hbm = float(peaks.get("hbm_gbs", 6800.0))
-    sort_ms = max(ms_per_step - mask_ms - resolve_ms, 0.0)
-    kernels = {"rank_sort_gather_ms_est": sort_ms, "iou_mask_ms": mask_ms,
-               "resolve_ms": resolve_ms}
-    dominant = max(("iou_mask", mask_ms), ("resolve", resolve_ms), key=lambda x: x[1])[0]
+    mask_bytes = 8 * sum(Wn - i // 64 for i in range(n))  # triangle words written
+    n_pairs, n_kept = _graph_size(wl)
+    # Algorithmic bytes: sort = read scores and boxes, write perm and sorted
+    # boxes; resolve = read the pair list, the neighbour bitmap and perm of the
+    # kept, write the int64 keep list.
+    sort_bytes = n * (4 + 16 + 4 + 16)
+    resolve_bytes = 4 * n_pairs + n // 8 + n_kept * (4 + 8)
+    kernels = {"sort_gather_ms": sort_ms, "iou_mask_ms": mask_ms, "resolve_ms": resolve_ms,
+               "pairs_over_threshold": n_pairs}
+    dominant = max(("iou_mask", mask_ms), ("resolve", resolve_ms), ("sort", sort_ms),
+                   key=lambda x: x[1])[0]
     traffic = _ncu_traffic(dominant)
     if dominant == "iou_mask":
         roof = {"kernel": "iou_mask_kernel", "bound": "alu", "achieved": mask_tops,
@@ -388,10 +372,12 @@ def run_gbnms(args):
                 "note": f"FP32 ops, {OPS_PER_PAIR}/pair x {pairs} pairs; peak = {SMS} SMs x "
                         f"{FP32_LANES_PER_SM} lanes x {sm_max:.0f} MHz (max clock)"}
     else:
-        ach = resolve_bytes / (resolve_ms / 1000) / 1e9
-        roof = {"kernel": "resolve_single_kernel", "bound": "hbm", "achieved": ach, "peak": hbm,
-                "unit": "GB/s", "frac": ach / hbm, "traffic": traffic,
-                "note": f"algorithmic mask bytes read {resolve_bytes}; peak {peak_kind}"}
+        name, ms, nbytes = (("resolve_single_kernel", resolve_ms, resolve_bytes) if dominant == "resolve"
+                            else ("bucket_rank_kernel", sort_ms, sort_bytes))
+        ach = nbytes / (ms / 1000) / 1e9
+        roof = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "traffic": traffic,
+                "note": f"algorithmic bytes {nbytes}; peak {peak_kind}"}
 
     per_config = None
     if not args.no_configs:
@@ -423,7 +409,7 @@ def run_gbnms(args):
         "cpu_baseline": cpu,
         "e2e": {"value": n / (e2e_ms / 1000), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 3 * args.steps,  # sort, mask, resolve per call at this size
         "clocks": clocks,
         "parity_vs_oracle": parity,
         "peaks": peak_kind,
@@ -434,7 +420,7 @@ def run_gbnms(args):
     return 0
 
 
-KERNEL_SOURCES = {"iou_mask": "k_mask.cu", "resolve": "k_resolve.cu"}
+KERNEL_SOURCES = {"iou_mask": "k_mask.cu", "resolve": "k_resolve.cu", "sort": "k_sort.cu"}
 
 
 def kernel_source_sha(kernel):

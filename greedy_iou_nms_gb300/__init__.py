@@ -28,8 +28,8 @@ NMS_ERR_CUDA = 4
 NMS_ERR_TIMEOUT = 5
 NMS_MAX_SINGLE_N = 1 << 18
 
-EXPORTED = ("nms_status_string", "nms_workspace_size", "nms_run", "nms_mask_row_words",
-            "nms_iou_mask", "nms_resolve_mask", "nms_resolve_mask_noalloc")
+EXPORTED = ("nms_status_string", "nms_workspace_size", "nms_run", "nms_run_timed",
+            "nms_mask_row_words", "nms_iou_mask", "nms_resolve_mask", "nms_resolve_mask_noalloc")
 NMS_NOALLOC_MAX_N = 16384
 
 _lib = None
@@ -62,6 +62,9 @@ def load():
     lib.nms_workspace_size.restype = ctypes.c_int
     lib.nms_run.argtypes = [vp, vp, i64, vp, i32, vp, i32, f32, f32, i32, vp, i64, vp, vp, vp, sz, vp]
     lib.nms_run.restype = ctypes.c_int
+    lib.nms_run_timed.argtypes = [vp, vp, i64, vp, i32, vp, i32, f32, f32, i32, vp, i64, vp, vp, vp,
+                                  sz, vp, ctypes.POINTER(vp), i32]
+    lib.nms_run_timed.restype = ctypes.c_int
     lib.nms_mask_row_words.argtypes = [i64]
     lib.nms_mask_row_words.restype = i64
     lib.nms_iou_mask.argtypes = [vp, i64, f32, vp, i64, vp]
@@ -102,6 +105,25 @@ def nms_run(boxes: int, scores: int, n: int, class_ids: int, num_classes: int,
                           float(score_thr), int(max_out), keep or None, int(keep_cap),
                           counts or None, dev_status or None, workspace or None,
                           int(workspace_bytes), stream or None)
+
+
+def nms_run_timed(boxes: int, scores: int, n: int, class_ids: int, num_classes: int,
+                  batch_offsets: int, batch: int, iou_thr: float, score_thr: float, max_out: int,
+                  keep: int, keep_cap: int, counts: int, dev_status: int, workspace: int,
+                  workspace_bytes: int, stream: int, events) -> int:
+    """nms_run that also records the given CUDA events (handles as ints, or
+    objects with a ``cuda_event`` handle such as torch.cuda.Event) between its
+    stages: before the first kernel, then after each stage.  The events must
+    exist already (a torch.cuda.Event creates its handle at its first record)."""
+    handles = [e if isinstance(e, int) else int(e.cuda_event) for e in events]
+    if not all(handles):
+        raise ValueError("nms_run_timed: every event must already be created")
+    arr = (ctypes.c_void_p * max(len(handles), 1))(*[h or None for h in handles])
+    return load().nms_run_timed(boxes or None, scores or None, int(n), class_ids or None,
+                                int(num_classes), batch_offsets or None, int(batch), float(iou_thr),
+                                float(score_thr), int(max_out), keep or None, int(keep_cap),
+                                counts or None, dev_status or None, workspace or None,
+                                int(workspace_bytes), stream or None, arr, len(handles))
 
 
 def nms_iou_mask(boxes_sorted: int, n: int, iou_thr: float, mask: int, mask_words: int,

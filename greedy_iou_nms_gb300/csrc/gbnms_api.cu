@@ -178,12 +178,13 @@ extern "C" int64_t nms_mask_row_words(int64_t n)
     return n <= 0 ? 0 : 4 * ((n + 255) / 256);
 }
 
-extern "C" nms_status nms_run(const float* boxes, const float* scores, int64_t n,
-                              const int32_t* class_ids, int32_t num_classes,
-                              const int64_t* batch_offsets, int32_t batch, float iou_thr,
-                              float score_thr, int32_t max_out, int64_t* keep, int64_t keep_cap,
-                              int64_t* counts, int32_t* dev_status, void* workspace,
-                              size_t workspace_bytes, void* stream)
+namespace {
+
+nms_status run_impl(const float* boxes, const float* scores, int64_t n, const int32_t* class_ids,
+                    int32_t num_classes, const int64_t* batch_offsets, int32_t batch, float iou_thr,
+                    float score_thr, int32_t max_out, int64_t* keep, int64_t keep_cap,
+                    int64_t* counts, int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                    void* stream, const Stamps& stamps)
 {
     if (n < 0 || n > INT32_MAX) return NMS_ERR_INVALID_ARG;
     if (std::isnan(iou_thr) || std::isnan(score_thr)) return NMS_ERR_INVALID_ARG;
@@ -214,13 +215,16 @@ extern "C" nms_status nms_run(const float* boxes, const float* scores, int64_t n
         const SingleLayout L = single_layout(n);
         int32_t* status = dev_status ? dev_status : at<int32_t>(workspace, L.status);
         if (n == 0) {
+            stamps.record(0, st);
             cudaMemsetAsync(counts, 0, sizeof(int64_t), st);
             cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+            for (int k = 1; k <= 3; ++k) stamps.record(k, st);
             return cuda_status();
         }
         const ThrParams p = make_thr(iou_thr);
         int* m_count = nullptr;
         int* cand = nullptr;
+        stamps.record(0, st);
         if (use_thr) {
             m_count = at<int>(workspace, L.m_count);
             cand = at<int>(workspace, L.cand);
@@ -236,11 +240,14 @@ extern "C" nms_status nms_run(const float* boxes, const float* scores, int64_t n
         uint64_t* keys = sort_keys_bytes(static_cast<int>(n)) ? at<uint64_t>(workspace, L.keys) : nullptr;
         launch_sort(scores, reinterpret_cast<const float4*>(boxes), cand, m_count, static_cast<int>(n),
                     perm, boxes_s, keys, status, rowbits, L.NB, ecount, haspred, st);
+        stamps.record(1, st);
         uint64_t* band = at<uint64_t>(workspace, L.band);
         launch_iou_mask(boxes_s, m_count, static_cast<int>(n), p, mask, L.ldw, rowbits, L.NB, band,
                         edges, ecount, L.ecap, haspred, st);
+        stamps.record(2, st);
         launch_resolve_single(mask, L.ldw, rowbits, L.NB, band, edges, ecount, haspred, m_count,
                               static_cast<int>(n), perm, max_out, keep, counts, status, st);
+        stamps.record(3, st);
         return cuda_status();
     }
 
@@ -272,8 +279,38 @@ extern "C" nms_status nms_run(const float* boxes, const float* scores, int64_t n
     a.keep = keep;
     a.counts = counts;
     a.status = dev_status ? dev_status : at<int32_t>(workspace, L.status);
-    launch_batched(a, st);
+    launch_batched(a, st, stamps);
     return cuda_status();
+}
+
+}  // namespace
+
+extern "C" nms_status nms_run(const float* boxes, const float* scores, int64_t n,
+                              const int32_t* class_ids, int32_t num_classes,
+                              const int64_t* batch_offsets, int32_t batch, float iou_thr,
+                              float score_thr, int32_t max_out, int64_t* keep, int64_t keep_cap,
+                              int64_t* counts, int32_t* dev_status, void* workspace,
+                              size_t workspace_bytes, void* stream)
+{
+    return run_impl(boxes, scores, n, class_ids, num_classes, batch_offsets, batch, iou_thr,
+                    score_thr, max_out, keep, keep_cap, counts, dev_status, workspace,
+                    workspace_bytes, stream, Stamps{});
+}
+
+extern "C" nms_status nms_run_timed(const float* boxes, const float* scores, int64_t n,
+                                    const int32_t* class_ids, int32_t num_classes,
+                                    const int64_t* batch_offsets, int32_t batch, float iou_thr,
+                                    float score_thr, int32_t max_out, int64_t* keep,
+                                    int64_t keep_cap, int64_t* counts, int32_t* dev_status,
+                                    void* workspace, size_t workspace_bytes, void* stream,
+                                    void* const* events, int32_t nevents)
+{
+    Stamps sp;
+    sp.ev = events;
+    sp.n = events && nevents > 0 ? nevents : 0;
+    return run_impl(boxes, scores, n, class_ids, num_classes, batch_offsets, batch, iou_thr,
+                    score_thr, max_out, keep, keep_cap, counts, dev_status, workspace,
+                    workspace_bytes, stream, sp);
 }
 
 extern "C" nms_status nms_iou_mask(const float* boxes_sorted, int64_t n, float iou_thr,

@@ -8,6 +8,17 @@ namespace gbnms {
 
 struct ThrParams;
 
+// Caller's stage events of nms_run_timed: record(k) records events[k] on the
+// stream when present.
+struct Stamps {
+    void* const* ev = nullptr;
+    int n = 0;
+    void record(int k, cudaStream_t st) const
+    {
+        if (k < n && ev && ev[k]) cudaEventRecord(static_cast<cudaEvent_t>(ev[k]), st);
+    }
+};
+
 // Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
 // current device; the runtime is called only when the limit recorded for
 // that (device, kernel) is lower, so repeated launches pay nothing.
@@ -62,6 +73,6 @@ struct BatchedArgs {
     int32_t* status;
 };
 
-void launch_batched(const BatchedArgs& a, cudaStream_t st);
+void launch_batched(const BatchedArgs& a, cudaStream_t st, const Stamps& stamps);
 
 }  // namespace gbnms

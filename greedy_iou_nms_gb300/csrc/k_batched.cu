@@ -409,10 +409,11 @@ merge_kernel(const int* __restrict__ seg_off, const int* __restrict__ kept_cnt,
 
 // ------------------------------------------------------------------ launches
 
-void launch_batched(const BatchedArgs& a, cudaStream_t st)
+void launch_batched(const BatchedArgs& a, cudaStream_t st, const Stamps& stamps)
 {
     const int n = a.n;
     const int S = a.S;
+    stamps.record(0, st);
     batched_setup_kernel<<<1, 1024, 0, st>>>(a.off, a.batch, n, S, a.seg_cnt, a.ok, a.status);
     if (n > 0) {
         batched_count_kernel<<<(n + 255) / 256, 256, 0, st>>>(
@@ -421,13 +422,16 @@ void launch_batched(const BatchedArgs& a, cudaStream_t st)
     }
     batched_scan_kernel<<<1, 1024, 0, st>>>(a.seg_cnt, S, a.seg_off);
     if (n > 0) batched_scatter_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.seg_of, a.slot, a.seg_off, n, a.ok, a.cand);
+    stamps.record(1, st);
     seg_small_kernel<<<(S + SS_WARPS - 1) / SS_WARPS, SS_WARPS * 32, 0, st>>>(
         a.boxes, a.scores, a.seg_off, a.cand, S, a.ok, a.thr, a.max_out, a.kept_key, a.kept_cnt);
     seg_large_kernel<<<S, SL_THREADS, 0, st>>>(a.boxes, a.scores, a.seg_off, a.cand, S, a.ok, a.thr,
                                                a.max_out, a.sorted_key, a.sorted_box, a.kept_key,
                                                a.kept_cnt);
+    stamps.record(2, st);
     merge_kernel<<<a.batch, MG_THREADS, 0, st>>>(a.seg_off, a.kept_cnt, a.kept_key, a.C, a.off,
                                                   a.ok, a.max_out, a.stage, a.keep, a.counts);
+    stamps.record(3, st);
 }
 
 }  // namespace gbnms

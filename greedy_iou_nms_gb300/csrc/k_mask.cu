@@ -9,10 +9,10 @@
 // (Part 2)", section "Optimization 1: tile the IoU matrix": coordinates loaded
 // once per tile and reused by every row.
 //
-// GB300 shape: a CTA computes a 128-row x 256-column tile.  Each lane holds two
-// row boxes in registers and walks the 256 staged column boxes (broadcast
-// shared-memory reads), so a row's four words of the tile (one 32-byte
-// sector) are built in registers and written with two 16-byte stores.  The
+// GB300 shape: a CTA computes a tile of M_WARPS*64 rows x MT columns.  Each
+// lane holds two row boxes in registers and walks the MT staged column boxes
+// (broadcast shared-memory reads), so a row's words of the tile are built in
+// registers and written with 16-byte stores.  The
 // triangle of tiles is enumerated column by column.  Each row also records,
 // one bit per 256-column chunk, which of its chunks hold a set bit, and the
 // 64x64 blocks within BAND_L tiles of the diagonal are also written in column
@@ -28,18 +28,23 @@
 #include "internal.h"
 
 #ifndef GBNMS_MASK_WARPS
-#define GBNMS_MASK_WARPS 4
+#define GBNMS_MASK_WARPS 2
 #endif
 #ifndef GBNMS_MASK_UNROLL
-#define GBNMS_MASK_UNROLL 8
+#define GBNMS_MASK_UNROLL 2
+#endif
+#ifndef GBNMS_MASK_MT
+#define GBNMS_MASK_MT 128
 #endif
 namespace gbnms {
-constexpr int kMaskUnroll = GBNMS_MASK_UNROLL;  // unroll of the 32-column inner loop
+constexpr int kMaskUnroll = GBNMS_MASK_UNROLL;  // unroll of the inner loop (4 columns per step)
 }
 
 namespace gbnms {
 
-constexpr int MT = 256;         // tile width (columns)
+constexpr int MT = GBNMS_MASK_MT;  // tile width (columns)
+constexpr int NQ = MT / 64;        // 64-bit words of a row per tile
+static_assert(NQ == 1 || NQ == 2 || NQ == 4, "tile width of 64, 128 or 256 columns");
 constexpr int M_WARPS = GBNMS_MASK_WARPS;  // warps of 64 rows per tile
 constexpr int MR = M_WARPS * 64;  // tile height (rows)
 constexpr int M_THREADS = M_WARPS * 32;
@@ -60,7 +65,7 @@ __device__ __forceinline__ void tri_coords(long long k, int& a, int& c)
     c = static_cast<int>(cc);
     a = static_cast<int>(k - r * cc * (cc + 1) / 2);
 }
-static_assert(MT == 2 * MR || MT == MR, "tri_coords handles column tiles one or two row tiles wide");
+static_assert(MT % MR == 0, "a column tile spans a whole number of row tiles");
 
 // Sign bit of RN(k*s - a): set iff the exact k*s - a is negative, i.e.
 // a > k*s (the product inside a fused multiply-add is not rounded).
@@ -69,45 +74,66 @@ __device__ __forceinline__ uint32_t sign_above(float k, float s, float a)
     return __float_as_uint(__fmaf_rn(k, s, -a));
 }
 
-// One 32-column half of the division-free test for one row: shifts the
-// decision bits into `yes` and the "not surely below" bits into `maybe`,
-// highest column first, so bit k ends up meaning column k.  For well-formed
-// boxes and the constants of ThrParams, a > k_hi*s proves suppression and
-// a <= k_lo*s proves no suppression (common.cuh); a pair with maybe and not
-// yes is left to the exact division.  The intersection is fmax(w,0)*h with h
-// unclamped: when h <= 0 the product is <= 0 and both tests say no, as the
-// canonical (clamped) intersection 0 would.
-__device__ __forceinline__ void half_fast(const float4* __restrict__ cb, const float* __restrict__ ca,
-                                          float4 r, float ar, float khi, float klo, uint32_t& yes,
-                                          uint32_t& maybe)
+// One pair of the division-free test, shifted into the accumulators: `yes`
+// takes the decision bit and `maybe` the "not surely below" bit.  For
+// well-formed boxes and the constants of ThrParams, a > k_hi*s proves
+// suppression and a <= k_lo*s proves no suppression (common.cuh); a pair with
+// maybe and not yes is left to the exact division.  The test runs on doubled
+// values: w + |w| = 2 max(w, 0) exactly, so a2 = (w + |w|) h = 2 a with h
+// unclamped (when h <= 0 the product is <= 0 and both tests say no, as the
+// canonical clamped intersection 0 would), compared against the doubled
+// constants khi2 = 2 k_hi and klo2 = 2 k_lo.  Doubling is exact here: well-
+// formed areas are at most 2^58, and an intersection small enough to round
+// differently (below 2^-125) is far below k_lo * s >= 2^-78 either way.
+__device__ __forceinline__ void pair_fast(float4 r, float ar, float4 c, float ac, float khi2, float klo2,
+                                          uint32_t& yes, uint32_t& maybe)
 {
+    const float w = __fsub_rn(fminf(r.z, c.z), fmaxf(r.x, c.x));
+    const float w2 = __fadd_rn(w, fabsf(w));
+    const float h = __fsub_rn(fminf(r.w, c.w), fmaxf(r.y, c.y));
+    const float a2 = __fmul_rn(w2, h);
+    const float s = __fadd_rn(ar, ac);
+    yes = __funnelshift_l(sign_above(khi2, s, a2), yes, 1);
+    maybe = __funnelshift_l(sign_above(klo2, s, a2), maybe, 1);
+}
+
+// Both rows of a lane against 32 staged columns (cb, ca 16-byte aligned),
+// highest column first so that bit k ends up meaning column k; one shared
+// load of a column box feeds both rows, one 16-byte load brings 4 areas.
+__device__ __forceinline__ void half_fast(const float4* __restrict__ cb, const float* __restrict__ ca,
+                                          float4 r0, float ar0, float4 r1, float ar1, float khi2,
+                                          float klo2, uint32_t& y0, uint32_t& m0, uint32_t& y1,
+                                          uint32_t& m1)
+{
+    const float4* ca4 = reinterpret_cast<const float4*>(ca);
 #pragma unroll kMaskUnroll
-    for (int k = 31; k >= 0; --k) {
-        const float4 c = cb[k];
-        const float w = fmaxf(__fsub_rn(fminf(r.z, c.z), fmaxf(r.x, c.x)), 0.0f);
-        const float h = __fsub_rn(fminf(r.w, c.w), fmaxf(r.y, c.y));
-        const float a = __fmul_rn(w, h);
-        const float s = __fadd_rn(ar, ca[k]);
-        yes = __funnelshift_l(sign_above(khi, s, a), yes, 1);
-        maybe = __funnelshift_l(sign_above(klo, s, a), maybe, 1);
+    for (int g = 7; g >= 0; --g) {
+        const float4 a4 = ca4[g];
+        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+        for (int e = 3; e >= 0; --e) {
+            const float4 c = cb[4 * g + e];
+            pair_fast(r0, ar0, c, av[e], khi2, klo2, y0, m0);
+            pair_fast(r1, ar1, c, av[e], khi2, klo2, y1, m1);
+        }
     }
 }
 
 template <bool FAST>
 __device__ __forceinline__ void tile_rows(const float4* __restrict__ cbox, const float* __restrict__ carea,
                                           float4 r0, float ar0, float4 r1, float ar1,
-                                          const ThrParams& p, uint64_t (&w0)[4], uint64_t (&w1)[4],
+                                          const ThrParams& p, uint64_t (&w0)[NQ], uint64_t (&w1)[NQ],
                                           bool& unsure)
 {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < NQ; ++q) {
         uint32_t lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
         if (FAST) {
             uint32_t ml0 = 0, mh0 = 0, ml1 = 0, mh1 = 0;
-            half_fast(cbox + q * 64, carea + q * 64, r0, ar0, p.k_hi, p.k_lo, lo0, ml0);
-            half_fast(cbox + q * 64, carea + q * 64, r1, ar1, p.k_hi, p.k_lo, lo1, ml1);
-            half_fast(cbox + q * 64 + 32, carea + q * 64 + 32, r0, ar0, p.k_hi, p.k_lo, hi0, mh0);
-            half_fast(cbox + q * 64 + 32, carea + q * 64 + 32, r1, ar1, p.k_hi, p.k_lo, hi1, mh1);
+            const float khi2 = __fmul_rn(2.0f, p.k_hi), klo2 = __fmul_rn(2.0f, p.k_lo);
+            half_fast(cbox + q * 64, carea + q * 64, r0, ar0, r1, ar1, khi2, klo2, lo0, ml0, lo1, ml1);
+            half_fast(cbox + q * 64 + 32, carea + q * 64 + 32, r0, ar0, r1, ar1, khi2, klo2, hi0, mh0,
+                      hi1, mh1);
             unsure |= ((ml0 & ~lo0) | (mh0 & ~hi0) | (ml1 & ~lo1) | (mh1 & ~hi1)) != 0;
         } else {
 #pragma unroll 8
@@ -131,10 +157,10 @@ __device__ __forceinline__ void tile_rows(const float4* __restrict__ cbox, const
 }
 
 // Keep only bits j with j > i and j < n of the four words at column base cb.
-__device__ __forceinline__ void clip_words(uint64_t (&w)[4], int i, int cb, int n)
+__device__ __forceinline__ void clip_words(uint64_t (&w)[NQ], int i, int cb, int n)
 {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < NQ; ++q) {
         int j0 = cb + 64 * q;
         uint64_t keep = ~0ull;
         int lo = i + 1 - j0;                    // first allowed bit
@@ -147,12 +173,12 @@ __device__ __forceinline__ void clip_words(uint64_t (&w)[4], int i, int cb, int 
     }
 }
 
-// Append the set bits of row i's four words at column base cb as packed
+// Append the set bits of row i's words at column base cb as packed
 // (i << 16 | j) pairs.
-__device__ __forceinline__ uint32_t* emit_row(uint32_t* dst, const uint64_t (&w)[4], int i, int cb)
+__device__ __forceinline__ uint32_t* emit_row(uint32_t* dst, const uint64_t (&w)[NQ], int i, int cb)
 {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < NQ; ++q) {
         uint64_t x = w[q];
         while (x) {
             const int b = __ffsll(static_cast<long long>(x)) - 1;
@@ -163,9 +189,31 @@ __device__ __forceinline__ uint32_t* emit_row(uint32_t* dst, const uint64_t (&w)
     return dst;
 }
 
-__device__ __forceinline__ int popc4(const uint64_t (&w)[4])
+__device__ __forceinline__ int popc_words(const uint64_t (&w)[NQ])
 {
-    return __popcll(w[0]) + __popcll(w[1]) + __popcll(w[2]) + __popcll(w[3]);
+    int c = 0;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) c += __popcll(w[q]);
+    return c;
+}
+
+__device__ __forceinline__ uint64_t or_words(const uint64_t (&w)[NQ])
+{
+    uint64_t v = 0;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) v |= w[q];
+    return v;
+}
+
+// Row i's words of the tile: 16-byte stores (one 8-byte store for one word).
+__device__ __forceinline__ void store_words(uint64_t* dst, const uint64_t (&w)[NQ])
+{
+    if constexpr (NQ == 1) {
+        dst[0] = w[0];
+    } else {
+#pragma unroll
+        for (int q = 0; q < NQ; q += 2) reinterpret_cast<ulonglong2*>(dst)[q / 2] = make_ulonglong2(w[q], w[q + 1]);
+    }
 }
 
 __global__ void __launch_bounds__(M_THREADS)
@@ -176,7 +224,7 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
                 unsigned long long* __restrict__ haspred)
 {
     __shared__ float4 cbox[MT];
-    __shared__ float carea[MT];
+    __shared__ __align__(16) float carea[MT];
 
     const int n = m_dev ? *m_dev : m_bound;
     int a, c;
@@ -207,17 +255,17 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
     if (i1 < n) ok &= well_formed(r1, ar1);
     const bool fast = __syncthreads_and(ok) && p.fast_ok;
 
-    uint64_t w0[4], w1[4];
+    uint64_t w0[NQ], w1[NQ];
     bool unsure = false;
     if (fast) {
         tile_rows<true>(cbox, carea, r0, ar0, r1, ar1, p, w0, w1, unsure);
         if (__any_sync(FULL, unsure)) {
-            uint64_t e0[4], e1[4];
+            uint64_t e0[NQ], e1[NQ];
             bool dummy = false;
             if (unsure) {
                 tile_rows<false>(cbox, carea, r0, ar0, r1, ar1, p, e0, e1, dummy);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) { w0[q] = e0[q]; w1[q] = e1[q]; }
+                for (int q = 0; q < NQ; ++q) { w0[q] = e0[q]; w1[q] = e1[q]; }
             }
         }
     } else {
@@ -238,8 +286,8 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
         const int R = rbase / 64 + wp;
         const int T64 = (n + 63) / 64;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int C = 4 * c + q;
+        for (int q = 0; q < NQ; ++q) {
+            const int C = cb / 64 + q;
             const int d = C - R;
             if (d < 0 || d > BAND_L || C >= T64) continue;  // warp-uniform
             uint64_t colA = w0[q], colB = w1[q];
@@ -247,26 +295,23 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
             band[(static_cast<int64_t>(C) * (BAND_L + 1) + d) * 32 + l] = make_ulonglong2(colA, colB);
         }
     }
-    const int64_t wcol = static_cast<int64_t>(c) * 4;
+    const int64_t wcol = cb / 64;
+    const int chunk = cb >> 8;  // 256-column chunk of the per-row bitmap
     if (i0 < n) {
-        uint64_t* dst = mask + static_cast<int64_t>(i0) * ldw + wcol;
-        reinterpret_cast<ulonglong2*>(dst)[0] = make_ulonglong2(w0[0], w0[1]);
-        reinterpret_cast<ulonglong2*>(dst)[1] = make_ulonglong2(w0[2], w0[3]);
-        if (rowbits && (w0[0] | w0[1] | w0[2] | w0[3]))
-            atomicOr(rowbits + static_cast<int64_t>(i0) * NB + (c >> 6), 1ull << (c & 63));
+        store_words(mask + static_cast<int64_t>(i0) * ldw + wcol, w0);
+        if (rowbits && or_words(w0))
+            atomicOr(rowbits + static_cast<int64_t>(i0) * NB + (chunk >> 6), 1ull << (chunk & 63));
     }
     if (i1 < n) {
-        uint64_t* dst = mask + static_cast<int64_t>(i1) * ldw + wcol;
-        reinterpret_cast<ulonglong2*>(dst)[0] = make_ulonglong2(w1[0], w1[1]);
-        reinterpret_cast<ulonglong2*>(dst)[1] = make_ulonglong2(w1[2], w1[3]);
-        if (rowbits && (w1[0] | w1[1] | w1[2] | w1[3]))
-            atomicOr(rowbits + static_cast<int64_t>(i1) * NB + (c >> 6), 1ull << (c & 63));
+        store_words(mask + static_cast<int64_t>(i1) * ldw + wcol, w1);
+        if (rowbits && or_words(w1))
+            atomicOr(rowbits + static_cast<int64_t>(i1) * NB + (chunk >> 6), 1ull << (chunk & 63));
     }
     // Boxes with at least one earlier box over the threshold: the OR of the
     // warp's rows, one atomic per non-zero 64-column word.
     if (haspred) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < NQ; ++q) {
             const uint64_t v = (i0 < n ? w0[q] : 0ull) | (i1 < n ? w1[q] : 0ull);
             const unsigned lo = __reduce_or_sync(FULL, static_cast<unsigned>(v));
             const unsigned hi = __reduce_or_sync(FULL, static_cast<unsigned>(v >> 32));
@@ -279,7 +324,7 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
     // count still grows (it tells the resolve the list is incomplete) and
     // nothing is written.
     if (edges) {
-        const int cnt = (i0 < n ? popc4(w0) : 0) + (i1 < n ? popc4(w1) : 0);
+        const int cnt = (i0 < n ? popc_words(w0) : 0) + (i1 < n ? popc_words(w1) : 0);
         int x = cnt;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {

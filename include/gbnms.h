@@ -168,6 +168,27 @@ nms_status nms_resolve_mask(const uint64_t* mask, int64_t n, const int32_t* perm
                             int32_t max_out, int64_t* keep, int64_t* count,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * nms_run with stage timing, for measurement: the same call, plus up to
+ * nevents caller-created CUDA events (cudaEvent_t, created with timing
+ * enabled) that it records on `stream`: events[0] before its first kernel and
+ * events[k] when stage k has been enqueued.
+ *   One image:  1 = pre-filter, sort and gather; 2 = IoU mask (with the pair
+ *               list); 3 = resolve and output.
+ *   Batched:    1 = pre-filter and bucketing into (image, class) segments;
+ *               2 = per-segment NMS; 3 = per-image merge and output.
+ * NULL entries and entries past nevents are skipped (nevents may be 0).  The
+ * events are only recorded, never synchronised.  Arguments, errors and
+ * results otherwise as for nms_run.
+ */
+nms_status nms_run_timed(const float* boxes, const float* scores, int64_t n,
+                         const int32_t* class_ids, int32_t num_classes,
+                         const int64_t* batch_offsets, int32_t batch, float iou_thr,
+                         float score_thr, int32_t max_out, int64_t* keep, int64_t keep_cap,
+                         int64_t* counts, int32_t* dev_status, void* workspace,
+                         size_t workspace_bytes, void* stream, void* const* events,
+                         int32_t nevents);
+
 /* Largest n nms_resolve_mask_noalloc accepts. */
 #define NMS_NOALLOC_MAX_N 16384
 

@@ -99,6 +99,21 @@ def test_host_validation(lib):
                 keep_cap=19, workspace_bytes=wsb) == g.NMS_ERR_CAPACITY
 
 
+def test_timed_entry_validates_like_nms_run(lib):
+    """nms_run_timed checks its arguments exactly as nms_run does, before any
+    event is touched (the event handles here are fake and never used)."""
+    ws = g.nms_workspace_size(10)
+    a = dict(boxes=FAKE, scores=FAKE, n=10, class_ids=0, num_classes=0, batch_offsets=0, batch=0,
+             iou_thr=0.5, score_thr=-math.inf, max_out=0, keep=FAKE, keep_cap=10, counts=FAKE,
+             dev_status=0, workspace=FAKE, workspace_bytes=ws, stream=0)
+    fake_events = [FAKE, FAKE, FAKE, FAKE]
+    for bad, code in ((dict(n=-1), g.NMS_ERR_INVALID_ARG), (dict(iou_thr=math.nan), g.NMS_ERR_INVALID_ARG),
+                      (dict(keep_cap=9), g.NMS_ERR_CAPACITY), (dict(workspace_bytes=ws - 1), g.NMS_ERR_WORKSPACE)):
+        kw = dict(a, **bad)
+        assert g.nms_run_timed(**kw, events=fake_events) == code
+        assert g.nms_run(**kw) == code
+
+
 def test_mask_entry_validation(lib):
     assert g.nms_iou_mask(FAKE, -1, 0.5, FAKE, 0, 0) == g.NMS_ERR_INVALID_ARG
     assert g.nms_iou_mask(FAKE, 10, math.nan, FAKE, 40, 0) == g.NMS_ERR_INVALID_ARG

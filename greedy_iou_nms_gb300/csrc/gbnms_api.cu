@@ -50,8 +50,8 @@ struct SingleLayout {
     int64_t ldw = 0;
     int NB = 0;  // 64-bit words of the per-row chunk bitmap
     unsigned ecap = 0;  // pairs of the sparse list (0: no list, the walk resolves)
-    size_t status, m_count, ecount, cand, perm, boxes_s, keys, rowbits, band, edges, haspred, mask,
-        total;
+    size_t status, m_count, ecount, done, cand, perm, boxes_s, keys, rowbits, band, edges, haspred,
+        mask, total;
 };
 
 SingleLayout single_layout(int64_t n)
@@ -65,6 +65,7 @@ SingleLayout single_layout(int64_t n)
     s.status = L.add(4);
     s.m_count = L.add(4);
     s.ecount = L.add(4);
+    s.done = L.add(4);
     s.cand = L.add(4 * static_cast<size_t>(n));
     s.perm = L.add(4 * static_cast<size_t>(n));
     s.boxes_s = L.add(16 * static_cast<size_t>(n));
@@ -242,11 +243,33 @@ nms_status run_impl(const float* boxes, const float* scores, int64_t n, const in
                     perm, boxes_s, keys, status, rowbits, L.NB, ecount, haspred, st);
         stamps.record(1, st);
         uint64_t* band = at<uint64_t>(workspace, L.band);
-        launch_iou_mask(boxes_s, m_count, static_cast<int>(n), p, mask, L.ldw, rowbits, L.NB, band,
-                        edges, ecount, L.ecap, haspred, st);
-        stamps.record(2, st);
-        launch_resolve_single(mask, L.ldw, rowbits, L.NB, band, edges, ecount, haspred, m_count,
-                              static_cast<int>(n), perm, max_out, keep, counts, status, st);
+        const int nb = static_cast<int>(n);
+        // With max_out, the first kept boxes depend only on a prefix of the
+        // score order: mask and resolve the leading 2*max_out boxes first, and
+        // the rest only if that prefix held fewer than max_out kept boxes (the
+        // later launches find the device flag set and return at once).
+        const int64_t k1 = max_out > 0 ? (2 * static_cast<int64_t>(max_out) + MASK_TILE_W - 1) /
+                                             MASK_TILE_W * MASK_TILE_W
+                                       : n;
+        if (k1 >= n) {
+            launch_iou_mask(boxes_s, m_count, nb, p, mask, L.ldw, rowbits, L.NB, band, edges, ecount,
+                            L.ecap, haspred, st);
+            stamps.record(2, st);
+            launch_resolve_single(mask, L.ldw, rowbits, L.NB, band, edges, ecount, haspred, m_count, nb,
+                                  perm, max_out, keep, counts, status, st);
+        } else {
+            int* done = at<int>(workspace, L.done);
+            const int k = static_cast<int>(k1);
+            launch_iou_mask(boxes_s, m_count, nb, p, mask, L.ldw, rowbits, L.NB, band, edges, ecount,
+                            L.ecap, haspred, st, 0, k);
+            stamps.record(2, st);
+            launch_resolve_single(mask, L.ldw, rowbits, L.NB, band, edges, ecount, haspred, m_count, nb,
+                                  perm, max_out, keep, counts, status, st, k, nullptr, done);
+            launch_iou_mask(boxes_s, m_count, nb, p, mask, L.ldw, rowbits, L.NB, band, edges, ecount,
+                            L.ecap, haspred, st, k, nb, done);
+            launch_resolve_single(mask, L.ldw, rowbits, L.NB, band, edges, ecount, haspred, m_count, nb,
+                                  perm, max_out, keep, counts, status, st, 1 << 30, done, nullptr);
+        }
         stamps.record(3, st);
         return cuda_status();
     }

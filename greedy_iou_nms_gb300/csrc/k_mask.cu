@@ -33,9 +33,6 @@
 #ifndef GBNMS_MASK_UNROLL
 #define GBNMS_MASK_UNROLL 2
 #endif
-#ifndef GBNMS_MASK_MT
-#define GBNMS_MASK_MT 128
-#endif
 namespace gbnms {
 constexpr int kMaskUnroll = GBNMS_MASK_UNROLL;  // unroll of the inner loop (4 columns per step)
 }
@@ -44,6 +41,7 @@ namespace gbnms {
 
 constexpr int MT = GBNMS_MASK_MT;  // tile width (columns)
 constexpr int NQ = MT / 64;        // 64-bit words of a row per tile
+static_assert(MT == MASK_TILE_W, "the tile width the host stages by");
 static_assert(NQ == 1 || NQ == 2 || NQ == 4, "tile width of 64, 128 or 256 columns");
 constexpr int M_WARPS = GBNMS_MASK_WARPS;  // warps of 64 rows per tile
 constexpr int MR = M_WARPS * 64;  // tile height (rows)
@@ -221,14 +219,16 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
                 ThrParams p, uint64_t* __restrict__ mask, int64_t ldw,
                 unsigned long long* __restrict__ rowbits, int NB, ulonglong2* __restrict__ band,
                 uint32_t* __restrict__ edges, unsigned* __restrict__ ecount, unsigned ecap,
-                unsigned long long* __restrict__ haspred)
+                unsigned long long* __restrict__ haspred, int limit, long long tile_off,
+                const int* __restrict__ done)
 {
     __shared__ float4 cbox[MT];
     __shared__ __align__(16) float carea[MT];
 
-    const int n = m_dev ? *m_dev : m_bound;
+    if (done && *done) return;  // an earlier stage already reached max_out
+    const int n = min(m_dev ? *m_dev : m_bound, limit);
     int a, c;
-    tri_coords(blockIdx.x, a, c);
+    tri_coords(blockIdx.x + tile_off, a, c);
     const int T = (n + MT - 1) / MT;
     if (c >= T || a * MR >= n) return;  // beyond the device-side count
 
@@ -354,16 +354,21 @@ int64_t mask_tiles(int64_t n)
 void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const ThrParams& p,
                      uint64_t* mask, int64_t ldw, uint64_t* rowbits, int NB, uint64_t* band,
                      uint32_t* edges, unsigned* ecount, unsigned ecap, uint64_t* haspred,
-                     cudaStream_t st)
+                     cudaStream_t st, int col_lo, int col_hi, const int* done)
 {
-    int64_t tiles = mask_tiles(m_bound);
-    if (tiles == 0) return;
+    // The triangle's tiles whose columns lie in [col_lo, col_hi) (multiples of
+    // the tile width, or col_hi = m_bound), all rows above them.
+    const int hi = min(col_hi, m_bound);
+    const int64_t t0 = mask_tiles(col_lo), t1 = mask_tiles(hi);
+    const int64_t tiles = t1 - t0;
+    if (tiles <= 0) return;
     iou_mask_kernel<<<static_cast<unsigned>(tiles), M_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, p,
                                                                         mask, ldw,
                                                                         reinterpret_cast<unsigned long long*>(rowbits), NB,
                                                                         reinterpret_cast<ulonglong2*>(band),
                                                                         edges, ecount, ecap,
-                                                                        reinterpret_cast<unsigned long long*>(haspred));
+                                                                        reinterpret_cast<unsigned long long*>(haspred),
+                                                                        hi, t0, done);
 }
 
 }  // namespace gbnms

@@ -286,7 +286,8 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
 __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedges, unsigned E,
                               const uint32_t* __restrict__ haspred, int n, int NWp,
                               const int* __restrict__ perm, int max_out, int64_t* __restrict__ keep,
-                              int64_t* __restrict__ counts, int32_t* status, uint32_t* sm)
+                              int64_t* __restrict__ counts, int32_t* status, uint32_t* sm,
+                              int* done_out)
 {
     int* scratch = reinterpret_cast<int*>(sm);
     unsigned long long* bar = reinterpret_cast<unsigned long long*>(sm + 32);
@@ -424,7 +425,10 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
             base += __popc(bits[u]);
         }
     }
-    if (tid == 0) counts[0] = total < cap ? total : cap;
+    if (tid == 0) {
+        counts[0] = total < cap ? total : cap;
+        if (done_out && total >= cap) *done_out = 1;
+    }
     return true;
 }
 
@@ -436,16 +440,20 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
                       unsigned ecap, const uint32_t* __restrict__ haspred,
                       const int* __restrict__ m_dev, int m_bound, const int* __restrict__ perm,
                       int max_out, int64_t* __restrict__ keep, int64_t* __restrict__ counts,
-                      int32_t* status)
+                      int32_t* status, int limit, const int* __restrict__ done_in, int* done_out)
 {
     extern __shared__ __align__(128) uint64_t smem[];
     __shared__ ResolveShared S;
 
-    const int n = m_dev ? *m_dev : m_bound;
+    if (done_in && *done_in) return;  // an earlier stage already finished
+    const int n_all = m_dev ? *m_dev : m_bound;
+    const int n = min(n_all, limit);
+    if (done_out && threadIdx.x == 0) *done_out = n >= n_all;  // raised below on max_out
     if (edges) {
         const unsigned E = *ecount;
         if (E <= ecap && graph_resolve(edges, E, haspred, n, graph_words(m_bound), perm, max_out,
-                                       keep, counts, status, reinterpret_cast<uint32_t*>(smem)))
+                                       keep, counts, status, reinterpret_cast<uint32_t*>(smem),
+                                       done_out))
             return;
         __syncthreads();  // the walk reuses the shared memory
     }
@@ -683,7 +691,10 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
             if (t < nt) opre[t] = carry + x - c;
             carry += __shfl_sync(FULL, x, 31);
         }
-        if (l == 0) counts[0] = carry;
+        if (l == 0) {
+            counts[0] = carry;
+            if (done_out && max_out > 0 && carry >= max_out) *done_out = 1;
+        }
     }
     __syncthreads();
     for (int t = warp; t < nt; t += RV_WARPS) {
@@ -739,7 +750,7 @@ void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* ro
                            const uint64_t* band, const uint32_t* edges, const unsigned* ecount,
                            const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm,
                            int max_out, int64_t* keep, int64_t* counts, int32_t* status,
-                           cudaStream_t st)
+                           cudaStream_t st, int limit, const int* done_in, int* done_out)
 {
     size_t smem = resolve_smem_bytes(m_bound, NB);
     const unsigned ecap = edges ? graph_edge_cap(m_bound) : 0u;
@@ -748,7 +759,7 @@ void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* ro
     resolve_single_kernel<<<1, RV_THREADS, smem, st>>>(mask, ldw, rowbits, NB, band, edges, ecount,
                                                        ecap, reinterpret_cast<const uint32_t*>(haspred),
                                                        m_dev, m_bound, perm, max_out, keep, counts,
-                                                       status);
+                                                       status, limit, done_in, done_out);
 }
 
 }  // namespace gbnms

@@ -174,7 +174,10 @@ nms_status nms_resolve_mask(const uint64_t* mask, int64_t n, const int32_t* perm
  * enabled) that it records on `stream`: events[0] before its first kernel and
  * events[k] when stage k has been enqueued.
  *   One image:  1 = pre-filter, sort and gather; 2 = IoU mask (with the pair
- *               list); 3 = resolve and output.
+ *               list; with max_out, of the leading 2*max_out boxes); 3 =
+ *               resolve and output (with max_out, also the rest of the mask
+ *               and a second resolve when the leading boxes held fewer than
+ *               max_out kept boxes).
  *   Batched:    1 = pre-filter and bucketing into (image, class) segments;
  *               2 = per-segment NMS; 3 = per-image merge and output.
  * NULL entries and entries past nevents are skipped (nevents may be 0).  The

@@ -357,3 +357,35 @@ def test_dependency_chains_of_many_links(n_chains, length):
         _check_single(b, s, thr)
     _check_single(b, s, 0.5, max_out=len(s) // 3)
     _check_single(b, s, 0.5, score_thr=0.25)
+
+
+def test_pairs_concentrated_on_few_targets():
+    """Many pairs ending in a narrow range of sorted positions (400 identical
+    low-score boxes under 7792 scattered ones, ~80k pairs): more than one
+    share of the graph path holds, so the walk decides instead."""
+    rng = np.random.default_rng(5)
+    g_side = 89
+    gx, gy = np.meshgrid(np.arange(g_side), np.arange(g_side))
+    cx = (gx.ravel()[:7792] * 50.0).astype(np.float32)
+    cy = (gy.ravel()[:7792] * 50.0).astype(np.float32)
+    sparse = np.stack([cx, cy, cx + 10, cy + 10], 1)
+    dup = np.tile(np.array([[10000.0, 10000.0, 10020.0, 10020.0]], np.float32), (400, 1))
+    b = np.concatenate([sparse, dup]).astype(np.float32)
+    s = np.concatenate([rng.uniform(0.5, 1.0, 7792), rng.uniform(0.0, 0.5, 400)]).astype(np.float32)
+    p = rng.permutation(len(s))
+    _check_single(b[p], s[p], 0.5)
+
+
+@pytest.mark.parametrize("max_out,score_thr", [(100, None), (40, 0.3), (1, None), (3000, None)])
+def test_max_out_needs_the_rest_of_the_mask(max_out, score_thr):
+    """Heavy suppression (tight clusters): the leading 2*max_out boxes hold
+    fewer than max_out kept boxes, so the rest of the mask and a second
+    resolve are needed; small max_out values stop in the first part."""
+    rng = np.random.default_rng(11)
+    n = 6000
+    centres = rng.uniform(0, 3000, (120, 2))
+    c = centres[rng.integers(0, 120, n)] + rng.normal(0, 2, (n, 2))
+    wh = rng.uniform(20, 40, (n, 2))
+    b = np.concatenate([c - wh / 2, c + wh / 2], 1).astype(np.float32)
+    s = rng.uniform(0, 1, n).astype(np.float32)
+    _check_single(b, s, 0.5, max_out=max_out, score_thr=score_thr)

@@ -233,6 +233,90 @@ def nms(boxes, scores, iou_thr: float, *, class_ids=None, num_classes: Optional[
     return (out, counts) if return_counts else out
 
 
+class HostPipeline:
+    """Greedy NMS of one image held in host memory, replayed as one CUDA graph
+    per call: a host->device copy of the input, the nms_run kernels and a
+    device->host copy of the result.
+
+    The input is one pinned buffer: n boxes (xyxy fp32) followed by n scores;
+    write them through ``boxes`` / ``scores`` (numpy views of the first n
+    entries, see ``set_n``) or ``load``.  ``run`` replays the graph captured
+    for (n, iou_thr, score_thr, max_out) (capturing it on first use, after one
+    plain call that also warms the library up), waits for it and returns the
+    kept indices: a numpy view of the pinned output buffer (the count, then
+    the indices), valid until the next call.
+    """
+
+    def __init__(self, n_max: int, device="cuda"):
+        torch = _torch()
+        self.n_max = int(n_max)
+        self.device = torch.device(device)
+        self._h_in = torch.empty(max(5 * self.n_max, 4), dtype=torch.float32).pin_memory()
+        self._d_in = torch.empty(max(5 * self.n_max, 4), dtype=torch.float32, device=self.device)
+        self._h_out = torch.empty(self.n_max + 1, dtype=torch.int64).pin_memory()
+        self._d_out = torch.empty(self.n_max + 1, dtype=torch.int64, device=self.device)
+        self._status = torch.empty(1, dtype=torch.int32, device=self.device)
+        self._out_np = self._h_out.numpy()
+        self.workspace = Workspace(self.n_max, device=self.device)
+        self._graphs = {}
+        self.set_n(self.n_max)
+
+    def set_n(self, n: int) -> None:
+        """Use the first n boxes: boxes is [n,4] at the start of the input
+        buffer, scores [n] right after them (16n bytes in: 16-byte aligned)."""
+        if not 0 <= n <= self.n_max:
+            raise ValueError("HostPipeline: n out of range")
+        self.n = int(n)
+        flat = self._h_in.numpy()
+        self.boxes = flat[: 4 * self.n].reshape(self.n, 4)
+        self.scores = flat[4 * self.n: 5 * self.n]
+
+    def load(self, boxes, scores) -> None:
+        import numpy as np
+        n = len(scores)
+        self.set_n(n)
+        self.boxes[...] = np.asarray(boxes, dtype=np.float32).reshape(n, 4)
+        self.scores[...] = np.asarray(scores, dtype=np.float32)
+
+    @property
+    def in_bytes(self) -> int:
+        return 20 * self.n
+
+    def out_bytes(self, max_out: int = 0) -> int:
+        return 8 * (1 + keep_capacity(self.n, None, max_out))
+
+    def _enqueue(self, n, iou_thr, score_thr, max_out, stream):
+        cap = keep_capacity(n, None, max_out)
+        self._d_in[: 5 * n].copy_(self._h_in[: 5 * n], non_blocking=True)
+        base_in = self._d_in.data_ptr()
+        base_out = self._d_out.data_ptr()
+        st = nms_run(base_in if n else 0, base_in + 16 * n if n else 0, n, 0, 0, 0, 0, iou_thr,
+                     -math.inf if score_thr is None else score_thr, max_out, base_out + 8,
+                     max(cap, 1), base_out, self._status.data_ptr(), self.workspace.ptr,
+                     self.workspace.bytes, stream.cuda_stream)
+        if st != NMS_OK:
+            raise NmsError(st, "nms_run")
+        self._h_out[: cap + 1].copy_(self._d_out[: cap + 1], non_blocking=True)
+
+    def run(self, iou_thr: float, score_thr: Optional[float] = None, max_out: int = 0):
+        torch = _torch()
+        key = (self.n, float(iou_thr), score_thr, int(max_out))
+        graph = self._graphs.get(key)
+        if graph is None:
+            stream = torch.cuda.current_stream(self.device)
+            self._enqueue(self.n, iou_thr, score_thr, max_out, stream)  # checks and warms up
+            stream.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                self._enqueue(self.n, iou_thr, score_thr, max_out,
+                              torch.cuda.current_stream(self.device))
+            self._graphs[key] = graph
+        graph.replay()
+        torch.cuda.current_stream(self.device).synchronize()
+        out = self._out_np
+        return out[1: 1 + int(out[0])]
+
+
 def iou_mask(boxes_sorted, iou_thr: float):
     """Suppression bitmask of score-sorted boxes: int64 tensor [n, nms_mask_row_words(n)]
     holding the uint64 words (bit j%64 of word j//64 of row i: j > i and IoU > thr).

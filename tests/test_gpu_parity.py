@@ -389,3 +389,18 @@ def test_max_out_needs_the_rest_of_the_mask(max_out, score_thr):
     b = np.concatenate([c - wh / 2, c + wh / 2], 1).astype(np.float32)
     s = rng.uniform(0, 1, n).astype(np.float32)
     _check_single(b, s, 0.5, max_out=max_out, score_thr=score_thr)
+
+
+def test_host_pipeline_matches_oracle():
+    """HostPipeline: one packed host->device copy in, one device->host copy
+    out; the kept indices equal the oracle's, for several sizes in one
+    pipeline (the tail of the buffers is reused)."""
+    pipe = g.HostPipeline(9000)
+    for name, seed in (("single_n8192", 0), ("single_n1000_ties", 2)):
+        wl = W.make(name, seed)
+        pipe.load(wl.boxes, wl.scores)
+        got = pipe.run(wl.iou_thr, wl.score_thr, wl.max_out)
+        exp = oracle.nms_single(wl.boxes, wl.scores, wl.iou_thr, max_out=wl.max_out)
+        assert got.tolist() == exp.tolist()
+    pipe.set_n(0)
+    assert len(pipe.run(0.5)) == 0

@@ -49,9 +49,11 @@ struct Layout {
 struct SingleLayout {
     int64_t ldw = 0;
     int NB = 0;  // 64-bit words of the per-row chunk bitmap
-    unsigned ecap = 0;  // pairs of the sparse list (0: no list, the walk resolves)
-    size_t status, m_count, ecount, done, cand, perm, boxes_s, keys, rowbits, band, edges, haspred,
-        mask, total;
+    unsigned ecap = 0;   // pairs one CTA's graph path holds (0: no list, the walk resolves)
+    unsigned lcap = 0;   // pairs the list holds (more when the all-SM graph path exists)
+    bool grid = false;   // the all-SM graph path exists at this size
+    size_t status, m_count, ecount, done, cand, perm, boxes_s, keys, rowbits, band, edges, haspred, gstate,
+        gctl, mask, total;
 };
 
 SingleLayout single_layout(int64_t n)
@@ -62,6 +64,9 @@ SingleLayout single_layout(int64_t n)
     s.NB = static_cast<int>((T + 63) / 64 > 0 ? (T + 63) / 64 : 1);
     Layout L;
     s.ecap = graph_edge_cap(static_cast<int>(n));
+    const unsigned gcap = graph_grid_cap(static_cast<int>(n));
+    s.grid = gcap > s.ecap;
+    s.lcap = s.grid ? gcap : s.ecap;
     s.status = L.add(4);
     s.m_count = L.add(4);
     s.ecount = L.add(4);
@@ -72,8 +77,10 @@ SingleLayout single_layout(int64_t n)
     s.keys = L.add(sort_keys_bytes(static_cast<int>(n)));
     s.rowbits = L.add(8 * static_cast<size_t>(n) * static_cast<size_t>(s.NB));
     s.band = L.add(8 * static_cast<size_t>((n + 63) / 64) * (BAND_L + 1) * 64);
-    s.edges = L.add(4 * static_cast<size_t>(s.ecap));
+    s.edges = L.add(4 * static_cast<size_t>(s.lcap));
     s.haspred = L.add(s.ecap ? 8 * static_cast<size_t>((n + 63) / 64) : 0);
+    s.gstate = L.add(s.grid ? graph_grid_state_bytes(static_cast<int>(n)) : 0);
+    s.gctl = L.add(s.grid ? graph_grid_ctl_bytes() : 0);
     s.mask = L.add(8 * static_cast<size_t>(n) * static_cast<size_t>(s.ldw));
     s.total = L.total;
     return s;
@@ -239,8 +246,11 @@ nms_status run_impl(const float* boxes, const float* scores, int64_t n, const in
         unsigned* ecount = at<unsigned>(workspace, L.ecount);
         uint64_t* haspred = L.ecap ? at<uint64_t>(workspace, L.haspred) : nullptr;
         uint64_t* keys = sort_keys_bytes(static_cast<int>(n)) ? at<uint64_t>(workspace, L.keys) : nullptr;
+        // The all-SM path's control block: its first 8 ints (barrier count,
+        // round flags, per-stage "resolved" flags at 4..7) are zeroed by the sort.
+        int* gctl = L.grid ? at<int>(workspace, L.gctl) : nullptr;
         launch_sort(scores, reinterpret_cast<const float4*>(boxes), cand, m_count, static_cast<int>(n),
-                    perm, boxes_s, keys, status, rowbits, L.NB, ecount, haspred, st);
+                    perm, boxes_s, keys, status, rowbits, L.NB, ecount, haspred, gctl, st);
         stamps.record(1, st);
         uint64_t* band = at<uint64_t>(workspace, L.band);
         const int nb = static_cast<int>(n);
@@ -251,24 +261,34 @@ nms_status run_impl(const float* boxes, const float* scores, int64_t n, const in
         const int64_t k1 = max_out > 0 ? (2 * static_cast<int64_t>(max_out) + MASK_TILE_W - 1) /
                                              MASK_TILE_W * MASK_TILE_W
                                        : n;
+        uint64_t* gstate = L.grid ? at<uint64_t>(workspace, L.gstate) : nullptr;
+        // Resolve of one stage: with a list too long for one CTA, the all-SM
+        // graph path first; one CTA's graph path or the walk otherwise.
+        auto resolve = [&](int limit, const int* done_in, int* done_out, int stage) {
+            const int* gd = nullptr;
+            if (L.grid && limit > graph_grid_min_n()) {
+                launch_graph_grid(edges, ecount, haspred, m_count, nb, perm, max_out, keep, counts, status, st,
+                                  limit, done_in, done_out, gctl + 4 + stage, gstate, gctl);
+                gd = gctl + 4 + stage;
+            }
+            launch_resolve_single(mask, L.ldw, rowbits, L.NB, band, edges, ecount, haspred, m_count, nb, perm,
+                                  max_out, keep, counts, status, st, limit, done_in, done_out, gd);
+        };
         if (k1 >= n) {
             launch_iou_mask(boxes_s, m_count, nb, p, mask, L.ldw, rowbits, L.NB, band, edges, ecount,
-                            L.ecap, haspred, st);
+                            L.lcap, haspred, st);
             stamps.record(2, st);
-            launch_resolve_single(mask, L.ldw, rowbits, L.NB, band, edges, ecount, haspred, m_count, nb,
-                                  perm, max_out, keep, counts, status, st);
+            resolve(1 << 30, nullptr, nullptr, 0);
         } else {
             int* done = at<int>(workspace, L.done);
             const int k = static_cast<int>(k1);
             launch_iou_mask(boxes_s, m_count, nb, p, mask, L.ldw, rowbits, L.NB, band, edges, ecount,
-                            L.ecap, haspred, st, 0, k);
+                            L.lcap, haspred, st, 0, k);
             stamps.record(2, st);
-            launch_resolve_single(mask, L.ldw, rowbits, L.NB, band, edges, ecount, haspred, m_count, nb,
-                                  perm, max_out, keep, counts, status, st, k, nullptr, done);
+            resolve(k, nullptr, done, 0);
             launch_iou_mask(boxes_s, m_count, nb, p, mask, L.ldw, rowbits, L.NB, band, edges, ecount,
-                            L.ecap, haspred, st, k, nb, done);
-            launch_resolve_single(mask, L.ldw, rowbits, L.NB, band, edges, ecount, haspred, m_count, nb,
-                                  perm, max_out, keep, counts, status, st, 1 << 30, done, nullptr);
+                            L.lcap, haspred, st, k, nb, done);
+            resolve(1 << 30, done, nullptr, 1);
         }
         stamps.record(3, st);
         return cuda_status();

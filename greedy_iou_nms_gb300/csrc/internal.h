@@ -29,7 +29,7 @@ void launch_prefilter(const float* scores, int n, float score_thr, int* cand, in
 size_t sort_keys_bytes(int m_bound);
 void launch_sort(const float* scores, const float4* boxes, const int* cand, const int* m_dev,
                  int m_bound, int* perm, float4* boxes_s, uint64_t* keys, int32_t* status,
-                 uint64_t* rowbits, int NB, unsigned* ecount, uint64_t* haspred, cudaStream_t st);
+                 uint64_t* rowbits, int NB, unsigned* ecount, uint64_t* haspred, int* zero8, cudaStream_t st);
 int64_t mask_tiles(int64_t n);
 // Tile width of the mask kernel (columns); stages of the max_out early exit
 // start on a multiple of it.
@@ -55,7 +55,25 @@ void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* ro
                            const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm,
                            int max_out, int64_t* keep, int64_t* counts, int32_t* status,
                            cudaStream_t st, int limit = 1 << 30, const int* done_in = nullptr,
-                           int* done_out = nullptr);
+                           int* done_out = nullptr, const int* grid_done = nullptr);
+
+// Pair-list capacity of the all-SM graph path (0 below its size range) and
+// its scratch: graph_grid_state_bytes of bitmaps and a control block.
+unsigned graph_grid_cap(int m_bound);
+size_t graph_grid_ctl_bytes();
+int graph_grid_min_n();  // stages of at most this many boxes never take the all-SM path
+// The control block starts with 8 ints that must be zero on entry (barrier
+// count, round flags, per-stage "resolved" flags at ints 4..7).
+inline size_t graph_grid_state_bytes(int m_bound) { return 16 * static_cast<size_t>(((m_bound + 31) / 32 + 3) & ~3); }
+// Resolves boxes [0, min(n, limit)) over a pair list too long for one CTA
+// (more than graph_edge_cap pairs, at most graph_grid_cap); on success sets
+// *grid_done (and *done_out as launch_resolve_single would); otherwise leaves
+// them for the walk.  The control block's barrier count and flags must be
+// zero on entry.
+void launch_graph_grid(uint32_t* edges, const unsigned* ecount, const uint64_t* haspred, const int* m_dev,
+                       int m_bound, const int* perm, int max_out, int64_t* keep, int64_t* counts,
+                       int32_t* status, cudaStream_t st, int limit, const int* done_in, int* done_out,
+                       int* grid_done, uint64_t* state, void* ctl);
 
 struct BatchedArgs {
     const float4* boxes;

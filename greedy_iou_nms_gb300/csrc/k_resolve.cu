@@ -53,6 +53,7 @@
 // stay idle.  Kept sets go to shared memory; the output list is written by
 // the whole CTA after the walk.
 #include <climits>
+#include <cstddef>
 
 #include "common.cuh"
 #include "internal.h"
@@ -241,6 +242,20 @@ constexpr int GR_COPY = 32 * 1024;    // bytes per bulk copy of the pair list
 // 32-bit bitmap words for m_bound boxes, rounded up to a multiple of 4 so the
 // pair list that follows starts 16-byte aligned.
 __host__ __device__ __forceinline__ int graph_words(int m_bound) { return ((m_bound + 31) / 32 + 3) & ~3; }
+
+// Above GR_GRID_MIN_N boxes a list larger than one CTA's shared memory is
+// resolved by graph_grid_kernel (all SMs, the list in global memory), up to
+// GR_GRID_MAX_PAIRS pairs.
+constexpr int GR_GRID_MIN_N = 16384;
+constexpr unsigned GR_GRID_MAX_PAIRS = 1u << 24;
+constexpr int GG_THREADS = 1024;
+
+unsigned graph_grid_cap(int m_bound)
+{
+    if (m_bound <= GR_GRID_MIN_N || m_bound > GR_MAX_N) return 0;
+    const unsigned long long all = static_cast<unsigned long long>(m_bound) * (m_bound - 1) / 2;
+    return static_cast<unsigned>(all < GR_GRID_MAX_PAIRS ? ((all + 3) & ~3ull) : GR_GRID_MAX_PAIRS);
+}
 
 unsigned graph_edge_cap(int m_bound)
 {
@@ -440,12 +455,14 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
                       unsigned ecap, const uint32_t* __restrict__ haspred,
                       const int* __restrict__ m_dev, int m_bound, const int* __restrict__ perm,
                       int max_out, int64_t* __restrict__ keep, int64_t* __restrict__ counts,
-                      int32_t* status, int limit, const int* __restrict__ done_in, int* done_out)
+                      int32_t* status, int limit, const int* __restrict__ done_in, int* done_out,
+                      const int* __restrict__ grid_done)
 {
     extern __shared__ __align__(128) uint64_t smem[];
     __shared__ ResolveShared S;
 
-    if (done_in && *done_in) return;  // an earlier stage already finished
+    if (done_in && *done_in) return;      // an earlier stage already finished
+    if (grid_done && *grid_done) return;  // graph_grid_kernel resolved this stage
     const int n_all = m_dev ? *m_dev : m_bound;
     const int n = min(n_all, limit);
     if (done_out && threadIdx.x == 0) *done_out = n >= n_all;  // raised below on max_out
@@ -711,6 +728,229 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
     }
 }
 
+
+// ------------------------------------------------------- graph path, all SMs
+// The rounds of graph_resolve over a pair list too long for one CTA's shared
+// memory, by one CTA per SM (a cooperative launch: all CTAs are resident, so
+// a barrier over the grid is safe).  The (kept, removed) and (hit, blocked)
+// bitmaps live in global memory; CTA b owns a range of their words and a
+// contiguous slice of the list, which its threads compact in place.  A round:
+// the owners update their words; grid barrier; every CTA copies the (kept,
+// removed) bitmap into shared memory, passes over its live pairs marking hit
+// and blocked targets in shared memory, and ORs its non-zero mark words into
+// the global bitmaps; grid barrier.  Cross-CTA data is read through L2
+// (__ldcg), and the barrier orders it with fences.  Returns without output
+// (the walk then runs) when the rounds outnumber the walk's tiles plus 16.
+struct GridCtl {
+    unsigned count, gen;  // barrier arrivals, generation
+    int more[2];          // "some box still open", by round parity
+    int resolved[4];      // per stage: this path decided it (the walk then returns)
+    int cnt[1024];        // kept boxes per CTA
+};
+static_assert(offsetof(GridCtl, resolved) == 16, "stage flags at ints 4..7 of the control block");
+
+__device__ __forceinline__ bool grid_barrier(GridCtl* ctl, unsigned nblocks, int* ok_s)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        volatile unsigned* vgen = &ctl->gen;
+        const unsigned g = *vgen;
+        __threadfence();
+        bool ok = true;
+        if (atomicAdd(&ctl->count, 1u) == nblocks - 1) {
+            atomicExch(&ctl->count, 0u);
+            __threadfence();
+            atomicAdd(&ctl->gen, 1u);
+        } else {
+            long long tries = 0;
+            while (*vgen == g) {
+                if (++tries > RV_WAIT_LIMIT) { ok = false; break; }
+                __nanosleep(32);
+            }
+        }
+        __threadfence();
+        *ok_s = ok;
+    }
+    __syncthreads();
+    return *ok_s != 0;
+}
+
+__global__ void __launch_bounds__(GG_THREADS, 1)
+graph_grid_kernel(uint32_t* __restrict__ edges, const unsigned* __restrict__ ecount, unsigned ecap_smem,
+                  unsigned ecap_list, const uint32_t* __restrict__ haspred, const int* __restrict__ m_dev,
+                  int m_bound, int limit, const int* __restrict__ perm, int max_out,
+                  int64_t* __restrict__ keep, int64_t* __restrict__ counts, int32_t* status,
+                  const int* __restrict__ done_in, int* done_out, int* grid_done, uint2* KRg, uint2* HBg,
+                  GridCtl* ctl)
+{
+    extern __shared__ __align__(16) uint2 gsm[];  // (kept, removed) copy, then local (hit, blocked)
+    __shared__ int ok_s;
+    __shared__ int scratch[32];
+    if (done_in && *done_in) return;
+    const unsigned E = *ecount;
+    if (E <= ecap_smem || E > ecap_list) return;  // one CTA's path, or the walk
+    const int n_all = m_dev ? *m_dev : m_bound;
+    const int n = min(n_all, limit);
+    const int NW = (n + 31) / 32;
+    uint2* KRs = gsm;
+    uint2* HBs = gsm + NW;
+    const unsigned nb = gridDim.x, b = blockIdx.x;
+    const int tid = threadIdx.x;
+    const unsigned l = lane_id();
+    const int warp = tid >> 5;
+    const int wpb = (NW + static_cast<int>(nb) - 1) / static_cast<int>(nb);
+    const int w0 = min(static_cast<int>(b) * wpb, NW), w1 = min(w0 + wpb, NW);
+    const unsigned epb = (E + nb - 1) / nb;
+    const unsigned e0 = min(b * epb, E), e1 = min(e0 + epb, E);
+    int live = e1 > e0 + tid ? static_cast<int>((e1 - e0 - tid + GG_THREADS - 1) / GG_THREADS) : 0;
+
+    for (int w = w0 + tid; w < w1; w += GG_THREADS) {
+        KRg[w] = make_uint2(0u, 0u);
+        HBg[w] = make_uint2(0u, haspred[w]);  // before the first round every target is blocked
+    }
+    if (!grid_barrier(ctl, nb, &ok_s)) goto fail;
+    {
+        const int max_rounds = (n + 63) / 64 + 16;
+        for (int round = 0;; ++round) {
+            bool more = false;
+            for (int w = w0 + tid; w < w1; w += GG_THREADS) {
+                const uint2 kr = __ldcg(KRg + w);
+                const uint32_t valid = (w == NW - 1 && (n & 31)) ? (1u << (n & 31)) - 1u : ~0u;
+                const uint32_t open = ~(kr.x | kr.y) & valid;
+                if (open) {
+                    const uint2 hb = __ldcg(HBg + w);
+                    KRg[w] = make_uint2(kr.x | (open & ~hb.x & ~hb.y), kr.y | (open & hb.x));
+                    HBg[w] = make_uint2(0u, 0u);
+                    more |= (open & ~hb.x & hb.y) != 0;
+                }
+            }
+            if (__syncthreads_or(more) && tid == 0) atomicOr(&ctl->more[round & 1], 1);
+            if (!grid_barrier(ctl, nb, &ok_s)) goto fail;
+            if (!__ldcg(&ctl->more[round & 1])) break;
+            if (round == max_rounds) return;  // no output: the walk decides
+            if (b == 0 && tid == 0) ctl->more[(round + 1) & 1] = 0;
+            for (int w = tid; w < NW; w += GG_THREADS) {
+                KRs[w] = __ldcg(KRg + w);
+                HBs[w] = make_uint2(0u, 0u);
+            }
+            __syncthreads();
+            int nl = 0;
+            for (int k0 = 0; k0 < live; k0 += 4) {
+                uint32_t e[4];
+                uint2 ki[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    e[u] = k0 + u < live ? edges[e0 + tid + GG_THREADS * (k0 + u)] : 0xffffffffu;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (e[u] != 0xffffffffu) ki[u] = KRs[e[u] >> 21];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (e[u] == 0xffffffffu) continue;
+                    const uint32_t j = e[u] & 0xffffu;
+                    const uint32_t bi = 1u << ((e[u] >> 16) & 31);
+                    if (ki[u].x & bi) {
+                        atomicOr(&HBs[j >> 5].x, 1u << (j & 31));
+                    } else if (!(ki[u].y & bi)) {
+                        atomicOr(&HBs[j >> 5].y, 1u << (j & 31));
+                        edges[e0 + tid + GG_THREADS * nl++] = e[u];
+                    }
+                }
+            }
+            live = nl;
+            __syncthreads();
+            for (int w = tid; w < NW; w += GG_THREADS) {
+                const uint2 hb = HBs[w];
+                if (hb.x) atomicOr(&HBg[w].x, hb.x);
+                if (hb.y) atomicOr(&HBg[w].y, hb.y);
+            }
+            if (!grid_barrier(ctl, nb, &ok_s)) goto fail;
+        }
+        // Output of the owned words in score order: kept counts per CTA, a
+        // prefix over the CTAs, then lane l of a warp writes box 32w+l.
+        const int nown = w1 - w0;
+        const int wpw = (nown + 31) / 32;
+        const int a0 = min(w0 + warp * wpw, w1), a1 = min(a0 + wpw, w1);
+        int c = 0;
+        for (int w = a0 + static_cast<int>(l); w < a1; w += 32) c += __popc(__ldcg(&KRg[w].x));
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) c += __shfl_xor_sync(FULL, c, d);
+        if (l == 0) scratch[warp] = c;
+        __syncthreads();
+        if (warp == 0) {
+            int v = scratch[l];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(FULL, v, d);
+                if (static_cast<int>(l) >= d) v += y;
+            }
+            scratch[l] = v;
+            if (l == 31) ctl->cnt[b] = v;
+        }
+        if (!grid_barrier(ctl, nb, &ok_s)) goto fail;
+        int total = 0, cbase = 0;
+        for (unsigned q = 0; q < nb; ++q) {
+            const int v = __ldcg(&ctl->cnt[q]);
+            if (q < b) cbase += v;
+            total += v;
+        }
+        const int cap = max_out > 0 ? max_out : INT_MAX;
+        int base = cbase + (warp ? scratch[warp - 1] : 0);
+        const uint32_t below = (1u << l) - 1u;
+        for (int w = a0; w < a1 && base < cap; ++w) {
+            const uint32_t bits = __ldcg(&KRg[w].x);
+            if ((bits >> l) & 1u) {
+                const int pos = base + __popc(bits & below);
+                const int j = 32 * w + static_cast<int>(l);
+                if (pos < cap) keep[pos] = perm ? perm[j] : j;
+            }
+            base += __popc(bits);
+        }
+        if (b == 0 && tid == 0) {
+            counts[0] = total < cap ? total : cap;
+            if (done_out) *done_out = (n >= n_all) || (max_out > 0 && total >= max_out);
+            *grid_done = 1;
+        }
+        return;
+    }
+fail:
+    if (tid == 0 && status) set_status(status, NMS_ERR_TIMEOUT);
+}
+
+size_t graph_grid_smem(int m_bound) { return 2 * sizeof(uint2) * static_cast<size_t>(graph_words(m_bound)); }
+size_t graph_grid_ctl_bytes() { return sizeof(GridCtl); }
+int graph_grid_min_n() { return GR_GRID_MIN_N; }
+
+void launch_graph_grid(uint32_t* edges, const unsigned* ecount, const uint64_t* haspred, const int* m_dev,
+                       int m_bound, const int* perm, int max_out, int64_t* keep, int64_t* counts,
+                       int32_t* status, cudaStream_t st, int limit, const int* done_in, int* done_out,
+                       int* grid_done, uint64_t* state, void* ctl)
+{
+    const unsigned ecap_list = graph_grid_cap(m_bound);
+    if (!ecap_list) return;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) return;
+    const size_t smem = graph_grid_smem(m_bound);
+    ensure_dynamic_smem(reinterpret_cast<const void*>(graph_grid_kernel), smem);
+    uint2* KRg = reinterpret_cast<uint2*>(state);
+    uint2* HBg = KRg + graph_words(m_bound);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(sms < 1024 ? sms : 1024));
+    cfg.blockDim = dim3(GG_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, graph_grid_kernel, edges, ecount, graph_edge_cap(m_bound), ecap_list,
+                       reinterpret_cast<const uint32_t*>(haspred), m_dev, m_bound, limit, perm, max_out, keep,
+                       counts, status, done_in, done_out, grid_done, KRg, HBg, static_cast<GridCtl*>(ctl));
+}
+
 size_t resolve_smem_bytes(int m_bound, int NB) { return resolve_layout(m_bound, NB).total; }
 
 // Column view of the band blocks of a row-major mask: one warp per (column
@@ -750,7 +990,8 @@ void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* ro
                            const uint64_t* band, const uint32_t* edges, const unsigned* ecount,
                            const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm,
                            int max_out, int64_t* keep, int64_t* counts, int32_t* status,
-                           cudaStream_t st, int limit, const int* done_in, int* done_out)
+                           cudaStream_t st, int limit, const int* done_in, int* done_out,
+                           const int* grid_done)
 {
     size_t smem = resolve_smem_bytes(m_bound, NB);
     const unsigned ecap = edges ? graph_edge_cap(m_bound) : 0u;
@@ -759,7 +1000,7 @@ void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* ro
     resolve_single_kernel<<<1, RV_THREADS, smem, st>>>(mask, ldw, rowbits, NB, band, edges, ecount,
                                                        ecap, reinterpret_cast<const uint32_t*>(haspred),
                                                        m_dev, m_bound, perm, max_out, keep, counts,
-                                                       status, limit, done_in, done_out);
+                                                       status, limit, done_in, done_out, grid_done);
 }
 
 }  // namespace gbnms

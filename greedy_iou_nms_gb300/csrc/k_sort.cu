@@ -128,7 +128,7 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
                    const int* __restrict__ cand, const int* __restrict__ m_dev, int m_bound,
                    uint64_t* __restrict__ keys_out, int* __restrict__ perm, float4* __restrict__ boxes_s,
                    int32_t* status, uint64_t* __restrict__ rowbits, int NB, unsigned* __restrict__ ecount,
-                   uint64_t* __restrict__ haspred)
+                   uint64_t* __restrict__ haspred, int* __restrict__ zero8)
 {
     extern __shared__ __align__(16) uint64_t list[];                 // MS_CHUNK keys, bucket order
     int* start = reinterpret_cast<int*>(list + MS_CHUNK);            // [BR_BUCKETS + 1]
@@ -140,9 +140,12 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
     const int tid = threadIdx.x;
     const int c0 = blockIdx.y * MS_CHUNK;
     const int q0 = c0 + blockIdx.x * BR_CAND;  // this CTA's candidates [q0, q0 + BR_CAND)
-    if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) {
-        if (status) *status = 0;
-        if (ecount) *ecount = 0;
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+        if (tid == 0) {
+            if (status) *status = 0;
+            if (ecount) *ecount = 0;
+        }
+        if (zero8 && tid < 8) zero8[tid] = 0;  // the resolve's flags and barrier counter
     }
     const int r1 = min(q0 + BR_CAND, m_bound);
     if (haspred && (q0 & 63) == 0)
@@ -351,7 +354,7 @@ size_t sort_keys_bytes(int m_bound)
 
 void launch_sort(const float* scores, const float4* boxes, const int* cand, const int* m_dev,
                  int m_bound, int* perm, float4* boxes_s, uint64_t* keys, int32_t* status,
-                 uint64_t* rowbits, int NB, unsigned* ecount, uint64_t* haspred, cudaStream_t st)
+                 uint64_t* rowbits, int NB, unsigned* ecount, uint64_t* haspred, int* zero8, cudaStream_t st)
 {
     const int chunks = sort_chunks(m_bound);
     const int per_chunk = chunks > 1 ? MS_CHUNK / BR_CAND : (m_bound + BR_CAND - 1) / BR_CAND;
@@ -361,7 +364,7 @@ void launch_sort(const float* scores, const float4* boxes, const int* cand, cons
     uint64_t* k0 = keys;
     uint64_t* k1 = keys ? keys + half : nullptr;
     bucket_rank_kernel<<<dim3(per_chunk > 0 ? per_chunk : 1, chunks), BR_THREADS, rank_smem, st>>>(
-        scores, boxes, cand, m_dev, m_bound, k0, perm, boxes_s, status, rowbits, NB, ecount, haspred);
+        scores, boxes, cand, m_dev, m_bound, k0, perm, boxes_s, status, rowbits, NB, ecount, haspred, zero8);
     if (chunks == 1) return;
     const size_t smem = sizeof(uint64_t) * MS_SLOTS;
     ensure_dynamic_smem(reinterpret_cast<const void*>(merge_level_kernel), smem);

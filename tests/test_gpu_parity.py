@@ -404,3 +404,17 @@ def test_host_pipeline_matches_oracle():
         assert got.tolist() == exp.tolist()
     pipe.set_n(0)
     assert len(pipe.run(0.5)) == 0
+
+
+@pytest.mark.parametrize("max_out", [0, 150])
+def test_pair_list_beyond_one_cta(max_out):
+    """20000 boxes in tight clusters (~10^6 pairs over the threshold): more
+    pairs than one CTA's shared memory holds, so all SMs take the rounds."""
+    rng = np.random.default_rng(21)
+    n = 20000
+    centres = rng.uniform(0, 6000, (200, 2))
+    c = centres[rng.integers(0, 200, n)] + rng.normal(0, 1.5, (n, 2))
+    wh = rng.uniform(20, 30, (n, 2))
+    b = np.concatenate([c - wh / 2, c + wh / 2], 1).astype(np.float32)
+    s = rng.uniform(0, 1, n).astype(np.float32)
+    _check_single(b, s, 0.5, max_out=max_out)

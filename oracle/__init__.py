@@ -52,6 +52,8 @@ def _load():
                                    ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_int32,
                                    i64p, i64p]
         lib.oracle_nms.restype = ctypes.c_int64
+        lib.oracle_fast_nms.argtypes = lib.oracle_nms.argtypes
+        lib.oracle_fast_nms.restype = ctypes.c_int64
         lib.oracle_score_order.argtypes = [f32p, i64p, ctypes.c_int64]
         lib.oracle_score_order.restype = None
         lib.oracle_mask.argtypes = [f32p, ctypes.c_int64, ctypes.c_float, u64p]
@@ -80,11 +82,11 @@ def score_order(scores) -> np.ndarray:
 
 
 def nms(boxes, scores, iou_thr, *, class_ids=None, batch_offsets=None, score_thr=None,
-        max_out=0):
-    """Greedy NMS.  Returns (keep, counts) exactly as the library lays them out:
-    image b's kept indices sit at keep[b*max_out] (max_out > 0) or at
-    keep[batch_offsets[b]] (no cap); counts[b] is their number.  For a single
-    image, keep[:counts[0]] is the answer."""
+        max_out=0, fast=False):
+    """Greedy NMS (Fast NMS with fast=True).  Returns (keep, counts) exactly as
+    the library lays them out: image b's kept indices sit at keep[b*max_out]
+    (max_out > 0) or at keep[batch_offsets[b]] (no cap); counts[b] is their
+    number.  For a single image, keep[:counts[0]] is the answer."""
     bx = np.ascontiguousarray(boxes, dtype=np.float32).reshape(-1, 4)
     sc = np.ascontiguousarray(scores, dtype=np.float32).reshape(-1)
     n = sc.shape[0]
@@ -95,7 +97,8 @@ def nms(boxes, scores, iou_thr, *, class_ids=None, batch_offsets=None, score_thr
     cap = batch * max_out if max_out > 0 else n
     keep = np.full(max(cap, 1), -1, dtype=np.int64)
     counts = np.zeros(batch, dtype=np.int64)
-    total = _load().oracle_nms(
+    fn = _load().oracle_fast_nms if fast else _load().oracle_nms
+    total = fn(
         _ptr(bx, ctypes.c_float), _ptr(sc, ctypes.c_float), n,
         None if cls is None else _ptr(cls, ctypes.c_int32),
         None if off is None else _ptr(off, ctypes.c_int64), batch,
@@ -107,9 +110,9 @@ def nms(boxes, scores, iou_thr, *, class_ids=None, batch_offsets=None, score_thr
     return keep[:cap], counts
 
 
-def nms_single(boxes, scores, iou_thr, *, max_out=0, score_thr=None) -> np.ndarray:
+def nms_single(boxes, scores, iou_thr, *, max_out=0, score_thr=None, fast=False) -> np.ndarray:
     """Single image, single class: the kept indices in score order."""
-    keep, counts = nms(boxes, scores, iou_thr, max_out=max_out, score_thr=score_thr)
+    keep, counts = nms(boxes, scores, iou_thr, max_out=max_out, score_thr=score_thr, fast=fast)
     return keep[: counts[0]].copy()
 
 

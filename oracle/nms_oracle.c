@@ -148,6 +148,70 @@ int64_t oracle_nms(const float* boxes, const float* scores, int64_t n,
 }
 
 /*
+ * Fast NMS over one image [lo, hi): a box is dropped when ANY box before it
+ * in the priority order (same class) overlaps it with IoU > thr, whether or
+ * not that box was itself dropped.
+ *
+ *   "YOLOv5后处理GPU移植实战", section 2.2 稳定性增强方案: each box is tested
+ *     against every other box of its class; it is suppressed when a box of
+ *     higher priority (higher score, or equal score and lower index) has
+ *     IoU above the threshold.  Section 2.1: without the index tie-break,
+ *     equal-score overlapping boxes would all drop each other.
+ *
+ * Readings (also in the design doc): the output is the kept indices in the same
+ * priority order as greedy NMS, cut at max_out; the pre-filter and the batch
+ * layout are those of oracle_nms.
+ */
+static int64_t fast_image(const float* boxes, const float* scores, const int32_t* class_ids,
+                          int64_t lo, int64_t hi, float iou_thr, int use_score_thr, float score_thr,
+                          int32_t max_out, int64_t* order, int64_t* out)
+{
+    int64_t m = 0;
+    for (int64_t i = lo; i < hi; ++i)
+        if (!use_score_thr || scores[i] > score_thr) order[m++] = i;
+    oracle_score_order(scores, order, m);
+
+    int64_t nkept = 0;
+    for (int64_t p = 0; p < m; ++p) {
+        int64_t i = order[p];
+        int suppressed = 0;
+        for (int64_t q = 0; q < p && !suppressed; ++q) {
+            int64_t k = order[q];
+            if (class_ids && class_ids[k] != class_ids[i]) continue;
+            if (oracle_iou(boxes + 4 * k, boxes + 4 * i) > iou_thr) suppressed = 1;
+        }
+        if (suppressed) continue;
+        out[nkept++] = i;
+        if (max_out > 0 && nkept == max_out) break;
+    }
+    return nkept;
+}
+
+/* Fast NMS entry: arguments, output layout and return value as oracle_nms. */
+int64_t oracle_fast_nms(const float* boxes, const float* scores, int64_t n,
+                        const int32_t* class_ids, const int64_t* batch_offsets, int32_t batch,
+                        float iou_thr, int use_score_thr, float score_thr, int32_t max_out,
+                        int64_t* keep, int64_t* counts)
+{
+    if (n < 0 || batch < 1) return -1;
+    if (!batch_offsets && batch != 1) return -1;
+    int64_t* order = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    if (!order) return -1;
+    int64_t total = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        int64_t lo = batch_offsets ? batch_offsets[b] : 0;
+        int64_t hi = batch_offsets ? batch_offsets[b + 1] : n;
+        if (lo < 0 || hi < lo || hi > n) { free(order); return -1; }
+        int64_t base = (max_out > 0) ? (int64_t)b * max_out : lo;
+        counts[b] = fast_image(boxes, scores, class_ids, lo, hi, iou_thr, use_score_thr, score_thr,
+                               max_out, order, keep + base);
+        total += counts[b];
+    }
+    free(order);
+    return total;
+}
+
+/*
  * Suppression bitmask of boxes that are already in score order, as the pages
  * define it ("NMS CUDA代码学习", section Phase 1): bit (j mod 64) of word
  * j/64 in row i is set iff j > i and IoU(i, j) > thr.  Row-major [n][W]

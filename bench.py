@@ -172,9 +172,10 @@ def _graph_size(wl):
     return bits, len(keep)
 
 
-def time_workload(g, torch, wl, dev, flush, reps=30):
-    """Device time of one nms_run call on workload wl (inputs resident, L2
-    flushed before each call): median, p10 and p90 in microseconds."""
+def time_workload(g, torch, wl, dev, flush, reps=30, fast=False):
+    """Device time of one nms_run call (nms_fast_run with fast=True) on
+    workload wl (inputs resident, L2 flushed before each call): median, p10
+    and p90 in microseconds."""
     stream = torch.cuda.current_stream(dev)
     batched = wl.class_ids is not None or wl.batch_offsets is not None
     B = wl.batch if wl.batch_offsets is not None else 0
@@ -189,8 +190,10 @@ def time_workload(g, torch, wl, dev, flush, reps=30):
     ws = g.Workspace(wl.n, B, C, device=dev)
     score_thr = -math.inf if wl.score_thr is None else wl.score_thr
 
+    entry = g.nms_fast_run if fast else g.nms_run
+
     def call():
-        st = g.nms_run(boxes.data_ptr(), scores.data_ptr(), wl.n,
+        st = entry(boxes.data_ptr(), scores.data_ptr(), wl.n,
                        cls.data_ptr() if cls is not None else 0, C,
                        off.data_ptr() if off is not None else 0, B, wl.iou_thr, score_thr,
                        wl.max_out, keep.data_ptr(), cap, counts.data_ptr(), 0, ws.ptr, ws.bytes,
@@ -366,11 +369,13 @@ def run_gbnms(args):
                 "frac": ach / hbm, "traffic": traffic,
                 "note": f"algorithmic bytes {nbytes}; peak {peak_kind}"}
 
-    per_config = None
+    per_config = fast_nms = None
     if not args.no_configs:
-        per_config = {}
+        per_config, fast_nms = {}, {}
         for name in W.CONFIGS:
-            per_config[name] = time_workload(g, torch, W.make(name, 0), dev, flush)
+            wl_c = W.make(name, 0)
+            per_config[name] = time_workload(g, torch, wl_c, dev, flush)
+            fast_nms[name] = time_workload(g, torch, wl_c, dev, flush, fast=True)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -392,6 +397,7 @@ def run_gbnms(args):
         "mask_hbm_frac": mask_bytes / (mask_ms / 1000) / 1e9 / hbm,
         "kernels": kernels,
         "per_config": per_config,
+        "fast_nms_per_config": fast_nms,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": n / (e2e_ms / 1000), "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -28,7 +28,7 @@ NMS_ERR_CUDA = 4
 NMS_ERR_TIMEOUT = 5
 NMS_MAX_SINGLE_N = 1 << 18
 
-EXPORTED = ("nms_status_string", "nms_workspace_size", "nms_run", "nms_run_timed",
+EXPORTED = ("nms_status_string", "nms_workspace_size", "nms_run", "nms_fast_run", "nms_run_timed",
             "nms_mask_row_words", "nms_iou_mask", "nms_resolve_mask", "nms_resolve_mask_noalloc")
 NMS_NOALLOC_MAX_N = 16384
 
@@ -62,6 +62,8 @@ def load():
     lib.nms_workspace_size.restype = ctypes.c_int
     lib.nms_run.argtypes = [vp, vp, i64, vp, i32, vp, i32, f32, f32, i32, vp, i64, vp, vp, vp, sz, vp]
     lib.nms_run.restype = ctypes.c_int
+    lib.nms_fast_run.argtypes = lib.nms_run.argtypes
+    lib.nms_fast_run.restype = ctypes.c_int
     lib.nms_run_timed.argtypes = [vp, vp, i64, vp, i32, vp, i32, f32, f32, i32, vp, i64, vp, vp, vp,
                                   sz, vp, ctypes.POINTER(vp), i32]
     lib.nms_run_timed.restype = ctypes.c_int
@@ -105,6 +107,18 @@ def nms_run(boxes: int, scores: int, n: int, class_ids: int, num_classes: int,
                           float(score_thr), int(max_out), keep or None, int(keep_cap),
                           counts or None, dev_status or None, workspace or None,
                           int(workspace_bytes), stream or None)
+
+
+def nms_fast_run(boxes: int, scores: int, n: int, class_ids: int, num_classes: int,
+                 batch_offsets: int, batch: int, iou_thr: float, score_thr: float, max_out: int,
+                 keep: int, keep_cap: int, counts: int, dev_status: int, workspace: int,
+                 workspace_bytes: int, stream: int) -> int:
+    """Fast NMS through the C entry point (arguments as nms_run)."""
+    return load().nms_fast_run(boxes or None, scores or None, int(n), class_ids or None,
+                               int(num_classes), batch_offsets or None, int(batch), float(iou_thr),
+                               float(score_thr), int(max_out), keep or None, int(keep_cap),
+                               counts or None, dev_status or None, workspace or None,
+                               int(workspace_bytes), stream or None)
 
 
 def nms_run_timed(boxes: int, scores: int, n: int, class_ids: int, num_classes: int,
@@ -176,15 +190,16 @@ class Workspace:
 
 def nms(boxes, scores, iou_thr: float, *, class_ids=None, num_classes: Optional[int] = None,
         batch_offsets=None, score_thr: Optional[float] = None, max_out: int = 0,
-        workspace: Optional[Workspace] = None, return_counts: bool = False):
+        workspace: Optional[Workspace] = None, return_counts: bool = False, fast: bool = False):
     """Greedy IoU NMS on CUDA tensors.
 
     boxes [n,4] fp32 xyxy and scores [n] fp32 on one CUDA device; class_ids
     int32 [n] (optional, with num_classes), batch_offsets int64 [B+1]
     (optional).  Returns the int64 kept indices: for one image a 1-D tensor in
     score order; with batch_offsets a list of per-image tensors.  With
-    return_counts=True also returns the device counts tensor.  Runs on the
-    current stream and synchronises it once to read the counts.
+    return_counts=True also returns the device counts tensor; fast=True runs
+    Fast NMS (nms_fast_run) instead of greedy NMS.  Runs on the current stream
+    and synchronises it once to read the counts.
     """
     torch = _torch()
     if not (boxes.is_cuda and scores.is_cuda):
@@ -212,7 +227,7 @@ def nms(boxes, scores, iou_thr: float, *, class_ids=None, num_classes: Optional[
     counts = torch.empty(max(B, 1), dtype=torch.int64, device=dev)
     status = torch.empty(1, dtype=torch.int32, device=dev)
     ws = workspace if workspace is not None else Workspace(n, B, C, device=dev)
-    st = nms_run(boxes.data_ptr() if n else 0, scores.data_ptr() if n else 0, n, cls_ptr, C,
+    st = (nms_fast_run if fast else nms_run)(boxes.data_ptr() if n else 0, scores.data_ptr() if n else 0, n, cls_ptr, C,
                  off_ptr, B, iou_thr, -math.inf if score_thr is None else score_thr, max_out,
                  keep.data_ptr(), cap, counts.data_ptr(), status.data_ptr(), ws.ptr, ws.bytes,
                  torch.cuda.current_stream(dev).cuda_stream)

@@ -78,7 +78,7 @@ SingleLayout single_layout(int64_t n)
     s.rowbits = L.add(8 * static_cast<size_t>(n) * static_cast<size_t>(s.NB));
     s.band = L.add(8 * static_cast<size_t>((n + 63) / 64) * (BAND_L + 1) * 64);
     s.edges = L.add(4 * static_cast<size_t>(s.lcap));
-    s.haspred = L.add(s.ecap ? 8 * static_cast<size_t>((n + 63) / 64) : 0);
+    s.haspred = L.add(8 * static_cast<size_t>((n + 63) / 64));
     s.gstate = L.add(s.grid ? graph_grid_state_bytes(static_cast<int>(n)) : 0);
     s.gctl = L.add(s.grid ? graph_grid_ctl_bytes() : 0);
     s.mask = L.add(8 * static_cast<size_t>(n) * static_cast<size_t>(s.ldw));
@@ -192,7 +192,7 @@ nms_status run_impl(const float* boxes, const float* scores, int64_t n, const in
                     int32_t num_classes, const int64_t* batch_offsets, int32_t batch, float iou_thr,
                     float score_thr, int32_t max_out, int64_t* keep, int64_t keep_cap,
                     int64_t* counts, int32_t* dev_status, void* workspace, size_t workspace_bytes,
-                    void* stream, const Stamps& stamps)
+                    void* stream, const Stamps& stamps, bool fast = false)
 {
     if (n < 0 || n > INT32_MAX) return NMS_ERR_INVALID_ARG;
     if (std::isnan(iou_thr) || std::isnan(score_thr)) return NMS_ERR_INVALID_ARG;
@@ -242,9 +242,25 @@ nms_status run_impl(const float* boxes, const float* scores, int64_t n, const in
         float4* boxes_s = at<float4>(workspace, L.boxes_s);
         uint64_t* mask = at<uint64_t>(workspace, L.mask);
         uint64_t* rowbits = at<uint64_t>(workspace, L.rowbits);
+        uint64_t* haspred = at<uint64_t>(workspace, L.haspred);
+        if (fast) {
+            // Fast NMS ("YOLOv5后处理GPU移植实战" 2.2): the boxes with no earlier
+            // box over the threshold, i.e. the clear bits of haspred.
+            launch_sort(scores, reinterpret_cast<const float4*>(boxes), cand, m_count, static_cast<int>(n),
+                        perm, boxes_s, sort_keys_bytes(static_cast<int>(n)) ? at<uint64_t>(workspace, L.keys)
+                                                                            : nullptr,
+                        status, nullptr, L.NB, nullptr, haspred, nullptr, st);
+            stamps.record(1, st);
+            launch_iou_mask(boxes_s, m_count, static_cast<int>(n), p, nullptr, L.ldw, nullptr, L.NB, nullptr,
+                            nullptr, nullptr, 0u, haspred, st);
+            stamps.record(2, st);
+            launch_fast_emit(haspred, m_count, static_cast<int>(n), perm, max_out, keep, counts, st);
+            stamps.record(3, st);
+            return cuda_status();
+        }
         uint32_t* edges = L.ecap ? at<uint32_t>(workspace, L.edges) : nullptr;
         unsigned* ecount = at<unsigned>(workspace, L.ecount);
-        uint64_t* haspred = L.ecap ? at<uint64_t>(workspace, L.haspred) : nullptr;
+        if (!L.ecap) haspred = nullptr;  // the walk needs no neighbour bitmap
         uint64_t* keys = sort_keys_bytes(static_cast<int>(n)) ? at<uint64_t>(workspace, L.keys) : nullptr;
         // The all-SM path's control block: its first 8 ints (barrier count,
         // round flags, per-stage "resolved" flags at 4..7) are zeroed by the sort.
@@ -308,6 +324,7 @@ nms_status run_impl(const float* boxes, const float* scores, int64_t n, const in
     a.score_thr = score_thr;
     a.thr = iou_thr;
     a.max_out = max_out;
+    a.fast = fast ? 1 : 0;
     a.seg_cnt = at<int>(workspace, L.seg_cnt);
     a.seg_off = at<int>(workspace, L.seg_off);
     a.seg_of = at<int>(workspace, L.seg_of);
@@ -338,6 +355,18 @@ extern "C" nms_status nms_run(const float* boxes, const float* scores, int64_t n
     return run_impl(boxes, scores, n, class_ids, num_classes, batch_offsets, batch, iou_thr,
                     score_thr, max_out, keep, keep_cap, counts, dev_status, workspace,
                     workspace_bytes, stream, Stamps{});
+}
+
+extern "C" nms_status nms_fast_run(const float* boxes, const float* scores, int64_t n,
+                                   const int32_t* class_ids, int32_t num_classes,
+                                   const int64_t* batch_offsets, int32_t batch, float iou_thr,
+                                   float score_thr, int32_t max_out, int64_t* keep, int64_t keep_cap,
+                                   int64_t* counts, int32_t* dev_status, void* workspace,
+                                   size_t workspace_bytes, void* stream)
+{
+    return run_impl(boxes, scores, n, class_ids, num_classes, batch_offsets, batch, iou_thr,
+                    score_thr, max_out, keep, keep_cap, counts, dev_status, workspace,
+                    workspace_bytes, stream, Stamps{}, true);
 }
 
 extern "C" nms_status nms_run_timed(const float* boxes, const float* scores, int64_t n,

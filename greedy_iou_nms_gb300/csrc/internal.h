@@ -75,6 +75,11 @@ void launch_graph_grid(uint32_t* edges, const unsigned* ecount, const uint64_t* 
                        int32_t* status, cudaStream_t st, int limit, const int* done_in, int* done_out,
                        int* grid_done, uint64_t* state, void* ctl);
 
+// Fast NMS output of one image: the boxes whose bit in haspred is clear, in
+// sorted order, mapped through perm, cut at max_out.
+void launch_fast_emit(const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm, int max_out,
+                      int64_t* keep, int64_t* counts, cudaStream_t st);
+
 struct BatchedArgs {
     const float4* boxes;
     const float* scores;
@@ -88,6 +93,7 @@ struct BatchedArgs {
     float score_thr;
     float thr;
     int max_out;
+    int fast;  // Fast NMS: drop a box any earlier box of its segment suppresses
     int* seg_cnt;
     int* seg_off;
     int* seg_of;

@@ -154,7 +154,7 @@ constexpr int SS_WARPS = 4;
 __global__ void __launch_bounds__(SS_WARPS * 32)
 seg_small_kernel(const float4* __restrict__ boxes, const float* __restrict__ scores,
                  const int* __restrict__ seg_off, const int* __restrict__ cand, int S,
-                 const int* __restrict__ ok, float thr, int max_out,
+                 const int* __restrict__ ok, float thr, int max_out, int fast,
                  uint64_t* __restrict__ kept_key, int* __restrict__ kept_cnt)
 {
     __shared__ float4 sbox[SS_WARPS][64];
@@ -204,7 +204,9 @@ seg_small_kernel(const float4* __restrict__ boxes, const float* __restrict__ sco
         colB |= static_cast<uint64_t>(vb) << r;
     }
     const uint64_t valid = m >= 64 ? ~0ull : ((1ull << m) - 1ull);
-    uint64_t K = resolve_tile_col(valid, colA, colB);
+    // Greedy: resolve the column view; Fast NMS: keep the boxes no earlier
+    // box suppresses.
+    uint64_t K = fast ? ballot64(ha && colA == 0, hb && colB == 0) & valid : resolve_tile_col(valid, colA, colB);
     if (max_out > 0 && __popcll(K) > max_out) K = lowest_bits(K, max_out);
     if ((K >> l) & 1ull) kept_key[lo + __popcll(K & ((1ull << l) - 1ull))] = skey[wp][l];
     if ((K >> (l + 32)) & 1ull)
@@ -224,7 +226,7 @@ constexpr int SL_CACHE = 2048;  // kept boxes cached in shared memory (40 KB)
 __global__ void __launch_bounds__(SL_THREADS)
 seg_large_kernel(const float4* __restrict__ boxes, const float* __restrict__ scores,
                  const int* __restrict__ seg_off, const int* __restrict__ cand, int S,
-                 const int* __restrict__ ok, float thr, int max_out,
+                 const int* __restrict__ ok, float thr, int max_out, int fast,
                  uint64_t* __restrict__ sorted_key, float4* __restrict__ sorted_box,
                  uint64_t* __restrict__ kept_key, int* __restrict__ kept_cnt)
 {
@@ -263,7 +265,8 @@ seg_large_kernel(const float4* __restrict__ boxes, const float* __restrict__ sco
         if (threadIdx.x == 0) s_removed = 0;
         if (threadIdx.x < 64) diag[threadIdx.x] = 0;
         __syncthreads();
-        // (a) candidates of the tile against every kept box.
+        // (a) candidates of the tile against every kept box (Fast NMS: every
+        //     earlier box of the segment).
         {
             const int cidx = threadIdx.x & 63;
             const int slice = threadIdx.x >> 6;
@@ -272,7 +275,13 @@ seg_large_kernel(const float4* __restrict__ boxes, const float* __restrict__ sco
                 const float4 cbx = sorted_box[lo + t0 + cidx];
                 const float car = box_area(cbx);
                 bool hit = false;
-                for (int k = slice; k < nk && !hit; k += nslice) {
+                if (fast) {
+                    for (int k = slice; k < t0 && !hit; k += nslice) {
+                        const float4 kb = sorted_box[lo + k];
+                        hit = suppress_exact(kb, box_area(kb), cbx, car, thr);
+                    }
+                }
+                for (int k = slice; !fast && k < nk && !hit; k += nslice) {
                     float4 kb;
                     float ka;
                     if (k < SL_CACHE) {
@@ -302,7 +311,9 @@ seg_large_kernel(const float4* __restrict__ boxes, const float* __restrict__ sco
         __syncthreads();
         if (threadIdx.x < 32) {
             const uint64_t valid = tn >= 64 ? ~0ull : ((1ull << tn) - 1ull);
-            uint64_t K = resolve_tile_col(valid & ~static_cast<uint64_t>(s_removed), diag[l], diag[l + 32]);
+            const uint64_t cand = valid & ~static_cast<uint64_t>(s_removed);
+            uint64_t K = fast ? cand & ballot64(diag[l] == 0, diag[l + 32] == 0)
+                              : resolve_tile_col(cand, diag[l], diag[l + 32]);
             const int room = cap - nk;
             if (__popcll(K) > room) K = lowest_bits(K, room);
             if (l == 0) { s_kept = K; s_nk = __popcll(K); }
@@ -424,9 +435,9 @@ void launch_batched(const BatchedArgs& a, cudaStream_t st, const Stamps& stamps)
     if (n > 0) batched_scatter_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.seg_of, a.slot, a.seg_off, n, a.ok, a.cand);
     stamps.record(1, st);
     seg_small_kernel<<<(S + SS_WARPS - 1) / SS_WARPS, SS_WARPS * 32, 0, st>>>(
-        a.boxes, a.scores, a.seg_off, a.cand, S, a.ok, a.thr, a.max_out, a.kept_key, a.kept_cnt);
+        a.boxes, a.scores, a.seg_off, a.cand, S, a.ok, a.thr, a.max_out, a.fast, a.kept_key, a.kept_cnt);
     seg_large_kernel<<<S, SL_THREADS, 0, st>>>(a.boxes, a.scores, a.seg_off, a.cand, S, a.ok, a.thr,
-                                               a.max_out, a.sorted_key, a.sorted_box, a.kept_key,
+                                               a.max_out, a.fast, a.sorted_key, a.sorted_box, a.kept_key,
                                                a.kept_cnt);
     stamps.record(2, st);
     merge_kernel<<<a.batch, MG_THREADS, 0, st>>>(a.seg_off, a.kept_cnt, a.kept_key, a.C, a.off,

@@ -1,0 +1,85 @@
+// Fast NMS output for one image: the boxes no earlier box suppresses.
+//
+// "YOLOv5后处理GPU移植实战", section 2.2 稳定性增强方案: a box is suppressed
+// when a box of higher priority (higher score, or equal score and lower
+// index) has IoU above the threshold with it, whether or not that box was
+// suppressed itself.  In sorted positions that is exactly bit p of the
+// mask kernel's bitmap of boxes with an earlier neighbour over the threshold,
+// so the answer is the clear bits, in order, mapped through the sort
+// permutation.
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gbnms {
+
+constexpr int FE_THREADS = 1024;
+
+// One CTA: warp w owns the 32-box words [w*wpw, (w+1)*wpw); a block prefix of
+// the warps' kept counts places them, and within a word lane l writes box
+// 32w+l (coalesced perm loads and keep stores).
+__global__ void __launch_bounds__(FE_THREADS)
+fast_emit_kernel(const uint32_t* __restrict__ haspred, const int* __restrict__ m_dev, int m_bound,
+                 const int* __restrict__ perm, int max_out, int64_t* __restrict__ keep,
+                 int64_t* __restrict__ counts)
+{
+    __shared__ int scratch[32];
+    const int n = m_dev ? *m_dev : m_bound;
+    const int NW = (n + 31) / 32;
+    const unsigned l = lane_id();
+    const int warp = threadIdx.x >> 5;
+    auto kept_word = [&](int w) {
+        const uint32_t valid = (w == NW - 1 && (n & 31)) ? (1u << (n & 31)) - 1u : ~0u;
+        return ~haspred[w] & valid;
+    };
+    const int wpw = (NW + 31) / 32;
+    const int a0 = min(warp * wpw, NW), a1 = min(a0 + wpw, NW);
+    int c = 0;
+    for (int w = a0 + static_cast<int>(l); w < a1; w += 32) c += __popc(kept_word(w));
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) c += __shfl_xor_sync(FULL, c, d);
+    if (l == 0) scratch[warp] = c;
+    __syncthreads();
+    if (warp == 0) {
+        int v = scratch[l];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(FULL, v, d);
+            if (static_cast<int>(l) >= d) v += y;
+        }
+        scratch[l] = v;
+    }
+    __syncthreads();
+    const int total = scratch[31];
+    const int cap = max_out > 0 ? max_out : INT_MAX;
+    int base = warp ? scratch[warp - 1] : 0;
+    const uint32_t below = (1u << l) - 1u;
+    constexpr int OW = 8;  // words whose loads are in flight together
+    for (int wb = a0; wb < a1 && base < cap; wb += OW) {
+        uint32_t bits[OW];
+        int v[OW];
+#pragma unroll
+        for (int u = 0; u < OW; ++u) {
+            bits[u] = wb + u < a1 ? kept_word(wb + u) : 0u;
+            const int j = 32 * (wb + u) + static_cast<int>(l);
+            v[u] = ((bits[u] >> l) & 1u) ? (perm ? perm[j] : j) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < OW; ++u) {
+            const int pos = base + __popc(bits[u] & below);
+            if (((bits[u] >> l) & 1u) && pos < cap) keep[pos] = v[u];
+            base += __popc(bits[u]);
+        }
+    }
+    if (threadIdx.x == 0) counts[0] = total < cap ? total : cap;
+}
+
+void launch_fast_emit(const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm, int max_out,
+                      int64_t* keep, int64_t* counts, cudaStream_t st)
+{
+    fast_emit_kernel<<<1, FE_THREADS, 0, st>>>(reinterpret_cast<const uint32_t*>(haspred), m_dev, m_bound,
+                                               perm, max_out, keep, counts);
+}
+
+}  // namespace gbnms

@@ -298,12 +298,12 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
     const int64_t wcol = cb / 64;
     const int chunk = cb >> 8;  // 256-column chunk of the per-row bitmap
     if (i0 < n) {
-        store_words(mask + static_cast<int64_t>(i0) * ldw + wcol, w0);
+        if (mask) store_words(mask + static_cast<int64_t>(i0) * ldw + wcol, w0);
         if (rowbits && or_words(w0))
             atomicOr(rowbits + static_cast<int64_t>(i0) * NB + (chunk >> 6), 1ull << (chunk & 63));
     }
     if (i1 < n) {
-        store_words(mask + static_cast<int64_t>(i1) * ldw + wcol, w1);
+        if (mask) store_words(mask + static_cast<int64_t>(i1) * ldw + wcol, w1);
         if (rowbits && or_words(w1))
             atomicOr(rowbits + static_cast<int64_t>(i1) * NB + (chunk >> 6), 1ull << (chunk & 63));
     }

@@ -169,6 +169,21 @@ nms_status nms_resolve_mask(const uint64_t* mask, int64_t n, const int32_t* perm
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Fast NMS ("YOLOv5后处理GPU移植实战", sections 2.1 and 2.2): a box is dropped
+ * when any box of higher priority (higher score, or equal score and lower
+ * index) of the same image and class has IoU > iou_thr with it, whether or
+ * not that box was dropped itself.  It keeps a subset of what nms_run keeps,
+ * in the same order, and needs no sequential resolve.  Arguments, output
+ * layout, workspace and errors exactly as for nms_run.
+ */
+nms_status nms_fast_run(const float* boxes, const float* scores, int64_t n,
+                        const int32_t* class_ids, int32_t num_classes,
+                        const int64_t* batch_offsets, int32_t batch, float iou_thr,
+                        float score_thr, int32_t max_out, int64_t* keep, int64_t keep_cap,
+                        int64_t* counts, int32_t* dev_status, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/*
  * nms_run with stage timing, for measurement: the same call, plus up to
  * nevents caller-created CUDA events (cudaEvent_t, created with timing
  * enabled) that it records on `stream`: events[0] before its first kernel and

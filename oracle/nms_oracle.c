@@ -212,6 +212,67 @@ int64_t oracle_fast_nms(const float* boxes, const float* scores, int64_t n,
 }
 
 /*
+ * Matrix NMS, Gaussian decay, one image:
+ *
+ *   "Fastest Matrix NMS in the West (Part 2)", section "What do we need to
+ *   compute?": with boxes sorted by score (highest first), O[i][j] is the IoU
+ *   of box j with a higher-scoring father box i (i before j), O_max[i] the
+ *   largest overlap of box i with its own fathers, the decay that father i
+ *   gives box j is exp((O_max[i]^2 - O[i][j]^2) / sigma), and the final score
+ *   is s'[j] = s[j] * min over fathers i of that decay.  Section
+ *   "Optimization 4": a box is dropped when its final score is below the
+ *   threshold t.
+ *
+ * Readings (also in the design doc): the sort is the stable descending one of
+ * greedy NMS (ties to the lower index) over the pre-filtered candidates; IoUs
+ * are the canonical binary32 ones; a box with no father (the first) keeps
+ * s[j] (the minimum over no fathers is 1); the exponent, the exponential, the
+ * product and the comparison are evaluated in binary64 from those binary32
+ * values, with NaN decays ignored by the minimum; the output is the kept
+ * indices in score order with their final scores rounded to binary32, cut at
+ * max_out.  This is the literal O(n^2) evaluation.
+ */
+int64_t oracle_matrix_nms(const float* boxes, const float* scores, int64_t n, float sigma,
+                          int use_score_thr, float score_thr, float decay_thr, int32_t max_out,
+                          int64_t* keep, float* out_scores)
+{
+    if (n < 0) return -1;
+    int64_t* order = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    float* omax = (float*)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
+    if (!order || !omax) { free(order); free(omax); return -1; }
+    int64_t m = 0;
+    for (int64_t i = 0; i < n; ++i)
+        if (!use_score_thr || scores[i] > score_thr) order[m++] = i;
+    oracle_score_order(scores, order, m);
+    for (int64_t p = 0; p < m; ++p) {
+        float best = 0.0f;
+        for (int64_t q = 0; q < p; ++q) {
+            float o = oracle_iou(boxes + 4 * order[q], boxes + 4 * order[p]);
+            if (o > best) best = o;
+        }
+        omax[p] = best;
+    }
+    int64_t nkept = 0;
+    for (int64_t p = 0; p < m && !(max_out > 0 && nkept == max_out); ++p) {
+        double dmin = 1.0;
+        for (int64_t q = 0; q < p; ++q) {
+            float o = oracle_iou(boxes + 4 * order[q], boxes + 4 * order[p]);
+            double x = ((double)omax[q] * (double)omax[q] - (double)o * (double)o) / (double)sigma;
+            double d = exp(x);
+            if (d < dmin) dmin = d;
+        }
+        double fs = (double)scores[order[p]] * dmin;
+        if (fs < (double)decay_thr) continue;
+        keep[nkept] = order[p];
+        if (out_scores) out_scores[nkept] = (float)fs;
+        ++nkept;
+    }
+    free(order);
+    free(omax);
+    return nkept;
+}
+
+/*
  * Suppression bitmask of boxes that are already in score order, as the pages
  * define it ("NMS CUDA代码学习", section Phase 1): bit (j mod 64) of word
  * j/64 in row i is set iff j > i and IoU(i, j) > thr.  Row-major [n][W]

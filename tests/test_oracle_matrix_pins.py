@@ -1,0 +1,125 @@
+"""Pins of the Matrix NMS oracle ("Fastest Matrix NMS in the West (Part 2)",
+section "What do we need to compute?" and section "Optimization 4") to facts
+that do not come from the oracle: closed forms (disjoint boxes, a pair at an
+exact IoU, identical boxes), a hand-worked three-box chain with exact rational
+IoUs, the page's own restatement of the drop rule (a box goes when some
+father's candidate decayed score is below the threshold), and invariants."""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+def test_disjoint_boxes_keep_their_scores():
+    b = np.array([[0, 0, 1, 1], [5, 5, 6, 6], [10, 0, 11, 1], [0, 10, 1, 11]], np.float32)
+    s = np.array([0.9, 0.2, 0.6, 0.4], np.float32)
+    keep, fs = oracle.matrix_nms(b, s, 0.3)
+    assert keep.tolist() == [0, 2, 3]
+    assert fs.tolist() == [np.float32(0.9), np.float32(0.6), np.float32(0.4)]
+    # the threshold is inclusive for keeping: final score == t stays
+    keep, _ = oracle.matrix_nms(b, s, np.float32(0.4))
+    assert keep.tolist() == [0, 2, 3]
+
+
+@pytest.mark.parametrize("sigma", [0.5, 2.0])
+def test_pair_at_exact_iou(sigma):
+    """IoU([0,0,4,4], [0,0,4,2]) = 8/16 = 0.5 exactly: the second box decays by
+    exp(-0.25/sigma); the first (no father) keeps its score."""
+    b = np.array([[0, 0, 4, 4], [0, 0, 4, 2]], np.float32)
+    s = np.array([0.9, 0.8], np.float32)
+    keep, fs = oracle.matrix_nms(b, s, 0.0, sigma=sigma)
+    assert keep.tolist() == [0, 1]
+    assert fs[0] == np.float32(0.9)
+    assert fs[1] == np.float32(float(np.float32(0.8)) * math.exp(-0.25 / float(np.float32(sigma))))
+
+
+def test_identical_boxes():
+    """k identical boxes: the first keeps its score; every other one decays by
+    exp(-1/sigma) (its top father overlaps it at 1 and has no father itself;
+    the other fathers overlap at 1 with their own maximum 1, decay 1)."""
+    k = 6
+    b = np.tile(np.array([[3, 3, 9, 7]], np.float32), (k, 1))
+    s = np.linspace(0.9, 0.4, k).astype(np.float32)
+    keep, fs = oracle.matrix_nms(b, s, 0.0)
+    assert keep.tolist() == list(range(k))
+    assert fs[0] == s[0]
+    for j in range(1, k):
+        assert fs[j] == np.float32(float(s[j]) * math.exp(-2.0))
+
+
+def test_chain_hand_worked():
+    """a=[0,0,10,1], b=[3,0,13,1], c=[6,0,16,1]: IoU(a,b) = IoU(b,c) = 7/13,
+    IoU(a,c) = 1/4.  O_max: a 0, b 7/13, c 7/13.  Decays (sigma 1/2): b gets
+    exp(-2 (7/13)^2) from a; c gets min(exp(-2 (1/4)^2) from a, exp(0) from b)."""
+    b = np.array([[0, 0, 10, 1], [3, 0, 13, 1], [6, 0, 16, 1]], np.float32)
+    s = np.array([0.9, 0.8, 0.7], np.float32)
+    keep, fs = oracle.matrix_nms(b, s, 0.0)
+    r = float(Fraction(7, 13))
+    exp_b = float(np.float32(0.8)) * math.exp(-2 * r * r)
+    exp_c = float(np.float32(0.7)) * math.exp(-2 * 0.25 * 0.25)
+    assert keep.tolist() == [0, 1, 2]
+    assert abs(fs[1] - exp_b) <= 2e-7 and abs(fs[2] - exp_c) <= 2e-7  # binary32 IoUs of 7/13
+    assert fs[0] == np.float32(0.9)
+    # final scores: a 0.9, b ~0.448, c ~0.618; a threshold between b and c
+    # drops b only, one between c and a keeps a only
+    assert exp_b < exp_c < 0.9
+    assert oracle.matrix_nms(b, s, (exp_b + exp_c) / 2)[0].tolist() == [0, 2]
+    assert oracle.matrix_nms(b, s, (exp_c + 0.9) / 2)[0].tolist() == [0]
+
+
+def _clustered(rng, n):
+    c = rng.uniform(0, 200, (max(n // 6, 1), 2))[rng.integers(0, max(n // 6, 1), n)] + rng.normal(0, 5, (n, 2))
+    wh = rng.uniform(8, 40, (n, 2))
+    return np.concatenate([c - wh / 2, c + wh / 2], 1).astype(np.float32), rng.uniform(0, 1, n).astype(np.float32)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_pages_exists_restatement(seed):
+    """Section "Optimization 4": since scores are non-negative, s_j min_i d_ij < t
+    exactly when some father i has s_j d_ij < t.  The drop decisions of the
+    oracle (a minimum, then one comparison) equal that existence form,
+    evaluated here pair by pair from the binary32 IoUs."""
+    rng = np.random.default_rng(seed)
+    n = 60
+    b, s = _clustered(rng, n)
+    t = 0.25
+    keep, _ = oracle.matrix_nms(b, s, t)
+    order = oracle.score_order(s)
+    O = np.zeros((n, n))
+    for p in range(n):
+        for q in range(p):
+            O[q, p] = float(oracle.iou(b[order[q]], b[order[p]]))
+    omax = np.array([max([O[q, p] for q in range(p)], default=0.0) for p in range(n)])
+    kept = []
+    for p in range(n):
+        sj = float(s[order[p]])
+        drop = sj < t if p == 0 else any(sj * math.exp((omax[q] ** 2 - O[q, p] ** 2) / 0.5) < t for q in range(p))
+        if not drop:
+            kept.append(int(order[p]))
+    assert keep.tolist() == kept
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_invariants(seed):
+    rng = np.random.default_rng(10 + seed)
+    b, s = _clustered(rng, 200)
+    # a very wide Gaussian decays nothing
+    keep, fs = oracle.matrix_nms(b, s, 0.0, sigma=1e7)
+    order = oracle.score_order(s)
+    assert keep.tolist() == order.tolist()
+    assert np.allclose(fs, s[order], rtol=1e-6)
+    # decayed scores never exceed the scores; a higher threshold keeps a subset
+    keep, fs = oracle.matrix_nms(b, s, 0.0)
+    assert np.all(fs <= s[keep])
+    k2, _ = oracle.matrix_nms(b, s, 0.3)
+    assert set(k2.tolist()) <= set(keep.tolist())
+    assert [x for x in keep.tolist() if x in set(k2.tolist())] == k2.tolist()
+    # max_out keeps a prefix; the pre-filter is strict
+    k3, f3 = oracle.matrix_nms(b, s, 0.1, max_out=9)
+    kf, ff = oracle.matrix_nms(b, s, 0.1)
+    assert k3.tolist() == kf.tolist()[:9] and f3.tolist() == ff.tolist()[:9]
+    kp, _ = oracle.matrix_nms(b, s, 0.0, score_thr=0.5)
+    assert all(s[i] > np.float32(0.5) for i in kp)

@@ -220,6 +220,45 @@ def time_workload(g, torch, wl, dev, flush, reps=30, fast=False):
             "kept": int(counts.sum().item()), "batched": batched}
 
 
+def time_matrix(g, torch, wl, dev, flush, decay_thr=0.1, reps=20):
+    """Device time of one nms_matrix_run call (Gaussian decay, sigma 0.5) on
+    a one-image workload: median, p10, p90 in microseconds."""
+    stream = torch.cuda.current_stream(dev)
+    boxes = torch.from_numpy(wl.boxes).to(dev)
+    scores = torch.from_numpy(wl.scores).to(dev)
+    n = wl.n
+    cap = g.keep_capacity(n, None, wl.max_out)
+    keep = torch.empty(max(cap, 1), dtype=torch.int64, device=dev)
+    ks = torch.empty(max(cap, 1), dtype=torch.float32, device=dev)
+    count = torch.empty(1, dtype=torch.int64, device=dev)
+    wsb = g.nms_matrix_workspace_size(n)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    score_thr = -math.inf if wl.score_thr is None else wl.score_thr
+
+    def call():
+        st = g.nms_matrix_run(boxes.data_ptr(), scores.data_ptr(), n, 0.5, score_thr, decay_thr, wl.max_out,
+                              keep.data_ptr(), ks.data_ptr(), cap, count.data_ptr(), 0, ws.data_ptr(), wsb,
+                              stream.cuda_stream)
+        if st != g.NMS_OK:
+            raise g.NmsError(st, "nms_matrix_run")
+
+    for _ in range(3):
+        call()
+    evs = []
+    for _ in range(reps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    us = sorted(1000 * a.elapsed_time(b) for a, b in evs)
+    med = statistics.median(us)
+    return {"us_median": med, "us_p10": us[len(us) // 10], "us_p90": us[min(len(us) - 1, 9 * len(us) // 10)],
+            "boxes_per_s": n / (med / 1e6), "decay_thr": decay_thr, "kept": int(count.item())}
+
+
 def run_gbnms(args):
     import torch
     import greedy_iou_nms_gb300 as g
@@ -369,13 +408,15 @@ def run_gbnms(args):
                 "frac": ach / hbm, "traffic": traffic,
                 "note": f"algorithmic bytes {nbytes}; peak {peak_kind}"}
 
-    per_config = fast_nms = None
+    per_config = fast_nms = matrix_nms = None
     if not args.no_configs:
-        per_config, fast_nms = {}, {}
+        per_config, fast_nms, matrix_nms = {}, {}, {}
         for name in W.CONFIGS:
             wl_c = W.make(name, 0)
             per_config[name] = time_workload(g, torch, wl_c, dev, flush)
             fast_nms[name] = time_workload(g, torch, wl_c, dev, flush, fast=True)
+            if wl_c.class_ids is None and wl_c.batch_offsets is None:
+                matrix_nms[name] = time_matrix(g, torch, wl_c, dev, flush)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -398,6 +439,7 @@ def run_gbnms(args):
         "kernels": kernels,
         "per_config": per_config,
         "fast_nms_per_config": fast_nms,
+        "matrix_nms_per_config": matrix_nms,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": n / (e2e_ms / 1000), "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -29,7 +29,8 @@ NMS_ERR_TIMEOUT = 5
 NMS_MAX_SINGLE_N = 1 << 18
 
 EXPORTED = ("nms_status_string", "nms_workspace_size", "nms_run", "nms_fast_run", "nms_run_timed",
-            "nms_mask_row_words", "nms_iou_mask", "nms_resolve_mask", "nms_resolve_mask_noalloc")
+            "nms_matrix_workspace_size", "nms_matrix_run", "nms_mask_row_words", "nms_iou_mask",
+            "nms_resolve_mask", "nms_resolve_mask_noalloc")
 NMS_NOALLOC_MAX_N = 16384
 
 _lib = None
@@ -62,6 +63,10 @@ def load():
     lib.nms_workspace_size.restype = ctypes.c_int
     lib.nms_run.argtypes = [vp, vp, i64, vp, i32, vp, i32, f32, f32, i32, vp, i64, vp, vp, vp, sz, vp]
     lib.nms_run.restype = ctypes.c_int
+    lib.nms_matrix_workspace_size.argtypes = [i64, ctypes.POINTER(sz)]
+    lib.nms_matrix_workspace_size.restype = ctypes.c_int
+    lib.nms_matrix_run.argtypes = [vp, vp, i64, f32, f32, f32, i32, vp, vp, i64, vp, vp, vp, sz, vp]
+    lib.nms_matrix_run.restype = ctypes.c_int
     lib.nms_fast_run.argtypes = lib.nms_run.argtypes
     lib.nms_fast_run.restype = ctypes.c_int
     lib.nms_run_timed.argtypes = [vp, vp, i64, vp, i32, vp, i32, f32, f32, i32, vp, i64, vp, vp, vp,
@@ -119,6 +124,51 @@ def nms_fast_run(boxes: int, scores: int, n: int, class_ids: int, num_classes: i
                                float(score_thr), int(max_out), keep or None, int(keep_cap),
                                counts or None, dev_status or None, workspace or None,
                                int(workspace_bytes), stream or None)
+
+
+def nms_matrix_workspace_size(n: int) -> int:
+    out = ctypes.c_size_t(0)
+    st = load().nms_matrix_workspace_size(int(n), ctypes.byref(out))
+    if st != NMS_OK:
+        raise NmsError(st, "nms_matrix_workspace_size")
+    return out.value
+
+
+def nms_matrix_run(boxes: int, scores: int, n: int, sigma: float, score_thr: float, decay_thr: float,
+                   max_out: int, keep: int, keep_scores: int, keep_cap: int, count: int, dev_status: int,
+                   workspace: int, workspace_bytes: int, stream: int) -> int:
+    """Matrix NMS through the C entry point (device addresses as ints)."""
+    return load().nms_matrix_run(boxes or None, scores or None, int(n), float(sigma), float(score_thr),
+                                 float(decay_thr), int(max_out), keep or None, keep_scores or None,
+                                 int(keep_cap), count or None, dev_status or None, workspace or None,
+                                 int(workspace_bytes), stream or None)
+
+
+def matrix_nms(boxes, scores, decay_thr: float, *, sigma: float = 0.5, score_thr: Optional[float] = None,
+               max_out: int = 0):
+    """Matrix NMS (Gaussian decay) on CUDA tensors: (kept int64 indices in score
+    order, their float32 final scores).  Synchronises the current stream once."""
+    torch = _torch()
+    if not (boxes.is_cuda and scores.is_cuda):
+        raise ValueError("matrix_nms: boxes and scores must be CUDA tensors")
+    boxes = boxes.contiguous()
+    scores = scores.contiguous()
+    n = scores.shape[0]
+    dev = boxes.device
+    cap = keep_capacity(n, None, max_out)
+    keep = torch.empty(max(cap, 1), dtype=torch.int64, device=dev)
+    ks = torch.empty(max(cap, 1), dtype=torch.float32, device=dev)
+    count = torch.empty(1, dtype=torch.int64, device=dev)
+    ws_bytes = nms_matrix_workspace_size(n)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    st = nms_matrix_run(boxes.data_ptr() if n else 0, scores.data_ptr() if n else 0, n, sigma,
+                        -math.inf if score_thr is None else score_thr, decay_thr, max_out, keep.data_ptr(),
+                        ks.data_ptr(), cap, count.data_ptr(), 0, ws.data_ptr(), ws_bytes,
+                        torch.cuda.current_stream(dev).cuda_stream)
+    if st != NMS_OK:
+        raise NmsError(st, "nms_matrix_run")
+    k = int(count.item())
+    return keep[:k], ks[:k]
 
 
 def nms_run_timed(boxes: int, scores: int, n: int, class_ids: int, num_classes: int,

@@ -86,6 +86,27 @@ SingleLayout single_layout(int64_t n)
     return s;
 }
 
+struct MatrixLayout {
+    size_t status, m_count, cand, perm, boxes_s, keys, omax, xmin, total;
+};
+
+MatrixLayout matrix_layout(int64_t n)
+{
+    MatrixLayout m;
+    Layout L;
+    const size_t N = static_cast<size_t>(n);
+    m.status = L.add(4);
+    m.m_count = L.add(4);
+    m.cand = L.add(4 * N);
+    m.perm = L.add(4 * N);
+    m.boxes_s = L.add(16 * N);
+    m.keys = L.add(sort_keys_bytes(static_cast<int>(n)));
+    m.omax = L.add(4 * N);
+    m.xmin = L.add(8 * N);
+    m.total = L.total;
+    return m;
+}
+
 struct BatchedLayout {
     size_t status, ok, seg_cnt, seg_off, seg_of, slot, cand, kept_key, kept_cnt, sorted_key,
         sorted_box, stage, total;
@@ -367,6 +388,57 @@ extern "C" nms_status nms_fast_run(const float* boxes, const float* scores, int6
     return run_impl(boxes, scores, n, class_ids, num_classes, batch_offsets, batch, iou_thr,
                     score_thr, max_out, keep, keep_cap, counts, dev_status, workspace,
                     workspace_bytes, stream, Stamps{}, true);
+}
+
+extern "C" nms_status nms_matrix_workspace_size(int64_t n, size_t* bytes)
+{
+    if (!bytes || n < 0) return NMS_ERR_INVALID_ARG;
+    if (n > NMS_MAX_SINGLE_N) return NMS_ERR_CAPACITY;
+    *bytes = matrix_layout(n).total;
+    return NMS_OK;
+}
+
+extern "C" nms_status nms_matrix_run(const float* boxes, const float* scores, int64_t n, float sigma,
+                                     float score_thr, float decay_thr, int32_t max_out, int64_t* keep,
+                                     float* keep_scores, int64_t keep_cap, int64_t* count,
+                                     int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                                     void* stream)
+{
+    if (n < 0) return NMS_ERR_INVALID_ARG;
+    if (!(sigma > 0.0f) || std::isinf(sigma) || std::isnan(score_thr) || std::isnan(decay_thr))
+        return NMS_ERR_INVALID_ARG;
+    if (n > 0 && (!boxes || !scores || !aligned(boxes, 16))) return NMS_ERR_INVALID_ARG;
+    if (!keep || !count || keep_cap < 0) return NMS_ERR_INVALID_ARG;
+    if (n > NMS_MAX_SINGLE_N) return NMS_ERR_CAPACITY;
+    const int64_t need = max_out > 0 ? (n < max_out ? n : max_out) : n;
+    if (keep_cap < need) return NMS_ERR_CAPACITY;
+    const MatrixLayout L = matrix_layout(n);
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < L.total) return NMS_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();
+    int32_t* status = dev_status ? dev_status : at<int32_t>(workspace, L.status);
+    if (n == 0) {
+        cudaMemsetAsync(count, 0, sizeof(int64_t), st);
+        cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+        return cuda_status();
+    }
+    const bool use_thr = !(std::isinf(score_thr) && score_thr < 0);
+    int* m_count = nullptr;
+    int* cand = nullptr;
+    if (use_thr) {
+        m_count = at<int>(workspace, L.m_count);
+        cand = at<int>(workspace, L.cand);
+        launch_prefilter(scores, static_cast<int>(n), score_thr, cand, m_count, st);
+    }
+    int* perm = at<int>(workspace, L.perm);
+    float4* boxes_s = at<float4>(workspace, L.boxes_s);
+    uint64_t* keys = sort_keys_bytes(static_cast<int>(n)) ? at<uint64_t>(workspace, L.keys) : nullptr;
+    launch_sort(scores, reinterpret_cast<const float4*>(boxes), cand, m_count, static_cast<int>(n), perm, boxes_s,
+                keys, status, nullptr, 1, nullptr, nullptr, nullptr, st);
+    launch_matrix(boxes_s, scores, perm, m_count, static_cast<int>(n), sigma, decay_thr, max_out,
+                  at<unsigned>(workspace, L.omax), at<unsigned long long>(workspace, L.xmin), keep, keep_scores,
+                  count, st);
+    return cuda_status();
 }
 
 extern "C" nms_status nms_run_timed(const float* boxes, const float* scores, int64_t n,

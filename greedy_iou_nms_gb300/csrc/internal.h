@@ -80,6 +80,14 @@ void launch_graph_grid(uint32_t* edges, const unsigned* ecount, const uint64_t* 
 void launch_fast_emit(const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm, int max_out,
                       int64_t* keep, int64_t* counts, cudaStream_t st);
 
+// Matrix NMS (Gaussian decay) of the sorted boxes: zeroes its scratch, runs
+// the two tiled passes and writes the kept indices, their final scores and
+// the count.
+void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, const int* m_dev, int m_bound,
+                   float sigma, float decay_thr, int max_out, unsigned* omax_bits,
+                   unsigned long long* xmin_key, int64_t* keep, float* keep_scores, int64_t* count,
+                   cudaStream_t st);
+
 struct BatchedArgs {
     const float4* boxes;
     const float* scores;

@@ -1,0 +1,71 @@
+"""GPU parity of Matrix NMS (nms_matrix_run) with the oracle: kept indices
+and their order bit-exact, final scores within 4 binary32 ulp (the binary32
+exponential's bound), on hand-worked cases, the workloads' shapes, clusters,
+the pre-filter, max_out and thresholds."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import greedy_iou_nms_gb300 as g
+from greedy_iou_nms_gb300 import workloads as W
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    g.build()
+    g.load()
+
+
+def _check(boxes, scores, t, **kw):
+    b = torch.from_numpy(np.ascontiguousarray(boxes, np.float32)).cuda()
+    s = torch.from_numpy(np.ascontiguousarray(scores, np.float32)).cuda()
+    k, fs = g.matrix_nms(b, s, t, **kw)
+    ek, efs = oracle.matrix_nms(boxes, scores, t, **kw)
+    assert k.cpu().numpy().tolist() == ek.tolist()
+    got = fs.cpu().numpy().astype(np.float64)
+    ulp = np.spacing(np.abs(efs).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(got - efs) <= 4 * ulp + 1e-38)
+
+
+def test_hand_worked():
+    b = np.array([[0, 0, 10, 1], [3, 0, 13, 1], [6, 0, 16, 1], [0, 0, 4, 4], [0, 0, 4, 2]], np.float32)
+    s = np.array([0.9, 0.8, 0.7, 0.6, 0.5], np.float32)
+    for t in (0.0, 0.3, 0.45, 0.62):
+        _check(b, s, t)
+
+
+@pytest.mark.parametrize("name", ["single_n1000_ties", "single_n8192"])
+@pytest.mark.parametrize("t", [0.05, 0.2])
+def test_workload_shapes(name, t):
+    wl = W.make(name, 0)
+    _check(wl.boxes, wl.scores, t)
+
+
+@pytest.mark.parametrize("n", [1, 2, 127, 128, 129, 3000])
+@pytest.mark.parametrize("sigma", [0.5, 2.0])
+def test_clusters(n, sigma):
+    rng = np.random.default_rng(n)
+    k = max(n // 10, 1)
+    c = rng.uniform(0, 500, (k, 2))[rng.integers(0, k, n)] + rng.normal(0, 5, (n, 2))
+    wh = rng.uniform(10, 50, (n, 2))
+    b = np.concatenate([c - wh / 2, c + wh / 2], 1).astype(np.float32)
+    s = rng.uniform(0, 1, n).astype(np.float32)
+    _check(b, s, 0.1, sigma=sigma)
+    _check(b, s, 0.1, sigma=sigma, max_out=max(n // 7, 1))
+    _check(b, s, 0.1, sigma=sigma, score_thr=0.3)
+
+
+def test_identical_boxes_and_empty():
+    b = np.tile(np.array([[1, 1, 5, 5]], np.float32), (200, 1))
+    s = np.linspace(1.0, 0.2, 200).astype(np.float32)
+    _check(b, s, 0.05)
+    _check(b, s, float(np.float32(0.9) * np.float32(math.exp(-2.0))))
+    k, fs = g.matrix_nms(torch.zeros((0, 4), device="cuda"), torch.zeros(0, device="cuda"), 0.1)
+    assert len(k) == 0

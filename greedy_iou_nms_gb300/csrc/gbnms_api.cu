@@ -87,7 +87,7 @@ SingleLayout single_layout(int64_t n)
 }
 
 struct MatrixLayout {
-    size_t status, m_count, cand, perm, boxes_s, keys, omax, xmin, total;
+    size_t status, m_count, cand, perm, boxes_s, keys, omax, xmin, fs, kept, total;
 };
 
 MatrixLayout matrix_layout(int64_t n)
@@ -103,6 +103,8 @@ MatrixLayout matrix_layout(int64_t n)
     m.keys = L.add(sort_keys_bytes(static_cast<int>(n)));
     m.omax = L.add(4 * N);
     m.xmin = L.add(8 * N);
+    m.fs = L.add(4 * N);
+    m.kept = L.add(4 * ((N + 31) / 32 + 8));
     m.total = L.total;
     return m;
 }
@@ -436,8 +438,8 @@ extern "C" nms_status nms_matrix_run(const float* boxes, const float* scores, in
     launch_sort(scores, reinterpret_cast<const float4*>(boxes), cand, m_count, static_cast<int>(n), perm, boxes_s,
                 keys, status, nullptr, 1, nullptr, nullptr, nullptr, st);
     launch_matrix(boxes_s, scores, perm, m_count, static_cast<int>(n), sigma, decay_thr, max_out,
-                  at<unsigned>(workspace, L.omax), at<unsigned long long>(workspace, L.xmin), keep, keep_scores,
-                  count, st);
+                  at<unsigned>(workspace, L.omax), at<unsigned long long>(workspace, L.xmin),
+                  at<float>(workspace, L.fs), at<uint32_t>(workspace, L.kept), keep, keep_scores, count, st);
     return cuda_status();
 }
 

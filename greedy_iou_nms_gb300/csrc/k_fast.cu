@@ -1,4 +1,5 @@
-// Fast NMS output for one image: the boxes no earlier box suppresses.
+// Ordered output of a kept bitmap; for Fast NMS of one image, the boxes no
+// earlier box suppresses.
 //
 // "YOLOv5后处理GPU移植实战", section 2.2 稳定性增强方案: a box is suppressed
 // when a box of higher priority (higher score, or equal score and lower
@@ -19,10 +20,12 @@ constexpr int FE_THREADS = 1024;
 // One CTA: warp w owns the 32-box words [w*wpw, (w+1)*wpw); a block prefix of
 // the warps' kept counts places them, and within a word lane l writes box
 // 32w+l (coalesced perm loads and keep stores).
+// bits: 32-box words whose set bits (clear bits when `clear`) are the kept
+// boxes; fs (optional): a value per sorted box written beside each kept one.
 __global__ void __launch_bounds__(FE_THREADS)
-fast_emit_kernel(const uint32_t* __restrict__ haspred, const int* __restrict__ m_dev, int m_bound,
-                 const int* __restrict__ perm, int max_out, int64_t* __restrict__ keep,
-                 int64_t* __restrict__ counts)
+bits_emit_kernel(const uint32_t* __restrict__ bits_in, int clear, const int* __restrict__ m_dev, int m_bound,
+                 const int* __restrict__ perm, const float* __restrict__ fs, int max_out,
+                 int64_t* __restrict__ keep, float* __restrict__ keep_fs, int64_t* __restrict__ counts)
 {
     __shared__ int scratch[32];
     const int n = m_dev ? *m_dev : m_bound;
@@ -31,7 +34,7 @@ fast_emit_kernel(const uint32_t* __restrict__ haspred, const int* __restrict__ m
     const int warp = threadIdx.x >> 5;
     auto kept_word = [&](int w) {
         const uint32_t valid = (w == NW - 1 && (n & 31)) ? (1u << (n & 31)) - 1u : ~0u;
-        return ~haspred[w] & valid;
+        return (clear ? ~bits_in[w] : bits_in[w]) & valid;
     };
     const int wpw = (NW + 31) / 32;
     const int a0 = min(warp * wpw, NW), a1 = min(a0 + wpw, NW);
@@ -59,16 +62,22 @@ fast_emit_kernel(const uint32_t* __restrict__ haspred, const int* __restrict__ m
     for (int wb = a0; wb < a1 && base < cap; wb += OW) {
         uint32_t bits[OW];
         int v[OW];
+        float f[OW];
 #pragma unroll
         for (int u = 0; u < OW; ++u) {
             bits[u] = wb + u < a1 ? kept_word(wb + u) : 0u;
             const int j = 32 * (wb + u) + static_cast<int>(l);
-            v[u] = ((bits[u] >> l) & 1u) ? (perm ? perm[j] : j) : 0;
+            const bool k = (bits[u] >> l) & 1u;
+            v[u] = k ? (perm ? perm[j] : j) : 0;
+            f[u] = k && fs ? fs[j] : 0.0f;
         }
 #pragma unroll
         for (int u = 0; u < OW; ++u) {
             const int pos = base + __popc(bits[u] & below);
-            if (((bits[u] >> l) & 1u) && pos < cap) keep[pos] = v[u];
+            if (((bits[u] >> l) & 1u) && pos < cap) {
+                keep[pos] = v[u];
+                if (keep_fs) keep_fs[pos] = f[u];
+            }
             base += __popc(bits[u]);
         }
     }
@@ -78,8 +87,14 @@ fast_emit_kernel(const uint32_t* __restrict__ haspred, const int* __restrict__ m
 void launch_fast_emit(const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm, int max_out,
                       int64_t* keep, int64_t* counts, cudaStream_t st)
 {
-    fast_emit_kernel<<<1, FE_THREADS, 0, st>>>(reinterpret_cast<const uint32_t*>(haspred), m_dev, m_bound,
-                                               perm, max_out, keep, counts);
+    bits_emit_kernel<<<1, FE_THREADS, 0, st>>>(reinterpret_cast<const uint32_t*>(haspred), 1, m_dev, m_bound,
+                                               perm, nullptr, max_out, keep, nullptr, counts);
+}
+
+void launch_bits_emit(const uint32_t* bits, const int* m_dev, int m_bound, const int* perm, const float* fs,
+                      int max_out, int64_t* keep, float* keep_fs, int64_t* counts, cudaStream_t st)
+{
+    bits_emit_kernel<<<1, FE_THREADS, 0, st>>>(bits, 0, m_dev, m_bound, perm, fs, max_out, keep, keep_fs, counts);
 }
 
 }  // namespace gbnms

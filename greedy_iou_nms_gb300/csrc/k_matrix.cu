@@ -13,14 +13,16 @@
 // fathers), and only overlapping pairs (IoU > 0) need work:
 //   pass A: tiles of the upper triangle; where two boxes overlap, the exact
 //           binary32 IoU, atomically maxed into O_max of the child;
-//   pass B: the same tiles; for each overlapping pair the binary64 exponent
-//           (O_max[i]^2 - O[i][j]^2) / sigma, atomically minimised per child
-//           through an order-preserving 64-bit key;
-//   emit:   per box, s * exp(min(0, smallest exponent)) against the
-//           threshold, decided in binary32 with expf when the result is
+//   pass B: the same tiles; for each overlapping pair the binary64 numerator
+//           O_max[i]^2 - O[i][j]^2, atomically minimised per child through an
+//           order-preserving 64-bit key (dividing once per box by sigma > 0
+//           afterwards gives the smallest quotient: correctly rounded
+//           division by a positive number keeps the order);
+//   decide: per box (all SMs), s * exp(min(0, smallest exponent)) against
+//           the threshold, decided in binary32 with expf when the result is
 //           clear of the threshold by more than its error bound, in binary64
-//           otherwise; the kept boxes in score order with their final scores.
-#include <climits>
+//           otherwise, into a kept bitmap and a final-score array;
+//   emit:   the kept boxes in score order with their final scores.
 
 #include "common.cuh"
 #include "internal.h"
@@ -29,7 +31,6 @@ namespace gbnms {
 
 constexpr int MX_T = 128;             // tile rows and columns
 constexpr int MX_THREADS = 64;        // 2 warps x 2 rows per lane = 128 rows
-constexpr int ME_THREADS = 1024;
 
 // Order-preserving key of a non-NaN binary64 value (-0 below +0).
 __device__ __forceinline__ unsigned long long dkey(double x)
@@ -43,6 +44,18 @@ __device__ __forceinline__ double dkey_value(unsigned long long k)
     const unsigned long long b = (k >> 63) ? (k & 0x7fffffffffffffffull) : ~k;
     return __longlong_as_double(static_cast<long long>(b));
 }
+
+// Each warp reduces a column over its 64 rows before one atomic, and skips a
+// column no lane overlaps with one vote.
+
+// Order-preserving 32-bit key of a binary32 value (NaN not expected) and back.
+__device__ __forceinline__ unsigned fkey(float x)
+{
+    const unsigned b = __float_as_uint(x);
+    return (b >> 31) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ unsigned fkey_value(unsigned k) { return (k >> 31) ? (k & 0x7fffffffu) : ~k; }
 
 // Linear index k of the triangle of MX_T x MX_T tiles, column by column ->
 // (row tile a, column tile c), a <= c.
@@ -86,106 +99,116 @@ matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m
     }
     __syncthreads();
     const int kend = min(MX_T, n - cb);
-    auto pair = [&](int i, const float4& r, float ar, double om, int k) {
-        const int j = cb + k;
+    // Row i's overlap with column box k, if any (IoU > 0, i before j).
+    auto overlap = [&](int i, const float4& r, float ar, int k, float& o) -> bool {
         const float4 cbx = cbox[k];
         const float w = __fsub_rn(fminf(r.z, cbx.z), fmaxf(r.x, cbx.x));
         const float h = __fsub_rn(fminf(r.w, cbx.w), fmaxf(r.y, cbx.y));
-        if (w > 0.0f && h > 0.0f && i < j) {
-            const float o = iou_exact(r, ar, cbx, carea[k]);
-            if (o > 0.0f) {
-                if (PASS == 0) {
-                    atomicMax(omax_bits + j, __float_as_uint(o));
-                } else {
-                    const double od = static_cast<double>(o);
-                    const double x = __ddiv_rn(__dsub_rn(__dmul_rn(om, om), __dmul_rn(od, od)),
-                                               static_cast<double>(sigma));
-                    if (x == x) atomicMin(xmin_key + j, dkey(x));
-                }
-            }
-        }
+        if (!(w > 0.0f && h > 0.0f && i < cb + k)) return false;
+        o = iou_exact(r, ar, cbx, carea[k]);
+        return o > 0.0f;
     };
     for (int k = 0; k < kend; ++k) {
-        if (v0) pair(i0, r0, ar0, om0, k);
-        if (v1) pair(i1, r1, ar1, om1, k);
+        const float4 cbx = cbox[k];
+        const bool maybe0 = v0 && fminf(r0.z, cbx.z) > fmaxf(r0.x, cbx.x) && fminf(r0.w, cbx.w) > fmaxf(r0.y, cbx.y);
+        const bool maybe1 = v1 && fminf(r1.z, cbx.z) > fmaxf(r1.x, cbx.x) && fminf(r1.w, cbx.w) > fmaxf(r1.y, cbx.y);
+        if (!__any_sync(FULL, maybe0 || maybe1)) continue;  // no lane overlaps column k
+        float o0 = 0.0f, o1 = 0.0f;
+        const bool ov0 = maybe0 && overlap(i0, r0, ar0, k, o0);
+        const bool ov1 = maybe1 && overlap(i1, r1, ar1, k, o1);
+        const int j = cb + k;
+        if (PASS == 0) {
+            // largest overlap of the column over the warp's rows, one atomic
+            const unsigned m = max(ov0 ? __float_as_uint(o0) : 0u, ov1 ? __float_as_uint(o1) : 0u);
+            const unsigned r = __reduce_max_sync(FULL, m);
+            if (l == 0 && r) atomicMax(omax_bits + j, r);
+        } else {
+            // Smallest numerator O_max[i]^2 - O[i][j]^2 (binary64, products
+            // exact, one rounding) over the warp's rows, one atomic.  Only
+            // rows that can hold the minimum compute it in binary64: each
+            // overlapping row bounds its numerator in binary32 (three
+            // roundings, each within 2^-24 of a term of magnitude at most
+            // om^2 + o^2), the warp takes the smallest upper bound, and rows
+            // whose lower bound does not exceed it are the candidates.
+            float lo0 = INFINITY, lo1 = INFINITY, ub = INFINITY;
+            if (ov0) {
+                const float a = __fmul_rn(static_cast<float>(om0), static_cast<float>(om0)), b = __fmul_rn(o0, o0);
+                const float e = __fmul_rn(0x1p-22f, __fadd_rn(a, b)) + 0x1p-140f;
+                const float x = __fsub_rn(a, b);
+                lo0 = x - e;
+                ub = x + e;
+            }
+            if (ov1) {
+                const float a = __fmul_rn(static_cast<float>(om1), static_cast<float>(om1)), b = __fmul_rn(o1, o1);
+                const float e = __fmul_rn(0x1p-22f, __fadd_rn(a, b)) + 0x1p-140f;
+                const float x = __fsub_rn(a, b);
+                lo1 = x - e;
+                ub = fminf(ub, x + e);
+            }
+            const float best = __uint_as_float(fkey_value(__reduce_min_sync(FULL, fkey(ub))));
+            unsigned long long key = ~0ull;
+            if (ov0 && !(lo0 > best)) {
+                const double od = static_cast<double>(o0);
+                const double x = __dsub_rn(__dmul_rn(om0, om0), __dmul_rn(od, od));
+                if (x == x) key = dkey(x);
+            }
+            if (ov1 && !(lo1 > best)) {
+                const double od = static_cast<double>(o1);
+                const double x = __dsub_rn(__dmul_rn(om1, om1), __dmul_rn(od, od));
+                if (x == x) key = min(key, dkey(x));
+            }
+            const unsigned hi = __reduce_min_sync(FULL, static_cast<unsigned>(key >> 32));
+            const unsigned lo = __reduce_min_sync(FULL, static_cast<unsigned>(key >> 32) == hi
+                                                            ? static_cast<unsigned>(key) : ~0u);
+            const unsigned long long mk = (static_cast<unsigned long long>(hi) << 32) | lo;
+            if (l == 0 && mk != ~0ull) atomicMin(xmin_key + j, mk);
+        }
     }
 }
 
-// One CTA: warp w owns the 32-box words [w*wpw, (w+1)*wpw); a block prefix of
-// the kept counts places them; lane l decides box 32w+l.
-__global__ void __launch_bounds__(ME_THREADS)
-matrix_emit_kernel(const float* __restrict__ scores, const int* __restrict__ perm,
-                   const unsigned long long* __restrict__ xmin_key, const int* __restrict__ m_dev,
-                   int m_bound, float decay_thr, int max_out, int64_t* __restrict__ keep,
-                   float* __restrict__ keep_scores, int64_t* __restrict__ count)
+// One thread per sorted box: its final score and whether it stays; lane l of
+// a warp decides box 32w+l and the warp writes word w of the kept bitmap.
+__global__ void __launch_bounds__(256)
+matrix_decide_kernel(const float* __restrict__ scores, const int* __restrict__ perm,
+                     const unsigned long long* __restrict__ xmin_key, const int* __restrict__ m_dev,
+                     int m_bound, float sigma, float decay_thr, float* __restrict__ fs_out,
+                     uint32_t* __restrict__ kept)
 {
-    __shared__ int scratch[32];
     const int n = m_dev ? *m_dev : m_bound;
-    const int NW = (n + 31) / 32;
-    const unsigned l = lane_id();
-    const int warp = threadIdx.x >> 5;
-    const int wpw = (NW + 31) / 32;
-    const int a0 = min(warp * wpw, NW), a1 = min(a0 + wpw, NW);
-    // Final score of sorted box j and whether it stays (>= the threshold).
-    auto decide = [&](int j, float& fs) -> bool {
-        if (j >= n) return false;
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j - static_cast<int>(lane_id()) >= n) return;  // whole warp past the end
+    bool keep_j = false;
+    if (j < n) {
         const float s = scores[perm[j]];
         const unsigned long long k = xmin_key[j];
-        const double x = k == ~0ull ? 0.0 : fmin(dkey_value(k), 0.0);
+        // the smallest exponent is the smallest numerator over sigma (a
+        // positive divisor keeps the order of correctly rounded quotients)
+        const double x = k == ~0ull ? 0.0 : fmin(__ddiv_rn(dkey_value(k), static_cast<double>(sigma)), 0.0);
         const float x32 = static_cast<float>(x);
         const float f = __fmul_rn(s, expf(x32));
-        // |f - s exp(x)| <= |f| (2^-22 (expf, 2 ulp) + 2^-24 (1 + |x|)
-        // (product and the exponent's rounding)) + 2^-126; a margin four
-        // times that decides in binary32, anything closer in binary64.
+        // |f - s exp(x)| <= |f| (2^-22 (expf, 2 ulp) + 2^-24 (1 + |x|) (the
+        // product and the exponent's rounding)) + 2^-126; a margin four times
+        // that decides in binary32, anything closer in binary64.
         const float tol = fabsf(f) * (4.0f * (0x1p-22f + 0x1p-24f * (1.0f + fabsf(x32)))) + 0x1p-124f;
+        float fs;
         if (fabsf(f - decay_thr) > tol) {
             fs = f;
-            return !(f < decay_thr);
+            keep_j = !(f < decay_thr);
+        } else {
+            const double fd = static_cast<double>(s) * exp(x);
+            fs = static_cast<float>(fd);
+            keep_j = !(fd < static_cast<double>(decay_thr));
         }
-        const double fd = static_cast<double>(s) * exp(x);
-        fs = static_cast<float>(fd);
-        return !(fd < static_cast<double>(decay_thr));
-    };
-    int c = 0;
-    for (int w = a0; w < a1; ++w) {
-        float fs;
-        c += __popc(__ballot_sync(FULL, decide(32 * w + static_cast<int>(l), fs)));
+        fs_out[j] = fs;
     }
-    if (l == 0) scratch[warp] = c;
-    __syncthreads();
-    if (warp == 0) {
-        int v = scratch[l];
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(FULL, v, d);
-            if (static_cast<int>(l) >= d) v += y;
-        }
-        scratch[l] = v;
-    }
-    __syncthreads();
-    const int total = scratch[31];
-    const int cap = max_out > 0 ? max_out : INT_MAX;
-    int base = warp ? scratch[warp - 1] : 0;
-    const uint32_t below = (1u << l) - 1u;
-    for (int w = a0; w < a1 && base < cap; ++w) {
-        const int j = 32 * w + static_cast<int>(l);
-        float fs = 0.0f;
-        const bool kept = decide(j, fs);
-        const uint32_t bits = __ballot_sync(FULL, kept);
-        const int pos = base + __popc(bits & below);
-        if (kept && pos < cap) {
-            keep[pos] = perm[j];
-            if (keep_scores) keep_scores[pos] = fs;
-        }
-        base += __popc(bits);
-    }
-    if (threadIdx.x == 0) count[0] = total < cap ? total : cap;
+    const uint32_t w = __ballot_sync(FULL, keep_j);
+    if (lane_id() == 0) kept[j >> 5] = w;
 }
 
 void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, const int* m_dev, int m_bound,
                    float sigma, float decay_thr, int max_out, unsigned* omax_bits,
-                   unsigned long long* xmin_key, int64_t* keep, float* keep_scores, int64_t* count,
-                   cudaStream_t st)
+                   unsigned long long* xmin_key, float* fs, uint32_t* kept, int64_t* keep, float* keep_scores,
+                   int64_t* count, cudaStream_t st)
 {
     cudaMemsetAsync(omax_bits, 0, sizeof(unsigned) * static_cast<size_t>(m_bound), st);
     cudaMemsetAsync(xmin_key, 0xff, sizeof(unsigned long long) * static_cast<size_t>(m_bound), st);
@@ -197,8 +220,9 @@ void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, 
         matrix_pass_kernel<1><<<static_cast<unsigned>(tiles), MX_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, sigma,
                                                                                  omax_bits, xmin_key);
     }
-    matrix_emit_kernel<<<1, ME_THREADS, 0, st>>>(scores, perm, xmin_key, m_dev, m_bound, decay_thr, max_out,
-                                                 keep, keep_scores, count);
+    matrix_decide_kernel<<<(m_bound + 255) / 256, 256, 0, st>>>(scores, perm, xmin_key, m_dev, m_bound, sigma,
+                                                                decay_thr, fs, kept);
+    launch_bits_emit(kept, m_dev, m_bound, perm, fs, max_out, keep, keep_scores, count, st);
 }
 
 }  // namespace gbnms

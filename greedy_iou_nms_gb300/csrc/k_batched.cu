@@ -216,7 +216,7 @@ seg_small_kernel(const float4* __restrict__ boxes, const float* __restrict__ sco
 
 // ------------------------------------------------------- large segments (> 64)
 //
-// One CTA per segment, no mask in memory: the segment is ranked by counting,
+// A CTA per segment in turn, no mask in memory: the segment is ranked by counting,
 // then walked tile by tile.  Each 64-candidate tile is first tested against
 // every box kept so far (all threads), then its own 64x64 block is built (in
 // column view) and resolved by warp 0.  Exact greedy; cost O(kept * m) IoUs on one SM.
@@ -237,115 +237,142 @@ seg_large_kernel(const float4* __restrict__ boxes, const float* __restrict__ sco
     __shared__ uint64_t s_kept;
     __shared__ int s_nk;
 
-    const int s = blockIdx.x;
     if (!*ok) return;
-    const int lo = seg_off[s];
-    const int m = seg_off[s + 1] - lo;
-    if (m <= 64) return;
+    // A few CTAs per SM take the segments in turn and skip the small ones
+    // (the warp kernel's).
+    for (int s = blockIdx.x; s < S; s += gridDim.x) {
+        const int lo = seg_off[s];
+        const int m = seg_off[s + 1] - lo;
+        if (m <= 64) continue;
+        __syncthreads();  // the previous segment's shared state is no longer read
 
-    // Rank each candidate of the segment by counting smaller keys.
-    for (int e = threadIdx.x; e < m; e += blockDim.x) {
-        const int x = cand[lo + e];
-        const uint64_t k = order_key(scores[x], x);
-        int r = 0;
-        for (int f = 0; f < m; ++f) {
-            const int y = cand[lo + f];
-            r += order_key(scores[y], y) < k;
+        // Rank each candidate of the segment by counting smaller keys.
+        for (int e = threadIdx.x; e < m; e += blockDim.x) {
+            const int x = cand[lo + e];
+            const uint64_t k = order_key(scores[x], x);
+            int r = 0;
+            for (int f = 0; f < m; ++f) {
+                const int y = cand[lo + f];
+                r += order_key(scores[y], y) < k;
+            }
+            sorted_key[lo + r] = k;
+            sorted_box[lo + r] = boxes[x];
         }
-        sorted_key[lo + r] = k;
-        sorted_box[lo + r] = boxes[x];
-    }
-    __syncthreads();
+        __syncthreads();
 
-    int nk = 0;  // kept so far (uniform)
-    const int cap = max_out > 0 ? max_out : m;
-    const unsigned l = lane_id();
-    for (int t0 = 0; t0 < m && nk < cap; t0 += 64) {
-        const int tn = min(64, m - t0);
-        if (threadIdx.x == 0) s_removed = 0;
-        if (threadIdx.x < 64) diag[threadIdx.x] = 0;
-        __syncthreads();
-        // (a) candidates of the tile against every kept box (Fast NMS: every
-        //     earlier box of the segment).
-        {
-            const int cidx = threadIdx.x & 63;
-            const int slice = threadIdx.x >> 6;
-            const int nslice = blockDim.x >> 6;
-            if (cidx < tn) {
-                const float4 cbx = sorted_box[lo + t0 + cidx];
-                const float car = box_area(cbx);
-                bool hit = false;
-                if (fast) {
-                    for (int k = slice; k < t0 && !hit; k += nslice) {
-                        const float4 kb = sorted_box[lo + k];
-                        hit = suppress_exact(kb, box_area(kb), cbx, car, thr);
+        int nk = 0;  // kept so far (uniform)
+        const int cap = max_out > 0 ? max_out : m;
+        const unsigned l = lane_id();
+        for (int t0 = 0; t0 < m && nk < cap; t0 += 64) {
+            const int tn = min(64, m - t0);
+            if (threadIdx.x == 0) s_removed = 0;
+            if (threadIdx.x < 64) diag[threadIdx.x] = 0;
+            __syncthreads();
+            // (a) candidates of the tile against every kept box (Fast NMS: every
+            //     earlier box of the segment).
+            {
+                const int cidx = threadIdx.x & 63;
+                const int slice = threadIdx.x >> 6;
+                const int nslice = blockDim.x >> 6;
+                if (cidx < tn) {
+                    const float4 cbx = sorted_box[lo + t0 + cidx];
+                    const float car = box_area(cbx);
+                    bool hit = false;
+                    if (fast) {
+                        for (int k = slice; k < t0 && !hit; k += nslice) {
+                            const float4 kb = sorted_box[lo + k];
+                            hit = suppress_exact(kb, box_area(kb), cbx, car, thr);
+                        }
                     }
-                }
-                for (int k = slice; !fast && k < nk && !hit; k += nslice) {
-                    float4 kb;
-                    float ka;
-                    if (k < SL_CACHE) {
-                        kb = kbox[k];
-                        ka = karea[k];
-                    } else {
-                        // Beyond the cache: kept_key holds the kept box's sorted position.
-                        kb = sorted_box[lo + static_cast<int>(kept_key[lo + k])];
-                        ka = box_area(kb);
+                    for (int k = slice; !fast && k < nk && !hit; k += nslice) {
+                        float4 kb;
+                        float ka;
+                        if (k < SL_CACHE) {
+                            kb = kbox[k];
+                            ka = karea[k];
+                        } else {
+                            // Beyond the cache: kept_key holds the kept box's sorted position.
+                            kb = sorted_box[lo + static_cast<int>(kept_key[lo + k])];
+                            ka = box_area(kb);
+                        }
+                        hit = suppress_exact(kb, ka, cbx, car, thr);
                     }
-                    hit = suppress_exact(kb, ka, cbx, car, thr);
+                    if (hit) atomicOr(&s_removed, 1ull << cidx);
                 }
-                if (hit) atomicOr(&s_removed, 1ull << cidx);
             }
-        }
-        // (b) the tile's own 64x64 block in column view: bit i of diag[j] set iff
-        //     i < j and i suppresses j.
-        for (int q = threadIdx.x; q < 64 * 64; q += blockDim.x) {
-            const int i = q >> 6, j = q & 63;
-            if (i < j && j < tn) {
-                const float4 bi = sorted_box[lo + t0 + i];
-                const float4 bj = sorted_box[lo + t0 + j];
-                if (suppress_exact(bi, box_area(bi), bj, box_area(bj), thr))
-                    atomicOr(reinterpret_cast<unsigned long long*>(&diag[j]), 1ull << i);
+            // (b) the tile's own 64x64 block in column view: bit i of diag[j] set iff
+            //     i < j and i suppresses j.
+            for (int q = threadIdx.x; q < 64 * 64; q += blockDim.x) {
+                const int i = q >> 6, j = q & 63;
+                if (i < j && j < tn) {
+                    const float4 bi = sorted_box[lo + t0 + i];
+                    const float4 bj = sorted_box[lo + t0 + j];
+                    if (suppress_exact(bi, box_area(bi), bj, box_area(bj), thr))
+                        atomicOr(reinterpret_cast<unsigned long long*>(&diag[j]), 1ull << i);
+                }
             }
+            __syncthreads();
+            if (threadIdx.x < 32) {
+                const uint64_t valid = tn >= 64 ? ~0ull : ((1ull << tn) - 1ull);
+                const uint64_t cand = valid & ~static_cast<uint64_t>(s_removed);
+                uint64_t K = fast ? cand & ballot64(diag[l] == 0, diag[l + 32] == 0)
+                                  : resolve_tile_col(cand, diag[l], diag[l + 32]);
+                const int room = cap - nk;
+                if (__popcll(K) > room) K = lowest_bits(K, room);
+                if (l == 0) { s_kept = K; s_nk = __popcll(K); }
+            }
+            __syncthreads();
+            const uint64_t K = s_kept;
+            // Append the tile's kept boxes in order: cache + record the sorted position.
+            if (threadIdx.x < 64 && ((K >> threadIdx.x) & 1ull)) {
+                const int r = nk + __popcll(K & ((1ull << threadIdx.x) - 1ull));
+                const float4 b = sorted_box[lo + t0 + threadIdx.x];
+                if (r < SL_CACHE) { kbox[r] = b; karea[r] = box_area(b); }
+                // Temporarily store the sorted position; replaced by the key at the end.
+                kept_key[lo + r] = static_cast<uint64_t>(t0 + threadIdx.x);
+            }
+            nk += s_nk;
+            __syncthreads();
         }
+        // Replace the recorded sorted positions by the (score key, index) keys.
         __syncthreads();
-        if (threadIdx.x < 32) {
-            const uint64_t valid = tn >= 64 ? ~0ull : ((1ull << tn) - 1ull);
-            const uint64_t cand = valid & ~static_cast<uint64_t>(s_removed);
-            uint64_t K = fast ? cand & ballot64(diag[l] == 0, diag[l + 32] == 0)
-                              : resolve_tile_col(cand, diag[l], diag[l + 32]);
-            const int room = cap - nk;
-            if (__popcll(K) > room) K = lowest_bits(K, room);
-            if (l == 0) { s_kept = K; s_nk = __popcll(K); }
+        for (int r = threadIdx.x; r < nk; r += blockDim.x) {
+            const int pos = static_cast<int>(kept_key[lo + r]);
+            kept_key[lo + r] = sorted_key[lo + pos];
         }
-        __syncthreads();
-        const uint64_t K = s_kept;
-        // Append the tile's kept boxes in order: cache + record the sorted position.
-        if (threadIdx.x < 64 && ((K >> threadIdx.x) & 1ull)) {
-            const int r = nk + __popcll(K & ((1ull << threadIdx.x) - 1ull));
-            const float4 b = sorted_box[lo + t0 + threadIdx.x];
-            if (r < SL_CACHE) { kbox[r] = b; karea[r] = box_area(b); }
-            // Temporarily store the sorted position; replaced by the key at the end.
-            kept_key[lo + r] = static_cast<uint64_t>(t0 + threadIdx.x);
-        }
-        nk += s_nk;
-        __syncthreads();
+        if (threadIdx.x == 0) kept_cnt[s] = nk;
     }
-    // Replace the recorded sorted positions by the (score key, index) keys.
-    for (int r = threadIdx.x; r < nk; r += blockDim.x) {
-        const int pos = static_cast<int>(kept_key[lo + r]);
-        kept_key[lo + r] = sorted_key[lo + pos];
-    }
-    if (threadIdx.x == 0) kept_cnt[s] = nk;
 }
 
 // ------------------------------------------------------------ per-image merge
 //
 // One CTA per image: gather the kept keys of the image's segments into a
-// contiguous run, rank each by counting smaller keys, and write the index of
-// every key ranked below the cap at its rank.
+// contiguous run, sort them (a bitonic sort in shared memory up to MG_CHUNK
+// keys, ranking by counting beyond) and write the indices of the first `cap`
+// in order.
 constexpr int MG_THREADS = 1024;
 constexpr int MG_CHUNK = 4096;
+
+// Ascending bitonic sort of the np (a power of two) unique keys in s (the
+// padding keys, all ones, sort last), by the CTA.
+__device__ __forceinline__ void bitonic_sort(uint64_t* s, int np)
+{
+    for (int k = 2; k <= np; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < np; i += blockDim.x) {
+                const int p = i ^ j;
+                if (p > i) {
+                    const uint64_t x = s[i], y = s[p];
+                    if ((x > y) == ((i & k) == 0)) {
+                        s[i] = y;
+                        s[p] = x;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
 
 __global__ void __launch_bounds__(MG_THREADS)
 merge_kernel(const int* __restrict__ seg_off, const int* __restrict__ kept_cnt,
@@ -354,6 +381,7 @@ merge_kernel(const int* __restrict__ seg_off, const int* __restrict__ kept_cnt,
              int64_t* __restrict__ keep, int64_t* __restrict__ counts)
 {
     __shared__ uint64_t ck[MG_CHUNK];
+    __shared__ int seg_pre[MG_THREADS];
     __shared__ int s_tot;
     __shared__ int warp_sums[32];
     const int b = blockIdx.x;
@@ -363,6 +391,60 @@ merge_kernel(const int* __restrict__ seg_off, const int* __restrict__ kept_cnt,
     }
     const int s0 = b * C;
     const int base = seg_off[s0];  // the image's segments are contiguous
+    const int64_t out0 = max_out > 0 ? static_cast<int64_t>(b) * max_out : off ? off[b] : 0;
+    if (C <= MG_THREADS) {
+        // Kept counts of the image's segments and their exclusive prefix in
+        // shared memory; with at most MG_CHUNK keys each thread fetches keys
+        // straight into the sort buffer (its segment by binary search).
+        const int v = static_cast<int>(threadIdx.x) < C ? kept_cnt[s0 + threadIdx.x] : 0;
+        int x = v;
+        const unsigned ll = lane_id();
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(FULL, x, d);
+            if (static_cast<int>(ll) >= d) x += y;
+        }
+        const int w = threadIdx.x >> 5;
+        if (ll == 31) warp_sums[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            int ws = static_cast<int>(ll) < static_cast<int>(blockDim.x >> 5) ? warp_sums[ll] : 0;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(FULL, ws, d);
+                if (static_cast<int>(ll) >= d) ws += y;
+            }
+            warp_sums[ll] = ws;
+        }
+        __syncthreads();
+        const int pre = (w > 0 ? warp_sums[w - 1] : 0) + x - v;
+        if (static_cast<int>(threadIdx.x) < C) seg_pre[threadIdx.x] = pre;
+        const int tot = warp_sums[31];
+        __syncthreads();
+        if (tot <= MG_CHUNK) {
+            const int cap = max_out > 0 ? min(max_out, tot) : tot;
+            int np = 1;
+            while (np < tot) np <<= 1;
+            for (int e = threadIdx.x; e < np; e += blockDim.x) {
+                uint64_t k = ~0ull;
+                if (e < tot) {
+                    int lo = 0, hi = C;  // last segment with prefix <= e
+                    while (hi - lo > 1) {
+                        const int mid = (lo + hi) >> 1;
+                        if (seg_pre[mid] <= e) lo = mid; else hi = mid;
+                    }
+                    k = kept_key[seg_off[s0 + lo] + (e - seg_pre[lo])];
+                }
+                ck[e] = k;
+            }
+            __syncthreads();
+            bitonic_sort(ck, np);
+            for (int r = threadIdx.x; r < cap; r += blockDim.x)
+                keep[out0 + r] = static_cast<int64_t>(ck[r] & 0xffffffffu);
+            if (threadIdx.x == 0) counts[b] = cap;
+            return;
+        }
+    }
     // Exclusive scan of kept counts over the image's segments, then copy.
     if (threadIdx.x == 0) s_tot = 0;
     __syncthreads();
@@ -400,8 +482,19 @@ merge_kernel(const int* __restrict__ seg_off, const int* __restrict__ kept_cnt,
     }
     const int tot = s_tot;
     const int cap = max_out > 0 ? min(max_out, tot) : tot;
-    const int64_t out0 = max_out > 0 ? static_cast<int64_t>(b) * max_out : off ? off[b] : 0;
-    // Rank by counting (keys are unique), staged through shared memory.
+    if (tot <= MG_CHUNK) {
+        int np = 1;
+        while (np < tot) np <<= 1;
+        __syncthreads();
+        for (int e = threadIdx.x; e < np; e += blockDim.x) ck[e] = e < tot ? stage[base + e] : ~0ull;
+        __syncthreads();
+        bitonic_sort(ck, np);
+        for (int r = threadIdx.x; r < cap; r += blockDim.x) keep[out0 + r] = static_cast<int64_t>(ck[r] & 0xffffffffu);
+        if (threadIdx.x == 0) counts[b] = cap;
+        return;
+    }
+    // More than MG_CHUNK keys: rank by counting (keys are unique), staged
+    // through shared memory.
     for (int e0 = 0; e0 < tot; e0 += blockDim.x) {
         const int e = e0 + threadIdx.x;
         const uint64_t k = e < tot ? stage[base + e] : ~0ull;
@@ -436,7 +529,11 @@ void launch_batched(const BatchedArgs& a, cudaStream_t st, const Stamps& stamps)
     stamps.record(1, st);
     seg_small_kernel<<<(S + SS_WARPS - 1) / SS_WARPS, SS_WARPS * 32, 0, st>>>(
         a.boxes, a.scores, a.seg_off, a.cand, S, a.ok, a.thr, a.max_out, a.fast, a.kept_key, a.kept_cnt);
-    seg_large_kernel<<<S, SL_THREADS, 0, st>>>(a.boxes, a.scores, a.seg_off, a.cand, S, a.ok, a.thr,
+    int sms = 0, dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int large_grid = max(1, min(S, 2 * (sms > 0 ? sms : 1)));
+    seg_large_kernel<<<large_grid, SL_THREADS, 0, st>>>(a.boxes, a.scores, a.seg_off, a.cand, S, a.ok, a.thr,
                                                a.max_out, a.fast, a.sorted_key, a.sorted_box, a.kept_key,
                                                a.kept_cnt);
     stamps.record(2, st);

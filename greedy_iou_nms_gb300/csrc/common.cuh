@@ -78,19 +78,16 @@ __device__ __forceinline__ bool well_formed(float4 b, float area)
            fabsf(b.z) <= 0x1p100f && fabsf(b.w) <= 0x1p100f;
 }
 
-// Threshold constants of the division-free test (computed on the host).
+// Threshold constant of the mask kernel's filter (computed on the host).
 //   With s = area_a + area_b and a = inter as binary32 values, for well-formed
-//   boxes and 2^-20 <= thr <= 2^20, and k*s the exact real product:
-//     a >  k_hi * s  implies  RN(a / RN(s - a)) >  thr   (suppress)
-//     a <= k_lo * s  implies  RN(a / RN(s - a)) <= thr   (keep)
-//   and any pair between the two bounds is decided by the exact division.
+//   boxes and 2^-20 <= thr <= 2^20, and k_lo*s the exact real product:
+//     a <= k_lo * s  implies  RN(a / RN(s - a)) <= thr   (no suppression)
+//   so every suppressing pair has a > k_lo * s.
 //   Proof sketch: q = a/(s-a) and the two roundings put the canonical IoU in
-//   q(1 +- 2^-23); q > T2 = thr(1+2^-21) <=> a > s T2/(1+T2), and k_hi exceeds
-//   that ratio by a factor 1+2^-22 (likewise k_lo is below T1/(1+T1), T1 =
-//   thr(1-2^-21)), so the rounded IoU lands strictly on the proven side.
+//   q(1 +- 2^-23); q <= T1 = thr(1-2^-21) <=> a <= s T1/(1+T1), and k_lo is
+//   below that ratio by a factor 1-2^-22, so the rounded IoU cannot exceed thr.
 struct ThrParams {
     float thr;     // the binary32 threshold
-    float k_hi;    // >= (T2/(1+T2)) (1+2^-22), T2 = thr (1+2^-21)
     float k_lo;    // <= (T1/(1+T1)) (1-2^-22), T1 = thr (1-2^-21)
     int fast_ok;   // thr within [2^-20, 2^20]
 };

@@ -135,7 +135,6 @@ BatchedLayout batched_layout(int64_t n, int64_t S)
     return b;
 }
 
-float next_up(float x) { return std::nextafter(x, INFINITY); }
 float next_down(float x) { return std::nextafter(x, -INFINITY); }
 
 // Constants of the division-free test; the bounds are proved in common.cuh.
@@ -145,17 +144,12 @@ ThrParams make_thr(float thr)
     p.thr = thr;
     const double t = thr;
     p.fast_ok = (t >= 0x1p-20 && t <= 0x1p20) ? 1 : 0;
-    p.k_hi = 1.0f;
     p.k_lo = 0.0f;
     if (p.fast_ok) {
-        const double T2 = t * (1.0 + 0x1p-21), T1 = t * (1.0 - 0x1p-21);
-        const double k2 = T2 / (1.0 + T2) * (1.0 + 0x1p-22);
+        const double T1 = t * (1.0 - 0x1p-21);
         const double k1 = T1 / (1.0 + T1) * (1.0 - 0x1p-22);
-        float f2 = static_cast<float>(k2);
-        if (static_cast<double>(f2) < k2) f2 = next_up(f2);
         float f1 = static_cast<float>(k1);
         if (static_cast<double>(f1) > k1) f1 = next_down(f1);
-        p.k_hi = f2;
         p.k_lo = f1;
     }
     return p;

@@ -11,8 +11,8 @@
 //
 // GB300 shape: a CTA computes a tile of M_WARPS*64 rows x MT columns.  Each
 // lane holds two row boxes in registers and walks the MT staged column boxes
-// (broadcast shared-memory reads), so a row's words of the tile are built in
-// registers and written with 16-byte stores.  The
+// (broadcast shared-memory reads of 4 columns at a time), so a row's words of
+// the tile are built in registers and written with 16-byte stores.  The
 // triangle of tiles is enumerated column by column.  Each row also records,
 // one bit per 256-column chunk, which of its chunks hold a set bit, and the
 // 64x64 blocks within BAND_L tiles of the diagonal are also written in column
@@ -20,10 +20,17 @@
 // decide a tile with lane-local tests.  When asked, every set bit is also
 // appended to a list of (row, column) pairs, the sparse form of the same
 // graph, as long as the list has room, and every column with a set bit is
-// marked in a bitmap of boxes that have an earlier neighbour.  Pairs are
-// decided by the
-// division-free test of common.cuh and, for the rare pair it leaves open and
-// for tiles holding a malformed box, by the exact binary32 division.
+// marked in a bitmap of boxes that have an earlier neighbour.
+//
+// Deciding a pair takes two steps.  A filter, run on every pair, sets a
+// "maybe" bit for a superset of the suppressing pairs: it bounds the
+// intersection from above with packed two-column binary32 arithmetic (one
+// instruction for two columns) and compares it against k_lo times the area
+// sum, a comparison the canonical IoU > thr implies (see ThrParams).  Only
+// the maybe bits, a small fraction of the pairs, are then decided by the
+// canonical IoU itself, so every stored bit is exactly the definition's.
+// Tiles holding a malformed box, and thresholds outside the filter's range,
+// send every pair of the tile to the canonical test.
 #include "common.cuh"
 #include "internal.h"
 
@@ -57,100 +64,144 @@ __device__ __forceinline__ float4 pad_box() { return make_float4(3e38f, 3e38f, 3
 __device__ __forceinline__ void tri_coords(long long k, int& a, int& c)
 {
     constexpr long long r = MT / MR;
-    long long cc = static_cast<long long>((sqrt(8.0 * static_cast<double>(k) / r + 1.0) - 1.0) * 0.5);
+    // A binary32 estimate (no binary64 on the hot path), made exact by the
+    // integer corrections.
+    long long cc = static_cast<long long>((sqrtf(8.0f * static_cast<float>(k) / r + 1.0f) - 1.0f) * 0.5f);
+    if (cc < 0) cc = 0;
     while (r * (cc + 1) * (cc + 2) / 2 <= k) ++cc;
-    while (r * cc * (cc + 1) / 2 > k) --cc;
+    while (cc > 0 && r * cc * (cc + 1) / 2 > k) --cc;
     c = static_cast<int>(cc);
     a = static_cast<int>(k - r * cc * (cc + 1) / 2);
 }
 static_assert(MT % MR == 0, "a column tile spans a whole number of row tiles");
 
-// Sign bit of RN(k*s - a): set iff the exact k*s - a is negative, i.e.
-// a > k*s (the product inside a fused multiply-add is not rounded).
-__device__ __forceinline__ uint32_t sign_above(float k, float s, float a)
+// Column boxes of a tile in shared memory, one array per coordinate, with
+// x1 and y2 negated so that every difference below is a sum.
+struct ColsSoA {
+    float* nx1;  // -x1
+    float* x2;
+    float* y1;
+    float* ny2;  // -y2
+    float* ar;   // canonical area
+};
+
+__device__ __forceinline__ float4 col_box(const ColsSoA& C, int t)
 {
-    return __float_as_uint(__fmaf_rn(k, s, -a));
+    return make_float4(-C.nx1[t], C.y1[t], C.x2[t], -C.ny2[t]);
 }
 
-// One pair of the division-free test, shifted into the accumulators: `yes`
-// takes the decision bit and `maybe` the "not surely below" bit.  For
-// well-formed boxes and the constants of ThrParams, a > k_hi*s proves
-// suppression and a <= k_lo*s proves no suppression (common.cuh); a pair with
-// maybe and not yes is left to the exact division.  The test runs on doubled
-// values: w + |w| = 2 max(w, 0) exactly, so a2 = (w + |w|) h = 2 a with h
-// unclamped (when h <= 0 the product is <= 0 and both tests say no, as the
-// canonical clamped intersection 0 would), compared against the doubled
-// constants khi2 = 2 k_hi and klo2 = 2 k_lo.  Doubling is exact here: well-
-// formed areas are at most 2^58, and an intersection small enough to round
-// differently (below 2^-125) is far below k_lo * s >= 2^-78 either way.
-__device__ __forceinline__ void pair_fast(float4 r, float ar, float4 c, float ac, float khi2, float klo2,
-                                          uint32_t& yes, uint32_t& maybe)
+// A row box spread over register pairs (both halves equal) for the packed
+// instructions.
+struct RowF2 {
+    float2 z;   // (x2, x2)
+    float2 nx;  // (-x1, -x1)
+    float2 nw;  // (-y2, -y2)
+    float2 y;   // (y1, y1)
+    float2 ar;  // (area, area)
+};
+
+__device__ __forceinline__ float2 dup2(float v) { return make_float2(v, v); }
+
+__device__ __forceinline__ RowF2 make_row(float4 b, float ar)
 {
-    const float w = __fsub_rn(fminf(r.z, c.z), fmaxf(r.x, c.x));
-    const float w2 = __fadd_rn(w, fabsf(w));
-    const float h = __fsub_rn(fminf(r.w, c.w), fmaxf(r.y, c.y));
-    const float a2 = __fmul_rn(w2, h);
-    const float s = __fadd_rn(ar, ac);
-    yes = __funnelshift_l(sign_above(khi2, s, a2), yes, 1);
-    maybe = __funnelshift_l(sign_above(klo2, s, a2), maybe, 1);
+    RowF2 r;
+    r.z = dup2(b.z);
+    r.nx = dup2(-b.x);
+    r.nw = dup2(-b.w);
+    r.y = dup2(b.y);
+    r.ar = dup2(ar);
+    return r;
 }
 
-// Both rows of a lane against 32 staged columns (cb, ca 16-byte aligned),
-// highest column first so that bit k ends up meaning column k; one shared
-// load of a column box feeds both rows, one 16-byte load brings 4 areas.
-__device__ __forceinline__ void half_fast(const float4* __restrict__ cb, const float* __restrict__ ca,
-                                          float4 r0, float ar0, float4 r1, float ar1, float khi2,
-                                          float klo2, uint32_t& y0, uint32_t& m0, uint32_t& y1,
-                                          uint32_t& m1)
+// The filter for one row and two adjacent columns, shifted into `acc`
+// (second column first, so that bit k ends up meaning column k when the
+// columns are walked from the highest down).
+//   width bound  w' = min(RN(r.x2 - c.x1), RN(c.x2 - r.x1)) >= the canonical
+//                RN(min(x2) - max(x1)) (both operands of each difference are
+//                bounds and rounding is monotone); w2 = w' + |w'| = 2 max(w', 0)
+//   height bound h' likewise, computed negated: -h' = max(RN(c.y1 - r.y2),
+//                RN(r.y1 - c.y2))
+//   maybe        RN(2 k_lo * s - w2 h') < 0, s = RN(area_r + area_c); exact
+//                sign of the fused product.
+// For well-formed boxes a canonical suppression has inter > k_lo * s with
+// inter > 0, hence w2 h' >= 2 inter > 2 k_lo s and the maybe bit is set.  A
+// negative h' gives a non-positive product (no bit), as the clamped canonical
+// height 0 would.
+__device__ __forceinline__ void maybe2(const RowF2& r, float2 cnx1, float2 cx2, float2 cy1, float2 cny2, float2 car,
+                                       float2 klo2, uint32_t& acc)
 {
-    const float4* ca4 = reinterpret_cast<const float4*>(ca);
+    const float2 ax = __fadd2_rn(r.z, cnx1);  // r.x2 - c.x1
+    const float2 bx = __fadd2_rn(cx2, r.nx);  // c.x2 - r.x1
+    float2 w2;
+    w2.x = fminf(ax.x, bx.x);
+    w2.y = fminf(ax.y, bx.y);
+    w2.x = __fadd_rn(w2.x, fabsf(w2.x));
+    w2.y = __fadd_rn(w2.y, fabsf(w2.y));
+    const float2 ay = __fadd2_rn(cy1, r.nw);  // c.y1 - r.y2
+    const float2 by = __fadd2_rn(r.y, cny2);  // r.y1 - c.y2
+    float2 nh;
+    nh.x = fmaxf(ay.x, by.x);
+    nh.y = fmaxf(ay.y, by.y);
+    const float2 s = __fadd2_rn(r.ar, car);
+    const float2 na2 = __fmul2_rn(w2, nh);
+    const float2 t = __ffma2_rn(klo2, s, na2);
+    acc = __funnelshift_l(__float_as_uint(t.y), acc, 1);
+    acc = __funnelshift_l(__float_as_uint(t.x), acc, 1);
+}
+
+// Both rows of a lane against 32 staged columns starting at `base` (a
+// multiple of 4): one 16-byte shared load per coordinate brings 4 columns,
+// shared by both rows.
+__device__ __forceinline__ void maybe_half(const ColsSoA& C, int base, const RowF2& r0, const RowF2& r1,
+                                           float2 klo2, uint32_t& m0, uint32_t& m1)
+{
 #pragma unroll kMaskUnroll
     for (int g = 7; g >= 0; --g) {
-        const float4 a4 = ca4[g];
-        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-        for (int e = 3; e >= 0; --e) {
-            const float4 c = cb[4 * g + e];
-            pair_fast(r0, ar0, c, av[e], khi2, klo2, y0, m0);
-            pair_fast(r1, ar1, c, av[e], khi2, klo2, y1, m1);
-        }
+        const int o = base + 4 * g;
+        const float4 a = *reinterpret_cast<const float4*>(C.nx1 + o);
+        const float4 b = *reinterpret_cast<const float4*>(C.x2 + o);
+        const float4 c = *reinterpret_cast<const float4*>(C.y1 + o);
+        const float4 d = *reinterpret_cast<const float4*>(C.ny2 + o);
+        const float4 e = *reinterpret_cast<const float4*>(C.ar + o);
+        const float2 ahi = make_float2(a.z, a.w), bhi = make_float2(b.z, b.w), chi = make_float2(c.z, c.w),
+                     dhi = make_float2(d.z, d.w), ehi = make_float2(e.z, e.w);
+        const float2 alo = make_float2(a.x, a.y), blo = make_float2(b.x, b.y), clo = make_float2(c.x, c.y),
+                     dlo = make_float2(d.x, d.y), elo = make_float2(e.x, e.y);
+        maybe2(r0, ahi, bhi, chi, dhi, ehi, klo2, m0);
+        maybe2(r1, ahi, bhi, chi, dhi, ehi, klo2, m1);
+        maybe2(r0, alo, blo, clo, dlo, elo, klo2, m0);
+        maybe2(r1, alo, blo, clo, dlo, elo, klo2, m1);
     }
 }
 
-template <bool FAST>
-__device__ __forceinline__ void tile_rows(const float4* __restrict__ cbox, const float* __restrict__ carea,
-                                          float4 r0, float ar0, float4 r1, float ar1,
-                                          const ThrParams& p, uint64_t (&w0)[NQ], uint64_t (&w1)[NQ],
-                                          bool& unsure)
+// The maybe words of two rows over the tile's NQ words.
+__device__ __forceinline__ void maybe_rows(const ColsSoA& C, const RowF2& r0, const RowF2& r1, float klo,
+                                           uint64_t (&w0)[NQ], uint64_t (&w1)[NQ])
 {
+    const float2 klo2 = dup2(__fmul_rn(2.0f, klo));
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
         uint32_t lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
-        if (FAST) {
-            uint32_t ml0 = 0, mh0 = 0, ml1 = 0, mh1 = 0;
-            const float khi2 = __fmul_rn(2.0f, p.k_hi), klo2 = __fmul_rn(2.0f, p.k_lo);
-            half_fast(cbox + q * 64, carea + q * 64, r0, ar0, r1, ar1, khi2, klo2, lo0, ml0, lo1, ml1);
-            half_fast(cbox + q * 64 + 32, carea + q * 64 + 32, r0, ar0, r1, ar1, khi2, klo2, hi0, mh0,
-                      hi1, mh1);
-            unsure |= ((ml0 & ~lo0) | (mh0 & ~hi0) | (ml1 & ~lo1) | (mh1 & ~hi1)) != 0;
-        } else {
-#pragma unroll 8
-            for (int k = 0; k < 32; ++k) {
-                const float4 c = cbox[q * 64 + k];
-                const float ac = carea[q * 64 + k];
-                lo0 |= static_cast<uint32_t>(suppress_exact(r0, ar0, c, ac, p.thr)) << k;
-                lo1 |= static_cast<uint32_t>(suppress_exact(r1, ar1, c, ac, p.thr)) << k;
-            }
-#pragma unroll 8
-            for (int k = 0; k < 32; ++k) {
-                const float4 c = cbox[q * 64 + 32 + k];
-                const float ac = carea[q * 64 + 32 + k];
-                hi0 |= static_cast<uint32_t>(suppress_exact(r0, ar0, c, ac, p.thr)) << k;
-                hi1 |= static_cast<uint32_t>(suppress_exact(r1, ar1, c, ac, p.thr)) << k;
-            }
-        }
+        maybe_half(C, q * 64, r0, r1, klo2, lo0, lo1);
+        maybe_half(C, q * 64 + 32, r0, r1, klo2, hi0, hi1);
         w0[q] = (static_cast<uint64_t>(hi0) << 32) | lo0;
         w1[q] = (static_cast<uint64_t>(hi1) << 32) | lo1;
+    }
+}
+
+// Keeps the bits of `w` whose pair passes the canonical test.
+__device__ __forceinline__ void verify_words(const ColsSoA& C, float4 b, float ar, float thr, uint64_t (&w)[NQ])
+{
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        uint64_t x = w[q], keep = 0;
+        while (x) {
+            const int bit = __ffsll(static_cast<long long>(x)) - 1;
+            x &= x - 1;
+            const int t = 64 * q + bit;
+            if (suppress_exact(b, ar, col_box(C, t), C.ar[t], thr)) keep |= 1ull << bit;
+        }
+        w[q] = keep;
     }
 }
 
@@ -222,8 +273,12 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
                 unsigned long long* __restrict__ haspred, int limit, long long tile_off,
                 const int* __restrict__ done)
 {
-    __shared__ float4 cbox[MT];
-    __shared__ __align__(16) float carea[MT];
+    __shared__ __align__(16) float s_nx1[MT];
+    __shared__ __align__(16) float s_x2[MT];
+    __shared__ __align__(16) float s_y1[MT];
+    __shared__ __align__(16) float s_ny2[MT];
+    __shared__ __align__(16) float s_ar[MT];
+    const ColsSoA C{s_nx1, s_x2, s_y1, s_ny2, s_ar};
 
     if (done && *done) return;  // an earlier stage already reached max_out
     const int n = min(m_dev ? *m_dev : m_bound, limit);
@@ -236,42 +291,38 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
     const int rbase = a * MR;
     bool ok = true;
     for (int t = threadIdx.x; t < MT; t += M_THREADS) {
-        int j = cb + t;
-        float4 b = j < n ? boxes_s[j] : pad_box();
-        float ar = j < n ? box_area(b) : 0.0f;
+        const int j = cb + t;
+        const float4 b = j < n ? boxes_s[j] : pad_box();
+        const float ar = j < n ? box_area(b) : 0.0f;
         if (j < n) ok &= well_formed(b, ar);
-        cbox[t] = b;
-        carea[t] = ar;
+        s_nx1[t] = -b.x;
+        s_x2[t] = b.z;
+        s_y1[t] = b.y;
+        s_ny2[t] = -b.w;
+        s_ar[t] = ar;
     }
     const unsigned l = lane_id();
     const int wp = threadIdx.x >> 5;
     const int i0 = rbase + wp * 64 + l;
     const int i1 = i0 + 32;
-    float4 r0 = i0 < n ? boxes_s[i0] : pad_box();
-    float4 r1 = i1 < n ? boxes_s[i1] : pad_box();
-    float ar0 = i0 < n ? box_area(r0) : 0.0f;
-    float ar1 = i1 < n ? box_area(r1) : 0.0f;
-    if (i0 < n) ok &= well_formed(r0, ar0);
-    if (i1 < n) ok &= well_formed(r1, ar1);
+    const float4 b0 = i0 < n ? boxes_s[i0] : pad_box();
+    const float4 b1 = i1 < n ? boxes_s[i1] : pad_box();
+    const float ar0 = i0 < n ? box_area(b0) : 0.0f;
+    const float ar1 = i1 < n ? box_area(b1) : 0.0f;
+    if (i0 < n) ok &= well_formed(b0, ar0);
+    if (i1 < n) ok &= well_formed(b1, ar1);
     const bool fast = __syncthreads_and(ok) && p.fast_ok;
 
     uint64_t w0[NQ], w1[NQ];
-    bool unsure = false;
     if (fast) {
-        tile_rows<true>(cbox, carea, r0, ar0, r1, ar1, p, w0, w1, unsure);
-        if (__any_sync(FULL, unsure)) {
-            uint64_t e0[NQ], e1[NQ];
-            bool dummy = false;
-            if (unsure) {
-                tile_rows<false>(cbox, carea, r0, ar0, r1, ar1, p, e0, e1, dummy);
-#pragma unroll
-                for (int q = 0; q < NQ; ++q) { w0[q] = e0[q]; w1[q] = e1[q]; }
-            }
-        }
+        maybe_rows(C, make_row(b0, ar0), make_row(b1, ar1), p.k_lo, w0, w1);
     } else {
-        tile_rows<false>(cbox, carea, r0, ar0, r1, ar1, p, w0, w1, unsure);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            w0[q] = ~0ull;
+            w1[q] = ~0ull;
+        }
     }
-
     if (rbase + MR > cb) {  // the tile meets the diagonal
         clip_words(w0, i0, cb, n);
         clip_words(w1, i1, cb, n);
@@ -279,6 +330,17 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
         clip_words(w0, -1, cb, n);
         clip_words(w1, -1, cb, n);
     }
+    if (i0 >= n) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) w0[q] = 0;
+    }
+    if (i1 >= n) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) w1[q] = 0;
+    }
+    verify_words(C, b0, ar0, p.thr, w0);
+    verify_words(C, b1, ar1, p.thr, w1);
+
     // Column view of the blocks within BAND_L tiles of the diagonal (64-row
     // tile R of this warp, 64-column tile C = 4c+q): a warp transpose of the
     // block's final words leaves columns l and l+32 in lane l.

@@ -137,6 +137,57 @@ def test_mask_parity_integer_grid_ties():
                 assert np.array_equal(m[i, w0:ref.shape[1]], ref[i, w0:])
 
 
+def _canonical_iou32(a, b):
+    """Canonical binary32 IoU of two boxes, used only to pick thresholds."""
+    f = np.float32
+    xx1, yy1 = max(f(a[0]), f(b[0])), max(f(a[1]), f(b[1]))
+    xx2, yy2 = min(f(a[2]), f(b[2])), min(f(a[3]), f(b[3]))
+    w, h = max(f(xx2 - xx1), f(0)), max(f(yy2 - yy1), f(0))
+    inter = f(w * h)
+    aa, ab = f(f(a[2] - a[0]) * f(a[3] - a[1])), f(f(b[2] - b[0]) * f(b[3] - b[1]))
+    return f(inter / f(f(aa + ab) - inter))
+
+
+def _mask_equal(b, thr):
+    m = g.iou_mask(torch.from_numpy(np.ascontiguousarray(b, np.float32)).cuda(), thr).cpu().numpy().view(np.uint64)
+    ref = oracle.mask(b, thr)
+    for i in range(b.shape[0]):
+        w0 = i // 64
+        assert np.array_equal(m[i, w0:ref.shape[1]], ref[i, w0:]), (i, thr)
+
+
+def test_mask_parity_nested_and_threshold_ulps():
+    # Boxes nested in one axis or both (the filter's width and height bounds
+    # are loosest there), with thresholds equal to, and one ulp either side
+    # of, IoUs that occur in the set: every such pair sits on the strict
+    # comparison's edge and must come out exactly as the definition says.
+    rng = np.random.default_rng(21)
+    n = 700
+    big = np.array([0, 0, 200, 200], np.float32)
+    c = rng.uniform(10, 190, (n, 2))
+    wh = rng.uniform(1, 200, (n, 2))
+    b = np.concatenate([c - wh / 2, c + wh / 2], 1).astype(np.float32)
+    b[::5] = big
+    b[1::7, 0], b[1::7, 2] = 0, 200          # spans the big box in x
+    b[2::9, 1], b[2::9, 3] = 0, 200          # spans it in y
+    picks = [_canonical_iou32(b[i], b[j]) for i, j in rng.integers(0, n, (40, 2)) if i != j]
+    picks = [p for p in picks if 0.01 < p < 0.99][:8]
+    assert picks
+    for p in picks:
+        for thr in (p, np.nextafter(p, np.float32(0)), np.nextafter(p, np.float32(1))):
+            _mask_equal(b, float(thr))
+
+
+@pytest.mark.parametrize("scale", [2.0 ** -40, 2.0 ** -20, 2.0 ** 20, 2.0 ** 40])
+def test_mask_parity_scaled_coordinates(scale):
+    # The same boxes at scales where every area is well inside the filter's
+    # range (2^-20, 2^20) and where areas leave it (2^-40, 2^40: the tiles
+    # then take the canonical test for every pair).
+    b = (_sorted_random(500, 33, span=120.0) * np.float32(scale)).astype(np.float32)
+    for thr in (0.5, 0.3):
+        _mask_equal(b, thr)
+
+
 # ------------------------------------------------------- workload parity
 
 SINGLE = ["single_n1000_ties", "single_n8192", "single_n32768_maxout1000"]

@@ -98,10 +98,11 @@ __device__ __forceinline__ void emit_sorted(uint64_t k, int r, int m, const floa
 // shared memory (order inside a bucket does not matter) and then counts, for
 // each of its BR_CAND candidates, the smaller keys of its own bucket: the
 // work per CTA is linear in the chunk plus the candidates' bucket sizes.
-// The bucket of a key is its score key's place in the [lo, hi] range of the
-// chunk's finite scores, scaled by a fixed-point multiply (score keys beyond
-// the range, i.e. +inf, -inf and NaN, go to the end buckets); it is monotone
-// in the key, so buckets come in key order and equal scores share one.
+// The bucket of a key is its score key's offset in the [lo, hi] range of the
+// chunk's finite scores, shifted right so that the range fits the buckets
+// (score keys beyond the range, i.e. +inf, -inf and NaN, go to the end
+// buckets); it is monotone in the key, so buckets come in key order and
+// equal scores share one.
 // With one chunk the kernel writes perm and boxes_s, otherwise the chunk's
 // sorted keys for the merge levels.  It also clears what the mask kernel
 // accumulates into: the status, the pair counter, the bitmap of boxes with an
@@ -111,15 +112,17 @@ constexpr int BR_CAND = 128;                   // candidates ranked per CTA
 constexpr int BR_BUCKETS = 4096;
 constexpr int BR_KPT = MS_CHUNK / BR_THREADS;  // chunk keys per thread
 
+constexpr int BR_SOLO = 64;                    // buckets a single lane scans alone
+
 struct BucketMap {
     uint32_t lo, hi;  // score-key range of the finite scores
-    uint64_t mul;     // floor((BR_BUCKETS-1) * 2^32 / (hi - lo + 1))
+    int shift;        // (hi - lo) >> shift < BR_BUCKETS
     __device__ __forceinline__ int operator()(uint64_t key) const
     {
         const uint32_t k = static_cast<uint32_t>(key >> 32);
         if (k < lo) return 0;
         if (k > hi) return BR_BUCKETS - 1;
-        return static_cast<int>((static_cast<uint64_t>(k - lo) * mul) >> 32);
+        return static_cast<int>((k - lo) >> shift);
     }
 };
 
@@ -168,21 +171,25 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
         }
         ckey[tid] = key;
     }
+    // The chunk's keys, BR_KPT per thread: all index loads, then all score
+    // loads, so that each round of loads is in flight at once.
     uint64_t k[BR_KPT];
-    uint32_t lo = 0xffffffffu, hi = 0u;
+    int xs[BR_KPT];
+    float sc[BR_KPT];
 #pragma unroll
     for (int u = 0; u < BR_KPT; ++u) {
         const int t = tid + u * BR_THREADS;
-        if (t < cn) {
-            const int x = cand ? cand[c0 + t] : c0 + t;
-            const float sc = scores[x];
-            k[u] = order_key(sc, static_cast<uint32_t>(x));
-            if (isfinite(sc)) {
-                lo = min(lo, static_cast<uint32_t>(k[u] >> 32));
-                hi = max(hi, static_cast<uint32_t>(k[u] >> 32));
-            }
-        } else {
-            k[u] = MS_PAD;
+        xs[u] = t < cn ? (cand ? cand[c0 + t] : c0 + t) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < BR_KPT; ++u) sc[u] = xs[u] >= 0 ? scores[xs[u]] : 0.0f;
+    uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+    for (int u = 0; u < BR_KPT; ++u) {
+        k[u] = xs[u] >= 0 ? order_key(sc[u], static_cast<uint32_t>(xs[u])) : MS_PAD;
+        if (xs[u] >= 0 && isfinite(sc[u])) {
+            lo = min(lo, static_cast<uint32_t>(k[u] >> 32));
+            hi = max(hi, static_cast<uint32_t>(k[u] >> 32));
         }
     }
     const unsigned l = lane_id();
@@ -194,14 +201,14 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
     }
     __syncthreads();
     BucketMap bm;
-    bm.lo = 0xffffffffu;
-    bm.hi = 0u;
-    for (int w = 0; w < BR_THREADS / 32; ++w) {
-        bm.lo = min(bm.lo, wlo[w]);
-        bm.hi = max(bm.hi, whi[w]);
-    }
+    constexpr int NWARP = BR_THREADS / 32;
+    bm.lo = __reduce_min_sync(FULL, l < NWARP ? wlo[l] : 0xffffffffu);
+    bm.hi = __reduce_max_sync(FULL, l < NWARP ? whi[l] : 0u);
     if (bm.lo > bm.hi) bm.lo = bm.hi = 0u;  // no finite score
-    bm.mul = (static_cast<uint64_t>(BR_BUCKETS - 1) << 32) / (static_cast<uint64_t>(bm.hi - bm.lo) + 1);
+    // Smallest shift with (hi - lo) >> shift < BR_BUCKETS (a power of two).
+    static_assert((BR_BUCKETS & (BR_BUCKETS - 1)) == 0, "power-of-two bucket count");
+    const int span_bits = 32 - __clz(static_cast<int>(bm.hi - bm.lo));
+    bm.shift = max(0, span_bits - (31 - __clz(BR_BUCKETS)));
 #pragma unroll
     for (int u = 0; u < BR_KPT; ++u)
         if (k[u] != MS_PAD) atomicAdd(&start[bm(k[u])], 1);
@@ -222,8 +229,7 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
     }
     if (l == 31) wsum[tid >> 5] = x;
     __syncthreads();
-    int before = x - run;
-    for (int w = 0; w < (tid >> 5); ++w) before += wsum[w];
+    int before = x - run + __reduce_add_sync(FULL, static_cast<int>(l) < (tid >> 5) ? wsum[l] : 0);
 #pragma unroll
     for (int u = 0; u < BPT; ++u) {
         start[tid * BPT + u] = before;
@@ -232,25 +238,46 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
     }
     if (tid == BR_THREADS - 1) start[BR_BUCKETS] = before;
     __syncthreads();
+    // Slots in bucket order: every atomic first, then the stores.
+    int slot[BR_KPT];
+#pragma unroll
+    for (int u = 0; u < BR_KPT; ++u) slot[u] = k[u] != MS_PAD ? atomicAdd(&cur[bm(k[u])], 1) : -1;
 #pragma unroll
     for (int u = 0; u < BR_KPT; ++u)
-        if (k[u] != MS_PAD) list[atomicAdd(&cur[bm(k[u])], 1)] = k[u];
+        if (slot[u] >= 0) list[slot[u]] = k[u];
     __syncthreads();
-    // Rank: warp w takes candidates w, w + 16, ...; lanes split the bucket.
-    const int warp = tid >> 5;
-    for (int e = warp; e < BR_CAND; e += BR_THREADS / 32) {
-        const uint64_t key = ckey[e];
-        int r = q0 + e - c0;                   // pads keep their place at the end
+    // Rank: thread e < BR_CAND counts the smaller keys of its candidate's
+    // bucket alone; a bucket of more than BR_SOLO keys is counted by the
+    // candidate's whole warp, lanes splitting it.
+    if (tid < BR_CAND) {
+        const uint64_t key = ckey[tid];
+        int r = q0 + tid - c0;                 // pads keep their place at the end
+        bool big = false;
+        int s0 = 0, s1 = 0;
         if (key != MS_PAD) {
             const int b = bm(key);
-            const int s0 = start[b], s1 = start[b + 1];
-            int c = 0;
-            for (int i = s0 + static_cast<int>(l); i < s1; i += 32) c += list[i] < key;
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1) c += __shfl_xor_sync(FULL, c, d);
-            r = s0 + c;
+            s0 = start[b];
+            s1 = start[b + 1];
+            big = s1 - s0 > BR_SOLO;
+            if (!big) {
+                int c = 0;
+#pragma unroll 4
+                for (int i = s0; i < s1; ++i) c += list[i] < key;
+                r = s0 + c;
+            }
         }
-        if (l == 0) crank[e] = r;
+        unsigned todo = __ballot_sync(FULL, big);
+        while (todo) {
+            const int src = __ffs(todo) - 1;
+            todo &= todo - 1;
+            const uint64_t kk = __shfl_sync(FULL, key, src);
+            const int b0 = __shfl_sync(FULL, s0, src), b1 = __shfl_sync(FULL, s1, src);
+            int c = 0;
+            for (int i = b0 + static_cast<int>(l); i < b1; i += 32) c += list[i] < kk;
+            c = __reduce_add_sync(FULL, c);
+            if (static_cast<int>(l) == src) r = b0 + c;
+        }
+        crank[tid] = r;
     }
     __syncthreads();
     if (tid < BR_CAND && q0 + tid < c0 + MS_CHUNK) {

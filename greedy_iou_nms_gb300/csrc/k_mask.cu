@@ -9,13 +9,15 @@
 // (Part 2)", section "Optimization 1: tile the IoU matrix": coordinates loaded
 // once per tile and reused by every row.
 //
-// GB300 shape: a CTA computes a tile of M_WARPS*64 rows x MT columns.  Each
-// lane holds two row boxes in registers and walks the MT staged column boxes
-// (broadcast shared-memory reads of 4 columns at a time), so a row's words of
-// the tile are built in registers and written with 16-byte stores.  The
-// triangle of tiles is enumerated column by column.  Each row also records,
-// one bit per 256-column chunk, which of its chunks hold a set bit, and the
-// 64x64 blocks within BAND_L tiles of the diagonal are also written in column
+// GB300 shape: the triangle is cut into units of 64 rows x MT columns, each
+// taken by one warp on its own (its column boxes staged in its own slice of
+// shared memory, so no CTA barrier), enumerated column by column; warps
+// stride over the units when the grid is smaller than the units.  Each lane holds two row boxes in
+// registers and walks the MT staged column boxes (broadcast shared-memory
+// reads of 4 columns at a time), so a row's words of the unit are built in
+// registers and written with 16-byte stores.  Each row also records, one bit
+// per 256-column chunk, which of its chunks hold a set bit, and the 64x64
+// blocks within BAND_L tiles of the diagonal are also written in column
 // view; the resolve uses the first to skip all-zero chunks and the second to
 // decide a tile with lane-local tests.  When asked, every set bit is also
 // appended to a list of (row, column) pairs, the sparse form of the same
@@ -35,7 +37,10 @@
 #include "internal.h"
 
 #ifndef GBNMS_MASK_WARPS
-#define GBNMS_MASK_WARPS 2
+#define GBNMS_MASK_WARPS 4
+#endif
+#ifndef GBNMS_MASK_CTAS_PER_SM
+#define GBNMS_MASK_CTAS_PER_SM 8
 #endif
 #ifndef GBNMS_MASK_UNROLL
 #define GBNMS_MASK_UNROLL 2
@@ -50,20 +55,19 @@ constexpr int MT = GBNMS_MASK_MT;  // tile width (columns)
 constexpr int NQ = MT / 64;        // 64-bit words of a row per tile
 static_assert(MT == MASK_TILE_W, "the tile width the host stages by");
 static_assert(NQ == 1 || NQ == 2 || NQ == 4, "tile width of 64, 128 or 256 columns");
-constexpr int M_WARPS = GBNMS_MASK_WARPS;  // warps of 64 rows per tile
-constexpr int MR = M_WARPS * 64;  // tile height (rows)
+constexpr int M_WARPS = GBNMS_MASK_WARPS;  // warps per CTA, each on its own units
 constexpr int M_THREADS = M_WARPS * 32;
+constexpr int M_CTAS_PER_SM = GBNMS_MASK_CTAS_PER_SM;  // resident CTAs per SM the grid is sized for
 
 // Far-away zero-area box used to pad ragged tiles: overlaps nothing.
 __device__ __forceinline__ float4 pad_box() { return make_float4(3e38f, 3e38f, 3e38f, 3e38f); }
 
-// Linear index k of the tile triangle -> (row tile a, column tile c).  With
-// r = MT/MR row tiles per column tile, column tile c meets row tiles
-// a = 0 .. r(c+1)-1, so the tiles of columns before c number r c(c+1)/2;
-// enumeration is column by column.
+// Linear index k of the unit triangle -> (64-row tile a, MT-column tile c).
+// Column tile c meets row tiles a = 0 .. NQ(c+1)-1, so the units of columns
+// before c number NQ c(c+1)/2; enumeration is column by column.
 __device__ __forceinline__ void tri_coords(long long k, int& a, int& c)
 {
-    constexpr long long r = MT / MR;
+    constexpr long long r = NQ;
     // A binary32 estimate (no binary64 on the hot path), made exact by the
     // integer corrections.
     long long cc = static_cast<long long>((sqrtf(8.0f * static_cast<float>(k) / r + 1.0f) - 1.0f) * 0.5f);
@@ -73,7 +77,6 @@ __device__ __forceinline__ void tri_coords(long long k, int& a, int& c)
     c = static_cast<int>(cc);
     a = static_cast<int>(k - r * cc * (cc + 1) / 2);
 }
-static_assert(MT % MR == 0, "a column tile spans a whole number of row tiles");
 
 // Column boxes of a tile in shared memory, one array per coordinate, with
 // x1 and y2 negated so that every difference below is a sum.
@@ -265,87 +268,21 @@ __device__ __forceinline__ void store_words(uint64_t* dst, const uint64_t (&w)[N
     }
 }
 
-__global__ void __launch_bounds__(M_THREADS)
-iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_dev, int m_bound,
-                ThrParams p, uint64_t* __restrict__ mask, int64_t ldw,
-                unsigned long long* __restrict__ rowbits, int NB, ulonglong2* __restrict__ band,
-                uint32_t* __restrict__ edges, unsigned* __restrict__ ecount, unsigned ecap,
-                unsigned long long* __restrict__ haspred, int limit, long long tile_off,
-                const int* __restrict__ done)
+// The unit's outputs from its final words: the band blocks in column view,
+// the mask words, the per-row chunk bits, the neighbour bitmap and the pair
+// list.
+__device__ __forceinline__ void store_unit(const uint64_t (&w0)[NQ], const uint64_t (&w1)[NQ], int i0, int i1,
+                                           int a, int cb, int n, unsigned l, uint64_t* __restrict__ mask,
+                                           int64_t ldw, unsigned long long* __restrict__ rowbits, int NB,
+                                           ulonglong2* __restrict__ band, uint32_t* __restrict__ edges,
+                                           unsigned* __restrict__ ecount, unsigned ecap,
+                                           unsigned long long* __restrict__ haspred)
 {
-    __shared__ __align__(16) float s_nx1[MT];
-    __shared__ __align__(16) float s_x2[MT];
-    __shared__ __align__(16) float s_y1[MT];
-    __shared__ __align__(16) float s_ny2[MT];
-    __shared__ __align__(16) float s_ar[MT];
-    const ColsSoA C{s_nx1, s_x2, s_y1, s_ny2, s_ar};
-
-    if (done && *done) return;  // an earlier stage already reached max_out
-    const int n = min(m_dev ? *m_dev : m_bound, limit);
-    int a, c;
-    tri_coords(blockIdx.x + tile_off, a, c);
-    const int T = (n + MT - 1) / MT;
-    if (c >= T || a * MR >= n) return;  // beyond the device-side count
-
-    const int cb = c * MT;
-    const int rbase = a * MR;
-    bool ok = true;
-    for (int t = threadIdx.x; t < MT; t += M_THREADS) {
-        const int j = cb + t;
-        const float4 b = j < n ? boxes_s[j] : pad_box();
-        const float ar = j < n ? box_area(b) : 0.0f;
-        if (j < n) ok &= well_formed(b, ar);
-        s_nx1[t] = -b.x;
-        s_x2[t] = b.z;
-        s_y1[t] = b.y;
-        s_ny2[t] = -b.w;
-        s_ar[t] = ar;
-    }
-    const unsigned l = lane_id();
-    const int wp = threadIdx.x >> 5;
-    const int i0 = rbase + wp * 64 + l;
-    const int i1 = i0 + 32;
-    const float4 b0 = i0 < n ? boxes_s[i0] : pad_box();
-    const float4 b1 = i1 < n ? boxes_s[i1] : pad_box();
-    const float ar0 = i0 < n ? box_area(b0) : 0.0f;
-    const float ar1 = i1 < n ? box_area(b1) : 0.0f;
-    if (i0 < n) ok &= well_formed(b0, ar0);
-    if (i1 < n) ok &= well_formed(b1, ar1);
-    const bool fast = __syncthreads_and(ok) && p.fast_ok;
-
-    uint64_t w0[NQ], w1[NQ];
-    if (fast) {
-        maybe_rows(C, make_row(b0, ar0), make_row(b1, ar1), p.k_lo, w0, w1);
-    } else {
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-            w0[q] = ~0ull;
-            w1[q] = ~0ull;
-        }
-    }
-    if (rbase + MR > cb) {  // the tile meets the diagonal
-        clip_words(w0, i0, cb, n);
-        clip_words(w1, i1, cb, n);
-    } else {
-        clip_words(w0, -1, cb, n);
-        clip_words(w1, -1, cb, n);
-    }
-    if (i0 >= n) {
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) w0[q] = 0;
-    }
-    if (i1 >= n) {
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) w1[q] = 0;
-    }
-    verify_words(C, b0, ar0, p.thr, w0);
-    verify_words(C, b1, ar1, p.thr, w1);
-
     // Column view of the blocks within BAND_L tiles of the diagonal (64-row
-    // tile R of this warp, 64-column tile C = 4c+q): a warp transpose of the
-    // block's final words leaves columns l and l+32 in lane l.
+    // tile R = a of the unit, 64-column tile C = NQ c + q): a warp transpose of
+    // the block's final words leaves columns l and l+32 in lane l.
     if (band) {
-        const int R = rbase / 64 + wp;
+        const int R = a;
         const int T64 = (n + 63) / 64;
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
@@ -407,10 +344,89 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
     }
 }
 
+__global__ void __launch_bounds__(M_THREADS, M_CTAS_PER_SM)
+iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_dev, int m_bound,
+                ThrParams p, uint64_t* __restrict__ mask, int64_t ldw,
+                unsigned long long* __restrict__ rowbits, int NB, ulonglong2* __restrict__ band,
+                uint32_t* __restrict__ edges, unsigned* __restrict__ ecount, unsigned ecap,
+                unsigned long long* __restrict__ haspred, int limit, long long u_begin, long long u_end,
+                const int* __restrict__ done)
+{
+    __shared__ __align__(16) float s_cols[M_WARPS][5][MT];  // per warp: -x1, x2, y1, -y2, area
+
+    if (done && *done) return;  // an earlier stage already reached max_out
+    const int n = min(m_dev ? *m_dev : m_bound, limit);
+    const int T = (n + MT - 1) / MT;
+    const unsigned l = lane_id();
+    const int wp = threadIdx.x >> 5;
+    const ColsSoA C{s_cols[wp][0], s_cols[wp][1], s_cols[wp][2], s_cols[wp][3], s_cols[wp][4]};
+    const long long stride = static_cast<long long>(gridDim.x) * M_WARPS;
+    for (long long u = u_begin + static_cast<long long>(blockIdx.x) * M_WARPS + wp; u < u_end; u += stride) {
+        int a, c;
+        tri_coords(u, a, c);
+        if (c >= T || a * 64 >= n) continue;  // beyond the device-side count (warp-uniform)
+        const int cb = c * MT;
+        const int rbase = a * 64;
+        __syncwarp();  // the previous unit's reads of the staged columns are done
+        bool ok = true;
+#pragma unroll
+        for (int t = static_cast<int>(l); t < MT; t += 32) {
+            const int j = cb + t;
+            const float4 b = j < n ? boxes_s[j] : pad_box();
+            const float ar = j < n ? box_area(b) : 0.0f;
+            if (j < n) ok &= well_formed(b, ar);
+            C.nx1[t] = -b.x;
+            C.x2[t] = b.z;
+            C.y1[t] = b.y;
+            C.ny2[t] = -b.w;
+            C.ar[t] = ar;
+        }
+        const int i0 = rbase + static_cast<int>(l);
+        const int i1 = i0 + 32;
+        const float4 b0 = i0 < n ? boxes_s[i0] : pad_box();
+        const float4 b1 = i1 < n ? boxes_s[i1] : pad_box();
+        const float ar0 = i0 < n ? box_area(b0) : 0.0f;
+        const float ar1 = i1 < n ? box_area(b1) : 0.0f;
+        if (i0 < n) ok &= well_formed(b0, ar0);
+        if (i1 < n) ok &= well_formed(b1, ar1);
+        const bool fast = __all_sync(FULL, ok) && p.fast_ok;
+        __syncwarp();  // the staged columns are visible to the whole warp
+
+        uint64_t w0[NQ], w1[NQ];
+        if (fast) {
+            maybe_rows(C, make_row(b0, ar0), make_row(b1, ar1), p.k_lo, w0, w1);
+        } else {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                w0[q] = ~0ull;
+                w1[q] = ~0ull;
+            }
+        }
+        if (rbase + 64 > cb) {  // the unit meets the diagonal
+            clip_words(w0, i0, cb, n);
+            clip_words(w1, i1, cb, n);
+        } else if (cb + MT > n) {  // ragged last column tile
+            clip_words(w0, -1, cb, n);
+            clip_words(w1, -1, cb, n);
+        }
+        if (i0 >= n) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) w0[q] = 0;
+        }
+        if (i1 >= n) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) w1[q] = 0;
+        }
+        verify_words(C, b0, ar0, p.thr, w0);
+        verify_words(C, b1, ar1, p.thr, w1);
+        store_unit(w0, w1, i0, i1, a, cb, n, l, mask, ldw, rowbits, NB, band, edges, ecount, ecap, haspred);
+    }
+}
+
 int64_t mask_tiles(int64_t n)
 {
     int64_t T = (n + MT - 1) / MT;
-    return (MT / MR) * T * (T + 1) / 2;
+    return NQ * T * (T + 1) / 2;
 }
 
 void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const ThrParams& p,
@@ -418,19 +434,25 @@ void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const
                      uint32_t* edges, unsigned* ecount, unsigned ecap, uint64_t* haspred,
                      cudaStream_t st, int col_lo, int col_hi, const int* done)
 {
-    // The triangle's tiles whose columns lie in [col_lo, col_hi) (multiples of
+    // The triangle's units whose columns lie in [col_lo, col_hi) (multiples of
     // the tile width, or col_hi = m_bound), all rows above them.
     const int hi = min(col_hi, m_bound);
-    const int64_t t0 = mask_tiles(col_lo), t1 = mask_tiles(hi);
-    const int64_t tiles = t1 - t0;
-    if (tiles <= 0) return;
-    iou_mask_kernel<<<static_cast<unsigned>(tiles), M_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, p,
-                                                                        mask, ldw,
-                                                                        reinterpret_cast<unsigned long long*>(rowbits), NB,
-                                                                        reinterpret_cast<ulonglong2*>(band),
-                                                                        edges, ecount, ecap,
-                                                                        reinterpret_cast<unsigned long long*>(haspred),
-                                                                        hi, t0, done);
+    const int64_t u0 = mask_tiles(col_lo), u1 = mask_tiles(hi);
+    if (u1 <= u0) return;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+    // A unit per warp, the hardware balancing the CTAs; a launch that may find
+    // its work already done (a later max_out stage) strides over the units
+    // with one resident wave instead, so that finding the flag set costs a
+    // few CTAs per SM.
+    int64_t grid = (u1 - u0 + M_WARPS - 1) / M_WARPS;
+    if (done) grid = min(grid, static_cast<int64_t>(sms) * M_CTAS_PER_SM);
+    iou_mask_kernel<<<static_cast<unsigned>(grid), M_THREADS, 0, st>>>(
+        boxes_s, m_dev, m_bound, p, mask, ldw, reinterpret_cast<unsigned long long*>(rowbits), NB,
+        reinterpret_cast<ulonglong2*>(band), edges, ecount, ecap, reinterpret_cast<unsigned long long*>(haspred),
+        hi, u0, u1, done);
 }
 
 }  // namespace gbnms

@@ -36,21 +36,23 @@ __global__ void prefilter_kernel(const float* __restrict__ scores, int n, float 
 //
 // Chunks of MS_CHUNK keys are sorted by bucketed ranking (below), every
 // chunk by many CTAs.  Larger inputs then merge pairs of sorted runs in
-// global memory, one launch per doubling: a CTA produces one MS_CHUNK tile of
+// global memory, one launch per doubling: a CTA produces one ML_TILE tile of
 // the output, loads the two input ranges it covers (found by a 32-way
 // search) into shared memory, and each thread merges MS_P outputs after a
 // merge-path search for its first one.  Shared memory keeps one spare slot
 // per MS_P keys so that lanes MS_P keys apart do not share banks.  The last
 // step writes the permutation and the gathered boxes instead of keys.
-constexpr int MS_THREADS = 1024;
-constexpr int MS_P = 8;                        // keys per thread
-constexpr int MS_CHUNK = MS_THREADS * MS_P;    // keys per CTA
+constexpr int MS_P = 8;                        // keys merged per thread
+constexpr int MS_CHUNK = 8192;                 // keys of a bucket-ranked chunk
 constexpr uint64_t MS_PAD = ~0ull;
 
 // Shared-memory slot of logical key i: one spare slot after every MS_P keys,
 // so the lanes of a warp, MS_P keys apart, hit different banks.
 __device__ __forceinline__ int sk(int i) { return i + i / MS_P; }
-constexpr int MS_SLOTS = MS_CHUNK + MS_CHUNK / MS_P;
+constexpr int ML_THREADS = 256;                // merge level: threads per CTA
+constexpr int ML_TILE = ML_THREADS * MS_P;     // merge level: outputs per CTA
+constexpr int ML_SLOTS = ML_TILE + ML_TILE / MS_P;
+static_assert(MS_CHUNK % ML_TILE == 0, "merge tiles split the runs evenly");
 
 // Number of A elements among the first d outputs of merge(A, B) (A first on
 // ties), A = keys [a0, a0+na) and B = keys [b0, b0+nb) of the skewed buffer.
@@ -315,33 +317,33 @@ __device__ __forceinline__ int merge_path_warp(const uint64_t* __restrict__ A, i
 
 // One doubling of the global merge: pairs of sorted runs of `run` keys from
 // keys_in into keys_out (or, when `last`, into perm and boxes_s).  CTA b makes
-// output tile [b*MS_CHUNK, (b+1)*MS_CHUNK).
-__global__ void __launch_bounds__(MS_THREADS, 1)
+// output tile [b*ML_TILE, (b+1)*ML_TILE).
+__global__ void __launch_bounds__(ML_THREADS)
 merge_level_kernel(const uint64_t* __restrict__ keys_in, uint64_t* __restrict__ keys_out, int run,
                    int last, const int* __restrict__ m_dev, int m_bound,
                    const float4* __restrict__ boxes, int* __restrict__ perm,
                    float4* __restrict__ boxes_s)
 {
-    extern __shared__ __align__(16) uint64_t buf[];  // MS_CHUNK keys, A part then B part, skewed
+    __shared__ __align__(16) uint64_t buf[ML_SLOTS];  // ML_TILE keys, A part then B part, skewed
     __shared__ int split[2];
     const int tid = threadIdx.x;
-    const int o0 = blockIdx.x * MS_CHUNK;
+    const int o0 = blockIdx.x * ML_TILE;
     const int pb = o0 & ~(2 * run - 1);       // start of the merge pair
     const uint64_t* A = keys_in + pb;
     const uint64_t* B = A + run;
     const int warp = tid >> 5;
     if (warp < 2) {
-        const int d = o0 - pb + warp * MS_CHUNK;
+        const int d = o0 - pb + warp * ML_TILE;
         const int i = merge_path_warp(A, run, B, run, d);
         if (lane_id() == 0) split[warp] = i;
     }
     __syncthreads();
     const int d0 = o0 - pb;
     const int ia = split[0], ib = split[1];
-    const int ja = d0 - ia, jb = d0 + MS_CHUNK - ib;
+    const int ja = d0 - ia, jb = d0 + ML_TILE - ib;
     const int na = ib - ia, nb = jb - ja;
-    for (int t = tid; t < na; t += MS_THREADS) buf[sk(t)] = A[ia + t];
-    for (int t = tid; t < nb; t += MS_THREADS) buf[sk(na + t)] = B[ja + t];
+    for (int t = tid; t < na; t += ML_THREADS) buf[sk(t)] = A[ia + t];
+    for (int t = tid; t < nb; t += ML_THREADS) buf[sk(na + t)] = B[ja + t];
     __syncthreads();
     uint64_t k[MS_P];
     merge_p(buf, 0, na, na, nb, tid * MS_P, k);
@@ -393,12 +395,11 @@ void launch_sort(const float* scores, const float4* boxes, const int* cand, cons
     bucket_rank_kernel<<<dim3(per_chunk > 0 ? per_chunk : 1, chunks), BR_THREADS, rank_smem, st>>>(
         scores, boxes, cand, m_dev, m_bound, k0, perm, boxes_s, status, rowbits, NB, ecount, haspred, zero8);
     if (chunks == 1) return;
-    const size_t smem = sizeof(uint64_t) * MS_SLOTS;
-    ensure_dynamic_smem(reinterpret_cast<const void*>(merge_level_kernel), smem);
+    const int tiles = chunks * (MS_CHUNK / ML_TILE);
     for (int run = MS_CHUNK; run < chunks * MS_CHUNK; run *= 2) {
         const bool last = 2 * run >= chunks * MS_CHUNK;
-        merge_level_kernel<<<chunks, MS_THREADS, smem, st>>>(k0, k1, run, last ? 1 : 0, m_dev, m_bound,
-                                                             boxes, perm, boxes_s);
+        merge_level_kernel<<<tiles, ML_THREADS, 0, st>>>(k0, k1, run, last ? 1 : 0, m_dev, m_bound,
+                                                         boxes, perm, boxes_s);
         uint64_t* t = k0;
         k0 = k1;
         k1 = t;

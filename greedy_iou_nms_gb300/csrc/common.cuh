@@ -166,9 +166,8 @@ __device__ __forceinline__ uint64_t resolve_tile_col(uint64_t cand, uint64_t ca,
     return kept;
 }
 
-// Band of 64-box tiles below the diagonal whose blocks the mask kernel also
-// stores in column view: block (row tile C-d, column tile C) for d = 0..BAND_L
-// lives at band[(C*(BAND_L+1) + d)*64 ...] as 32 (C[l], C[l+32]) pairs.
+// Tiles below the diagonal whose 64x64 blocks the walk reads in column view
+// (block (row tile C-d, column tile C) for d = 0..BAND_L).
 constexpr int BAND_L = 16;
 
 __device__ __forceinline__ void set_status(int32_t* status, int code)

@@ -52,7 +52,7 @@ struct SingleLayout {
     unsigned ecap = 0;   // pairs one CTA's graph path holds (0: no list, the walk resolves)
     unsigned lcap = 0;   // pairs the list holds (more when the all-SM graph path exists)
     bool grid = false;   // the all-SM graph path exists at this size
-    size_t status, m_count, ecount, done, cand, perm, boxes_s, keys, rowbits, band, edges, haspred, gstate,
+    size_t status, m_count, ecount, done, cand, perm, boxes_s, keys, rowbits, edges, haspred, gstate,
         gctl, mask, total;
 };
 
@@ -76,7 +76,6 @@ SingleLayout single_layout(int64_t n)
     s.boxes_s = L.add(16 * static_cast<size_t>(n));
     s.keys = L.add(sort_keys_bytes(static_cast<int>(n)));
     s.rowbits = L.add(8 * static_cast<size_t>(n) * static_cast<size_t>(s.NB));
-    s.band = L.add(8 * static_cast<size_t>((n + 63) / 64) * (BAND_L + 1) * 64);
     s.edges = L.add(4 * static_cast<size_t>(s.lcap));
     s.haspred = L.add(8 * static_cast<size_t>((n + 63) / 64));
     s.gstate = L.add(s.grid ? graph_grid_state_bytes(static_cast<int>(n)) : 0);
@@ -269,7 +268,7 @@ nms_status run_impl(const float* boxes, const float* scores, int64_t n, const in
                         status, nullptr, L.NB, nullptr, haspred, nullptr, st);
             stamps.record(1, st);
             launch_iou_mask(boxes_s, m_count, static_cast<int>(n), p, nullptr, L.ldw, nullptr, L.NB, nullptr,
-                            nullptr, nullptr, 0u, haspred, st);
+                            nullptr, 0u, haspred, st);
             stamps.record(2, st);
             launch_fast_emit(haspred, m_count, static_cast<int>(n), perm, max_out, keep, counts, st);
             stamps.record(3, st);
@@ -285,7 +284,6 @@ nms_status run_impl(const float* boxes, const float* scores, int64_t n, const in
         launch_sort(scores, reinterpret_cast<const float4*>(boxes), cand, m_count, static_cast<int>(n),
                     perm, boxes_s, keys, status, rowbits, L.NB, ecount, haspred, gctl, st);
         stamps.record(1, st);
-        uint64_t* band = at<uint64_t>(workspace, L.band);
         const int nb = static_cast<int>(n);
         // With max_out, the first kept boxes depend only on a prefix of the
         // score order: mask and resolve the leading 2*max_out boxes first, and
@@ -304,22 +302,22 @@ nms_status run_impl(const float* boxes, const float* scores, int64_t n, const in
                                   limit, done_in, done_out, gctl + 4 + stage, gstate, gctl);
                 gd = gctl + 4 + stage;
             }
-            launch_resolve_single(mask, L.ldw, rowbits, L.NB, band, edges, ecount, haspred, m_count, nb, perm,
+            launch_resolve_single(mask, L.ldw, rowbits, L.NB, edges, ecount, haspred, m_count, nb, perm,
                                   max_out, keep, counts, status, st, limit, done_in, done_out, gd);
         };
         if (k1 >= n) {
-            launch_iou_mask(boxes_s, m_count, nb, p, mask, L.ldw, rowbits, L.NB, band, edges, ecount,
+            launch_iou_mask(boxes_s, m_count, nb, p, mask, L.ldw, rowbits, L.NB, edges, ecount,
                             L.lcap, haspred, st);
             stamps.record(2, st);
             resolve(1 << 30, nullptr, nullptr, 0);
         } else {
             int* done = at<int>(workspace, L.done);
             const int k = static_cast<int>(k1);
-            launch_iou_mask(boxes_s, m_count, nb, p, mask, L.ldw, rowbits, L.NB, band, edges, ecount,
+            launch_iou_mask(boxes_s, m_count, nb, p, mask, L.ldw, rowbits, L.NB, edges, ecount,
                             L.lcap, haspred, st, 0, k);
             stamps.record(2, st);
             resolve(k, nullptr, done, 0);
-            launch_iou_mask(boxes_s, m_count, nb, p, mask, L.ldw, rowbits, L.NB, band, edges, ecount,
+            launch_iou_mask(boxes_s, m_count, nb, p, mask, L.ldw, rowbits, L.NB, edges, ecount,
                             L.lcap, haspred, st, k, nb, done);
             resolve(1 << 30, done, nullptr, 1);
         }
@@ -465,7 +463,7 @@ extern "C" nms_status nms_iou_mask(const float* boxes_sorted, int64_t n, float i
     if (mask_words < n * ldw) return NMS_ERR_CAPACITY;
     cudaGetLastError();
     launch_iou_mask(reinterpret_cast<const float4*>(boxes_sorted), nullptr, static_cast<int>(n),
-                    make_thr(iou_thr), mask, ldw, nullptr, 1, nullptr, nullptr, nullptr, 0u, nullptr,
+                    make_thr(iou_thr), mask, ldw, nullptr, 1, nullptr, nullptr, 0u, nullptr,
                     static_cast<cudaStream_t>(stream));
     return cuda_status();
 }
@@ -485,9 +483,7 @@ extern "C" nms_status nms_resolve_mask(const uint64_t* mask, int64_t n, const in
         cudaMemsetAsync(count, 0, sizeof(int64_t), st);
         return cuda_status();
     }
-    uint64_t* band = at<uint64_t>(workspace, L.band);
-    launch_band_from_mask(mask, L.ldw, static_cast<int>(n), band, st);
-    launch_resolve_single(mask, L.ldw, nullptr, 1, band, nullptr, nullptr, nullptr, nullptr,
+    launch_resolve_single(mask, L.ldw, nullptr, 1, nullptr, nullptr, nullptr, nullptr,
                           static_cast<int>(n), perm, max_out, keep, count, nullptr, st);
     return cuda_status();
 }

@@ -41,17 +41,16 @@ constexpr int MASK_TILE_W = GBNMS_MASK_MT;
 // Mask tiles whose columns lie in [col_lo, min(col_hi, m_bound)); with `done`
 // set on the device the launch does nothing.
 void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const ThrParams& p,
-                     uint64_t* mask, int64_t ldw, uint64_t* rowbits, int NB, uint64_t* band,
+                     uint64_t* mask, int64_t ldw, uint64_t* rowbits, int NB,
                      uint32_t* edges, unsigned* ecount, unsigned ecap, uint64_t* haspred,
                      cudaStream_t st, int col_lo = 0, int col_hi = 1 << 30, const int* done = nullptr);
 size_t resolve_smem_bytes(int m_bound, int NB);
 unsigned graph_edge_cap(int m_bound);
-void launch_band_from_mask(const uint64_t* mask, int64_t ldw, int n, uint64_t* band, cudaStream_t st);
 // Resolves boxes [0, min(n, limit)).  done_in set on the device: nothing to
 // do; done_out: set to 1 when the call found max_out kept boxes or covered
 // all n boxes (a later stage then has nothing to do).
 void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* rowbits, int NB,
-                           const uint64_t* band, const uint32_t* edges, const unsigned* ecount,
+                           const uint32_t* edges, const unsigned* ecount,
                            const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm,
                            int max_out, int64_t* keep, int64_t* counts, int32_t* status,
                            cudaStream_t st, int limit = 1 << 30, const int* done_in = nullptr,

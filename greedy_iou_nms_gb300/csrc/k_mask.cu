@@ -16,10 +16,8 @@
 // registers and walks the MT staged column boxes (broadcast shared-memory
 // reads of 4 columns at a time), so a row's words of the unit are built in
 // registers and written with 16-byte stores.  Each row also records, one bit
-// per 256-column chunk, which of its chunks hold a set bit, and the 64x64
-// blocks within BAND_L tiles of the diagonal are also written in column
-// view; the resolve uses the first to skip all-zero chunks and the second to
-// decide a tile with lane-local tests.  When asked, every set bit is also
+// per 256-column chunk, which of its chunks hold a set bit (the walk skips
+// all-zero chunks).  When asked, every set bit is also
 // appended to a list of (row, column) pairs, the sparse form of the same
 // graph, as long as the list has room, and every column with a set bit is
 // marked in a bitmap of boxes that have an earlier neighbour.
@@ -268,32 +266,15 @@ __device__ __forceinline__ void store_words(uint64_t* dst, const uint64_t (&w)[N
     }
 }
 
-// The unit's outputs from its final words: the band blocks in column view,
-// the mask words, the per-row chunk bits, the neighbour bitmap and the pair
-// list.
+// The unit's outputs from its final words: the mask words, the per-row chunk
+// bits, the neighbour bitmap and the pair list.
 __device__ __forceinline__ void store_unit(const uint64_t (&w0)[NQ], const uint64_t (&w1)[NQ], int i0, int i1,
-                                           int a, int cb, int n, unsigned l, uint64_t* __restrict__ mask,
+                                           int cb, int n, unsigned l, uint64_t* __restrict__ mask,
                                            int64_t ldw, unsigned long long* __restrict__ rowbits, int NB,
-                                           ulonglong2* __restrict__ band, uint32_t* __restrict__ edges,
+                                           uint32_t* __restrict__ edges,
                                            unsigned* __restrict__ ecount, unsigned ecap,
                                            unsigned long long* __restrict__ haspred)
 {
-    // Column view of the blocks within BAND_L tiles of the diagonal (64-row
-    // tile R = a of the unit, 64-column tile C = NQ c + q): a warp transpose of
-    // the block's final words leaves columns l and l+32 in lane l.
-    if (band) {
-        const int R = a;
-        const int T64 = (n + 63) / 64;
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-            const int C = cb / 64 + q;
-            const int d = C - R;
-            if (d < 0 || d > BAND_L || C >= T64) continue;  // warp-uniform
-            uint64_t colA = w0[q], colB = w1[q];
-            transpose64(colA, colB);
-            band[(static_cast<int64_t>(C) * (BAND_L + 1) + d) * 32 + l] = make_ulonglong2(colA, colB);
-        }
-    }
     const int64_t wcol = cb / 64;
     const int chunk = cb >> 8;  // 256-column chunk of the per-row bitmap
     if (i0 < n) {
@@ -347,7 +328,7 @@ __device__ __forceinline__ void store_unit(const uint64_t (&w0)[NQ], const uint6
 __global__ void __launch_bounds__(M_THREADS, M_CTAS_PER_SM)
 iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_dev, int m_bound,
                 ThrParams p, uint64_t* __restrict__ mask, int64_t ldw,
-                unsigned long long* __restrict__ rowbits, int NB, ulonglong2* __restrict__ band,
+                unsigned long long* __restrict__ rowbits, int NB,
                 uint32_t* __restrict__ edges, unsigned* __restrict__ ecount, unsigned ecap,
                 unsigned long long* __restrict__ haspred, int limit, long long u_begin, long long u_end,
                 const int* __restrict__ done)
@@ -419,7 +400,7 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
         }
         verify_words(C, b0, ar0, p.thr, w0);
         verify_words(C, b1, ar1, p.thr, w1);
-        store_unit(w0, w1, i0, i1, a, cb, n, l, mask, ldw, rowbits, NB, band, edges, ecount, ecap, haspred);
+        store_unit(w0, w1, i0, i1, cb, n, l, mask, ldw, rowbits, NB, edges, ecount, ecap, haspred);
     }
 }
 
@@ -430,7 +411,7 @@ int64_t mask_tiles(int64_t n)
 }
 
 void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const ThrParams& p,
-                     uint64_t* mask, int64_t ldw, uint64_t* rowbits, int NB, uint64_t* band,
+                     uint64_t* mask, int64_t ldw, uint64_t* rowbits, int NB,
                      uint32_t* edges, unsigned* ecount, unsigned ecap, uint64_t* haspred,
                      cudaStream_t st, int col_lo, int col_hi, const int* done)
 {
@@ -451,7 +432,7 @@ void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const
     if (done) grid = min(grid, static_cast<int64_t>(sms) * M_CTAS_PER_SM);
     iou_mask_kernel<<<static_cast<unsigned>(grid), M_THREADS, 0, st>>>(
         boxes_s, m_dev, m_bound, p, mask, ldw, reinterpret_cast<unsigned long long*>(rowbits), NB,
-        reinterpret_cast<ulonglong2*>(band), edges, ecount, ecap, reinterpret_cast<unsigned long long*>(haspred),
+        edges, ecount, ecap, reinterpret_cast<unsigned long long*>(haspred),
         hi, u0, u1, done);
 }
 

@@ -27,9 +27,10 @@
 //   (a) the kept sets of tiles t-1 .. t-RV_DR,          -> the resolver warp,
 //   (b) the kept sets of tiles t-RV_DR-1 .. t-BAND_L,   -> helper warps,
 //   (c) the kept sets of tiles <= t-BAND_L-1,           -> worker warp groups.
-// (a) and (b) use the column views of the blocks (tile t-d, tile t) that the
-// mask kernel writes for d <= BAND_L: lane l ANDs its two boxes' columns with
-// the kept sets and one pair of ballots gives the removed word.  (c) ORs the
+// (a) and (b) use the column views of the blocks (tile t-d, tile t) for
+// d <= BAND_L, which the helper of tile t builds from the row-major mask (a
+// warp transpose per block): lane l ANDs its two boxes' columns with the kept
+// sets and one pair of ballots gives the removed word.  (c) ORs the
 // kept rows of the row-major mask into a shared removed-bitmap with shared
 // atomics, skipping the 256-column chunks the per-row chunk bitmap marks
 // all-zero.
@@ -42,11 +43,11 @@
 // without the boxes (a) removed.  Its critical path per tile is the (a) test
 // and the hand-over of the kept set.
 //
-// The column-view windows arrive by lane-parallel cp.async copies (bulk
-// copies cost ~200 cycles of issue each on this SM, too much for one small
-// window per tile) into the helpers' shared-memory rings; the resolver reads
-// the blocks it needs from the helper's slot, so it issues no global memory
-// operation of its own.  Every hand-over between roles is
+// The windows arrive by lane-parallel 8-byte cp.async copies of mask words
+// (bulk copies cost ~200 cycles of issue each on this SM, too much for one
+// small window per tile) into the helpers' shared-memory rings, where the
+// helper turns them into column view; the resolver reads the blocks it needs
+// from the helper's slot, so it issues no global memory operation of its own.  Every hand-over between roles is
 // an mbarrier, waiters off the critical path nap between attempts, and every
 // wait is bounded and gives up with NMS_ERR_TIMEOUT.  The resolver owns a
 // scheduler partition: the warps that share warp 0's partition (4, 8, ...)
@@ -60,7 +61,7 @@
 
 namespace gbnms {
 
-constexpr int RV_L = BAND_L;               // tiles covered by the column-view band
+constexpr int RV_L = BAND_L;               // tiles covered by the column-view windows
 constexpr int RV_DR = 4;                   // distances the resolver tests itself
 constexpr int RV_HW = RV_L + 1;            // blocks of a window: the whole band of one tile
 constexpr int RV_NH = 4;                   // helper warps (tiles round-robin)
@@ -152,16 +153,45 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long* b, int k, const in
     return true;
 }
 
-// Lane-parallel copy of NB16 16-byte pieces per lane (32*NB16*16 contiguous
-// bytes) from global to shared memory; commit_group() closes a window.
-template <int NB16>
-__device__ __forceinline__ void window_copy(uint64_t* dst, const uint64_t* src, unsigned l)
+// The band window of tile tt, straight from the row-major mask: the words of
+// column tile tt in the 64 rows of each tile tt-d, d = 0..RV_L, one 8-byte
+// copy per row, so lane l's pair of slots (2l, 2l+1) of block d holds rows l
+// and l+32.  Rows before the first tile or past n are zero-filled.
+// commit_group() closes a window.
+__device__ __forceinline__ void window_from_mask(uint64_t* dst, const uint64_t* __restrict__ mask, int64_t ldw,
+                                                 int tt, int n, unsigned l)
 {
 #pragma unroll
-    for (int q = 0; q < NB16; ++q) {
-        const int w = 2 * (q * 32 + static_cast<int>(l));
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(dst + w)), "l"(src + w)
-                     : "memory");
+    for (int d = 0; d <= RV_L; ++d) {
+        const int R = tt - d;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t row = static_cast<int64_t>(R) * 64 + l + 32 * h;
+            const bool ok = R >= 0 && row < n;
+            const uint64_t* src = ok ? mask + row * ldw + tt : mask;
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(smem_addr(dst + d * 64 + 2 * l + h)),
+                         "l"(src), "r"(ok ? 8u : 0u)
+                         : "memory");
+        }
+    }
+}
+
+// In place: each block of a window from window_from_mask turned into column
+// view (lane l's slot pair then holds columns l and l+32: bit r set iff row r
+// suppresses that column), keeping only bits above the diagonal in block 0.
+__device__ __forceinline__ void window_to_columns(uint64_t* win, unsigned l)
+{
+    ulonglong2* wv = reinterpret_cast<ulonglong2*>(win);
+#pragma unroll 1
+    for (int d = 0; d <= RV_L; ++d) {
+        const ulonglong2 v = wv[d * 32 + l];
+        uint64_t a = v.x, b = v.y;
+        if (d == 0) {
+            a &= ~0ull << (l + 1);
+            b &= l + 33 < 64 ? ~0ull << (l + 33) : 0ull;
+        }
+        transpose64(a, b);
+        wv[d * 32 + l] = make_ulonglong2(a, b);
     }
 }
 __device__ __forceinline__ void commit_group() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
@@ -260,13 +290,13 @@ unsigned graph_grid_cap(int m_bound)
 unsigned graph_edge_cap(int m_bound)
 {
     if (m_bound <= 0 || m_bound > GR_MAX_N) return 0;
-    const long long room = GR_SMEM - 4ll * (GR_HEAD + 4ll * graph_words(m_bound));
+    const long long room = GR_SMEM - 4ll * GR_HEAD - 40ll * graph_words(m_bound);
     return room > 0 ? static_cast<unsigned>((room / 4) & ~3ll) : 0u;
 }
 
 size_t graph_smem_bytes(int m_bound)
 {
-    return 4 * (GR_HEAD + 4 * static_cast<size_t>(graph_words(m_bound))) +
+    return 4 * GR_HEAD + 40 * static_cast<size_t>(graph_words(m_bound)) +
            4 * static_cast<size_t>(graph_edge_cap(m_bound));
 }
 
@@ -287,14 +317,53 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
         : "memory");
 }
 
+// Decides the open boxes of bitmap word w (boxes 32w .. 32w+31): kept if no
+// open source blocked them (a box a kept source hit is already removed).
+// Clears the word's blocked flags; returns whether a blocked box stays open.
+__device__ __forceinline__ bool decide_word(uint2* KR, uint8_t* BLK, int w, int NW, int n)
+{
+    const uint2 kr = KR[w];
+    const uint32_t valid = (w == NW - 1 && (n & 31)) ? (1u << (n & 31)) - 1u : ~0u;
+    const uint32_t open = ~(kr.x | kr.y) & valid;
+    if (!open) return false;
+    uint4* bq = reinterpret_cast<uint4*>(BLK + 32 * w);
+    const uint4 b0 = bq[0], b1 = bq[1];
+    const uint32_t bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    uint32_t blk = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) blk |= ((bv[q] * 0x01020408u) >> 24 & 0xfu) << (4 * q);  // bytes 0/1 -> bits
+    KR[w].x = kr.x | (open & ~blk);
+    bq[0] = make_uint4(0u, 0u, 0u, 0u);
+    bq[1] = make_uint4(0u, 0u, 0u, 0u);
+    return (open & blk) != 0;
+}
+
+// One live pair e (source << 16 | target) given its source's (kept, removed)
+// word ks.  A kept source removes the target at once (the removal is final,
+// so other pairs may see it in this same pass); an open source blocks the
+// target, with a plain byte store (every writer stores 1).  Returns whether
+// the pair stays (its source is still open).
+__device__ __forceinline__ bool mark_pair(uint2* KR, uint8_t* BLK, uint32_t e, uint2 ks)
+{
+    const uint32_t j = e & 0xffffu;
+    const uint32_t bi = 1u << ((e >> 16) & 31);
+    if (ks.x & bi) {
+        atomicOr(&KR[j >> 5].y, 1u << (j & 31));
+        return false;
+    }
+    if (ks.y & bi) return false;
+    BLK[j] = 1;
+    return true;
+}
+
 // Rounds over the pair list gedges[0..E) of n sorted boxes (haspred: bit j
 // set iff box j has a pair).  Returns false, with nothing written, when the
 // rounds outnumber the walk's tiles plus 16 (a long chain of dependencies:
 // the walk is then the faster way).
 //
-// Shared layout (32-bit words): scratch and the copy barrier, then the
-// (kept, removed) bits of 32 boxes per uint2, then the (hit by a kept box,
-// blocked by an open box) bits per uint2, then the live pairs.  Thread t owns
+// Shared layout: scratch and the copy barrier (GR_HEAD words), then the
+// (kept, removed) bits of 32 boxes per uint2, then one "blocked by an open
+// box" byte per box, then the live pairs.  Thread t owns
 // the pairs at t, t + RV_THREADS, ... and compacts its own share in place.
 // A pair leaves the list once its source is decided; while the source is
 // open the target is open too (a box is decided only after all its sources).
@@ -307,8 +376,8 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
     int* scratch = reinterpret_cast<int*>(sm);
     unsigned long long* bar = reinterpret_cast<unsigned long long*>(sm + 32);
     uint2* KR = reinterpret_cast<uint2*>(sm + GR_HEAD);
-    uint2* HB = KR + NWp;
-    uint32_t* Es = sm + GR_HEAD + 4 * NWp;
+    uint8_t* BLK = reinterpret_cast<uint8_t*>(KR + NWp);
+    uint32_t* Es = reinterpret_cast<uint32_t*>(BLK + 32 * NWp);
     const int tid = threadIdx.x;
     const unsigned l = lane_id();
     const int warp = tid >> 5;
@@ -332,7 +401,13 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
     }
     for (int w = tid; w < NW; w += RV_THREADS) {
         KR[w] = make_uint2(0u, 0u);
-        HB[w] = make_uint2(0u, haspred[w]);  // before the first round every target is blocked
+        const uint32_t hp = haspred[w];  // before the first round every target is blocked
+        uint32_t bx[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) bx[q] = (((hp >> (4 * q)) & 0xfu) * 0x00204081u) & 0x01010101u;  // bits -> bytes
+        uint4* bq = reinterpret_cast<uint4*>(BLK + 32 * w);
+        bq[0] = make_uint4(bx[0], bx[1], bx[2], bx[3]);
+        bq[1] = make_uint4(bx[4], bx[5], bx[6], bx[7]);
     }
     bool copied = true;
     if (bytes) {
@@ -354,23 +429,12 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
     int live = E > static_cast<unsigned>(tid) ? static_cast<int>((E - tid + RV_THREADS - 1) / RV_THREADS) : 0;
     const int max_rounds = (n + 63) / 64 + 16;
     for (int round = 0;; ++round) {
-        // Decide every open box: removed if a kept source hit it, kept if no
-        // open source blocked it.
+        // Decide every open box: kept if no open source blocked it.
         bool more = false;
-        for (int w = tid; w < NW; w += RV_THREADS) {
-            const uint2 kr = KR[w];
-            const uint32_t valid = (w == NW - 1 && (n & 31)) ? (1u << (n & 31)) - 1u : ~0u;
-            const uint32_t open = ~(kr.x | kr.y) & valid;
-            if (open) {
-                const uint2 hb = HB[w];
-                KR[w] = make_uint2(kr.x | (open & ~hb.x & ~hb.y), kr.y | (open & hb.x));
-                HB[w] = make_uint2(0u, 0u);
-                more |= (open & ~hb.x & hb.y) != 0;
-            }
-        }
+        for (int w = tid; w < NW; w += RV_THREADS) more |= decide_word(KR, BLK, w, NW, n);
         if (!__syncthreads_or(more)) break;
         if (round == max_rounds) return false;
-        // One pass over the live pairs: a kept source hits its target, a
+        // One pass over the live pairs: a kept source removes its target, a
         // removed source no longer matters, an open source blocks its target
         // and the pair stays.
         int nl = 0;
@@ -385,14 +449,7 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 if (e[u] == 0xffffffffu) continue;
-                const uint32_t j = e[u] & 0xffffu;
-                const uint32_t bi = 1u << ((e[u] >> 16) & 31);
-                if (ki[u].x & bi) {
-                    atomicOr(&HB[j >> 5].x, 1u << (j & 31));
-                } else if (!(ki[u].y & bi)) {
-                    atomicOr(&HB[j >> 5].y, 1u << (j & 31));
-                    Es[tid + RV_THREADS * nl++] = e[u];
-                }
+                if (mark_pair(KR, BLK, e[u], ki[u])) Es[tid + RV_THREADS * nl++] = e[u];
             }
         }
         live = nl;
@@ -450,7 +507,6 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
 __global__ void __launch_bounds__(RV_THREADS, 1)
 resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
                       const uint64_t* __restrict__ rowbits, int NB,
-                      const uint64_t* __restrict__ band,
                       const uint32_t* __restrict__ edges, const unsigned* __restrict__ ecount,
                       unsigned ecap, const uint32_t* __restrict__ haspred,
                       const int* __restrict__ m_dev, int m_bound, const int* __restrict__ perm,
@@ -484,7 +540,6 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
     unsigned char* wlist = reinterpret_cast<unsigned char*>(smem + LY.wlist);  // per worker warp
     uint64_t* kept = smem + LY.kept;          // [tiles]
     int* opre = reinterpret_cast<int*>(smem + LY.opre);
-    constexpr int BW = (BAND_L + 1) * 64;     // words of one tile's band
 
     const int Wpad = resolve_bitmap_words(m_bound);
     for (int w = threadIdx.x; w < Wpad; w += blockDim.x) removed[w] = 0;
@@ -552,9 +607,7 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
         uint64_t* myw = hwin + static_cast<size_t>(h) * RV_HR * RV_HW * 64;
         auto fill = [&](int i) {  // own tile i: its whole band window into slot i % RV_HR
             const int tt = h + RV_NH * i;
-            if (tt < T)
-                window_copy<RV_HW>(myw + static_cast<size_t>(i % RV_HR) * RV_HW * 64,
-                                   band + static_cast<int64_t>(tt) * BW, l);
+            if (tt < T) window_from_mask(myw + static_cast<size_t>(i % RV_HR) * RV_HW * 64, mask, ldw, tt, n, l);
             commit_group();
         };
         for (int i = 0; i < RV_HR - 1; ++i) fill(i);
@@ -577,6 +630,8 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
                 ok = mbar_wait(&S.done[f % RV_KR], f / RV_KR, &S.stop, RV_NAP_HELPER);
             if (!ok) break;
             wait_groups<RV_HR - 1>();
+            __syncwarp();
+            window_to_columns(myw + static_cast<size_t>(i % RV_HR) * RV_HW * 64, l);
             __syncwarp();
             const ulonglong2* wv =
                 reinterpret_cast<const ulonglong2*>(myw + static_cast<size_t>(i % RV_HR) * RV_HW * 64);
@@ -953,41 +1008,8 @@ void launch_graph_grid(uint32_t* edges, const unsigned* ecount, const uint64_t* 
 
 size_t resolve_smem_bytes(int m_bound, int NB) { return resolve_layout(m_bound, NB).total; }
 
-// Column view of the band blocks of a row-major mask: one warp per (column
-// tile C, distance d) transposes block (C-d, C).
-// Used when the caller brings its own mask (nms_resolve_mask).
-__global__ void band_from_mask_kernel(const uint64_t* __restrict__ mask, int64_t ldw, int n,
-                                      ulonglong2* __restrict__ band)
-{
-    const int T64 = (n + 63) / 64;
-    const int blk = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (blk >= T64 * (BAND_L + 1)) return;
-    const int C = blk / (BAND_L + 1), d = blk % (BAND_L + 1), R = C - d;
-    const unsigned l = lane_id();
-    uint64_t ra = 0, rb = 0;
-    if (R >= 0) {
-        const int64_t ia = static_cast<int64_t>(R) * 64 + l, ib = ia + 32;
-        if (ia < n) ra = mask[ia * ldw + C];
-        if (ib < n) rb = mask[ib * ldw + C];
-        if (d == 0) {  // only bits above the diagonal belong to the mask
-            ra &= (l + 1 < 64) ? (~0ull << (l + 1)) : 0ull;
-            rb &= (l + 33 < 64) ? (~0ull << (l + 33)) : 0ull;
-        }
-    }
-    transpose64(ra, rb);
-    band[static_cast<int64_t>(blk) * 32 + l] = make_ulonglong2(ra, rb);
-}
-
-void launch_band_from_mask(const uint64_t* mask, int64_t ldw, int n, uint64_t* band, cudaStream_t st)
-{
-    const int blocks = ((n + 63) / 64) * (BAND_L + 1);
-    if (blocks == 0) return;
-    band_from_mask_kernel<<<(blocks + 7) / 8, 256, 0, st>>>(mask, ldw, n,
-                                                            reinterpret_cast<ulonglong2*>(band));
-}
-
 void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* rowbits, int NB,
-                           const uint64_t* band, const uint32_t* edges, const unsigned* ecount,
+                           const uint32_t* edges, const unsigned* ecount,
                            const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm,
                            int max_out, int64_t* keep, int64_t* counts, int32_t* status,
                            cudaStream_t st, int limit, const int* done_in, int* done_out,
@@ -997,7 +1019,7 @@ void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* ro
     const unsigned ecap = edges ? graph_edge_cap(m_bound) : 0u;
     if (edges && graph_smem_bytes(m_bound) > smem) smem = graph_smem_bytes(m_bound);
     ensure_dynamic_smem(reinterpret_cast<const void*>(resolve_single_kernel), smem);
-    resolve_single_kernel<<<1, RV_THREADS, smem, st>>>(mask, ldw, rowbits, NB, band, edges, ecount,
+    resolve_single_kernel<<<1, RV_THREADS, smem, st>>>(mask, ldw, rowbits, NB, edges, ecount,
                                                        ecap, reinterpret_cast<const uint32_t*>(haspred),
                                                        m_dev, m_bound, perm, max_out, keep, counts,
                                                        status, limit, done_in, done_out, grid_done);

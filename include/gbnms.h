@@ -240,24 +240,19 @@ nms_status nms_run_timed(const float* boxes, const float* scores, int64_t n,
 #define NMS_NOALLOC_MAX_N 16384
 
 /*
- * nms_resolve_mask without a workspace: the same resolve, with its scratch in
- * a device array that the library holds for the life of the process.  The
- * pages have no counterpart to this entry point; it exists for callers that
- * cannot allocate device memory where they run NMS (a plugin whose host
- * framework owns every allocation, a real-time loop whose memory is planned
- * at start-up, a deployment that bans allocation after initialisation).
+ * nms_resolve_mask without a workspace: the same resolve, which keeps all its
+ * state in the shared memory of one thread block, so it needs no device
+ * scratch at all.  The pages have no counterpart to this entry point; it
+ * exists for callers that cannot allocate device memory where they run NMS
+ * (a plugin whose host framework owns every allocation, a real-time loop
+ * whose memory is planned at start-up, a deployment that bans allocation
+ * after initialisation).
  *
  *   mask, perm, max_out, keep, count: as for nms_resolve_mask; n must be
- *            <= NMS_NOALLOC_MAX_N (about 2.2 MB of scratch per GPU, held by
- *            every GPU that loads the library until the process exits).
- * The first call on a device looks up the scratch array's device address on
- * that device (cudaGetSymbolAddress, with the device current); make that
- * first call before any stream capture.  The call allocates nothing: no
- * cudaMalloc, cudaFree or allocating library routine.  All calls share the
- * one array, so calls that may overlap on the GPU (other streams, other host
- * threads, the same device) race on it and must be serialised by the caller;
- * calls on one stream are ordered and safe.  Each call rewrites all the
- * scratch it reads, so what an earlier call left behind never matters.
+ *            <= NMS_NOALLOC_MAX_N.
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine) and holds nothing between calls, so calls on any streams, host
+ * threads or devices may overlap.
  * Errors: NMS_ERR_INVALID_ARG (n < 0, NULL or unaligned pointers),
  *         NMS_ERR_CAPACITY (n > NMS_NOALLOC_MAX_N), NMS_ERR_CUDA.
  */

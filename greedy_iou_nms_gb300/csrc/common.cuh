@@ -170,6 +170,14 @@ __device__ __forceinline__ uint64_t resolve_tile_col(uint64_t cand, uint64_t ca,
 // (block (row tile C-d, column tile C) for d = 0..BAND_L).
 constexpr int BAND_L = 16;
 
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may be scheduled while its predecessor in
+// the stream still runs; it must wait here before reading what the
+// predecessor writes (a no-op for an ordinary launch).  The predecessor lets
+// it be scheduled early with pdl_release().
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 __device__ __forceinline__ void set_status(int32_t* status, int code)
 {
     atomicCAS(reinterpret_cast<int*>(status), 0, code);

@@ -19,6 +19,17 @@ struct Stamps {
     }
 };
 
+// Launch attribute that lets a kernel be scheduled while its predecessor in
+// the stream finishes (the kernel calls pdl_wait() before reading the
+// predecessor's output).
+inline cudaLaunchAttribute pdl_attribute()
+{
+    cudaLaunchAttribute a{};
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return a;
+}
+
 // Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
 // current device; the runtime is called only when the limit recorded for
 // that (device, kernel) is lower, so repeated launches pay nothing.

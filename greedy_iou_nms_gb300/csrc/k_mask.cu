@@ -335,6 +335,8 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
 {
     __shared__ __align__(16) float s_cols[M_WARPS][5][MT];  // per warp: -x1, x2, y1, -y2, area
 
+    pdl_wait();     // the sort (or an earlier stage) has finished
+    pdl_release();  // the resolve may be scheduled
     if (done && *done) return;  // an earlier stage already reached max_out
     const int n = min(m_dev ? *m_dev : m_bound, limit);
     const int T = (n + MT - 1) / MT;
@@ -430,10 +432,17 @@ void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const
     // few CTAs per SM.
     int64_t grid = (u1 - u0 + M_WARPS - 1) / M_WARPS;
     if (done) grid = min(grid, static_cast<int64_t>(sms) * M_CTAS_PER_SM);
-    iou_mask_kernel<<<static_cast<unsigned>(grid), M_THREADS, 0, st>>>(
-        boxes_s, m_dev, m_bound, p, mask, ldw, reinterpret_cast<unsigned long long*>(rowbits), NB,
-        edges, ecount, ecap, reinterpret_cast<unsigned long long*>(haspred),
-        hi, u0, u1, done);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(M_THREADS);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, iou_mask_kernel, boxes_s, m_dev, m_bound, p, mask, ldw,
+                       reinterpret_cast<unsigned long long*>(rowbits), NB, edges, ecount, ecap,
+                       reinterpret_cast<unsigned long long*>(haspred), hi, static_cast<long long>(u0),
+                       static_cast<long long>(u1), done);
 }
 
 }  // namespace gbnms

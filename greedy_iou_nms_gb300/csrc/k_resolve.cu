@@ -517,6 +517,7 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
     extern __shared__ __align__(128) uint64_t smem[];
     __shared__ ResolveShared S;
 
+    pdl_wait();                           // the mask (or an earlier kernel) has finished
     if (done_in && *done_in) return;      // an earlier stage already finished
     if (grid_done && *grid_done) return;  // graph_grid_kernel resolved this stage
     const int n_all = m_dev ? *m_dev : m_bound;
@@ -1019,10 +1020,17 @@ void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* ro
     const unsigned ecap = edges ? graph_edge_cap(m_bound) : 0u;
     if (edges && graph_smem_bytes(m_bound) > smem) smem = graph_smem_bytes(m_bound);
     ensure_dynamic_smem(reinterpret_cast<const void*>(resolve_single_kernel), smem);
-    resolve_single_kernel<<<1, RV_THREADS, smem, st>>>(mask, ldw, rowbits, NB, edges, ecount,
-                                                       ecap, reinterpret_cast<const uint32_t*>(haspred),
-                                                       m_dev, m_bound, perm, max_out, keep, counts,
-                                                       status, limit, done_in, done_out, grid_done);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(RV_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, resolve_single_kernel, mask, ldw, rowbits, NB, edges, ecount, ecap,
+                       reinterpret_cast<const uint32_t*>(haspred), m_dev, m_bound, perm, max_out, keep, counts,
+                       status, limit, done_in, done_out, grid_done);
 }
 
 }  // namespace gbnms

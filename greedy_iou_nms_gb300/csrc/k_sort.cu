@@ -142,6 +142,7 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
     __shared__ uint32_t wlo[BR_THREADS / 32], whi[BR_THREADS / 32];
     __shared__ uint64_t ckey[BR_CAND];  // this CTA's candidates
     __shared__ int crank[BR_CAND];
+    pdl_release();  // the mask kernel may be scheduled (it waits for this grid's results)
     const int tid = threadIdx.x;
     const int c0 = blockIdx.y * MS_CHUNK;
     const int q0 = c0 + blockIdx.x * BR_CAND;  // this CTA's candidates [q0, q0 + BR_CAND)
@@ -326,6 +327,7 @@ merge_level_kernel(const uint64_t* __restrict__ keys_in, uint64_t* __restrict__ 
 {
     __shared__ __align__(16) uint64_t buf[ML_SLOTS];  // ML_TILE keys, A part then B part, skewed
     __shared__ int split[2];
+    pdl_release();
     const int tid = threadIdx.x;
     const int o0 = blockIdx.x * ML_TILE;
     const int pb = o0 & ~(2 * run - 1);       // start of the merge pair

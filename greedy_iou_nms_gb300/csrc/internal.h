@@ -30,6 +30,22 @@ inline cudaLaunchAttribute pdl_attribute()
     return a;
 }
 
+// Launch with pdl_attribute().
+template <typename... KArgs, typename... Args>
+inline void launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Raises a kernel's dynamic shared-memory limit to at least `bytes` on the
 // current device; the runtime is called only when the limit recorded for
 // that (device, kernel) is lower, so repeated launches pay nothing.

@@ -25,6 +25,7 @@ __global__ void batched_setup_kernel(const int64_t* __restrict__ off, int batch,
                                      int S, int* __restrict__ seg_cnt, int* __restrict__ ok,
                                      int32_t* status)
 {
+    pdl_release();
     for (int s = threadIdx.x; s < S; s += blockDim.x) seg_cnt[s] = 0;
     int bad = 0;
     if (off) {
@@ -63,6 +64,8 @@ __global__ void batched_count_kernel(const float* __restrict__ scores,
                                      int* __restrict__ seg_cnt, int* __restrict__ seg_of,
                                      int* __restrict__ slot, int32_t* status)
 {
+    pdl_wait();
+    pdl_release();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (!*ok) return;
     int seg = -1;
@@ -94,6 +97,8 @@ __global__ void batched_count_kernel(const float* __restrict__ scores,
 __global__ void batched_scan_kernel(const int* __restrict__ seg_cnt, int S,
                                     int* __restrict__ seg_off)
 {
+    pdl_wait();
+    pdl_release();
     __shared__ int carry;
     __shared__ int warp_sums[32];
     if (threadIdx.x == 0) carry = 0;
@@ -137,6 +142,8 @@ __global__ void batched_scatter_kernel(const int* __restrict__ seg_of, const int
                                        const int* __restrict__ seg_off, int n,
                                        const int* __restrict__ ok, int* __restrict__ cand)
 {
+    pdl_wait();
+    pdl_release();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n || !*ok) return;
     const int s = seg_of[i];
@@ -157,6 +164,8 @@ seg_small_kernel(const float4* __restrict__ boxes, const float* __restrict__ sco
                  const int* __restrict__ ok, float thr, int max_out, int fast,
                  uint64_t* __restrict__ kept_key, int* __restrict__ kept_cnt)
 {
+    pdl_wait();
+    pdl_release();
     __shared__ float4 sbox[SS_WARPS][64];
     __shared__ float sarea[SS_WARPS][64];
     __shared__ uint64_t skey[SS_WARPS][64];
@@ -237,111 +246,114 @@ seg_large_kernel(const float4* __restrict__ boxes, const float* __restrict__ sco
     __shared__ uint64_t s_kept;
     __shared__ int s_nk;
 
-    if (!*ok) return;
-    // A few CTAs per SM take the segments in turn and skip the small ones
-    // (the warp kernel's).
-    for (int s = blockIdx.x; s < S; s += gridDim.x) {
-        const int lo = seg_off[s];
-        const int m = seg_off[s + 1] - lo;
-        if (m <= 64) continue;
-        __syncthreads();  // the previous segment's shared state is no longer read
+    pdl_release();  // runs beside the small-segment kernel, which ends before this grid does
+    if (*ok) {
+        // A few CTAs per SM take the segments in turn and skip the small ones
+        // (the warp kernel's).
+        for (int s = blockIdx.x; s < S; s += gridDim.x) {
+            const int lo = seg_off[s];
+            const int m = seg_off[s + 1] - lo;
+            if (m <= 64) continue;
+            __syncthreads();  // the previous segment's shared state is no longer read
 
-        // Rank each candidate of the segment by counting smaller keys.
-        for (int e = threadIdx.x; e < m; e += blockDim.x) {
-            const int x = cand[lo + e];
-            const uint64_t k = order_key(scores[x], x);
-            int r = 0;
-            for (int f = 0; f < m; ++f) {
-                const int y = cand[lo + f];
-                r += order_key(scores[y], y) < k;
+            // Rank each candidate of the segment by counting smaller keys.
+            for (int e = threadIdx.x; e < m; e += blockDim.x) {
+                const int x = cand[lo + e];
+                const uint64_t k = order_key(scores[x], x);
+                int r = 0;
+                for (int f = 0; f < m; ++f) {
+                    const int y = cand[lo + f];
+                    r += order_key(scores[y], y) < k;
+                }
+                sorted_key[lo + r] = k;
+                sorted_box[lo + r] = boxes[x];
             }
-            sorted_key[lo + r] = k;
-            sorted_box[lo + r] = boxes[x];
-        }
-        __syncthreads();
+            __syncthreads();
 
-        int nk = 0;  // kept so far (uniform)
-        const int cap = max_out > 0 ? max_out : m;
-        const unsigned l = lane_id();
-        for (int t0 = 0; t0 < m && nk < cap; t0 += 64) {
-            const int tn = min(64, m - t0);
-            if (threadIdx.x == 0) s_removed = 0;
-            if (threadIdx.x < 64) diag[threadIdx.x] = 0;
-            __syncthreads();
-            // (a) candidates of the tile against every kept box (Fast NMS: every
-            //     earlier box of the segment).
-            {
-                const int cidx = threadIdx.x & 63;
-                const int slice = threadIdx.x >> 6;
-                const int nslice = blockDim.x >> 6;
-                if (cidx < tn) {
-                    const float4 cbx = sorted_box[lo + t0 + cidx];
-                    const float car = box_area(cbx);
-                    bool hit = false;
-                    if (fast) {
-                        for (int k = slice; k < t0 && !hit; k += nslice) {
-                            const float4 kb = sorted_box[lo + k];
-                            hit = suppress_exact(kb, box_area(kb), cbx, car, thr);
+            int nk = 0;  // kept so far (uniform)
+            const int cap = max_out > 0 ? max_out : m;
+            const unsigned l = lane_id();
+            for (int t0 = 0; t0 < m && nk < cap; t0 += 64) {
+                const int tn = min(64, m - t0);
+                if (threadIdx.x == 0) s_removed = 0;
+                if (threadIdx.x < 64) diag[threadIdx.x] = 0;
+                __syncthreads();
+                // (a) candidates of the tile against every kept box (Fast NMS: every
+                //     earlier box of the segment).
+                {
+                    const int cidx = threadIdx.x & 63;
+                    const int slice = threadIdx.x >> 6;
+                    const int nslice = blockDim.x >> 6;
+                    if (cidx < tn) {
+                        const float4 cbx = sorted_box[lo + t0 + cidx];
+                        const float car = box_area(cbx);
+                        bool hit = false;
+                        if (fast) {
+                            for (int k = slice; k < t0 && !hit; k += nslice) {
+                                const float4 kb = sorted_box[lo + k];
+                                hit = suppress_exact(kb, box_area(kb), cbx, car, thr);
+                            }
                         }
-                    }
-                    for (int k = slice; !fast && k < nk && !hit; k += nslice) {
-                        float4 kb;
-                        float ka;
-                        if (k < SL_CACHE) {
-                            kb = kbox[k];
-                            ka = karea[k];
-                        } else {
-                            // Beyond the cache: kept_key holds the kept box's sorted position.
-                            kb = sorted_box[lo + static_cast<int>(kept_key[lo + k])];
-                            ka = box_area(kb);
+                        for (int k = slice; !fast && k < nk && !hit; k += nslice) {
+                            float4 kb;
+                            float ka;
+                            if (k < SL_CACHE) {
+                                kb = kbox[k];
+                                ka = karea[k];
+                            } else {
+                                // Beyond the cache: kept_key holds the kept box's sorted position.
+                                kb = sorted_box[lo + static_cast<int>(kept_key[lo + k])];
+                                ka = box_area(kb);
+                            }
+                            hit = suppress_exact(kb, ka, cbx, car, thr);
                         }
-                        hit = suppress_exact(kb, ka, cbx, car, thr);
+                        if (hit) atomicOr(&s_removed, 1ull << cidx);
                     }
-                    if (hit) atomicOr(&s_removed, 1ull << cidx);
                 }
-            }
-            // (b) the tile's own 64x64 block in column view: bit i of diag[j] set iff
-            //     i < j and i suppresses j.
-            for (int q = threadIdx.x; q < 64 * 64; q += blockDim.x) {
-                const int i = q >> 6, j = q & 63;
-                if (i < j && j < tn) {
-                    const float4 bi = sorted_box[lo + t0 + i];
-                    const float4 bj = sorted_box[lo + t0 + j];
-                    if (suppress_exact(bi, box_area(bi), bj, box_area(bj), thr))
-                        atomicOr(reinterpret_cast<unsigned long long*>(&diag[j]), 1ull << i);
+                // (b) the tile's own 64x64 block in column view: bit i of diag[j] set iff
+                //     i < j and i suppresses j.
+                for (int q = threadIdx.x; q < 64 * 64; q += blockDim.x) {
+                    const int i = q >> 6, j = q & 63;
+                    if (i < j && j < tn) {
+                        const float4 bi = sorted_box[lo + t0 + i];
+                        const float4 bj = sorted_box[lo + t0 + j];
+                        if (suppress_exact(bi, box_area(bi), bj, box_area(bj), thr))
+                            atomicOr(reinterpret_cast<unsigned long long*>(&diag[j]), 1ull << i);
+                    }
                 }
+                __syncthreads();
+                if (threadIdx.x < 32) {
+                    const uint64_t valid = tn >= 64 ? ~0ull : ((1ull << tn) - 1ull);
+                    const uint64_t cand = valid & ~static_cast<uint64_t>(s_removed);
+                    uint64_t K = fast ? cand & ballot64(diag[l] == 0, diag[l + 32] == 0)
+                                      : resolve_tile_col(cand, diag[l], diag[l + 32]);
+                    const int room = cap - nk;
+                    if (__popcll(K) > room) K = lowest_bits(K, room);
+                    if (l == 0) { s_kept = K; s_nk = __popcll(K); }
+                }
+                __syncthreads();
+                const uint64_t K = s_kept;
+                // Append the tile's kept boxes in order: cache + record the sorted position.
+                if (threadIdx.x < 64 && ((K >> threadIdx.x) & 1ull)) {
+                    const int r = nk + __popcll(K & ((1ull << threadIdx.x) - 1ull));
+                    const float4 b = sorted_box[lo + t0 + threadIdx.x];
+                    if (r < SL_CACHE) { kbox[r] = b; karea[r] = box_area(b); }
+                    // Temporarily store the sorted position; replaced by the key at the end.
+                    kept_key[lo + r] = static_cast<uint64_t>(t0 + threadIdx.x);
+                }
+                nk += s_nk;
+                __syncthreads();
             }
+            // Replace the recorded sorted positions by the (score key, index) keys.
             __syncthreads();
-            if (threadIdx.x < 32) {
-                const uint64_t valid = tn >= 64 ? ~0ull : ((1ull << tn) - 1ull);
-                const uint64_t cand = valid & ~static_cast<uint64_t>(s_removed);
-                uint64_t K = fast ? cand & ballot64(diag[l] == 0, diag[l + 32] == 0)
-                                  : resolve_tile_col(cand, diag[l], diag[l + 32]);
-                const int room = cap - nk;
-                if (__popcll(K) > room) K = lowest_bits(K, room);
-                if (l == 0) { s_kept = K; s_nk = __popcll(K); }
+            for (int r = threadIdx.x; r < nk; r += blockDim.x) {
+                const int pos = static_cast<int>(kept_key[lo + r]);
+                kept_key[lo + r] = sorted_key[lo + pos];
             }
-            __syncthreads();
-            const uint64_t K = s_kept;
-            // Append the tile's kept boxes in order: cache + record the sorted position.
-            if (threadIdx.x < 64 && ((K >> threadIdx.x) & 1ull)) {
-                const int r = nk + __popcll(K & ((1ull << threadIdx.x) - 1ull));
-                const float4 b = sorted_box[lo + t0 + threadIdx.x];
-                if (r < SL_CACHE) { kbox[r] = b; karea[r] = box_area(b); }
-                // Temporarily store the sorted position; replaced by the key at the end.
-                kept_key[lo + r] = static_cast<uint64_t>(t0 + threadIdx.x);
-            }
-            nk += s_nk;
-            __syncthreads();
+            if (threadIdx.x == 0) kept_cnt[s] = nk;
         }
-        // Replace the recorded sorted positions by the (score key, index) keys.
-        __syncthreads();
-        for (int r = threadIdx.x; r < nk; r += blockDim.x) {
-            const int pos = static_cast<int>(kept_key[lo + r]);
-            kept_key[lo + r] = sorted_key[lo + pos];
-        }
-        if (threadIdx.x == 0) kept_cnt[s] = nk;
     }
+    pdl_wait();  // the merge that follows also needs the small segments
 }
 
 // ------------------------------------------------------------ per-image merge
@@ -380,6 +392,8 @@ merge_kernel(const int* __restrict__ seg_off, const int* __restrict__ kept_cnt,
              const int* __restrict__ ok, int max_out, uint64_t* __restrict__ stage,
              int64_t* __restrict__ keep, int64_t* __restrict__ counts)
 {
+    pdl_wait();
+    pdl_release();
     __shared__ uint64_t ck[MG_CHUNK];
     __shared__ int seg_pre[MG_THREADS];
     __shared__ int s_tot;
@@ -520,25 +534,25 @@ void launch_batched(const BatchedArgs& a, cudaStream_t st, const Stamps& stamps)
     stamps.record(0, st);
     batched_setup_kernel<<<1, 1024, 0, st>>>(a.off, a.batch, n, S, a.seg_cnt, a.ok, a.status);
     if (n > 0) {
-        batched_count_kernel<<<(n + 255) / 256, 256, 0, st>>>(
-            a.scores, a.cls, a.C, a.off, a.batch, n, a.use_thr, a.score_thr, a.ok, a.seg_cnt,
-            a.seg_of, a.slot, a.status);
+        launch_pdl(batched_count_kernel, dim3((n + 255) / 256), dim3(256), 0, st, a.scores, a.cls, a.C, a.off,
+                   a.batch, n, a.use_thr, a.score_thr, a.ok, a.seg_cnt, a.seg_of, a.slot, a.status);
     }
-    batched_scan_kernel<<<1, 1024, 0, st>>>(a.seg_cnt, S, a.seg_off);
-    if (n > 0) batched_scatter_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.seg_of, a.slot, a.seg_off, n, a.ok, a.cand);
+    launch_pdl(batched_scan_kernel, dim3(1), dim3(1024), 0, st, a.seg_cnt, S, a.seg_off);
+    if (n > 0)
+        launch_pdl(batched_scatter_kernel, dim3((n + 255) / 256), dim3(256), 0, st, a.seg_of, a.slot, a.seg_off, n,
+                   a.ok, a.cand);
     stamps.record(1, st);
-    seg_small_kernel<<<(S + SS_WARPS - 1) / SS_WARPS, SS_WARPS * 32, 0, st>>>(
-        a.boxes, a.scores, a.seg_off, a.cand, S, a.ok, a.thr, a.max_out, a.fast, a.kept_key, a.kept_cnt);
+    launch_pdl(seg_small_kernel, dim3((S + SS_WARPS - 1) / SS_WARPS), dim3(SS_WARPS * 32), 0, st, a.boxes, a.scores,
+               a.seg_off, a.cand, S, a.ok, a.thr, a.max_out, a.fast, a.kept_key, a.kept_cnt);
     int sms = 0, dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int large_grid = max(1, min(S, 2 * (sms > 0 ? sms : 1)));
-    seg_large_kernel<<<large_grid, SL_THREADS, 0, st>>>(a.boxes, a.scores, a.seg_off, a.cand, S, a.ok, a.thr,
-                                               a.max_out, a.fast, a.sorted_key, a.sorted_box, a.kept_key,
-                                               a.kept_cnt);
+    launch_pdl(seg_large_kernel, dim3(large_grid), dim3(SL_THREADS), 0, st, a.boxes, a.scores, a.seg_off, a.cand, S,
+               a.ok, a.thr, a.max_out, a.fast, a.sorted_key, a.sorted_box, a.kept_key, a.kept_cnt);
     stamps.record(2, st);
-    merge_kernel<<<a.batch, MG_THREADS, 0, st>>>(a.seg_off, a.kept_cnt, a.kept_key, a.C, a.off,
-                                                  a.ok, a.max_out, a.stage, a.keep, a.counts);
+    launch_pdl(merge_kernel, dim3(a.batch), dim3(MG_THREADS), 0, st, a.seg_off, a.kept_cnt, a.kept_key, a.C, a.off,
+               a.ok, a.max_out, a.stage, a.keep, a.counts);
     stamps.record(3, st);
 }
 

@@ -27,6 +27,8 @@ bits_emit_kernel(const uint32_t* __restrict__ bits_in, int clear, const int* __r
                  const int* __restrict__ perm, const float* __restrict__ fs, int max_out,
                  int64_t* __restrict__ keep, float* __restrict__ keep_fs, int64_t* __restrict__ counts)
 {
+    pdl_wait();
+    pdl_release();
     __shared__ int scratch[32];
     const int n = m_dev ? *m_dev : m_bound;
     const int NW = (n + 31) / 32;
@@ -87,14 +89,15 @@ bits_emit_kernel(const uint32_t* __restrict__ bits_in, int clear, const int* __r
 void launch_fast_emit(const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm, int max_out,
                       int64_t* keep, int64_t* counts, cudaStream_t st)
 {
-    bits_emit_kernel<<<1, FE_THREADS, 0, st>>>(reinterpret_cast<const uint32_t*>(haspred), 1, m_dev, m_bound,
-                                               perm, nullptr, max_out, keep, nullptr, counts);
+    launch_pdl(bits_emit_kernel, dim3(1), dim3(FE_THREADS), 0, st, reinterpret_cast<const uint32_t*>(haspred), 1,
+               m_dev, m_bound, perm, nullptr, max_out, keep, nullptr, counts);
 }
 
 void launch_bits_emit(const uint32_t* bits, const int* m_dev, int m_bound, const int* perm, const float* fs,
                       int max_out, int64_t* keep, float* keep_fs, int64_t* counts, cudaStream_t st)
 {
-    bits_emit_kernel<<<1, FE_THREADS, 0, st>>>(bits, 0, m_dev, m_bound, perm, fs, max_out, keep, keep_fs, counts);
+    launch_pdl(bits_emit_kernel, dim3(1), dim3(FE_THREADS), 0, st, bits, 0, m_dev, m_bound, perm, fs, max_out, keep,
+               keep_fs, counts);
 }
 
 }  // namespace gbnms

@@ -367,7 +367,7 @@ __device__ __forceinline__ bool mark_pair(uint2* KR, uint8_t* BLK, uint32_t e, u
 // the pairs at t, t + RV_THREADS, ... and compacts its own share in place.
 // A pair leaves the list once its source is decided; while the source is
 // open the target is open too (a box is decided only after all its sources).
-__device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedges, unsigned E,
+__device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedges, unsigned E, unsigned cap_words,
                               const uint32_t* __restrict__ haspred, int n, int NWp,
                               const int* __restrict__ perm, int max_out, int64_t* __restrict__ keep,
                               int64_t* __restrict__ counts, int32_t* status, uint32_t* sm,
@@ -384,20 +384,32 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
     const int NW = (n + 31) / 32;
 
     // Stage the list with bulk copies (the list is 16-byte aligned and padded
-    // to a multiple of 4 pairs) while the bitmaps are set up.
+    // to a multiple of 4 pairs) while the bitmaps are set up; the sort
+    // permutation follows it when both fit (the output then maps positions
+    // from shared memory).
     const unsigned bytes = 16u * ((E + 3) / 4);
     const unsigned ncopy = (bytes + GR_COPY - 1) / GR_COPY;
+    const unsigned pbytes = 16u * ((static_cast<unsigned>(n) + 3) / 4);
+    const bool perm_here = perm && (bytes + pbytes) / 4 <= cap_words;
+    const int* perm_s = perm_here ? reinterpret_cast<const int*>(reinterpret_cast<const char*>(Es) + bytes) : nullptr;
+    const unsigned pcopy = perm_here ? (pbytes + GR_COPY - 1) / GR_COPY : 0u;
     if (tid == 0) {
         mbar_init(bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     __syncthreads();
-    if (tid == 0 && bytes) mbar_expect_tx(bar, bytes);
+    const unsigned tx = bytes + (perm_here ? pbytes : 0u);  // bytes the barrier waits for
+    if (tid == 0 && tx) mbar_expect_tx(bar, tx);
     __syncwarp();
     if (warp == 0 && l < ncopy) {
         const unsigned off = l * GR_COPY;
         const unsigned len = min(static_cast<unsigned>(GR_COPY), bytes - off);
         bulk_g2s(reinterpret_cast<char*>(Es) + off, reinterpret_cast<const char*>(gedges) + off, len, bar);
+    }
+    if (warp == 1 && l < pcopy) {
+        const unsigned off = l * GR_COPY;
+        const unsigned len = min(static_cast<unsigned>(GR_COPY), pbytes - off);
+        bulk_g2s(reinterpret_cast<char*>(Es) + bytes + off, reinterpret_cast<const char*>(perm) + off, len, bar);
     }
     for (int w = tid; w < NW; w += RV_THREADS) {
         KR[w] = make_uint2(0u, 0u);
@@ -410,7 +422,7 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
         bq[1] = make_uint4(bx[4], bx[5], bx[6], bx[7]);
     }
     bool copied = true;
-    if (bytes) {
+    if (tx) {
         long long tries = 0;
         while (!mbar_try_wait(bar, 0)) {
             if (++tries > RV_WAIT_LIMIT) { copied = false; break; }
@@ -488,7 +500,7 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
         for (int u = 0; u < OW; ++u) {
             bits[u] = wb + u < w1 ? KR[wb + u].x : 0u;
             const int j = 32 * (wb + u) + static_cast<int>(l);
-            v[u] = ((bits[u] >> l) & 1u) ? (perm ? perm[j] : j) : 0;
+            v[u] = ((bits[u] >> l) & 1u) ? (perm_s ? perm_s[j] : perm ? perm[j] : j) : 0;
         }
 #pragma unroll
         for (int u = 0; u < OW; ++u) {
@@ -525,7 +537,7 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
     if (done_out && threadIdx.x == 0) *done_out = n >= n_all;  // raised below on max_out
     if (edges) {
         const unsigned E = *ecount;
-        if (E <= ecap && graph_resolve(edges, E, haspred, n, graph_words(m_bound), perm, max_out,
+        if (E <= ecap && graph_resolve(edges, E, ecap, haspred, n, graph_words(m_bound), perm, max_out,
                                        keep, counts, status, reinterpret_cast<uint32_t*>(smem),
                                        done_out))
             return;

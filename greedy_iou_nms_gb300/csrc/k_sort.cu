@@ -327,6 +327,7 @@ merge_level_kernel(const uint64_t* __restrict__ keys_in, uint64_t* __restrict__ 
 {
     __shared__ __align__(16) uint64_t buf[ML_SLOTS];  // ML_TILE keys, A part then B part, skewed
     __shared__ int split[2];
+    pdl_wait();
     pdl_release();
     const int tid = threadIdx.x;
     const int o0 = blockIdx.x * ML_TILE;
@@ -400,8 +401,8 @@ void launch_sort(const float* scores, const float4* boxes, const int* cand, cons
     const int tiles = chunks * (MS_CHUNK / ML_TILE);
     for (int run = MS_CHUNK; run < chunks * MS_CHUNK; run *= 2) {
         const bool last = 2 * run >= chunks * MS_CHUNK;
-        merge_level_kernel<<<tiles, ML_THREADS, 0, st>>>(k0, k1, run, last ? 1 : 0, m_dev, m_bound,
-                                                         boxes, perm, boxes_s);
+        launch_pdl(merge_level_kernel, dim3(tiles), dim3(ML_THREADS), 0, st, k0, k1, run, last ? 1 : 0, m_dev,
+                   m_bound, boxes, perm, boxes_s);
         uint64_t* t = k0;
         k0 = k1;
         k1 = t;

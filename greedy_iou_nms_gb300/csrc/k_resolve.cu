@@ -478,19 +478,11 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
     for (int d = 16; d > 0; d >>= 1) c += __shfl_xor_sync(FULL, c, d);
     if (l == 0) scratch[warp] = c;
     __syncthreads();
-    if (warp == 0) {
-        int v = scratch[l];
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(FULL, v, d);
-            if (static_cast<int>(l) >= d) v += y;
-        }
-        scratch[l] = v;
-    }
-    __syncthreads();
-    const int total = scratch[31];
+    // Every warp sums the counts of the warps before it (one barrier).
+    const int wc = scratch[l];
+    const int total = __reduce_add_sync(FULL, wc);
     const int cap = max_out > 0 ? max_out : INT_MAX;
-    int base = warp ? scratch[warp - 1] : 0;
+    int base = __reduce_add_sync(FULL, static_cast<int>(l) < warp ? wc : 0);
     const uint32_t below = (1u << l) - 1u;
     constexpr int OW = 8;  // words whose loads are in flight together
     for (int wb = w0; wb < w1 && base < cap; wb += OW) {

@@ -54,7 +54,7 @@ def _load():
         lib.oracle_nms.restype = ctypes.c_int64
         lib.oracle_fast_nms.argtypes = lib.oracle_nms.argtypes
         lib.oracle_fast_nms.restype = ctypes.c_int64
-        lib.oracle_matrix_nms.argtypes = [f32p, f32p, ctypes.c_int64, ctypes.c_float, ctypes.c_int,
+        lib.oracle_matrix_nms.argtypes = [f32p, f32p, ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_float, ctypes.c_float, ctypes.c_int32, i64p, f32p]
         lib.oracle_matrix_nms.restype = ctypes.c_int64
         lib.oracle_score_order.argtypes = [f32p, i64p, ctypes.c_int64]
@@ -119,16 +119,20 @@ def nms_single(boxes, scores, iou_thr, *, max_out=0, score_thr=None, fast=False)
     return keep[: counts[0]].copy()
 
 
-def matrix_nms(boxes, scores, decay_thr, *, sigma=0.5, score_thr=None, max_out=0):
-    """Matrix NMS (Gaussian decay) of one image: (kept indices in score order,
+def matrix_nms(boxes, scores, decay_thr, *, sigma=0.5, decay="gaussian", score_thr=None, max_out=0):
+    """Matrix NMS of one image with the Gaussian (exp((O_max^2 - O^2)/sigma))
+    or the linear ((1 - O)/(1 - O_max)) decay: (kept indices in score order,
     their final scores as binary32)."""
+    if decay not in ("gaussian", "linear"):
+        raise ValueError("matrix_nms: decay must be 'gaussian' or 'linear'")
     bx = np.ascontiguousarray(boxes, dtype=np.float32).reshape(-1, 4)
     sc = np.ascontiguousarray(scores, dtype=np.float32).reshape(-1)
     n = sc.shape[0]
     keep = np.full(max(n, 1), -1, dtype=np.int64)
     fs = np.zeros(max(n, 1), dtype=np.float32)
     k = _load().oracle_matrix_nms(_ptr(bx, ctypes.c_float), _ptr(sc, ctypes.c_float), n,
-                                  float(np.float32(sigma)), 0 if score_thr is None else 1,
+                                  float(np.float32(sigma)), 1 if decay == "linear" else 0,
+                                  0 if score_thr is None else 1,
                                   float(np.float32(score_thr if score_thr is not None else 0.0)),
                                   float(np.float32(decay_thr)), int(max_out),
                                   _ptr(keep, ctypes.c_int64), _ptr(fs, ctypes.c_float))

@@ -20,7 +20,7 @@
  *     lower index has priority, and suppression only happens between boxes of
  *     the same class.
  *
- * Readings where the pages are silent (each one also listed in the design doc):
+ * Readings where the pages are silent:
  *   - IoU on continuous xyxy coordinates, no "+1"; every step in IEEE binary32
  *     with round-to-nearest-even, in the fixed order of oracle_iou() below, no
  *     fused multiply-add (this file must be built with -ffp-contract=off and
@@ -158,7 +158,7 @@ int64_t oracle_nms(const float* boxes, const float* scores, int64_t n,
  *     IoU above the threshold.  Section 2.1: without the index tie-break,
  *     equal-score overlapping boxes would all drop each other.
  *
- * Readings (also in the design doc): the output is the kept indices in the same
+ * Readings: the output is the kept indices in the same
  * priority order as greedy NMS, cut at max_out; the pre-filter and the batch
  * layout are those of oracle_nms.
  */
@@ -212,7 +212,7 @@ int64_t oracle_fast_nms(const float* boxes, const float* scores, int64_t n,
 }
 
 /*
- * Matrix NMS, Gaussian decay, one image:
+ * Matrix NMS, one image, Gaussian (linear == 0) or linear (linear != 0) decay:
  *
  *   "Fastest Matrix NMS in the West (Part 2)", section "What do we need to
  *   compute?": with boxes sorted by score (highest first), O[i][j] is the IoU
@@ -221,18 +221,22 @@ int64_t oracle_fast_nms(const float* boxes, const float* scores, int64_t n,
  *   gives box j is exp((O_max[i]^2 - O[i][j]^2) / sigma), and the final score
  *   is s'[j] = s[j] * min over fathers i of that decay.  Section
  *   "Optimization 4": a box is dropped when its final score is below the
- *   threshold t.
+ *   threshold t.  The same section says the code also holds a linear decay;
+ *   the page does not print it.  The reading taken is the linear kernel of
+ *   the Matrix NMS method with the same compensation by the father's own
+ *   largest overlap: the decay is (1 - O[i][j]) / (1 - O_max[i]).
  *
- * Readings (also in the design doc): the sort is the stable descending one of
+ * Readings: the sort is the stable descending one of
  * greedy NMS (ties to the lower index) over the pre-filtered candidates; IoUs
  * are the canonical binary32 ones; a box with no father (the first) keeps
  * s[j] (the minimum over no fathers is 1); the exponent, the exponential, the
  * product and the comparison are evaluated in binary64 from those binary32
- * values, with NaN decays ignored by the minimum; the output is the kept
+ * values, with NaN decays (the linear 0/0 of a father that fully overlaps
+ * its own father and the box) ignored by the minimum; the output is the kept
  * indices in score order with their final scores rounded to binary32, cut at
  * max_out.  This is the literal O(n^2) evaluation.
  */
-int64_t oracle_matrix_nms(const float* boxes, const float* scores, int64_t n, float sigma,
+int64_t oracle_matrix_nms(const float* boxes, const float* scores, int64_t n, float sigma, int linear,
                           int use_score_thr, float score_thr, float decay_thr, int32_t max_out,
                           int64_t* keep, float* out_scores)
 {
@@ -257,8 +261,13 @@ int64_t oracle_matrix_nms(const float* boxes, const float* scores, int64_t n, fl
         double dmin = 1.0;
         for (int64_t q = 0; q < p; ++q) {
             float o = oracle_iou(boxes + 4 * order[q], boxes + 4 * order[p]);
-            double x = ((double)omax[q] * (double)omax[q] - (double)o * (double)o) / (double)sigma;
-            double d = exp(x);
+            double d;
+            if (linear) {
+                d = (1.0 - (double)o) / (1.0 - (double)omax[q]);
+            } else {
+                double x = ((double)omax[q] * (double)omax[q] - (double)o * (double)o) / (double)sigma;
+                d = exp(x);
+            }
             if (d < dmin) dmin = d;
         }
         double fs = (double)scores[order[p]] * dmin;

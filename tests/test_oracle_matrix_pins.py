@@ -123,3 +123,88 @@ def test_invariants(seed):
     assert k3.tolist() == kf.tolist()[:9] and f3.tolist() == ff.tolist()[:9]
     kp, _ = oracle.matrix_nms(b, s, 0.0, score_thr=0.5)
     assert all(s[i] > np.float32(0.5) for i in kp)
+
+
+# ------------------------------------------------------------- linear decay
+#
+# The page names a linear decay without printing it; the reading is
+# d_ij = (1 - O_ij) / (1 - O_max,i), the linear kernel with the same
+# compensation.  Pins by closed forms and hand-worked rationals.
+
+def test_linear_disjoint_and_exact_pair():
+    b = np.array([[0, 0, 1, 1], [5, 5, 6, 6], [10, 0, 11, 1]], np.float32)
+    s = np.array([0.9, 0.2, 0.6], np.float32)
+    keep, fs = oracle.matrix_nms(b, s, 0.0, decay="linear")
+    assert keep.tolist() == [0, 2, 1] and fs.tolist() == [np.float32(0.9), np.float32(0.6), np.float32(0.2)]
+    # IoU 1/2 exactly, father without fathers: decay (1 - 1/2) / 1
+    b = np.array([[0, 0, 4, 4], [0, 0, 4, 2]], np.float32)
+    s = np.array([0.9, 0.8], np.float32)
+    keep, fs = oracle.matrix_nms(b, s, 0.0, decay="linear")
+    assert keep.tolist() == [0, 1]
+    assert fs[1] == np.float32(float(np.float32(0.8)) * 0.5)
+    assert oracle.matrix_nms(b, s, np.float32(0.8) * np.float32(0.5), decay="linear")[0].tolist() == [0, 1]
+    assert oracle.matrix_nms(b, s, np.nextafter(np.float32(0.4), np.float32(1)), decay="linear")[0].tolist() == [0]
+
+
+def test_linear_identical_boxes():
+    """The second box overlaps its top father at 1: decay 0.  Later fathers
+    that overlap their own father at 1 give 0/0 (ignored) or x/0 (no effect)."""
+    k = 5
+    b = np.tile(np.array([[3, 3, 9, 7]], np.float32), (k, 1))
+    s = np.linspace(0.9, 0.5, k).astype(np.float32)
+    keep, fs = oracle.matrix_nms(b, s, 0.0, decay="linear")
+    assert keep.tolist() == list(range(k))
+    assert fs[0] == s[0] and all(f == 0.0 for f in fs[1:])
+    assert oracle.matrix_nms(b, s, 1e-30, decay="linear")[0].tolist() == [0]
+
+
+def test_linear_father_with_full_overlap():
+    """A and A' identical (O_max of A' is 1), C overlaps both at IoU 1/2: the
+    A' term is 0.5/0 = +inf and does not count; C decays by 1/2 from A."""
+    b = np.array([[0, 0, 4, 4], [0, 0, 4, 4], [0, 0, 4, 2]], np.float32)
+    s = np.array([0.9, 0.8, 0.7], np.float32)
+    keep, fs = oracle.matrix_nms(b, s, 0.0, decay="linear")
+    assert keep.tolist() == [0, 1, 2]
+    assert fs[1] == 0.0 and fs[2] == np.float32(float(np.float32(0.7)) * 0.5)
+
+
+def test_linear_chain_hand_worked():
+    """a=[0,0,10,1], b=[3,0,13,1], c=[6,0,16,1]: IoU(a,b) = IoU(b,c) = 7/13,
+    IoU(a,c) = 1/4; O_max of b is 7/13.  b decays by 1 - 7/13 = 6/13 (from a);
+    c by min(1 - 1/4 (from a), (1 - 7/13) / (1 - 7/13) = 1 (from b)) = 3/4."""
+    b = np.array([[0, 0, 10, 1], [3, 0, 13, 1], [6, 0, 16, 1]], np.float32)
+    s = np.array([0.9, 0.8, 0.7], np.float32)
+    keep, fs = oracle.matrix_nms(b, s, 0.0, decay="linear")
+    o = float(np.float32(7 / 13))  # the binary32 IoU of the two 7/13 pairs
+    assert keep.tolist() == [0, 1, 2]
+    assert fs[1] == np.float32(float(np.float32(0.8)) * (1.0 - o))
+    assert fs[2] == np.float32(float(np.float32(0.7)) * 0.75)
+    assert abs(float(fs[1]) - 0.8 * 6 / 13) < 1e-6
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_linear_exists_restatement(seed):
+    """The existence form of the drop rule ("Optimization 4") with the linear
+    decay, pair by pair from the binary32 IoUs (NaN terms never drop)."""
+    rng = np.random.default_rng(20 + seed)
+    n = 60
+    b, s = _clustered(rng, n)
+    t = 0.25
+    keep, _ = oracle.matrix_nms(b, s, t, decay="linear")
+    order = oracle.score_order(s)
+    O = np.zeros((n, n))
+    for p in range(n):
+        for q in range(p):
+            O[q, p] = float(oracle.iou(b[order[q]], b[order[p]]))
+    omax = np.array([max([O[q, p] for q in range(p)], default=0.0) for p in range(n)])
+    kept = []
+    for p in range(n):
+        sj = float(s[order[p]])
+        drop = sj < t
+        for q in range(p):
+            den = 1.0 - omax[q]
+            if den > 0 and sj * ((1.0 - O[q, p]) / den) < t:
+                drop = True
+        if not drop:
+            kept.append(int(order[p]))
+    assert keep.tolist() == kept

@@ -220,9 +220,10 @@ def time_workload(g, torch, wl, dev, flush, reps=30, fast=False):
             "kept": int(counts.sum().item()), "batched": batched}
 
 
-def time_matrix(g, torch, wl, dev, flush, decay_thr=0.1, reps=20):
-    """Device time of one nms_matrix_run call (Gaussian decay, sigma 0.5) on
-    a one-image workload: median, p10, p90 in microseconds."""
+def time_matrix(g, torch, wl, dev, flush, decay_thr=0.1, reps=20, decay=0):
+    """Device time of one nms_matrix_run call (Gaussian decay with sigma 0.5,
+    or the linear decay) on a one-image workload: median, p10, p90 in
+    microseconds."""
     stream = torch.cuda.current_stream(dev)
     boxes = torch.from_numpy(wl.boxes).to(dev)
     scores = torch.from_numpy(wl.scores).to(dev)
@@ -236,7 +237,7 @@ def time_matrix(g, torch, wl, dev, flush, decay_thr=0.1, reps=20):
     score_thr = -math.inf if wl.score_thr is None else wl.score_thr
 
     def call():
-        st = g.nms_matrix_run(boxes.data_ptr(), scores.data_ptr(), n, 0.5, score_thr, decay_thr, wl.max_out,
+        st = g.nms_matrix_run(boxes.data_ptr(), scores.data_ptr(), n, decay, 0.5, score_thr, decay_thr, wl.max_out,
                               keep.data_ptr(), ks.data_ptr(), cap, count.data_ptr(), 0, ws.data_ptr(), wsb,
                               stream.cuda_stream)
         if st != g.NMS_OK:
@@ -411,15 +412,16 @@ def run_gbnms(args):
         roof = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
                 "frac": ach / hbm, "traffic": _ncu_traffic(dominant), "note": note}
 
-    per_config = fast_nms = matrix_nms = None
+    per_config = fast_nms = matrix_nms = matrix_lin = None
     if not args.no_configs:
-        per_config, fast_nms, matrix_nms = {}, {}, {}
+        per_config, fast_nms, matrix_nms, matrix_lin = {}, {}, {}, {}
         for name in W.CONFIGS:
             wl_c = W.make(name, 0)
             per_config[name] = time_workload(g, torch, wl_c, dev, flush)
             fast_nms[name] = time_workload(g, torch, wl_c, dev, flush, fast=True)
             if wl_c.class_ids is None and wl_c.batch_offsets is None:
                 matrix_nms[name] = time_matrix(g, torch, wl_c, dev, flush)
+                matrix_lin[name] = time_matrix(g, torch, wl_c, dev, flush, decay=g.NMS_DECAY_LINEAR)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -443,6 +445,7 @@ def run_gbnms(args):
         "per_config": per_config,
         "fast_nms_per_config": fast_nms,
         "matrix_nms_per_config": matrix_nms,
+        "matrix_nms_linear_per_config": matrix_lin,
         "roofline": roof,
         "roofline_iou_mask": mask_roof,
         "cpu_baseline": cpu,

@@ -26,6 +26,8 @@ NMS_ERR_WORKSPACE = 2
 NMS_ERR_CAPACITY = 3
 NMS_ERR_CUDA = 4
 NMS_ERR_TIMEOUT = 5
+NMS_DECAY_GAUSSIAN = 0  # nms_matrix_run decay kernels
+NMS_DECAY_LINEAR = 1
 NMS_MAX_SINGLE_N = 1 << 18
 
 EXPORTED = ("nms_status_string", "nms_workspace_size", "nms_run", "nms_fast_run", "nms_run_timed",
@@ -65,7 +67,7 @@ def load():
     lib.nms_run.restype = ctypes.c_int
     lib.nms_matrix_workspace_size.argtypes = [i64, ctypes.POINTER(sz)]
     lib.nms_matrix_workspace_size.restype = ctypes.c_int
-    lib.nms_matrix_run.argtypes = [vp, vp, i64, f32, f32, f32, i32, vp, vp, i64, vp, vp, vp, sz, vp]
+    lib.nms_matrix_run.argtypes = [vp, vp, i64, i32, f32, f32, f32, i32, vp, vp, i64, vp, vp, vp, sz, vp]
     lib.nms_matrix_run.restype = ctypes.c_int
     lib.nms_fast_run.argtypes = lib.nms_run.argtypes
     lib.nms_fast_run.restype = ctypes.c_int
@@ -134,20 +136,24 @@ def nms_matrix_workspace_size(n: int) -> int:
     return out.value
 
 
-def nms_matrix_run(boxes: int, scores: int, n: int, sigma: float, score_thr: float, decay_thr: float,
-                   max_out: int, keep: int, keep_scores: int, keep_cap: int, count: int, dev_status: int,
-                   workspace: int, workspace_bytes: int, stream: int) -> int:
-    """Matrix NMS through the C entry point (device addresses as ints)."""
-    return load().nms_matrix_run(boxes or None, scores or None, int(n), float(sigma), float(score_thr),
+def nms_matrix_run(boxes: int, scores: int, n: int, decay: int, sigma: float, score_thr: float,
+                   decay_thr: float, max_out: int, keep: int, keep_scores: int, keep_cap: int, count: int,
+                   dev_status: int, workspace: int, workspace_bytes: int, stream: int) -> int:
+    """Matrix NMS through the C entry point (device addresses as ints; decay is
+    NMS_DECAY_GAUSSIAN or NMS_DECAY_LINEAR)."""
+    return load().nms_matrix_run(boxes or None, scores or None, int(n), int(decay), float(sigma), float(score_thr),
                                  float(decay_thr), int(max_out), keep or None, keep_scores or None,
                                  int(keep_cap), count or None, dev_status or None, workspace or None,
                                  int(workspace_bytes), stream or None)
 
 
-def matrix_nms(boxes, scores, decay_thr: float, *, sigma: float = 0.5, score_thr: Optional[float] = None,
-               max_out: int = 0):
-    """Matrix NMS (Gaussian decay) on CUDA tensors: (kept int64 indices in score
-    order, their float32 final scores).  Synchronises the current stream once."""
+def matrix_nms(boxes, scores, decay_thr: float, *, sigma: float = 0.5, decay: str = "gaussian",
+               score_thr: Optional[float] = None, max_out: int = 0):
+    """Matrix NMS on CUDA tensors with the Gaussian or the linear decay: (kept
+    int64 indices in score order, their float32 final scores).  Synchronises
+    the current stream once."""
+    if decay not in ("gaussian", "linear"):
+        raise ValueError("matrix_nms: decay must be 'gaussian' or 'linear'")
     torch = _torch()
     if not (boxes.is_cuda and scores.is_cuda):
         raise ValueError("matrix_nms: boxes and scores must be CUDA tensors")
@@ -161,7 +167,8 @@ def matrix_nms(boxes, scores, decay_thr: float, *, sigma: float = 0.5, score_thr
     count = torch.empty(1, dtype=torch.int64, device=dev)
     ws_bytes = nms_matrix_workspace_size(n)
     ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-    st = nms_matrix_run(boxes.data_ptr() if n else 0, scores.data_ptr() if n else 0, n, sigma,
+    st = nms_matrix_run(boxes.data_ptr() if n else 0, scores.data_ptr() if n else 0, n,
+                        NMS_DECAY_LINEAR if decay == "linear" else NMS_DECAY_GAUSSIAN, sigma,
                         -math.inf if score_thr is None else score_thr, decay_thr, max_out, keep.data_ptr(),
                         ks.data_ptr(), cap, count.data_ptr(), 0, ws.data_ptr(), ws_bytes,
                         torch.cuda.current_stream(dev).cuda_stream)

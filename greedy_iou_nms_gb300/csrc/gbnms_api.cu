@@ -392,15 +392,16 @@ extern "C" nms_status nms_matrix_workspace_size(int64_t n, size_t* bytes)
     return NMS_OK;
 }
 
-extern "C" nms_status nms_matrix_run(const float* boxes, const float* scores, int64_t n, float sigma,
-                                     float score_thr, float decay_thr, int32_t max_out, int64_t* keep,
-                                     float* keep_scores, int64_t keep_cap, int64_t* count,
+extern "C" nms_status nms_matrix_run(const float* boxes, const float* scores, int64_t n, int32_t decay,
+                                     float sigma, float score_thr, float decay_thr, int32_t max_out,
+                                     int64_t* keep, float* keep_scores, int64_t keep_cap, int64_t* count,
                                      int32_t* dev_status, void* workspace, size_t workspace_bytes,
                                      void* stream)
 {
     if (n < 0) return NMS_ERR_INVALID_ARG;
-    if (!(sigma > 0.0f) || std::isinf(sigma) || std::isnan(score_thr) || std::isnan(decay_thr))
-        return NMS_ERR_INVALID_ARG;
+    if (decay != NMS_DECAY_GAUSSIAN && decay != NMS_DECAY_LINEAR) return NMS_ERR_INVALID_ARG;
+    if (decay == NMS_DECAY_GAUSSIAN && (!(sigma > 0.0f) || std::isinf(sigma))) return NMS_ERR_INVALID_ARG;
+    if (std::isnan(score_thr) || std::isnan(decay_thr)) return NMS_ERR_INVALID_ARG;
     if (n > 0 && (!boxes || !scores || !aligned(boxes, 16))) return NMS_ERR_INVALID_ARG;
     if (!keep || !count || keep_cap < 0) return NMS_ERR_INVALID_ARG;
     if (n > NMS_MAX_SINGLE_N) return NMS_ERR_CAPACITY;
@@ -429,7 +430,8 @@ extern "C" nms_status nms_matrix_run(const float* boxes, const float* scores, in
     uint64_t* keys = sort_keys_bytes(static_cast<int>(n)) ? at<uint64_t>(workspace, L.keys) : nullptr;
     launch_sort(scores, reinterpret_cast<const float4*>(boxes), cand, m_count, static_cast<int>(n), perm, boxes_s,
                 keys, status, nullptr, 1, nullptr, nullptr, nullptr, st);
-    launch_matrix(boxes_s, scores, perm, m_count, static_cast<int>(n), sigma, decay_thr, max_out,
+    launch_matrix(boxes_s, scores, perm, m_count, static_cast<int>(n), sigma, decay == NMS_DECAY_LINEAR ? 1 : 0,
+                  decay_thr, max_out,
                   at<unsigned>(workspace, L.omax), at<unsigned long long>(workspace, L.xmin),
                   at<float>(workspace, L.fs), at<uint32_t>(workspace, L.kept), keep, keep_scores, count, st);
     return cuda_status();

@@ -111,11 +111,12 @@ void launch_fast_emit(const uint64_t* haspred, const int* m_dev, int m_bound, co
 void launch_bits_emit(const uint32_t* bits, const int* m_dev, int m_bound, const int* perm, const float* fs,
                       int max_out, int64_t* keep, float* keep_fs, int64_t* counts, cudaStream_t st);
 
-// Matrix NMS (Gaussian decay) of the sorted boxes: zeroes its scratch, runs
-// the two tiled passes, decides every box and writes the kept indices, their
-// final scores and the count.  fs: n floats, kept: ceil(n/32) words of scratch.
+// Matrix NMS (Gaussian decay, or linear when `linear`) of the sorted boxes:
+// zeroes its scratch, runs the two tiled passes, decides every box and writes
+// the kept indices, their final scores and the count.  fs: n floats, kept:
+// ceil(n/32) words of scratch.
 void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, const int* m_dev, int m_bound,
-                   float sigma, float decay_thr, int max_out, unsigned* omax_bits,
+                   float sigma, int linear, float decay_thr, int max_out, unsigned* omax_bits,
                    unsigned long long* xmin_key, float* fs, uint32_t* kept, int64_t* keep, float* keep_scores,
                    int64_t* count, cudaStream_t st);
 

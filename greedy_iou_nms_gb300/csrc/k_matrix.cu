@@ -1,4 +1,4 @@
-// Matrix NMS with Gaussian decay, one image.
+// Matrix NMS with Gaussian or linear decay, one image.
 //
 // "Fastest Matrix NMS in the West (Part 2)", section "What do we need to
 // compute?": boxes sorted by score, O[i][j] the IoU of box j with its father
@@ -23,6 +23,13 @@
 //           clear of the threshold by more than its error bound, in binary64
 //           otherwise, into a kept bitmap and a final-score array;
 //   emit:   the kept boxes in score order with their final scores.
+//
+// Linear decay (1 - O[i][j]) / (1 - O_max[i]): the same section of the page
+// says the code holds a linear formula without printing it; this is the
+// linear kernel with the same compensation.  A non-overlapping father gives
+// 1 / (1 - O_max[i]) >= 1, so again only overlapping pairs count.  Pass B
+// takes the binary64 quotient itself (a father with O_max = 1 gives x/0 or
+// 0/0, which the minimum ignores), and the decide multiplies in binary64.
 
 #include "common.cuh"
 #include "internal.h"
@@ -58,16 +65,19 @@ __device__ __forceinline__ unsigned fkey(float x)
 __device__ __forceinline__ unsigned fkey_value(unsigned k) { return (k >> 31) ? (k & 0x7fffffffu) : ~k; }
 
 // Linear index k of the triangle of MX_T x MX_T tiles, column by column ->
-// (row tile a, column tile c), a <= c.
+// (row tile a, column tile c), a <= c.  A binary32 estimate made exact by the
+// integer corrections.
 __device__ __forceinline__ void mx_coords(long long k, int& a, int& c)
 {
-    long long cc = static_cast<long long>((sqrt(8.0 * static_cast<double>(k) + 1.0) - 1.0) * 0.5);
+    long long cc = static_cast<long long>((sqrtf(8.0f * static_cast<float>(k) + 1.0f) - 1.0f) * 0.5f);
+    if (cc < 0) cc = 0;
     while ((cc + 1) * (cc + 2) / 2 <= k) ++cc;
-    while (cc * (cc + 1) / 2 > k) --cc;
+    while (cc > 0 && cc * (cc + 1) / 2 > k) --cc;
     c = static_cast<int>(cc);
     a = static_cast<int>(k - cc * (cc + 1) / 2);
 }
 
+// PASS 0: O_max; 1: smallest Gaussian numerator; 2: smallest linear decay.
 template <int PASS>
 __global__ void __launch_bounds__(MX_THREADS)
 matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_dev, int m_bound,
@@ -93,7 +103,7 @@ matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m
     const float4 r1 = v1 ? boxes_s[i1] : make_float4(0.f, 0.f, 0.f, 0.f);
     const float ar0 = box_area(r0), ar1 = box_area(r1);
     double om0 = 0.0, om1 = 0.0;
-    if (PASS == 1) {
+    if (PASS >= 1) {
         if (v0) om0 = static_cast<double>(__uint_as_float(omax_bits[i0]));
         if (v1) om1 = static_cast<double>(__uint_as_float(omax_bits[i1]));
     }
@@ -122,6 +132,38 @@ matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m
             const unsigned m = max(ov0 ? __float_as_uint(o0) : 0u, ov1 ? __float_as_uint(o1) : 0u);
             const unsigned r = __reduce_max_sync(FULL, m);
             if (l == 0 && r) atomicMax(omax_bits + j, r);
+        } else if (PASS == 2) {
+            // Smallest decay (1 - O[i][j]) / (1 - O_max[i]) over the warp's
+            // rows, one atomic.  Rows bound their quotient in binary32 (three
+            // roundings, each within 2^-24 relative; a margin of 2^-20), and
+            // only rows whose lower bound does not exceed the smallest upper
+            // bound take the binary64 quotient.  O_max = 1 (a zero
+            // denominator, the same in both precisions) contributes nothing.
+            float lo0 = INFINITY, lo1 = INFINITY, ub = INFINITY;
+            const bool d0 = ov0 && static_cast<float>(om0) < 1.0f, d1 = ov1 && static_cast<float>(om1) < 1.0f;
+            if (d0) {
+                const float q = __fdiv_rn(__fsub_rn(1.0f, o0), __fsub_rn(1.0f, static_cast<float>(om0)));
+                const float e = __fmul_rn(q, 0x1p-20f);
+                lo0 = q - e;
+                ub = q + e;
+            }
+            if (d1) {
+                const float q = __fdiv_rn(__fsub_rn(1.0f, o1), __fsub_rn(1.0f, static_cast<float>(om1)));
+                const float e = __fmul_rn(q, 0x1p-20f);
+                lo1 = q - e;
+                ub = fminf(ub, q + e);
+            }
+            const float best = __uint_as_float(fkey_value(__reduce_min_sync(FULL, fkey(ub))));
+            unsigned long long key = ~0ull;
+            if (d0 && !(lo0 > best))
+                key = dkey(__ddiv_rn(__dsub_rn(1.0, static_cast<double>(o0)), __dsub_rn(1.0, om0)));
+            if (d1 && !(lo1 > best))
+                key = min(key, dkey(__ddiv_rn(__dsub_rn(1.0, static_cast<double>(o1)), __dsub_rn(1.0, om1))));
+            const unsigned hi = __reduce_min_sync(FULL, static_cast<unsigned>(key >> 32));
+            const unsigned lo = __reduce_min_sync(FULL, static_cast<unsigned>(key >> 32) == hi
+                                                            ? static_cast<unsigned>(key) : ~0u);
+            const unsigned long long mk = (static_cast<unsigned long long>(hi) << 32) | lo;
+            if (l == 0 && mk != ~0ull) atomicMin(xmin_key + j, mk);
         } else {
             // Smallest numerator O_max[i]^2 - O[i][j]^2 (binary64, products
             // exact, one rounding) over the warp's rows, one atomic.  Only
@@ -171,14 +213,22 @@ matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m
 __global__ void __launch_bounds__(256)
 matrix_decide_kernel(const float* __restrict__ scores, const int* __restrict__ perm,
                      const unsigned long long* __restrict__ xmin_key, const int* __restrict__ m_dev,
-                     int m_bound, float sigma, float decay_thr, float* __restrict__ fs_out,
+                     int m_bound, float sigma, int linear, float decay_thr, float* __restrict__ fs_out,
                      uint32_t* __restrict__ kept)
 {
     const int n = m_dev ? *m_dev : m_bound;
     const int j = blockIdx.x * blockDim.x + threadIdx.x;
     if (j - static_cast<int>(lane_id()) >= n) return;  // whole warp past the end
     bool keep_j = false;
-    if (j < n) {
+    if (j < n && linear) {
+        // s * min(1, smallest decay) and the comparison, in binary64
+        const float s = scores[perm[j]];
+        const unsigned long long k = xmin_key[j];
+        const double m = k == ~0ull ? 1.0 : fmin(dkey_value(k), 1.0);
+        const double fd = __dmul_rn(static_cast<double>(s), m);
+        fs_out[j] = static_cast<float>(fd);
+        keep_j = !(fd < static_cast<double>(decay_thr));
+    } else if (j < n) {
         const float s = scores[perm[j]];
         const unsigned long long k = xmin_key[j];
         // the smallest exponent is the smallest numerator over sigma (a
@@ -206,7 +256,7 @@ matrix_decide_kernel(const float* __restrict__ scores, const int* __restrict__ p
 }
 
 void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, const int* m_dev, int m_bound,
-                   float sigma, float decay_thr, int max_out, unsigned* omax_bits,
+                   float sigma, int linear, float decay_thr, int max_out, unsigned* omax_bits,
                    unsigned long long* xmin_key, float* fs, uint32_t* kept, int64_t* keep, float* keep_scores,
                    int64_t* count, cudaStream_t st)
 {
@@ -217,11 +267,15 @@ void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, 
     if (tiles > 0) {
         matrix_pass_kernel<0><<<static_cast<unsigned>(tiles), MX_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, sigma,
                                                                                  omax_bits, xmin_key);
-        matrix_pass_kernel<1><<<static_cast<unsigned>(tiles), MX_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, sigma,
-                                                                                 omax_bits, xmin_key);
+        if (linear)
+            matrix_pass_kernel<2><<<static_cast<unsigned>(tiles), MX_THREADS, 0, st>>>(boxes_s, m_dev, m_bound,
+                                                                                     sigma, omax_bits, xmin_key);
+        else
+            matrix_pass_kernel<1><<<static_cast<unsigned>(tiles), MX_THREADS, 0, st>>>(boxes_s, m_dev, m_bound,
+                                                                                     sigma, omax_bits, xmin_key);
     }
     matrix_decide_kernel<<<(m_bound + 255) / 256, 256, 0, st>>>(scores, perm, xmin_key, m_dev, m_bound, sigma,
-                                                                decay_thr, fs, kept);
+                                                                linear, decay_thr, fs, kept);
     launch_bits_emit(kept, m_dev, m_bound, perm, fs, max_out, keep, keep_scores, count, st);
 }
 

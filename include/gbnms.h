@@ -183,32 +183,43 @@ nms_status nms_fast_run(const float* boxes, const float* scores, int64_t n,
                         int64_t* counts, int32_t* dev_status, void* workspace,
                         size_t workspace_bytes, void* stream);
 
+/* Decay kernels of nms_matrix_run. */
+#define NMS_DECAY_GAUSSIAN 0
+#define NMS_DECAY_LINEAR 1
+
 /*
- * Matrix NMS with Gaussian decay, one image ("Fastest Matrix NMS in the West
- * (Part 2)", sections "What do we need to compute?" and "Optimization 4").
- * Boxes in the greedy order (descending score, ties to the lower index),
- * O[i][j] the canonical binary32 IoU of box j with a father i before it,
- * O_max[i] the largest overlap of box i with its own fathers (0 for none):
- *   s'[j] = s[j] * min over fathers i of exp((O_max[i]^2 - O[i][j]^2) / sigma)
- * (1 for a box without fathers), evaluated in binary64 from the binary32
- * IoUs and scores; box j is dropped when s'[j] < decay_thr.
+ * Matrix NMS, one image ("Fastest Matrix NMS in the West (Part 2)", sections
+ * "What do we need to compute?" and "Optimization 4").  Boxes in the greedy
+ * order (descending score, ties to the lower index), O[i][j] the canonical
+ * binary32 IoU of box j with a father i before it, O_max[i] the largest
+ * overlap of box i with its own fathers (0 for none):
+ *   s'[j] = s[j] * min over fathers i of d[i][j]   (1 without fathers)
+ *   NMS_DECAY_GAUSSIAN: d = exp((O_max[i]^2 - O[i][j]^2) / sigma)
+ *   NMS_DECAY_LINEAR:   d = (1 - O[i][j]) / (1 - O_max[i])
+ * (the page names a linear decay without printing it; this is the linear
+ * kernel with the same compensation), evaluated in binary64 from the binary32
+ * IoUs and scores, NaN terms (a linear 0/0) ignored by the minimum; box j is
+ * dropped when s'[j] < decay_thr.
  *   boxes, scores, n, score_thr, max_out, dev_status, stream: as nms_run
  *                  (one image, one class).
- *   sigma          > 0, finite (the pages use 0.5).
+ *   decay          NMS_DECAY_GAUSSIAN or NMS_DECAY_LINEAR.
+ *   sigma          Gaussian only: > 0, finite (the pages use 0.5); ignored
+ *                  by the linear decay.
  *   decay_thr      threshold on the final scores (not NaN).
  *   keep           device int64 [keep_cap]: kept input indices in score order.
- *   keep_scores    device float [keep_cap] or NULL: their final scores,
- *                  within 4 binary32 ulp of the binary64 value (exactly it
- *                  rounded when the score lies near decay_thr).
+ *   keep_scores    device float [keep_cap] or NULL: their final scores, the
+ *                  binary64 value rounded (linear), or within 4 binary32 ulp
+ *                  of it (Gaussian; exactly it rounded when the score lies
+ *                  near decay_thr).
  *   count          device int64 [1].
  *   workspace      >= nms_matrix_workspace_size(n) bytes, 256-byte aligned.
  * Errors: NMS_ERR_INVALID_ARG, NMS_ERR_CAPACITY (n > NMS_MAX_SINGLE_N or
  * keep_cap too small), NMS_ERR_WORKSPACE, NMS_ERR_CUDA.
  */
 nms_status nms_matrix_workspace_size(int64_t n, size_t* bytes);
-nms_status nms_matrix_run(const float* boxes, const float* scores, int64_t n, float sigma,
-                          float score_thr, float decay_thr, int32_t max_out, int64_t* keep,
-                          float* keep_scores, int64_t keep_cap, int64_t* count,
+nms_status nms_matrix_run(const float* boxes, const float* scores, int64_t n, int32_t decay,
+                          float sigma, float score_thr, float decay_thr, int32_t max_out,
+                          int64_t* keep, float* keep_scores, int64_t keep_cap, int64_t* count,
                           int32_t* dev_status, void* workspace, size_t workspace_bytes,
                           void* stream);
 

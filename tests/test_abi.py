@@ -132,14 +132,18 @@ def test_no_cpu_fallback_when_library_missing(monkeypatch):
 
 def test_matrix_entry_validation(lib):
     ws = g.nms_matrix_workspace_size(10)
-    a = dict(boxes=FAKE, scores=FAKE, n=10, sigma=0.5, score_thr=-math.inf, decay_thr=0.1, max_out=0,
+    a = dict(boxes=FAKE, scores=FAKE, n=10, decay=g.NMS_DECAY_GAUSSIAN, sigma=0.5, score_thr=-math.inf,
+             decay_thr=0.1, max_out=0,
              keep=FAKE, keep_scores=0, keep_cap=10, count=FAKE, dev_status=0, workspace=FAKE,
              workspace_bytes=ws, stream=0)
     for bad, code in ((dict(n=-1), g.NMS_ERR_INVALID_ARG), (dict(sigma=0.0), g.NMS_ERR_INVALID_ARG),
                       (dict(sigma=-1.0), g.NMS_ERR_INVALID_ARG), (dict(sigma=math.inf), g.NMS_ERR_INVALID_ARG),
                       (dict(decay_thr=math.nan), g.NMS_ERR_INVALID_ARG), (dict(boxes=FAKE + 4), g.NMS_ERR_INVALID_ARG),
                       (dict(keep_cap=9), g.NMS_ERR_CAPACITY), (dict(max_out=3, keep_cap=2), g.NMS_ERR_CAPACITY),
-                      (dict(workspace_bytes=ws - 1), g.NMS_ERR_WORKSPACE), (dict(n=(1 << 18) + 1, keep_cap=1 << 19), g.NMS_ERR_CAPACITY)):
+                      (dict(workspace_bytes=ws - 1), g.NMS_ERR_WORKSPACE), (dict(n=(1 << 18) + 1, keep_cap=1 << 19), g.NMS_ERR_CAPACITY),
+                      (dict(decay=2), g.NMS_ERR_INVALID_ARG), (dict(decay=-1), g.NMS_ERR_INVALID_ARG),
+                      (dict(decay=g.NMS_DECAY_LINEAR, keep_cap=9), g.NMS_ERR_CAPACITY),
+                      (dict(decay=g.NMS_DECAY_LINEAR, decay_thr=math.nan), g.NMS_ERR_INVALID_ARG)):
         assert g.nms_matrix_run(**dict(a, **bad)) == code, bad
     with pytest.raises(g.NmsError):
         g.nms_matrix_workspace_size(-1)

@@ -69,3 +69,53 @@ def test_identical_boxes_and_empty():
     _check(b, s, float(np.float32(0.9) * np.float32(math.exp(-2.0))))
     k, fs = g.matrix_nms(torch.zeros((0, 4), device="cuda"), torch.zeros(0, device="cuda"), 0.1)
     assert len(k) == 0
+
+
+# ------------------------------------------------------------- linear decay
+
+def _check_linear(boxes, scores, t, **kw):
+    """Linear decay: indices and order bit-exact, final scores exactly the
+    binary64 value rounded to binary32 (both sides take the same binary64
+    quotient, minimum and product)."""
+    b = torch.from_numpy(np.ascontiguousarray(boxes, np.float32)).cuda()
+    s = torch.from_numpy(np.ascontiguousarray(scores, np.float32)).cuda()
+    k, fs = g.matrix_nms(b, s, t, decay="linear", **kw)
+    ek, efs = oracle.matrix_nms(boxes, scores, t, decay="linear", **kw)
+    assert k.cpu().numpy().tolist() == ek.tolist()
+    assert fs.cpu().numpy().tolist() == efs.tolist()
+
+
+def test_linear_hand_worked():
+    b = np.array([[0, 0, 10, 1], [3, 0, 13, 1], [6, 0, 16, 1], [0, 0, 4, 4], [0, 0, 4, 4], [0, 0, 4, 2]],
+                 np.float32)
+    s = np.array([0.9, 0.8, 0.7, 0.6, 0.55, 0.5], np.float32)
+    for t in (0.0, 0.2, 0.3, 0.37, 0.5):
+        _check_linear(b, s, t)
+
+
+@pytest.mark.parametrize("name", ["single_n1000_ties", "single_n8192", "single_n32768_maxout1000"])
+@pytest.mark.parametrize("t", [0.05, 0.2])
+def test_linear_workload_shapes(name, t):
+    wl = W.make(name, 0)
+    _check_linear(wl.boxes, wl.scores, t, max_out=wl.max_out)
+
+
+@pytest.mark.parametrize("n", [1, 2, 127, 128, 129, 3000])
+def test_linear_clusters(n):
+    rng = np.random.default_rng(100 + n)
+    k = max(n // 10, 1)
+    c = rng.uniform(0, 500, (k, 2))[rng.integers(0, k, n)] + rng.normal(0, 5, (n, 2))
+    wh = rng.uniform(10, 50, (n, 2))
+    b = np.concatenate([c - wh / 2, c + wh / 2], 1).astype(np.float32)
+    b[::17] = b[::17][0]  # a group of identical boxes: fathers that overlap their own father fully
+    s = rng.uniform(0, 1, n).astype(np.float32)
+    _check_linear(b, s, 0.1)
+    _check_linear(b, s, 0.1, max_out=max(n // 7, 1))
+    _check_linear(b, s, 0.1, score_thr=0.3)
+
+
+def test_linear_identical_boxes():
+    b = np.tile(np.array([[1, 1, 5, 5]], np.float32), (200, 1))
+    s = np.linspace(1.0, 0.2, 200).astype(np.float32)
+    _check_linear(b, s, 0.0)
+    _check_linear(b, s, 1e-30)

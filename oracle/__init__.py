@@ -61,6 +61,9 @@ def _load():
         lib.oracle_score_order.restype = None
         lib.oracle_mask.argtypes = [f32p, ctypes.c_int64, ctypes.c_float, u64p]
         lib.oracle_mask.restype = None
+        lib.oracle_decode_boxes7.argtypes = [f32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                             ctypes.c_int32, f32p]
+        lib.oracle_decode_boxes7.restype = None
         _lib = lib
     return _lib
 
@@ -150,3 +153,37 @@ def mask(boxes_sorted, iou_thr) -> np.ndarray:
     _load().oracle_mask(_ptr(bx, ctypes.c_float), n, float(np.float32(iou_thr)),
                         _ptr(m, ctypes.c_uint64))
     return m[:, :W]
+
+
+def decode_boxes7(preds, conf_thr, max_objects) -> np.ndarray:
+    """The [count, 7-float rows] buffers of YOLO-shaped predictions
+    [batch, anchors, 5 + classes]: float32 [batch, 1 + 7 * max_objects],
+    unused rows zero."""
+    p = np.ascontiguousarray(preds, dtype=np.float32)
+    if p.ndim != 3 or p.shape[2] < 6 or max_objects < 0:
+        raise ValueError("decode_boxes7: preds must be [batch, anchors, 5 + classes]")
+    batch, anchors, width = p.shape
+    out = np.zeros((batch, 1 + 7 * max_objects), dtype=np.float32)
+    _load().oracle_decode_boxes7(_ptr(p, ctypes.c_float), batch, anchors, width - 5,
+                                 float(np.float32(conf_thr)), int(max_objects), _ptr(out, ctypes.c_float))
+    return out
+
+
+def boxes7_nms(buffers, iou_thr, *, fast=False) -> np.ndarray:
+    """keep_flag of every row of [count, 7-float rows] buffers after class-aware
+    NMS in the buffer's own priority (confidence descending, then row
+    position), greedy or Fast NMS ("YOLOv5后处理GPU移植实战", section 2.2):
+    returns a copy of the buffers with row flags 1 (kept) or 0; rows past
+    min(count, max_objects) are untouched."""
+    out = np.array(buffers, dtype=np.float32, copy=True)
+    batch, width = out.shape
+    max_objects = (width - 1) // 7
+    for b in range(batch):
+        m = min(int(out[b, 0]), max_objects)
+        rows = out[b, 1:1 + 7 * m].reshape(m, 7)
+        keep, counts = nms(rows[:, :4], rows[:, 4], iou_thr, class_ids=rows[:, 5].astype(np.int32), fast=fast)
+        flags = np.zeros(m, dtype=np.float32)
+        flags[keep[:counts[0]]] = 1.0
+        rows[:, 6] = flags
+        out[b, 1:1 + 7 * m] = rows.reshape(-1)
+    return out

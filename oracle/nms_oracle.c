@@ -297,3 +297,59 @@ void oracle_mask(const float* boxes_sorted, int64_t n, float iou_thr, uint64_t* 
             if (oracle_iou(boxes_sorted + 4 * i, boxes_sorted + 4 * j) > iou_thr)
                 mask[i * W + j / 64] |= (uint64_t)1 << (j % 64);
 }
+
+/*
+ * Front end for YOLO-shaped outputs: the "count header + data body" buffer of
+ * "YOLOv5后处理GPU移植实战", section 1.1, filled from the head's predictions.
+ *
+ * Per image the buffer is float[1 + 7 * max_objects]: element 0 the number
+ * of candidates found, then one row of 7 floats per candidate: left, top,
+ * right, bottom, confidence, class, keep_flag.  Section 1.2: a slot is taken
+ * with an atomic counter and a candidate beyond max_objects is dropped, so
+ * the header may exceed max_objects and a reader takes min(header,
+ * max_objects) rows.
+ *
+ * The page gives the layout but not the decode itself.  Readings: preds is
+ * [batch][anchors][5 + num_classes] binary32, each row (cx, cy, w, h,
+ * objectness, class scores) as an exported detector emits it (activations
+ * already applied); the confidence is RN(objectness * max class score), the
+ * class is the first class with that maximum, a row is a candidate when its
+ * confidence is > conf_thr (strict, as the score pre-filter), the box is
+ * (RN(cx - RN(w / 2)), RN(cy - RN(h / 2)), RN(cx + RN(w / 2)), RN(cy +
+ * RN(h / 2))) and keep_flag starts at 1; candidates take the rows in anchor
+ * order (the order the page's atomic counter hands out when slots are taken
+ * in order: one valid outcome, and the reproducible one).  Unused rows are
+ * left as they are.
+ */
+void oracle_decode_boxes7(const float* preds, int32_t batch, int32_t anchors, int32_t num_classes,
+                          float conf_thr, int32_t max_objects, float* out)
+{
+    const int64_t rowlen = 5 + (int64_t)num_classes;
+    const int64_t stride = 1 + 7 * (int64_t)max_objects;
+    for (int32_t b = 0; b < batch; ++b) {
+        float* buf = out + b * stride;
+        int64_t count = 0;
+        for (int32_t a = 0; a < anchors; ++a) {
+            const float* p = preds + ((int64_t)b * anchors + a) * rowlen;
+            int32_t cls = 0;
+            float best = p[5];
+            for (int32_t c = 1; c < num_classes; ++c)
+                if (p[5 + c] > best) { best = p[5 + c]; cls = c; }
+            float conf = p[4] * best;
+            if (!(conf > conf_thr)) continue;
+            if (count < max_objects) {
+                float* r = buf + 1 + 7 * count;
+                float hw = p[2] / 2.0f, hh = p[3] / 2.0f;
+                r[0] = p[0] - hw;
+                r[1] = p[1] - hh;
+                r[2] = p[0] + hw;
+                r[3] = p[1] + hh;
+                r[4] = conf;
+                r[5] = (float)cls;
+                r[6] = 1.0f;
+            }
+            ++count;
+        }
+        buf[0] = (float)count;
+    }
+}

@@ -220,6 +220,56 @@ def time_workload(g, torch, wl, dev, flush, reps=30, fast=False):
             "kept": int(counts.sum().item()), "batched": batched}
 
 
+def time_front_end(g, torch, dev, flush, reps=20, conf_thr=0.25, max_objects=1000, iou_thr=0.45):
+    """YOLO-shaped head output (16 x 25200 x 85) through the front end: the
+    decode into count-header buffers alone, and decode plus greedy NMS over the
+    buffers (keep flags), device time per call; the decode's prediction bytes
+    against HBM."""
+    preds = torch.from_numpy(W.yolo_raw(0)).to(dev)
+    batch, anchors, width = preds.shape
+    buf = torch.zeros((batch, 1 + 7 * max_objects), dtype=torch.float32, device=dev)
+    wsd = g.nms_decode_workspace_size(batch, anchors)
+    ws_d = torch.empty(max(wsd, 256), dtype=torch.uint8, device=dev)
+    wsn = g.nms_boxes7_workspace_size(batch, max_objects, width - 5)
+    ws_n = torch.empty(max(wsn, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def decode():
+        st = g.nms_decode_boxes7(preds.data_ptr(), batch, anchors, width - 5, conf_thr, max_objects, buf.data_ptr(),
+                                 ws_d.data_ptr(), wsd, stream.cuda_stream)
+        if st != g.NMS_OK:
+            raise g.NmsError(st, "nms_decode_boxes7")
+
+    def nms():
+        st = g.nms_boxes7_run(buf.data_ptr(), batch, max_objects, width - 5, iou_thr, 0, 0, ws_n.data_ptr(), wsn,
+                              stream.cuda_stream)
+        if st != g.NMS_OK:
+            raise g.NmsError(st, "nms_boxes7_run")
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        evs = []
+        for _ in range(reps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.median(1000 * a.elapsed_time(b) for a, b in evs)
+
+    d_us = timed(decode)
+    t_us = timed(lambda: (decode(), nms()))
+    pbytes = preds.numel() * 4
+    return {"workload": f"yolo head output {batch}x{anchors}x{width} float32, conf > {conf_thr}, "
+                        f"max_objects {max_objects}, greedy IoU {iou_thr}",
+            "decode_us": d_us, "decode_plus_nms_us": t_us, "prediction_bytes": pbytes,
+            "decode_gbs": pbytes / (d_us / 1e6) / 1e9,
+            "candidates": int(buf[:, 0].sum().item())}
+
+
 def time_matrix(g, torch, wl, dev, flush, decay_thr=0.1, reps=20, decay=0):
     """Device time of one nms_matrix_run call (Gaussian decay with sigma 0.5,
     or the linear decay) on a one-image workload: median, p10, p90 in
@@ -412,7 +462,7 @@ def run_gbnms(args):
         roof = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
                 "frac": ach / hbm, "traffic": _ncu_traffic(dominant), "note": note}
 
-    per_config = fast_nms = matrix_nms = matrix_lin = None
+    per_config = fast_nms = matrix_nms = matrix_lin = front_end = None
     if not args.no_configs:
         per_config, fast_nms, matrix_nms, matrix_lin = {}, {}, {}, {}
         for name in W.CONFIGS:
@@ -422,6 +472,7 @@ def run_gbnms(args):
             if wl_c.class_ids is None and wl_c.batch_offsets is None:
                 matrix_nms[name] = time_matrix(g, torch, wl_c, dev, flush)
                 matrix_lin[name] = time_matrix(g, torch, wl_c, dev, flush, decay=g.NMS_DECAY_LINEAR)
+        front_end = time_front_end(g, torch, dev, flush)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -444,6 +495,7 @@ def run_gbnms(args):
         "kernels": kernels,
         "per_config": per_config,
         "fast_nms_per_config": fast_nms,
+        "front_end": front_end,
         "matrix_nms_per_config": matrix_nms,
         "matrix_nms_linear_per_config": matrix_lin,
         "roofline": roof,

@@ -32,8 +32,11 @@ NMS_MAX_SINGLE_N = 1 << 18
 
 EXPORTED = ("nms_status_string", "nms_workspace_size", "nms_run", "nms_fast_run", "nms_run_timed",
             "nms_matrix_workspace_size", "nms_matrix_run", "nms_mask_row_words", "nms_iou_mask",
-            "nms_resolve_mask", "nms_resolve_mask_noalloc")
+            "nms_resolve_mask", "nms_resolve_mask_noalloc", "nms_decode_workspace_size", "nms_decode_boxes7",
+            "nms_boxes7_workspace_size", "nms_boxes7_run")
 NMS_NOALLOC_MAX_N = 16384
+NMS_DECODE_MAX_ANCHORS = 1 << 20
+NMS_DECODE_MAX_CLASSES = 384
 
 _lib = None
 
@@ -82,6 +85,14 @@ def load():
     lib.nms_resolve_mask.restype = ctypes.c_int
     lib.nms_resolve_mask_noalloc.argtypes = [vp, i64, vp, i32, vp, vp, vp]
     lib.nms_resolve_mask_noalloc.restype = ctypes.c_int
+    lib.nms_decode_workspace_size.argtypes = [i32, i32, ctypes.POINTER(sz)]
+    lib.nms_decode_workspace_size.restype = ctypes.c_int
+    lib.nms_decode_boxes7.argtypes = [vp, i32, i32, i32, f32, i32, vp, vp, sz, vp]
+    lib.nms_decode_boxes7.restype = ctypes.c_int
+    lib.nms_boxes7_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
+    lib.nms_boxes7_workspace_size.restype = ctypes.c_int
+    lib.nms_boxes7_run.argtypes = [vp, i32, i32, i32, f32, i32, vp, vp, sz, vp]
+    lib.nms_boxes7_run.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -421,3 +432,82 @@ def resolve_mask(mask, max_out: int = 0, perm=None, workspace: Optional[Workspac
     if st != NMS_OK:
         raise NmsError(st, "nms_resolve_mask")
     return keep[: int(count.item())]
+
+
+# ------------------------------------------- front end for YOLO-shaped outputs
+
+def nms_decode_workspace_size(batch: int, anchors: int) -> int:
+    out = ctypes.c_size_t(0)
+    st = load().nms_decode_workspace_size(int(batch), int(anchors), ctypes.byref(out))
+    if st != NMS_OK:
+        raise NmsError(st, "nms_decode_workspace_size")
+    return int(out.value)
+
+
+def nms_decode_boxes7(preds: int, batch: int, anchors: int, num_classes: int, conf_thr: float, max_objects: int,
+                      buffers: int, workspace: int, workspace_bytes: int, stream: int) -> int:
+    """The C entry point (device addresses as ints)."""
+    return load().nms_decode_boxes7(preds or None, int(batch), int(anchors), int(num_classes), float(conf_thr),
+                                    int(max_objects), buffers or None, workspace or None, int(workspace_bytes),
+                                    stream or None)
+
+
+def nms_boxes7_workspace_size(batch: int, max_objects: int, num_classes: int) -> int:
+    out = ctypes.c_size_t(0)
+    st = load().nms_boxes7_workspace_size(int(batch), int(max_objects), int(num_classes), ctypes.byref(out))
+    if st != NMS_OK:
+        raise NmsError(st, "nms_boxes7_workspace_size")
+    return int(out.value)
+
+
+def nms_boxes7_run(buffers: int, batch: int, max_objects: int, num_classes: int, iou_thr: float, fast: int,
+                   dev_status: int, workspace: int, workspace_bytes: int, stream: int) -> int:
+    """The C entry point (device addresses as ints)."""
+    return load().nms_boxes7_run(buffers or None, int(batch), int(max_objects), int(num_classes), float(iou_thr),
+                                 int(fast), dev_status or None, workspace or None, int(workspace_bytes),
+                                 stream or None)
+
+
+def decode_boxes7(preds, conf_thr: float, max_objects: int):
+    """Count-header buffers [batch, 1 + 7 * max_objects] (float32, CUDA) from
+    YOLO-shaped predictions [batch, anchors, 5 + classes] (float32, CUDA).
+    Rows past the candidates are zero."""
+    torch = _torch()
+    if not preds.is_cuda or preds.dtype != torch.float32 or preds.dim() != 3 or preds.shape[2] < 6:
+        raise ValueError("decode_boxes7: preds must be a float32 CUDA tensor [batch, anchors, 5 + classes]")
+    preds = preds.contiguous()
+    batch, anchors, width = preds.shape
+    dev = preds.device
+    out = torch.zeros((batch, 1 + 7 * max_objects), dtype=torch.float32, device=dev)
+    wsb = nms_decode_workspace_size(batch, anchors)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    st = nms_decode_boxes7(preds.data_ptr(), batch, anchors, width - 5, conf_thr, max_objects, out.data_ptr(),
+                           ws.data_ptr(), wsb, torch.cuda.current_stream(dev).cuda_stream)
+    if st != NMS_OK:
+        raise NmsError(st, "nms_decode_boxes7")
+    return out
+
+
+def boxes7_nms(buffers, num_classes: int, iou_thr: float, *, fast: bool = False):
+    """NMS in place over count-header buffers [batch, 1 + 7 * max_objects]
+    (float32, CUDA): keep_flag of the taking-part rows becomes 1 or 0.
+    Synchronises the current stream once to read the device status."""
+    torch = _torch()
+    if not buffers.is_cuda or buffers.dtype != torch.float32 or buffers.dim() != 2 or not buffers.is_contiguous():
+        raise ValueError("boxes7_nms: buffers must be a contiguous float32 CUDA tensor [batch, 1 + 7 * max_objects]")
+    batch, width = buffers.shape
+    if (width - 1) % 7:
+        raise ValueError("boxes7_nms: the row length must be 1 + 7 * max_objects")
+    max_objects = (width - 1) // 7
+    dev = buffers.device
+    wsb = nms_boxes7_workspace_size(batch, max_objects, num_classes)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = nms_boxes7_run(buffers.data_ptr(), batch, max_objects, num_classes, iou_thr, 1 if fast else 0,
+                        status.data_ptr(), ws.data_ptr(), wsb, torch.cuda.current_stream(dev).cuda_stream)
+    if st != NMS_OK:
+        raise NmsError(st, "nms_boxes7_run")
+    dst = int(status.item())
+    if dst != NMS_OK:
+        raise NmsError(dst, "nms_boxes7_run (device)")
+    return buffers

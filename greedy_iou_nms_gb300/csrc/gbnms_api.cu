@@ -437,6 +437,142 @@ extern "C" nms_status nms_matrix_run(const float* boxes, const float* scores, in
     return cuda_status();
 }
 
+namespace gbnms {
+namespace {
+
+struct DecodeLayout {
+    size_t stage, blk_cnt, total;
+};
+
+DecodeLayout decode_layout(int32_t batch, int32_t anchors)
+{
+    DecodeLayout d;
+    Layout L;
+    const size_t slots = static_cast<size_t>(batch) * decode_blocks(anchors) * 128;
+    d.stage = L.add(7 * sizeof(float) * slots);
+    d.blk_cnt = L.add(sizeof(int) * static_cast<size_t>(batch) * decode_blocks(anchors));
+    d.total = L.total;
+    return d;
+}
+
+struct Boxes7Layout {
+    BatchedLayout batched;
+    size_t boxes, scores, cls, off, img_rows, keep, counts, total;
+};
+
+Boxes7Layout boxes7_layout(int32_t batch, int32_t max_objects, int32_t num_classes)
+{
+    Boxes7Layout b;
+    const int64_t n = static_cast<int64_t>(batch) * max_objects;
+    b.batched = batched_layout(n, static_cast<int64_t>(batch) * num_classes);
+    Layout L;
+    L.total = align_up(b.batched.total);
+    const size_t N = static_cast<size_t>(n > 0 ? n : 1);
+    b.boxes = L.add(16 * N);
+    b.scores = L.add(4 * N);
+    b.cls = L.add(4 * N);
+    b.off = L.add(8 * (static_cast<size_t>(batch) + 1));
+    b.img_rows = L.add(4 * static_cast<size_t>(batch));
+    b.keep = L.add(8 * N);
+    b.counts = L.add(8 * static_cast<size_t>(batch));
+    b.total = L.total;
+    return b;
+}
+
+}  // namespace
+}  // namespace gbnms
+
+extern "C" nms_status nms_decode_workspace_size(int32_t batch, int32_t anchors, size_t* bytes)
+{
+    if (!bytes || batch < 1 || anchors < 0) return NMS_ERR_INVALID_ARG;
+    if (anchors > NMS_DECODE_MAX_ANCHORS) return NMS_ERR_CAPACITY;
+    *bytes = decode_layout(batch, anchors).total;
+    return NMS_OK;
+}
+
+extern "C" nms_status nms_decode_boxes7(const float* preds, int32_t batch, int32_t anchors, int32_t num_classes,
+                                        float conf_thr, int32_t max_objects, float* buffers, void* workspace,
+                                        size_t workspace_bytes, void* stream)
+{
+    if (batch < 1 || anchors < 0 || num_classes < 1 || max_objects < 0 || std::isnan(conf_thr))
+        return NMS_ERR_INVALID_ARG;
+    if (anchors > NMS_DECODE_MAX_ANCHORS || num_classes > NMS_DECODE_MAX_CLASSES) return NMS_ERR_CAPACITY;
+    if (!buffers || (anchors > 0 && (!preds || !aligned(preds, 4)))) return NMS_ERR_INVALID_ARG;
+    const DecodeLayout L = decode_layout(batch, anchors);
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < L.total) return NMS_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();
+    launch_decode(preds, batch, anchors, num_classes, conf_thr, max_objects, buffers,
+                  at<float>(workspace, L.stage), at<int>(workspace, L.blk_cnt), st);
+    return cuda_status();
+}
+
+extern "C" nms_status nms_boxes7_workspace_size(int32_t batch, int32_t max_objects, int32_t num_classes,
+                                                size_t* bytes)
+{
+    if (!bytes || batch < 1 || max_objects < 0 || num_classes < 1) return NMS_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(batch) * max_objects > INT32_MAX ||
+        static_cast<int64_t>(batch) * num_classes > INT32_MAX / 2)
+        return NMS_ERR_INVALID_ARG;
+    *bytes = boxes7_layout(batch, max_objects, num_classes).total;
+    return NMS_OK;
+}
+
+extern "C" nms_status nms_boxes7_run(float* buffers, int32_t batch, int32_t max_objects, int32_t num_classes,
+                                     float iou_thr, int32_t fast, int32_t* dev_status, void* workspace,
+                                     size_t workspace_bytes, void* stream)
+{
+    size_t need = 0;
+    const nms_status s0 = nms_boxes7_workspace_size(batch, max_objects, num_classes, &need);
+    if (s0 != NMS_OK) return s0;
+    if (!buffers || std::isnan(iou_thr) || (fast != 0 && fast != 1)) return NMS_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < need) return NMS_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();
+    const Boxes7Layout L = boxes7_layout(batch, max_objects, num_classes);
+    float4* boxes = at<float4>(workspace, L.boxes);
+    float* scores = at<float>(workspace, L.scores);
+    int32_t* cls = at<int32_t>(workspace, L.cls);
+    int64_t* off = at<int64_t>(workspace, L.off);
+    int* img_rows = at<int>(workspace, L.img_rows);
+    int64_t* keep = at<int64_t>(workspace, L.keep);
+    int64_t* counts = at<int64_t>(workspace, L.counts);
+    launch_boxes7_gather(buffers, batch, max_objects, num_classes, boxes, scores, cls, off, img_rows, st);
+    const BatchedLayout& B = L.batched;
+    BatchedArgs a{};
+    a.boxes = boxes;
+    a.scores = scores;
+    a.cls = cls;
+    a.C = num_classes;
+    a.off = off;
+    a.batch = batch;
+    a.n = batch * max_objects;
+    a.S = batch * num_classes;
+    a.use_thr = 0;
+    a.score_thr = 0.0f;
+    a.thr = iou_thr;
+    a.max_out = 0;
+    a.fast = fast;
+    a.img_rows = img_rows;
+    a.seg_cnt = at<int>(workspace, B.seg_cnt);
+    a.seg_off = at<int>(workspace, B.seg_off);
+    a.seg_of = at<int>(workspace, B.seg_of);
+    a.slot = at<int>(workspace, B.slot);
+    a.cand = at<int>(workspace, B.cand);
+    a.ok = at<int>(workspace, B.ok);
+    a.kept_key = at<uint64_t>(workspace, B.kept_key);
+    a.kept_cnt = at<int>(workspace, B.kept_cnt);
+    a.sorted_key = at<uint64_t>(workspace, B.sorted_key);
+    a.sorted_box = at<float4>(workspace, B.sorted_box);
+    a.stage = at<uint64_t>(workspace, B.stage);
+    a.keep = keep;
+    a.counts = counts;
+    a.status = dev_status ? dev_status : at<int32_t>(workspace, B.status);
+    launch_batched(a, st, Stamps{});
+    launch_boxes7_flags(buffers, batch, max_objects, img_rows, keep, counts, st);
+    return cuda_status();
+}
+
 extern "C" nms_status nms_run_timed(const float* boxes, const float* scores, int64_t n,
                                     const int32_t* class_ids, int32_t num_classes,
                                     const int64_t* batch_offsets, int32_t batch, float iou_thr,

@@ -120,6 +120,17 @@ void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, 
                    unsigned long long* xmin_key, float* fs, uint32_t* kept, int64_t* keep, float* keep_scores,
                    int64_t* count, cudaStream_t st);
 
+// Front end (k_decode.cu): YOLO-shaped predictions to count-header buffers.
+int decode_blocks(int anchors);
+size_t decode_smem(int C);
+void launch_decode(const float* preds, int batch, int anchors, int C, float conf_thr, int max_objects, float* out,
+                   float* stage, int* blk_cnt, cudaStream_t st);
+// NMS over count-header buffers: rows to batched inputs, then keep_flag.
+void launch_boxes7_gather(const float* bufs, int batch, int max_objects, int C, float4* boxes, float* scores,
+                          int32_t* cls, int64_t* off, int* img_rows, cudaStream_t st);
+void launch_boxes7_flags(float* bufs, int batch, int max_objects, const int* img_rows, const int64_t* keep,
+                         const int64_t* counts, cudaStream_t st);
+
 struct BatchedArgs {
     const float4* boxes;
     const float* scores;
@@ -134,6 +145,7 @@ struct BatchedArgs {
     float thr;
     int max_out;
     int fast;  // Fast NMS: drop a box any earlier box of its segment suppresses
+    const int* img_rows;  // optional: only the first img_rows[b] rows of image b take part
     int* seg_cnt;
     int* seg_off;
     int* seg_of;

@@ -60,9 +60,9 @@ __device__ __forceinline__ int image_of(const int64_t* __restrict__ off, int bat
 __global__ void batched_count_kernel(const float* __restrict__ scores,
                                      const int32_t* __restrict__ cls, int C,
                                      const int64_t* __restrict__ off, int batch, int n,
-                                     int use_thr, float score_thr, const int* __restrict__ ok,
-                                     int* __restrict__ seg_cnt, int* __restrict__ seg_of,
-                                     int* __restrict__ slot, int32_t* status)
+                                     int use_thr, float score_thr, const int* __restrict__ img_rows,
+                                     const int* __restrict__ ok, int* __restrict__ seg_cnt,
+                                     int* __restrict__ seg_of, int* __restrict__ slot, int32_t* status)
 {
     pdl_wait();
     pdl_release();
@@ -70,11 +70,15 @@ __global__ void batched_count_kernel(const float* __restrict__ scores,
     if (!*ok) return;
     int seg = -1;
     if (i < n) {
-        int c = cls ? cls[i] : 0;
-        if (c < 0 || c >= C) {
-            set_status(status, NMS_ERR_INVALID_ARG);
-        } else if (!use_thr || scores[i] > score_thr) {
-            seg = image_of(off, batch, i) * C + c;
+        const int b = image_of(off, batch, i);
+        // With img_rows, only the first img_rows[b] rows of image b take part.
+        if (!img_rows || i - (off ? off[b] : 0) < img_rows[b]) {
+            const int c = cls ? cls[i] : 0;
+            if (c < 0 || c >= C) {
+                set_status(status, NMS_ERR_INVALID_ARG);
+            } else if (!use_thr || scores[i] > score_thr) {
+                seg = b * C + c;
+            }
         }
     }
     const unsigned active = __ballot_sync(FULL, seg >= 0);
@@ -535,7 +539,7 @@ void launch_batched(const BatchedArgs& a, cudaStream_t st, const Stamps& stamps)
     batched_setup_kernel<<<1, 1024, 0, st>>>(a.off, a.batch, n, S, a.seg_cnt, a.ok, a.status);
     if (n > 0) {
         launch_pdl(batched_count_kernel, dim3((n + 255) / 256), dim3(256), 0, st, a.scores, a.cls, a.C, a.off,
-                   a.batch, n, a.use_thr, a.score_thr, a.ok, a.seg_cnt, a.seg_of, a.slot, a.status);
+                   a.batch, n, a.use_thr, a.score_thr, a.img_rows, a.ok, a.seg_cnt, a.seg_of, a.slot, a.status);
     }
     launch_pdl(batched_scan_kernel, dim3(1), dim3(1024), 0, st, a.seg_cnt, S, a.seg_off);
     if (n > 0)

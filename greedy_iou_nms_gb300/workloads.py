@@ -140,6 +140,28 @@ def yolo_batched(seed: int = 0, batch: int = 16) -> Workload:
     return wl
 
 
+def yolo_raw(seed: int = 0, batch: int = 16, classes: int = 80) -> np.ndarray:
+    """YOLO-640 head output rows [batch, 25200, 5 + classes] float32, the
+    shape an exported detector emits: (cx, cy, w, h) of the yolo_batched
+    anchors (same layout and size law), objectness ~ Beta(0.5, 8), class
+    scores ~ U(0, 0.3) except one class per anchor (U{0..classes-1}) at
+    U(0.5, 1.0)."""
+    wl = yolo_batched(seed, batch)
+    rng = _rng(seed + 1000)
+    n = wl.boxes.shape[0]
+    b = wl.boxes.astype(np.float64)
+    out = np.empty((n, 5 + classes), np.float32)
+    out[:, 0] = (b[:, 0] + b[:, 2]) / 2
+    out[:, 1] = (b[:, 1] + b[:, 3]) / 2
+    out[:, 2] = b[:, 2] - b[:, 0]
+    out[:, 3] = b[:, 3] - b[:, 1]
+    out[:, 4] = rng.beta(0.5, 8, n)
+    out[:, 5:] = rng.uniform(0, 0.3, (n, classes))
+    cls = rng.integers(0, classes, n)
+    out[np.arange(n), 5 + cls] = rng.uniform(0.5, 1.0, n)
+    return out.reshape(batch, n // batch, 5 + classes)
+
+
 def stress_dense(seed: int = 0) -> Workload:
     """N=65536 dense: 500 tight clusters in 8192x8192 (jitter N(0,3)), w,h ~
     U(20,48): about 95% of the boxes are suppressed.  Scores U(0,1); 0.5."""

@@ -247,6 +247,64 @@ nms_status nms_run_timed(const float* boxes, const float* scores, int64_t n,
                          size_t workspace_bytes, void* stream, void* const* events,
                          int32_t nevents);
 
+/* Limits of the front end for YOLO-shaped outputs. */
+#define NMS_DECODE_MAX_ANCHORS (1 << 20)
+#define NMS_DECODE_MAX_CLASSES 384
+
+/*
+ * Front end for YOLO-shaped outputs: the "count header + data body" buffer of
+ * "YOLOv5后处理GPU移植实战" (section 1.1), one per image,
+ *   float buffers[batch][1 + 7 * max_objects]:
+ *   element 0     the number of candidates found (may exceed max_objects:
+ *                 section 1.2 drops a candidate past max_objects but still
+ *                 counts it; a reader takes min(count, max_objects) rows);
+ *   rows of 7     left, top, right, bottom, confidence, class, keep_flag.
+ * The page prints the layout, not the decode.  Readings: preds is
+ * [batch][anchors][5 + num_classes] binary32 (cx, cy, w, h, objectness, class
+ * scores; activations already applied), confidence = RN(objectness x largest
+ * class score), class = the first class with that maximum (as a float), a
+ * row is a candidate when confidence > conf_thr, the box is centre +- half
+ * size in binary32, keep_flag = 1, and candidates take the rows in anchor
+ * order (so the buffer is the same on every run).  Rows past the candidates
+ * are left as they are.
+ *   preds        device, 4-byte aligned.
+ *   batch        >= 1; anchors in [0, NMS_DECODE_MAX_ANCHORS];
+ *   num_classes  in [1, NMS_DECODE_MAX_CLASSES].
+ *   conf_thr     not NaN.
+ *   max_objects  >= 0 rows per image.
+ *   buffers      device float[batch * (1 + 7 * max_objects)].
+ *   workspace    >= nms_decode_workspace_size() bytes, 256-byte aligned.
+ * Errors: NMS_ERR_INVALID_ARG, NMS_ERR_CAPACITY (limits), NMS_ERR_WORKSPACE,
+ * NMS_ERR_CUDA.
+ */
+nms_status nms_decode_workspace_size(int32_t batch, int32_t anchors, size_t* bytes);
+nms_status nms_decode_boxes7(const float* preds, int32_t batch, int32_t anchors, int32_t num_classes,
+                             float conf_thr, int32_t max_objects, float* buffers, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
+ * NMS in place over count-header buffers (layout as above): for each image
+ * the first min(count, max_objects) rows take part (a count below 1 or NaN:
+ * none); boxes of one class interact; rows rank by confidence, then by the
+ * lower position ("YOLOv5后处理GPU移植实战", section 2.2); keep_flag of each
+ * taking-part row becomes 1 (kept) or 0.  fast = 0: exact greedy NMS (IoU >
+ * iou_thr, canonical binary32 IoU); fast = 1: the page's Fast NMS (a row goes
+ * when any higher-ranked row of its class, kept or not, overlaps it beyond
+ * iou_thr).  Rows past the taking-part ones are not touched.
+ *   num_classes   class values must be integers in [0, num_classes); any
+ *                 other value sets NMS_ERR_INVALID_ARG in the device status
+ *                 (dev_status, or the workspace's status word) and leaves
+ *                 that row out.
+ *   batch * max_objects <= INT32_MAX; batch * num_classes <= INT32_MAX / 2.
+ *   workspace     >= nms_boxes7_workspace_size() bytes, 256-byte aligned.
+ * Errors: NMS_ERR_INVALID_ARG, NMS_ERR_WORKSPACE, NMS_ERR_CUDA (host side);
+ * the device status as for nms_run.
+ */
+nms_status nms_boxes7_workspace_size(int32_t batch, int32_t max_objects, int32_t num_classes, size_t* bytes);
+nms_status nms_boxes7_run(float* buffers, int32_t batch, int32_t max_objects, int32_t num_classes, float iou_thr,
+                          int32_t fast, int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
 /* Largest n nms_resolve_mask_noalloc accepts. */
 #define NMS_NOALLOC_MAX_N 16384
 

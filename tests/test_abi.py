@@ -147,3 +147,28 @@ def test_matrix_entry_validation(lib):
         assert g.nms_matrix_run(**dict(a, **bad)) == code, bad
     with pytest.raises(g.NmsError):
         g.nms_matrix_workspace_size(-1)
+
+
+def test_front_end_entry_validation(lib):
+    ws = g.nms_decode_workspace_size(2, 100)
+    a = dict(preds=FAKE, batch=2, anchors=100, num_classes=80, conf_thr=0.25, max_objects=10, buffers=FAKE,
+             workspace=FAKE, workspace_bytes=ws, stream=0)
+    for bad, code in ((dict(batch=0), g.NMS_ERR_INVALID_ARG), (dict(anchors=-1), g.NMS_ERR_INVALID_ARG),
+                      (dict(num_classes=0), g.NMS_ERR_INVALID_ARG), (dict(max_objects=-1), g.NMS_ERR_INVALID_ARG),
+                      (dict(conf_thr=math.nan), g.NMS_ERR_INVALID_ARG), (dict(buffers=0), g.NMS_ERR_INVALID_ARG),
+                      (dict(preds=FAKE + 2), g.NMS_ERR_INVALID_ARG),
+                      (dict(anchors=g.NMS_DECODE_MAX_ANCHORS + 1), g.NMS_ERR_CAPACITY),
+                      (dict(num_classes=g.NMS_DECODE_MAX_CLASSES + 1), g.NMS_ERR_CAPACITY),
+                      (dict(workspace_bytes=ws - 1), g.NMS_ERR_WORKSPACE), (dict(workspace=FAKE + 8), g.NMS_ERR_WORKSPACE)):
+        assert g.nms_decode_boxes7(**dict(a, **bad)) == code, bad
+    wb = g.nms_boxes7_workspace_size(2, 10, 80)
+    b = dict(buffers=FAKE, batch=2, max_objects=10, num_classes=80, iou_thr=0.5, fast=0, dev_status=0,
+             workspace=FAKE, workspace_bytes=wb, stream=0)
+    for bad, code in ((dict(batch=0), g.NMS_ERR_INVALID_ARG), (dict(num_classes=0), g.NMS_ERR_INVALID_ARG),
+                      (dict(fast=2), g.NMS_ERR_INVALID_ARG), (dict(iou_thr=math.nan), g.NMS_ERR_INVALID_ARG),
+                      (dict(buffers=0), g.NMS_ERR_INVALID_ARG), (dict(max_objects=-1), g.NMS_ERR_INVALID_ARG),
+                      (dict(batch=1 << 20, max_objects=1 << 12), g.NMS_ERR_INVALID_ARG),
+                      (dict(workspace_bytes=wb - 1), g.NMS_ERR_WORKSPACE)):
+        assert g.nms_boxes7_run(**dict(b, **bad)) == code, bad
+    with pytest.raises(g.NmsError):
+        g.nms_decode_workspace_size(0, 10)

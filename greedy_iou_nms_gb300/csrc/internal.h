@@ -122,7 +122,6 @@ void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, 
 
 // Front end (k_decode.cu): YOLO-shaped predictions to count-header buffers.
 int decode_blocks(int anchors);
-size_t decode_smem(int C);
 void launch_decode(const float* preds, int batch, int anchors, int C, float conf_thr, int max_objects, float* out,
                    float* stage, int* blk_cnt, cudaStream_t st);
 // NMS over count-header buffers: rows to batched inputs, then keep_flag.

@@ -17,12 +17,12 @@
 // same on every run.
 //
 // GPU shape: one CTA per 128 anchors of an image stages their rows in shared
-// memory with coalesced loads (the rows are contiguous), decodes one anchor
-// per thread, compacts its candidates with a ballot per warp and a prefix
-// over its 4 warps, and writes them and its count to a staging area (the
-// local reduction).  One CTA per image then takes the prefix of its blocks'
-// counts, writes the header and copies the first max_objects candidates in
-// order.  NMS over buffers gathers the rows into the batched path's inputs
+// memory with asynchronous 16-byte copies (the rows are contiguous), decodes
+// one anchor per thread, compacts its candidates with a ballot per warp and a
+// prefix over its 4 warps, and writes them and its count to a staging area
+// (the local reduction).  One CTA per image then takes the prefix of the
+// image's block counts, writes the header and copies the first max_objects
+// candidates in order.  NMS over buffers gathers the rows into the batched path's inputs
 // (per image at a fixed stride of max_objects rows, only the first
 // min(header, max_objects) taking part), runs it, and writes keep_flag.
 #include "common.cuh"
@@ -31,20 +31,79 @@
 namespace gbnms {
 
 constexpr int DC_APB = 128;      // anchors per decode CTA
-constexpr int DC_EMIT = 256;     // threads of the emit CTA
+
+// The header and the first max_objects candidates of image b, in order, by
+// the calling CTA (blockDim.x threads, `pre` shared scratch of nblk + 1 ints).
+__device__ void emit_image(int b, const float* __restrict__ stage, const int* __restrict__ blk_cnt, int nblk,
+                           int max_objects, float* __restrict__ out, int* pre, int* wsum)
+{
+    const int nt = blockDim.x;
+    const int* cnt = blk_cnt + static_cast<int64_t>(b) * nblk;
+    // Thread t sums a contiguous run of blocks, then a block-wide scan.
+    const int per = (nblk + nt - 1) / nt;
+    const int k0 = min(nblk, static_cast<int>(threadIdx.x) * per), k1 = min(nblk, k0 + per);
+    int run = 0;
+    for (int k = k0; k < k1; ++k) run += cnt[k];
+    const unsigned l = lane_id();
+    const int w = threadIdx.x >> 5;
+    int x = run;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, d);
+        if (static_cast<int>(l) >= d) x += y;
+    }
+    if (l == 31) wsum[w] = x;
+    __syncthreads();
+    int before = x - run;
+    for (int q = 0; q < w; ++q) before += wsum[q];
+    for (int k = k0; k < k1; ++k) {
+        pre[k] = before;
+        before += cnt[k];
+    }
+    if (static_cast<int>(threadIdx.x) == nt - 1) pre[nblk] = before;
+    __syncthreads();
+    const int total = pre[nblk];
+    float* buf = out + static_cast<int64_t>(b) * (1 + 7 * static_cast<int64_t>(max_objects));
+    if (threadIdx.x == 0) buf[0] = static_cast<float>(total);
+    const int rows_out = min(total, max_objects);
+    for (int r = threadIdx.x; r < rows_out; r += nt) {
+        int lo = 0, hi = nblk;  // last block whose prefix is <= r
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (pre[mid] <= r) lo = mid; else hi = mid;
+        }
+        const float* srow = stage + 7 * ((static_cast<int64_t>(b) * nblk + lo) * DC_APB + (r - pre[lo]));
+        float* drow = buf + 1 + 7 * static_cast<int64_t>(r);
+#pragma unroll
+        for (int k = 0; k < 7; ++k) drow[k] = srow[k];
+    }
+}
 
 __global__ void __launch_bounds__(DC_APB)
 decode_kernel(const float* __restrict__ preds, int anchors, int C, float conf_thr, int nblk,
               float* __restrict__ stage, int* __restrict__ blk_cnt)
 {
-    extern __shared__ float rows[];  // up to DC_APB rows of 5 + C floats
+    extern __shared__ __align__(16) float rows[];  // DC_APB rows of 5 + C floats
     __shared__ int wcnt[DC_APB / 32];
+    pdl_release();  // the emit may be scheduled; it waits for this grid
     const int b = blockIdx.y, blk = blockIdx.x;
     const int a0 = blk * DC_APB;
     const int na = min(DC_APB, anchors - a0);
     const int W = 5 + C;
     const float* src = preds + (static_cast<int64_t>(b) * anchors + a0) * W;
-    for (int e = threadIdx.x; e < na * W; e += DC_APB) rows[e] = src[e];
+    const int nf = na * W;
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (nf & 3) == 0) {
+        // 16-byte asynchronous copies when the block's rows start on a
+        // 16-byte boundary: the whole block's rows are in flight at once.
+        const unsigned sbase = static_cast<unsigned>(__cvta_generic_to_shared(rows));
+        for (int e = threadIdx.x; e < nf / 4; e += DC_APB)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sbase + 16u * e), "l"(src + 4 * e)
+                         : "memory");
+        asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;\n" ::: "memory");
+    } else {
+#pragma unroll 4
+        for (int e = threadIdx.x; e < nf; e += DC_APB) rows[e] = src[e];
+    }
     __syncthreads();
     const int t = threadIdx.x;
     bool cand = false;
@@ -91,70 +150,39 @@ decode_kernel(const float* __restrict__ preds, int anchors, int C, float conf_th
     if (t == 0) blk_cnt[static_cast<int64_t>(b) * nblk + blk] = total;
 }
 
-// One CTA per image: the header and the first max_objects candidates in order.
-__global__ void __launch_bounds__(DC_EMIT)
+// One CTA per image: its header and its first max_objects candidates.
+__global__ void __launch_bounds__(DC_APB)
 decode_emit_kernel(const float* __restrict__ stage, const int* __restrict__ blk_cnt, int nblk, int max_objects,
                    float* __restrict__ out)
 {
-    extern __shared__ int pre[];  // nblk + 1 exclusive prefixes
-    __shared__ int wsum[DC_EMIT / 32];
+    extern __shared__ int pre[];  // nblk + 1 prefixes
+    __shared__ int wsum[DC_APB / 32];
     pdl_wait();
-    const int b = blockIdx.x;
-    const int* cnt = blk_cnt + static_cast<int64_t>(b) * nblk;
-    // Thread t sums a contiguous run of blocks, then a block-wide scan.
-    const int per = (nblk + DC_EMIT - 1) / DC_EMIT;
-    const int k0 = min(nblk, threadIdx.x * per), k1 = min(nblk, k0 + per);
-    int run = 0;
-    for (int k = k0; k < k1; ++k) run += cnt[k];
-    const unsigned l = lane_id();
-    const int w = threadIdx.x >> 5;
-    int x = run;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(FULL, x, d);
-        if (static_cast<int>(l) >= d) x += y;
-    }
-    if (l == 31) wsum[w] = x;
-    __syncthreads();
-    int before = x - run;
-    for (int q = 0; q < w; ++q) before += wsum[q];
-    for (int k = k0; k < k1; ++k) {
-        pre[k] = before;
-        before += cnt[k];
-    }
-    if (threadIdx.x == DC_EMIT - 1) pre[nblk] = before;
-    __syncthreads();
-    const int total = pre[nblk];
-    float* buf = out + static_cast<int64_t>(b) * (1 + 7 * static_cast<int64_t>(max_objects));
-    if (threadIdx.x == 0) buf[0] = static_cast<float>(total);
-    const int rows_out = min(total, max_objects);
-    for (int r = threadIdx.x; r < rows_out; r += DC_EMIT) {
-        int lo = 0, hi = nblk;  // last block whose prefix is <= r
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (pre[mid] <= r) lo = mid; else hi = mid;
-        }
-        const float* srow = stage + 7 * ((static_cast<int64_t>(b) * nblk + lo) * DC_APB + (r - pre[lo]));
-        float* drow = buf + 1 + 7 * static_cast<int64_t>(r);
-#pragma unroll
-        for (int k = 0; k < 7; ++k) drow[k] = srow[k];
-    }
+    emit_image(blockIdx.x, stage, blk_cnt, nblk, max_objects, out, pre, wsum);
+}
+
+__global__ void zero_headers_kernel(float* __restrict__ out, int batch, int max_objects)
+{
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < batch) out[static_cast<int64_t>(b) * (1 + 7 * static_cast<int64_t>(max_objects))] = 0.0f;
 }
 
 int decode_blocks(int anchors) { return (anchors + DC_APB - 1) / DC_APB; }
-
-size_t decode_smem(int C) { return sizeof(float) * DC_APB * static_cast<size_t>(5 + C); }
 
 void launch_decode(const float* preds, int batch, int anchors, int C, float conf_thr, int max_objects, float* out,
                    float* stage, int* blk_cnt, cudaStream_t st)
 {
     const int nblk = decode_blocks(anchors);
-    const size_t smem = decode_smem(C);
+    if (nblk == 0) {  // no anchors: every header is 0
+        zero_headers_kernel<<<(batch + 255) / 256, 256, 0, st>>>(out, batch, max_objects);
+        return;
+    }
+    const size_t smem = sizeof(float) * DC_APB * static_cast<size_t>(5 + C);
     ensure_dynamic_smem(reinterpret_cast<const void*>(decode_kernel), smem);
     decode_kernel<<<dim3(nblk, batch), DC_APB, smem, st>>>(preds, anchors, C, conf_thr, nblk, stage, blk_cnt);
     const size_t esmem = sizeof(int) * (static_cast<size_t>(nblk) + 1);
     ensure_dynamic_smem(reinterpret_cast<const void*>(decode_emit_kernel), esmem);
-    launch_pdl(decode_emit_kernel, dim3(batch), dim3(DC_EMIT), esmem, st, static_cast<const float*>(stage),
+    launch_pdl(decode_emit_kernel, dim3(batch), dim3(DC_APB), esmem, st, static_cast<const float*>(stage),
                static_cast<const int*>(blk_cnt), nblk, max_objects, out);
 }
 

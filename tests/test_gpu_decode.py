@@ -100,3 +100,17 @@ def test_boxes7_headers_and_invalid_class():
     bad[0, 1 + 5] = 9.0         # class beyond num_classes
     with pytest.raises(g.NmsError):
         g.boxes7_nms(torch.from_numpy(bad).cuda(), 4, 0.5)
+
+
+def test_decode_no_anchors_and_repeat():
+    p = np.zeros((3, 0, 9), np.float32)
+    out = g.decode_boxes7(torch.from_numpy(p).cuda(), 0.1, 4).cpu().numpy()
+    _same(out, oracle.decode_boxes7(p, 0.1, 4))
+    # repeated calls with one workspace give the same buffers (the per-image
+    # completion counters are reset by every call)
+    q = _random_preds(9, 5, 3000, 20)
+    t = torch.from_numpy(q).cuda()
+    first = g.decode_boxes7(t, 0.3, 700).cpu().numpy()
+    for _ in range(3):
+        _same(g.decode_boxes7(t, 0.3, 700).cpu().numpy(), first)
+    _same(first, oracle.decode_boxes7(q, 0.3, 700))

@@ -115,6 +115,19 @@ def _dist():
     return ws, rank, local
 
 
+def aggregate_over_ranks(total_ms: float, world: int, n: int, steps: int, device="cpu"):
+    """Whole-job timing of `world` replicas: the slowest rank's total time
+    (all_reduce MAX over the process group when world > 1) and the aggregate
+    boxes/s of all ranks (each rank processes n boxes per step).  Returns
+    (total_ms, value)."""
+    if world > 1:
+        import torch
+        t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, world * n * steps / (total_ms / 1000)
+
+
 def cpu_oracle_run(wl, budget_s: float):
     """Time the oracle (as it stands, one thread) on full copies of the workload
     until about budget_s seconds have passed.  Returns (boxes/s, reps, seconds)."""
@@ -370,12 +383,8 @@ def run_gbnms(args):
     step_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
     total_ms = sum(step_ms)
     clocks = sampler.stop()
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = aggregate_over_ranks(total_ms, world, n, args.steps, device=dev)
     ms_per_step = total_ms / args.steps
-    value = world * n * args.steps / (total_ms / 1000)
 
     # ---- per-stage durations of the same calls: nms_run_timed records CUDA
     # events on the launching stream between the stages (L2 flushed before

@@ -37,6 +37,9 @@
 #ifndef GBNMS_MASK_WARPS
 #define GBNMS_MASK_WARPS 4
 #endif
+#ifndef GBNMS_MASK_ROWS
+#define GBNMS_MASK_ROWS 2
+#endif
 #ifndef GBNMS_MASK_CTAS_PER_SM
 #define GBNMS_MASK_CTAS_PER_SM 8
 #endif
@@ -54,18 +57,22 @@ constexpr int NQ = MT / 64;        // 64-bit words of a row per tile
 static_assert(MT == MASK_TILE_W, "the tile width the host stages by");
 static_assert(NQ == 1 || NQ == 2 || NQ == 4, "tile width of 64, 128 or 256 columns");
 constexpr int M_WARPS = GBNMS_MASK_WARPS;  // warps per CTA, each on its own units
+constexpr int RPL = GBNMS_MASK_ROWS;        // row boxes per lane
+constexpr int UR = 32 * RPL;                // rows of a unit
+static_assert(MT % UR == 0, "a column tile spans a whole number of row units");
 constexpr int M_THREADS = M_WARPS * 32;
 constexpr int M_CTAS_PER_SM = GBNMS_MASK_CTAS_PER_SM;  // resident CTAs per SM the grid is sized for
 
 // Far-away zero-area box used to pad ragged tiles: overlaps nothing.
 __device__ __forceinline__ float4 pad_box() { return make_float4(3e38f, 3e38f, 3e38f, 3e38f); }
 
-// Linear index k of the unit triangle -> (64-row tile a, MT-column tile c).
-// Column tile c meets row tiles a = 0 .. NQ(c+1)-1, so the units of columns
-// before c number NQ c(c+1)/2; enumeration is column by column.
+// Linear index k of the unit triangle -> (UR-row tile a, MT-column tile c).
+// Column tile c meets row tiles a = 0 .. r(c+1)-1 with r = MT/UR, so the
+// units of columns before c number r c(c+1)/2; enumeration is column by
+// column.
 __device__ __forceinline__ void tri_coords(long long k, int& a, int& c)
 {
-    constexpr long long r = NQ;
+    constexpr long long r = MT / UR;
     // A binary32 estimate (no binary64 on the hot path), made exact by the
     // integer corrections.
     long long cc = static_cast<long long>((sqrtf(8.0f * static_cast<float>(k) / r + 1.0f) - 1.0f) * 0.5f);
@@ -150,11 +157,11 @@ __device__ __forceinline__ void maybe2(const RowF2& r, float2 cnx1, float2 cx2, 
     acc = __funnelshift_l(__float_as_uint(t.x), acc, 1);
 }
 
-// Both rows of a lane against 32 staged columns starting at `base` (a
+// The lane's RPL rows against 32 staged columns starting at `base` (a
 // multiple of 4): one 16-byte shared load per coordinate brings 4 columns,
-// shared by both rows.
-__device__ __forceinline__ void maybe_half(const ColsSoA& C, int base, const RowF2& r0, const RowF2& r1,
-                                           float2 klo2, uint32_t& m0, uint32_t& m1)
+// shared by all the rows.
+__device__ __forceinline__ void maybe_half(const ColsSoA& C, int base, const RowF2 (&r)[RPL], float2 klo2,
+                                           uint32_t (&m)[RPL])
 {
 #pragma unroll kMaskUnroll
     for (int g = 7; g >= 0; --g) {
@@ -168,25 +175,26 @@ __device__ __forceinline__ void maybe_half(const ColsSoA& C, int base, const Row
                      dhi = make_float2(d.z, d.w), ehi = make_float2(e.z, e.w);
         const float2 alo = make_float2(a.x, a.y), blo = make_float2(b.x, b.y), clo = make_float2(c.x, c.y),
                      dlo = make_float2(d.x, d.y), elo = make_float2(e.x, e.y);
-        maybe2(r0, ahi, bhi, chi, dhi, ehi, klo2, m0);
-        maybe2(r1, ahi, bhi, chi, dhi, ehi, klo2, m1);
-        maybe2(r0, alo, blo, clo, dlo, elo, klo2, m0);
-        maybe2(r1, alo, blo, clo, dlo, elo, klo2, m1);
+#pragma unroll
+        for (int k = 0; k < RPL; ++k) maybe2(r[k], ahi, bhi, chi, dhi, ehi, klo2, m[k]);
+#pragma unroll
+        for (int k = 0; k < RPL; ++k) maybe2(r[k], alo, blo, clo, dlo, elo, klo2, m[k]);
     }
 }
 
-// The maybe words of two rows over the tile's NQ words.
-__device__ __forceinline__ void maybe_rows(const ColsSoA& C, const RowF2& r0, const RowF2& r1, float klo,
-                                           uint64_t (&w0)[NQ], uint64_t (&w1)[NQ])
+// The maybe words of the lane's rows over the tile's NQ words.
+__device__ __forceinline__ void maybe_rows(const ColsSoA& C, const RowF2 (&r)[RPL], float klo, uint64_t (&w)[RPL][NQ])
 {
     const float2 klo2 = dup2(__fmul_rn(2.0f, klo));
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
-        uint32_t lo0 = 0, hi0 = 0, lo1 = 0, hi1 = 0;
-        maybe_half(C, q * 64, r0, r1, klo2, lo0, lo1);
-        maybe_half(C, q * 64 + 32, r0, r1, klo2, hi0, hi1);
-        w0[q] = (static_cast<uint64_t>(hi0) << 32) | lo0;
-        w1[q] = (static_cast<uint64_t>(hi1) << 32) | lo1;
+        uint32_t lo[RPL], hi[RPL];
+#pragma unroll
+        for (int k = 0; k < RPL; ++k) lo[k] = hi[k] = 0;
+        maybe_half(C, q * 64, r, klo2, lo);
+        maybe_half(C, q * 64 + 32, r, klo2, hi);
+#pragma unroll
+        for (int k = 0; k < RPL; ++k) w[k][q] = (static_cast<uint64_t>(hi[k]) << 32) | lo[k];
     }
 }
 
@@ -268,31 +276,29 @@ __device__ __forceinline__ void store_words(uint64_t* dst, const uint64_t (&w)[N
 
 // The unit's outputs from its final words: the mask words, the per-row chunk
 // bits, the neighbour bitmap and the pair list.
-__device__ __forceinline__ void store_unit(const uint64_t (&w0)[NQ], const uint64_t (&w1)[NQ], int i0, int i1,
-                                           int cb, int n, unsigned l, uint64_t* __restrict__ mask,
-                                           int64_t ldw, unsigned long long* __restrict__ rowbits, int NB,
-                                           uint32_t* __restrict__ edges,
-                                           unsigned* __restrict__ ecount, unsigned ecap,
-                                           unsigned long long* __restrict__ haspred)
+__device__ __forceinline__ void store_unit(const uint64_t (&w)[RPL][NQ], const int (&i)[RPL], int cb, int n,
+                                           unsigned l, uint64_t* __restrict__ mask, int64_t ldw,
+                                           unsigned long long* __restrict__ rowbits, int NB,
+                                           uint32_t* __restrict__ edges, unsigned* __restrict__ ecount,
+                                           unsigned ecap, unsigned long long* __restrict__ haspred)
 {
     const int64_t wcol = cb / 64;
     const int chunk = cb >> 8;  // 256-column chunk of the per-row bitmap
-    if (i0 < n) {
-        if (mask) store_words(mask + static_cast<int64_t>(i0) * ldw + wcol, w0);
-        if (rowbits && or_words(w0))
-            atomicOr(rowbits + static_cast<int64_t>(i0) * NB + (chunk >> 6), 1ull << (chunk & 63));
-    }
-    if (i1 < n) {
-        if (mask) store_words(mask + static_cast<int64_t>(i1) * ldw + wcol, w1);
-        if (rowbits && or_words(w1))
-            atomicOr(rowbits + static_cast<int64_t>(i1) * NB + (chunk >> 6), 1ull << (chunk & 63));
+#pragma unroll
+    for (int k = 0; k < RPL; ++k) {
+        if (i[k] >= n) continue;
+        if (mask) store_words(mask + static_cast<int64_t>(i[k]) * ldw + wcol, w[k]);
+        if (rowbits && or_words(w[k]))
+            atomicOr(rowbits + static_cast<int64_t>(i[k]) * NB + (chunk >> 6), 1ull << (chunk & 63));
     }
     // Boxes with at least one earlier box over the threshold: the OR of the
     // warp's rows, one atomic per non-zero 64-column word.
     if (haspred) {
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
-            const uint64_t v = (i0 < n ? w0[q] : 0ull) | (i1 < n ? w1[q] : 0ull);
+            uint64_t v = 0;
+#pragma unroll
+            for (int k = 0; k < RPL; ++k) v |= i[k] < n ? w[k][q] : 0ull;
             const unsigned lo = __reduce_or_sync(FULL, static_cast<unsigned>(v));
             const unsigned hi = __reduce_or_sync(FULL, static_cast<unsigned>(v >> 32));
             if (static_cast<int>(l) == q && (lo | hi))
@@ -304,7 +310,9 @@ __device__ __forceinline__ void store_unit(const uint64_t (&w0)[NQ], const uint6
     // count still grows (it tells the resolve the list is incomplete) and
     // nothing is written.
     if (edges) {
-        const int cnt = (i0 < n ? popc_words(w0) : 0) + (i1 < n ? popc_words(w1) : 0);
+        int cnt = 0;
+#pragma unroll
+        for (int k = 0; k < RPL; ++k) cnt += i[k] < n ? popc_words(w[k]) : 0;
         int x = cnt;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -318,8 +326,9 @@ __device__ __forceinline__ void store_unit(const uint64_t (&w0)[NQ], const uint6
             base = __shfl_sync(FULL, base, 31);
             if (base <= ecap && static_cast<unsigned>(total) <= ecap - base) {
                 uint32_t* dst = edges + base + (x - cnt);
-                if (i0 < n) dst = emit_row(dst, w0, i0, cb);
-                if (i1 < n) emit_row(dst, w1, i1, cb);
+#pragma unroll
+                for (int k = 0; k < RPL; ++k)
+                    if (i[k] < n) dst = emit_row(dst, w[k], i[k], cb);
             }
         }
     }
@@ -347,9 +356,9 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
     for (long long u = u_begin + static_cast<long long>(blockIdx.x) * M_WARPS + wp; u < u_end; u += stride) {
         int a, c;
         tri_coords(u, a, c);
-        if (c >= T || a * 64 >= n) continue;  // beyond the device-side count (warp-uniform)
+        if (c >= T || a * UR >= n) continue;  // beyond the device-side count (warp-uniform)
         const int cb = c * MT;
-        const int rbase = a * 64;
+        const int rbase = a * UR;
         __syncwarp();  // the previous unit's reads of the staged columns are done
         bool ok = true;
 #pragma unroll
@@ -364,52 +373,50 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
             C.ny2[t] = -b.w;
             C.ar[t] = ar;
         }
-        const int i0 = rbase + static_cast<int>(l);
-        const int i1 = i0 + 32;
-        const float4 b0 = i0 < n ? boxes_s[i0] : pad_box();
-        const float4 b1 = i1 < n ? boxes_s[i1] : pad_box();
-        const float ar0 = i0 < n ? box_area(b0) : 0.0f;
-        const float ar1 = i1 < n ? box_area(b1) : 0.0f;
-        if (i0 < n) ok &= well_formed(b0, ar0);
-        if (i1 < n) ok &= well_formed(b1, ar1);
+        int i[RPL];
+        float4 bx[RPL];
+        float ar[RPL];
+#pragma unroll
+        for (int k = 0; k < RPL; ++k) {
+            i[k] = rbase + static_cast<int>(l) + 32 * k;
+            bx[k] = i[k] < n ? boxes_s[i[k]] : pad_box();
+            ar[k] = i[k] < n ? box_area(bx[k]) : 0.0f;
+            if (i[k] < n) ok &= well_formed(bx[k], ar[k]);
+        }
         const bool fast = __all_sync(FULL, ok) && p.fast_ok;
         __syncwarp();  // the staged columns are visible to the whole warp
 
-        uint64_t w0[NQ], w1[NQ];
+        uint64_t w[RPL][NQ];
         if (fast) {
-            maybe_rows(C, make_row(b0, ar0), make_row(b1, ar1), p.k_lo, w0, w1);
+            RowF2 r[RPL];
+#pragma unroll
+            for (int k = 0; k < RPL; ++k) r[k] = make_row(bx[k], ar[k]);
+            maybe_rows(C, r, p.k_lo, w);
         } else {
 #pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                w0[q] = ~0ull;
-                w1[q] = ~0ull;
+            for (int k = 0; k < RPL; ++k)
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) w[k][q] = ~0ull;
+        }
+        const bool diag = rbase + UR > cb;  // the unit meets the diagonal
+#pragma unroll
+        for (int k = 0; k < RPL; ++k) {
+            if (diag) clip_words(w[k], i[k], cb, n);
+            else if (cb + MT > n) clip_words(w[k], -1, cb, n);  // ragged last column tile
+            if (i[k] >= n) {
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) w[k][q] = 0;
             }
+            verify_words(C, bx[k], ar[k], p.thr, w[k]);
         }
-        if (rbase + 64 > cb) {  // the unit meets the diagonal
-            clip_words(w0, i0, cb, n);
-            clip_words(w1, i1, cb, n);
-        } else if (cb + MT > n) {  // ragged last column tile
-            clip_words(w0, -1, cb, n);
-            clip_words(w1, -1, cb, n);
-        }
-        if (i0 >= n) {
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) w0[q] = 0;
-        }
-        if (i1 >= n) {
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) w1[q] = 0;
-        }
-        verify_words(C, b0, ar0, p.thr, w0);
-        verify_words(C, b1, ar1, p.thr, w1);
-        store_unit(w0, w1, i0, i1, cb, n, l, mask, ldw, rowbits, NB, edges, ecount, ecap, haspred);
+        store_unit(w, i, cb, n, l, mask, ldw, rowbits, NB, edges, ecount, ecap, haspred);
     }
 }
 
 int64_t mask_tiles(int64_t n)
 {
     int64_t T = (n + MT - 1) / MT;
-    return NQ * T * (T + 1) / 2;
+    return (MT / UR) * T * (T + 1) / 2;
 }
 
 void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const ThrParams& p,

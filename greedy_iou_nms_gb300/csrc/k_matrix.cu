@@ -77,6 +77,24 @@ __device__ __forceinline__ void mx_coords(long long k, int& a, int& c)
     a = static_cast<int>(k - cc * (cc + 1) / 2);
 }
 
+// Binary64 work of pass B, queued per warp: a candidate (child column j, the
+// father's O_max, their IoU) is finished later with the other candidates of
+// the warp, one per lane, so that each binary64 instruction serves up to 32
+// candidates instead of the one or two rows a column leaves.
+constexpr int MX_Q = 96;  // queue entries per warp: flushed at 32, one column adds at most 64
+
+template <int PASS>
+__device__ __forceinline__ void mx_flush(const int* qj, const float* qom, const float* qo, int cnt,
+                                         unsigned long long* __restrict__ xmin_key)
+{
+    for (int e = static_cast<int>(lane_id()); e < cnt; e += 32) {
+        const double om = static_cast<double>(qom[e]), od = static_cast<double>(qo[e]);
+        const double x = PASS == 2 ? __ddiv_rn(__dsub_rn(1.0, od), __dsub_rn(1.0, om))
+                                   : __dsub_rn(__dmul_rn(om, om), __dmul_rn(od, od));
+        if (x == x) atomicMin(xmin_key + qj[e], dkey(x));
+    }
+}
+
 // PASS 0: O_max; 1: smallest Gaussian numerator; 2: smallest linear decay.
 template <int PASS>
 __global__ void __launch_bounds__(MX_THREADS)
@@ -85,6 +103,8 @@ matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m
 {
     __shared__ float4 cbox[MX_T];
     __shared__ float carea[MX_T];
+    __shared__ int q_j[PASS ? MX_THREADS / 32 : 1][MX_Q];
+    __shared__ float q_om[PASS ? MX_THREADS / 32 : 1][MX_Q], q_o[PASS ? MX_THREADS / 32 : 1][MX_Q];
     const int n = m_dev ? *m_dev : m_bound;
     int a, c;
     mx_coords(blockIdx.x, a, c);
@@ -117,6 +137,32 @@ matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m
         if (!(w > 0.0f && h > 0.0f && i < cb + k)) return false;
         o = iou_exact(r, ar, cbx, carea[k]);
         return o > 0.0f;
+    };
+    // The warp's queue of binary64 candidates (pass B).
+    const int wq = PASS ? (threadIdx.x >> 5) : 0;
+    int qn = 0;
+    auto queue = [&](bool c0, bool c1, int j, float o0, float o1) {
+        const unsigned b0 = __ballot_sync(FULL, c0), b1 = __ballot_sync(FULL, c1);
+        const unsigned below = (1u << l) - 1u;
+        if (c0) {
+            const int e = qn + __popc(b0 & below);
+            q_j[wq][e] = j;
+            q_om[wq][e] = static_cast<float>(om0);
+            q_o[wq][e] = o0;
+        }
+        if (c1) {
+            const int e = qn + __popc(b0) + __popc(b1 & below);
+            q_j[wq][e] = j;
+            q_om[wq][e] = static_cast<float>(om1);
+            q_o[wq][e] = o1;
+        }
+        qn += __popc(b0) + __popc(b1);
+        if (qn >= 32) {
+            __syncwarp();
+            mx_flush<PASS>(q_j[wq], q_om[wq], q_o[wq], qn, xmin_key);
+            __syncwarp();
+            qn = 0;
+        }
     };
     for (int k = 0; k < kend; ++k) {
         const float4 cbx = cbox[k];
@@ -154,16 +200,7 @@ matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m
                 ub = fminf(ub, q + e);
             }
             const float best = __uint_as_float(fkey_value(__reduce_min_sync(FULL, fkey(ub))));
-            unsigned long long key = ~0ull;
-            if (d0 && !(lo0 > best))
-                key = dkey(__ddiv_rn(__dsub_rn(1.0, static_cast<double>(o0)), __dsub_rn(1.0, om0)));
-            if (d1 && !(lo1 > best))
-                key = min(key, dkey(__ddiv_rn(__dsub_rn(1.0, static_cast<double>(o1)), __dsub_rn(1.0, om1))));
-            const unsigned hi = __reduce_min_sync(FULL, static_cast<unsigned>(key >> 32));
-            const unsigned lo = __reduce_min_sync(FULL, static_cast<unsigned>(key >> 32) == hi
-                                                            ? static_cast<unsigned>(key) : ~0u);
-            const unsigned long long mk = (static_cast<unsigned long long>(hi) << 32) | lo;
-            if (l == 0 && mk != ~0ull) atomicMin(xmin_key + j, mk);
+            queue(d0 && !(lo0 > best), d1 && !(lo1 > best), j, o0, o1);
         } else {
             // Smallest numerator O_max[i]^2 - O[i][j]^2 (binary64, products
             // exact, one rounding) over the warp's rows, one atomic.  Only
@@ -188,23 +225,12 @@ matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m
                 ub = fminf(ub, x + e);
             }
             const float best = __uint_as_float(fkey_value(__reduce_min_sync(FULL, fkey(ub))));
-            unsigned long long key = ~0ull;
-            if (ov0 && !(lo0 > best)) {
-                const double od = static_cast<double>(o0);
-                const double x = __dsub_rn(__dmul_rn(om0, om0), __dmul_rn(od, od));
-                if (x == x) key = dkey(x);
-            }
-            if (ov1 && !(lo1 > best)) {
-                const double od = static_cast<double>(o1);
-                const double x = __dsub_rn(__dmul_rn(om1, om1), __dmul_rn(od, od));
-                if (x == x) key = min(key, dkey(x));
-            }
-            const unsigned hi = __reduce_min_sync(FULL, static_cast<unsigned>(key >> 32));
-            const unsigned lo = __reduce_min_sync(FULL, static_cast<unsigned>(key >> 32) == hi
-                                                            ? static_cast<unsigned>(key) : ~0u);
-            const unsigned long long mk = (static_cast<unsigned long long>(hi) << 32) | lo;
-            if (l == 0 && mk != ~0ull) atomicMin(xmin_key + j, mk);
+            queue(ov0 && !(lo0 > best), ov1 && !(lo1 > best), j, o0, o1);
         }
+    }
+    if (PASS >= 1) {
+        __syncwarp();
+        mx_flush<PASS>(q_j[wq], q_om[wq], q_o[wq], qn, xmin_key);
     }
 }
 

@@ -100,12 +100,14 @@ __device__ __forceinline__ void emit_sorted(uint64_t k, int r, int m, const floa
 // shared memory (order inside a bucket does not matter) and then counts, for
 // each of its BR_CAND candidates, the smaller keys of its own bucket: the
 // work per CTA is linear in the chunk plus the candidates' bucket sizes.
-// The bucket of a key is its score key's offset in the [lo, hi] range of the
+// The bucket of a key is its offset in the [lo, hi] range of the keys of the
 // chunk's finite scores, shifted right so that the range fits the buckets
-// (score keys beyond the range, i.e. +inf, -inf and NaN, go to the end
-// buckets); it is monotone in the key, so buckets come in key order and
-// equal scores share one.
-// With one chunk the kernel writes perm and boxes_s, otherwise the chunk's
+// (keys beyond the range, i.e. of +inf, -inf and NaN, go to the end
+// buckets); it is monotone in the key, so buckets come in key order.  The
+// range is of whole keys, score and index, so that a run of equal scores
+// spreads over buckets by index instead of filling one.
+// With one chunk the kernel writes perm and boxes_s (the candidates' boxes
+// are loaded with their scores, at the start), otherwise the chunk's
 // sorted keys for the merge levels.  It also clears what the mask kernel
 // accumulates into: the status, the pair counter, the bitmap of boxes with an
 // earlier neighbour and the per-row chunk bitmaps of its candidates' rows.
@@ -117,16 +119,35 @@ constexpr int BR_KPT = MS_CHUNK / BR_THREADS;  // chunk keys per thread
 constexpr int BR_SOLO = 64;                    // buckets a single lane scans alone
 
 struct BucketMap {
-    uint32_t lo, hi;  // score-key range of the finite scores
+    uint64_t lo, hi;  // key range of the finite scores
     int shift;        // (hi - lo) >> shift < BR_BUCKETS
     __device__ __forceinline__ int operator()(uint64_t key) const
     {
-        const uint32_t k = static_cast<uint32_t>(key >> 32);
-        if (k < lo) return 0;
-        if (k > hi) return BR_BUCKETS - 1;
-        return static_cast<int>((k - lo) >> shift);
+        if (key < lo) return 0;
+        if (key > hi) return BR_BUCKETS - 1;
+        return static_cast<int>((key - lo) >> shift);
     }
 };
+
+__device__ __forceinline__ uint64_t warp_min_u64(uint64_t v)
+{
+#pragma unroll
+    for (int d = 16; d; d >>= 1) {
+        const uint64_t o = __shfl_xor_sync(FULL, v, d);
+        v = o < v ? o : v;
+    }
+    return v;
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v)
+{
+#pragma unroll
+    for (int d = 16; d; d >>= 1) {
+        const uint64_t o = __shfl_xor_sync(FULL, v, d);
+        v = o > v ? o : v;
+    }
+    return v;
+}
 
 __global__ void __launch_bounds__(BR_THREADS)
 bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ boxes,
@@ -139,7 +160,7 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
     int* start = reinterpret_cast<int*>(list + MS_CHUNK);            // [BR_BUCKETS + 1]
     int* cur = start + BR_BUCKETS + 1;                               // [BR_BUCKETS]
     __shared__ int wsum[BR_THREADS / 32];
-    __shared__ uint32_t wlo[BR_THREADS / 32], whi[BR_THREADS / 32];
+    __shared__ uint64_t wlo[BR_THREADS / 32], whi[BR_THREADS / 32];
     __shared__ uint64_t ckey[BR_CAND];  // this CTA's candidates
     __shared__ int crank[BR_CAND];
     pdl_release();  // the mask kernel may be scheduled (it waits for this grid's results)
@@ -165,12 +186,14 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
     if (!multi && q0 >= m) return;
 
     for (int b = tid; b < BR_BUCKETS; b += BR_THREADS) start[b] = 0;
+    float4 cbox = make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid < BR_CAND) {
         const int p = q0 + tid;
         uint64_t key = MS_PAD;
         if (p < m && p < c0 + MS_CHUNK) {
             const int xi = cand ? cand[p] : p;
             key = order_key(scores[xi], static_cast<uint32_t>(xi));
+            if (!multi) cbox = boxes[xi];
         }
         ckey[tid] = key;
     }
@@ -186,18 +209,18 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
     }
 #pragma unroll
     for (int u = 0; u < BR_KPT; ++u) sc[u] = xs[u] >= 0 ? scores[xs[u]] : 0.0f;
-    uint32_t lo = 0xffffffffu, hi = 0u;
+    uint64_t lo = ~0ull, hi = 0ull;
 #pragma unroll
     for (int u = 0; u < BR_KPT; ++u) {
         k[u] = xs[u] >= 0 ? order_key(sc[u], static_cast<uint32_t>(xs[u])) : MS_PAD;
         if (xs[u] >= 0 && isfinite(sc[u])) {
-            lo = min(lo, static_cast<uint32_t>(k[u] >> 32));
-            hi = max(hi, static_cast<uint32_t>(k[u] >> 32));
+            lo = min(lo, k[u]);
+            hi = max(hi, k[u]);
         }
     }
     const unsigned l = lane_id();
-    lo = __reduce_min_sync(FULL, lo);
-    hi = __reduce_max_sync(FULL, hi);
+    lo = warp_min_u64(lo);
+    hi = warp_max_u64(hi);
     if (l == 0) {
         wlo[tid >> 5] = lo;
         whi[tid >> 5] = hi;
@@ -205,12 +228,12 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
     __syncthreads();
     BucketMap bm;
     constexpr int NWARP = BR_THREADS / 32;
-    bm.lo = __reduce_min_sync(FULL, l < NWARP ? wlo[l] : 0xffffffffu);
-    bm.hi = __reduce_max_sync(FULL, l < NWARP ? whi[l] : 0u);
-    if (bm.lo > bm.hi) bm.lo = bm.hi = 0u;  // no finite score
+    bm.lo = warp_min_u64(l < NWARP ? wlo[l] : ~0ull);
+    bm.hi = warp_max_u64(l < NWARP ? whi[l] : 0ull);
+    if (bm.lo > bm.hi) bm.lo = bm.hi = 0ull;  // no finite score
     // Smallest shift with (hi - lo) >> shift < BR_BUCKETS (a power of two).
     static_assert((BR_BUCKETS & (BR_BUCKETS - 1)) == 0, "power-of-two bucket count");
-    const int span_bits = 32 - __clz(static_cast<int>(bm.hi - bm.lo));
+    const int span_bits = 64 - __clzll(static_cast<long long>(bm.hi - bm.lo));
     bm.shift = max(0, span_bits - (31 - __clz(BR_BUCKETS)));
 #pragma unroll
     for (int u = 0; u < BR_KPT; ++u)
@@ -285,7 +308,10 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
     __syncthreads();
     if (tid < BR_CAND && q0 + tid < c0 + MS_CHUNK) {
         if (multi) keys_out[c0 + crank[tid]] = ckey[tid];
-        else emit_sorted(ckey[tid], crank[tid], m, boxes, perm, boxes_s);
+        else if (crank[tid] < m) {
+            perm[crank[tid]] = static_cast<int>(static_cast<uint32_t>(ckey[tid]));
+            boxes_s[crank[tid]] = cbox;
+        }
     }
 }
 

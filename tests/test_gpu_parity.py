@@ -260,6 +260,20 @@ def test_identical_boxes_and_ties():
     _check_single(b, s, 0.99)
 
 
+@pytest.mark.parametrize("n", [8192, 20000])
+@pytest.mark.parametrize("levels", [1, 3, 16, 256])
+def test_score_runs_of_ties(n, levels):
+    # Runs of equal scores (one value, a few, quantised) over one sort chunk
+    # and over several (merged by index across chunk boundaries), with a
+    # sprinkle of infinities and NaN among them.
+    wl = W.single_8192(5)
+    rng = np.random.default_rng(levels)
+    b = np.concatenate([wl.boxes] * ((n + 8191) // 8192))[:n]
+    s = (rng.integers(0, levels, n) / levels + 0.25).astype(np.float32)
+    s[rng.choice(n, 5, replace=False)] = [np.inf, -np.inf, np.nan, np.inf, np.nan]
+    _check_single(b, s, 0.5)
+
+
 @pytest.mark.parametrize("max_out", [1, 2, 63, 64, 65, 500, 5000])
 def test_max_out_single(max_out):
     wl = W.single_8192(3)

@@ -86,9 +86,13 @@ __device__ __forceinline__ bool well_formed(float4 b, float area)
 //   Proof sketch: q = a/(s-a) and the two roundings put the canonical IoU in
 //   q(1 +- 2^-23); q <= T1 = thr(1-2^-21) <=> a <= s T1/(1+T1), and k_lo is
 //   below that ratio by a factor 1-2^-22, so the rounded IoU cannot exceed thr.
+//   The mask filter scales each box's area by k2 = 2 k_lo (1-2^-20), rounded
+//   down, once per box, and its proof (iou_mask) spends the 2^-20 on the
+//   roundings of those products.
 struct ThrParams {
     float thr;     // the binary32 threshold
     float k_lo;    // <= (T1/(1+T1)) (1-2^-22), T1 = thr (1-2^-21)
+    float k2;      // <= 2 k_lo (1-2^-20)
     int fast_ok;   // thr within [2^-20, 2^20]
 };
 

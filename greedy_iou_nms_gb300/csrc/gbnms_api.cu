@@ -144,12 +144,17 @@ ThrParams make_thr(float thr)
     const double t = thr;
     p.fast_ok = (t >= 0x1p-20 && t <= 0x1p20) ? 1 : 0;
     p.k_lo = 0.0f;
+    p.k2 = 0.0f;
     if (p.fast_ok) {
         const double T1 = t * (1.0 - 0x1p-21);
         const double k1 = T1 / (1.0 + T1) * (1.0 - 0x1p-22);
         float f1 = static_cast<float>(k1);
         if (static_cast<double>(f1) > k1) f1 = next_down(f1);
         p.k_lo = f1;
+        const double k2 = 2.0 * static_cast<double>(f1) * (1.0 - 0x1p-20);  // exact in binary64
+        float f2 = static_cast<float>(k2);
+        if (static_cast<double>(f2) > k2) f2 = next_down(f2);
+        p.k2 = f2;
     }
     return p;
 }

@@ -26,7 +26,8 @@
 // "maybe" bit for a superset of the suppressing pairs: it bounds the
 // intersection from above with packed two-column binary32 arithmetic (one
 // instruction for two columns) and compares it against k_lo times the area
-// sum, a comparison the canonical IoU > thr implies (see ThrParams).  Only
+// sum, a comparison the canonical IoU > thr implies (see ThrParams), with the
+// areas scaled once per box.  Only
 // the maybe bits, a small fraction of the pairs, are then decided by the
 // canonical IoU itself, so every stored bit is exactly the definition's.
 // Tiles holding a malformed box, and thresholds outside the filter's range,
@@ -90,7 +91,7 @@ struct ColsSoA {
     float* x2;
     float* y1;
     float* ny2;  // -y2
-    float* ar;   // canonical area
+    float* ka;   // RN(k2 * canonical area)
 };
 
 __device__ __forceinline__ float4 col_box(const ColsSoA& C, int t)
@@ -105,19 +106,19 @@ struct RowF2 {
     float2 nx;  // (-x1, -x1)
     float2 nw;  // (-y2, -y2)
     float2 y;   // (y1, y1)
-    float2 ar;  // (area, area)
+    float2 ka;  // RN(k2 * area), twice
 };
 
 __device__ __forceinline__ float2 dup2(float v) { return make_float2(v, v); }
 
-__device__ __forceinline__ RowF2 make_row(float4 b, float ar)
+__device__ __forceinline__ RowF2 make_row(float4 b, float ka)
 {
     RowF2 r;
     r.z = dup2(b.z);
     r.nx = dup2(-b.x);
     r.nw = dup2(-b.w);
     r.y = dup2(b.y);
-    r.ar = dup2(ar);
+    r.ka = dup2(ka);
     return r;
 }
 
@@ -125,18 +126,27 @@ __device__ __forceinline__ RowF2 make_row(float4 b, float ar)
 // (second column first, so that bit k ends up meaning column k when the
 // columns are walked from the highest down).
 //   width bound  w' = min(RN(r.x2 - c.x1), RN(c.x2 - r.x1)) >= the canonical
-//                RN(min(x2) - max(x1)) (both operands of each difference are
-//                bounds and rounding is monotone); w2 = w' + |w'| = 2 max(w', 0)
+//                w = RN(min(x2) - max(x1)) (both operands of each difference
+//                are bounds and rounding is monotone); w2 = w' + |w'| =
+//                2 max(w', 0)
 //   height bound h' likewise, computed negated: -h' = max(RN(c.y1 - r.y2),
 //                RN(r.y1 - c.y2))
-//   maybe        RN(2 k_lo * s - w2 h') < 0, s = RN(area_r + area_c); exact
-//                sign of the fused product.
-// For well-formed boxes a canonical suppression has inter > k_lo * s with
-// inter > 0, hence w2 h' >= 2 inter > 2 k_lo s and the maybe bit is set.  A
-// negative h' gives a non-positive product (no bit), as the clamped canonical
-// height 0 would.
-__device__ __forceinline__ void maybe2(const RowF2& r, float2 cnx1, float2 cx2, float2 cy1, float2 cny2, float2 car,
-                                       float2 klo2, uint32_t& acc)
+//   maybe        RN(RN(w2 (-h') + kc) + kr) < 0, with kc = RN(k2 area_c),
+//                kr = RN(k2 area_r) and k2 <= 2 k_lo (1 - 2^-20).
+// Why every suppressing pair of well-formed boxes gets its bit: it has
+// a = inter > k_lo s (ThrParams), w, h > 0 and so h' > 0.  With
+// A = 2 k_lo (area_r + area_c) and u = 2^-24:
+//   P = w2 h' >= 2 w h >= 2 a (1 - u) > 2 k_lo s (1 - u) >= A (1 - 2u),
+//   kc + kr <= k2 (area_r + area_c)(1 + u) <= A (1 - 2^-20)(1 + u),
+// so P - kc - kr > A (2^-20 - 3u) = 13 u A.  The first rounding, of
+// kc - P < 0, moves it by at most u (P - kc), and kr <= A (1 + u), so
+// t1 + kr < 0 still holds exactly and the second rounding keeps the sign
+// (a negative sum rounds to a negative number or -0, both with the sign bit
+// set).  A product past the binary32 range becomes -inf and sets the bit too.
+// A negative h' gives a non-negative product and no bit, as the clamped
+// canonical height 0 would give no suppression.
+__device__ __forceinline__ void maybe2(const RowF2& r, float2 cnx1, float2 cx2, float2 cy1, float2 cny2, float2 ckc,
+                                       uint32_t& acc)
 {
     const float2 ax = __fadd2_rn(r.z, cnx1);  // r.x2 - c.x1
     const float2 bx = __fadd2_rn(cx2, r.nx);  // c.x2 - r.x1
@@ -150,9 +160,7 @@ __device__ __forceinline__ void maybe2(const RowF2& r, float2 cnx1, float2 cx2, 
     float2 nh;
     nh.x = fmaxf(ay.x, by.x);
     nh.y = fmaxf(ay.y, by.y);
-    const float2 s = __fadd2_rn(r.ar, car);
-    const float2 na2 = __fmul2_rn(w2, nh);
-    const float2 t = __ffma2_rn(klo2, s, na2);
+    const float2 t = __fadd2_rn(__ffma2_rn(w2, nh, ckc), r.ka);
     acc = __funnelshift_l(__float_as_uint(t.y), acc, 1);
     acc = __funnelshift_l(__float_as_uint(t.x), acc, 1);
 }
@@ -160,8 +168,7 @@ __device__ __forceinline__ void maybe2(const RowF2& r, float2 cnx1, float2 cx2, 
 // The lane's RPL rows against 32 staged columns starting at `base` (a
 // multiple of 4): one 16-byte shared load per coordinate brings 4 columns,
 // shared by all the rows.
-__device__ __forceinline__ void maybe_half(const ColsSoA& C, int base, const RowF2 (&r)[RPL], float2 klo2,
-                                           uint32_t (&m)[RPL])
+__device__ __forceinline__ void maybe_half(const ColsSoA& C, int base, const RowF2 (&r)[RPL], uint32_t (&m)[RPL])
 {
 #pragma unroll kMaskUnroll
     for (int g = 7; g >= 0; --g) {
@@ -170,29 +177,28 @@ __device__ __forceinline__ void maybe_half(const ColsSoA& C, int base, const Row
         const float4 b = *reinterpret_cast<const float4*>(C.x2 + o);
         const float4 c = *reinterpret_cast<const float4*>(C.y1 + o);
         const float4 d = *reinterpret_cast<const float4*>(C.ny2 + o);
-        const float4 e = *reinterpret_cast<const float4*>(C.ar + o);
+        const float4 e = *reinterpret_cast<const float4*>(C.ka + o);
         const float2 ahi = make_float2(a.z, a.w), bhi = make_float2(b.z, b.w), chi = make_float2(c.z, c.w),
                      dhi = make_float2(d.z, d.w), ehi = make_float2(e.z, e.w);
         const float2 alo = make_float2(a.x, a.y), blo = make_float2(b.x, b.y), clo = make_float2(c.x, c.y),
                      dlo = make_float2(d.x, d.y), elo = make_float2(e.x, e.y);
 #pragma unroll
-        for (int k = 0; k < RPL; ++k) maybe2(r[k], ahi, bhi, chi, dhi, ehi, klo2, m[k]);
+        for (int k = 0; k < RPL; ++k) maybe2(r[k], ahi, bhi, chi, dhi, ehi, m[k]);
 #pragma unroll
-        for (int k = 0; k < RPL; ++k) maybe2(r[k], alo, blo, clo, dlo, elo, klo2, m[k]);
+        for (int k = 0; k < RPL; ++k) maybe2(r[k], alo, blo, clo, dlo, elo, m[k]);
     }
 }
 
 // The maybe words of the lane's rows over the tile's NQ words.
-__device__ __forceinline__ void maybe_rows(const ColsSoA& C, const RowF2 (&r)[RPL], float klo, uint64_t (&w)[RPL][NQ])
+__device__ __forceinline__ void maybe_rows(const ColsSoA& C, const RowF2 (&r)[RPL], uint64_t (&w)[RPL][NQ])
 {
-    const float2 klo2 = dup2(__fmul_rn(2.0f, klo));
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
         uint32_t lo[RPL], hi[RPL];
 #pragma unroll
         for (int k = 0; k < RPL; ++k) lo[k] = hi[k] = 0;
-        maybe_half(C, q * 64, r, klo2, lo);
-        maybe_half(C, q * 64 + 32, r, klo2, hi);
+        maybe_half(C, q * 64, r, lo);
+        maybe_half(C, q * 64 + 32, r, hi);
 #pragma unroll
         for (int k = 0; k < RPL; ++k) w[k][q] = (static_cast<uint64_t>(hi[k]) << 32) | lo[k];
     }
@@ -208,7 +214,8 @@ __device__ __forceinline__ void verify_words(const ColsSoA& C, float4 b, float a
             const int bit = __ffsll(static_cast<long long>(x)) - 1;
             x &= x - 1;
             const int t = 64 * q + bit;
-            if (suppress_exact(b, ar, col_box(C, t), C.ar[t], thr)) keep |= 1ull << bit;
+            const float4 c = col_box(C, t);
+            if (suppress_exact(b, ar, c, box_area(c), thr)) keep |= 1ull << bit;
         }
         w[q] = keep;
     }
@@ -342,7 +349,7 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
                 unsigned long long* __restrict__ haspred, int limit, long long u_begin, long long u_end,
                 const int* __restrict__ done)
 {
-    __shared__ __align__(16) float s_cols[M_WARPS][5][MT];  // per warp: -x1, x2, y1, -y2, area
+    __shared__ __align__(16) float s_cols[M_WARPS][5][MT];  // per warp: -x1, x2, y1, -y2, k2 area
 
     pdl_wait();     // the sort (or an earlier stage) has finished
     pdl_release();  // the resolve may be scheduled
@@ -371,7 +378,7 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
             C.x2[t] = b.z;
             C.y1[t] = b.y;
             C.ny2[t] = -b.w;
-            C.ar[t] = ar;
+            C.ka[t] = __fmul_rn(p.k2, ar);
         }
         int i[RPL];
         float4 bx[RPL];
@@ -390,8 +397,8 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
         if (fast) {
             RowF2 r[RPL];
 #pragma unroll
-            for (int k = 0; k < RPL; ++k) r[k] = make_row(bx[k], ar[k]);
-            maybe_rows(C, r, p.k_lo, w);
+            for (int k = 0; k < RPL; ++k) r[k] = make_row(bx[k], __fmul_rn(p.k2, ar[k]));
+            maybe_rows(C, r, w);
         } else {
 #pragma unroll
             for (int k = 0; k < RPL; ++k)

@@ -450,16 +450,16 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
         // removed source no longer matters, an open source blocks its target
         // and the pair stays.
         int nl = 0;
-        for (int k0 = 0; k0 < live; k0 += 4) {
-            uint32_t e[4];
-            uint2 ki[4];
+        for (int k0 = 0; k0 < live; k0 += 2) {  // two pairs a step (a short loop body)
+            uint32_t e[2];
+            uint2 ki[2];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) e[u] = k0 + u < live ? Es[tid + RV_THREADS * (k0 + u)] : 0xffffffffu;
+            for (int u = 0; u < 2; ++u) e[u] = k0 + u < live ? Es[tid + RV_THREADS * (k0 + u)] : 0xffffffffu;
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 2; ++u)
                 if (e[u] != 0xffffffffu) ki[u] = KR[e[u] >> 21];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 2; ++u) {
                 if (e[u] == 0xffffffffu) continue;
                 if (mark_pair(KR, BLK, e[u], ki[u])) Es[tid + RV_THREADS * nl++] = e[u];
             }
@@ -484,7 +484,7 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
     const int cap = max_out > 0 ? max_out : INT_MAX;
     int base = __reduce_add_sync(FULL, static_cast<int>(l) < warp ? wc : 0);
     const uint32_t below = (1u << l) - 1u;
-    constexpr int OW = 8;  // words whose loads are in flight together
+    constexpr int OW = 2;  // words per step (a short loop: its code is fetched cold after an L2 flush)
     for (int wb = w0; wb < w1 && base < cap; wb += OW) {
         uint32_t bits[OW];
         int v[OW];

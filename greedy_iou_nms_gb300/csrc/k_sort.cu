@@ -111,10 +111,14 @@ __device__ __forceinline__ void emit_sorted(uint64_t k, int r, int m, const floa
 // sorted keys for the merge levels.  It also clears what the mask kernel
 // accumulates into: the status, the pair counter, the bitmap of boxes with an
 // earlier neighbour and the per-row chunk bitmaps of its candidates' rows.
-constexpr int BR_THREADS = 512;
+// Threads of a ranking CTA: 1024 when the input is one chunk (half the
+// unrolled code per thread, which is fetched cold after an L2 flush, and the
+// chunk's loads spread over more threads), 512 with several chunks (two CTAs
+// per SM, so that the chunks' CTAs fit in one wave).
+constexpr int BR_THREADS_ONE = 1024;
+constexpr int BR_THREADS_MULTI = 512;
 constexpr int BR_CAND = 128;                   // candidates ranked per CTA
 constexpr int BR_BUCKETS = 4096;
-constexpr int BR_KPT = MS_CHUNK / BR_THREADS;  // chunk keys per thread
 
 constexpr int BR_SOLO = 64;                    // buckets a single lane scans alone
 
@@ -149,6 +153,7 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v)
     return v;
 }
 
+template <int BR_THREADS>
 __global__ void __launch_bounds__(BR_THREADS)
 bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ boxes,
                    const int* __restrict__ cand, const int* __restrict__ m_dev, int m_bound,
@@ -156,6 +161,7 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
                    int32_t* status, uint64_t* __restrict__ rowbits, int NB, unsigned* __restrict__ ecount,
                    uint64_t* __restrict__ haspred, int* __restrict__ zero8)
 {
+    constexpr int BR_KPT = MS_CHUNK / BR_THREADS;  // chunk keys per thread
     extern __shared__ __align__(16) uint64_t list[];                 // MS_CHUNK keys, bucket order
     int* start = reinterpret_cast<int*>(list + MS_CHUNK);            // [BR_BUCKETS + 1]
     int* cur = start + BR_BUCKETS + 1;                               // [BR_BUCKETS]
@@ -417,12 +423,19 @@ void launch_sort(const float* scores, const float4* boxes, const int* cand, cons
     const int chunks = sort_chunks(m_bound);
     const int per_chunk = chunks > 1 ? MS_CHUNK / BR_CAND : (m_bound + BR_CAND - 1) / BR_CAND;
     const size_t rank_smem = sizeof(uint64_t) * MS_CHUNK + sizeof(int) * (2 * BR_BUCKETS + 1);
-    ensure_dynamic_smem(reinterpret_cast<const void*>(bucket_rank_kernel), rank_smem);
     const size_t half = static_cast<size_t>(chunks) * MS_CHUNK;
     uint64_t* k0 = keys;
     uint64_t* k1 = keys ? keys + half : nullptr;
-    bucket_rank_kernel<<<dim3(per_chunk > 0 ? per_chunk : 1, chunks), BR_THREADS, rank_smem, st>>>(
-        scores, boxes, cand, m_dev, m_bound, k0, perm, boxes_s, status, rowbits, NB, ecount, haspred, zero8);
+    const dim3 grid(per_chunk > 0 ? per_chunk : 1, chunks);
+    if (chunks == 1) {
+        ensure_dynamic_smem(reinterpret_cast<const void*>(bucket_rank_kernel<BR_THREADS_ONE>), rank_smem);
+        bucket_rank_kernel<BR_THREADS_ONE><<<grid, BR_THREADS_ONE, rank_smem, st>>>(
+            scores, boxes, cand, m_dev, m_bound, k0, perm, boxes_s, status, rowbits, NB, ecount, haspred, zero8);
+    } else {
+        ensure_dynamic_smem(reinterpret_cast<const void*>(bucket_rank_kernel<BR_THREADS_MULTI>), rank_smem);
+        bucket_rank_kernel<BR_THREADS_MULTI><<<grid, BR_THREADS_MULTI, rank_smem, st>>>(
+            scores, boxes, cand, m_dev, m_bound, k0, perm, boxes_s, status, rowbits, NB, ecount, haspred, zero8);
+    }
     if (chunks == 1) return;
     const int tiles = chunks * (MS_CHUNK / ML_TILE);
     for (int run = MS_CHUNK; run < chunks * MS_CHUNK; run *= 2) {

@@ -405,28 +405,33 @@ def run_gbnms(args):
             stage_t[k].append(ev[k].elapsed_time(ev[k + 1]))
     sort_ms, mask_ms, resolve_ms = (statistics.mean(t) for t in stage_t)  # average launch duration
 
-    # ---- end to end through the host-memory pipeline: per step one pinned
-    # host->device copy of boxes and scores, nms_run, and one device->host
-    # copy of the count and the keep list, all inside the timed region.
-    pipe = g.HostPipeline(n, device=dev)
-    pipe.load(wl.boxes, wl.scores)
-    for _ in range(3):
-        pipe.run(wl.iou_thr, wl.score_thr, wl.max_out)
-    torch.cuda.synchronize()
-    e2e_t = []
-    for _ in range(args.steps):
-        flush.fill_(1)
+    # ---- end to end through the host-memory pipeline, inputs and outputs in
+    # pinned host memory and every transfer inside the timed region: by
+    # default the kernels read the input and write the count and the kept
+    # indices across the host link themselves (zero-copy); for comparison,
+    # one host->device copy in and one device->host copy out around nms_run.
+    def time_pipe(zero_copy):
+        pipe = g.HostPipeline(n, device=dev, zero_copy=zero_copy)
+        pipe.load(wl.boxes, wl.scores)
+        for _ in range(3):
+            pipe.run(wl.iou_thr, wl.score_thr, wl.max_out)
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        got_e2e = pipe.run(wl.iou_thr, wl.score_thr, wl.max_out)
-        b.record(stream)
-        b.synchronize()
-        e2e_t.append(a.elapsed_time(b))
-    e2e_ms = statistics.mean(e2e_t)
-    h2d = pipe.in_bytes
-    d2h = pipe.out_bytes(wl.max_out)
-    e2e_parity = bool(got_e2e.tolist() == got.tolist())
+        ts = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            res = pipe.run(wl.iou_thr, wl.score_thr, wl.max_out)
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return (statistics.mean(ts), pipe.in_bytes, pipe.out_bytes(wl.max_out), pipe.zero_copy,
+                bool(res.tolist() == got.tolist()))
+
+    e2e_ms, h2d, d2h, e2e_zc, e2e_parity = time_pipe(True)
+    cp_ms, cp_h2d, cp_d2h, _, cp_parity = time_pipe(False)
+    e2e_parity = e2e_parity and cp_parity
 
     if rank != 0:
         return 0
@@ -511,7 +516,11 @@ def run_gbnms(args):
         "roofline_iou_mask": mask_roof,
         "cpu_baseline": cpu,
         "e2e": {"value": n / (e2e_ms / 1000), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "transfer": ("zero-copy: the kernels read the pinned input and write the pinned output"
+                             if e2e_zc else "copies")},
+        "e2e_with_copies": {"value": n / (cp_ms / 1000), "unit": UNIT, "h2d_bytes_per_step": cp_h2d,
+                            "d2h_bytes_per_step": cp_d2h, "ms_per_step": cp_ms},
         "gpu_launches": 3 * args.steps,  # sort, mask, resolve per call at this size
         "clocks": clocks,
         "parity_vs_oracle": parity and e2e_parity,

@@ -33,7 +33,7 @@ NMS_MAX_SINGLE_N = 1 << 18
 EXPORTED = ("nms_status_string", "nms_workspace_size", "nms_run", "nms_fast_run", "nms_run_timed",
             "nms_matrix_workspace_size", "nms_matrix_run", "nms_mask_row_words", "nms_iou_mask",
             "nms_resolve_mask", "nms_resolve_mask_noalloc", "nms_decode_workspace_size", "nms_decode_boxes7",
-            "nms_boxes7_workspace_size", "nms_boxes7_run")
+            "nms_boxes7_workspace_size", "nms_boxes7_run", "nms_mapped_pointer")
 NMS_NOALLOC_MAX_N = 16384
 NMS_DECODE_MAX_ANCHORS = 1 << 20
 NMS_DECODE_MAX_CLASSES = 384
@@ -93,6 +93,8 @@ def load():
     lib.nms_boxes7_workspace_size.restype = ctypes.c_int
     lib.nms_boxes7_run.argtypes = [vp, i32, i32, i32, f32, i32, vp, vp, sz, vp]
     lib.nms_boxes7_run.restype = ctypes.c_int
+    lib.nms_mapped_pointer.argtypes = [vp, ctypes.POINTER(vp)]
+    lib.nms_mapped_pointer.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -101,6 +103,14 @@ def load():
 
 def nms_status_string(code: int) -> str:
     return load().nms_status_string(int(code)).decode()
+
+
+def nms_mapped_pointer(host_ptr: int) -> Optional[int]:
+    """Device address of mapped page-locked host memory, or None when host_ptr
+    is not such memory."""
+    out = ctypes.c_void_p()
+    st = load().nms_mapped_pointer(ctypes.c_void_p(host_ptr), ctypes.byref(out))
+    return out.value if st == NMS_OK and out.value else None
 
 
 def nms_workspace_size(n: int, batch: int = 0, num_classes: int = 0) -> int:
@@ -318,8 +328,7 @@ def nms(boxes, scores, iou_thr: float, *, class_ids=None, num_classes: Optional[
 
 class HostPipeline:
     """Greedy NMS of one image held in host memory, replayed as one CUDA graph
-    per call: a host->device copy of the input, the nms_run kernels and a
-    device->host copy of the result.
+    per call.
 
     The input is one pinned buffer: n boxes (xyxy fp32) followed by n scores;
     write them through ``boxes`` / ``scores`` (numpy views of the first n
@@ -328,20 +337,34 @@ class HostPipeline:
     plain call that also warms the library up), waits for it and returns the
     kept indices: a numpy view of the pinned output buffer (the count, then
     the indices), valid until the next call.
+
+    With ``zero_copy`` (the default, when the pinned buffers are mapped into
+    the device address space) the kernels read the input from host memory and
+    write the count and the kept indices there themselves: the graph is the
+    nms_run kernels alone.  Otherwise it is a host->device copy of the input,
+    the kernels and a device->host copy of the count and the output capacity.
     """
 
-    def __init__(self, n_max: int, device="cuda"):
+    def __init__(self, n_max: int, device="cuda", zero_copy: bool = True):
         torch = _torch()
         self.n_max = int(n_max)
         self.device = torch.device(device)
         self._h_in = torch.empty(max(5 * self.n_max, 4), dtype=torch.float32).pin_memory()
-        self._d_in = torch.empty(max(5 * self.n_max, 4), dtype=torch.float32, device=self.device)
         self._h_out = torch.empty(self.n_max + 1, dtype=torch.int64).pin_memory()
-        self._d_out = torch.empty(self.n_max + 1, dtype=torch.int64, device=self.device)
         self._status = torch.empty(1, dtype=torch.int32, device=self.device)
         self._out_np = self._h_out.numpy()
         self.workspace = Workspace(self.n_max, device=self.device)
         self._graphs = {}
+        self.zero_copy = False
+        if zero_copy:
+            din, dout = nms_mapped_pointer(self._h_in.data_ptr()), nms_mapped_pointer(self._h_out.data_ptr())
+            if din is not None and dout is not None:
+                self.zero_copy = True
+                self._in_addr, self._out_addr = din, dout
+        if not self.zero_copy:
+            self._d_in = torch.empty(max(5 * self.n_max, 4), dtype=torch.float32, device=self.device)
+            self._d_out = torch.empty(self.n_max + 1, dtype=torch.int64, device=self.device)
+            self._in_addr, self._out_addr = self._d_in.data_ptr(), self._d_out.data_ptr()
         self.set_n(self.n_max)
 
     def set_n(self, n: int) -> None:
@@ -363,23 +386,30 @@ class HostPipeline:
 
     @property
     def in_bytes(self) -> int:
+        """Input bytes that cross to the device per call."""
         return 20 * self.n
 
-    def out_bytes(self, max_out: int = 0) -> int:
+    def out_bytes(self, max_out: int = 0, kept: Optional[int] = None) -> int:
+        """Output bytes that cross to the host per call: the count and the
+        kept indices written in place (zero-copy; `kept` from the last run),
+        else the count and the whole output capacity copied."""
+        if self.zero_copy:
+            return 8 * (1 + (int(self._out_np[0]) if kept is None else int(kept)))
         return 8 * (1 + keep_capacity(self.n, None, max_out))
 
     def _enqueue(self, n, iou_thr, score_thr, max_out, stream):
         cap = keep_capacity(n, None, max_out)
-        self._d_in[: 5 * n].copy_(self._h_in[: 5 * n], non_blocking=True)
-        base_in = self._d_in.data_ptr()
-        base_out = self._d_out.data_ptr()
+        if not self.zero_copy:
+            self._d_in[: 5 * n].copy_(self._h_in[: 5 * n], non_blocking=True)
+        base_in, base_out = self._in_addr, self._out_addr
         st = nms_run(base_in if n else 0, base_in + 16 * n if n else 0, n, 0, 0, 0, 0, iou_thr,
                      -math.inf if score_thr is None else score_thr, max_out, base_out + 8,
                      max(cap, 1), base_out, self._status.data_ptr(), self.workspace.ptr,
                      self.workspace.bytes, stream.cuda_stream)
         if st != NMS_OK:
             raise NmsError(st, "nms_run")
-        self._h_out[: cap + 1].copy_(self._d_out[: cap + 1], non_blocking=True)
+        if not self.zero_copy:
+            self._h_out[: cap + 1].copy_(self._d_out[: cap + 1], non_blocking=True)
 
     def run(self, iou_thr: float, score_thr: Optional[float] = None, max_out: int = 0):
         torch = _torch()

@@ -187,6 +187,23 @@ extern "C" const char* nms_status_string(nms_status s)
     return "NMS_ERR_UNKNOWN";
 }
 
+extern "C" nms_status nms_mapped_pointer(const void* host_ptr, void** device_ptr)
+{
+    if (!host_ptr || !device_ptr) return NMS_ERR_INVALID_ARG;
+    *device_ptr = nullptr;
+    cudaGetLastError();
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, host_ptr) != cudaSuccess) {
+        cudaGetLastError();  // clear it: the pointer is simply not CUDA memory
+        return NMS_ERR_INVALID_ARG;
+    }
+    if (a.type != cudaMemoryTypeHost || !a.devicePointer) return NMS_ERR_INVALID_ARG;
+    // The offset of host_ptr inside its allocation carries over to the mapping.
+    const char* base_host = static_cast<const char*>(a.hostPointer);
+    *device_ptr = static_cast<char*>(a.devicePointer) + (static_cast<const char*>(host_ptr) - base_host);
+    return NMS_OK;
+}
+
 extern "C" nms_status nms_workspace_size(int64_t n, int32_t batch, int32_t num_classes,
                                          size_t* bytes)
 {

@@ -69,9 +69,25 @@ const char* nms_status_string(nms_status s);
 nms_status nms_workspace_size(int64_t n, int32_t batch, int32_t num_classes, size_t* bytes);
 
 /*
+ * The device address of page-locked host memory that is mapped into the
+ * device address space (memory from cudaHostAlloc or cudaMallocHost on a
+ * system with unified addressing).  Every "device" pointer argument of this
+ * library may be such an address: the kernels then read the input, or write
+ * the output, across the host link themselves, so a caller with its data in
+ * host memory needs no separate copies.
+ *   host_ptr       any address inside such an allocation.
+ *   device_ptr     receives the matching device address.
+ * Errors: NMS_ERR_INVALID_ARG (NULL arguments, or host_ptr is not mapped
+ *         page-locked host memory: device memory, pageable memory).  Pure
+ *         host query; enqueues nothing.
+ */
+nms_status nms_mapped_pointer(const void* host_ptr, void** device_ptr);
+
+/*
  * Greedy IoU NMS.
  *
- *   boxes          device fp32 [n][4] xyxy, 16-byte aligned.
+ *   boxes          device fp32 [n][4] xyxy, 16-byte aligned (see
+ *                  nms_mapped_pointer for host memory).
  *   scores         device fp32 [n].
  *   n              number of boxes, 0 <= n < 2^31.
  *   class_ids      device int32 [n] with values in [0, num_classes), or NULL

@@ -456,19 +456,40 @@ def test_max_out_needs_the_rest_of_the_mask(max_out, score_thr):
     _check_single(b, s, 0.5, max_out=max_out, score_thr=score_thr)
 
 
-def test_host_pipeline_matches_oracle():
-    """HostPipeline: one packed host->device copy in, one device->host copy
-    out; the kept indices equal the oracle's, for several sizes in one
-    pipeline (the tail of the buffers is reused)."""
-    pipe = g.HostPipeline(9000)
-    for name, seed in (("single_n8192", 0), ("single_n1000_ties", 2)):
+@pytest.mark.parametrize("zero_copy", [True, False])
+def test_host_pipeline_matches_oracle(zero_copy):
+    """HostPipeline, with the kernels reading and writing the pinned host
+    buffers in place (zero_copy) or with one packed host->device copy in and
+    one device->host copy out: the kept indices equal the oracle's, for
+    several sizes in one pipeline (the tail of the buffers is reused), and a
+    later call sees new inputs written into the same buffer."""
+    pipe = g.HostPipeline(9000, zero_copy=zero_copy)
+    assert pipe.zero_copy == zero_copy  # pinned torch memory is mapped here
+    for name, seed in (("single_n8192", 0), ("single_n1000_ties", 2), ("single_n8192", 1)):
         wl = W.make(name, seed)
         pipe.load(wl.boxes, wl.scores)
         got = pipe.run(wl.iou_thr, wl.score_thr, wl.max_out)
         exp = oracle.nms_single(wl.boxes, wl.scores, wl.iou_thr, max_out=wl.max_out)
         assert got.tolist() == exp.tolist()
+        assert pipe.out_bytes(wl.max_out) == 8 * (1 + (len(exp) if zero_copy else wl.boxes.shape[0]))
+    for mo in (5, 0):  # max_out through the captured graphs
+        wl = W.make("single_n1000_ties", 3)
+        pipe.load(wl.boxes, wl.scores)
+        exp = oracle.nms_single(wl.boxes, wl.scores, wl.iou_thr, max_out=mo)
+        assert pipe.run(wl.iou_thr, None, mo).tolist() == exp.tolist()
     pipe.set_n(0)
     assert len(pipe.run(0.5)) == 0
+
+
+def test_mapped_pointer():
+    """nms_mapped_pointer: pinned host memory maps (offsets carry over),
+    device memory and pageable memory do not."""
+    pinned = torch.empty(64, dtype=torch.float32).pin_memory()
+    base = g.nms_mapped_pointer(pinned.data_ptr())
+    assert base is not None
+    assert g.nms_mapped_pointer(pinned.data_ptr() + 16) == base + 16
+    assert g.nms_mapped_pointer(torch.empty(64, device="cuda").data_ptr()) is None
+    assert g.nms_mapped_pointer(np.zeros(64, np.float32).ctypes.data) is None
 
 
 @pytest.mark.parametrize("max_out", [0, 150])

@@ -10,14 +10,21 @@
 // The first box is a father of every other box and gives it a decay of at
 // most 1; a father that does not overlap box j gives exp(O_max[i]^2 / sigma)
 // >= 1.  So the smallest decay is min(1, smallest decay over the OVERLAPPING
-// fathers), and only overlapping pairs (IoU > 0) need work:
-//   pass A: tiles of the upper triangle; where two boxes overlap, the exact
-//           binary32 IoU, atomically maxed into O_max of the child;
-//   pass B: the same tiles; for each overlapping pair the binary64 numerator
-//           O_max[i]^2 - O[i][j]^2, atomically minimised per child through an
+// fathers), and only overlapping pairs (IoU > 0) need work.  Both passes walk
+// the upper triangle in units of 64 rows x 128 columns, one warp per unit:
+// a packed binary32 filter marks the pairs that may overlap (a superset, two
+// columns per instruction), the warp queues those pairs in shared memory and
+// takes them one per lane, and each unit folds its results per column in
+// shared memory before one global atomic per column:
+//   pass A: where two boxes overlap, the exact binary32 IoU, maxed into
+//           O_max of the child;
+//   pass B: for each overlapping pair the binary64 numerator
+//           O_max[i]^2 - O[i][j]^2, minimised per child through an
 //           order-preserving 64-bit key (dividing once per box by sigma > 0
 //           afterwards gives the smallest quotient: correctly rounded
-//           division by a positive number keeps the order);
+//           division by a positive number keeps the order); only pairs whose
+//           binary32 bound can still be the column's minimum take the
+//           binary64 value;
 //   decide: per box (all SMs), s * exp(min(0, smallest exponent)) against
 //           the threshold, decided in binary32 with expf when the result is
 //           clear of the threshold by more than its error bound, in binary64
@@ -36,8 +43,13 @@
 
 namespace gbnms {
 
-constexpr int MX_T = 128;             // tile rows and columns
-constexpr int MX_THREADS = 64;        // 2 warps x 2 rows per lane = 128 rows
+// Units of MU_ROWS rows x MU_COLS columns of the upper triangle, one per warp
+// (columns staged in the warp's own slice of shared memory, no CTA barrier).
+constexpr int MU_WARPS = 4;              // warps per CTA
+constexpr int MU_ROWS = 64;              // rows of a unit: two per lane
+constexpr int MU_COLS = 128;             // columns of a unit
+constexpr int MU_Q = 128;                // queued pairs per warp and round
+constexpr int MU_THREADS = 32 * MU_WARPS;
 
 // Order-preserving key of a non-NaN binary64 value (-0 below +0).
 __device__ __forceinline__ unsigned long long dkey(double x)
@@ -52,9 +64,6 @@ __device__ __forceinline__ double dkey_value(unsigned long long k)
     return __longlong_as_double(static_cast<long long>(b));
 }
 
-// Each warp reduces a column over its 64 rows before one atomic, and skips a
-// column no lane overlaps with one vote.
-
 // Order-preserving 32-bit key of a binary32 value (NaN not expected) and back.
 __device__ __forceinline__ unsigned fkey(float x)
 {
@@ -64,173 +73,278 @@ __device__ __forceinline__ unsigned fkey(float x)
 
 __device__ __forceinline__ unsigned fkey_value(unsigned k) { return (k >> 31) ? (k & 0x7fffffffu) : ~k; }
 
-// Linear index k of the triangle of MX_T x MX_T tiles, column by column ->
-// (row tile a, column tile c), a <= c.  A binary32 estimate made exact by the
-// integer corrections.
-__device__ __forceinline__ void mx_coords(long long k, int& a, int& c)
+// Linear index k of the triangle of units, column by column -> (row unit a,
+// column tile c): column tile c meets row units 0 .. 2(c+1)-1.  A binary32
+// estimate made exact by the integer corrections.
+__device__ __forceinline__ void mu_coords(long long k, int& a, int& c)
 {
-    long long cc = static_cast<long long>((sqrtf(8.0f * static_cast<float>(k) + 1.0f) - 1.0f) * 0.5f);
+    constexpr long long r = MU_COLS / MU_ROWS;
+    long long cc = static_cast<long long>((sqrtf(8.0f * static_cast<float>(k) / r + 1.0f) - 1.0f) * 0.5f);
     if (cc < 0) cc = 0;
-    while ((cc + 1) * (cc + 2) / 2 <= k) ++cc;
-    while (cc > 0 && cc * (cc + 1) / 2 > k) --cc;
+    while (r * (cc + 1) * (cc + 2) / 2 <= k) ++cc;
+    while (cc > 0 && r * cc * (cc + 1) / 2 > k) --cc;
     c = static_cast<int>(cc);
-    a = static_cast<int>(k - cc * (cc + 1) / 2);
+    a = static_cast<int>(k - r * cc * (cc + 1) / 2);
 }
 
-// Binary64 work of pass B, queued per warp: a candidate (child column j, the
-// father's O_max, their IoU) is finished later with the other candidates of
-// the warp, one per lane, so that each binary64 instruction serves up to 32
-// candidates instead of the one or two rows a column leaves.
-constexpr int MX_Q = 96;  // queue entries per warp: flushed at 32, one column adds at most 64
-
-template <int PASS>
-__device__ __forceinline__ void mx_flush(const int* qj, const float* qom, const float* qo, int cnt,
-                                         unsigned long long* __restrict__ xmin_key)
+long long matrix_units(long long n)
 {
-    for (int e = static_cast<int>(lane_id()); e < cnt; e += 32) {
-        const double om = static_cast<double>(qom[e]), od = static_cast<double>(qo[e]);
-        const double x = PASS == 2 ? __ddiv_rn(__dsub_rn(1.0, od), __dsub_rn(1.0, om))
-                                   : __dsub_rn(__dmul_rn(om, om), __dmul_rn(od, od));
-        if (x == x) atomicMin(xmin_key + qj[e], dkey(x));
-    }
+    const long long T = (n + MU_COLS - 1) / MU_COLS;
+    return (MU_COLS / MU_ROWS) * T * (T + 1) / 2;
 }
+
+// A coordinate the packed overlap filter takes: 0, or a finite magnitude in
+// [2^-40, 2^40].  Any nonzero difference of two such values is at least 2^-63
+// and at most 2^41, so the product of two differences is a normal binary32
+// number of the right sign (no underflow to 0, no overflow).
+__device__ __forceinline__ bool filter_coord(float v)
+{
+    const float a = fabsf(v);
+    return a == 0.0f || (a >= 0x1p-40f && a <= 0x1p40f);
+}
+
+__device__ __forceinline__ bool filter_box(float4 b)
+{
+    return filter_coord(b.x) && filter_coord(b.y) && filter_coord(b.z) && filter_coord(b.w);
+}
+
+// A row box spread over register pairs (both halves equal).
+struct RowO {
+    float2 x2, nx1, ny2, y1;
+};
+
+// The overlap filter for one row and two adjacent columns, shifted into acc
+// (second column first).  A pair overlaps (the canonical w > 0 and h > 0)
+// only if r.x2 > c.x1 and c.x2 > r.x1, i.e. both rounded differences
+// ax = r.x2 - c.x1 and bx = c.x2 - r.x1 are positive and so is their product X
+// (at most one of them is negative for boxes with x2 >= x1, and a product of
+// a positive and a negative one is negative); likewise Y, the product of
+// c.y1 - r.y2 and r.y1 - c.y2, both negative where they overlap in y.  The bit
+// is the sign of max(-X, -Y): set where both products are positive (or -0 when
+// X or Y is 0: a superset, which the exact test below sorts out).
+__device__ __forceinline__ void overlap2(const RowO& r, float2 cnx1, float2 cx2, float2 cy1, float2 cny2,
+                                         uint32_t& acc)
+{
+    const float2 ax = __fadd2_rn(r.x2, cnx1);
+    const float2 bx = __fadd2_rn(cx2, r.nx1);
+    const float2 ay = __fadd2_rn(cy1, r.ny2);
+    const float2 by = __fadd2_rn(r.y1, cny2);
+    const float2 X = __fmul2_rn(ax, bx);
+    const float2 Y = __fmul2_rn(ay, by);
+    const float tx = fmaxf(-X.x, -Y.x), ty = fmaxf(-X.y, -Y.y);
+    acc = __funnelshift_l(__float_as_uint(ty), acc, 1);
+    acc = __funnelshift_l(__float_as_uint(tx), acc, 1);
+}
+
+// Per-warp shared memory of the passes.
+struct MxWarp {
+    unsigned long long colmin[MU_COLS];  // passes 1, 2: smallest binary64 key per column
+    float4 rows[MU_ROWS];                // the unit's row boxes
+    float nx1[MU_COLS], x2[MU_COLS], y1[MU_COLS], ny2[MU_COLS];  // columns, x1 and y2 negated
+    unsigned colacc[MU_COLS];            // pass 0: largest IoU bits; passes 1, 2: smallest upper-bound key
+    uint32_t qe[MU_Q];                   // queued pairs: row << 8 | column
+    float qo[MU_Q];                      // their IoU (0: no overlap)
+    float qlo[MU_Q];                     // lower bound of their binary32 value (passes 1, 2)
+    float om[MU_ROWS];                   // O_max of the rows (passes 1, 2)
+};
 
 // PASS 0: O_max; 1: smallest Gaussian numerator; 2: smallest linear decay.
 template <int PASS>
-__global__ void __launch_bounds__(MX_THREADS)
+__global__ void __launch_bounds__(MU_THREADS, 8)
 matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_dev, int m_bound,
-                   float sigma, unsigned* __restrict__ omax_bits, unsigned long long* __restrict__ xmin_key)
+                   long long units, unsigned* __restrict__ omax_bits, unsigned long long* __restrict__ xmin_key)
 {
-    __shared__ float4 cbox[MX_T];
-    __shared__ float carea[MX_T];
-    __shared__ int q_j[PASS ? MX_THREADS / 32 : 1][MX_Q];
-    __shared__ float q_om[PASS ? MX_THREADS / 32 : 1][MX_Q], q_o[PASS ? MX_THREADS / 32 : 1][MX_Q];
+    __shared__ __align__(16) MxWarp sw[MU_WARPS];
+    const int wp = threadIdx.x >> 5;
+    const long long u = static_cast<long long>(blockIdx.x) * MU_WARPS + wp;
+    if (u >= units) return;  // warp-uniform
     const int n = m_dev ? *m_dev : m_bound;
     int a, c;
-    mx_coords(blockIdx.x, a, c);
-    const int cb = c * MX_T, rb = a * MX_T;
-    if (cb >= n) return;
-    for (int t = threadIdx.x; t < MX_T; t += MX_THREADS) {
+    mu_coords(u, a, c);
+    const int cb = c * MU_COLS, rbase = a * MU_ROWS;
+    if (cb >= n || rbase >= n) return;
+    MxWarp& W = sw[wp];
+    const unsigned l = lane_id();
+    bool ok = true;
+#pragma unroll
+    for (int t = static_cast<int>(l); t < MU_COLS; t += 32) {
         const int j = cb + t;
         const float4 b = j < n ? boxes_s[j] : make_float4(0.f, 0.f, 0.f, 0.f);
-        cbox[t] = b;
-        carea[t] = box_area(b);
+        ok &= filter_box(b);
+        W.nx1[t] = -b.x;
+        W.x2[t] = b.z;
+        W.y1[t] = b.y;
+        W.ny2[t] = -b.w;
+        W.colacc[t] = PASS == 0 ? 0u : 0xffffffffu;
+        if (PASS) W.colmin[t] = ~0ull;
     }
-    const unsigned l = lane_id();
-    const int i0 = rb + (threadIdx.x >> 5) * 64 + static_cast<int>(l), i1 = i0 + 32;
-    const bool v0 = i0 < n, v1 = i1 < n;
-    const float4 r0 = v0 ? boxes_s[i0] : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4 r1 = v1 ? boxes_s[i1] : make_float4(0.f, 0.f, 0.f, 0.f);
-    const float ar0 = box_area(r0), ar1 = box_area(r1);
-    double om0 = 0.0, om1 = 0.0;
-    if (PASS >= 1) {
-        if (v0) om0 = static_cast<double>(__uint_as_float(omax_bits[i0]));
-        if (v1) om1 = static_cast<double>(__uint_as_float(omax_bits[i1]));
+    int i[2];
+    float4 rb[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        i[k] = rbase + static_cast<int>(l) + 32 * k;
+        rb[k] = i[k] < n ? boxes_s[i[k]] : make_float4(0.f, 0.f, 0.f, 0.f);
+        ok &= filter_box(rb[k]);
+        W.rows[l + 32 * k] = rb[k];
+        if (PASS) W.om[l + 32 * k] = i[k] < n ? __uint_as_float(omax_bits[i[k]]) : 0.0f;
     }
-    __syncthreads();
-    const int kend = min(MX_T, n - cb);
-    // Row i's overlap with column box k, if any (IoU > 0, i before j).
-    auto overlap = [&](int i, const float4& r, float ar, int k, float& o) -> bool {
-        const float4 cbx = cbox[k];
-        const float w = __fsub_rn(fminf(r.z, cbx.z), fmaxf(r.x, cbx.x));
-        const float h = __fsub_rn(fminf(r.w, cbx.w), fmaxf(r.y, cbx.y));
-        if (!(w > 0.0f && h > 0.0f && i < cb + k)) return false;
-        o = iou_exact(r, ar, cbx, carea[k]);
-        return o > 0.0f;
-    };
-    // The warp's queue of binary64 candidates (pass B).
-    const int wq = PASS ? (threadIdx.x >> 5) : 0;
-    int qn = 0;
-    auto queue = [&](bool c0, bool c1, int j, float o0, float o1) {
-        const unsigned b0 = __ballot_sync(FULL, c0), b1 = __ballot_sync(FULL, c1);
-        const unsigned below = (1u << l) - 1u;
-        if (c0) {
-            const int e = qn + __popc(b0 & below);
-            q_j[wq][e] = j;
-            q_om[wq][e] = static_cast<float>(om0);
-            q_o[wq][e] = o0;
+    const bool fast = __all_sync(FULL, ok);
+    __syncwarp();
+
+    // Candidate bits: row k of the lane, 64-column word q.
+    uint64_t w[2][2];
+    if (fast) {
+        RowO r[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            r[k].x2 = make_float2(rb[k].z, rb[k].z);
+            r[k].nx1 = make_float2(-rb[k].x, -rb[k].x);
+            r[k].ny2 = make_float2(-rb[k].w, -rb[k].w);
+            r[k].y1 = make_float2(rb[k].y, rb[k].y);
         }
-        if (c1) {
-            const int e = qn + __popc(b0) + __popc(b1 & below);
-            q_j[wq][e] = j;
-            q_om[wq][e] = static_cast<float>(om1);
-            q_o[wq][e] = o1;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            uint32_t h[2][2] = {{0u, 0u}, {0u, 0u}};  // [half][row]
+#pragma unroll
+            for (int half = 1; half >= 0; --half) {
+#pragma unroll 2
+                for (int g = 7; g >= 0; --g) {
+                    const int o = 64 * q + 32 * half + 4 * g;
+                    const float4 A = *reinterpret_cast<const float4*>(W.nx1 + o);
+                    const float4 B = *reinterpret_cast<const float4*>(W.x2 + o);
+                    const float4 C = *reinterpret_cast<const float4*>(W.y1 + o);
+                    const float4 D = *reinterpret_cast<const float4*>(W.ny2 + o);
+#pragma unroll
+                    for (int k = 0; k < 2; ++k)
+                        overlap2(r[k], make_float2(A.z, A.w), make_float2(B.z, B.w), make_float2(C.z, C.w),
+                                 make_float2(D.z, D.w), h[half][k]);
+#pragma unroll
+                    for (int k = 0; k < 2; ++k)
+                        overlap2(r[k], make_float2(A.x, A.y), make_float2(B.x, B.y), make_float2(C.x, C.y),
+                                 make_float2(D.x, D.y), h[half][k]);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) w[k][q] = (static_cast<uint64_t>(h[1][k]) << 32) | h[0][k];
         }
-        qn += __popc(b0) + __popc(b1);
-        if (qn >= 32) {
-            __syncwarp();
-            mx_flush<PASS>(q_j[wq], q_om[wq], q_o[wq], qn, xmin_key);
-            __syncwarp();
-            qn = 0;
-        }
-    };
-    for (int k = 0; k < kend; ++k) {
-        const float4 cbx = cbox[k];
-        const bool maybe0 = v0 && fminf(r0.z, cbx.z) > fmaxf(r0.x, cbx.x) && fminf(r0.w, cbx.w) > fmaxf(r0.y, cbx.y);
-        const bool maybe1 = v1 && fminf(r1.z, cbx.z) > fmaxf(r1.x, cbx.x) && fminf(r1.w, cbx.w) > fmaxf(r1.y, cbx.y);
-        if (!__any_sync(FULL, maybe0 || maybe1)) continue;  // no lane overlaps column k
-        float o0 = 0.0f, o1 = 0.0f;
-        const bool ov0 = maybe0 && overlap(i0, r0, ar0, k, o0);
-        const bool ov1 = maybe1 && overlap(i1, r1, ar1, k, o1);
-        const int j = cb + k;
-        if (PASS == 0) {
-            // largest overlap of the column over the warp's rows, one atomic
-            const unsigned m = max(ov0 ? __float_as_uint(o0) : 0u, ov1 ? __float_as_uint(o1) : 0u);
-            const unsigned r = __reduce_max_sync(FULL, m);
-            if (l == 0 && r) atomicMax(omax_bits + j, r);
-        } else if (PASS == 2) {
-            // Smallest decay (1 - O[i][j]) / (1 - O_max[i]) over the warp's
-            // rows, one atomic.  Rows bound their quotient in binary32 (three
-            // roundings, each within 2^-24 relative; a margin of 2^-20), and
-            // only rows whose lower bound does not exceed the smallest upper
-            // bound take the binary64 quotient.  O_max = 1 (a zero
-            // denominator, the same in both precisions) contributes nothing.
-            float lo0 = INFINITY, lo1 = INFINITY, ub = INFINITY;
-            const bool d0 = ov0 && static_cast<float>(om0) < 1.0f, d1 = ov1 && static_cast<float>(om1) < 1.0f;
-            if (d0) {
-                const float q = __fdiv_rn(__fsub_rn(1.0f, o0), __fsub_rn(1.0f, static_cast<float>(om0)));
-                const float e = __fmul_rn(q, 0x1p-20f);
-                lo0 = q - e;
-                ub = q + e;
-            }
-            if (d1) {
-                const float q = __fdiv_rn(__fsub_rn(1.0f, o1), __fsub_rn(1.0f, static_cast<float>(om1)));
-                const float e = __fmul_rn(q, 0x1p-20f);
-                lo1 = q - e;
-                ub = fminf(ub, q + e);
-            }
-            const float best = __uint_as_float(fkey_value(__reduce_min_sync(FULL, fkey(ub))));
-            queue(d0 && !(lo0 > best), d1 && !(lo1 > best), j, o0, o1);
-        } else {
-            // Smallest numerator O_max[i]^2 - O[i][j]^2 (binary64, products
-            // exact, one rounding) over the warp's rows, one atomic.  Only
-            // rows that can hold the minimum compute it in binary64: each
-            // overlapping row bounds its numerator in binary32 (three
-            // roundings, each within 2^-24 of a term of magnitude at most
-            // om^2 + o^2), the warp takes the smallest upper bound, and rows
-            // whose lower bound does not exceed it are the candidates.
-            float lo0 = INFINITY, lo1 = INFINITY, ub = INFINITY;
-            if (ov0) {
-                const float a = __fmul_rn(static_cast<float>(om0), static_cast<float>(om0)), b = __fmul_rn(o0, o0);
-                const float e = __fmul_rn(0x1p-22f, __fadd_rn(a, b)) + 0x1p-140f;
-                const float x = __fsub_rn(a, b);
-                lo0 = x - e;
-                ub = x + e;
-            }
-            if (ov1) {
-                const float a = __fmul_rn(static_cast<float>(om1), static_cast<float>(om1)), b = __fmul_rn(o1, o1);
-                const float e = __fmul_rn(0x1p-22f, __fadd_rn(a, b)) + 0x1p-140f;
-                const float x = __fsub_rn(a, b);
-                lo1 = x - e;
-                ub = fminf(ub, x + e);
-            }
-            const float best = __uint_as_float(fkey_value(__reduce_min_sync(FULL, fkey(ub))));
-            queue(ov0 && !(lo0 > best), ov1 && !(lo1 > best), j, o0, o1);
-        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) w[k][0] = w[k][1] = ~0ull;
     }
-    if (PASS >= 1) {
+    // Only j > i, j < n.
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int j0 = cb + 64 * q;
+            uint64_t keep = ~0ull;
+            const int lo = i[k] + 1 - j0, hi = n - j0;
+            if (i[k] >= n || lo >= 64 || hi <= 0) keep = 0;
+            else {
+                if (lo > 0) keep &= ~0ull << lo;
+                if (hi < 64) keep &= (1ull << hi) - 1ull;
+            }
+            w[k][q] &= keep;
+        }
+
+    // The candidates of the warp, MU_Q at a time, one per lane: the exact
+    // test and IoU, then the pass's reduction into the column accumulators.
+    int cnt = 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) cnt += __popcll(w[k][0]) + __popcll(w[k][1]);
+    int x = cnt;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, d);
+        if (static_cast<int>(l) >= d) x += y;
+    }
+    const int total = __shfl_sync(FULL, x, 31);
+    int rk = x - cnt;  // rank of the lane's next candidate
+    const int rend = x;
+    for (int base = 0; base < total; base += MU_Q) {
+        const int lim = min(rend, base + MU_Q);
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+                while (w[k][q] && rk < lim) {
+                    const int bit = __ffsll(static_cast<long long>(w[k][q])) - 1;
+                    w[k][q] &= w[k][q] - 1;
+                    W.qe[rk - base] = (static_cast<uint32_t>(32 * k + static_cast<int>(l)) << 8) |
+                                      static_cast<uint32_t>(64 * q + bit);
+                    ++rk;
+                }
         __syncwarp();
-        mx_flush<PASS>(q_j[wq], q_om[wq], q_o[wq], qn, xmin_key);
+        const int m = min(MU_Q, total - base);
+        for (int e = static_cast<int>(l); e < m; e += 32) {
+            const uint32_t qe = W.qe[e];
+            const int rl = static_cast<int>(qe >> 8), t = static_cast<int>(qe & 255u);
+            const float4 r = W.rows[rl];
+            const float4 cbx = make_float4(-W.nx1[t], W.y1[t], W.x2[t], -W.ny2[t]);
+            // Overlap (IoU > 0) exactly as the canonical formula has it.
+            const float ww = __fsub_rn(fminf(r.z, cbx.z), fmaxf(r.x, cbx.x));
+            const float hh = __fsub_rn(fminf(r.w, cbx.w), fmaxf(r.y, cbx.y));
+            float o = 0.0f;
+            if (ww > 0.0f && hh > 0.0f) {
+                o = iou_exact(r, box_area(r), cbx, box_area(cbx));
+                if (!(o > 0.0f)) o = 0.0f;
+            }
+            if (PASS == 0) {
+                if (o > 0.0f) atomicMax(&W.colacc[t], __float_as_uint(o));
+            } else {
+                const float om = W.om[rl];
+                float lo = INFINITY;
+                if (PASS == 2) {
+                    // The decay (1 - o) / (1 - om) in binary32 within a 2^-20
+                    // margin (three roundings of 2^-24 each); om = 1 gives
+                    // nothing.
+                    if (o > 0.0f && om < 1.0f) {
+                        const float q = __fdiv_rn(__fsub_rn(1.0f, o), __fsub_rn(1.0f, om));
+                        const float eb = __fmul_rn(q, 0x1p-20f);
+                        lo = q - eb;
+                        atomicMin(&W.colacc[t], fkey(q + eb));
+                    }
+                } else if (o > 0.0f) {
+                    // The numerator om^2 - o^2 in binary32, within a margin of
+                    // 2^-22 of om^2 + o^2 (three roundings) plus an absolute
+                    // term for tiny values.
+                    const float aa = __fmul_rn(om, om), bb = __fmul_rn(o, o);
+                    const float eb = __fmul_rn(0x1p-22f, __fadd_rn(aa, bb)) + 0x1p-140f;
+                    const float xx = __fsub_rn(aa, bb);
+                    lo = xx - eb;
+                    atomicMin(&W.colacc[t], fkey(xx + eb));
+                }
+                W.qo[e] = o;
+                W.qlo[e] = lo;
+            }
+        }
+        if (PASS) {
+            __syncwarp();
+            // Candidates that can hold the column's minimum: the binary64
+            // value, products exact and one rounding (Gaussian), or the
+            // correctly rounded quotient (linear).
+            for (int e = static_cast<int>(l); e < m; e += 32) {
+                const float lo = W.qlo[e];
+                const int t = static_cast<int>(W.qe[e] & 255u);
+                if (lo == INFINITY || lo > __uint_as_float(fkey_value(W.colacc[t]))) continue;
+                const double om = static_cast<double>(W.om[W.qe[e] >> 8]), od = static_cast<double>(W.qo[e]);
+                const double v = PASS == 2 ? __ddiv_rn(__dsub_rn(1.0, od), __dsub_rn(1.0, om))
+                                           : __dsub_rn(__dmul_rn(om, om), __dmul_rn(od, od));
+                if (v == v) atomicMin(&W.colmin[t], dkey(v));
+            }
+        }
+        __syncwarp();  // the queue is reused
+    }
+    // The unit's column results into the global ones.
+#pragma unroll
+    for (int t = static_cast<int>(l); t < MU_COLS; t += 32) {
+        if (PASS == 0) {
+            const unsigned v = W.colacc[t];
+            if (v) atomicMax(omax_bits + cb + t, v);
+        } else {
+            const unsigned long long v = W.colmin[t];
+            if (v != ~0ull) atomicMin(xmin_key + cb + t, v);
+        }
     }
 }
 
@@ -288,17 +402,14 @@ void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, 
 {
     cudaMemsetAsync(omax_bits, 0, sizeof(unsigned) * static_cast<size_t>(m_bound), st);
     cudaMemsetAsync(xmin_key, 0xff, sizeof(unsigned long long) * static_cast<size_t>(m_bound), st);
-    const long long T = (m_bound + MX_T - 1) / MX_T;
-    const long long tiles = T * (T + 1) / 2;
-    if (tiles > 0) {
-        matrix_pass_kernel<0><<<static_cast<unsigned>(tiles), MX_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, sigma,
-                                                                                 omax_bits, xmin_key);
+    const long long units = matrix_units(m_bound);
+    if (units > 0) {
+        const unsigned grid = static_cast<unsigned>((units + MU_WARPS - 1) / MU_WARPS);
+        matrix_pass_kernel<0><<<grid, MU_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, units, omax_bits, xmin_key);
         if (linear)
-            matrix_pass_kernel<2><<<static_cast<unsigned>(tiles), MX_THREADS, 0, st>>>(boxes_s, m_dev, m_bound,
-                                                                                     sigma, omax_bits, xmin_key);
+            matrix_pass_kernel<2><<<grid, MU_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, units, omax_bits, xmin_key);
         else
-            matrix_pass_kernel<1><<<static_cast<unsigned>(tiles), MX_THREADS, 0, st>>>(boxes_s, m_dev, m_bound,
-                                                                                     sigma, omax_bits, xmin_key);
+            matrix_pass_kernel<1><<<grid, MU_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, units, omax_bits, xmin_key);
     }
     matrix_decide_kernel<<<(m_bound + 255) / 256, 256, 0, st>>>(scores, perm, xmin_key, m_dev, m_bound, sigma,
                                                                 linear, decay_thr, fs, kept);

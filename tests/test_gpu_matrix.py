@@ -62,6 +62,30 @@ def test_clusters(n, sigma):
     _check(b, s, 0.1, sigma=sigma, score_thr=0.3)
 
 
+@pytest.mark.parametrize("decay", ["gaussian", "linear"])
+def test_overlap_filter_edges(decay):
+    """Pairs at the edges of the packed overlap filter: boxes that touch (a
+    zero difference), nested boxes, degenerate boxes, and groups scaled by
+    2^-45 and 2^45 (outside the filter's coordinate range, so those units
+    test every pair exactly), next to ordinary ones in the same units."""
+    rng = np.random.default_rng(7)
+    x = rng.integers(0, 40, 300).astype(np.float32)
+    y = rng.integers(0, 40, 300).astype(np.float32)
+    w = rng.integers(0, 6, 300).astype(np.float32)  # zero widths too
+    h = rng.integers(1, 6, 300).astype(np.float32)
+    b = np.stack([x, y, x + w, y + h], 1)  # integer grid: many touching edges
+    nest = np.array([[0, 0, 100, 100], [10, 10, 90, 90], [20, 20, 80, 80], [30, 30, 70, 70]], np.float32)
+    tiny = (b[:100] * np.float32(2.0 ** -45)).astype(np.float32)
+    huge = (b[100:200] * np.float32(2.0 ** 45)).astype(np.float32)
+    allb = np.concatenate([b, nest, tiny, huge]).astype(np.float32)
+    s = rng.uniform(0, 1, len(allb)).astype(np.float32)
+    for t in (0.01, 0.1):
+        if decay == "gaussian":
+            _check(allb, s, t)
+        else:
+            _check_linear(allb, s, t)
+
+
 def test_identical_boxes_and_empty():
     b = np.tile(np.array([[1, 1, 5, 5]], np.float32), (200, 1))
     s = np.linspace(1.0, 0.2, 200).astype(np.float32)

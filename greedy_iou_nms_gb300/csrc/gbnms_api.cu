@@ -289,8 +289,23 @@ nms_status run_impl(const float* boxes, const float* scores, int64_t n, const in
                                                                             : nullptr,
                         status, nullptr, L.NB, nullptr, haspred, nullptr, st);
             stamps.record(1, st);
-            launch_iou_mask(boxes_s, m_count, static_cast<int>(n), p, nullptr, L.ldw, nullptr, L.NB, nullptr,
-                            nullptr, 0u, haspred, st);
+            // With max_out, the mask of the leading 2*max_out boxes first;
+            // the rest only if that prefix held fewer than max_out kept boxes.
+            const int64_t kf = max_out > 0 ? (2 * static_cast<int64_t>(max_out) + MASK_TILE_W - 1) /
+                                                 MASK_TILE_W * MASK_TILE_W
+                                           : n;
+            if (kf >= n) {
+                launch_iou_mask(boxes_s, m_count, static_cast<int>(n), p, nullptr, L.ldw, nullptr, L.NB, nullptr,
+                                nullptr, 0u, haspred, st);
+            } else {
+                int* done = at<int>(workspace, L.done);
+                const int k = static_cast<int>(kf), nb = static_cast<int>(n);
+                launch_iou_mask(boxes_s, m_count, nb, p, nullptr, L.ldw, nullptr, L.NB, nullptr, nullptr, 0u,
+                                haspred, st, 0, k);
+                launch_fast_prefix(haspred, m_count, nb, k, max_out, done, st);
+                launch_iou_mask(boxes_s, m_count, nb, p, nullptr, L.ldw, nullptr, L.NB, nullptr, nullptr, 0u,
+                                haspred, st, k, nb, done);
+            }
             stamps.record(2, st);
             launch_fast_emit(haspred, m_count, static_cast<int>(n), perm, max_out, keep, counts, st);
             stamps.record(3, st);

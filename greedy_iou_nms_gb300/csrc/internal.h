@@ -103,6 +103,8 @@ void launch_graph_grid(uint32_t* edges, const unsigned* ecount, const uint64_t* 
 
 // Fast NMS output of one image: the boxes whose bit in haspred is clear, in
 // sorted order, mapped through perm, cut at max_out.
+void launch_fast_prefix(const uint64_t* haspred, const int* m_dev, int m_bound, int k, int max_out, int* done,
+                        cudaStream_t st);
 void launch_fast_emit(const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm, int max_out,
                       int64_t* keep, int64_t* counts, cudaStream_t st);
 

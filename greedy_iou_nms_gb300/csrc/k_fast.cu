@@ -60,7 +60,7 @@ bits_emit_kernel(const uint32_t* __restrict__ bits_in, int clear, const int* __r
     const int cap = max_out > 0 ? max_out : INT_MAX;
     int base = warp ? scratch[warp - 1] : 0;
     const uint32_t below = (1u << l) - 1u;
-    constexpr int OW = 8;  // words whose loads are in flight together
+    constexpr int OW = 2;  // words per step (a short loop: its code is fetched cold after an L2 flush)
     for (int wb = a0; wb < a1 && base < cap; wb += OW) {
         uint32_t bits[OW];
         int v[OW];
@@ -84,6 +84,43 @@ bits_emit_kernel(const uint32_t* __restrict__ bits_in, int clear, const int* __r
         }
     }
     if (threadIdx.x == 0) counts[0] = total < cap ? total : cap;
+}
+
+// With max_out, whether the leading k sorted boxes already hold max_out boxes
+// that Fast NMS keeps.  Their bits of the neighbour bitmap are final once the
+// mask of that prefix is done (every earlier box of a box in the prefix is in
+// the prefix), and the first max_out kept boxes are then all among them.
+// Sets *done (also when the prefix is every box) so that the mask of the rest
+// returns at once.
+__global__ void __launch_bounds__(FE_THREADS)
+fast_prefix_kernel(const uint32_t* __restrict__ haspred, const int* __restrict__ m_dev, int m_bound, int k,
+                   int max_out, int* __restrict__ done)
+{
+    pdl_wait();
+    pdl_release();
+    __shared__ int wsum[FE_THREADS / 32];
+    const int n = m_dev ? *m_dev : m_bound;
+    const int kk = min(n, k);
+    const int NW = (kk + 31) / 32;
+    int c = 0;
+    for (int w = threadIdx.x; w < NW; w += FE_THREADS) {
+        const uint32_t valid = (w == NW - 1 && (kk & 31)) ? (1u << (kk & 31)) - 1u : ~0u;
+        c += __popc(~haspred[w] & valid);
+    }
+    c = __reduce_add_sync(FULL, c);
+    if (lane_id() == 0) wsum[threadIdx.x >> 5] = c;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int t = __reduce_add_sync(FULL, wsum[threadIdx.x]);
+        if (threadIdx.x == 0) *done = (n <= k || t >= max_out) ? 1 : 0;
+    }
+}
+
+void launch_fast_prefix(const uint64_t* haspred, const int* m_dev, int m_bound, int k, int max_out, int* done,
+                        cudaStream_t st)
+{
+    launch_pdl(fast_prefix_kernel, dim3(1), dim3(FE_THREADS), 0, st, reinterpret_cast<const uint32_t*>(haspred),
+               m_dev, m_bound, k, max_out, done);
 }
 
 void launch_fast_emit(const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm, int max_out,

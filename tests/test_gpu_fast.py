@@ -88,6 +88,26 @@ def test_random_clusters(n, thr):
     _check_single(b, s, thr, score_thr=0.4)
 
 
+@pytest.mark.parametrize("max_out", [1, 64, 100, 1000])
+def test_max_out_prefix(max_out):
+    """max_out runs the mask of the leading 2*max_out boxes first: a prefix
+    that holds max_out kept boxes (spread boxes), one that does not (a stack
+    of overlapping boxes ahead of the spread ones), and a pre-filter that
+    leaves fewer boxes than the prefix."""
+    rng = np.random.default_rng(max_out)
+    n = 6000
+    c = rng.uniform(0, 3000, (n, 2))
+    wh = rng.uniform(5, 20, (n, 2))
+    spread = np.concatenate([c - wh / 2, c + wh / 2], 1).astype(np.float32)
+    s = rng.uniform(0, 0.9, n).astype(np.float32)
+    _check_single(spread, s, 0.5, max_out=max_out)
+    stack = np.tile(np.array([[100, 100, 140, 140]], np.float32), (3000, 1)) + rng.uniform(0, 1, (3000, 1))
+    b = np.concatenate([stack.astype(np.float32), spread])
+    s2 = np.concatenate([rng.uniform(0.95, 1.0, 3000), s]).astype(np.float32)
+    _check_single(b, s2, 0.5, max_out=max_out)
+    _check_single(b, s2, 0.5, max_out=max_out, score_thr=0.955)
+
+
 def test_empty_and_ties():
     assert len(_fast(np.zeros((0, 4), np.float32), np.zeros(0, np.float32), 0.5)) == 0
     b = np.tile(np.array([[0, 0, 10, 10]], np.float32), (70, 1))

@@ -86,7 +86,7 @@ SingleLayout single_layout(int64_t n)
 }
 
 struct MatrixLayout {
-    size_t status, m_count, cand, perm, boxes_s, keys, omax, xmin, fs, kept, total;
+    size_t status, m_count, cand, perm, boxes_s, keys, omax, xmin, fs, kept, done, total;
 };
 
 MatrixLayout matrix_layout(int64_t n)
@@ -104,6 +104,7 @@ MatrixLayout matrix_layout(int64_t n)
     m.xmin = L.add(8 * N);
     m.fs = L.add(4 * N);
     m.kept = L.add(4 * ((N + 31) / 32 + 8));
+    m.done = L.add(4);
     m.total = L.total;
     return m;
 }
@@ -470,7 +471,8 @@ extern "C" nms_status nms_matrix_run(const float* boxes, const float* scores, in
     launch_matrix(boxes_s, scores, perm, m_count, static_cast<int>(n), sigma, decay == NMS_DECAY_LINEAR ? 1 : 0,
                   decay_thr, max_out,
                   at<unsigned>(workspace, L.omax), at<unsigned long long>(workspace, L.xmin),
-                  at<float>(workspace, L.fs), at<uint32_t>(workspace, L.kept), keep, keep_scores, count, st);
+                  at<float>(workspace, L.fs), at<uint32_t>(workspace, L.kept), at<int>(workspace, L.done), keep,
+                  keep_scores, count, st);
     return cuda_status();
 }
 

@@ -103,6 +103,8 @@ void launch_graph_grid(uint32_t* edges, const unsigned* ecount, const uint64_t* 
 
 // Fast NMS output of one image: the boxes whose bit in haspred is clear, in
 // sorted order, mapped through perm, cut at max_out.
+void launch_kept_prefix(const uint32_t* kept, const int* m_dev, int m_bound, int k, int max_out, int* done,
+                        cudaStream_t st);
 void launch_fast_prefix(const uint64_t* haspred, const int* m_dev, int m_bound, int k, int max_out, int* done,
                         cudaStream_t st);
 void launch_fast_emit(const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm, int max_out,
@@ -119,8 +121,8 @@ void launch_bits_emit(const uint32_t* bits, const int* m_dev, int m_bound, const
 // ceil(n/32) words of scratch.
 void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, const int* m_dev, int m_bound,
                    float sigma, int linear, float decay_thr, int max_out, unsigned* omax_bits,
-                   unsigned long long* xmin_key, float* fs, uint32_t* kept, int64_t* keep, float* keep_scores,
-                   int64_t* count, cudaStream_t st);
+                   unsigned long long* xmin_key, float* fs, uint32_t* kept, int* done, int64_t* keep,
+                   float* keep_scores, int64_t* count, cudaStream_t st);
 
 // Front end (k_decode.cu): YOLO-shaped predictions to count-header buffers.
 int decode_blocks(int anchors);

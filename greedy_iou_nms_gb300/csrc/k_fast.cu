@@ -86,15 +86,16 @@ bits_emit_kernel(const uint32_t* __restrict__ bits_in, int clear, const int* __r
     if (threadIdx.x == 0) counts[0] = total < cap ? total : cap;
 }
 
-// With max_out, whether the leading k sorted boxes already hold max_out boxes
-// that Fast NMS keeps.  Their bits of the neighbour bitmap are final once the
-// mask of that prefix is done (every earlier box of a box in the prefix is in
-// the prefix), and the first max_out kept boxes are then all among them.
-// Sets *done (also when the prefix is every box) so that the mask of the rest
-// returns at once.
+// With max_out, whether the leading k sorted boxes already hold max_out kept
+// boxes (bits: 32-box words whose set bits, or clear bits when `clear`, are
+// the kept ones).  For Fast NMS (the clear bits of the neighbour bitmap) and
+// Matrix NMS (the kept bitmap) a box's decision depends only on the boxes
+// before it, so once the prefix is done its decisions are final and the
+// first max_out kept boxes are all among them.  Sets *done (also when the
+// prefix is every box) so that the later stage returns at once.
 __global__ void __launch_bounds__(FE_THREADS)
-fast_prefix_kernel(const uint32_t* __restrict__ haspred, const int* __restrict__ m_dev, int m_bound, int k,
-                   int max_out, int* __restrict__ done)
+prefix_kernel(const uint32_t* __restrict__ bits, int clear, const int* __restrict__ m_dev, int m_bound, int k,
+              int max_out, int* __restrict__ done)
 {
     pdl_wait();
     pdl_release();
@@ -105,7 +106,7 @@ fast_prefix_kernel(const uint32_t* __restrict__ haspred, const int* __restrict__
     int c = 0;
     for (int w = threadIdx.x; w < NW; w += FE_THREADS) {
         const uint32_t valid = (w == NW - 1 && (kk & 31)) ? (1u << (kk & 31)) - 1u : ~0u;
-        c += __popc(~haspred[w] & valid);
+        c += __popc((clear ? ~bits[w] : bits[w]) & valid);
     }
     c = __reduce_add_sync(FULL, c);
     if (lane_id() == 0) wsum[threadIdx.x >> 5] = c;
@@ -119,8 +120,14 @@ fast_prefix_kernel(const uint32_t* __restrict__ haspred, const int* __restrict__
 void launch_fast_prefix(const uint64_t* haspred, const int* m_dev, int m_bound, int k, int max_out, int* done,
                         cudaStream_t st)
 {
-    launch_pdl(fast_prefix_kernel, dim3(1), dim3(FE_THREADS), 0, st, reinterpret_cast<const uint32_t*>(haspred),
+    launch_pdl(prefix_kernel, dim3(1), dim3(FE_THREADS), 0, st, reinterpret_cast<const uint32_t*>(haspred), 1,
                m_dev, m_bound, k, max_out, done);
+}
+
+void launch_kept_prefix(const uint32_t* kept, const int* m_dev, int m_bound, int k, int max_out, int* done,
+                        cudaStream_t st)
+{
+    launch_pdl(prefix_kernel, dim3(1), dim3(FE_THREADS), 0, st, kept, 0, m_dev, m_bound, k, max_out, done);
 }
 
 void launch_fast_emit(const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm, int max_out,

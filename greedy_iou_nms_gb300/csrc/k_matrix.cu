@@ -38,6 +38,8 @@
 // takes the binary64 quotient itself (a father with O_max = 1 gives x/0 or
 // 0/0, which the minimum ignores), and the decide multiplies in binary64.
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -148,22 +150,13 @@ struct MxWarp {
     float om[MU_ROWS];                   // O_max of the rows (passes 1, 2)
 };
 
+// One unit (64 rows from rbase, 128 columns from cb) of a pass, by one warp.
 // PASS 0: O_max; 1: smallest Gaussian numerator; 2: smallest linear decay.
 template <int PASS>
-__global__ void __launch_bounds__(MU_THREADS, 8)
-matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_dev, int m_bound,
-                   long long units, unsigned* __restrict__ omax_bits, unsigned long long* __restrict__ xmin_key)
+__device__ __forceinline__ void matrix_unit(MxWarp& W, const float4* __restrict__ boxes_s, int n, int cb, int rbase,
+                                            unsigned* __restrict__ omax_bits,
+                                            unsigned long long* __restrict__ xmin_key)
 {
-    __shared__ __align__(16) MxWarp sw[MU_WARPS];
-    const int wp = threadIdx.x >> 5;
-    const long long u = static_cast<long long>(blockIdx.x) * MU_WARPS + wp;
-    if (u >= units) return;  // warp-uniform
-    const int n = m_dev ? *m_dev : m_bound;
-    int a, c;
-    mu_coords(u, a, c);
-    const int cb = c * MU_COLS, rbase = a * MU_ROWS;
-    if (cb >= n || rbase >= n) return;
-    MxWarp& W = sw[wp];
     const unsigned l = lane_id();
     bool ok = true;
 #pragma unroll
@@ -348,16 +341,41 @@ matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m
     }
 }
 
+// A pass over the units [u_begin, u_end), one warp per unit; the grid strides
+// over them when it is smaller.  A later max_out stage (done given) returns at
+// once when the earlier stage has already found max_out kept boxes.
+template <int PASS>
+__global__ void __launch_bounds__(MU_THREADS, 8)
+matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_dev, int m_bound,
+                   long long u_begin, long long u_end, const int* __restrict__ done,
+                   unsigned* __restrict__ omax_bits, unsigned long long* __restrict__ xmin_key)
+{
+    __shared__ __align__(16) MxWarp sw[MU_WARPS];
+    if (done && *done) return;
+    const int wp = threadIdx.x >> 5;
+    const int n = m_dev ? *m_dev : m_bound;
+    const long long stride = static_cast<long long>(gridDim.x) * MU_WARPS;
+    for (long long u = u_begin + static_cast<long long>(blockIdx.x) * MU_WARPS + wp; u < u_end; u += stride) {
+        int a, c;
+        mu_coords(u, a, c);
+        const int cb = c * MU_COLS, rbase = a * MU_ROWS;
+        if (cb >= n || rbase >= n) continue;  // beyond the device-side count (warp-uniform)
+        __syncwarp();  // the previous unit's use of the warp's shared memory is over
+        matrix_unit<PASS>(sw[wp], boxes_s, n, cb, rbase, omax_bits, xmin_key);
+    }
+}
+
 // One thread per sorted box: its final score and whether it stays; lane l of
 // a warp decides box 32w+l and the warp writes word w of the kept bitmap.
 __global__ void __launch_bounds__(256)
 matrix_decide_kernel(const float* __restrict__ scores, const int* __restrict__ perm,
                      const unsigned long long* __restrict__ xmin_key, const int* __restrict__ m_dev,
                      int m_bound, float sigma, int linear, float decay_thr, float* __restrict__ fs_out,
-                     uint32_t* __restrict__ kept)
+                     uint32_t* __restrict__ kept, int lo, const int* __restrict__ done)
 {
+    if (done && *done) return;  // an earlier max_out stage found enough kept boxes
     const int n = m_dev ? *m_dev : m_bound;
-    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    const int j = lo + blockIdx.x * blockDim.x + threadIdx.x;  // lo: a multiple of 32
     if (j - static_cast<int>(lane_id()) >= n) return;  // whole warp past the end
     bool keep_j = false;
     if (j < n && linear) {
@@ -397,22 +415,52 @@ matrix_decide_kernel(const float* __restrict__ scores, const int* __restrict__ p
 
 void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, const int* m_dev, int m_bound,
                    float sigma, int linear, float decay_thr, int max_out, unsigned* omax_bits,
-                   unsigned long long* xmin_key, float* fs, uint32_t* kept, int64_t* keep, float* keep_scores,
-                   int64_t* count, cudaStream_t st)
+                   unsigned long long* xmin_key, float* fs, uint32_t* kept, int* done, int64_t* keep,
+                   float* keep_scores, int64_t* count, cudaStream_t st)
 {
     cudaMemsetAsync(omax_bits, 0, sizeof(unsigned) * static_cast<size_t>(m_bound), st);
     cudaMemsetAsync(xmin_key, 0xff, sizeof(unsigned long long) * static_cast<size_t>(m_bound), st);
-    const long long units = matrix_units(m_bound);
-    if (units > 0) {
-        const unsigned grid = static_cast<unsigned>((units + MU_WARPS - 1) / MU_WARPS);
-        matrix_pass_kernel<0><<<grid, MU_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, units, omax_bits, xmin_key);
-        if (linear)
-            matrix_pass_kernel<2><<<grid, MU_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, units, omax_bits, xmin_key);
-        else
-            matrix_pass_kernel<1><<<grid, MU_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, units, omax_bits, xmin_key);
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+    // Boxes [lo, hi): the passes over the units of columns [lo, hi) (all rows
+    // above them) and the decisions of boxes [lo, hi).  A stage given `done`
+    // strides over its units with one resident wave, so that finding the flag
+    // set costs a few CTAs per SM.
+    auto stage = [&](int lo, int hi, const int* dn) {
+        const long long u0 = matrix_units(lo), u1 = matrix_units(hi);
+        if (u1 > u0) {
+            long long g = (u1 - u0 + MU_WARPS - 1) / MU_WARPS;
+            if (dn) g = std::min(g, static_cast<long long>(sms) * 8);
+            const unsigned grid = static_cast<unsigned>(g);
+            matrix_pass_kernel<0><<<grid, MU_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, u0, u1, dn, omax_bits,
+                                                                xmin_key);
+            if (linear)
+                matrix_pass_kernel<2><<<grid, MU_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, u0, u1, dn, omax_bits,
+                                                                    xmin_key);
+            else
+                matrix_pass_kernel<1><<<grid, MU_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, u0, u1, dn, omax_bits,
+                                                                    xmin_key);
+        }
+        if (hi > lo)
+            matrix_decide_kernel<<<(hi - lo + 255) / 256, 256, 0, st>>>(scores, perm, xmin_key, m_dev, m_bound,
+                                                                        sigma, linear, decay_thr, fs, kept, lo, dn);
+    };
+    // With max_out, a box's decay depends only on the boxes before it, so the
+    // first max_out kept boxes depend only on a prefix of the score order:
+    // the leading 2*max_out boxes first, the rest only if they held fewer
+    // than max_out kept boxes.
+    const long long k = max_out > 0 ? (2LL * max_out + MU_COLS - 1) / MU_COLS * MU_COLS : m_bound;
+    if (k >= m_bound) {
+        stage(0, m_bound, nullptr);
+    } else {
+        // The rest's decisions may be skipped: their kept words must read 0.
+        cudaMemsetAsync(kept, 0, sizeof(uint32_t) * static_cast<size_t>((m_bound + 31) / 32), st);
+        stage(0, static_cast<int>(k), nullptr);
+        launch_kept_prefix(kept, m_dev, m_bound, static_cast<int>(k), max_out, done, st);
+        stage(static_cast<int>(k), m_bound, done);
     }
-    matrix_decide_kernel<<<(m_bound + 255) / 256, 256, 0, st>>>(scores, perm, xmin_key, m_dev, m_bound, sigma,
-                                                                linear, decay_thr, fs, kept);
     launch_bits_emit(kept, m_dev, m_bound, perm, fs, max_out, keep, keep_scores, count, st);
 }
 

@@ -86,6 +86,28 @@ def test_overlap_filter_edges(decay):
             _check_linear(allb, s, t)
 
 
+@pytest.mark.parametrize("max_out", [1, 64, 100, 1000])
+@pytest.mark.parametrize("decay", ["gaussian", "linear"])
+def test_max_out_prefix(max_out, decay):
+    """max_out decides the leading 2*max_out boxes first: a prefix that holds
+    max_out kept boxes (spread boxes), one that does not (a stack of
+    overlapping boxes ahead of the spread ones, decayed below the threshold),
+    and a pre-filter that leaves fewer boxes than the prefix."""
+    rng = np.random.default_rng(max_out + 17)
+    n = 5000
+    c = rng.uniform(0, 3000, (n, 2))
+    wh = rng.uniform(5, 20, (n, 2))
+    spread = np.concatenate([c - wh / 2, c + wh / 2], 1).astype(np.float32)
+    s = rng.uniform(0.3, 0.9, n).astype(np.float32)
+    stack = np.tile(np.array([[100, 100, 140, 140]], np.float32), (2500, 1)) + rng.uniform(0, 1, (2500, 1))
+    b = np.concatenate([stack.astype(np.float32), spread])
+    s2 = np.concatenate([rng.uniform(0.95, 1.0, 2500), s]).astype(np.float32)
+    chk = _check if decay == "gaussian" else _check_linear
+    chk(spread, s, 0.2, max_out=max_out)
+    chk(b, s2, 0.2, max_out=max_out)
+    chk(b, s2, 0.2, max_out=max_out, score_thr=0.955)
+
+
 def test_identical_boxes_and_empty():
     b = np.tile(np.array([[1, 1, 5, 5]], np.float32), (200, 1))
     s = np.linspace(1.0, 0.2, 200).astype(np.float32)

@@ -390,6 +390,86 @@ __device__ __forceinline__ void bitonic_sort(uint64_t* s, int np)
     }
 }
 
+// Ascending bitonic sort of R * MG_THREADS unique keys held in registers:
+// key e is v[e / MG_THREADS] of thread e % MG_THREADS.  Partners fewer than 32
+// apart are in the same warp and swap by shuffles, partners MG_THREADS or more
+// apart are in the same thread, and only the steps in between go through
+// shared memory s (R * MG_THREADS keys), with two CTA barriers each.
+template <int R>
+__device__ __forceinline__ void bitonic_sort_regs(uint64_t (&v)[R], uint64_t* s)
+{
+    const int t = threadIdx.x;
+    constexpr int NP = R * MG_THREADS;
+    for (int k = 2; k <= NP; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j >= MG_THREADS) {
+                const int jr = j / MG_THREADS;  // the partner is register r ^ jr of this thread
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int q = r + 1; q < R; ++q)
+                        if (q == (r ^ jr)) {
+                            const uint64_t x = v[r], y = v[q];
+                            const bool asc = ((r * MG_THREADS + t) & k) == 0;
+                            v[r] = asc ? min(x, y) : max(x, y);
+                            v[q] = asc ? max(x, y) : min(x, y);
+                        }
+            } else if (j >= 32) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) s[r * MG_THREADS + t] = v[r];
+                __syncthreads();
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int e = r * MG_THREADS + t;
+                    const uint64_t y = s[e ^ j];
+                    const bool keep_min = ((e & j) == 0) == ((e & k) == 0);
+                    v[r] = keep_min ? min(v[r], y) : max(v[r], y);
+                }
+                __syncthreads();
+            } else {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const int e = r * MG_THREADS + t;
+                    const uint64_t y = __shfl_xor_sync(FULL, v[r], j);
+                    const bool keep_min = ((e & j) == 0) == ((e & k) == 0);
+                    v[r] = keep_min ? min(v[r], y) : max(v[r], y);
+                }
+            }
+        }
+    }
+}
+
+// Kept keys of the image's segments [s0, s0 + C) into registers (key e to
+// v[e / MG_THREADS] of thread e % MG_THREADS, ~0 past tot), sorted, and the
+// first cap written out.
+template <int R>
+__device__ __forceinline__ void merge_regs(const int* __restrict__ seg_off, const uint64_t* __restrict__ kept_key,
+                                           const int* seg_pre, int s0, int C, int tot, int cap,
+                                           int64_t* __restrict__ keep, int64_t out0, uint64_t* s)
+{
+    uint64_t v[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int e = r * MG_THREADS + static_cast<int>(threadIdx.x);
+        uint64_t k = ~0ull;
+        if (e < tot) {
+            int lo = 0, hi = C;  // last segment with prefix <= e
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (seg_pre[mid] <= e) lo = mid; else hi = mid;
+            }
+            k = kept_key[seg_off[s0 + lo] + (e - seg_pre[lo])];
+        }
+        v[r] = k;
+    }
+    bitonic_sort_regs<R>(v, s);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int e = r * MG_THREADS + static_cast<int>(threadIdx.x);
+        if (e < cap) keep[out0 + e] = static_cast<int64_t>(v[r] & 0xffffffffu);
+    }
+}
+
 __global__ void __launch_bounds__(MG_THREADS)
 merge_kernel(const int* __restrict__ seg_off, const int* __restrict__ kept_cnt,
              const uint64_t* __restrict__ kept_key, int C, const int64_t* __restrict__ off,
@@ -441,24 +521,9 @@ merge_kernel(const int* __restrict__ seg_off, const int* __restrict__ kept_cnt,
         __syncthreads();
         if (tot <= MG_CHUNK) {
             const int cap = max_out > 0 ? min(max_out, tot) : tot;
-            int np = 1;
-            while (np < tot) np <<= 1;
-            for (int e = threadIdx.x; e < np; e += blockDim.x) {
-                uint64_t k = ~0ull;
-                if (e < tot) {
-                    int lo = 0, hi = C;  // last segment with prefix <= e
-                    while (hi - lo > 1) {
-                        const int mid = (lo + hi) >> 1;
-                        if (seg_pre[mid] <= e) lo = mid; else hi = mid;
-                    }
-                    k = kept_key[seg_off[s0 + lo] + (e - seg_pre[lo])];
-                }
-                ck[e] = k;
-            }
-            __syncthreads();
-            bitonic_sort(ck, np);
-            for (int r = threadIdx.x; r < cap; r += blockDim.x)
-                keep[out0 + r] = static_cast<int64_t>(ck[r] & 0xffffffffu);
+            if (tot <= MG_THREADS) merge_regs<1>(seg_off, kept_key, seg_pre, s0, C, tot, cap, keep, out0, ck);
+            else if (tot <= 2 * MG_THREADS) merge_regs<2>(seg_off, kept_key, seg_pre, s0, C, tot, cap, keep, out0, ck);
+            else merge_regs<4>(seg_off, kept_key, seg_pre, s0, C, tot, cap, keep, out0, ck);
             if (threadIdx.x == 0) counts[b] = cap;
             return;
         }

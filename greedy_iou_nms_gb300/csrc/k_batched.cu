@@ -187,6 +187,9 @@ seg_small_kernel(const float4* __restrict__ boxes, const float* __restrict__ sco
     const bool ha = static_cast<int>(l) < m, hb = static_cast<int>(l) + 32 < m;
     const int xa = ha ? cand[lo + l] : 0;
     const int xb = hb ? cand[lo + 32 + l] : 0;
+    // The boxes are loaded with the scores (one round of dependent loads).
+    const float4 bxa = ha ? boxes[xa] : make_float4(0, 0, 0, 0);
+    const float4 bxb = hb ? boxes[xb] : make_float4(0, 0, 0, 0);
     const uint64_t ka = ha ? order_key(scores[xa], xa) : ~0ull;
     const uint64_t kb = hb ? order_key(scores[xb], xb) : ~0ull;
     int ra = 0, rb = 0;
@@ -195,8 +198,8 @@ seg_small_kernel(const float4* __restrict__ boxes, const float* __restrict__ sco
         ra += ke < ka;
         rb += ke < kb;
     }
-    if (ha) { sbox[wp][ra] = boxes[xa]; skey[wp][ra] = ka; }
-    if (hb) { sbox[wp][rb] = boxes[xb]; skey[wp][rb] = kb; }
+    if (ha) { sbox[wp][ra] = bxa; skey[wp][ra] = ka; }
+    if (hb) { sbox[wp][rb] = bxb; skey[wp][rb] = kb; }
     __syncwarp();
     if (ha) sarea[wp][l] = box_area(sbox[wp][l]);
     if (hb) sarea[wp][l + 32] = box_area(sbox[wp][l + 32]);
@@ -208,13 +211,20 @@ seg_small_kernel(const float4* __restrict__ boxes, const float* __restrict__ sco
     // Column view of the segment's mask: bit r of colA is set iff sorted box r
     // suppresses sorted box l (r < l); colB likewise for box l+32.
     uint64_t colA = 0, colB = 0;
-    for (int r = 0; r < m; ++r) {
-        const float4 rbx = sbox[wp][r];
-        const float rar = sarea[wp][r];
-        const bool va = ha && static_cast<int>(l) > r && suppress_exact(rbx, rar, ca, aa, thr);
-        const bool vb = hb && static_cast<int>(l) + 32 > r && suppress_exact(rbx, rar, cb, ab, thr);
-        colA |= static_cast<uint64_t>(va) << r;
-        colB |= static_cast<uint64_t>(vb) << r;
+    if (m <= 32) {  // most segments: one column per lane
+        for (int r = 0; r < m; ++r) {
+            const bool va = ha && static_cast<int>(l) > r && suppress_exact(sbox[wp][r], sarea[wp][r], ca, aa, thr);
+            colA |= static_cast<uint64_t>(va) << r;
+        }
+    } else {
+        for (int r = 0; r < m; ++r) {
+            const float4 rbx = sbox[wp][r];
+            const float rar = sarea[wp][r];
+            const bool va = ha && static_cast<int>(l) > r && suppress_exact(rbx, rar, ca, aa, thr);
+            const bool vb = hb && static_cast<int>(l) + 32 > r && suppress_exact(rbx, rar, cb, ab, thr);
+            colA |= static_cast<uint64_t>(va) << r;
+            colB |= static_cast<uint64_t>(vb) << r;
+        }
     }
     const uint64_t valid = m >= 64 ? ~0ull : ((1ull << m) - 1ull);
     // Greedy: resolve the column view; Fast NMS: keep the boxes no earlier

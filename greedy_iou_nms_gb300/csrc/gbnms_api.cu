@@ -34,7 +34,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 // Region offsets inside the caller's workspace.
 struct Layout {
-    size_t off[16] = {};
+    size_t off[32] = {};
     size_t total = 0;
     int k = 0;
     size_t add(size_t bytes)
@@ -86,7 +86,8 @@ SingleLayout single_layout(int64_t n)
 }
 
 struct MatrixLayout {
-    size_t status, m_count, cand, perm, boxes_s, keys, omax, xmin, fs, kept, done, total;
+    size_t status, m_count, cand, perm, boxes_s, keys, omax, xmin, fs, kept, done, list_count, colhi, list_ij,
+        list_o, total;
 };
 
 MatrixLayout matrix_layout(int64_t n)
@@ -105,6 +106,10 @@ MatrixLayout matrix_layout(int64_t n)
     m.fs = L.add(4 * N);
     m.kept = L.add(4 * ((N + 31) / 32 + 8));
     m.done = L.add(4);
+    m.list_count = L.add(8);
+    m.colhi = L.add(4 * N);
+    m.list_ij = L.add(8 * static_cast<size_t>(matrix_list_cap(n)));
+    m.list_o = L.add(4 * static_cast<size_t>(matrix_list_cap(n)));
     m.total = L.total;
     return m;
 }
@@ -471,7 +476,10 @@ extern "C" nms_status nms_matrix_run(const float* boxes, const float* scores, in
     launch_matrix(boxes_s, scores, perm, m_count, static_cast<int>(n), sigma, decay == NMS_DECAY_LINEAR ? 1 : 0,
                   decay_thr, max_out,
                   at<unsigned>(workspace, L.omax), at<unsigned long long>(workspace, L.xmin),
-                  at<float>(workspace, L.fs), at<uint32_t>(workspace, L.kept), at<int>(workspace, L.done), keep,
+                  at<float>(workspace, L.fs), at<uint32_t>(workspace, L.kept), at<int>(workspace, L.done),
+                  at<unsigned long long>(workspace, L.list_ij), at<float>(workspace, L.list_o),
+                  at<unsigned long long>(workspace, L.list_count), matrix_list_cap(n),
+                  at<unsigned>(workspace, L.colhi), keep,
                   keep_scores, count, st);
     return cuda_status();
 }

@@ -121,8 +121,11 @@ void launch_bits_emit(const uint32_t* bits, const int* m_dev, int m_bound, const
 // ceil(n/32) words of scratch.
 void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, const int* m_dev, int m_bound,
                    float sigma, int linear, float decay_thr, int max_out, unsigned* omax_bits,
-                   unsigned long long* xmin_key, float* fs, uint32_t* kept, int* done, int64_t* keep,
+                   unsigned long long* xmin_key, float* fs, uint32_t* kept, int* done, unsigned long long* list_ij,
+                   float* list_o, unsigned long long* list_count, unsigned list_cap, unsigned* colhi, int64_t* keep,
                    float* keep_scores, int64_t* count, cudaStream_t st);
+// Entries of the Matrix NMS list of overlapping pairs for n boxes.
+unsigned matrix_list_cap(int64_t n);
 
 // Front end (k_decode.cu): YOLO-shaped predictions to count-header buffers.
 int decode_blocks(int anchors);

@@ -89,6 +89,17 @@ __device__ __forceinline__ void mu_coords(long long k, int& a, int& c)
     a = static_cast<int>(k - r * cc * (cc + 1) / 2);
 }
 
+constexpr int MX_LIST_MIN_N = 16384;  // boxes from which pass B takes the list
+
+// About 96 overlapping pairs per box, plus a floor: beyond that pass B walks
+// the units again.
+unsigned matrix_list_cap(int64_t n)
+{
+    const unsigned long long all = n > 1 ? static_cast<unsigned long long>(n) * (n - 1) / 2 : 1ull;
+    const unsigned long long c = std::min(all, 96ull * static_cast<unsigned long long>(n) + (1ull << 20));
+    return static_cast<unsigned>(std::min(c, 1ull << 31));
+}
+
 long long matrix_units(long long n)
 {
     const long long T = (n + MU_COLS - 1) / MU_COLS;
@@ -150,12 +161,58 @@ struct MxWarp {
     float om[MU_ROWS];                   // O_max of the rows (passes 1, 2)
 };
 
+// The binary32 bounds [lo, ub] of a pair's term in pass B (PASS 1: the
+// numerator om^2 - o^2; PASS 2: the decay (1 - o) / (1 - om)); false when the
+// pair contributes nothing (no overlap, or om = 1 in the linear decay).
+template <int PASS>
+__device__ __forceinline__ bool mx_bound(float o, float om, float& lo, float& ub)
+{
+    if (!(o > 0.0f)) return false;
+    if (PASS == 2) {
+        // binary32 quotient within a 2^-20 margin (three roundings of 2^-24)
+        if (!(om < 1.0f)) return false;
+        const float q = __fdiv_rn(__fsub_rn(1.0f, o), __fsub_rn(1.0f, om));
+        const float eb = __fmul_rn(q, 0x1p-20f);
+        lo = q - eb;
+        ub = q + eb;
+    } else {
+        // within 2^-22 of om^2 + o^2 (three roundings) plus an absolute term
+        // for tiny values
+        const float aa = __fmul_rn(om, om), bb = __fmul_rn(o, o);
+        const float eb = __fmul_rn(0x1p-22f, __fadd_rn(aa, bb)) + 0x1p-140f;
+        const float xx = __fsub_rn(aa, bb);
+        lo = xx - eb;
+        ub = xx + eb;
+    }
+    return true;
+}
+
+// The pair's term in binary64: products exact and one rounding (Gaussian
+// numerator), or the correctly rounded quotient (linear decay).
+template <int PASS>
+__device__ __forceinline__ double mx_value(float o, float om)
+{
+    const double od = static_cast<double>(o), omd = static_cast<double>(om);
+    return PASS == 2 ? __ddiv_rn(__dsub_rn(1.0, od), __dsub_rn(1.0, omd))
+                     : __dsub_rn(__dmul_rn(omd, omd), __dmul_rn(od, od));
+}
+
+// The list of overlapping pairs that pass A records for pass B: (i << 32 | j)
+// and their IoU, count may grow past cap (the list is then incomplete and
+// pass B walks the units again).
+struct MxList {
+    unsigned long long* ij;
+    float* o;
+    unsigned long long* count;  // 64-bit: the pairs of the largest inputs exceed 2^32
+    unsigned cap;
+};
+
 // One unit (64 rows from rbase, 128 columns from cb) of a pass, by one warp.
 // PASS 0: O_max; 1: smallest Gaussian numerator; 2: smallest linear decay.
 template <int PASS>
 __device__ __forceinline__ void matrix_unit(MxWarp& W, const float4* __restrict__ boxes_s, int n, int cb, int rbase,
                                             unsigned* __restrict__ omax_bits,
-                                            unsigned long long* __restrict__ xmin_key)
+                                            unsigned long long* __restrict__ xmin_key, const MxList& L)
 {
     const unsigned l = lane_id();
     bool ok = true;
@@ -269,44 +326,41 @@ __device__ __forceinline__ void matrix_unit(MxWarp& W, const float4* __restrict_
                 }
         __syncwarp();
         const int m = min(MU_Q, total - base);
-        for (int e = static_cast<int>(l); e < m; e += 32) {
-            const uint32_t qe = W.qe[e];
-            const int rl = static_cast<int>(qe >> 8), t = static_cast<int>(qe & 255u);
-            const float4 r = W.rows[rl];
-            const float4 cbx = make_float4(-W.nx1[t], W.y1[t], W.x2[t], -W.ny2[t]);
-            // Overlap (IoU > 0) exactly as the canonical formula has it.
-            const float ww = __fsub_rn(fminf(r.z, cbx.z), fmaxf(r.x, cbx.x));
-            const float hh = __fsub_rn(fminf(r.w, cbx.w), fmaxf(r.y, cbx.y));
+        for (int e0 = 0; e0 < m; e0 += 32) {  // warp-uniform steps (the list reserves per warp)
+            const int e = e0 + static_cast<int>(l);
             float o = 0.0f;
-            if (ww > 0.0f && hh > 0.0f) {
-                o = iou_exact(r, box_area(r), cbx, box_area(cbx));
-                if (!(o > 0.0f)) o = 0.0f;
+            int rl = 0, t = 0;
+            if (e < m) {
+                const uint32_t qe = W.qe[e];
+                rl = static_cast<int>(qe >> 8);
+                t = static_cast<int>(qe & 255u);
+                const float4 r = W.rows[rl];
+                const float4 cbx = make_float4(-W.nx1[t], W.y1[t], W.x2[t], -W.ny2[t]);
+                // Overlap (IoU > 0) exactly as the canonical formula has it.
+                const float ww = __fsub_rn(fminf(r.z, cbx.z), fmaxf(r.x, cbx.x));
+                const float hh = __fsub_rn(fminf(r.w, cbx.w), fmaxf(r.y, cbx.y));
+                if (ww > 0.0f && hh > 0.0f) {
+                    o = iou_exact(r, box_area(r), cbx, box_area(cbx));
+                    if (!(o > 0.0f)) o = 0.0f;
+                }
             }
             if (PASS == 0) {
                 if (o > 0.0f) atomicMax(&W.colacc[t], __float_as_uint(o));
-            } else {
-                const float om = W.om[rl];
-                float lo = INFINITY;
-                if (PASS == 2) {
-                    // The decay (1 - o) / (1 - om) in binary32 within a 2^-20
-                    // margin (three roundings of 2^-24 each); om = 1 gives
-                    // nothing.
-                    if (o > 0.0f && om < 1.0f) {
-                        const float q = __fdiv_rn(__fsub_rn(1.0f, o), __fsub_rn(1.0f, om));
-                        const float eb = __fmul_rn(q, 0x1p-20f);
-                        lo = q - eb;
-                        atomicMin(&W.colacc[t], fkey(q + eb));
+                if (L.ij) {
+                    const unsigned b = __ballot_sync(FULL, o > 0.0f);
+                    unsigned long long base = 0;
+                    if (l == 0 && b) base = atomicAdd(L.count, static_cast<unsigned long long>(__popc(b)));
+                    base = __shfl_sync(FULL, base, 0) + static_cast<unsigned>(__popc(b & ((1u << l) - 1u)));
+                    if (o > 0.0f && base < L.cap) {
+                        L.ij[base] = (static_cast<unsigned long long>(rbase + rl) << 32) | static_cast<unsigned>(cb + t);
+                        L.o[base] = o;
                     }
-                } else if (o > 0.0f) {
-                    // The numerator om^2 - o^2 in binary32, within a margin of
-                    // 2^-22 of om^2 + o^2 (three roundings) plus an absolute
-                    // term for tiny values.
-                    const float aa = __fmul_rn(om, om), bb = __fmul_rn(o, o);
-                    const float eb = __fmul_rn(0x1p-22f, __fadd_rn(aa, bb)) + 0x1p-140f;
-                    const float xx = __fsub_rn(aa, bb);
-                    lo = xx - eb;
-                    atomicMin(&W.colacc[t], fkey(xx + eb));
                 }
+            } else if (e < m) {
+                const float om = W.om[rl];
+                float lo = INFINITY, ub;
+                if (mx_bound<PASS>(o, om, lo, ub)) atomicMin(&W.colacc[t], fkey(ub));
+                else lo = INFINITY;
                 W.qo[e] = o;
                 W.qlo[e] = lo;
             }
@@ -320,9 +374,7 @@ __device__ __forceinline__ void matrix_unit(MxWarp& W, const float4* __restrict_
                 const float lo = W.qlo[e];
                 const int t = static_cast<int>(W.qe[e] & 255u);
                 if (lo == INFINITY || lo > __uint_as_float(fkey_value(W.colacc[t]))) continue;
-                const double om = static_cast<double>(W.om[W.qe[e] >> 8]), od = static_cast<double>(W.qo[e]);
-                const double v = PASS == 2 ? __ddiv_rn(__dsub_rn(1.0, od), __dsub_rn(1.0, om))
-                                           : __dsub_rn(__dmul_rn(om, om), __dmul_rn(od, od));
+                const double v = mx_value<PASS>(W.qo[e], W.om[W.qe[e] >> 8]);
                 if (v == v) atomicMin(&W.colmin[t], dkey(v));
             }
         }
@@ -348,10 +400,12 @@ template <int PASS>
 __global__ void __launch_bounds__(MU_THREADS, 8)
 matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_dev, int m_bound,
                    long long u_begin, long long u_end, const int* __restrict__ done,
-                   unsigned* __restrict__ omax_bits, unsigned long long* __restrict__ xmin_key)
+                   unsigned* __restrict__ omax_bits, unsigned long long* __restrict__ xmin_key, MxList L)
 {
     __shared__ __align__(16) MxWarp sw[MU_WARPS];
     if (done && *done) return;
+    // Pass B with a list: the list kernels took the pairs unless it overflowed.
+    if (PASS && L.count && *L.count <= L.cap) return;
     const int wp = threadIdx.x >> 5;
     const int n = m_dev ? *m_dev : m_bound;
     const long long stride = static_cast<long long>(gridDim.x) * MU_WARPS;
@@ -361,7 +415,33 @@ matrix_pass_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m
         const int cb = c * MU_COLS, rbase = a * MU_ROWS;
         if (cb >= n || rbase >= n) continue;  // beyond the device-side count (warp-uniform)
         __syncwarp();  // the previous unit's use of the warp's shared memory is over
-        matrix_unit<PASS>(sw[wp], boxes_s, n, cb, rbase, omax_bits, xmin_key);
+        matrix_unit<PASS>(sw[wp], boxes_s, n, cb, rbase, omax_bits, xmin_key, L);
+    }
+}
+
+// Pass B over a complete list of overlapping pairs, in two sweeps: the
+// smallest binary32 upper bound per child, then the binary64 term of the pairs
+// whose lower bound does not exceed it, minimised per child.
+template <int PASS>
+__global__ void __launch_bounds__(256)
+matrix_list_kernel(MxList L, int sweep, const unsigned* __restrict__ omax_bits, unsigned* __restrict__ colhi,
+                   unsigned long long* __restrict__ xmin_key)
+{
+    const unsigned long long total = *L.count;
+    if (total > L.cap) return;  // incomplete: the unit pass takes over
+    const unsigned cnt = static_cast<unsigned>(total);
+    for (unsigned e = blockIdx.x * blockDim.x + threadIdx.x; e < cnt; e += gridDim.x * blockDim.x) {
+        const unsigned long long ij = L.ij[e];
+        const int i = static_cast<int>(ij >> 32), j = static_cast<int>(ij & 0xffffffffu);
+        const float o = L.o[e], om = __uint_as_float(omax_bits[i]);
+        float lo, ub;
+        if (!mx_bound<PASS>(o, om, lo, ub)) continue;
+        if (sweep == 0) {
+            atomicMin(colhi + j, fkey(ub));
+        } else if (!(lo > __uint_as_float(fkey_value(colhi[j])))) {
+            const double v = mx_value<PASS>(o, om);
+            if (v == v) atomicMin(xmin_key + j, dkey(v));
+        }
     }
 }
 
@@ -415,7 +495,8 @@ matrix_decide_kernel(const float* __restrict__ scores, const int* __restrict__ p
 
 void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, const int* m_dev, int m_bound,
                    float sigma, int linear, float decay_thr, int max_out, unsigned* omax_bits,
-                   unsigned long long* xmin_key, float* fs, uint32_t* kept, int* done, int64_t* keep,
+                   unsigned long long* xmin_key, float* fs, uint32_t* kept, int* done, unsigned long long* list_ij,
+                   float* list_o, unsigned long long* list_count, unsigned list_cap, unsigned* colhi, int64_t* keep,
                    float* keep_scores, int64_t* count, cudaStream_t st)
 {
     cudaMemsetAsync(omax_bits, 0, sizeof(unsigned) * static_cast<size_t>(m_bound), st);
@@ -428,20 +509,33 @@ void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, 
     // above them) and the decisions of boxes [lo, hi).  A stage given `done`
     // strides over its units with one resident wave, so that finding the flag
     // set costs a few CTAs per SM.
-    auto stage = [&](int lo, int hi, const int* dn) {
+    auto stage = [&](int lo, int hi, const int* dn, const MxList& L) {
         const long long u0 = matrix_units(lo), u1 = matrix_units(hi);
         if (u1 > u0) {
             long long g = (u1 - u0 + MU_WARPS - 1) / MU_WARPS;
             if (dn) g = std::min(g, static_cast<long long>(sms) * 8);
             const unsigned grid = static_cast<unsigned>(g);
             matrix_pass_kernel<0><<<grid, MU_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, u0, u1, dn, omax_bits,
-                                                                xmin_key);
+                                                                xmin_key, L);
+            // With a list, pass B takes its pairs in two flat sweeps, and the
+            // unit pass (one resident wave, striding) returns at once unless
+            // the list overflowed.
+            const unsigned gb = L.ij ? static_cast<unsigned>(std::min(g, static_cast<long long>(sms) * 8)) : grid;
+            if (L.ij) {
+                const unsigned gl = static_cast<unsigned>(sms) * 8;
+                for (int sweep = 0; sweep < 2; ++sweep) {
+                    if (linear)
+                        matrix_list_kernel<2><<<gl, 256, 0, st>>>(L, sweep, omax_bits, colhi, xmin_key);
+                    else
+                        matrix_list_kernel<1><<<gl, 256, 0, st>>>(L, sweep, omax_bits, colhi, xmin_key);
+                }
+            }
             if (linear)
-                matrix_pass_kernel<2><<<grid, MU_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, u0, u1, dn, omax_bits,
-                                                                    xmin_key);
+                matrix_pass_kernel<2><<<gb, MU_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, u0, u1, dn, omax_bits,
+                                                                  xmin_key, L);
             else
-                matrix_pass_kernel<1><<<grid, MU_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, u0, u1, dn, omax_bits,
-                                                                    xmin_key);
+                matrix_pass_kernel<1><<<gb, MU_THREADS, 0, st>>>(boxes_s, m_dev, m_bound, u0, u1, dn, omax_bits,
+                                                                  xmin_key, L);
         }
         if (hi > lo)
             matrix_decide_kernel<<<(hi - lo + 255) / 256, 256, 0, st>>>(scores, perm, xmin_key, m_dev, m_bound,
@@ -453,13 +547,22 @@ void launch_matrix(const float4* boxes_s, const float* scores, const int* perm, 
     // than max_out kept boxes.
     const long long k = max_out > 0 ? (2LL * max_out + MU_COLS - 1) / MU_COLS * MU_COLS : m_bound;
     if (k >= m_bound) {
-        stage(0, m_bound, nullptr);
+        // The list pays off when the unit walk of pass B is long; below
+        // MX_LIST_MIN_N boxes its extra launches cost more than they save.
+        const bool use_list = list_ij && m_bound >= MX_LIST_MIN_N;
+        MxList L{use_list ? list_ij : nullptr, list_o, use_list ? list_count : nullptr, list_cap};
+        if (use_list) {
+            cudaMemsetAsync(list_count, 0, sizeof(unsigned long long), st);
+            cudaMemsetAsync(colhi, 0xff, sizeof(unsigned) * static_cast<size_t>(m_bound), st);
+        }
+        stage(0, m_bound, nullptr, L);
     } else {
+        const MxList none{nullptr, nullptr, nullptr, 0u};
         // The rest's decisions may be skipped: their kept words must read 0.
         cudaMemsetAsync(kept, 0, sizeof(uint32_t) * static_cast<size_t>((m_bound + 31) / 32), st);
-        stage(0, static_cast<int>(k), nullptr);
+        stage(0, static_cast<int>(k), nullptr, none);
         launch_kept_prefix(kept, m_dev, m_bound, static_cast<int>(k), max_out, done, st);
-        stage(static_cast<int>(k), m_bound, done);
+        stage(static_cast<int>(k), m_bound, done, none);
     }
     launch_bits_emit(kept, m_dev, m_bound, perm, fs, max_out, keep, keep_scores, count, st);
 }

@@ -108,6 +108,26 @@ def test_max_out_prefix(max_out, decay):
     chk(b, s2, 0.2, max_out=max_out, score_thr=0.955)
 
 
+@pytest.mark.parametrize("decay", ["gaussian", "linear"])
+def test_pair_list(decay):
+    """From 16384 boxes pass A lists the overlapping pairs and pass B takes
+    the list (20000 clustered boxes); with more overlapping pairs than the
+    list holds (16384 boxes in a few tight stacks) pass B walks the units."""
+    chk = _check if decay == "gaussian" else _check_linear
+    rng = np.random.default_rng(31)
+    n = 20000
+    c = rng.uniform(0, 4000, (400, 2))[rng.integers(0, 400, n)] + rng.normal(0, 8, (n, 2))
+    wh = rng.uniform(8, 40, (n, 2))
+    b = np.concatenate([c - wh / 2, c + wh / 2], 1).astype(np.float32)
+    s = rng.uniform(0, 1, n).astype(np.float32)
+    chk(b, s, 0.2)
+    n = 16384
+    c = rng.uniform(0, 200, (4, 2))[rng.integers(0, 4, n)] + rng.normal(0, 2, (n, 2))
+    b = np.concatenate([c - 20, c + 20], 1).astype(np.float32)
+    s = rng.uniform(0, 1, n).astype(np.float32)
+    chk(b, s, 0.01)
+
+
 def test_identical_boxes_and_empty():
     b = np.tile(np.array([[1, 1, 5, 5]], np.float32), (200, 1))
     s = np.linspace(1.0, 0.2, 200).astype(np.float32)

@@ -150,13 +150,16 @@ decode_kernel(const float* __restrict__ preds, int anchors, int C, float conf_th
     if (t == 0) blk_cnt[static_cast<int64_t>(b) * nblk + blk] = total;
 }
 
-// One CTA per image: its header and its first max_objects candidates.
-__global__ void __launch_bounds__(DC_APB)
+// One CTA per image: its header and its first max_objects candidates (rows
+// copied by many threads at once: each copy is a dependent L2 round trip).
+constexpr int EM_THREADS = 1024;
+
+__global__ void __launch_bounds__(EM_THREADS)
 decode_emit_kernel(const float* __restrict__ stage, const int* __restrict__ blk_cnt, int nblk, int max_objects,
                    float* __restrict__ out)
 {
     extern __shared__ int pre[];  // nblk + 1 prefixes
-    __shared__ int wsum[DC_APB / 32];
+    __shared__ int wsum[EM_THREADS / 32];
     pdl_wait();
     emit_image(blockIdx.x, stage, blk_cnt, nblk, max_objects, out, pre, wsum);
 }
@@ -182,7 +185,7 @@ void launch_decode(const float* preds, int batch, int anchors, int C, float conf
     decode_kernel<<<dim3(nblk, batch), DC_APB, smem, st>>>(preds, anchors, C, conf_thr, nblk, stage, blk_cnt);
     const size_t esmem = sizeof(int) * (static_cast<size_t>(nblk) + 1);
     ensure_dynamic_smem(reinterpret_cast<const void*>(decode_emit_kernel), esmem);
-    launch_pdl(decode_emit_kernel, dim3(batch), dim3(DC_APB), esmem, st, static_cast<const float*>(stage),
+    launch_pdl(decode_emit_kernel, dim3(batch), dim3(EM_THREADS), esmem, st, static_cast<const float*>(stage),
                static_cast<const int*>(blk_cnt), nblk, max_objects, out);
 }
 

@@ -479,14 +479,19 @@ def run_gbnms(args):
     per_config = fast_nms = matrix_nms = matrix_lin = front_end = None
     if not args.no_configs:
         per_config, fast_nms, matrix_nms, matrix_lin = {}, {}, {}, {}
-        for name in W.CONFIGS:
+        sections = set(args.sections.split(","))
+        names = list(W.CONFIGS) if args.configs == "all" else args.configs.split(",")
+        for name in names:
             wl_c = W.make(name, 0)
-            per_config[name] = time_workload(g, torch, wl_c, dev, flush)
-            fast_nms[name] = time_workload(g, torch, wl_c, dev, flush, fast=True)
-            if wl_c.class_ids is None and wl_c.batch_offsets is None:
+            if "greedy" in sections:
+                per_config[name] = time_workload(g, torch, wl_c, dev, flush)
+            if "fast" in sections:
+                fast_nms[name] = time_workload(g, torch, wl_c, dev, flush, fast=True)
+            if "matrix" in sections and wl_c.class_ids is None and wl_c.batch_offsets is None:
                 matrix_nms[name] = time_matrix(g, torch, wl_c, dev, flush)
                 matrix_lin[name] = time_matrix(g, torch, wl_c, dev, flush, decay=g.NMS_DECAY_LINEAR)
-        front_end = time_front_end(g, torch, dev, flush)
+        if "front_end" in sections:
+            front_end = time_front_end(g, torch, dev, flush)
 
     cpu = None
     if not args.no_cpu_baseline:
@@ -568,6 +573,10 @@ def main():
     ap.add_argument("--workload", default=W.HEADLINE)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config timing table")
+    ap.add_argument("--configs", default="all",
+                    help="comma-separated workload names for the per-config tables (default: all)")
+    ap.add_argument("--sections", default="greedy,fast,matrix,front_end",
+                    help="per-config tables to time: greedy, fast, matrix, front_end")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.impl == "reference":

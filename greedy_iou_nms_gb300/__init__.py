@@ -411,7 +411,9 @@ class HostPipeline:
         if not self.zero_copy:
             self._h_out[: cap + 1].copy_(self._d_out[: cap + 1], non_blocking=True)
 
-    def run(self, iou_thr: float, score_thr: Optional[float] = None, max_out: int = 0):
+    def launch(self, iou_thr: float, score_thr: Optional[float] = None, max_out: int = 0) -> None:
+        """Enqueue one call on the current stream (the captured graph) without
+        waiting; ``result`` waits and returns the kept indices."""
         torch = _torch()
         key = (self.n, float(iou_thr), score_thr, int(max_out))
         graph = self._graphs.get(key)
@@ -425,9 +427,16 @@ class HostPipeline:
                               torch.cuda.current_stream(self.device))
             self._graphs[key] = graph
         graph.replay()
+
+    def result(self):
+        torch = _torch()
         torch.cuda.current_stream(self.device).synchronize()
         out = self._out_np
         return out[1: 1 + int(out[0])]
+
+    def run(self, iou_thr: float, score_thr: Optional[float] = None, max_out: int = 0):
+        self.launch(iou_thr, score_thr, max_out)
+        return self.result()
 
 
 def iou_mask(boxes_sorted, iou_thr: float):

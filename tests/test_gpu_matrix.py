@@ -121,6 +121,7 @@ def test_pair_list(decay):
     b = np.concatenate([c - wh / 2, c + wh / 2], 1).astype(np.float32)
     s = rng.uniform(0, 1, n).astype(np.float32)
     chk(b, s, 0.2)
+    chk(b, s, 0.2, score_thr=0.3)  # fewer candidates than the launch's bound
     n = 16384
     c = rng.uniform(0, 200, (4, 2))[rng.integers(0, 4, n)] + rng.normal(0, 2, (n, 2))
     b = np.concatenate([c - 20, c + 20], 1).astype(np.float32)

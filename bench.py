@@ -249,7 +249,7 @@ def time_front_end(g, torch, dev, flush, reps=20, conf_thr=0.25, max_objects=100
 
     def decode():
         st = g.nms_decode_boxes7(preds.data_ptr(), batch, anchors, width - 5, conf_thr, max_objects, buf.data_ptr(),
-                                 ws_d.data_ptr(), wsd, stream.cuda_stream)
+                                 0, ws_d.data_ptr(), wsd, stream.cuda_stream)
         if st != g.NMS_OK:
             raise g.NmsError(st, "nms_decode_boxes7")
 

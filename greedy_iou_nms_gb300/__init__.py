@@ -87,7 +87,7 @@ def load():
     lib.nms_resolve_mask_noalloc.restype = ctypes.c_int
     lib.nms_decode_workspace_size.argtypes = [i32, i32, ctypes.POINTER(sz)]
     lib.nms_decode_workspace_size.restype = ctypes.c_int
-    lib.nms_decode_boxes7.argtypes = [vp, i32, i32, i32, f32, i32, vp, vp, sz, vp]
+    lib.nms_decode_boxes7.argtypes = [vp, i32, i32, i32, f32, i32, vp, vp, vp, sz, vp]
     lib.nms_decode_boxes7.restype = ctypes.c_int
     lib.nms_boxes7_workspace_size.argtypes = [i32, i32, i32, ctypes.POINTER(sz)]
     lib.nms_boxes7_workspace_size.restype = ctypes.c_int
@@ -484,11 +484,11 @@ def nms_decode_workspace_size(batch: int, anchors: int) -> int:
 
 
 def nms_decode_boxes7(preds: int, batch: int, anchors: int, num_classes: int, conf_thr: float, max_objects: int,
-                      buffers: int, workspace: int, workspace_bytes: int, stream: int) -> int:
+                      buffers: int, dev_status: int, workspace: int, workspace_bytes: int, stream: int) -> int:
     """The C entry point (device addresses as ints)."""
     return load().nms_decode_boxes7(preds or None, int(batch), int(anchors), int(num_classes), float(conf_thr),
-                                    int(max_objects), buffers or None, workspace or None, int(workspace_bytes),
-                                    stream or None)
+                                    int(max_objects), buffers or None, dev_status or None, workspace or None,
+                                    int(workspace_bytes), stream or None)
 
 
 def nms_boxes7_workspace_size(batch: int, max_objects: int, num_classes: int) -> int:
@@ -520,10 +520,14 @@ def decode_boxes7(preds, conf_thr: float, max_objects: int):
     out = torch.zeros((batch, 1 + 7 * max_objects), dtype=torch.float32, device=dev)
     wsb = nms_decode_workspace_size(batch, anchors)
     ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
     st = nms_decode_boxes7(preds.data_ptr(), batch, anchors, width - 5, conf_thr, max_objects, out.data_ptr(),
-                           ws.data_ptr(), wsb, torch.cuda.current_stream(dev).cuda_stream)
+                           status.data_ptr(), ws.data_ptr(), wsb, torch.cuda.current_stream(dev).cuda_stream)
     if st != NMS_OK:
         raise NmsError(st, "nms_decode_boxes7")
+    dst = int(status.item())
+    if dst != NMS_OK:
+        raise NmsError(dst, "nms_decode_boxes7 (device)")
     return out
 
 

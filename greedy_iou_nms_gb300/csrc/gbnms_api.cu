@@ -488,7 +488,7 @@ namespace gbnms {
 namespace {
 
 struct DecodeLayout {
-    size_t stage, blk_cnt, total;
+    size_t status, stage, blk_cnt, total;
 };
 
 DecodeLayout decode_layout(int32_t batch, int32_t anchors)
@@ -496,6 +496,7 @@ DecodeLayout decode_layout(int32_t batch, int32_t anchors)
     DecodeLayout d;
     Layout L;
     const size_t slots = static_cast<size_t>(batch) * decode_blocks(anchors) * 128;
+    d.status = L.add(sizeof(int32_t));
     d.stage = L.add(7 * sizeof(float) * slots);
     d.blk_cnt = L.add(sizeof(int) * static_cast<size_t>(batch) * decode_blocks(anchors));
     d.total = L.total;
@@ -538,8 +539,8 @@ extern "C" nms_status nms_decode_workspace_size(int32_t batch, int32_t anchors, 
 }
 
 extern "C" nms_status nms_decode_boxes7(const float* preds, int32_t batch, int32_t anchors, int32_t num_classes,
-                                        float conf_thr, int32_t max_objects, float* buffers, void* workspace,
-                                        size_t workspace_bytes, void* stream)
+                                        float conf_thr, int32_t max_objects, float* buffers, int32_t* dev_status,
+                                        void* workspace, size_t workspace_bytes, void* stream)
 {
     if (batch < 1 || anchors < 0 || num_classes < 1 || max_objects < 0 || std::isnan(conf_thr))
         return NMS_ERR_INVALID_ARG;
@@ -550,7 +551,8 @@ extern "C" nms_status nms_decode_boxes7(const float* preds, int32_t batch, int32
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaGetLastError();
     launch_decode(preds, batch, anchors, num_classes, conf_thr, max_objects, buffers,
-                  at<float>(workspace, L.stage), at<int>(workspace, L.blk_cnt), st);
+                  at<float>(workspace, L.stage), at<int>(workspace, L.blk_cnt),
+                  dev_status ? dev_status : at<int32_t>(workspace, L.status), st);
     return cuda_status();
 }
 

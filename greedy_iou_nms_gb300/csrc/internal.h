@@ -130,7 +130,7 @@ unsigned matrix_list_cap(int64_t n);
 // Front end (k_decode.cu): YOLO-shaped predictions to count-header buffers.
 int decode_blocks(int anchors);
 void launch_decode(const float* preds, int batch, int anchors, int C, float conf_thr, int max_objects, float* out,
-                   float* stage, int* blk_cnt, cudaStream_t st);
+                   float* stage, int* blk_cnt, int32_t* status, cudaStream_t st);
 // NMS over count-header buffers: rows to batched inputs, then keep_flag.
 void launch_boxes7_gather(const float* bufs, int batch, int max_objects, int C, float4* boxes, float* scores,
                           int32_t* cls, int64_t* off, int* img_rows, cudaStream_t st);

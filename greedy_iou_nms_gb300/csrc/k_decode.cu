@@ -17,7 +17,8 @@
 // same on every run.
 //
 // GPU shape: one CTA per 128 anchors of an image stages their rows in shared
-// memory with asynchronous 16-byte copies (the rows are contiguous), decodes
+// memory with bulk copies (the rows are contiguous; the copy engine streams
+// them, completing on a shared-memory barrier with a bounded wait), decodes
 // one anchor per thread, compacts its candidates with a ballot per warp and a
 // prefix over its 4 warps, and writes them and its count to a staging area
 // (the local reduction).  One CTA per image then takes the prefix of the
@@ -79,12 +80,33 @@ __device__ void emit_image(int b, const float* __restrict__ stage, const int* __
     }
 }
 
+constexpr long long DC_WAIT_LIMIT = 1ll << 24;  // polls of the copy barrier before giving up
+constexpr unsigned DC_COPY = 8192;              // bytes per bulk copy (one per lane of warp 0)
+
+// Bounded wait for phase 0 of the barrier at shared address sb.
+__device__ __forceinline__ bool dc_wait(unsigned sb)
+{
+    for (long long k = 0; k < DC_WAIT_LIMIT; ++k) {
+        unsigned ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(sb)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
 __global__ void __launch_bounds__(DC_APB)
 decode_kernel(const float* __restrict__ preds, int anchors, int C, float conf_thr, int nblk,
-              float* __restrict__ stage, int* __restrict__ blk_cnt)
+              float* __restrict__ stage, int* __restrict__ blk_cnt, int32_t* status)
 {
     extern __shared__ __align__(16) float rows[];  // DC_APB rows of 5 + C floats
     __shared__ int wcnt[DC_APB / 32];
+    __shared__ __align__(8) unsigned long long bar;
+    __shared__ int s_ok;
     pdl_release();  // the emit may be scheduled; it waits for this grid
     const int b = blockIdx.y, blk = blockIdx.x;
     const int a0 = blk * DC_APB;
@@ -93,13 +115,43 @@ decode_kernel(const float* __restrict__ preds, int anchors, int C, float conf_th
     const float* src = preds + (static_cast<int64_t>(b) * anchors + a0) * W;
     const int nf = na * W;
     if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0 && (nf & 3) == 0) {
-        // 16-byte asynchronous copies when the block's rows start on a
-        // 16-byte boundary: the whole block's rows are in flight at once.
-        const unsigned sbase = static_cast<unsigned>(__cvta_generic_to_shared(rows));
-        for (int e = threadIdx.x; e < nf / 4; e += DC_APB)
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sbase + 16u * e), "l"(src + 4 * e)
-                         : "memory");
-        asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;\n" ::: "memory");
+        // Bulk copies when the block's rows start on a 16-byte boundary (and
+        // so, 16 bytes a row group, every copy's start and length): the whole
+        // block's rows in flight at once, issued by a few lanes.  Thread 0
+        // waits on the barrier (bounded) and the CTA barrier passes the rows
+        // on; on a wait that gives up, the status says so, the copies still
+        // in flight are waited for once more and the block writes nothing.
+        const unsigned sb = static_cast<unsigned>(__cvta_generic_to_shared(&bar));
+        const unsigned bytes = 4u * static_cast<unsigned>(nf);
+        if (threadIdx.x == 0) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(sb));
+            asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(sb), "r"(bytes) : "memory");
+        }
+        __syncwarp();
+        const unsigned nch = (bytes + DC_COPY - 1) / DC_COPY;
+        if (threadIdx.x < nch) {
+            const unsigned off = threadIdx.x * DC_COPY, len = min(DC_COPY, bytes - off);
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                    static_cast<unsigned>(__cvta_generic_to_shared(rows)) + off),
+                "l"(reinterpret_cast<const char*>(src) + off), "r"(len), "r"(sb)
+                : "memory");
+        }
+        if (threadIdx.x == 0) {
+            const bool ok = dc_wait(sb);
+            if (!ok) {
+                set_status(status, NMS_ERR_TIMEOUT);
+                dc_wait(sb);  // the copies in flight, once more
+            }
+            s_ok = ok;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(sb) : "memory");
+        if (!s_ok) {
+            if (threadIdx.x == 0) blk_cnt[static_cast<int64_t>(b) * nblk + blk] = 0;
+            return;
+        }
     } else {
 #pragma unroll 4
         for (int e = threadIdx.x; e < nf; e += DC_APB) rows[e] = src[e];
@@ -173,8 +225,9 @@ __global__ void zero_headers_kernel(float* __restrict__ out, int batch, int max_
 int decode_blocks(int anchors) { return (anchors + DC_APB - 1) / DC_APB; }
 
 void launch_decode(const float* preds, int batch, int anchors, int C, float conf_thr, int max_objects, float* out,
-                   float* stage, int* blk_cnt, cudaStream_t st)
+                   float* stage, int* blk_cnt, int32_t* status, cudaStream_t st)
 {
+    cudaMemsetAsync(status, 0, sizeof(int32_t), st);
     const int nblk = decode_blocks(anchors);
     if (nblk == 0) {  // no anchors: every header is 0
         zero_headers_kernel<<<(batch + 255) / 256, 256, 0, st>>>(out, batch, max_objects);
@@ -182,7 +235,8 @@ void launch_decode(const float* preds, int batch, int anchors, int C, float conf
     }
     const size_t smem = sizeof(float) * DC_APB * static_cast<size_t>(5 + C);
     ensure_dynamic_smem(reinterpret_cast<const void*>(decode_kernel), smem);
-    decode_kernel<<<dim3(nblk, batch), DC_APB, smem, st>>>(preds, anchors, C, conf_thr, nblk, stage, blk_cnt);
+    decode_kernel<<<dim3(nblk, batch), DC_APB, smem, st>>>(preds, anchors, C, conf_thr, nblk, stage, blk_cnt,
+                                                            status);
     const size_t esmem = sizeof(int) * (static_cast<size_t>(nblk) + 1);
     ensure_dynamic_smem(reinterpret_cast<const void*>(decode_emit_kernel), esmem);
     launch_pdl(decode_emit_kernel, dim3(batch), dim3(EM_THREADS), esmem, st, static_cast<const float*>(stage),

@@ -289,14 +289,17 @@ nms_status nms_run_timed(const float* boxes, const float* scores, int64_t n,
  *   conf_thr     not NaN.
  *   max_objects  >= 0 rows per image.
  *   buffers      device float[batch * (1 + 7 * max_objects)].
+ *   dev_status   device int32 [1] or NULL (then a word of the workspace):
+ *                NMS_OK, or NMS_ERR_TIMEOUT if a block's bounded wait for its
+ *                staged rows gave up (the buffers are then unspecified).
  *   workspace    >= nms_decode_workspace_size() bytes, 256-byte aligned.
  * Errors: NMS_ERR_INVALID_ARG, NMS_ERR_CAPACITY (limits), NMS_ERR_WORKSPACE,
- * NMS_ERR_CUDA.
+ * NMS_ERR_CUDA (host side); the device status above.
  */
 nms_status nms_decode_workspace_size(int32_t batch, int32_t anchors, size_t* bytes);
 nms_status nms_decode_boxes7(const float* preds, int32_t batch, int32_t anchors, int32_t num_classes,
-                             float conf_thr, int32_t max_objects, float* buffers, void* workspace,
-                             size_t workspace_bytes, void* stream);
+                             float conf_thr, int32_t max_objects, float* buffers, int32_t* dev_status,
+                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * NMS in place over count-header buffers (layout as above): for each image

@@ -152,7 +152,7 @@ def test_matrix_entry_validation(lib):
 def test_front_end_entry_validation(lib):
     ws = g.nms_decode_workspace_size(2, 100)
     a = dict(preds=FAKE, batch=2, anchors=100, num_classes=80, conf_thr=0.25, max_objects=10, buffers=FAKE,
-             workspace=FAKE, workspace_bytes=ws, stream=0)
+             dev_status=0, workspace=FAKE, workspace_bytes=ws, stream=0)
     for bad, code in ((dict(batch=0), g.NMS_ERR_INVALID_ARG), (dict(anchors=-1), g.NMS_ERR_INVALID_ARG),
                       (dict(num_classes=0), g.NMS_ERR_INVALID_ARG), (dict(max_objects=-1), g.NMS_ERR_INVALID_ARG),
                       (dict(conf_thr=math.nan), g.NMS_ERR_INVALID_ARG), (dict(buffers=0), g.NMS_ERR_INVALID_ARG),

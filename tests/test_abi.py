@@ -59,6 +59,31 @@ def test_workspace_size(lib):
         g.nms_workspace_size(-1)
 
 
+def test_matrix_and_front_end_workspace_sizes(lib):
+    # Matrix NMS: the pair list of pass A (about 96 pairs a box plus a floor,
+    # 12 bytes each, never more than the pairs there are) dominates.
+    for n in (2, 1000, 8192, 65536):
+        ws = g.nms_matrix_workspace_size(n)
+        pairs = min(n * (n - 1) // 2, 96 * n + (1 << 20))
+        assert ws >= 12 * pairs + 40 * n
+    assert g.nms_matrix_workspace_size(0) > 0
+    with pytest.raises(g.NmsError) as e:
+        g.nms_matrix_workspace_size((1 << 18) + 1)
+    assert e.value.code == g.NMS_ERR_CAPACITY
+    # Front end: 7 floats of staging per anchor slot, linear in batch.
+    d1 = g.nms_decode_workspace_size(1, 25200)
+    d16 = g.nms_decode_workspace_size(16, 25200)
+    assert d1 >= 7 * 4 * 25200 and 15 * d1 <= d16 <= 17 * d1
+
+
+def test_mapped_pointer_rejects_other_memory(lib):
+    # NULL and ordinary (unregistered) host memory have no device mapping; the
+    # query enqueues nothing and needs no GPU to say so.
+    import numpy as np
+    assert g.nms_mapped_pointer(0) is None
+    assert g.nms_mapped_pointer(np.zeros(16, np.float32).ctypes.data) is None
+
+
 def test_mask_row_words(lib):
     assert g.nms_mask_row_words(0) == 0
     assert g.nms_mask_row_words(1) == 4

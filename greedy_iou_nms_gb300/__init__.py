@@ -37,6 +37,7 @@ EXPORTED = ("nms_status_string", "nms_workspace_size", "nms_run", "nms_fast_run"
 NMS_NOALLOC_MAX_N = 16384
 NMS_DECODE_MAX_ANCHORS = 1 << 20
 NMS_DECODE_MAX_CLASSES = 384
+NMS_DECODE_MAX_BATCH = 65535
 
 _lib = None
 

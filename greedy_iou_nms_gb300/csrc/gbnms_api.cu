@@ -533,7 +533,7 @@ Boxes7Layout boxes7_layout(int32_t batch, int32_t max_objects, int32_t num_class
 extern "C" nms_status nms_decode_workspace_size(int32_t batch, int32_t anchors, size_t* bytes)
 {
     if (!bytes || batch < 1 || anchors < 0) return NMS_ERR_INVALID_ARG;
-    if (anchors > NMS_DECODE_MAX_ANCHORS) return NMS_ERR_CAPACITY;
+    if (anchors > NMS_DECODE_MAX_ANCHORS || batch > NMS_DECODE_MAX_BATCH) return NMS_ERR_CAPACITY;
     *bytes = decode_layout(batch, anchors).total;
     return NMS_OK;
 }
@@ -544,7 +544,8 @@ extern "C" nms_status nms_decode_boxes7(const float* preds, int32_t batch, int32
 {
     if (batch < 1 || anchors < 0 || num_classes < 1 || max_objects < 0 || std::isnan(conf_thr))
         return NMS_ERR_INVALID_ARG;
-    if (anchors > NMS_DECODE_MAX_ANCHORS || num_classes > NMS_DECODE_MAX_CLASSES) return NMS_ERR_CAPACITY;
+    if (anchors > NMS_DECODE_MAX_ANCHORS || num_classes > NMS_DECODE_MAX_CLASSES || batch > NMS_DECODE_MAX_BATCH)
+        return NMS_ERR_CAPACITY;
     if (!buffers || (anchors > 0 && (!preds || !aligned(preds, 4)))) return NMS_ERR_INVALID_ARG;
     const DecodeLayout L = decode_layout(batch, anchors);
     if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < L.total) return NMS_ERR_WORKSPACE;
@@ -563,6 +564,7 @@ extern "C" nms_status nms_boxes7_workspace_size(int32_t batch, int32_t max_objec
     if (static_cast<int64_t>(batch) * max_objects > INT32_MAX ||
         static_cast<int64_t>(batch) * num_classes > INT32_MAX / 2)
         return NMS_ERR_INVALID_ARG;
+    if (batch > NMS_DECODE_MAX_BATCH) return NMS_ERR_CAPACITY;
     *bytes = boxes7_layout(batch, max_objects, num_classes).total;
     return NMS_OK;
 }

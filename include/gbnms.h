@@ -266,6 +266,9 @@ nms_status nms_run_timed(const float* boxes, const float* scores, int64_t n,
 /* Limits of the front end for YOLO-shaped outputs. */
 #define NMS_DECODE_MAX_ANCHORS (1 << 20)
 #define NMS_DECODE_MAX_CLASSES 384
+/* Largest batch of the front end and of NMS over count-header buffers (the
+ * images are one dimension of the launch grids). */
+#define NMS_DECODE_MAX_BATCH 65535
 
 /*
  * Front end for YOLO-shaped outputs: the "count header + data body" buffer of
@@ -284,7 +287,7 @@ nms_status nms_run_timed(const float* boxes, const float* scores, int64_t n,
  * order (so the buffer is the same on every run).  Rows past the candidates
  * are left as they are.
  *   preds        device, 4-byte aligned.
- *   batch        >= 1; anchors in [0, NMS_DECODE_MAX_ANCHORS];
+ *   batch        in [1, NMS_DECODE_MAX_BATCH]; anchors in [0, NMS_DECODE_MAX_ANCHORS];
  *   num_classes  in [1, NMS_DECODE_MAX_CLASSES].
  *   conf_thr     not NaN.
  *   max_objects  >= 0 rows per image.
@@ -314,6 +317,7 @@ nms_status nms_decode_boxes7(const float* preds, int32_t batch, int32_t anchors,
  *                 other value sets NMS_ERR_INVALID_ARG in the device status
  *                 (dev_status, or the workspace's status word) and leaves
  *                 that row out.
+ *   batch <= NMS_DECODE_MAX_BATCH (else NMS_ERR_CAPACITY);
  *   batch * max_objects <= INT32_MAX; batch * num_classes <= INT32_MAX / 2.
  *   workspace     >= nms_boxes7_workspace_size() bytes, 256-byte aligned.
  * Errors: NMS_ERR_INVALID_ARG, NMS_ERR_WORKSPACE, NMS_ERR_CUDA (host side);

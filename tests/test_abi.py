@@ -184,6 +184,7 @@ def test_front_end_entry_validation(lib):
                       (dict(preds=FAKE + 2), g.NMS_ERR_INVALID_ARG),
                       (dict(anchors=g.NMS_DECODE_MAX_ANCHORS + 1), g.NMS_ERR_CAPACITY),
                       (dict(num_classes=g.NMS_DECODE_MAX_CLASSES + 1), g.NMS_ERR_CAPACITY),
+                      (dict(batch=g.NMS_DECODE_MAX_BATCH + 1), g.NMS_ERR_CAPACITY),
                       (dict(workspace_bytes=ws - 1), g.NMS_ERR_WORKSPACE), (dict(workspace=FAKE + 8), g.NMS_ERR_WORKSPACE)):
         assert g.nms_decode_boxes7(**dict(a, **bad)) == code, bad
     wb = g.nms_boxes7_workspace_size(2, 10, 80)
@@ -193,6 +194,7 @@ def test_front_end_entry_validation(lib):
                       (dict(fast=2), g.NMS_ERR_INVALID_ARG), (dict(iou_thr=math.nan), g.NMS_ERR_INVALID_ARG),
                       (dict(buffers=0), g.NMS_ERR_INVALID_ARG), (dict(max_objects=-1), g.NMS_ERR_INVALID_ARG),
                       (dict(batch=1 << 20, max_objects=1 << 12), g.NMS_ERR_INVALID_ARG),
+                      (dict(batch=g.NMS_DECODE_MAX_BATCH + 1), g.NMS_ERR_CAPACITY),
                       (dict(workspace_bytes=wb - 1), g.NMS_ERR_WORKSPACE)):
         assert g.nms_boxes7_run(**dict(b, **bad)) == code, bad
     with pytest.raises(g.NmsError):

@@ -41,9 +41,15 @@ UNIT = "boxes/s"
 # FP32 operations of one canonical IoU test (4 min/max, 2 sub, 2 clamp, 1 mul,
 # 1 add, 1 sub, 1 div, 1 compare): the algorithmic work per pair.
 OPS_PER_PAIR = 13
-SMS = 152
-FP32_LANES_PER_SM = 128
+# How those 13 operations fall on the SM's pipes: the 4 min/max, the 2 clamps
+# and the compare run on the ALU pipe (min.f32 and setp class); the 2 subs of
+# the sides, the product, the sum, the union's sub and the division (charged
+# as one operation) run on the FMA pipe, where the packed f32x2 forms can
+# take two of them per instruction.
+ALU_OPS_PER_PAIR = 7
+FMA_OPS_PER_PAIR = 6
 L2_FLUSH_BYTES = 256 << 20
+PROBE_LIB = os.path.join(ROOT, "greedy_iou_nms_gb300", "_build", "libgbprobe.so")
 
 
 def _peaks():
@@ -109,6 +115,103 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def measure_alu_peaks(torch, dev, ctas_per_sm=4, iters=2048, reps=5):
+    """Measured instruction throughput of the SM (the probe library: each form
+    as independent chains on ctas_per_sm CTAs of 256 threads per SM), and the
+    FP32 operation roof of the canonical IoU test built from it.
+
+    Per form: operations per second (CUDA events, best of `reps`), the SM
+    clock the CTAs saw (clock64 cycles per global-timer nanosecond) and from
+    the two the lane operations per SM clock.  The roof: a pair costs
+    7 ALU-pipe operations (at the measured min.f32 rate), 6 FMA-pipe
+    operations (at the best measured add rate, packed or not) and their
+    instructions (at the best measured issue rate); the slowest of the three
+    sets the pairs per SM clock, times 13 operations per pair, times the SM
+    count and the clock the probe ran at."""
+    import ctypes
+    lib = ctypes.CDLL(PROBE_LIB)
+    lib.gbprobe_form_name.restype = ctypes.c_char_p
+    lib.gbprobe_ops_per_thread.restype = ctypes.c_double
+    lib.gbprobe_ops_per_thread.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.gbprobe_insts_per_thread.restype = ctypes.c_double
+    lib.gbprobe_insts_per_thread.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.gbprobe_launch.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_void_p]
+    sms = int(lib.gbprobe_sm_count())
+    if sms <= 0:
+        raise RuntimeError("probe: no SM count from the device")
+    tpc = int(lib.gbprobe_threads_per_cta())
+    ctas = sms * ctas_per_sm
+    out = torch.empty(ctas * tpc, dtype=torch.float32, device=dev)
+    cyc = torch.empty(ctas, dtype=torch.int64, device=dev)
+    nsec = torch.empty(ctas, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    forms = {}
+    mhz = []
+    for f in range(int(lib.gbprobe_forms())):
+        name = lib.gbprobe_form_name(f).decode()
+        ops = lib.gbprobe_ops_per_thread(f, iters) * tpc * ctas
+        ins = lib.gbprobe_insts_per_thread(f, iters) * tpc * ctas
+        best_s = None
+        for r in range(reps + 1):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            rc = lib.gbprobe_launch(f, ctas, iters, out.data_ptr(), cyc.data_ptr(), nsec.data_ptr(),
+                                    stream.cuda_stream)
+            b.record(stream)
+            if rc != 0:
+                raise RuntimeError(f"probe launch of {name} failed: cudaError {rc}")
+            torch.cuda.synchronize()
+            if r == 0:
+                continue  # warm-up
+            s = a.elapsed_time(b) / 1000
+            best_s = s if best_s is None else min(best_s, s)
+            mhz.append(1000.0 * float((cyc.double() / nsec.double()).median().item()))
+        f_mhz = statistics.median(mhz[-reps:])
+        # Per SM clock from the event-timed rate and the clock the CTAs
+        # measured (a CTA's own span can miss part of the kernel, so only
+        # its cycles per nanosecond are used).
+        ops_clk = ops / best_s / (sms * f_mhz * 1e6)
+        forms[name] = {"lane_ops_per_clk_per_sm": ops_clk,
+                       "lane_insts_per_clk_per_sm": ops_clk * ins / ops,
+                       "tops": ops / best_s / 1e12, "mhz": f_mhz}
+    r_alu = forms["fmnmx"]["lane_ops_per_clk_per_sm"]
+    add_form = max(("fadd", "fadd2"), key=lambda k: forms[k]["lane_ops_per_clk_per_sm"])
+    r_fma = forms[add_form]["lane_ops_per_clk_per_sm"]
+    ops_per_ins = r_fma / forms[add_form]["lane_insts_per_clk_per_sm"]
+    r_issue = max(v["lane_insts_per_clk_per_sm"] for v in forms.values())
+    t_alu = ALU_OPS_PER_PAIR / r_alu
+    t_fma = FMA_OPS_PER_PAIR / r_fma
+    t_issue = (ALU_OPS_PER_PAIR + FMA_OPS_PER_PAIR / ops_per_ins) / r_issue
+    pairs_clk = 1.0 / max(t_alu, t_fma, t_issue)
+    mhz = statistics.median(v["mhz"] for v in forms.values())
+    # The roof per second: pairs per SM clock at the clock the probe ran at.
+    roof_tops = OPS_PER_PAIR * pairs_clk * sms * mhz * 1e6 / 1e12
+    best = max(forms, key=lambda k: forms[k]["tops"])
+    return {"sm_count": sms, "probe_mhz": mhz, "ctas_per_sm": ctas_per_sm, "threads_per_cta": tpc,
+            "forms": forms, "roof_pairs_per_clk_per_sm": pairs_clk, "roof_tops": roof_tops,
+            "roof_bound": min((("alu", t_alu), ("fma", t_fma), ("issue", t_issue)), key=lambda x: -x[1])[0],
+            "roof_add_form": add_form, "best_form": best, "best_form_tops": forms[best]["tops"]}
+
+
+def bench_config(wl, world):
+    """The `config` of both arms' lines (the same dict, so the two lines name
+    the same workload the same way)."""
+    return {"workload": wl.name, "n": wl.n, "iou_thr": wl.iou_thr, "max_out": wl.max_out,
+            "l2": "flushed (256 MiB write) before every timed step",
+            "parallelism": f"replicas x{world}"}
+
+
+def mask_pairs(n, max_out, tile=128):
+    """Pairs of the first mask launch of nms_run: the whole triangle, or with
+    max_out the leading 2*max_out boxes rounded up to the mask tile width
+    (when that is fewer than n)."""
+    k = n
+    if max_out > 0:
+        k = min(n, (2 * max_out + tile - 1) // tile * tile)
+    return k * (k - 1) // 2
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -166,7 +269,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": wl.name, "n": wl.n, "iou_thr": wl.iou_thr},
+        "config": bench_config(wl, ws),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{reps_total} full runs of {wl.name} (one per step)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -186,7 +289,7 @@ def _graph_size(wl):
     return bits, len(keep)
 
 
-def time_workload(g, torch, wl, dev, flush, reps=30, fast=False):
+def time_workload(g, torch, wl, dev, flush, reps=30, fast=False, stage_reps=20):
     """Device time of one nms_run call (nms_fast_run with fast=True) on
     workload wl (inputs resident, L2 flushed before each call): median, p10
     and p90 in microseconds."""
@@ -229,9 +332,37 @@ def time_workload(g, torch, wl, dev, flush, reps=30, fast=False):
     us = sorted(1000 * a.elapsed_time(b) for a, b in evs)
     q = lambda f: us[min(len(us) - 1, int(f * len(us)))]
     med = statistics.median(us)
-    return {"us_median": med, "us_p10": q(0.1), "us_p90": q(0.9), "boxes_per_s": wl.n / (med / 1e6),
-            "gpairs_per_s": wl.pairs / (med / 1e6) / 1e9, "n": wl.n,
-            "kept": int(counts.sum().item()), "batched": batched}
+    res = {"us_median": med, "us_p10": q(0.1), "us_p90": q(0.9), "boxes_per_s": wl.n / (med / 1e6),
+           "gpairs_per_s": wl.pairs / (med / 1e6) / 1e9, "n": wl.n,
+           "kept": int(counts.sum().item()), "batched": batched}
+    if fast:
+        return res
+    # Stage durations of the same call (nms_run_timed: events between the
+    # stages on the launching stream, L2 flushed before each call): for one
+    # image sort | first mask launch | resolve and any later stage; batched:
+    # pre-filter and segmenting | segment NMS | per-image merge.
+    stage = [[], [], []]
+    for it in range(3 + stage_reps):
+        flush.fill_(1)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        for e in ev:
+            e.record(stream)
+        st = g.nms_run_timed(boxes.data_ptr(), scores.data_ptr(), wl.n, cls.data_ptr() if cls is not None else 0,
+                             C, off.data_ptr() if off is not None else 0, B, wl.iou_thr, score_thr, wl.max_out,
+                             keep.data_ptr(), cap, counts.data_ptr(), 0, ws.ptr, ws.bytes, stream.cuda_stream, ev)
+        if st != g.NMS_OK:
+            raise g.NmsError(st, "nms_run_timed")
+        torch.cuda.synchronize()
+        if it >= 3:
+            for k in range(3):
+                stage[k].append(1000 * ev[k].elapsed_time(ev[k + 1]))
+    s0, s1, s2 = (statistics.mean(t) for t in stage)
+    if batched:
+        res["stages_us"] = {"segmenting": s0, "segment_nms": s1, "merge": s2}
+    else:
+        res["stages_us"] = {"sort": s0, "mask": s1, "resolve": s2}
+        res["mask_pairs"] = mask_pairs(wl.n, wl.max_out)
+    return res
 
 
 def time_front_end(g, torch, dev, flush, reps=20, conf_thr=0.25, max_objects=1000, iou_thr=0.45):
@@ -446,11 +577,12 @@ def run_gbnms(args):
     parity = bool(got.tolist() == exp.tolist())
 
     peaks, peak_kind = _peaks()
-    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
-    alu_peak_tops = SMS * FP32_LANES_PER_SM * sm_max * 1e6 / 1e12
     hbm = float(peaks.get("hbm_gbs", 6800.0))
+    alu = measure_alu_peaks(torch, dev)
+    fp32_roof = alu["roof_tops"]
     pairs = n * (n - 1) // 2
-    mask_tops = OPS_PER_PAIR * pairs / (mask_ms / 1000) / 1e12
+    m_pairs = mask_pairs(n, wl.max_out)
+    mask_tops = OPS_PER_PAIR * m_pairs / (mask_ms / 1000) / 1e12
     Wn = (n + 63) // 64
     mask_bytes = 8 * sum(Wn - i // 64 for i in range(n))  # triangle words written
     n_pairs, n_kept = _graph_size(wl)
@@ -464,17 +596,22 @@ def run_gbnms(args):
     dominant = max(("iou_mask", mask_ms), ("resolve", resolve_ms), ("sort", sort_ms),
                    key=lambda x: x[1])[0]
     mask_roof = {"kernel": "iou_mask_kernel", "bound": "alu", "achieved": mask_tops,
-                 "peak": alu_peak_tops, "unit": "TFLOP/s", "frac": mask_tops / alu_peak_tops,
+                 "peak": fp32_roof, "unit": "TFLOP/s", "frac": mask_tops / fp32_roof,
                  "traffic": _ncu_traffic("iou_mask"),
-                 "note": f"FP32 ops, {OPS_PER_PAIR}/pair x {pairs} pairs; peak = {SMS} SMs x "
-                         f"{FP32_LANES_PER_SM} lanes x {sm_max:.0f} MHz (max clock)"}
+                 "frac_of_best_form": mask_tops / alu["best_form_tops"],
+                 "note": (f"FP32 ops, {OPS_PER_PAIR}/pair x {m_pairs} pairs over the event-timed kernel; peak of "
+                          f"measured: the canonical test's {ALU_OPS_PER_PAIR} ALU-pipe + {FMA_OPS_PER_PAIR} "
+                          f"FMA-pipe ops at the probed pipe rates ({alu['roof_bound']}-bound, "
+                          f"{alu['roof_pairs_per_clk_per_sm']:.2f} pairs/clk/SM) x {alu['sm_count']} SMs x "
+                          f"{alu['probe_mhz']:.0f} MHz; frac_of_best_form is against the fastest probed form "
+                          f"({alu['best_form']}, {alu['best_form_tops']:.1f} Tops/s)")}
     if dominant == "iou_mask":
         roof = mask_roof
     else:
         name, ms, nbytes = (("resolve_single_kernel", resolve_ms, resolve_bytes) if dominant == "resolve"
                             else ("bucket_rank_kernel", sort_ms, sort_bytes))
         ach = nbytes / (ms / 1000) / 1e9
-        note = f"algorithmic bytes {nbytes}; peak {peak_kind}"
+        note = f"algorithmic bytes {nbytes}; peak of {peak_kind} (HBM copy)"
         if dominant == "resolve":
             note += ("; the resolve runs on one SM by design (dependency rounds over the pair list in "
                      "shared memory), so its time is set by round latency, not by HBM")
@@ -482,6 +619,7 @@ def run_gbnms(args):
                 "frac": ach / hbm, "traffic": _ncu_traffic(dominant), "note": note}
 
     per_config = fast_nms = matrix_nms = matrix_lin = front_end = None
+    summary = None
     if not args.no_configs:
         per_config, fast_nms, matrix_nms, matrix_lin = {}, {}, {}, {}
         sections = set(args.sections.split(","))
@@ -497,49 +635,103 @@ def run_gbnms(args):
                 matrix_lin[name] = time_matrix(g, torch, wl_c, dev, flush, decay=g.NMS_DECAY_LINEAR)
         if "front_end" in sections:
             front_end = time_front_end(g, torch, dev, flush)
+        summary = greedy_summary(per_config, fp32_roof, hbm)
 
     cpu = None
+    cpu_all = None
     if not args.no_cpu_baseline:
         v, reps_cpu, secs = cpu_oracle_run(wl, args.cpu_seconds)
         cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{reps_cpu} full runs of {wl.name} in {secs:.1f} s"}
+               "sample": f"{reps_cpu} full runs of {wl.name} in {secs:.1f} s",
+               "cpu_model": cpu_model()}
 
+    alu_brief = {"sm_count": alu["sm_count"], "probe_mhz": round(alu["probe_mhz"], 1),
+                 "roof_tops": round(fp32_roof, 3), "roof_bound": alu["roof_bound"],
+                 "lane_ops_per_clk_per_sm": {k: round(v["lane_ops_per_clk_per_sm"], 1)
+                                             for k, v in alu["forms"].items()}}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": wl.name, "n": n, "iou_thr": wl.iou_thr, "max_out": wl.max_out,
-                   "l2": "flushed (256 MiB write) before every timed step",
-                   "parallelism": f"replicas x{world}"},
-        "us_per_call": 1000 * ms_per_step,
-        "gpairs_per_s": pairs / (ms_per_step / 1000) / 1e9,
-        "mask_gpairs_per_s": pairs / (mask_ms / 1000) / 1e9,
-        "mask_gbs": mask_bytes / (mask_ms / 1000) / 1e9,
-        "mask_hbm_frac": mask_bytes / (mask_ms / 1000) / 1e9 / hbm,
-        "kernels": kernels,
-        "per_config": per_config,
+        "config": bench_config(wl, world),
+        "alu_peaks": alu,
         "fast_nms_per_config": fast_nms,
         "front_end": front_end,
         "matrix_nms_per_config": matrix_nms,
         "matrix_nms_linear_per_config": matrix_lin,
-        "roofline": roof,
-        "roofline_iou_mask": mask_roof,
+        "per_config": per_config,
+        "e2e_with_copies": {"value": n / (cp_ms / 1000), "unit": UNIT, "h2d_bytes_per_step": cp_h2d,
+                            "d2h_bytes_per_step": cp_d2h, "ms_per_step": cp_ms, "host_ms_per_step": cp_host_ms},
+        "cpu_baseline_all_cores": cpu_all,
+        "kernels": kernels,
+        "us_per_call": 1000 * ms_per_step,
+        "gpairs_per_s": pairs / (ms_per_step / 1000) / 1e9,
+        "mask_gpairs_per_s": m_pairs / (mask_ms / 1000) / 1e9,
+        "mask_gbs": mask_bytes / (mask_ms / 1000) / 1e9,
+        "mask_hbm_frac": mask_bytes / (mask_ms / 1000) / 1e9 / hbm,
         "cpu_baseline": cpu,
         "e2e": {"value": n / (e2e_ms / 1000), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "host_ms_per_step": e2e_host_ms,
                 "transfer": ("zero-copy: the kernels read the pinned input and write the pinned output"
                              if e2e_zc else "copies")},
-        "e2e_with_copies": {"value": n / (cp_ms / 1000), "unit": UNIT, "h2d_bytes_per_step": cp_h2d,
-                            "d2h_bytes_per_step": cp_d2h, "ms_per_step": cp_ms, "host_ms_per_step": cp_host_ms},
         "gpu_launches": 3 * args.steps,  # sort, mask, resolve per call at this size
-        "clocks": clocks,
         "parity_vs_oracle": parity and e2e_parity,
-        "peaks": peak_kind,
+        "peaks": {"hbm": peak_kind, "fp32": "measured (probe in this run)"},
+        # Last, so that a reader keeping only the end of the line has them.
+        "roofline": roof,
+        "roofline_iou_mask": mask_roof,
+        "alu_roof": alu_brief,
+        "per_config_greedy": summary,
+        "clocks": clocks,
     }
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def greedy_summary(per_config, fp32_roof, hbm):
+    """Compact per-workload table of nms_run: median us per call, M boxes/s,
+    the first mask launch's us, G pairs/s, fraction of the FP32 op roof and
+    mask GB/s (written triangle words), and the other two stages' us."""
+    out = {}
+    for name, r in per_config.items():
+        row = {"us": round(r["us_median"], 1), "Mboxes_s": round(r["boxes_per_s"] / 1e6, 1)}
+        st = r.get("stages_us")
+        if st and "mask" in st:
+            n = r["n"]
+            m_us = st["mask"]
+            k = int(round((1 + math.sqrt(1 + 8 * r["mask_pairs"])) / 2))  # boxes of the first mask launch
+            wn = (n + 63) // 64
+            words = sum(wn - i // 64 for i in range(k))
+            row.update({"sort_us": round(st["sort"], 1), "mask_us": round(m_us, 1),
+                        "mask_Gpairs_s": round(r["mask_pairs"] / m_us / 1e3, 1),
+                        "mask_frac": round(OPS_PER_PAIR * r["mask_pairs"] / (m_us / 1e6) / 1e12 / fp32_roof, 3),
+                        "mask_GBs": round(8 * words / m_us / 1e3, 1), "resolve_us": round(st["resolve"], 1)})
+        elif st:
+            row.update({k: round(v, 1) for k, v in st.items()})
+        out[name] = row
+    return out
+
+
+def cpu_model():
+    """The host CPU's model string (/proc/cpuinfo, or lscpu on Arm hosts whose
+    cpuinfo has no model name)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return "unknown"
 
 
 KERNEL_SOURCES = {"iou_mask": "k_mask.cu", "resolve": "k_resolve.cu", "sort": "k_sort.cu"}

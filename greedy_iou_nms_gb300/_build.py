@@ -19,6 +19,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libgbnms.so")
+# Instruction-throughput probe for the roofline denominators (bench.py only).
+PROBE_SRC = os.path.join(PKG, "probe", "alu_probe.cu")
+PROBE_LIB = os.path.join(BUILD, "libgbprobe.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC",
@@ -37,7 +40,9 @@ def sources():
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(PROBE_LIB):
+        return True
+    if os.path.getmtime(PROBE_SRC) > os.path.getmtime(PROBE_LIB):
         return True
     t = os.path.getmtime(LIB)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
@@ -64,10 +69,16 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             raise RuntimeError("nvcc failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
         return r.stderr
 
+    probe_tmp = PROBE_LIB + ".tmp%d" % os.getpid()
+    # The probe has no binary32 contraction concern (its instructions are
+    # inline PTX) and builds straight to its own shared library.
+    cmds.append([cc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", *extra_flags,
+                 "-shared", PROBE_SRC, "-o", probe_tmp])
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(cmds), os.cpu_count() or 1))) as ex:
         for out in ex.map(run, cmds):
             if verbose and out:
                 print(out)
+    os.replace(probe_tmp, PROBE_LIB)
     tmp = LIB + ".tmp%d" % os.getpid()
     run([cc, *ARCH, "-shared", "-o", tmp, *objs])
     os.replace(tmp, LIB)

@@ -32,6 +32,10 @@
 // canonical IoU itself, so every stored bit is exactly the definition's.
 // Tiles holding a malformed box, and thresholds outside the filter's range,
 // send every pair of the tile to the canonical test.
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -420,6 +424,50 @@ iou_mask_kernel(const float4* __restrict__ boxes_s, const int* __restrict__ m_de
     }
 }
 
+// Dynamic shared memory that holds the kernel to at most `cap` resident CTAs
+// per SM (0 when the other limits already do), for the current device.
+// Cached per (device, cap): the occupancy query runs once.
+static size_t mask_smem_for_cap(int cap)
+{
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, size_t> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find({dev, cap});
+    if (it != cache.end()) return it->second;
+    int per_sm = 0, reserved = 0, optin = 0;
+    cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncAttributes fa{};
+    cudaFuncGetAttributes(&fa, iou_mask_kernel);
+    size_t dyn = 0;
+    int blocks = 0;
+    if (per_sm > 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, iou_mask_kernel, M_THREADS, 0) ==
+                          cudaSuccess &&
+        blocks > cap) {
+        // The smallest CTA footprint (static + dynamic + reserved) of which
+        // cap + 1 no longer fit, grown by 128 bytes until the query agrees.
+        const long long need = static_cast<long long>(per_sm) / (cap + 1) + 1 - reserved -
+                               static_cast<long long>(fa.sharedSizeBytes);
+        dyn = need > 0 ? static_cast<size_t>(need) : 0;
+        dyn = (dyn + 127) / 128 * 128;
+        const size_t max_dyn = optin > static_cast<int>(fa.sharedSizeBytes) ? optin - fa.sharedSizeBytes : 0;
+        for (int tries = 0; tries < 64 && dyn <= max_dyn; ++tries, dyn += 128) {
+            ensure_dynamic_smem(reinterpret_cast<const void*>(iou_mask_kernel), dyn);
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, iou_mask_kernel, M_THREADS, dyn) !=
+                cudaSuccess)
+                break;
+            if (blocks <= cap) break;
+        }
+        if (blocks > cap || dyn > max_dyn) dyn = 0;  // no footprint found: leave the placement to the hardware
+        cudaGetLastError();
+    }
+    cache[{dev, cap}] = dyn;
+    return dyn;
+}
+
 int64_t mask_tiles(int64_t n)
 {
     int64_t T = (n + MT - 1) / MT;
@@ -446,9 +494,17 @@ void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const
     // few CTAs per SM.
     int64_t grid = (u1 - u0 + M_WARPS - 1) / M_WARPS;
     if (done) grid = min(grid, static_cast<int64_t>(sms) * M_CTAS_PER_SM);
+    // A grid of one wave or less is held to ceil(grid / SMs) CTAs per SM.
+    // The launch may be placed while the previous kernel still holds some
+    // SMs (programmatic dependent launch); without the cap the free SMs
+    // would take the full 8 CTAs each, finish last and set the kernel's time.
+    size_t dyn = 0;
+    const int64_t per_sm = (grid + sms - 1) / sms;
+    if (!done && per_sm < M_CTAS_PER_SM) dyn = mask_smem_for_cap(static_cast<int>(per_sm));
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(M_THREADS);
+    cfg.dynamicSmemBytes = dyn;
     cfg.stream = st;
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;

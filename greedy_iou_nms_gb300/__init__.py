@@ -234,8 +234,9 @@ def nms_resolve_mask(mask: int, n: int, perm: int, max_out: int, keep: int, coun
 
 def nms_resolve_mask_noalloc(mask: int, n: int, perm: int, max_out: int, keep: int, count: int,
                              stream: int) -> int:
-    """nms_resolve_mask with its scratch in a library-held device array (no
-    workspace, no allocation in the call); n <= NMS_NOALLOC_MAX_N."""
+    """nms_resolve_mask without a workspace: the resolve keeps all its state
+    in the shared memory of its one thread block, so the call allocates
+    nothing and holds nothing between calls; n <= NMS_NOALLOC_MAX_N."""
     return load().nms_resolve_mask_noalloc(mask or None, int(n), perm or None, int(max_out),
                                            keep or None, count or None, stream or None)
 

@@ -635,6 +635,12 @@ extern "C" nms_status nms_run_timed(const float* boxes, const float* scores, int
     Stamps sp;
     sp.ev = events;
     sp.n = events && nevents > 0 ? nevents : 0;
+    // Plain launches between the stage events (see pdl_disabled).
+    struct NoPdl {
+        bool prev = pdl_disabled();
+        NoPdl() { pdl_disabled() = true; }
+        ~NoPdl() { pdl_disabled() = prev; }
+    } no_pdl;
     return run_impl(boxes, scores, n, class_ids, num_classes, batch_offsets, batch, iou_thr,
                     score_thr, max_out, keep, keep_cap, counts, dev_status, workspace,
                     workspace_bytes, stream, sp);
@@ -663,7 +669,9 @@ extern "C" nms_status nms_resolve_mask(const uint64_t* mask, int64_t n, const in
 {
     if (n < 0) return NMS_ERR_INVALID_ARG;
     if (n > NMS_MAX_SINGLE_N) return NMS_ERR_CAPACITY;
-    if (!count || (n > 0 && (!mask || !keep || !aligned(mask, 16)))) return NMS_ERR_INVALID_ARG;
+    if (!count || !aligned(count, 8) || (n > 0 && (!mask || !keep || !aligned(mask, 16) || !aligned(keep, 8) ||
+                                                   (perm && !aligned(perm, 4)))))
+        return NMS_ERR_INVALID_ARG;
     const SingleLayout L = single_layout(n);
     if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < L.total) return NMS_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

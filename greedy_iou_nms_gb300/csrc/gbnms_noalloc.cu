@@ -19,8 +19,12 @@ extern "C" nms_status nms_resolve_mask_noalloc(const uint64_t* mask, int64_t n, 
 {
     if (n < 0) return NMS_ERR_INVALID_ARG;
     if (n > NMS_NOALLOC_MAX_N) return NMS_ERR_CAPACITY;
-    if (!count || (n > 0 && (!mask || !keep))) return NMS_ERR_INVALID_ARG;
-    if (n > 0 && reinterpret_cast<uintptr_t>(mask) % 16 != 0) return NMS_ERR_INVALID_ARG;
+    // The resolve reads the mask with 16-byte loads and perm as int32, and
+    // writes keep and count as int64: misaligned pointers are refused here.
+    auto misaligned = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a != 0; };
+    if (!count || misaligned(count, 8)) return NMS_ERR_INVALID_ARG;
+    if (n > 0 && (!mask || !keep || misaligned(mask, 16) || misaligned(keep, 8) || (perm && misaligned(perm, 4))))
+        return NMS_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaGetLastError();
     if (n == 0) {

@@ -30,7 +30,18 @@ inline cudaLaunchAttribute pdl_attribute()
     return a;
 }
 
-// Launch with pdl_attribute().
+// Whether this host thread's launches leave out the programmatic-dependent
+// launch attribute (nms_run_timed sets it for its call: its stage events sit
+// between the kernels, so no kernel could start early anyway, and stage
+// durations are then measured on plain launches).
+inline bool& pdl_disabled()
+{
+    static thread_local bool off = false;
+    return off;
+}
+inline unsigned pdl_attr_count() { return pdl_disabled() ? 0u : 1u; }
+
+// Launch with pdl_attribute() (unless disabled for this thread).
 template <typename... KArgs, typename... Args>
 inline void launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                        Args&&... args)
@@ -42,7 +53,7 @@ inline void launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     cfg.stream = st;
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_attr_count();
     cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 

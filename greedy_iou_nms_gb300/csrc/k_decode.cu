@@ -80,13 +80,27 @@ __device__ void emit_image(int b, const float* __restrict__ stage, const int* __
     }
 }
 
-constexpr long long DC_WAIT_LIMIT = 1ll << 24;  // polls of the copy barrier before giving up
-constexpr unsigned DC_COPY = 8192;              // bytes per bulk copy (one per lane of warp 0)
+constexpr unsigned long long DC_WAIT_NS = 10000000ull;  // 10 ms of global time before giving up
+constexpr long long DC_WAIT_POLLS = 1ll << 26;              // and a poll count as a second bound
+constexpr unsigned DC_COPY = 8192;                           // bytes per bulk copy (one per lane of warp 0)
+// Every copy is issued by a lane of warp 0, the warp whose thread 0 set up the
+// barrier (only a warp barrier lies between the two).
+static_assert(4 * DC_APB * (5 + NMS_DECODE_MAX_CLASSES) <= 32 * DC_COPY,
+              "a block's rows take at most 32 bulk copies");
 
-// Bounded wait for phase 0 of the barrier at shared address sb.
+__device__ __forceinline__ unsigned long long dc_now()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for phase 0 of the barrier at shared address sb: at most
+// DC_WAIT_NS nanoseconds of the global timer (and DC_WAIT_POLLS polls).
 __device__ __forceinline__ bool dc_wait(unsigned sb)
 {
-    for (long long k = 0; k < DC_WAIT_LIMIT; ++k) {
+    const unsigned long long t0 = dc_now();
+    for (long long k = 0; k < DC_WAIT_POLLS; ++k) {
         unsigned ok;
         asm volatile(
             "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n"
@@ -95,6 +109,7 @@ __device__ __forceinline__ bool dc_wait(unsigned sb)
             : "r"(sb)
             : "memory");
         if (ok) return true;
+        if ((k & 15) == 15 && dc_now() - t0 > DC_WAIT_NS) break;
     }
     return false;
 }
@@ -120,7 +135,10 @@ decode_kernel(const float* __restrict__ preds, int anchors, int C, float conf_th
         // block's rows in flight at once, issued by a few lanes.  Thread 0
         // waits on the barrier (bounded) and the CTA barrier passes the rows
         // on; on a wait that gives up, the status says so, the copies still
-        // in flight are waited for once more and the block writes nothing.
+        // in flight are waited for once more (bounded too) and the block
+        // writes nothing.  If that second wait gives up as well, copies may
+        // still be landing in the block's shared memory as it exits; the
+        // call's buffers are then invalid, which NMS_ERR_TIMEOUT reports.
         const unsigned sb = static_cast<unsigned>(__cvta_generic_to_shared(&bar));
         const unsigned bytes = 4u * static_cast<unsigned>(nf);
         if (threadIdx.x == 0) {

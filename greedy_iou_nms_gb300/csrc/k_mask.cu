@@ -508,7 +508,7 @@ void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const
     cfg.stream = st;
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_attr_count();
     cudaLaunchKernelEx(&cfg, iou_mask_kernel, boxes_s, m_dev, m_bound, p, mask, ldw,
                        reinterpret_cast<unsigned long long*>(rowbits), NB, edges, ecount, ecap,
                        reinterpret_cast<unsigned long long*>(haspred), hi, static_cast<long long>(u0),

@@ -483,6 +483,11 @@ matrix_decide_kernel(const float* __restrict__ scores, const int* __restrict__ p
             fs = f;
             keep_j = !(f < decay_thr);
         } else {
+            // The same binary64 comparison as the definition's evaluation on
+            // the host, with CUDA's binary64 exp (at most 1 ulp from e^x) in
+            // place of the C library's: the two can only disagree on a box
+            // whose binary64 final score lies within about 2 ulp of the
+            // threshold (a band of relative width 2^-51).
             const double fd = static_cast<double>(s) * exp(x);
             fs = static_cast<float>(fd);
             keep_j = !(fd < static_cast<double>(decay_thr));

@@ -1031,7 +1031,7 @@ void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* ro
     cfg.stream = st;
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl_attr_count();
     cudaLaunchKernelEx(&cfg, resolve_single_kernel, mask, ldw, rowbits, NB, edges, ecount, ecap,
                        reinterpret_cast<const uint32_t*>(haspred), m_dev, m_bound, perm, max_out, keep, counts,
                        status, limit, done_in, done_out, grid_done);

@@ -171,14 +171,19 @@ nms_status nms_iou_mask(const float* boxes_sorted, int64_t n, float iou_thr,
  *   perm     device int32 [n]: input index of each sorted position, or NULL
  *            (the output is then the kept sorted positions themselves).
  *   max_out  cap on the number of outputs; <= 0 means none.
- *   keep     device int64 [min(n, max_out) or n]: kept entries in order.
- *   count    device int64 [1]: number of kept entries.
+ *   perm is 4-byte aligned when given.
+ *   keep     device int64 [min(n, max_out) or n], 8-byte aligned: kept
+ *            entries in order.
+ *   count    device int64 [1], 8-byte aligned: number of kept entries.
  *   workspace device scratch of >= nms_workspace_size(n, 0, 0) bytes,
- *            256-byte aligned (the column view of the blocks near the
- *            diagonal is rebuilt there from the mask).
- * Errors: NMS_ERR_INVALID_ARG (NULL or unaligned pointers with n > 0, n < 0),
- *         NMS_ERR_CAPACITY (n > NMS_MAX_SINGLE_N), NMS_ERR_WORKSPACE,
- *         NMS_ERR_CUDA.
+ *            256-byte aligned.  It is checked and reserved for the resolve,
+ *            which at present keeps all its state (the removed-bitmap and
+ *            the column view of the blocks near the diagonal, rebuilt from
+ *            the mask) in the shared memory of its thread block and does not
+ *            touch it.
+ * Errors: NMS_ERR_INVALID_ARG (NULL or unaligned pointers with n > 0, an
+ *         unaligned count, n < 0), NMS_ERR_CAPACITY (n > NMS_MAX_SINGLE_N),
+ *         NMS_ERR_WORKSPACE, NMS_ERR_CUDA.
  */
 nms_status nms_resolve_mask(const uint64_t* mask, int64_t n, const int32_t* perm,
                             int32_t max_out, int64_t* keep, int64_t* count,
@@ -340,8 +345,8 @@ nms_status nms_boxes7_run(float* buffers, int32_t batch, int32_t max_objects, in
  * whose memory is planned at start-up, a deployment that bans allocation
  * after initialisation).
  *
- *   mask, perm, max_out, keep, count: as for nms_resolve_mask; n must be
- *            <= NMS_NOALLOC_MAX_N.
+ *   mask, perm, max_out, keep, count: as for nms_resolve_mask (with the
+ *            same alignment); n must be <= NMS_NOALLOC_MAX_N.
  * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
  * routine) and holds nothing between calls, so calls on any streams, host
  * threads or devices may overlap.

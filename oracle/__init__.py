@@ -27,6 +27,13 @@ CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-s
 
 _lib = None
 
+# The multi-core bitmask baseline (cpu_baseline.c): its own library, built with
+# OpenMP; bench.py's CPU-baseline leg and its pin tests use it.
+_BASE_SRC = os.path.join(_HERE, "cpu_baseline.c")
+_BASE_LIB = os.path.join(_HERE, "_build", "libcpubase.so")
+BASE_CFLAGS = ["-O3", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+_base = None
+
 
 def build(force: bool = False) -> str:
     """Compile the oracle shared library with gcc (idempotent)."""
@@ -57,6 +64,10 @@ def _load():
         lib.oracle_matrix_nms.argtypes = [f32p, f32p, ctypes.c_int64, ctypes.c_float, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_float, ctypes.c_float, ctypes.c_int32, i64p, f32p]
         lib.oracle_matrix_nms.restype = ctypes.c_int64
+        lib.oracle_matrix_decide_at.argtypes = [f32p, f32p, ctypes.c_int64, ctypes.c_float, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_float, ctypes.c_float, i64p,
+                                                ctypes.c_int64, i64p, ctypes.POINTER(ctypes.c_int32), f32p]
+        lib.oracle_matrix_decide_at.restype = ctypes.c_int64
         lib.oracle_score_order.argtypes = [f32p, i64p, ctypes.c_int64]
         lib.oracle_score_order.restype = None
         lib.oracle_mask.argtypes = [f32p, ctypes.c_int64, ctypes.c_float, u64p]
@@ -144,6 +155,30 @@ def matrix_nms(boxes, scores, decay_thr, *, sigma=0.5, decay="gaussian", score_t
     return keep[:k].copy(), fs[:k].copy()
 
 
+def matrix_decide_at(boxes, scores, decay_thr, positions, *, sigma=0.5, decay="gaussian", score_thr=None):
+    """Matrix NMS (no max_out) decided box by box at the given sorted
+    positions: (input indices there, kept flags, final scores as binary32)."""
+    if decay not in ("gaussian", "linear"):
+        raise ValueError("matrix_decide_at: decay must be 'gaussian' or 'linear'")
+    bx = np.ascontiguousarray(boxes, dtype=np.float32).reshape(-1, 4)
+    sc = np.ascontiguousarray(scores, dtype=np.float32).reshape(-1)
+    pos = np.ascontiguousarray(positions, dtype=np.int64).reshape(-1)
+    k = pos.shape[0]
+    idx = np.zeros(max(k, 1), dtype=np.int64)
+    kept = np.zeros(max(k, 1), dtype=np.int32)
+    fs = np.zeros(max(k, 1), dtype=np.float32)
+    m = _load().oracle_matrix_decide_at(_ptr(bx, ctypes.c_float), _ptr(sc, ctypes.c_float), sc.shape[0],
+                                        float(np.float32(sigma)), 1 if decay == "linear" else 0,
+                                        0 if score_thr is None else 1,
+                                        float(np.float32(score_thr if score_thr is not None else 0.0)),
+                                        float(np.float32(decay_thr)), _ptr(pos, ctypes.c_int64), k,
+                                        _ptr(idx, ctypes.c_int64), _ptr(kept, ctypes.c_int32),
+                                        _ptr(fs, ctypes.c_float))
+    if m < 0:
+        raise ValueError("oracle_matrix_decide_at: invalid arguments")
+    return idx[:k].copy(), kept[:k].astype(bool), fs[:k].copy()
+
+
 def mask(boxes_sorted, iou_thr) -> np.ndarray:
     """Row-major [n][ceil(n/64)] uint64 suppression bitmask of score-sorted boxes."""
     bx = np.ascontiguousarray(boxes_sorted, dtype=np.float32).reshape(-1, 4)
@@ -187,3 +222,56 @@ def boxes7_nms(buffers, iou_thr, *, fast=False) -> np.ndarray:
         rows[:, 6] = flags
         out[b, 1:1 + 7 * m] = rows.reshape(-1)
     return out
+
+
+def build_cpu_baseline(force: bool = False) -> str:
+    """Compile the multi-core CPU baseline with gcc and OpenMP (idempotent)."""
+    os.makedirs(os.path.dirname(_BASE_LIB), exist_ok=True)
+    if force or not os.path.exists(_BASE_LIB) or os.path.getmtime(_BASE_LIB) < os.path.getmtime(_BASE_SRC):
+        tmp = _BASE_LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", *BASE_CFLAGS, "-o", tmp, _BASE_SRC, "-lm"])
+        os.replace(tmp, _BASE_LIB)
+    return _BASE_LIB
+
+
+def _load_base():
+    global _base
+    if _base is None:
+        lib = ctypes.CDLL(build_cpu_baseline())
+        f32p = ctypes.POINTER(ctypes.c_float)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        lib.cpu_baseline_threads.restype = ctypes.c_int
+        lib.cpu_baseline_nms.argtypes = [f32p, f32p, ctypes.c_int64, i32p, i64p, ctypes.c_int32, ctypes.c_float,
+                                         ctypes.c_int, ctypes.c_float, ctypes.c_int32, i64p, i64p]
+        lib.cpu_baseline_nms.restype = ctypes.c_int64
+        _base = lib
+    return _base
+
+
+def cpu_baseline_threads() -> int:
+    """Threads the multi-core baseline runs on."""
+    return int(_load_base().cpu_baseline_threads())
+
+
+def cpu_baseline_nms(boxes, scores, iou_thr, *, class_ids=None, batch_offsets=None, score_thr=None, max_out=0):
+    """Greedy NMS on all host cores (bitmask and resolve, cpu_baseline.c):
+    (keep, counts) laid out as for nms()."""
+    bx = np.ascontiguousarray(boxes, dtype=np.float32).reshape(-1, 4)
+    sc = np.ascontiguousarray(scores, dtype=np.float32).reshape(-1)
+    n = sc.shape[0]
+    cls = None if class_ids is None else np.ascontiguousarray(class_ids, dtype=np.int32)
+    off = None if batch_offsets is None else np.ascontiguousarray(batch_offsets, dtype=np.int64)
+    B = 1 if off is None else off.shape[0] - 1
+    cap = B * max_out if max_out > 0 else n  # the layout of nms()
+    keep = np.full(max(cap, 1), -1, dtype=np.int64)
+    counts = np.zeros(max(B, 1), dtype=np.int64)
+    tot = _load_base().cpu_baseline_nms(_ptr(bx, ctypes.c_float), _ptr(sc, ctypes.c_float), n,
+                                        None if cls is None else _ptr(cls, ctypes.c_int32),
+                                        None if off is None else _ptr(off, ctypes.c_int64), B,
+                                        float(np.float32(iou_thr)), 0 if score_thr is None else 1,
+                                        float(np.float32(score_thr if score_thr is not None else 0.0)),
+                                        int(max_out), _ptr(keep, ctypes.c_int64), _ptr(counts, ctypes.c_int64))
+    if tot < 0:
+        raise ValueError("cpu_baseline_nms: invalid arguments")
+    return keep, counts

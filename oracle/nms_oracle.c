@@ -282,6 +282,70 @@ int64_t oracle_matrix_nms(const float* boxes, const float* scores, int64_t n, fl
 }
 
 /*
+ * Matrix NMS decisions at chosen sorted positions, for images too large for
+ * oracle_matrix_nms to finish in a test.  Same definition, evaluated box by
+ * box: without max_out every box is decided on its own (its final score
+ * depends only on its fathers and theirs, never on another decision).
+ *
+ * For the box at sorted position p (positions[k], among the m candidates
+ * that pass the pre-filter, in the order of oracle_score_order):
+ *   final = s[j] * min over fathers q < p of the decay of (O[q][p], O_max[q]),
+ * kept when final >= t, exactly as oracle_matrix_nms computes them.  A father
+ * with O[q][p] = 0 gives the Gaussian decay exp(O_max[q]^2 / sigma) >= 1 and
+ * the linear decay 1 / (1 - O_max[q]) >= 1 (or +inf), and a NaN overlap a NaN
+ * decay; none of them can lower the minimum, which starts at 1, so only the
+ * fathers with O[q][p] > 0 are visited, and O_max[q] is computed for those
+ * alone (the largest overlap of box q with its own fathers, as above).  The
+ * result is the same value bit for bit.
+ *
+ * Out, per requested position: index[k] the input index there, kept[k] 0 or
+ * 1, final_scores[k] the final score rounded to binary32.  Returns m, or -1
+ * on invalid arguments (a position outside [0, m)).
+ */
+int64_t oracle_matrix_decide_at(const float* boxes, const float* scores, int64_t n, float sigma, int linear,
+                                int use_score_thr, float score_thr, float decay_thr, const int64_t* positions,
+                                int64_t npos, int64_t* index, int32_t* kept, float* final_scores)
+{
+    if (n < 0 || npos < 0) return -1;
+    int64_t* order = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    if (!order) return -1;
+    int64_t m = 0;
+    for (int64_t i = 0; i < n; ++i)
+        if (!use_score_thr || scores[i] > score_thr) order[m++] = i;
+    oracle_score_order(scores, order, m);
+    for (int64_t k = 0; k < npos; ++k) {
+        const int64_t p = positions[k];
+        if (p < 0 || p >= m) { free(order); return -1; }
+        const float* bp = boxes + 4 * order[p];
+        double dmin = 1.0;
+        for (int64_t q = 0; q < p; ++q) {
+            const float* bq = boxes + 4 * order[q];
+            float o = oracle_iou(bq, bp);
+            if (!(o > 0.0f)) continue;
+            float omax = 0.0f;  /* O_max of father q */
+            for (int64_t r = 0; r < q; ++r) {
+                float oq = oracle_iou(boxes + 4 * order[r], bq);
+                if (oq > omax) omax = oq;
+            }
+            double d;
+            if (linear) {
+                d = (1.0 - (double)o) / (1.0 - (double)omax);
+            } else {
+                double x = ((double)omax * (double)omax - (double)o * (double)o) / (double)sigma;
+                d = exp(x);
+            }
+            if (d < dmin) dmin = d;
+        }
+        double fs = (double)scores[order[p]] * dmin;
+        index[k] = order[p];
+        kept[k] = fs < (double)decay_thr ? 0 : 1;
+        final_scores[k] = (float)fs;
+    }
+    free(order);
+    return m;
+}
+
+/*
  * Suppression bitmask of boxes that are already in score order, as the pages
  * define it ("NMS CUDA代码学习", section Phase 1): bit (j mod 64) of word
  * j/64 in row i is set iff j > i and IoU(i, j) > thr.  Row-major [n][W]

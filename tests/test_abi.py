@@ -148,6 +148,19 @@ def test_mask_entry_validation(lib):
     assert g.nms_iou_mask(0, 0, 0.5, 0, 0, 0) == g.NMS_OK
 
 
+def test_resolve_entries_reject_misaligned_pointers(lib):
+    """Both resolve entry points refuse, on the host, a count or keep that is
+    not 8-byte aligned and a perm that is not 4-byte aligned (the resolve
+    stores int64 and loads int32 there)."""
+    ws = 1 << 20  # 256-byte aligned fake device address, never dereferenced
+    big = 1 << 40
+    for perm, keep, count in ((FAKE + 2, FAKE, FAKE), (FAKE, FAKE + 4, FAKE), (FAKE, FAKE, FAKE + 4), (0, FAKE, FAKE + 1)):
+        assert g.nms_resolve_mask(FAKE, 100, perm, 0, keep, count, ws, big, 0) == g.NMS_ERR_INVALID_ARG
+        assert g.nms_resolve_mask_noalloc(FAKE, 100, perm, 0, keep, count, 0) == g.NMS_ERR_INVALID_ARG
+    assert g.nms_resolve_mask(FAKE + 8, 100, 0, 0, FAKE, FAKE, ws, big, 0) == g.NMS_ERR_INVALID_ARG
+    assert g.nms_resolve_mask_noalloc(FAKE + 8, 100, 0, 0, FAKE, FAKE, 0) == g.NMS_ERR_INVALID_ARG
+
+
 def test_no_cpu_fallback_when_library_missing(monkeypatch):
     monkeypatch.setattr(g, "_lib", None)
     monkeypatch.setattr(g, "LIB_PATH", "/nonexistent/libgbnms.so")

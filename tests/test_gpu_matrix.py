@@ -186,3 +186,48 @@ def test_linear_identical_boxes():
     s = np.linspace(1.0, 0.2, 200).astype(np.float32)
     _check_linear(b, s, 0.0)
     _check_linear(b, s, 1e-30)
+
+
+# ------------------------------------------------ the benchmark's full sizes
+
+@pytest.mark.parametrize("name,nrand", [("stress_n65536_dense", 96), ("stress_n65536_sparse", 384)])
+@pytest.mark.parametrize("decay", ["gaussian", "linear"])
+def test_full_size_sampled(name, nrand, decay):
+    """The 65536-box stress images at the benchmark's threshold (t = 0.1):
+    the whole output satisfies what holds at any size (kept boxes in score
+    order, final scores in [t, score]); sampled positions are checked one by
+    one against the oracle's box-by-box form: random positions, the first
+    boxes and the kept boxes closest to t.  Kept or not must agree; a kept
+    box's final score is within 4 ulp (Gaussian) or exact (linear)."""
+    t = 0.1
+    wl = W.make(name, 0)
+    n = wl.n
+    k, fs = g.matrix_nms(torch.from_numpy(wl.boxes).cuda(), torch.from_numpy(wl.scores).cuda(), t, decay=decay)
+    k = k.cpu().numpy()
+    fs = fs.cpu().numpy()
+    order = oracle.score_order(wl.scores)
+    pos_of = np.empty(n, np.int64)
+    pos_of[order] = np.arange(n)
+    kp = pos_of[k]
+    assert np.all(np.diff(kp) > 0)
+    assert np.all(fs >= np.float32(t)) and np.all(fs <= wl.scores[k])
+    rng = np.random.default_rng(5)
+    pos = np.unique(np.concatenate([rng.choice(n, nrand, replace=False), np.arange(16),
+                                    kp[np.argsort(fs, kind="stable")[:32]]]))
+    idx, kept, efs = oracle.matrix_decide_at(wl.boxes, wl.scores, t, pos, decay=decay)
+    assert np.isin(idx, k).tolist() == kept.tolist()
+    got = dict(zip(k.tolist(), fs.tolist()))
+    g_fs = np.array([got[i] for i in idx[kept].tolist()], np.float64)
+    e_fs = efs[kept].astype(np.float64)
+    if decay == "linear":
+        assert g_fs.tolist() == e_fs.tolist()
+    else:
+        ulp = np.spacing(np.abs(efs[kept])).astype(np.float64)
+        assert np.all(np.abs(g_fs - e_fs) <= 4 * ulp)
+
+
+def test_gaussian_maxout_config():
+    """The 32768-box image with max_out 1000 (Gaussian, t = 0.1) against the
+    whole-image oracle."""
+    wl = W.make("single_n32768_maxout1000", 0)
+    _check(wl.boxes, wl.scores, 0.1, max_out=wl.max_out)

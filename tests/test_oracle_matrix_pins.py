@@ -208,3 +208,73 @@ def test_linear_exists_restatement(seed):
         if not drop:
             kept.append(int(order[p]))
     assert keep.tolist() == kept
+
+
+# ------------------------------------------ box-by-box form (large images)
+
+def _decide_all(b, s, t, **kw):
+    pos = np.arange(len(s) if kw.get("score_thr") is None else int((np.asarray(s) > kw["score_thr"]).sum()))
+    idx, kept, fs = oracle.matrix_decide_at(b, s, t, pos, **kw)
+    return idx[kept], fs[kept]
+
+
+@pytest.mark.parametrize("sigma", [0.5, 2.0])
+def test_decide_at_closed_forms(sigma):
+    """The box-by-box form on the closed forms above: the pair at IoU exactly
+    1/2 decays by exp(-0.25/sigma) (Gaussian) and by exactly 1/2 (linear);
+    disjoint boxes keep their scores; identical boxes decay by exp(-2) after
+    the first (sigma 1/2)."""
+    b = np.array([[0, 0, 4, 4], [0, 0, 4, 2]], np.float32)
+    s = np.array([0.9, 0.8], np.float32)
+    idx, kept, fs = oracle.matrix_decide_at(b, s, 0.0, [1, 0], sigma=sigma)
+    assert idx.tolist() == [1, 0] and kept.tolist() == [True, True]
+    assert fs[0] == np.float32(float(np.float32(0.8)) * math.exp(-0.25 / float(np.float32(sigma))))
+    assert fs[1] == np.float32(0.9)
+    idx, kept, fs = oracle.matrix_decide_at(b, s, 0.0, [1], decay="linear")
+    assert fs[0] == np.float32(0.4)
+    d = np.array([[0, 0, 1, 1], [5, 5, 6, 6], [10, 0, 11, 1], [0, 10, 1, 11]], np.float32)
+    sd = np.array([0.9, 0.2, 0.6, 0.4], np.float32)
+    idx, kept, fs = oracle.matrix_decide_at(d, sd, 0.3, [0, 1, 2, 3])
+    assert idx.tolist() == [0, 2, 3, 1] and kept.tolist() == [True, True, True, False]
+    assert fs.tolist() == sd[[0, 2, 3, 1]].tolist()
+    k = 6
+    same = np.tile(np.array([[3, 3, 9, 7]], np.float32), (k, 1))
+    ss = np.linspace(0.9, 0.4, k).astype(np.float32)
+    idx, kept, fs = oracle.matrix_decide_at(same, ss, 0.0, np.arange(k))
+    assert fs[0] == ss[0]
+    assert all(fs[j] == np.float32(float(ss[j]) * math.exp(-2.0)) for j in range(1, k))
+
+
+def test_decide_at_chain_hand_worked():
+    """The three-box chain: c's decay is min(exp(-2 (1/4)^2), exp(0)) from
+    fathers a and b, b's exp(-2 (7/13)^2)."""
+    b = np.array([[0, 0, 10, 1], [3, 0, 13, 1], [6, 0, 16, 1]], np.float32)
+    s = np.array([0.9, 0.8, 0.7], np.float32)
+    _, _, fs = oracle.matrix_decide_at(b, s, 0.0, [0, 1, 2])
+    r = float(Fraction(7, 13))
+    # within 2e-7: the binary32 IoU of 7/13 is not 7/13 itself
+    assert abs(fs[1] - float(s[1]) * math.exp(-2 * r * r)) <= 2e-7
+    assert abs(fs[2] - float(s[2]) * math.exp(-2 * 0.0625)) <= 2e-7
+    assert fs[0] == np.float32(0.9)
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("decay", ["gaussian", "linear"])
+def test_decide_at_matches_whole_image(seed, decay):
+    """On clustered images with identical boxes, NaN boxes, a pre-filter and
+    two thresholds, the box-by-box form keeps exactly the boxes the whole-image
+    evaluation keeps, with the same final scores bit for bit."""
+    rng = np.random.default_rng(seed)
+    n = 300
+    c = rng.uniform(0, 200, (12, 2))[rng.integers(0, 12, n)] + rng.normal(0, 4, (n, 2))
+    wh = rng.uniform(5, 30, (n, 2))
+    b = np.concatenate([c - wh / 2, c + wh / 2], 1).astype(np.float32)
+    b[::23] = b[0]
+    b[5] = np.nan
+    s = rng.uniform(0, 1, n).astype(np.float32)
+    for t in (0.05, 0.3):
+        for thr in (None, 0.4):
+            k, fs = oracle.matrix_nms(b, s, t, decay=decay, score_thr=thr)
+            k2, fs2 = _decide_all(b, s, t, decay=decay, score_thr=thr)
+            assert k2.tolist() == k.tolist()
+            assert fs2.tobytes() == fs.tobytes()

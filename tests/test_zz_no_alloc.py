@@ -3,12 +3,15 @@
 nms_resolve_mask_noalloc serves callers that cannot allocate device memory
 where they run NMS (a plugin whose host framework owns all allocations, a
 real-time loop with memory planned at start-up, a deployment that bans
-allocation after initialisation).  Its scratch lives in a device array the
-library holds, so this test checks that two calls in a row through the C ABI
-give exactly the keep list and count of nms_resolve_mask, which uses a
-caller-provided workspace.  Keep indices are integers, so the comparison is
-exact, as in the other parity tests.  This file is collected last so that a
-run stopping at the first failure has already run every other test.
+allocation after initialisation).  It keeps all its state in the shared
+memory of its one thread block and holds nothing between calls.  Two calls in
+a row through the C ABI, on different masks, must each give exactly the keep
+list and count of nms_resolve_mask (the workspace entry point, which today
+runs the same resolve and leaves its workspace untouched) and, the check that
+counts, of the oracle: calls in a row must be independent.  Keep indices are
+integers, so the comparisons are exact, as in the other parity tests.  This
+file is collected last so that a run stopping at the first failure has
+already run every other test.
 """
 import numpy as np
 import pytest
@@ -43,7 +46,7 @@ def test_noalloc_matches_workspace_entry_point_twice(n, span, max_out):
         pytest.skip("no CUDA device")
     g.build()
     g.load()
-    for call in range(2):  # two calls in a row share the library-held scratch
+    for call in range(2):  # two calls in a row, on different masks, are independent
         b = _sorted_boxes(n, 10 * n + call, span)
         m = g.iou_mask(torch.from_numpy(b).cuda(), 0.5)
         ref = g.resolve_mask(m, max_out=max_out).cpu().numpy()

@@ -198,3 +198,50 @@ HEADLINE = "single_n8192"
 
 def make(name: str, seed: int = 0) -> Workload:
     return CONFIGS[name](seed)
+
+
+# ------------------------------------------------------------ lane candidates
+
+LANE_VALUES = 77  # two class scores, start row, start x, length, 72 x samples
+LANE_ROWS = 72
+
+
+def lanes(seed: int = 0, n: int = 1000, true_lanes: int = 4, width: float = 640.0):
+    """Lane candidates of one road image, shaped like an anchor-based lane
+    detector's output before NMS: (props float32 [n, 77], scores float32 [n]).
+
+    Four true lanes x(r) = x0 + a r + b r^2 over the 72 sample rows (r = 0 at
+    the top), x0 ~ U(0.15, 0.85) width, a ~ U(-3, 3), b ~ U(-0.02, 0.02).  85%
+    of the candidates follow a true lane (a whole-lane shift N(0, 12) px and
+    per-row noise N(0, 2) px), the rest are random straight lanes; every
+    candidate has a start row U{0..47} and a length U{16..72 - start}; x is
+    quantised to 1/16 px.  The two class scores are (1 - s, s) with s, the
+    score passed beside the candidates, ~ Beta(4, 2) for lane followers and
+    Beta(1, 4) for the random ones.  Values 0, 1, 2, 3, 4: class scores,
+    start row, x at the start row, length."""
+    rng = _rng(seed)
+    r = np.arange(LANE_ROWS, dtype=np.float64)
+    x0 = rng.uniform(0.15, 0.85, true_lanes) * width
+    a = rng.uniform(-3.0, 3.0, true_lanes)
+    b = rng.uniform(-0.02, 0.02, true_lanes)
+    follow = rng.uniform(0, 1, n) < 0.85
+    which = rng.integers(0, true_lanes, n)
+    shift = rng.normal(0, 12.0, n)
+    noise = rng.normal(0, 2.0, (n, LANE_ROWS))
+    rx0 = rng.uniform(0, width, n)
+    ra = rng.uniform(-6.0, 6.0, n)
+    x = np.where(follow[:, None],
+                 x0[which, None] + a[which, None] * r + b[which, None] * r * r + shift[:, None] + noise,
+                 rx0[:, None] + ra[:, None] * r)
+    x = np.round(x * 16.0) / 16.0
+    start = rng.integers(0, 48, n)
+    length = np.array([rng.integers(16, LANE_ROWS - s + 1) for s in start])
+    s = np.where(follow, rng.beta(4, 2, n), rng.beta(1, 4, n))
+    props = np.zeros((n, LANE_VALUES), dtype=np.float64)
+    props[:, 0] = 1 - s
+    props[:, 1] = s
+    props[:, 2] = start
+    props[:, 3] = x[np.arange(n), start]
+    props[:, 4] = length
+    props[:, 5:] = x
+    return props.astype(np.float32), s.astype(np.float32)

@@ -68,6 +68,10 @@ def _load():
                                                 ctypes.c_int, ctypes.c_float, ctypes.c_float, i64p,
                                                 ctypes.c_int64, i64p, ctypes.POINTER(ctypes.c_int32), f32p]
         lib.oracle_matrix_decide_at.restype = ctypes.c_int64
+        lib.oracle_lane_distance.argtypes = [f32p, f32p]
+        lib.oracle_lane_distance.restype = ctypes.c_float
+        lib.oracle_lane_nms.argtypes = [f32p, f32p, ctypes.c_int64, ctypes.c_float, ctypes.c_int32, i64p]
+        lib.oracle_lane_nms.restype = ctypes.c_int64
         lib.oracle_score_order.argtypes = [f32p, i64p, ctypes.c_int64]
         lib.oracle_score_order.restype = None
         lib.oracle_mask.argtypes = [f32p, ctypes.c_int64, ctypes.c_float, u64p]
@@ -177,6 +181,32 @@ def matrix_decide_at(boxes, scores, decay_thr, positions, *, sigma=0.5, decay="g
     if m < 0:
         raise ValueError("oracle_matrix_decide_at: invalid arguments")
     return idx[:k].copy(), kept[:k].astype(bool), fs[:k].copy()
+
+
+LANE_VALUES = 77  # values of one lane candidate (see oracle_lane_nms)
+LANE_ROWS = 72
+
+
+def lane_distance(a, b) -> np.float32:
+    """Distance of two lane candidates (77 values each): mean |x_a - x_b| over
+    the rows both cover, +inf without common rows."""
+    a = np.ascontiguousarray(a, dtype=np.float32).reshape(LANE_VALUES)
+    b = np.ascontiguousarray(b, dtype=np.float32).reshape(LANE_VALUES)
+    return np.float32(_load().oracle_lane_distance(_ptr(a, ctypes.c_float), _ptr(b, ctypes.c_float)))
+
+
+def lane_nms(props, scores, thr, *, max_out=0) -> np.ndarray:
+    """Greedy NMS of lane candidates [n, 77]: kept input indices in score
+    order (a lane goes when its distance to a kept lane is below thr)."""
+    pr = np.ascontiguousarray(props, dtype=np.float32).reshape(-1, LANE_VALUES)
+    sc = np.ascontiguousarray(scores, dtype=np.float32).reshape(-1)
+    n = sc.shape[0]
+    keep = np.full(max(n, 1), -1, dtype=np.int64)
+    k = _load().oracle_lane_nms(_ptr(pr, ctypes.c_float), _ptr(sc, ctypes.c_float), n, float(np.float32(thr)),
+                                int(max_out), _ptr(keep, ctypes.c_int64))
+    if k < 0:
+        raise ValueError("oracle_lane_nms: invalid arguments")
+    return keep[:k].copy()
 
 
 def mask(boxes_sorted, iou_thr) -> np.ndarray:

@@ -346,6 +346,84 @@ int64_t oracle_matrix_decide_at(const float* boxes, const float* scores, int64_t
 }
 
 /*
+ * Lane-proposal NMS ("nms_kernel.cu 파일 분석 -2"): the same greedy NMS over
+ * lane candidates instead of boxes.  The page gives: a candidate holds
+ * PROP_SIZE = 77 values; candidates are visited in score order through idx
+ * (the sorted order), each compared with every later one; the comparison is
+ * symmetric ("A against B is the same as B against A, because it compares by
+ * absolute value"); nms_overlap_thresh is the threshold that decides whether
+ * two lanes are alike.  The page stops before the comparison itself.
+ *
+ * Readings taken:
+ *   - the 77 values: two class scores, the start row, the start x, the
+ *     length (in rows), then the lane's x at 72 fixed image rows, row 0
+ *     first (the distance uses only the start row, the length and the x's;
+ *     the NMS order comes from the scores passed beside the candidates);
+ *   - a lane's rows are [floor(start), floor(start) + floor(length)) clipped
+ *     to [0, 72); a NaN, infinite or larger than 2^20 start or length gives
+ *     no rows;
+ *   - the distance of two lanes: over the rows both cover, the sum of
+ *     |x_a - x_b| in binary32, added row by row from the lowest row, then
+ *     divided by the number of those rows (binary32, round to nearest); no
+ *     common row gives +inf;
+ *   - a later lane is suppressed when its distance to a kept lane is
+ *     strictly below the threshold (a NaN distance never suppresses).
+ * Order, ties, max_out and the output are those of greedy NMS above.
+ */
+#define LANE_VALUES 77
+#define LANE_ROWS 72
+#define LANE_X0 5
+
+static void lane_rows(const float* p, int* lo, int* hi)
+{
+    const float s = p[2], l = p[4];
+    *lo = 0;
+    *hi = 0;
+    if (!(s >= -1048576.0f && s <= 1048576.0f && l >= -1048576.0f && l <= 1048576.0f)) return;
+    int a = (int)floorf(s);
+    int b = a + (int)floorf(l);
+    if (a < 0) a = 0;
+    if (b > LANE_ROWS) b = LANE_ROWS;
+    if (b > a) {
+        *lo = a;
+        *hi = b;
+    }
+}
+
+float oracle_lane_distance(const float* a, const float* b)
+{
+    int la, ha, lb, hb;
+    lane_rows(a, &la, &ha);
+    lane_rows(b, &lb, &hb);
+    const int lo = la > lb ? la : lb, hi = ha < hb ? ha : hb;
+    if (hi <= lo) return INFINITY;
+    float sum = 0.0f;
+    for (int k = lo; k < hi; ++k) sum = sum + fabsf(a[LANE_X0 + k] - b[LANE_X0 + k]);
+    return sum / (float)(hi - lo);
+}
+
+int64_t oracle_lane_nms(const float* props, const float* scores, int64_t n, float thr, int32_t max_out,
+                        int64_t* keep)
+{
+    if (n < 0) return -1;
+    int64_t* order = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    if (!order) return -1;
+    for (int64_t i = 0; i < n; ++i) order[i] = i;
+    oracle_score_order(scores, order, n);
+    int64_t nk = 0;
+    for (int64_t p = 0; p < n; ++p) {
+        if (max_out > 0 && nk == max_out) break;
+        const float* cand = props + LANE_VALUES * order[p];
+        int suppressed = 0;
+        for (int64_t k = 0; k < nk && !suppressed; ++k)
+            if (oracle_lane_distance(props + LANE_VALUES * keep[k], cand) < thr) suppressed = 1;
+        if (!suppressed) keep[nk++] = order[p];
+    }
+    free(order);
+    return nk;
+}
+
+/*
  * Suppression bitmask of boxes that are already in score order, as the pages
  * define it ("NMS CUDA代码学习", section Phase 1): bit (j mod 64) of word
  * j/64 in row i is set iff j > i and IoU(i, j) > thr.  Row-major [n][W]

@@ -33,8 +33,12 @@ NMS_MAX_SINGLE_N = 1 << 18
 EXPORTED = ("nms_status_string", "nms_workspace_size", "nms_run", "nms_fast_run", "nms_run_timed",
             "nms_matrix_workspace_size", "nms_matrix_run", "nms_mask_row_words", "nms_iou_mask",
             "nms_resolve_mask", "nms_resolve_mask_noalloc", "nms_decode_workspace_size", "nms_decode_boxes7",
-            "nms_boxes7_workspace_size", "nms_boxes7_run", "nms_mapped_pointer")
+            "nms_boxes7_workspace_size", "nms_boxes7_run", "nms_mapped_pointer", "nms_lane_workspace_size",
+            "nms_lane_run")
 NMS_NOALLOC_MAX_N = 16384
+NMS_LANE_VALUES = 77  # values of one lane candidate (nms_lane_run)
+NMS_LANE_ROWS = 72
+NMS_LANE_MAX_N = 16384
 NMS_DECODE_MAX_ANCHORS = 1 << 20
 NMS_DECODE_MAX_CLASSES = 384
 NMS_DECODE_MAX_BATCH = 65535
@@ -96,6 +100,10 @@ def load():
     lib.nms_boxes7_run.restype = ctypes.c_int
     lib.nms_mapped_pointer.argtypes = [vp, ctypes.POINTER(vp)]
     lib.nms_mapped_pointer.restype = ctypes.c_int
+    lib.nms_lane_workspace_size.argtypes = [i64, ctypes.POINTER(sz)]
+    lib.nms_lane_workspace_size.restype = ctypes.c_int
+    lib.nms_lane_run.argtypes = [vp, vp, i64, f32, i32, vp, i64, vp, vp, vp, sz, vp]
+    lib.nms_lane_run.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -167,6 +175,43 @@ def nms_matrix_run(boxes: int, scores: int, n: int, decay: int, sigma: float, sc
                                  float(decay_thr), int(max_out), keep or None, keep_scores or None,
                                  int(keep_cap), count or None, dev_status or None, workspace or None,
                                  int(workspace_bytes), stream or None)
+
+
+def nms_lane_workspace_size(n: int) -> int:
+    b = ctypes.c_size_t(0)
+    st = load().nms_lane_workspace_size(int(n), ctypes.byref(b))
+    if st != NMS_OK:
+        raise NmsError(st, "nms_lane_workspace_size")
+    return int(b.value)
+
+
+def nms_lane_run(props: int, scores: int, n: int, dist_thr: float, max_out: int, keep: int, keep_cap: int,
+                 count: int, dev_status: int, workspace: int, workspace_bytes: int, stream: int) -> int:
+    return load().nms_lane_run(props or None, scores or None, int(n), float(dist_thr), int(max_out), keep or None,
+                               int(keep_cap), count or None, dev_status or None, workspace or None,
+                               int(workspace_bytes), stream or None)
+
+
+def lane_nms(props, scores, dist_thr: float, *, max_out: int = 0):
+    """Greedy NMS of lane candidates (CUDA tensors props [n, 77], scores [n]):
+    int64 kept indices in score order.  Synchronises the current stream once."""
+    torch = _torch()
+    if not (props.is_cuda and scores.is_cuda):
+        raise ValueError("lane_nms: props and scores must be CUDA tensors")
+    props = props.contiguous()
+    scores = scores.contiguous()
+    n = scores.shape[0]
+    cap = max(keep_capacity(n, None, max_out), 1)
+    keep = torch.empty(cap, dtype=torch.int64, device=props.device)
+    count = torch.empty(1, dtype=torch.int64, device=props.device)
+    wsb = nms_lane_workspace_size(n)
+    ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=props.device)
+    st = nms_lane_run(props.data_ptr() if n else 0, scores.data_ptr() if n else 0, n, dist_thr, max_out,
+                      keep.data_ptr(), cap, count.data_ptr(), 0, ws.data_ptr(), wsb,
+                      torch.cuda.current_stream(props.device).cuda_stream)
+    if st != NMS_OK:
+        raise NmsError(st, "nms_lane_run")
+    return keep[: int(count.item())]
 
 
 def matrix_nms(boxes, scores, decay_thr: float, *, sigma: float = 0.5, decay: str = "gaussian",

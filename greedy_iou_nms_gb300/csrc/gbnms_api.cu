@@ -646,6 +646,79 @@ extern "C" nms_status nms_run_timed(const float* boxes, const float* scores, int
                     workspace_bytes, stream, sp);
 }
 
+namespace {
+
+struct LaneLayout {
+    SingleLayout s;
+    size_t xs, span, flag, total;
+};
+
+LaneLayout lane_layout(int64_t n)
+{
+    LaneLayout L;
+    L.s = single_layout(n);
+    Layout X;
+    X.total = L.s.total;
+    const size_t ld = static_cast<size_t>(lane_ld(static_cast<int>(n)));
+    L.xs = X.add(4 * static_cast<size_t>(NMS_LANE_ROWS) * ld);
+    L.span = X.add(4 * ld);
+    L.flag = X.add(4 * ld);
+    L.total = X.total;
+    return L;
+}
+
+}  // namespace
+
+extern "C" nms_status nms_lane_workspace_size(int64_t n, size_t* bytes)
+{
+    if (!bytes || n < 0) return NMS_ERR_INVALID_ARG;
+    if (n > NMS_LANE_MAX_N) return NMS_ERR_CAPACITY;
+    *bytes = lane_layout(n).total;
+    return NMS_OK;
+}
+
+extern "C" nms_status nms_lane_run(const float* props, const float* scores, int64_t n, float dist_thr,
+                                   int32_t max_out, int64_t* keep, int64_t keep_cap, int64_t* count,
+                                   int32_t* dev_status, void* workspace, size_t workspace_bytes, void* stream)
+{
+    if (n < 0 || std::isnan(dist_thr)) return NMS_ERR_INVALID_ARG;
+    if (n > NMS_LANE_MAX_N) return NMS_ERR_CAPACITY;
+    if (!count || !aligned(count, 8)) return NMS_ERR_INVALID_ARG;
+    if (n > 0 && (!props || !scores || !keep || !aligned(props, 4) || !aligned(scores, 4) || !aligned(keep, 8)))
+        return NMS_ERR_INVALID_ARG;
+    if (dev_status && !aligned(dev_status, 4)) return NMS_ERR_INVALID_ARG;
+    const int64_t need = max_out > 0 ? (n < max_out ? n : max_out) : n;
+    if (keep_cap < need) return NMS_ERR_CAPACITY;
+    const LaneLayout L = lane_layout(n);
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < L.total) return NMS_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();
+    int32_t* status = dev_status ? dev_status : at<int32_t>(workspace, L.s.status);
+    if (n == 0) {
+        cudaMemsetAsync(count, 0, sizeof(int64_t), st);
+        cudaMemsetAsync(status, 0, sizeof(int32_t), st);
+        return cuda_status();
+    }
+    const int nb = static_cast<int>(n);
+    int* perm = at<int>(workspace, L.s.perm);
+    uint64_t* mask = at<uint64_t>(workspace, L.s.mask);
+    uint64_t* rowbits = at<uint64_t>(workspace, L.s.rowbits);
+    uint64_t* haspred = at<uint64_t>(workspace, L.s.haspred);
+    uint32_t* edges = L.s.ecap ? at<uint32_t>(workspace, L.s.edges) : nullptr;
+    unsigned* ecount = at<unsigned>(workspace, L.s.ecount);
+    uint64_t* keys = sort_keys_bytes(nb) ? at<uint64_t>(workspace, L.s.keys) : nullptr;
+    // Sort only (no boxes to gather); it also zeroes the status, the pair
+    // count, the per-row chunk bits and the neighbour bitmap.
+    launch_sort(scores, nullptr, nullptr, nullptr, nb, perm, nullptr, keys, status, rowbits, L.s.NB, ecount,
+                haspred, nullptr, st);
+    launch_lane_mask(props, perm, nb, dist_thr, at<float>(workspace, L.xs), at<uint32_t>(workspace, L.span),
+                     at<uint32_t>(workspace, L.flag), mask, L.s.ldw, rowbits, L.s.NB, edges, ecount, L.s.lcap,
+                     L.s.ecap ? haspred : nullptr, st);
+    launch_resolve_single(mask, L.s.ldw, rowbits, L.s.NB, edges, ecount, L.s.ecap ? haspred : nullptr, nullptr, nb,
+                          perm, max_out, keep, count, status, st);
+    return cuda_status();
+}
+
 extern "C" nms_status nms_iou_mask(const float* boxes_sorted, int64_t n, float iou_thr,
                                    uint64_t* mask, int64_t mask_words, void* stream)
 {

@@ -65,6 +65,8 @@ void ensure_dynamic_smem(const void* kernel, size_t bytes);
 void launch_prefilter(const float* scores, int n, float score_thr, int* cand, int* m_count,
                       cudaStream_t st);
 size_t sort_keys_bytes(int m_bound);
+// Sort of the candidates' score keys into perm; with boxes, their boxes are
+// gathered into boxes_s in the same order (boxes may be NULL: perm only).
 void launch_sort(const float* scores, const float4* boxes, const int* cand, const int* m_dev,
                  int m_bound, int* perm, float4* boxes_s, uint64_t* keys, int32_t* status,
                  uint64_t* rowbits, int NB, unsigned* ecount, uint64_t* haspred, int* zero8, cudaStream_t st);
@@ -111,6 +113,14 @@ void launch_graph_grid(uint32_t* edges, const unsigned* ecount, const uint64_t* 
                        int m_bound, const int* perm, int max_out, int64_t* keep, int64_t* counts,
                        int32_t* status, cudaStream_t st, int limit, const int* done_in, int* done_out,
                        int* grid_done, uint64_t* state, void* ctl);
+
+// Lane candidates (k_lane.cu): the SoA stride for n lanes, and the gather
+// and mask launches over the sorted permutation (outputs in the layout of
+// launch_iou_mask).  xs: 72 x lane_ld(n) floats; span, flag: lane_ld(n) each.
+int lane_ld(int n);
+void launch_lane_mask(const float* props, const int* perm, int n, float thr, float* xs, uint32_t* span,
+                      uint32_t* flag, uint64_t* mask, int64_t ldw, uint64_t* rowbits, int NB, uint32_t* edges,
+                      unsigned* ecount, unsigned ecap, uint64_t* haspred, cudaStream_t st);
 
 // Fast NMS output of one image: the boxes whose bit in haspred is clear, in
 // sorted order, mapped through perm, cut at max_out.

@@ -1,0 +1,267 @@
+// Greedy NMS of lane candidates ("nms_kernel.cu 파일 분석 -2"): the page's
+// candidate holds PROP_SIZE = 77 values, candidates are compared in score
+// order through the sorted index, in 64-candidate tiles above the diagonal
+// (sections row_start/col_start and 중복 비교 제거), and the comparison is
+// symmetric, by absolute values, against a similarity threshold.  The page
+// stops before the comparison; the reading (include/gbnms.h, nms_lane_run):
+// two class scores, start row, start x, length and the x of 72 rows; a lane
+// covers rows [floor(start), floor(start) + floor(length)) within [0, 72);
+// the distance is the binary32 sum of |dx| over the common rows, lowest row
+// first, over their number; a later lane goes when it is below the
+// threshold.
+//
+// GB300 shape:
+//   gather: the sorted lanes' x as 72 rows of n floats (row-major, so a
+//           warp's lanes are contiguous), NaN in the rows a lane does not
+//           cover, its row span, and a flag for a lane with a non-finite x
+//           in a covered row;
+//   mask:   one CTA of 256 threads per 64 x 64 tile of the upper triangle;
+//           thread (q, r) holds row lane r's 72 x in registers and takes 16
+//           of the tile's 64 column lanes (staged in shared memory, negated,
+//           row by row) -- per row one add, one max and one add:
+//             acc += max(|x_r + (-x_c)|, 0)
+//           max(NaN, 0) is 0, so a row either lane does not cover adds +0,
+//           which leaves a non-negative sum unchanged: the sum is the
+//           definition's sum over the common rows in row order.  Pairs with
+//           a flagged lane take the definition's loop over the common rows
+//           on the original values instead.  The words, the per-row chunk
+//           bits, the neighbour bitmap and the pair list come out in the
+//           layout of the box mask kernel, so the resolve is the same;
+//   resolve: launch_resolve_single (rounds over the pair list, or the walk).
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gbnms {
+
+constexpr int LN_VALUES = NMS_LANE_VALUES;  // values of one candidate
+constexpr int LN_ROWS = NMS_LANE_ROWS;      // x samples of one candidate
+constexpr int LN_X0 = 5;                    // index of the first x sample
+constexpr int LN_TILE = 64;                 // rows and columns of a mask tile
+constexpr int LN_THREADS = 256;             // 64 row lanes x 4 column quarters
+constexpr int LN_QCOLS = LN_TILE / (LN_THREADS / LN_TILE);  // column lanes per thread (16)
+static_assert(LN_ROWS < 256, "a span packs two row indices into bytes");
+
+// Row span [lo, hi) of a candidate, packed as lo | hi << 8 (0 for none).
+__device__ __forceinline__ uint32_t lane_span(const float* __restrict__ p)
+{
+    const float s = p[2], l = p[4];
+    if (!(s >= -1048576.0f && s <= 1048576.0f && l >= -1048576.0f && l <= 1048576.0f)) return 0u;
+    int a = static_cast<int>(floorf(s));
+    int b = a + static_cast<int>(floorf(l));
+    a = max(a, 0);
+    b = min(b, LN_ROWS);
+    return b > a ? static_cast<uint32_t>(a) | (static_cast<uint32_t>(b) << 8) : 0u;
+}
+
+// The definition's distance, row by row over the common rows, on the
+// original values (pairs with a non-finite x in a covered row).
+__device__ float lane_distance_exact(const float* __restrict__ a, const float* __restrict__ b, uint32_t sa,
+                                     uint32_t sb)
+{
+    const int lo = max(static_cast<int>(sa & 255u), static_cast<int>(sb & 255u));
+    const int hi = min(static_cast<int>(sa >> 8), static_cast<int>(sb >> 8));
+    if (hi <= lo) return __int_as_float(0x7f800000);  // +inf: no common row
+    float sum = 0.0f;
+    for (int k = lo; k < hi; ++k) sum = __fadd_rn(sum, fabsf(__fsub_rn(a[LN_X0 + k], b[LN_X0 + k])));
+    return __fdiv_rn(sum, static_cast<float>(hi - lo));
+}
+
+// Sorted lanes to the mask kernel's layout: xs[k * ld + p] = x_k of the lane
+// at sorted position p (NaN where it does not cover row k), span[p], and
+// flag[p] = 1 when a covered row holds a non-finite x.
+__global__ void __launch_bounds__(256)
+lane_gather_kernel(const float* __restrict__ props, const int* __restrict__ perm, int n, int ld,
+                   float* __restrict__ xs, uint32_t* __restrict__ span, uint32_t* __restrict__ flag)
+{
+    pdl_wait();
+    pdl_release();
+    const int p = blockIdx.x * blockDim.x + threadIdx.x;
+    if (p >= ld) return;
+    if (p >= n) {  // padding lanes: no rows
+        for (int k = 0; k < LN_ROWS; ++k) xs[static_cast<int64_t>(k) * ld + p] = __int_as_float(0x7fc00000);
+        span[p] = 0u;
+        flag[p] = 0u;
+        return;
+    }
+    const float* src = props + static_cast<int64_t>(perm[p]) * LN_VALUES;
+    const uint32_t sp = lane_span(src);
+    const int lo = static_cast<int>(sp & 255u), hi = static_cast<int>(sp >> 8);
+    uint32_t bad = 0u;
+    for (int k = 0; k < LN_ROWS; ++k) {
+        const float x = src[LN_X0 + k];
+        const bool cov = k >= lo && k < hi;
+        if (cov && !(fabsf(x) <= 3.4028235e38f)) bad = 1u;
+        xs[static_cast<int64_t>(k) * ld + p] = cov ? x : __int_as_float(0x7fc00000);
+    }
+    span[p] = sp;
+    flag[p] = bad;
+}
+
+// Linear tile index -> (row tile a, column tile c), a <= c, column by column.
+__device__ __forceinline__ void lane_tile(int u, int& a, int& c)
+{
+    int cc = static_cast<int>((sqrtf(8.0f * static_cast<float>(u) + 1.0f) - 1.0f) * 0.5f);
+    if (cc < 0) cc = 0;
+    while ((cc + 1) * (cc + 2) / 2 <= u) ++cc;
+    while (cc > 0 && cc * (cc + 1) / 2 > u) --cc;
+    c = cc;
+    a = u - cc * (cc + 1) / 2;
+}
+
+__global__ void __launch_bounds__(LN_THREADS, 2)
+lane_mask_kernel(const float* __restrict__ xs, const uint32_t* __restrict__ span,
+                 const uint32_t* __restrict__ flag, const float* __restrict__ props, const int* __restrict__ perm,
+                 int n, int ld, float thr, uint64_t* __restrict__ mask, int64_t ldw,
+                 unsigned long long* __restrict__ rowbits, int NB, uint32_t* __restrict__ edges,
+                 unsigned* __restrict__ ecount, unsigned ecap, unsigned long long* __restrict__ haspred)
+{
+    __shared__ __align__(16) float s_nx[LN_ROWS][LN_TILE];  // -x of the column lanes, row by row
+    __shared__ uint32_t s_span[LN_TILE];
+    __shared__ uint32_t s_flag[LN_TILE];
+    __shared__ uint16_t s_piece[LN_TILE][LN_THREADS / LN_TILE];
+    __shared__ unsigned long long s_or[2];
+    __shared__ int s_cnt[2];
+    __shared__ int s_total;
+    __shared__ unsigned s_base;
+
+    pdl_wait();  // the gather has finished
+    pdl_release();
+    int ta, tc;
+    lane_tile(blockIdx.x, ta, tc);
+    const int rbase = ta * LN_TILE, cbase = tc * LN_TILE;
+    const int t = threadIdx.x;
+    const int r = t & (LN_TILE - 1), q = t / LN_TILE;
+    // Stage the column lanes (negated; NaN stays NaN).
+    for (int e = t; e < LN_ROWS * LN_TILE; e += LN_THREADS) {
+        const int k = e / LN_TILE, c = e % LN_TILE;
+        s_nx[k][c] = -xs[static_cast<int64_t>(k) * ld + cbase + c];
+    }
+    if (t < LN_TILE) {
+        s_span[t] = span[cbase + t];
+        s_flag[t] = flag[cbase + t];
+    }
+    const int i = rbase + r;
+    float xr[LN_ROWS];
+#pragma unroll
+    for (int k = 0; k < LN_ROWS; ++k) xr[k] = xs[static_cast<int64_t>(k) * ld + i];
+    const uint32_t sr = span[i];
+    const uint32_t fr = flag[i];
+    __syncthreads();
+
+    uint32_t bits = 0u;
+    const int c0 = q * LN_QCOLS;
+#pragma unroll 1
+    for (int g = 0; g < LN_QCOLS; g += 4) {
+        float acc0 = 0.0f, acc1 = 0.0f, acc2 = 0.0f, acc3 = 0.0f;
+#pragma unroll
+        for (int k = 0; k < LN_ROWS; ++k) {
+            const float4 nc = *reinterpret_cast<const float4*>(&s_nx[k][c0 + g]);
+            acc0 = __fadd_rn(acc0, fmaxf(fabsf(__fadd_rn(xr[k], nc.x)), 0.0f));
+            acc1 = __fadd_rn(acc1, fmaxf(fabsf(__fadd_rn(xr[k], nc.y)), 0.0f));
+            acc2 = __fadd_rn(acc2, fmaxf(fabsf(__fadd_rn(xr[k], nc.z)), 0.0f));
+            acc3 = __fadd_rn(acc3, fmaxf(fabsf(__fadd_rn(xr[k], nc.w)), 0.0f));
+        }
+        const float acc[4] = {acc0, acc1, acc2, acc3};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int cl = c0 + g + u, j = cbase + cl;
+            if (j <= i || j >= n || i >= n) continue;  // the upper triangle only
+            const uint32_t sc = s_span[cl];
+            const int lo = max(static_cast<int>(sr & 255u), static_cast<int>(sc & 255u));
+            const int hi = min(static_cast<int>(sr >> 8), static_cast<int>(sc >> 8));
+            if (hi <= lo) continue;  // no common row: +inf, never below the threshold
+            float d;
+            if (fr | s_flag[cl])
+                d = lane_distance_exact(props + static_cast<int64_t>(perm[i]) * LN_VALUES,
+                                        props + static_cast<int64_t>(perm[j]) * LN_VALUES, sr, sc);
+            else
+                d = __fdiv_rn(acc[u], static_cast<float>(hi - lo));
+            if (d < thr) bits |= 1u << (g + u);
+        }
+    }
+    s_piece[r][q] = static_cast<uint16_t>(bits);
+    __syncthreads();
+    // Threads 0..63 own the tile's rows: word, chunk bit, pair count.
+    uint64_t w = 0;
+    int cnt = 0;
+    if (t < LN_TILE) {
+#pragma unroll
+        for (int k = 0; k < LN_THREADS / LN_TILE; ++k)
+            w |= static_cast<uint64_t>(s_piece[t][k]) << (LN_QCOLS * k);
+        const int row = rbase + t;
+        if (row < n) {
+            mask[static_cast<int64_t>(row) * ldw + tc] = w;
+            if (w && rowbits) {
+                const int chunk = cbase >> 8;
+                atomicOr(rowbits + static_cast<int64_t>(row) * NB + (chunk >> 6), 1ull << (chunk & 63));
+            }
+        }
+        cnt = __popcll(w);
+        // Inclusive prefix of the counts within the warp.
+        const unsigned l = lane_id();
+        int x = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(FULL, x, d);
+            if (static_cast<int>(l) >= d) x += y;
+        }
+        const unsigned long long o = __reduce_or_sync(FULL, static_cast<unsigned>(w)) |
+                                     (static_cast<unsigned long long>(__reduce_or_sync(FULL,
+                                          static_cast<unsigned>(w >> 32))) << 32);
+        if (l == 31) {
+            s_cnt[t >> 5] = x;
+            s_or[t >> 5] = o;
+        }
+        cnt = x - cnt;  // exclusive prefix within the warp
+    }
+    __syncthreads();
+    if (t == 0) {
+        const unsigned long long o = s_or[0] | s_or[1];
+        if (o && haspred) atomicOr(haspred + tc, o);
+        const int total = s_cnt[0] + s_cnt[1];
+        s_base = total && edges ? atomicAdd(ecount, static_cast<unsigned>(total)) : 0u;
+        s_total = total;
+    }
+    __syncthreads();
+    // The pair list: the tile's pairs land contiguously, row by row.  Past
+    // the capacity the count still grows (the resolve then takes the walk)
+    // and nothing is written.
+    if (t < LN_TILE && edges && w) {
+        const unsigned total = static_cast<unsigned>(s_total);
+        const unsigned base = s_base;
+        if (base <= ecap && total <= ecap - base) {
+            uint32_t* dst = edges + base + cnt + (t >= 32 ? s_cnt[0] : 0);
+            const uint32_t row = static_cast<uint32_t>(rbase + t);
+            uint64_t x = w;
+            while (x) {
+                const int b = __ffsll(static_cast<long long>(x)) - 1;
+                x &= x - 1;
+                *dst++ = (row << 16) | static_cast<uint32_t>(cbase + b);
+            }
+        }
+    }
+}
+
+}  // namespace gbnms
+
+namespace gbnms {
+
+int lane_ld(int n) { return (n + LN_TILE - 1) / LN_TILE * LN_TILE; }
+
+void launch_lane_mask(const float* props, const int* perm, int n, float thr, float* xs, uint32_t* span,
+                      uint32_t* flag, uint64_t* mask, int64_t ldw, uint64_t* rowbits, int NB, uint32_t* edges,
+                      unsigned* ecount, unsigned ecap, uint64_t* haspred, cudaStream_t st)
+{
+    if (n <= 0) return;
+    const int ld = lane_ld(n);
+    launch_pdl(lane_gather_kernel, dim3((ld + 255) / 256), dim3(256), 0, st, props, perm, n, ld, xs, span, flag);
+    const int T = ld / LN_TILE;
+    launch_pdl(lane_mask_kernel, dim3(T * (T + 1) / 2), dim3(LN_THREADS), 0, st, xs,
+               static_cast<const uint32_t*>(span), static_cast<const uint32_t*>(flag), props, perm, n, ld, thr, mask,
+               ldw, reinterpret_cast<unsigned long long*>(rowbits), NB, edges, ecount, ecap,
+               reinterpret_cast<unsigned long long*>(haspred));
+}
+
+}  // namespace gbnms

@@ -82,14 +82,15 @@ __device__ __forceinline__ void merge_p(const uint64_t* buf, int a0, int na, int
     }
 }
 
-// Sorted position r holds key k: the permutation entry and the gathered box.
+// Sorted position r holds key k: the permutation entry and the gathered box
+// (no box when the caller sorts without boxes).
 __device__ __forceinline__ void emit_sorted(uint64_t k, int r, int m, const float4* __restrict__ boxes,
                                             int* __restrict__ perm, float4* __restrict__ boxes_s)
 {
     if (r < m) {
         const int x = static_cast<int>(static_cast<uint32_t>(k));
         perm[r] = x;
-        boxes_s[r] = boxes[x];
+        if (boxes) boxes_s[r] = boxes[x];
     }
 }
 
@@ -199,7 +200,7 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
         if (p < m && p < c0 + MS_CHUNK) {
             const int xi = cand ? cand[p] : p;
             key = order_key(scores[xi], static_cast<uint32_t>(xi));
-            if (!multi) cbox = boxes[xi];
+            if (!multi && boxes) cbox = boxes[xi];
         }
         ckey[tid] = key;
     }
@@ -316,7 +317,7 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
         if (multi) keys_out[c0 + crank[tid]] = ckey[tid];
         else if (crank[tid] < m) {
             perm[crank[tid]] = static_cast<int>(static_cast<uint32_t>(ckey[tid]));
-            boxes_s[crank[tid]] = cbox;
+            if (boxes) boxes_s[crank[tid]] = cbox;
         }
     }
 }

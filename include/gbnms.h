@@ -333,6 +333,52 @@ nms_status nms_boxes7_run(float* buffers, int32_t batch, int32_t max_objects, in
                           int32_t fast, int32_t* dev_status, void* workspace, size_t workspace_bytes,
                           void* stream);
 
+/* Lane candidates of nms_lane_run. */
+#define NMS_LANE_VALUES 77
+#define NMS_LANE_ROWS 72
+#define NMS_LANE_MAX_N 16384
+
+/*
+ * Greedy NMS of lane candidates ("nms_kernel.cu 파일 분석 -2": a candidate
+ * holds PROP_SIZE = 77 values; candidates are compared in score order in
+ * 64-candidate tiles above the diagonal; the comparison is symmetric, by
+ * absolute values, against the threshold that says whether two lanes are
+ * alike).  The page stops before the comparison; the reading taken:
+ *   values   0, 1: class scores (not used here); 2: start row; 3: start x
+ *            (not used here); 4: length in rows; 5..76: the lane's x at
+ *            rows 0..71;
+ *   rows     a lane covers rows [floor(start), floor(start) + floor(length))
+ *            within [0, 72); a NaN, infinite or beyond 2^20 start or length
+ *            covers none;
+ *   distance of two lanes: over the rows both cover, the binary32 sum of
+ *            |x_a - x_b|, added from the lowest row up, divided by the
+ *            number of those rows (+inf without any);
+ *   rule     greedy NMS in descending score (ties to the lower index): a
+ *            lane is dropped when its distance to a kept lane is strictly
+ *            below dist_thr (a NaN distance never drops).
+ *
+ *   props    device float [n][77], row-major, 4-byte aligned.
+ *   scores   device float [n]: the NMS order (descending; -0 = +0; NaN last).
+ *   n        0 <= n <= NMS_LANE_MAX_N.
+ *   max_out  at most this many outputs (<= 0: no cap).
+ *   keep     device int64 [keep_cap] (8-byte aligned), keep_cap >=
+ *            min(n, max_out) with max_out, else >= n: kept input indices in
+ *            score order.
+ *   count    device int64 [1] (8-byte aligned): their number.
+ *   dev_status optional device int32: NMS_ERR_TIMEOUT when a bounded wait
+ *            of the resolve gave up.
+ *   workspace device scratch of >= nms_lane_workspace_size(n) bytes,
+ *            256-byte aligned, owned by the caller.
+ * Asynchronous on `stream`; the library allocates nothing.
+ * Errors: NMS_ERR_INVALID_ARG (n < 0, NaN dist_thr, NULL or misaligned
+ *         pointers), NMS_ERR_CAPACITY (n > NMS_LANE_MAX_N, keep_cap too
+ *         small), NMS_ERR_WORKSPACE, NMS_ERR_CUDA.
+ */
+nms_status nms_lane_workspace_size(int64_t n, size_t* bytes);
+nms_status nms_lane_run(const float* props, const float* scores, int64_t n, float dist_thr, int32_t max_out,
+                        int64_t* keep, int64_t keep_cap, int64_t* count, int32_t* dev_status, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
 /* Largest n nms_resolve_mask_noalloc accepts. */
 #define NMS_NOALLOC_MAX_N 16384
 

@@ -161,6 +161,25 @@ def test_resolve_entries_reject_misaligned_pointers(lib):
     assert g.nms_resolve_mask_noalloc(FAKE + 8, 100, 0, 0, FAKE, FAKE, 0) == g.NMS_ERR_INVALID_ARG
 
 
+def test_lane_entry_validation(lib):
+    ws = 1 << 20
+    big = 1 << 40
+    assert g.nms_lane_workspace_size(1000) > 0
+    with pytest.raises(g.NmsError):
+        g.nms_lane_workspace_size(g.NMS_LANE_MAX_N + 1)
+    assert g.nms_lane_run(FAKE, FAKE, -1, 15.0, 0, FAKE, 10, FAKE, 0, ws, big, 0) == g.NMS_ERR_INVALID_ARG
+    assert g.nms_lane_run(FAKE, FAKE, 10, math.nan, 0, FAKE, 10, FAKE, 0, ws, big, 0) == g.NMS_ERR_INVALID_ARG
+    assert g.nms_lane_run(0, FAKE, 10, 15.0, 0, FAKE, 10, FAKE, 0, ws, big, 0) == g.NMS_ERR_INVALID_ARG
+    assert g.nms_lane_run(FAKE + 2, FAKE, 10, 15.0, 0, FAKE, 10, FAKE, 0, ws, big, 0) == g.NMS_ERR_INVALID_ARG
+    assert g.nms_lane_run(FAKE, FAKE, 10, 15.0, 0, FAKE + 4, 10, FAKE, 0, ws, big, 0) == g.NMS_ERR_INVALID_ARG
+    assert g.nms_lane_run(FAKE, FAKE, 10, 15.0, 0, FAKE, 10, FAKE + 4, 0, ws, big, 0) == g.NMS_ERR_INVALID_ARG
+    assert g.nms_lane_run(FAKE, FAKE, 10, 15.0, 0, FAKE, 9, FAKE, 0, ws, big, 0) == g.NMS_ERR_CAPACITY
+    assert g.nms_lane_run(FAKE, FAKE, 10, 15.0, 3, FAKE, 3, FAKE, 0, 0, big, 0) == g.NMS_ERR_WORKSPACE
+    assert g.nms_lane_run(FAKE, FAKE, 10, 15.0, 0, FAKE, 10, FAKE, 0, ws, 16, 0) == g.NMS_ERR_WORKSPACE
+    assert g.nms_lane_run(FAKE, FAKE, g.NMS_LANE_MAX_N + 1, 15.0, 0, FAKE, big, FAKE, 0, ws, big, 0) == \
+        g.NMS_ERR_CAPACITY
+
+
 def test_no_cpu_fallback_when_library_missing(monkeypatch):
     monkeypatch.setattr(g, "_lib", None)
     monkeypatch.setattr(g, "LIB_PATH", "/nonexistent/libgbnms.so")

@@ -478,6 +478,44 @@ def time_front_end(g, torch, dev, flush, reps=20, conf_thr=0.25, max_objects=100
             "candidates": int(buf[:, 0].sum().item())}
 
 
+def time_lanes(g, torch, dev, flush, sizes=(1000, 3000, 16384), thr=15.0, reps=20):
+    """Device time of one nms_lane_run call on the seeded lane workloads
+    (workloads.lanes: candidates of one road image, 77 values each) at a
+    15 px distance threshold: median us per call and lane pairs per second."""
+    out = {}
+    stream = torch.cuda.current_stream(dev)
+    for n in sizes:
+        props, scores = W.lanes(0, n=n)
+        p = torch.from_numpy(props).to(dev)
+        s = torch.from_numpy(scores).to(dev)
+        keep = torch.empty(n, dtype=torch.int64, device=dev)
+        count = torch.empty(1, dtype=torch.int64, device=dev)
+        wsb = g.nms_lane_workspace_size(n)
+        ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+
+        def call():
+            st = g.nms_lane_run(p.data_ptr(), s.data_ptr(), n, thr, 0, keep.data_ptr(), n, count.data_ptr(), 0,
+                                ws.data_ptr(), wsb, stream.cuda_stream)
+            if st != g.NMS_OK:
+                raise g.NmsError(st, "nms_lane_run")
+
+        for _ in range(3):
+            call()
+        evs = []
+        for _ in range(reps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        us = statistics.median(1000 * a.elapsed_time(b) for a, b in evs)
+        out[f"lanes_n{n}"] = {"us_median": us, "lane_pairs_per_s": n * (n - 1) / 2 / (us / 1e6),
+                              "kept": int(count.item()), "dist_thr": thr}
+    return out
+
+
 def time_matrix(g, torch, wl, dev, flush, decay_thr=0.1, reps=20, decay=0):
     """Device time of one nms_matrix_run call (Gaussian decay with sigma 0.5,
     or the linear decay) on a one-image workload: median, p10, p90 in
@@ -693,7 +731,7 @@ def run_gbnms(args):
         roof = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
                 "frac": ach / hbm, "traffic": _ncu_traffic(dominant), "note": note}
 
-    per_config = fast_nms = matrix_nms = matrix_lin = front_end = None
+    per_config = fast_nms = matrix_nms = matrix_lin = front_end = lanes = None
     summary = None
     if not args.no_configs:
         per_config, fast_nms, matrix_nms, matrix_lin = {}, {}, {}, {}
@@ -710,6 +748,8 @@ def run_gbnms(args):
                 matrix_lin[name] = time_matrix(g, torch, wl_c, dev, flush, decay=g.NMS_DECAY_LINEAR)
         if "front_end" in sections:
             front_end = time_front_end(g, torch, dev, flush)
+        if "lanes" in sections:
+            lanes = time_lanes(g, torch, dev, flush)
         summary = greedy_summary(per_config, fp32_roof, hbm)
 
     cpu = None
@@ -736,6 +776,7 @@ def run_gbnms(args):
         "alu_peaks": alu,
         "fast_nms_per_config": fast_nms,
         "front_end": front_end,
+        "lane_nms": lanes,
         "matrix_nms_per_config": matrix_nms,
         "matrix_nms_linear_per_config": matrix_lin,
         "per_config": per_config,
@@ -855,8 +896,8 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config timing table")
     ap.add_argument("--configs", default="all",
                     help="comma-separated workload names for the per-config tables (default: all)")
-    ap.add_argument("--sections", default="greedy,fast,matrix,front_end",
-                    help="per-config tables to time: greedy, fast, matrix, front_end")
+    ap.add_argument("--sections", default="greedy,fast,matrix,front_end,lanes",
+                    help="per-config tables to time: greedy, fast, matrix, front_end, lanes")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.impl == "reference":

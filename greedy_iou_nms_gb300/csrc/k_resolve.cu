@@ -290,13 +290,13 @@ unsigned graph_grid_cap(int m_bound)
 unsigned graph_edge_cap(int m_bound)
 {
     if (m_bound <= 0 || m_bound > GR_MAX_N) return 0;
-    const long long room = GR_SMEM - 4ll * GR_HEAD - 40ll * graph_words(m_bound);
+    const long long room = GR_SMEM - 4ll * GR_HEAD - 64ll * graph_words(m_bound);
     return room > 0 ? static_cast<unsigned>((room / 4) & ~3ll) : 0u;
 }
 
 size_t graph_smem_bytes(int m_bound)
 {
-    return 4 * GR_HEAD + 40 * static_cast<size_t>(graph_words(m_bound)) +
+    return 4 * GR_HEAD + 64 * static_cast<size_t>(graph_words(m_bound)) +
            4 * static_cast<size_t>(graph_edge_cap(m_bound));
 }
 
@@ -317,43 +317,40 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
         : "memory");
 }
 
-// Decides the open boxes of bitmap word w (boxes 32w .. 32w+31): kept if no
-// open source blocked them (a box a kept source hit is already removed).
-// Clears the word's blocked flags; returns whether a blocked box stays open.
-__device__ __forceinline__ bool decide_word(uint2* KR, uint8_t* BLK, int w, int NW, int n)
+// Kept bits of 32-box word w (lane l: box 32w + l) once the rounds are over.
+__device__ __forceinline__ uint32_t kept_word(const uint8_t* RMb, int w, int n, unsigned l)
 {
-    const uint2 kr = KR[w];
-    const uint32_t valid = (w == NW - 1 && (n & 31)) ? (1u << (n & 31)) - 1u : ~0u;
-    const uint32_t open = ~(kr.x | kr.y) & valid;
-    if (!open) return false;
-    uint4* bq = reinterpret_cast<uint4*>(BLK + 32 * w);
-    const uint4 b0 = bq[0], b1 = bq[1];
-    const uint32_t bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-    uint32_t blk = 0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) blk |= ((bv[q] * 0x01020408u) >> 24 & 0xfu) << (4 * q);  // bytes 0/1 -> bits
-    KR[w].x = kr.x | (open & ~blk);
-    bq[0] = make_uint4(0u, 0u, 0u, 0u);
-    bq[1] = make_uint4(0u, 0u, 0u, 0u);
-    return (open & blk) != 0;
+    const int j = 32 * w + static_cast<int>(l);
+    return __ballot_sync(FULL, j < n && RMb[j] == 0);
 }
 
-// One live pair e (source << 16 | target) given its source's (kept, removed)
-// word ks.  A kept source removes the target at once (the removal is final,
-// so other pairs may see it in this same pass); an open source blocks the
-// target, with a plain byte store (every writer stores 1).  Returns whether
-// the pair stays (its source is still open).
-__device__ __forceinline__ bool mark_pair(uint2* KR, uint8_t* BLK, uint32_t e, uint2 ks)
+// Writes the kept boxes of 32-box words [w0, w1) at positions base, base+1,
+// ... (below cap), lane l taking box 32w + l: OW words a step, their ballots
+// first and then all their permutation loads (from global memory when the
+// permutation did not fit in shared memory), so those latencies overlap.
+template <int OW>
+__device__ __forceinline__ void write_kept(const uint8_t* RMb, int w0, int w1, int n, unsigned l, int base, int cap,
+                                           const int* perm_s, const int* __restrict__ perm,
+                                           int64_t* __restrict__ keep)
 {
-    const uint32_t j = e & 0xffffu;
-    const uint32_t bi = 1u << ((e >> 16) & 31);
-    if (ks.x & bi) {
-        atomicOr(&KR[j >> 5].y, 1u << (j & 31));
-        return false;
+    const uint32_t below = (1u << l) - 1u;
+    for (int wb = w0; wb < w1 && base < cap; wb += OW) {
+        uint32_t bits[OW];
+        int v[OW];
+#pragma unroll
+        for (int u = 0; u < OW; ++u) bits[u] = wb + u < w1 ? kept_word(RMb, wb + u, n, l) : 0u;
+#pragma unroll
+        for (int u = 0; u < OW; ++u) {
+            const int j = 32 * (wb + u) + static_cast<int>(l);
+            v[u] = ((bits[u] >> l) & 1u) ? (perm_s ? perm_s[j] : perm ? perm[j] : j) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < OW; ++u) {
+            const int pos = base + __popc(bits[u] & below);
+            if (((bits[u] >> l) & 1u) && pos < cap) keep[pos] = v[u];
+            base += __popc(bits[u]);
+        }
     }
-    if (ks.y & bi) return false;
-    BLK[j] = 1;
-    return true;
 }
 
 // Rounds over the pair list gedges[0..E) of n sorted boxes (haspred: bit j
@@ -361,12 +358,27 @@ __device__ __forceinline__ bool mark_pair(uint2* KR, uint8_t* BLK, uint32_t e, u
 // rounds outnumber the walk's tiles plus 16 (a long chain of dependencies:
 // the walk is then the faster way).
 //
-// Shared layout: scratch and the copy barrier (GR_HEAD words), then the
-// (kept, removed) bits of 32 boxes per uint2, then one "blocked by an open
-// box" byte per box, then the live pairs.  Thread t owns
-// the pairs at t, t + RV_THREADS, ... and compacts its own share in place.
-// A pair leaves the list once its source is decided; while the source is
-// open the target is open too (a box is decided only after all its sources).
+// Shared layout: scratch and the copy barrier (GR_HEAD words), then one byte
+// per box holding the last pass that blocked it (plus 2, mod 256), then one
+// "removed" byte per box, then the live pairs.  Byte planes keep a warp's
+// stores conflict-free: its pairs come from one 128-column tile of the mask,
+// so their targets are 128 consecutive bytes.  Each warp owns an equal
+// contiguous share of the list and compacts it in place.
+//
+// One pass per round and one barrier: a source is kept in pass r when it is
+// not removed and no open box blocked it in pass r - 1.  A box blocked in
+// pass r was blocked in pass r - 1 too (its pairs only leave and an open
+// source was open before), so a byte written in pass r changes no reader's
+// decision in that pass; and a kept source's pairs all leave in the first
+// pass that finds it kept, so a live source's byte is r, r + 1 or r + 2 (mod
+// 256) and the wrap is harmless.  A pair leaves the list once its source is
+// decided; when none is left, the kept boxes are the ones not removed.
+//
+// Pass 0 is known in advance: a source without a source of its own is kept
+// and every other one is open, so a box with a source ends pass 0 removed or
+// blocked.  Its byte therefore starts at 2 (blocked in pass 0; 0 for a box
+// without a source), and pass 0 only removes: it reads no removed byte
+// (nothing is removed before it) and stores no block.
 __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedges, unsigned E, unsigned cap_words,
                               const uint32_t* __restrict__ haspred, int n, int NWp,
                               const int* __restrict__ perm, int max_out, int64_t* __restrict__ keep,
@@ -375,9 +387,9 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
 {
     int* scratch = reinterpret_cast<int*>(sm);
     unsigned long long* bar = reinterpret_cast<unsigned long long*>(sm + 32);
-    uint2* KR = reinterpret_cast<uint2*>(sm + GR_HEAD);
-    uint8_t* BLK = reinterpret_cast<uint8_t*>(KR + NWp);
-    uint32_t* Es = reinterpret_cast<uint32_t*>(BLK + 32 * NWp);
+    uint8_t* FL = reinterpret_cast<uint8_t*>(sm + GR_HEAD);
+    uint8_t* RMb = FL + 32 * NWp;
+    uint32_t* Es = sm + GR_HEAD + 16 * NWp;
     const int tid = threadIdx.x;
     const unsigned l = lane_id();
     const int warp = tid >> 5;
@@ -412,14 +424,16 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
         bulk_g2s(reinterpret_cast<char*>(Es) + bytes + off, reinterpret_cast<const char*>(perm) + off, len, bar);
     }
     for (int w = tid; w < NW; w += RV_THREADS) {
-        KR[w] = make_uint2(0u, 0u);
-        const uint32_t hp = haspred[w];  // before the first round every target is blocked
+        const uint32_t hp = haspred[w];  // a box with a source starts blocked in pass 0
         uint32_t bx[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) bx[q] = (((hp >> (4 * q)) & 0xfu) * 0x00204081u) & 0x01010101u;  // bits -> bytes
-        uint4* bq = reinterpret_cast<uint4*>(BLK + 32 * w);
-        bq[0] = make_uint4(bx[0], bx[1], bx[2], bx[3]);
-        bq[1] = make_uint4(bx[4], bx[5], bx[6], bx[7]);
+        for (int q = 0; q < 8; ++q) bx[q] = (((hp >> (4 * q)) & 0xfu) * 0x00204081u & 0x01010101u) << 1;  // bits -> 0/2
+        uint4* fq = reinterpret_cast<uint4*>(FL + 32 * w);
+        fq[0] = make_uint4(bx[0], bx[1], bx[2], bx[3]);
+        fq[1] = make_uint4(bx[4], bx[5], bx[6], bx[7]);
+        uint4* rq = reinterpret_cast<uint4*>(RMb + 32 * w);
+        rq[0] = make_uint4(0u, 0u, 0u, 0u);
+        rq[1] = make_uint4(0u, 0u, 0u, 0u);
     }
     bool copied = true;
     if (tx) {
@@ -438,42 +452,74 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
         }
         return true;
     }
-    int live = E > static_cast<unsigned>(tid) ? static_cast<int>((E - tid + RV_THREADS - 1) / RV_THREADS) : 0;
+    // Warp w owns the pairs [wbeg, wbeg + cnt): 32 a step, one a lane, its
+    // survivors packed in place at the front by a ballot.  A live pair in
+    // pass r: a removed source no longer matters; a source that no open box
+    // blocked in the previous pass (its byte == r mod 256) is kept and removes
+    // its target at once (the removal is final, so other pairs may see it in
+    // this same pass); any other source is still open, blocks its target for
+    // this pass (in pass 0 the target's byte already says so) and its pair
+    // stays.  Both are plain byte stores (every writer of a byte in one pass
+    // stores the same value).
+    const unsigned chunk = (E + 32u * RV_WARPS - 1) / (32u * RV_WARPS) * 32u;
+    const unsigned wbeg = min(E, static_cast<unsigned>(warp) * chunk);
+    unsigned cnt = min(E, wbeg + chunk) - wbeg;
+    uint32_t* Ew = Es + wbeg;
+    const uint32_t lt = (1u << l) - 1u;
     const int max_rounds = (n + 63) / 64 + 16;
-    for (int round = 0;; ++round) {
-        // Decide every open box: kept if no open source blocked it.
-        bool more = false;
-        for (int w = tid; w < NW; w += RV_THREADS) more |= decide_word(KR, BLK, w, NW, n);
-        if (!__syncthreads_or(more)) break;
-        if (round == max_rounds) return false;
-        // One pass over the live pairs: a kept source removes its target, a
-        // removed source no longer matters, an open source blocks its target
-        // and the pair stays.
-        int nl = 0;
-        for (int k0 = 0; k0 < live; k0 += 2) {  // two pairs a step (a short loop body)
-            uint32_t e[2];
-            uint2 ki[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) e[u] = k0 + u < live ? Es[tid + RV_THREADS * (k0 + u)] : 0xffffffffu;
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-                if (e[u] != 0xffffffffu) ki[u] = KR[e[u] >> 21];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                if (e[u] == 0xffffffffu) continue;
-                if (mark_pair(KR, BLK, e[u], ki[u])) Es[tid + RV_THREADS * nl++] = e[u];
-            }
+    // Pass 0: a source without a source of its own (byte 0) is kept and
+    // removes its target; every other pair stays.
+    bool any = false;
+    {
+        unsigned out = 0;
+        for (unsigned k = 0; k < cnt; k += 32) {
+            const bool have = k + l < cnt;
+            const uint32_t e = have ? Ew[k + l] : 0u;
+            const bool kept = have && FL[e >> 16] == 0;
+            if (kept) RMb[e & 0xffffu] = 1;
+            const bool stay = have && !kept;
+            const uint32_t b = __ballot_sync(FULL, stay);  // every lane has read its pair
+            if (stay) Ew[out + __popc(b & lt)] = e;
+            out += __popc(b);
         }
-        live = nl;
-        __syncthreads();
+        cnt = out;
+        any = __syncthreads_or(cnt > 0u);
+    }
+    for (int round = 1; any; ++round) {
+        if (round == max_rounds) return false;
+        const uint32_t kept_f = static_cast<uint32_t>(round) & 0xffu;
+        const uint8_t blk_f = static_cast<uint8_t>(round + 2);
+        unsigned out = 0;
+        for (unsigned k = 0; k < cnt; k += 32) {
+            const bool have = k + l < cnt;
+            const uint32_t e = have ? Ew[k + l] : 0u;
+            const uint32_t src = e >> 16, j = e & 0xffffu;
+            const uint32_t rm = have ? RMb[src] : 1u;
+            const uint32_t f = have ? FL[src] : 0u;
+            const bool kept = rm == 0u && f == kept_f;
+            const bool open = rm == 0u && f != kept_f;
+            if (kept) RMb[j] = 1;
+            if (open) FL[j] = blk_f;
+            const uint32_t b = __ballot_sync(FULL, open);  // every lane has read its pair
+            if (open) Ew[out + __popc(b & lt)] = e;
+            out += __popc(b);
+        }
+        cnt = out;
+        any = __syncthreads_or(cnt > 0u);
     }
     // Output: warp w owns 32-box words [w*wpw, (w+1)*wpw); a block-wide
     // prefix of the warps' kept counts places them, and within a word lane l
     // writes box 32w+l, so loads of perm and stores of keep are coalesced.
     const int wpw = (NW + 31) / 32;
     const int w0 = min(warp * wpw, NW), w1 = min(w0 + wpw, NW);
-    int c = 0;
-    for (int w = w0 + static_cast<int>(l); w < w1; w += 32) c += __popc(KR[w].x);
+    // Kept = boxes of the warp's words less the removed ones; a removed byte
+    // is 0 or 1 and no box past n is ever removed, so popcounts of 16-byte
+    // loads count them.
+    int c = static_cast<int>(l) == 0 ? max(0, min(32 * w1, n) - 32 * w0) : 0;
+    for (int j0 = 32 * w0 + 16 * static_cast<int>(l); j0 < 32 * w1; j0 += 512) {
+        const uint4 q = *reinterpret_cast<const uint4*>(RMb + j0);
+        c -= __popc(q.x) + __popc(q.y) + __popc(q.z) + __popc(q.w);
+    }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) c += __shfl_xor_sync(FULL, c, d);
     if (l == 0) scratch[warp] = c;
@@ -482,25 +528,13 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
     const int wc = scratch[l];
     const int total = __reduce_add_sync(FULL, wc);
     const int cap = max_out > 0 ? max_out : INT_MAX;
-    int base = __reduce_add_sync(FULL, static_cast<int>(l) < warp ? wc : 0);
-    const uint32_t below = (1u << l) - 1u;
-    constexpr int OW = 2;  // words per step (a short loop: its code is fetched cold after an L2 flush)
-    for (int wb = w0; wb < w1 && base < cap; wb += OW) {
-        uint32_t bits[OW];
-        int v[OW];
-#pragma unroll
-        for (int u = 0; u < OW; ++u) {
-            bits[u] = wb + u < w1 ? KR[wb + u].x : 0u;
-            const int j = 32 * (wb + u) + static_cast<int>(l);
-            v[u] = ((bits[u] >> l) & 1u) ? (perm_s ? perm_s[j] : perm ? perm[j] : j) : 0;
-        }
-#pragma unroll
-        for (int u = 0; u < OW; ++u) {
-            const int pos = base + __popc(bits[u] & below);
-            if (((bits[u] >> l) & 1u) && pos < cap) keep[pos] = v[u];
-            base += __popc(bits[u]);
-        }
-    }
+    const int base = __reduce_add_sync(FULL, static_cast<int>(l) < warp ? wc : 0);
+    // Words [w0, w1) in steps of eight when the warp has that many, else two
+    // (a short body, fetched cold after an L2 flush).
+    if (w1 - w0 >= 8)
+        write_kept<8>(RMb, w0, w1, n, l, base, cap, perm_s, perm, keep);
+    else
+        write_kept<2>(RMb, w0, w1, n, l, base, cap, perm_s, perm, keep);
     if (tid == 0) {
         counts[0] = total < cap ? total : cap;
         if (done_out && total >= cap) *done_out = 1;

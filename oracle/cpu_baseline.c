@@ -105,14 +105,24 @@ static int64_t greedy_sorted(const float* boxes, const int64_t* idx, int64_t m, 
     }
     const int64_t CH = 16;  /* words (1024 columns) per task */
     int64_t k = 0;
-    for (int64_t blk = 0; blk < W && k < cap; ++blk) {
-        const uint64_t live = ~removed[blk];
-        const int64_t nr = m - 64 * blk < 64 ? m - 64 * blk : 64;
-        const int64_t nch = (W - blk + CH - 1) / CH;
-#pragma omp parallel for collapse(2) schedule(dynamic, 1) if (parallel)
-        for (int64_t r = 0; r < nr; ++r) {
-            for (int64_t c = 0; c < nch; ++c) {
-                if (!(live >> r & 1)) continue;
+    int stop = 0;
+    /* One parallel region for the whole image: per block, the (live row,
+     * column chunk) tasks split statically over the threads, then one
+     * thread resolves the block; the barriers of `omp for` and `omp single`
+     * order the two, and every thread reads k and stop after them. */
+#pragma omp parallel if (parallel)
+    {
+        int64_t lr[64];
+        for (int64_t blk = 0; blk < W && !stop; ++blk) {
+            const uint64_t live = ~removed[blk];
+            const int64_t nr = m - 64 * blk < 64 ? m - 64 * blk : 64;
+            const int64_t nch = (W - blk + CH - 1) / CH;
+            int64_t nl = 0;
+            for (int64_t r = 0; r < nr; ++r)
+                if (live >> r & 1) lr[nl++] = r;
+#pragma omp for schedule(static)
+            for (int64_t t = 0; t < nl * nch; ++t) {
+                const int64_t r = lr[t / nch], c = t % nch;
                 const int64_t i = 64 * blk + r;
                 const float bx1 = X1[i], by1 = Y1[i], bx2 = X2[i], by2 = Y2[i];
                 const float ai = (bx2 - bx1) * (by2 - by1);
@@ -134,13 +144,17 @@ static int64_t greedy_sorted(const float* boxes, const int64_t* idx, int64_t m, 
                     rows[r * W + w] = pack_flags(f);
                 }
             }
-        }
-        for (int64_t r = 0; r < nr && k < cap; ++r) {
-            const int64_t i = 64 * blk + r;
-            if (removed[blk] >> r & 1) continue;
-            out[k++] = idx[i];
-            const uint64_t* row = rows + r * W;
-            for (int64_t w = blk; w < W; ++w) removed[w] |= row[w];
+#pragma omp single
+            {
+                for (int64_t r = 0; r < nr && k < cap; ++r) {
+                    const int64_t i = 64 * blk + r;
+                    if (removed[blk] >> r & 1) continue;
+                    out[k++] = idx[i];
+                    const uint64_t* row = rows + r * W;
+                    for (int64_t w = blk; w < W; ++w) removed[w] |= row[w];
+                }
+                if (k >= cap) stop = 1;
+            }
         }
     }
     free(rows);

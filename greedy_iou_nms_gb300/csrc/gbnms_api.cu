@@ -53,7 +53,7 @@ struct SingleLayout {
     unsigned lcap = 0;   // pairs the list holds (more when the all-SM graph path exists)
     bool grid = false;   // the all-SM graph path exists at this size
     size_t status, m_count, ecount, done, cand, perm, boxes_s, keys, rowbits, edges, haspred, gstate,
-        gctl, warm, mask, total;
+        gctl, mask, total;
 };
 
 SingleLayout single_layout(int64_t n)
@@ -80,7 +80,6 @@ SingleLayout single_layout(int64_t n)
     s.haspred = L.add(8 * static_cast<size_t>((n + 63) / 64));
     s.gstate = L.add(s.grid ? graph_grid_state_bytes(static_cast<int>(n)) : 0);
     s.gctl = L.add(s.grid ? graph_grid_ctl_bytes() : 0);
-    s.warm = L.add(4 * RV_WARM_WORDS);
     s.mask = L.add(8 * static_cast<size_t>(n) * static_cast<size_t>(s.ldw));
     s.total = L.total;
     return s;
@@ -347,8 +346,7 @@ nms_status run_impl(const float* boxes, const float* scores, int64_t n, const in
                 gd = gctl + 4 + stage;
             }
             launch_resolve_single(mask, L.ldw, rowbits, L.NB, edges, ecount, haspred, m_count, nb, perm,
-                                  max_out, keep, counts, status, st, limit, done_in, done_out, gd,
-                                  stage == 0 ? at<uint32_t>(workspace, L.warm) : nullptr);
+                                  max_out, keep, counts, status, st, limit, done_in, done_out, gd);
         };
         if (k1 >= n) {
             launch_iou_mask(boxes_s, m_count, nb, p, mask, L.ldw, rowbits, L.NB, edges, ecount,
@@ -717,8 +715,7 @@ extern "C" nms_status nms_lane_run(const float* props, const float* scores, int6
                      at<uint32_t>(workspace, L.flag), mask, L.s.ldw, rowbits, L.s.NB, edges, ecount, L.s.lcap,
                      L.s.ecap ? haspred : nullptr, st);
     launch_resolve_single(mask, L.s.ldw, rowbits, L.s.NB, edges, ecount, L.s.ecap ? haspred : nullptr, nullptr, nb,
-                          perm, max_out, keep, count, status, st, 1 << 30, nullptr, nullptr, nullptr,
-                          at<uint32_t>(workspace, L.s.warm));
+                          perm, max_out, keep, count, status, st);
     return cuda_status();
 }
 

@@ -94,10 +94,7 @@ void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* ro
                            const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm,
                            int max_out, int64_t* keep, int64_t* counts, int32_t* status,
                            cudaStream_t st, int limit = 1 << 30, const int* done_in = nullptr,
-                           int* done_out = nullptr, const int* grid_done = nullptr, uint32_t* warm = nullptr);
-// Words of the resolve's warm-up region (a small graph it resolves while it
-// waits for the mask, so that its code is in the instruction cache).
-constexpr size_t RV_WARM_WORDS = 256;
+                           int* done_out = nullptr, const int* grid_done = nullptr);
 
 // Pair-list capacity of the all-SM graph path (0 below its size range) and
 // its scratch: graph_grid_state_bytes of bitmaps and a control block.

@@ -542,21 +542,6 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
     return true;
 }
 
-// The warm-up graph: 64 boxes, a chain 0 -> 1 -> 2 -> 3, a root 5 over 6..37
-// and a chain 40 -> 41 -> 42 (37 pairs, a few rounds: every branch of the
-// rounds and of the output is taken).  Layout of the caller's RV_WARM_WORDS
-// words: pairs [0, 40), the neighbour bitmap [64, 66), the kept positions as
-// int64 at [72, 200), the count at [200, 202).
-constexpr int RV_WARM_N = 64;
-constexpr unsigned RV_WARM_E = 37;
-
-__device__ __forceinline__ uint32_t warm_pair(int t)
-{
-    if (t < 3) return static_cast<uint32_t>((t << 16) | (t + 1));   // 0->1, 1->2, 2->3
-    if (t < 35) return static_cast<uint32_t>((5 << 16) | (t + 3));  // 5 -> 6..37
-    return t == 35 ? static_cast<uint32_t>((40 << 16) | 41) : static_cast<uint32_t>((41 << 16) | 42);
-}
-
 __global__ void __launch_bounds__(RV_THREADS, 1)
 resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
                       const uint64_t* __restrict__ rowbits, int NB,
@@ -565,48 +550,23 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
                       const int* __restrict__ m_dev, int m_bound, const int* __restrict__ perm,
                       int max_out, int64_t* __restrict__ keep, int64_t* __restrict__ counts,
                       int32_t* status, int limit, const int* __restrict__ done_in, int* done_out,
-                      const int* __restrict__ grid_done, uint32_t* __restrict__ warm)
+                      const int* __restrict__ grid_done)
 {
     extern __shared__ __align__(128) uint64_t smem[];
     __shared__ ResolveShared S;
 
-    // With `warm`, the rounds first run on a small graph while the mask is
-    // still being computed (the loop's first pass, before the dependency
-    // wait): the same instructions as the real rounds, which then find them
-    // in the SM's instruction cache instead of fetching them, after an L2
-    // flush from HBM, a few lines at a time on the critical path.
-    const bool warm_up = warm && edges && m_bound >= RV_WARM_N;
-    if (warm_up) {
-        const int tid = threadIdx.x;
-        if (tid < 40) warm[tid] = tid < static_cast<int>(RV_WARM_E) ? warm_pair(tid) : 0xffffffffu;
-        if (tid == 0) warm[64] = 0xfffffffeu & ~0x30u;            // boxes 1..3 and 6..31 have a source
-        if (tid == 1) warm[65] = 0x3fu | (1u << 9) | (1u << 10);  // 32..37, 41, 42
-        __threadfence();
-        asm volatile("fence.proxy.async.global;\n" ::: "memory");  // the bulk copy reads these words
-        __syncthreads();
-    }
-    int n = 0;
-    for (int pass = warm_up ? 0 : 1; pass < 2; ++pass) {
-        const bool real = pass == 1;
-        if (real) {
-            pdl_wait();                           // the mask (or an earlier kernel) has finished
-            if (done_in && *done_in) return;      // an earlier stage already finished
-            if (grid_done && *grid_done) return;  // graph_grid_kernel resolved this stage
-            const int n_all = m_dev ? *m_dev : m_bound;
-            n = min(n_all, limit);
-            if (done_out && threadIdx.x == 0) *done_out = n >= n_all;  // raised below on max_out
-        }
-        if (!edges) break;
-        const unsigned E = real ? *ecount : RV_WARM_E;
-        if (E <= ecap &&
-            graph_resolve(real ? edges : warm, E, ecap, real ? haspred : warm + 64, real ? n : RV_WARM_N,
-                          graph_words(m_bound), real ? perm : nullptr, real ? max_out : 0,
-                          real ? keep : reinterpret_cast<int64_t*>(warm + 72),
-                          real ? counts : reinterpret_cast<int64_t*>(warm + 200), real ? status : nullptr,
-                          reinterpret_cast<uint32_t*>(smem), real ? done_out : nullptr) &&
-            real)
+    pdl_wait();                           // the mask (or an earlier kernel) has finished
+    if (done_in && *done_in) return;      // an earlier stage already finished
+    if (grid_done && *grid_done) return;  // graph_grid_kernel resolved this stage
+    const int n_all = m_dev ? *m_dev : m_bound;
+    const int n = min(n_all, limit);
+    if (done_out && threadIdx.x == 0) *done_out = n >= n_all;  // raised below on max_out
+    if (edges) {
+        const unsigned E = *ecount;
+        if (E <= ecap && graph_resolve(edges, E, ecap, haspred, n, graph_words(m_bound), perm, max_out, keep, counts,
+                                       status, reinterpret_cast<uint32_t*>(smem), done_out))
             return;
-        __syncthreads();  // the next pass (or the walk) reuses the shared memory
+        __syncthreads();  // the walk reuses the shared memory
     }
     const int T = (n + 63) / 64;              // tiles
     const int T256 = (n + 255) / 256;         // 256-column chunks
@@ -1091,12 +1051,9 @@ void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* ro
                            const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm,
                            int max_out, int64_t* keep, int64_t* counts, int32_t* status,
                            cudaStream_t st, int limit, const int* done_in, int* done_out,
-                           const int* grid_done, uint32_t* warm)
+                           const int* grid_done)
 {
     size_t smem = resolve_smem_bytes(m_bound, NB);
-    // The warm-up only pays while the kernel waits for its predecessor, i.e.
-    // under programmatic dependent launch.
-    if (!pdl_attr_count()) warm = nullptr;
     const unsigned ecap = edges ? graph_edge_cap(m_bound) : 0u;
     if (edges && graph_smem_bytes(m_bound) > smem) smem = graph_smem_bytes(m_bound);
     ensure_dynamic_smem(reinterpret_cast<const void*>(resolve_single_kernel), smem);
@@ -1110,7 +1067,7 @@ void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* ro
     cfg.numAttrs = pdl_attr_count();
     cudaLaunchKernelEx(&cfg, resolve_single_kernel, mask, ldw, rowbits, NB, edges, ecount, ecap,
                        reinterpret_cast<const uint32_t*>(haspred), m_dev, m_bound, perm, max_out, keep, counts,
-                       status, limit, done_in, done_out, grid_done, warm);
+                       status, limit, done_in, done_out, grid_done);
 }
 
 }  // namespace gbnms

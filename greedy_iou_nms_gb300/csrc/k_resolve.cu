@@ -11,9 +11,11 @@
 // (induction over the score order), in as many rounds as the longest chain of
 // such dependencies.  For detector-like inputs that chain is a handful of
 // links even when the walk below would take thousands of steps.  One CTA
-// keeps the kept/removed bitmaps and the live pairs in shared memory; a round
-// is one pass over the pairs whose target is still open plus one word-wide
-// pass over the bitmaps.
+// keeps a byte per box (the last pass that blocked it), a removed byte per
+// box and the live pairs in shared memory; a round is one pass over the pairs
+// whose source is still open and one barrier (graph_resolve).  Lists beyond
+// one CTA above 16384 boxes go to graph_grid_kernel, the same rounds on every
+// SM with grid barriers.
 //
 // Walk (everything else, and a caller's own mask):
 // "NMS CUDA代码学习", section Phase 2: one thread block walks the boxes from

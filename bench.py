@@ -643,9 +643,11 @@ def run_gbnms(args):
 
     # ---- end to end through the host-memory pipeline, inputs and outputs in
     # pinned host memory and every transfer inside the timed region: by
-    # default the kernels read the input and write the count and the kept
-    # indices across the host link themselves (zero-copy); for comparison,
-    # one host->device copy in and one device->host copy out around nms_run.
+    # default the kernels move the data across the host link themselves
+    # (zero-copy: a copy kernel stages the input into device memory in one
+    # pass, the resolve writes the count and the kept indices into the pinned
+    # output); for comparison, one host->device copy in and one device->host
+    # copy out around nms_run.
     # The events bracket the graph launch (from before the host launches it
     # to the end of its last transfer); the host then reads the result.
     def time_pipe(zero_copy):
@@ -791,7 +793,8 @@ def run_gbnms(args):
         "cpu_baseline": cpu,
         "e2e": {"value": n / (e2e_ms / 1000), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "host_ms_per_step": e2e_host_ms,
-                "transfer": ("zero-copy: the kernels read the pinned input and write the pinned output"
+                "transfer": ("zero-copy: a copy kernel stages the pinned input into device memory in one "
+                             "pass; the resolve writes the count and the kept indices into the pinned output"
                              if e2e_zc else "copies")},
         "gpu_launches": 3 * args.steps,  # sort, mask, resolve per call at this size
         "parity_vs_oracle": parity and e2e_parity,

@@ -33,7 +33,7 @@ NMS_MAX_SINGLE_N = 1 << 18
 EXPORTED = ("nms_status_string", "nms_workspace_size", "nms_run", "nms_fast_run", "nms_run_timed",
             "nms_matrix_workspace_size", "nms_matrix_run", "nms_mask_row_words", "nms_iou_mask",
             "nms_resolve_mask", "nms_resolve_mask_noalloc", "nms_decode_workspace_size", "nms_decode_boxes7",
-            "nms_boxes7_workspace_size", "nms_boxes7_run", "nms_mapped_pointer", "nms_lane_workspace_size",
+            "nms_boxes7_workspace_size", "nms_boxes7_run", "nms_mapped_pointer", "nms_copy", "nms_lane_workspace_size",
             "nms_lane_run")
 NMS_NOALLOC_MAX_N = 16384
 NMS_LANE_VALUES = 77  # values of one lane candidate (nms_lane_run)
@@ -100,6 +100,8 @@ def load():
     lib.nms_boxes7_run.restype = ctypes.c_int
     lib.nms_mapped_pointer.argtypes = [vp, ctypes.POINTER(vp)]
     lib.nms_mapped_pointer.restype = ctypes.c_int
+    lib.nms_copy.argtypes = [vp, vp, sz, vp]
+    lib.nms_copy.restype = ctypes.c_int
     lib.nms_lane_workspace_size.argtypes = [i64, ctypes.POINTER(sz)]
     lib.nms_lane_workspace_size.restype = ctypes.c_int
     lib.nms_lane_run.argtypes = [vp, vp, i64, f32, i32, vp, i64, vp, vp, vp, sz, vp]
@@ -120,6 +122,10 @@ def nms_mapped_pointer(host_ptr: int) -> Optional[int]:
     out = ctypes.c_void_p()
     st = load().nms_mapped_pointer(ctypes.c_void_p(host_ptr), ctypes.byref(out))
     return out.value if st == NMS_OK and out.value else None
+
+
+def nms_copy(dst: int, src: int, nbytes: int, stream: int) -> int:
+    return load().nms_copy(dst or None, src or None, int(nbytes), stream or None)
 
 
 def nms_workspace_size(n: int, batch: int = 0, num_classes: int = 0) -> int:
@@ -386,9 +392,10 @@ class HostPipeline:
     the indices), valid until the next call.
 
     With ``zero_copy`` (the default, when the pinned buffers are mapped into
-    the device address space) the kernels read the input from host memory and
-    write the count and the kept indices there themselves: the graph is the
-    nms_run kernels alone.  Otherwise it is a host->device copy of the input,
+    the device address space) the kernels move the data across the host link
+    themselves: a copy kernel (nms_copy) stages the input into device memory in
+    one pass, and the resolve writes the count and the kept indices into the
+    pinned output.  Otherwise the graph is a host->device copy of the input,
     the kernels and a device->host copy of the count and the output capacity.
     """
 
@@ -396,22 +403,24 @@ class HostPipeline:
         torch = _torch()
         self.n_max = int(n_max)
         self.device = torch.device(device)
-        self._h_in = torch.empty(max(5 * self.n_max, 4), dtype=torch.float32).pin_memory()
+        # 16 spare bytes: the staging copy moves whole 16-byte words
+        self._h_in = torch.empty(5 * self.n_max + 4, dtype=torch.float32).pin_memory()
         self._h_out = torch.empty(self.n_max + 1, dtype=torch.int64).pin_memory()
         self._status = torch.empty(1, dtype=torch.int32, device=self.device)
         self._out_np = self._h_out.numpy()
         self.workspace = Workspace(self.n_max, device=self.device)
         self._graphs = {}
+        self._d_in = torch.empty(5 * self.n_max + 4, dtype=torch.float32, device=self.device)
+        self._in_addr = self._d_in.data_ptr()
         self.zero_copy = False
         if zero_copy:
             din, dout = nms_mapped_pointer(self._h_in.data_ptr()), nms_mapped_pointer(self._h_out.data_ptr())
             if din is not None and dout is not None:
                 self.zero_copy = True
-                self._in_addr, self._out_addr = din, dout
+                self._h_in_dev, self._out_addr = din, dout
         if not self.zero_copy:
-            self._d_in = torch.empty(max(5 * self.n_max, 4), dtype=torch.float32, device=self.device)
             self._d_out = torch.empty(self.n_max + 1, dtype=torch.int64, device=self.device)
-            self._in_addr, self._out_addr = self._d_in.data_ptr(), self._d_out.data_ptr()
+            self._out_addr = self._d_out.data_ptr()
         self.set_n(self.n_max)
 
     def set_n(self, n: int) -> None:
@@ -446,7 +455,11 @@ class HostPipeline:
 
     def _enqueue(self, n, iou_thr, score_thr, max_out, stream):
         cap = keep_capacity(n, None, max_out)
-        if not self.zero_copy:
+        if self.zero_copy:
+            st = nms_copy(self._d_in.data_ptr(), self._h_in_dev, (20 * n + 15) // 16 * 16, stream.cuda_stream)
+            if st != NMS_OK:
+                raise NmsError(st, "nms_copy")
+        else:
             self._d_in[: 5 * n].copy_(self._h_in[: 5 * n], non_blocking=True)
         base_in, base_out = self._in_addr, self._out_addr
         st = nms_run(base_in if n else 0, base_in + 16 * n if n else 0, n, 0, 0, 0, 0, iou_thr,

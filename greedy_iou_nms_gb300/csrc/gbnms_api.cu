@@ -210,6 +210,15 @@ extern "C" nms_status nms_mapped_pointer(const void* host_ptr, void** device_ptr
     return NMS_OK;
 }
 
+extern "C" nms_status nms_copy(void* dst, const void* src, size_t bytes, void* stream)
+{
+    if (bytes == 0) return NMS_OK;
+    if (!dst || !src) return NMS_ERR_INVALID_ARG;
+    cudaGetLastError();
+    launch_copy(dst, src, bytes, static_cast<cudaStream_t>(stream));
+    return cuda_status();
+}
+
 extern "C" nms_status nms_workspace_size(int64_t n, int32_t batch, int32_t num_classes,
                                          size_t* bytes)
 {

@@ -191,4 +191,8 @@ struct BatchedArgs {
 
 void launch_batched(const BatchedArgs& a, cudaStream_t st, const Stamps& stamps);
 
+// dst[0..bytes) = src[0..bytes) by every SM (programmatic dependent launch;
+// it waits for the previous kernel before writing dst).
+void launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t st);
+
 }  // namespace gbnms

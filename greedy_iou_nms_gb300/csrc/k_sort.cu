@@ -171,6 +171,7 @@ bucket_rank_kernel(const float* __restrict__ scores, const float4* __restrict__ 
     __shared__ uint64_t ckey[BR_CAND];  // this CTA's candidates
     __shared__ int crank[BR_CAND];
     pdl_release();  // the mask kernel may be scheduled (it waits for this grid's results)
+    pdl_wait();     // a kernel before nms_run (a staging copy, a previous call) has finished
     const int tid = threadIdx.x;
     const int c0 = blockIdx.y * MS_CHUNK;
     const int q0 = c0 + blockIdx.x * BR_CAND;  // this CTA's candidates [q0, q0 + BR_CAND)
@@ -430,12 +431,12 @@ void launch_sort(const float* scores, const float4* boxes, const int* cand, cons
     const dim3 grid(per_chunk > 0 ? per_chunk : 1, chunks);
     if (chunks == 1) {
         ensure_dynamic_smem(reinterpret_cast<const void*>(bucket_rank_kernel<BR_THREADS_ONE>), rank_smem);
-        bucket_rank_kernel<BR_THREADS_ONE><<<grid, BR_THREADS_ONE, rank_smem, st>>>(
-            scores, boxes, cand, m_dev, m_bound, k0, perm, boxes_s, status, rowbits, NB, ecount, haspred, zero8);
+        launch_pdl(bucket_rank_kernel<BR_THREADS_ONE>, grid, dim3(BR_THREADS_ONE), rank_smem, st, scores, boxes,
+                   cand, m_dev, m_bound, k0, perm, boxes_s, status, rowbits, NB, ecount, haspred, zero8);
     } else {
         ensure_dynamic_smem(reinterpret_cast<const void*>(bucket_rank_kernel<BR_THREADS_MULTI>), rank_smem);
-        bucket_rank_kernel<BR_THREADS_MULTI><<<grid, BR_THREADS_MULTI, rank_smem, st>>>(
-            scores, boxes, cand, m_dev, m_bound, k0, perm, boxes_s, status, rowbits, NB, ecount, haspred, zero8);
+        launch_pdl(bucket_rank_kernel<BR_THREADS_MULTI>, grid, dim3(BR_THREADS_MULTI), rank_smem, st, scores, boxes,
+                   cand, m_dev, m_bound, k0, perm, boxes_s, status, rowbits, NB, ecount, haspred, zero8);
     }
     if (chunks == 1) return;
     const int tiles = chunks * (MS_CHUNK / ML_TILE);

@@ -84,6 +84,23 @@ nms_status nms_workspace_size(int64_t n, int32_t batch, int32_t num_classes, siz
 nms_status nms_mapped_pointer(const void* host_ptr, void** device_ptr);
 
 /*
+ * Copies bytes from src to dst with every SM, for a caller whose input sits in
+ * mapped page-locked host memory (nms_mapped_pointer): one pass across the
+ * host link into a device buffer, which nms_run then reads.  Read in place,
+ * the same input would cross the link many times (each CTA of the score sort
+ * reads every score).
+ *   dst, src       device addresses (either may be mapped host memory); the
+ *                  ranges must not overlap.  16-byte aligned pointers and a
+ *                  size that is a multiple of 16 take 16-byte accesses.
+ *   bytes          bytes to copy (0: nothing is enqueued).
+ *   stream         cudaStream_t; the copy waits for the stream's previous
+ *                  kernel before it writes dst (programmatic dependent launch).
+ * Errors: NMS_ERR_INVALID_ARG (NULL dst or src with bytes > 0),
+ *         NMS_ERR_CUDA.  Asynchronous; ownership stays with the caller.
+ */
+nms_status nms_copy(void* dst, const void* src, size_t bytes, void* stream);
+
+/*
  * Greedy IoU NMS.
  *
  *   boxes          device fp32 [n][4] xyxy, 16-byte aligned (see

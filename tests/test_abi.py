@@ -84,6 +84,14 @@ def test_mapped_pointer_rejects_other_memory(lib):
     assert g.nms_mapped_pointer(np.zeros(16, np.float32).ctypes.data) is None
 
 
+def test_copy_entry_validation(lib):
+    # NULL pointers with bytes to copy are refused on the host; nothing to
+    # copy enqueues nothing (no GPU needed for either).
+    assert g.nms_copy(0, 0, 0, 0) == g.NMS_OK
+    assert g.nms_copy(0, 16, 16, 0) == g.NMS_ERR_INVALID_ARG
+    assert g.nms_copy(16, 0, 16, 0) == g.NMS_ERR_INVALID_ARG
+
+
 def test_mask_row_words(lib):
     assert g.nms_mask_row_words(0) == 0
     assert g.nms_mask_row_words(1) == 4

@@ -458,9 +458,10 @@ def test_max_out_needs_the_rest_of_the_mask(max_out, score_thr):
 
 @pytest.mark.parametrize("zero_copy", [True, False])
 def test_host_pipeline_matches_oracle(zero_copy):
-    """HostPipeline, with the kernels reading and writing the pinned host
-    buffers in place (zero_copy) or with one packed host->device copy in and
-    one device->host copy out: the kept indices equal the oracle's, for
+    """HostPipeline, with the kernels moving the data across the host link
+    (zero_copy: a copy kernel stages the pinned input, the resolve writes the
+    pinned output) or with one packed host->device copy in and one
+    device->host copy out: the kept indices equal the oracle's, for
     several sizes in one pipeline (the tail of the buffers is reused), and a
     later call sees new inputs written into the same buffer."""
     pipe = g.HostPipeline(9000, zero_copy=zero_copy)
@@ -479,6 +480,26 @@ def test_host_pipeline_matches_oracle(zero_copy):
         assert pipe.run(wl.iou_thr, None, mo).tolist() == exp.tolist()
     pipe.set_n(0)
     assert len(pipe.run(0.5)) == 0
+
+
+@pytest.mark.parametrize("nbytes,offset", [(163840, 0), (20 * 1001 + 4, 0), (37, 3), (16, 16)])
+def test_copy_entry(nbytes, offset):
+    """nms_copy: from mapped pinned host memory and from device memory into a
+    device buffer, 16-byte words when the pointers and size allow and bytes
+    otherwise (odd sizes, misaligned ends); the bytes around the range stay."""
+    rng = np.random.default_rng(nbytes)
+    src = torch.from_numpy(rng.integers(0, 256, nbytes + 64, dtype=np.uint8)).pin_memory()
+    hsrc = g.nms_mapped_pointer(src.data_ptr())
+    dsrc = src.cuda()
+    stream = torch.cuda.current_stream().cuda_stream
+    for s_addr in (hsrc + offset, dsrc.data_ptr() + offset):
+        dst = torch.full((nbytes + 64,), 7, dtype=torch.uint8, device="cuda")
+        assert g.nms_copy(dst.data_ptr() + offset, s_addr, nbytes, stream) == g.NMS_OK
+        torch.cuda.synchronize()
+        out = dst.cpu().numpy()
+        assert np.array_equal(out[offset:offset + nbytes], src.numpy()[offset:offset + nbytes])
+        assert (out[:offset] == 7).all() and (out[offset + nbytes:] == 7).all()
+    assert g.nms_copy(dsrc.data_ptr(), hsrc, 0, stream) == g.NMS_OK  # nothing to do
 
 
 def test_mapped_pointer():

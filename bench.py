@@ -248,11 +248,10 @@ def cpu_oracle_run(wl, budget_s: float):
     return wl.n * reps / dt, reps, dt
 
 
-def cpu_all_cores_run(wl, budget_s: float):
-    """Time the multi-core CPU baseline (OpenMP bitmask and resolve,
-    oracle/cpu_baseline.c) on full copies of the workload for about budget_s
-    seconds.  Returns (boxes/s, reps, seconds, threads)."""
+def cpu_all_cores_child(name: str, budget_s: float) -> dict:
+    """The all-core timing loop of cpu_all_cores_run, in a process of its own."""
     import oracle
+    wl = W.make(name, 0)
     oracle.build_cpu_baseline()
     kw = dict(class_ids=wl.class_ids, batch_offsets=wl.batch_offsets, score_thr=wl.score_thr, max_out=wl.max_out)
     oracle.cpu_baseline_nms(wl.boxes, wl.scores, wl.iou_thr, **kw)  # warm-up (thread pool, pages)
@@ -263,7 +262,21 @@ def cpu_all_cores_run(wl, budget_s: float):
         dt = time.perf_counter() - t0
         if dt >= budget_s:
             break
-    return wl.n * reps / dt, reps, dt, oracle.cpu_baseline_threads()
+    return {"value": wl.n * reps / dt, "reps": reps, "secs": dt, "threads": oracle.cpu_baseline_threads()}
+
+
+def cpu_all_cores_run(wl, budget_s: float):
+    """Time the multi-core CPU baseline (OpenMP bitmask and resolve,
+    oracle/cpu_baseline.c) on full copies of workload wl (by its config name)
+    for about budget_s seconds, in a child process: in this one PyTorch's own
+    thread pool competes for the cores (the baseline ran 4 times slower).
+    Returns (boxes/s, reps, seconds, threads)."""
+    code = ("import sys, json; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.cpu_all_cores_child(sys.argv[1], float(sys.argv[2]))))" % ROOT)
+    out = subprocess.run([sys.executable, "-c", code, wl.name, str(budget_s)], capture_output=True, text=True,
+                         check=True, cwd=ROOT).stdout
+    r = json.loads(out.strip().splitlines()[-1])
+    return r["value"], r["reps"], r["secs"], r["threads"]
 
 
 def run_reference(args):

@@ -413,10 +413,13 @@ def _parallel_chains(n_chains, length, step=0.3):
     return b[perm], s[perm]
 
 
-@pytest.mark.parametrize("n_chains,length", [(100, 60), (64, 200), (8, 700), (1, 40)])
+@pytest.mark.parametrize("n_chains,length", [(100, 60), (64, 200), (64, 400), (8, 700), (1, 40)])
 def test_dependency_chains_of_many_links(n_chains, length):
     """Chains deep enough to take many rounds of the sparse-graph resolve (and
-    the longest ones past its round limit, where the walk takes over)."""
+    the longest ones past its round limit, where the walk takes over).  64
+    chains of 400 links (25600 boxes, a round limit of 416, about 25 K pairs
+    in one CTA) take about 306 passes (320 links took 257), past the wrap
+    of the pass number that the per-box bytes hold."""
     b, s = _parallel_chains(n_chains, length)
     for thr in (0.5, 0.3):
         _check_single(b, s, thr)

@@ -50,7 +50,7 @@ struct SingleLayout {
     int64_t ldw = 0;
     int NB = 0;  // 64-bit words of the per-row chunk bitmap
     unsigned ecap = 0;   // pairs one CTA's graph path holds (0: no list, the walk resolves)
-    unsigned lcap = 0;   // pairs the list holds (more when the all-SM graph path exists)
+    unsigned lcap = 0;   // pairs the list holds (graph_list_cap: more than ecap when it fits)
     bool grid = false;   // the all-SM graph path exists at this size
     size_t status, m_count, ecount, done, cand, perm, boxes_s, keys, rowbits, edges, haspred, gstate,
         gctl, mask, total;
@@ -66,7 +66,7 @@ SingleLayout single_layout(int64_t n)
     s.ecap = graph_edge_cap(static_cast<int>(n));
     const unsigned gcap = graph_grid_cap(static_cast<int>(n));
     s.grid = gcap > s.ecap;
-    s.lcap = s.grid ? gcap : s.ecap;
+    s.lcap = graph_list_cap(static_cast<int>(n));
     s.status = L.add(4);
     s.m_count = L.add(4);
     s.ecount = L.add(4);
@@ -354,7 +354,7 @@ nms_status run_impl(const float* boxes, const float* scores, int64_t n, const in
                                   limit, done_in, done_out, gctl + 4 + stage, gstate, gctl);
                 gd = gctl + 4 + stage;
             }
-            launch_resolve_single(mask, L.ldw, rowbits, L.NB, edges, ecount, haspred, m_count, nb, perm,
+            launch_resolve_single(mask, L.ldw, rowbits, L.NB, edges, ecount, L.lcap, haspred, m_count, nb, perm,
                                   max_out, keep, counts, status, st, limit, done_in, done_out, gd);
         };
         if (k1 >= n) {
@@ -659,7 +659,8 @@ namespace {
 
 struct LaneLayout {
     SingleLayout s;
-    size_t xs, span, flag, total;
+    size_t xs, span, flag, pre_planes, pre_count, pre_edges, total;
+    size_t plane = 0;  // bytes of each prepass byte plane
 };
 
 LaneLayout lane_layout(int64_t n)
@@ -672,6 +673,12 @@ LaneLayout lane_layout(int64_t n)
     L.xs = X.add(4 * static_cast<size_t>(NMS_LANE_ROWS) * ld);
     L.span = X.add(4 * ld);
     L.flag = X.add(4 * ld);
+    // The graph prepass (lane lists are dense cliques): its removed and
+    // blocked planes, its pair count and the pairs it leaves.
+    L.plane = graph_pre_plane_bytes(static_cast<int>(n));
+    L.pre_planes = X.add(2 * L.plane);
+    L.pre_count = X.add(4);
+    L.pre_edges = X.add(4 * static_cast<size_t>(L.s.lcap));
     L.total = X.total;
     return L;
 }
@@ -720,11 +727,21 @@ extern "C" nms_status nms_lane_run(const float* props, const float* scores, int6
     // count, the per-row chunk bits and the neighbour bitmap.
     launch_sort(scores, nullptr, nullptr, nullptr, nb, perm, nullptr, keys, status, rowbits, L.s.NB, ecount,
                 haspred, nullptr, st);
+    GraphPre pre{};
+    if (edges) {
+        pre.edges = at<uint32_t>(workspace, L.pre_edges);
+        pre.ecount = at<unsigned>(workspace, L.pre_count);
+        pre.cap = L.s.lcap;
+        pre.removed = at<uint8_t>(workspace, L.pre_planes);
+        pre.blocked = pre.removed + L.plane;
+    }
     launch_lane_mask(props, perm, nb, dist_thr, at<float>(workspace, L.xs), at<uint32_t>(workspace, L.span),
                      at<uint32_t>(workspace, L.flag), mask, L.s.ldw, rowbits, L.s.NB, edges, ecount, L.s.lcap,
-                     L.s.ecap ? haspred : nullptr, st);
-    launch_resolve_single(mask, L.s.ldw, rowbits, L.s.NB, edges, ecount, L.s.ecap ? haspred : nullptr, nullptr, nb,
-                          perm, max_out, keep, count, status, st);
+                     L.s.ecap ? haspred : nullptr, st, edges ? pre.removed : nullptr, 2 * L.plane, pre.ecount);
+    if (edges) launch_graph_prepass(edges, ecount, L.s.lcap, haspred, nb, pre, st);
+    launch_resolve_single(mask, L.s.ldw, rowbits, L.s.NB, edges, ecount, L.s.lcap, L.s.ecap ? haspred : nullptr,
+                          nullptr, nb, perm, max_out, keep, count, status, st, 1 << 30, nullptr, nullptr, nullptr,
+                          edges ? &pre : nullptr);
     return cuda_status();
 }
 
@@ -762,7 +779,7 @@ extern "C" nms_status nms_resolve_mask(const uint64_t* mask, int64_t n, const in
         cudaMemsetAsync(count, 0, sizeof(int64_t), st);
         return cuda_status();
     }
-    launch_resolve_single(mask, L.ldw, nullptr, 1, nullptr, nullptr, nullptr, nullptr,
+    launch_resolve_single(mask, L.ldw, nullptr, 1, nullptr, nullptr, 0u, nullptr, nullptr,
                           static_cast<int>(n), perm, max_out, keep, count, nullptr, st);
     return cuda_status();
 }

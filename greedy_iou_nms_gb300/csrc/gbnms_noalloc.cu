@@ -31,7 +31,7 @@ extern "C" nms_status nms_resolve_mask_noalloc(const uint64_t* mask, int64_t n, 
         cudaMemsetAsync(count, 0, sizeof(int64_t), st);
         return cudaGetLastError() == cudaSuccess ? NMS_OK : NMS_ERR_CUDA;
     }
-    launch_resolve_single(mask, nms_mask_row_words(n), nullptr, 1, nullptr, nullptr, nullptr, nullptr,
+    launch_resolve_single(mask, nms_mask_row_words(n), nullptr, 1, nullptr, nullptr, 0u, nullptr, nullptr,
                           static_cast<int>(n), perm, max_out, keep, count, nullptr, st);
     return cudaGetLastError() == cudaSuccess ? NMS_OK : NMS_ERR_CUDA;
 }

@@ -86,15 +86,45 @@ void launch_iou_mask(const float4* boxes_s, const int* m_dev, int m_bound, const
                      cudaStream_t st, int col_lo = 0, int col_hi = 1 << 30, const int* done = nullptr);
 size_t resolve_smem_bytes(int m_bound, int NB);
 unsigned graph_edge_cap(int m_bound);
+// Passes 0 and 1 of the graph resolve over all SMs (launch_graph_prepass):
+// the pairs left after them (edges, up to cap, their count in *ecount), the
+// removed byte of each box after pass 0 (removed) and a 3 for each box that
+// pass 1 blocked (blocked).  removed and blocked hold 32 * ((n + 127) / 128
+// * 4) bytes each; they and *ecount must be zero before the mask runs.
+struct GraphPre {
+    uint32_t* edges;
+    unsigned* ecount;
+    unsigned cap;
+    uint8_t* removed;
+    uint8_t* blocked;
+};
+inline size_t graph_pre_plane_bytes(int n) { return 32 * static_cast<size_t>(((n + 31) / 32 + 3) & ~3); }
+// When the mask's list is complete (*ecount <= lcap) and longer than one
+// CTA's shared memory (> graph_edge_cap): pass 0 stores removed = 1 for the
+// target of every pair whose source has no source of its own; pass 1 keeps
+// the pairs whose source has a source and is not removed, compacted into
+// pre.edges, and stores blocked = 3 for their targets.  Otherwise nothing.
+void launch_graph_prepass(const uint32_t* edges, const unsigned* ecount, unsigned lcap, const uint64_t* haspred,
+                          int n, const GraphPre& pre, cudaStream_t st);
+
+// Pairs the list of m_bound boxes holds: graph_grid_cap where the all-SM
+// path exists, else up to 32 times graph_edge_cap (whose first passes the
+// resolve runs from global memory).
+unsigned graph_list_cap(int m_bound);
 // Resolves boxes [0, min(n, limit)).  done_in set on the device: nothing to
 // do; done_out: set to 1 when the call found max_out kept boxes or covered
-// all n boxes (a later stage then has nothing to do).
+// all n boxes (a later stage then has nothing to do).  lcap: the pairs the
+// list edges holds; on the last stage, with no grid_done, a list longer than
+// one CTA's shared memory is resolved from global memory (and compacted in
+// place).  pre: launch_graph_prepass ran over the list (one stage, all n
+// boxes), and the resolve starts from its results.
 void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* rowbits, int NB,
-                           const uint32_t* edges, const unsigned* ecount,
+                           uint32_t* edges, const unsigned* ecount, unsigned lcap,
                            const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm,
                            int max_out, int64_t* keep, int64_t* counts, int32_t* status,
                            cudaStream_t st, int limit = 1 << 30, const int* done_in = nullptr,
-                           int* done_out = nullptr, const int* grid_done = nullptr);
+                           int* done_out = nullptr, const int* grid_done = nullptr,
+                           const GraphPre* pre = nullptr);
 
 // Pair-list capacity of the all-SM graph path (0 below its size range) and
 // its scratch: graph_grid_state_bytes of bitmaps and a control block.
@@ -117,10 +147,13 @@ void launch_graph_grid(uint32_t* edges, const unsigned* ecount, const uint64_t* 
 // Lane candidates (k_lane.cu): the SoA stride for n lanes, and the gather
 // and mask launches over the sorted permutation (outputs in the layout of
 // launch_iou_mask).  xs: 72 x lane_ld(n) floats; span, flag: lane_ld(n) each.
+// The gather also zeroes zero_bytes (a multiple of 16, 16-byte aligned) at
+// zero and *zcount.
 int lane_ld(int n);
 void launch_lane_mask(const float* props, const int* perm, int n, float thr, float* xs, uint32_t* span,
                       uint32_t* flag, uint64_t* mask, int64_t ldw, uint64_t* rowbits, int NB, uint32_t* edges,
-                      unsigned* ecount, unsigned ecap, uint64_t* haspred, cudaStream_t st);
+                      unsigned* ecount, unsigned ecap, uint64_t* haspred, cudaStream_t st, void* zero = nullptr,
+                      size_t zero_bytes = 0, unsigned* zcount = nullptr);
 
 // Fast NMS output of one image: the boxes whose bit in haspred is clear, in
 // sorted order, mapped through perm, cut at max_out.

@@ -14,7 +14,8 @@
 //   gather: the sorted lanes' x as 72 rows of n floats (row-major, so a
 //           warp's lanes are contiguous), NaN in the rows a lane does not
 //           cover, its row span, and a flag for a lane with a non-finite x
-//           in a covered row;
+//           in a covered row; 32 lanes a CTA, transposed through shared
+//           memory;
 //   mask:   one CTA of 256 threads per 64 x 64 tile of the upper triangle;
 //           thread (q, r) holds row lane r's 72 x in registers and takes 16
 //           of the tile's 64 column lanes (staged in shared memory, negated,
@@ -27,7 +28,10 @@
 //           on the original values instead.  The words, the per-row chunk
 //           bits, the neighbour bitmap and the pair list come out in the
 //           layout of the box mask kernel, so the resolve is the same;
-//   resolve: launch_resolve_single (rounds over the pair list, or the walk).
+//   resolve: lane lists are dense cliques, so passes 0 and 1 of the graph
+//           rounds run on all SMs first (launch_graph_prepass), then
+//           launch_resolve_single (rounds over the pairs they leave, or the
+//           walk).
 #include <cstdint>
 
 #include "common.cuh"
@@ -70,33 +74,74 @@ __device__ float lane_distance_exact(const float* __restrict__ a, const float* _
 
 // Sorted lanes to the mask kernel's layout: xs[k * ld + p] = x_k of the lane
 // at sorted position p (NaN where it does not cover row k), span[p], and
-// flag[p] = 1 when a covered row holds a non-finite x.
-__global__ void __launch_bounds__(256)
+// flag[p] = 1 when a covered row holds a non-finite x.  A CTA takes 32 sorted
+// lanes: its warps copy the lanes' 77-value records into shared memory
+// (contiguous loads; the odd record length keeps the transposed reads
+// conflict-free), then warp w writes rows w, w + 8, ... of all 32 lanes
+// (128-byte stores).  Also zeroes z16 16-byte words at zero and the word
+// *zcount (the graph prepass's state).
+constexpr int LG_LANES = 32;
+constexpr int LG_THREADS = 256;
+static_assert(LN_TILE % LG_LANES == 0, "ld, a multiple of the tile, is a multiple of a CTA's lanes");
+__global__ void __launch_bounds__(LG_THREADS)
 lane_gather_kernel(const float* __restrict__ props, const int* __restrict__ perm, int n, int ld,
-                   float* __restrict__ xs, uint32_t* __restrict__ span, uint32_t* __restrict__ flag)
+                   float* __restrict__ xs, uint32_t* __restrict__ span, uint32_t* __restrict__ flag,
+                   uint4* __restrict__ zero, int z16, unsigned* __restrict__ zcount)
 {
+    __shared__ float rec[LG_LANES][LN_VALUES];
+    __shared__ uint32_t bad_s[LG_LANES];
+    static_assert(LN_VALUES % 2 == 1, "an odd record length spreads a column over the banks");
     pdl_wait();
     pdl_release();
-    const int p = blockIdx.x * blockDim.x + threadIdx.x;
-    if (p >= ld) return;
-    if (p >= n) {  // padding lanes: no rows
-        for (int k = 0; k < LN_ROWS; ++k) xs[static_cast<int64_t>(k) * ld + p] = __int_as_float(0x7fc00000);
-        span[p] = 0u;
-        flag[p] = 0u;
-        return;
+    const int tid = threadIdx.x, warp = tid >> 5, l = tid & 31;
+    const int g = blockIdx.x * LG_THREADS + tid;
+    for (int q = g; q < z16; q += gridDim.x * LG_THREADS) zero[q] = make_uint4(0u, 0u, 0u, 0u);
+    if (g == 0 && zcount) *zcount = 0u;
+    const int p0 = blockIdx.x * LG_LANES;
+    // Warp w stages lanes w, w + 8, w + 16, w + 24: their four perm loads,
+    // then all their record loads, are in flight together.
+    constexpr int RPW = LG_LANES / (LG_THREADS / 32);  // records a warp stages
+    constexpr int CPR = (LN_VALUES + 31) / 32;          // loads a lane per record
+    int src[RPW];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i) {
+        const int r = warp + i * (LG_THREADS / 32);
+        src[i] = p0 + r < n ? perm[p0 + r] : -1;
     }
-    const float* src = props + static_cast<int64_t>(perm[p]) * LN_VALUES;
-    const uint32_t sp = lane_span(src);
+    float v[RPW][CPR];
+#pragma unroll
+    for (int i = 0; i < RPW; ++i)
+#pragma unroll
+        for (int c = 0; c < CPR; ++c) {
+            const int col = l + 32 * c;
+            v[i][c] = src[i] >= 0 && col < LN_VALUES ? props[static_cast<int64_t>(src[i]) * LN_VALUES + col] : 0.0f;
+        }
+#pragma unroll
+    for (int i = 0; i < RPW; ++i)
+#pragma unroll
+        for (int c = 0; c < CPR; ++c) {
+            const int col = l + 32 * c;
+            if (src[i] >= 0 && col < LN_VALUES) rec[warp + i * (LG_THREADS / 32)][col] = v[i][c];
+        }
+    if (tid < LG_LANES) bad_s[tid] = 0u;
+    __syncthreads();
+    const int p = p0 + l;  // < ld: the grid covers ld lanes exactly
+    const bool real = p < n;
+    const uint32_t sp = real ? lane_span(&rec[l][0]) : 0u;
     const int lo = static_cast<int>(sp & 255u), hi = static_cast<int>(sp >> 8);
     uint32_t bad = 0u;
-    for (int k = 0; k < LN_ROWS; ++k) {
-        const float x = src[LN_X0 + k];
-        const bool cov = k >= lo && k < hi;
+    for (int k = warp; k < LN_ROWS; k += LG_THREADS / 32) {
+        const bool cov = k >= lo && k < hi;  // never for a padding lane (sp = 0)
+        const float x = cov ? rec[l][LN_X0 + k] : __int_as_float(0x7fc00000);
         if (cov && !(fabsf(x) <= 3.4028235e38f)) bad = 1u;
-        xs[static_cast<int64_t>(k) * ld + p] = cov ? x : __int_as_float(0x7fc00000);
+        xs[static_cast<int64_t>(k) * ld + p] = x;
     }
-    span[p] = sp;
-    flag[p] = bad;
+    if (bad) atomicOr(&bad_s[l], 1u);
+    __syncthreads();
+    if (warp == 0) {
+        span[p] = sp;
+        flag[p] = bad_s[l];
+    }
 }
 
 // Linear tile index -> (row tile a, column tile c), a <= c, column by column.
@@ -252,11 +297,13 @@ int lane_ld(int n) { return (n + LN_TILE - 1) / LN_TILE * LN_TILE; }
 
 void launch_lane_mask(const float* props, const int* perm, int n, float thr, float* xs, uint32_t* span,
                       uint32_t* flag, uint64_t* mask, int64_t ldw, uint64_t* rowbits, int NB, uint32_t* edges,
-                      unsigned* ecount, unsigned ecap, uint64_t* haspred, cudaStream_t st)
+                      unsigned* ecount, unsigned ecap, uint64_t* haspred, cudaStream_t st, void* zero,
+                      size_t zero_bytes, unsigned* zcount)
 {
     if (n <= 0) return;
     const int ld = lane_ld(n);
-    launch_pdl(lane_gather_kernel, dim3((ld + 255) / 256), dim3(256), 0, st, props, perm, n, ld, xs, span, flag);
+    launch_pdl(lane_gather_kernel, dim3(ld / LG_LANES), dim3(LG_THREADS), 0, st, props, perm, n, ld, xs, span, flag,
+               static_cast<uint4*>(zero), zero ? static_cast<int>(zero_bytes / 16) : 0, zcount);
     const int T = ld / LN_TILE;
     launch_pdl(lane_mask_kernel, dim3(T * (T + 1) / 2), dim3(LN_THREADS), 0, st, xs,
                static_cast<const uint32_t*>(span), static_cast<const uint32_t*>(flag), props, perm, n, ld, thr, mask,

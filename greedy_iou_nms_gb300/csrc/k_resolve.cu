@@ -13,9 +13,12 @@
 // links even when the walk below would take thousands of steps.  One CTA
 // keeps a byte per box (the last pass that blocked it), a removed byte per
 // box and the live pairs in shared memory; a round is one pass over the pairs
-// whose source is still open and one barrier (graph_resolve).  Lists beyond
-// one CTA above 16384 boxes go to graph_grid_kernel, the same rounds on every
-// SM with grid barriers.
+// whose source is still open and one barrier (graph_resolve).  Up to 16384
+// boxes, the first passes over a longer list run from global memory
+// (global_passes) until the rest fits; passes 0 and 1, which need no barrier
+// inside, can also run on every SM first (graph_pass0_kernel,
+// graph_pass1_kernel).  Lists beyond one CTA above 16384 boxes go to
+// graph_grid_kernel, the same rounds on every SM with grid barriers.
 //
 // Walk (everything else, and a caller's own mask):
 // "NMS CUDA代码学习", section Phase 2: one thread block walks the boxes from
@@ -279,6 +282,10 @@ __host__ __device__ __forceinline__ int graph_words(int m_bound) { return ((m_bo
 // resolved by graph_grid_kernel (all SMs, the list in global memory), up to
 // GR_GRID_MAX_PAIRS pairs.
 constexpr int GR_GRID_MIN_N = 16384;
+// Up to GR_GRID_MIN_N boxes the list holds GR_LIST_X times one CTA's pairs;
+// the first passes over a longer list than one CTA holds run from global
+// memory.
+constexpr unsigned GR_LIST_X = 32;
 constexpr unsigned GR_GRID_MAX_PAIRS = 1u << 24;
 constexpr int GG_THREADS = 1024;
 
@@ -294,6 +301,16 @@ unsigned graph_edge_cap(int m_bound)
     if (m_bound <= 0 || m_bound > GR_MAX_N) return 0;
     const long long room = GR_SMEM - 4ll * GR_HEAD - 64ll * graph_words(m_bound);
     return room > 0 ? static_cast<unsigned>((room / 4) & ~3ll) : 0u;
+}
+
+unsigned graph_list_cap(int m_bound)
+{
+    const unsigned e = graph_edge_cap(m_bound), g = graph_grid_cap(m_bound);
+    if (g > e) return g;
+    const unsigned long long all = static_cast<unsigned long long>(m_bound) * (m_bound - 1) / 2;
+    const unsigned long long x = static_cast<unsigned long long>(GR_LIST_X) * e;
+    const unsigned long long r = ((all + 3) & ~3ull) < x ? ((all + 3) & ~3ull) : x;
+    return r > e ? static_cast<unsigned>(r) : e;
 }
 
 size_t graph_smem_bytes(int m_bound)
@@ -355,6 +372,107 @@ __device__ __forceinline__ void write_kept(const uint8_t* RMb, int w0, int w1, i
     }
 }
 
+// Passes start, start + 1, ... of graph_resolve over a list too long for
+// shared memory,
+// straight from global memory (the per-box bytes FL and RMb stay in shared
+// memory).  Thread t owns the 16-byte quads t, t + RV_THREADS, ... of gedges
+// and packs its survivors in place into the pair slots of those quads (slot
+// s: quad t + RV_THREADS * (s / 4), element s % 4).  Four quads, sixteen
+// pairs, are taken a step, and the next step's quads are loaded before this
+// step's survivors are stored: a step stores only into quads it or an
+// earlier step has loaded.  The body is that of the rounds in shared memory
+// for every pass (in pass 0 an open source's store of 2 finds 2 already).
+// After each pass a block prefix counts the survivors; once they fit in cap
+// pairs each thread copies its own into Es at its prefix.  Returns the next
+// pass (*total: the pairs now in Es), or -1 after RV_GLOBAL_PASSES passes,
+// or at max_rounds, with too many left.
+constexpr int RV_GLOBAL_PASSES = 8;
+constexpr int GP_Q = 4;  // quads a step
+__device__ __forceinline__ uint32_t quad_at(const uint4& v, int i)
+{
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ int global_passes(uint32_t* __restrict__ gedges, unsigned E, unsigned cap, uint8_t* FL,
+                                             uint8_t* RMb, uint32_t* Es, int* scratch, int start,
+                                             int max_rounds, unsigned* total)
+{
+    const int tid = threadIdx.x;
+    const unsigned l = lane_id();
+    const int warp = tid >> 5;
+    uint4* Q = reinterpret_cast<uint4*>(gedges);
+    uint4* Qt = Q + tid;  // the thread's quads, RV_THREADS apart
+    // The thread's pairs: four per quad, less the padding of the last quad.
+    const unsigned nq = (E + 3) / 4;
+    const unsigned mine = nq > static_cast<unsigned>(tid) ? (nq - tid + RV_THREADS - 1) / RV_THREADS : 0u;
+    int live = static_cast<int>(4 * mine);
+    if (nq && (nq - 1) % RV_THREADS == static_cast<unsigned>(tid)) live -= static_cast<int>(4 * nq - E);
+    for (int round = start; round < start + RV_GLOBAL_PASSES && round < max_rounds; ++round) {
+        const uint32_t kept_f = static_cast<uint32_t>(round) & 0xffu;
+        const uint8_t blk_f = static_cast<uint8_t>(round + 2);
+        const int lq = (live + 3) >> 2;  // quads holding live pairs
+        uint4 cur[GP_Q];
+#pragma unroll
+        for (int u = 0; u < GP_Q; ++u) cur[u] = u < lq ? Qt[RV_THREADS * u] : make_uint4(0u, 0u, 0u, 0u);
+        int nl = 0;
+        for (int k0 = 0; k0 < lq; k0 += GP_Q) {
+            uint4 nxt[GP_Q];
+#pragma unroll
+            for (int u = 0; u < GP_Q; ++u)
+                nxt[u] = k0 + GP_Q + u < lq ? Qt[RV_THREADS * (k0 + GP_Q + u)] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int u = 0; u < 4 * GP_Q; ++u) {
+                if (4 * k0 + u >= live) break;
+                const uint32_t e = quad_at(cur[u >> 2], u & 3);
+                const uint32_t src = e >> 16, j = e & 0xffffu;
+                if (RMb[src]) continue;  // a removed source no longer matters
+                if (FL[src] == kept_f) {  // kept: the removal is final
+                    RMb[j] = 1;
+                    continue;
+                }
+                FL[j] = blk_f;  // open: blocks its target, the pair stays
+                gedges[4 * (tid + RV_THREADS * (nl >> 2)) + (nl & 3)] = e;
+                ++nl;
+            }
+#pragma unroll
+            for (int u = 0; u < GP_Q; ++u) cur[u] = nxt[u];
+        }
+        live = nl;
+        int x = nl;  // inclusive prefix of the survivors over the warp
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(FULL, x, d);
+            if (static_cast<int>(l) >= d) x += y;
+        }
+        if (l == 31) scratch[warp] = x;
+        __syncthreads();
+        int before = 0, tot = 0;
+#pragma unroll 8
+        for (int w = 0; w < RV_WARPS; ++w) {
+            const int v = scratch[w];
+            before += w < warp ? v : 0;
+            tot += v;
+        }
+        __syncthreads();  // scratch is written again after the next pass
+        if (static_cast<unsigned>(tot) <= cap) {
+            uint32_t* dst = Es + (before + x - nl);
+            const int sq = (nl + 3) >> 2;
+            for (int k0 = 0; k0 < sq; k0 += GP_Q) {
+                uint4 v[GP_Q];
+#pragma unroll
+                for (int u = 0; u < GP_Q; ++u)
+                    v[u] = k0 + u < sq ? Qt[RV_THREADS * (k0 + u)] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int u = 0; u < 4 * GP_Q; ++u)
+                    if (4 * k0 + u < nl) dst[4 * k0 + u] = quad_at(v[u >> 2], u & 3);
+            }
+            __syncthreads();
+            *total = static_cast<unsigned>(tot);
+            return round + 1;
+        }
+    }
+    return -1;
+}
+
 // Rounds over the pair list gedges[0..E) of n sorted boxes (haspred: bit j
 // set iff box j has a pair).  Returns false, with nothing written, when the
 // rounds outnumber the walk's tiles plus 16 (a long chain of dependencies:
@@ -381,11 +499,21 @@ __device__ __forceinline__ void write_kept(const uint8_t* RMb, int w0, int w1, i
 // blocked.  Its byte therefore starts at 2 (blocked in pass 0; 0 for a box
 // without a source), and pass 0 only removes: it reads no removed byte
 // (nothing is removed before it) and stores no block.
-__device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedges, unsigned E, unsigned cap_words,
+//
+// kLong: the list is longer than cap_words and is not staged; its first
+// passes run from global memory (global_passes), the rest here once the
+// survivors fit.  kPre: passes 0 and 1 were done over all SMs
+// (graph_pass0_kernel, graph_pass1_kernel): gedges holds the pairs left
+// after them, pre->removed the removed bytes and pre->blocked a 3 for each
+// box blocked in pass 1; the rounds start at pass 2.  Separate instances
+// keep the common one's code as it is.
+template <bool kLong, bool kPre>
+__device__ __forceinline__ bool graph_resolve(uint32_t* __restrict__ gedges, unsigned E, unsigned cap_words,
                               const uint32_t* __restrict__ haspred, int n, int NWp,
                               const int* __restrict__ perm, int max_out, int64_t* __restrict__ keep,
                               int64_t* __restrict__ counts, int32_t* status, uint32_t* sm,
-                              int* done_out)
+                              int* done_out, const uint8_t* __restrict__ pre_rm = nullptr,
+                              const uint8_t* __restrict__ pre_blk = nullptr)
 {
     int* scratch = reinterpret_cast<int*>(sm);
     unsigned long long* bar = reinterpret_cast<unsigned long long*>(sm + 32);
@@ -401,10 +529,10 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
     // to a multiple of 4 pairs) while the bitmaps are set up; the sort
     // permutation follows it when both fit (the output then maps positions
     // from shared memory).
-    const unsigned bytes = 16u * ((E + 3) / 4);
+    const unsigned bytes = kLong ? 0u : 16u * ((E + 3) / 4);
     const unsigned ncopy = (bytes + GR_COPY - 1) / GR_COPY;
     const unsigned pbytes = 16u * ((static_cast<unsigned>(n) + 3) / 4);
-    const bool perm_here = perm && (bytes + pbytes) / 4 <= cap_words;
+    const bool perm_here = !kLong && perm && (bytes + pbytes) / 4 <= cap_words;
     const int* perm_s = perm_here ? reinterpret_cast<const int*>(reinterpret_cast<const char*>(Es) + bytes) : nullptr;
     const unsigned pcopy = perm_here ? (pbytes + GR_COPY - 1) / GR_COPY : 0u;
     if (tid == 0) {
@@ -431,11 +559,21 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
 #pragma unroll
         for (int q = 0; q < 8; ++q) bx[q] = (((hp >> (4 * q)) & 0xfu) * 0x00204081u & 0x01010101u) << 1;  // bits -> 0/2
         uint4* fq = reinterpret_cast<uint4*>(FL + 32 * w);
-        fq[0] = make_uint4(bx[0], bx[1], bx[2], bx[3]);
-        fq[1] = make_uint4(bx[4], bx[5], bx[6], bx[7]);
         uint4* rq = reinterpret_cast<uint4*>(RMb + 32 * w);
-        rq[0] = make_uint4(0u, 0u, 0u, 0u);
-        rq[1] = make_uint4(0u, 0u, 0u, 0u);
+        if (kPre) {  // 2 | 3 = 3: a box blocked in pass 1 has a source
+            const uint4* bq = reinterpret_cast<const uint4*>(pre_blk + 32 * w);
+            const uint4 b0 = bq[0], b1 = bq[1];
+            fq[0] = make_uint4(bx[0] | b0.x, bx[1] | b0.y, bx[2] | b0.z, bx[3] | b0.w);
+            fq[1] = make_uint4(bx[4] | b1.x, bx[5] | b1.y, bx[6] | b1.z, bx[7] | b1.w);
+            const uint4* pq = reinterpret_cast<const uint4*>(pre_rm + 32 * w);
+            rq[0] = pq[0];
+            rq[1] = pq[1];
+        } else {
+            fq[0] = make_uint4(bx[0], bx[1], bx[2], bx[3]);
+            fq[1] = make_uint4(bx[4], bx[5], bx[6], bx[7]);
+            rq[0] = make_uint4(0u, 0u, 0u, 0u);
+            rq[1] = make_uint4(0u, 0u, 0u, 0u);
+        }
     }
     bool copied = true;
     if (tx) {
@@ -454,6 +592,14 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
         }
         return true;
     }
+    const int max_rounds = (n + 63) / 64 + 16;
+    int round0 = kPre ? 2 : 0;  // the first pass over the list in shared memory
+    if (kLong) {
+        unsigned left = 0;
+        round0 = global_passes(gedges, E, cap_words, FL, RMb, Es, scratch, round0, max_rounds, &left);
+        if (round0 < 0) return false;
+        E = left;
+    }
     // Warp w owns the pairs [wbeg, wbeg + cnt): 32 a step, one a lane, its
     // survivors packed in place at the front by a ballot.  A live pair in
     // pass r: a removed source no longer matters; a source that no open box
@@ -468,11 +614,10 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
     unsigned cnt = min(E, wbeg + chunk) - wbeg;
     uint32_t* Ew = Es + wbeg;
     const uint32_t lt = (1u << l) - 1u;
-    const int max_rounds = (n + 63) / 64 + 16;
     // Pass 0: a source without a source of its own (byte 0) is kept and
     // removes its target; every other pair stays.
-    bool any = false;
-    {
+    bool any = E > 0u;
+    if (round0 == 0) {
         unsigned out = 0;
         for (unsigned k = 0; k < cnt; k += 32) {
             const bool have = k + l < cnt;
@@ -487,7 +632,7 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
         cnt = out;
         any = __syncthreads_or(cnt > 0u);
     }
-    for (int round = 1; any; ++round) {
+    for (int round = round0 > 0 ? round0 : 1; any; ++round) {
         if (round == max_rounds) return false;
         const uint32_t kept_f = static_cast<uint32_t>(round) & 0xffu;
         const uint8_t blk_f = static_cast<uint8_t>(round + 2);
@@ -544,15 +689,18 @@ __device__ __forceinline__ bool graph_resolve(const uint32_t* __restrict__ gedge
     return true;
 }
 
+// kPre: passes 0 and 1 over a list longer than ecap ran on all SMs first
+// (launch_graph_prepass), their results in pre.
+template <bool kPre>
 __global__ void __launch_bounds__(RV_THREADS, 1)
 resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
                       const uint64_t* __restrict__ rowbits, int NB,
-                      const uint32_t* __restrict__ edges, const unsigned* __restrict__ ecount,
-                      unsigned ecap, const uint32_t* __restrict__ haspred,
+                      uint32_t* __restrict__ edges, const unsigned* __restrict__ ecount,
+                      unsigned ecap, unsigned lcap, const uint32_t* __restrict__ haspred,
                       const int* __restrict__ m_dev, int m_bound, const int* __restrict__ perm,
                       int max_out, int64_t* __restrict__ keep, int64_t* __restrict__ counts,
                       int32_t* status, int limit, const int* __restrict__ done_in, int* done_out,
-                      const int* __restrict__ grid_done)
+                      const int* __restrict__ grid_done, GraphPre pre)
 {
     extern __shared__ __align__(128) uint64_t smem[];
     __shared__ ResolveShared S;
@@ -564,10 +712,33 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
     const int n = min(n_all, limit);
     if (done_out && threadIdx.x == 0) *done_out = n >= n_all;  // raised below on max_out
     if (edges) {
+        // A list beyond shared memory is compacted in place by the first
+        // passes: only the last stage may do that, and only when no all-SM
+        // pass ran over it before.
         const unsigned E = *ecount;
-        if (E <= ecap && graph_resolve(edges, E, ecap, haspred, n, graph_words(m_bound), perm, max_out, keep, counts,
-                                       status, reinterpret_cast<uint32_t*>(smem), done_out))
-            return;
+        uint32_t* sm = reinterpret_cast<uint32_t*>(smem);
+        const int NWp = graph_words(m_bound);
+        if (E <= ecap) {
+            if (graph_resolve<false, false>(edges, E, ecap, haspred, n, NWp, perm, max_out, keep, counts, status,
+                                            sm, done_out))
+                return;
+        } else if (kPre && E <= lcap) {
+            // The pairs left after passes 0 and 1 (the list was complete).
+            const unsigned E2 = *pre.ecount;
+            if (E2 <= ecap) {
+                if (graph_resolve<false, true>(pre.edges, E2, ecap, haspred, n, NWp, perm, max_out, keep, counts,
+                                               status, sm, done_out, pre.removed, pre.blocked))
+                    return;
+            } else if (E2 <= pre.cap) {
+                if (graph_resolve<true, true>(pre.edges, E2, ecap, haspred, n, NWp, perm, max_out, keep, counts,
+                                              status, sm, done_out, pre.removed, pre.blocked))
+                    return;
+            }
+        } else if (!kPre && E <= lcap && !grid_done && n >= n_all) {
+            if (graph_resolve<true, false>(edges, E, ecap, haspred, n, NWp, perm, max_out, keep, counts, status,
+                                           sm, done_out))
+                return;
+        }
         __syncthreads();  // the walk reuses the shared memory
     }
     const int T = (n + 63) / 64;              // tiles
@@ -1046,19 +1217,135 @@ void launch_graph_grid(uint32_t* edges, const unsigned* ecount, const uint64_t* 
                        counts, status, done_in, done_out, grid_done, KRg, HBg, static_cast<GridCtl*>(ctl));
 }
 
+// Passes 0 and 1 of graph_resolve over all SMs, for a list longer than one
+// CTA's shared memory.  Neither needs a barrier inside: pass 0 keeps exactly
+// the sources without a source of their own (the clear bits of haspred) and
+// removes their targets; pass 1 keeps nothing (every box's byte is then 0 or
+// 2, never 1), drops the pairs whose source pass 0 removed and blocks the
+// targets of the rest.  Both are plain byte stores of one value.
+constexpr int GP_THREADS = 512;
+
+__device__ __forceinline__ bool has_source(const uint32_t* __restrict__ haspred, uint32_t i)
+{
+    return (haspred[i >> 5] >> (i & 31u)) & 1u;
+}
+
+__global__ void __launch_bounds__(GP_THREADS)
+graph_pass0_kernel(const uint32_t* __restrict__ edges, const unsigned* __restrict__ ecount, unsigned ecap,
+                   unsigned lcap, const uint32_t* __restrict__ haspred, uint8_t* __restrict__ removed)
+{
+    pdl_wait();  // the mask has finished
+    pdl_release();
+    const unsigned E = *ecount;
+    if (E <= ecap || E > lcap) return;  // one CTA holds it, or the list is incomplete
+    const unsigned nq = (E + 3) / 4;
+    const uint4* Q = reinterpret_cast<const uint4*>(edges);
+    for (unsigned q = blockIdx.x * GP_THREADS + threadIdx.x; q < nq; q += gridDim.x * GP_THREADS) {
+        const uint4 v = Q[q];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t e = quad_at(v, u);
+            if (4 * q + u < E && !has_source(haspred, e >> 16)) removed[e & 0xffffu] = 1;
+        }
+    }
+}
+
+// One tile of GP_THREADS quads a step: the kept pairs are counted by a block
+// prefix, one reservation in out per tile, and stored (none past ocap; the
+// count still grows, so the resolve sees the overflow).
+__global__ void __launch_bounds__(GP_THREADS)
+graph_pass1_kernel(const uint32_t* __restrict__ edges, const unsigned* __restrict__ ecount, unsigned ecap,
+                   unsigned lcap, const uint32_t* __restrict__ haspred, const uint8_t* __restrict__ removed,
+                   uint32_t* __restrict__ out, unsigned* __restrict__ ocount, unsigned ocap,
+                   uint8_t* __restrict__ blocked)
+{
+    constexpr int NWARP = GP_THREADS / 32;
+    __shared__ int wsum[NWARP];
+    __shared__ unsigned s_base;
+    pdl_wait();  // pass 0 has finished
+    pdl_release();
+    const unsigned E = *ecount;
+    if (E <= ecap || E > lcap) return;
+    const unsigned nq = (E + 3) / 4;
+    const unsigned tiles = (nq + GP_THREADS - 1) / GP_THREADS;
+    const uint4* Q = reinterpret_cast<const uint4*>(edges);
+    const unsigned l = lane_id();
+    const int warp = static_cast<int>(threadIdx.x) >> 5;
+    for (unsigned t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const unsigned q = t * GP_THREADS + threadIdx.x;
+        const uint4 v = q < nq ? Q[q] : make_uint4(0u, 0u, 0u, 0u);
+        uint32_t stay = 0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t e = quad_at(v, u), i = e >> 16;
+            if (q < nq && 4 * q + u < E && has_source(haspred, i) && !removed[i]) stay |= 1u << u;
+        }
+        const int c = __popc(stay);
+        int x = c;  // inclusive prefix over the warp
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(FULL, x, d);
+            if (static_cast<int>(l) >= d) x += y;
+        }
+        if (l == 31) wsum[warp] = x;
+        __syncthreads();
+        int before = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < NWARP; ++w) {
+            const int s = wsum[w];
+            before += w < warp ? s : 0;
+            total += s;
+        }
+        if (threadIdx.x == 0) s_base = total ? atomicAdd(ocount, static_cast<unsigned>(total)) : 0u;
+        __syncthreads();
+        const unsigned base = s_base;
+        const bool room = base <= ocap && static_cast<unsigned>(total) <= ocap - base;
+        unsigned o = base + static_cast<unsigned>(before + x - c);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (!((stay >> u) & 1u)) continue;
+            const uint32_t e = quad_at(v, u);
+            blocked[e & 0xffffu] = 3;
+            if (room) out[o] = e;
+            ++o;
+        }
+        __syncthreads();  // wsum and s_base are written again
+    }
+}
+
+void launch_graph_prepass(const uint32_t* edges, const unsigned* ecount, unsigned lcap, const uint64_t* haspred,
+                          int n, const GraphPre& pre, cudaStream_t st)
+{
+    if (n <= 0 || !edges || !ecount || !haspred || !pre.edges || !pre.ecount || !pre.removed || !pre.blocked)
+        return;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) return;
+    const unsigned ecap = graph_edge_cap(n);
+    const uint32_t* hp = reinterpret_cast<const uint32_t*>(haspred);
+    launch_pdl(graph_pass0_kernel, dim3(2 * sms), dim3(GP_THREADS), 0, st, edges, ecount, ecap, lcap, hp,
+               pre.removed);
+    launch_pdl(graph_pass1_kernel, dim3(2 * sms), dim3(GP_THREADS), 0, st, edges, ecount, ecap, lcap, hp,
+               static_cast<const uint8_t*>(pre.removed), pre.edges, pre.ecount, pre.cap, pre.blocked);
+}
+
 size_t resolve_smem_bytes(int m_bound, int NB) { return resolve_layout(m_bound, NB).total; }
 
 void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* rowbits, int NB,
-                           const uint32_t* edges, const unsigned* ecount,
+                           uint32_t* edges, const unsigned* ecount, unsigned lcap,
                            const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm,
                            int max_out, int64_t* keep, int64_t* counts, int32_t* status,
                            cudaStream_t st, int limit, const int* done_in, int* done_out,
-                           const int* grid_done)
+                           const int* grid_done, const GraphPre* pre)
 {
     size_t smem = resolve_smem_bytes(m_bound, NB);
     const unsigned ecap = edges ? graph_edge_cap(m_bound) : 0u;
     if (edges && graph_smem_bytes(m_bound) > smem) smem = graph_smem_bytes(m_bound);
-    ensure_dynamic_smem(reinterpret_cast<const void*>(resolve_single_kernel), smem);
+    if (!edges) pre = nullptr;
+    ensure_dynamic_smem(pre ? reinterpret_cast<const void*>(resolve_single_kernel<true>)
+                            : reinterpret_cast<const void*>(resolve_single_kernel<false>),
+                        smem);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(1);
     cfg.blockDim = dim3(RV_THREADS);
@@ -1067,9 +1354,16 @@ void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* ro
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = pdl_attr_count();
-    cudaLaunchKernelEx(&cfg, resolve_single_kernel, mask, ldw, rowbits, NB, edges, ecount, ecap,
-                       reinterpret_cast<const uint32_t*>(haspred), m_dev, m_bound, perm, max_out, keep, counts,
-                       status, limit, done_in, done_out, grid_done);
+    const uint32_t* hp = reinterpret_cast<const uint32_t*>(haspred);
+    const unsigned lc = edges ? lcap : 0u;
+    if (pre)
+        cudaLaunchKernelEx(&cfg, resolve_single_kernel<true>, mask, ldw, rowbits, NB, edges, ecount, ecap, lc, hp,
+                           m_dev, m_bound, perm, max_out, keep, counts, status, limit, done_in, done_out, grid_done,
+                           *pre);
+    else
+        cudaLaunchKernelEx(&cfg, resolve_single_kernel<false>, mask, ldw, rowbits, NB, edges, ecount, ecap, lc,
+                           hp, m_dev, m_bound, perm, max_out, keep, counts, status, limit, done_in, done_out,
+                           grid_done, GraphPre{});
 }
 
 }  // namespace gbnms

@@ -113,3 +113,28 @@ def test_repeat_calls_are_identical():
     a = _check(props, scores, 10.0)
     b = _check(props, scores, 10.0)
     assert a.tolist() == b.tolist()
+
+
+def test_one_workspace_across_calls():
+    """One workspace for calls of several sizes and densities in turn (lists
+    that one CTA holds, lists that the all-SM passes 0 and 1 shrink into one
+    CTA or leave longer, and lists longer than the workspace holds): every
+    call zeroes the passes' byte planes and pair count again, so a byte left
+    by an earlier call never removes a lane."""
+    n_max = 3000
+    wsb = g.nms_lane_workspace_size(n_max)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for seed, n, thr in [(0, 3000, 40.0), (1, 1000, 15.0), (2, 3000, 15.0), (3, 500, 5.0), (0, 3000, 40.0),
+                         (1, 1000, 15.0)]:
+        assert g.nms_lane_workspace_size(n) <= wsb
+        props, scores = W.lanes(seed, n=n)
+        p = torch.from_numpy(props).cuda()
+        s = torch.from_numpy(scores).cuda()
+        keep = torch.empty(n, dtype=torch.int64, device="cuda")
+        count = torch.empty(1, dtype=torch.int64, device="cuda")
+        st = g.nms_lane_run(p.data_ptr(), s.data_ptr(), n, thr, 0, keep.data_ptr(), n, count.data_ptr(), 0,
+                            ws.data_ptr(), wsb, stream.cuda_stream)
+        assert st == g.NMS_OK
+        got = keep[: int(count.item())].cpu().numpy()
+        assert got.tolist() == oracle.lane_nms(props, scores, thr).tolist(), (seed, n, thr)

@@ -430,7 +430,8 @@ def test_dependency_chains_of_many_links(n_chains, length):
 def test_pairs_concentrated_on_few_targets():
     """Many pairs ending in a narrow range of sorted positions (400 identical
     low-score boxes under 7792 scattered ones, ~80k pairs): more than one
-    share of the graph path holds, so the walk decides instead."""
+    CTA's shared memory holds, so the first passes run over the list in
+    global memory."""
     rng = np.random.default_rng(5)
     g_side = 89
     gx, gy = np.meshgrid(np.arange(g_side), np.arange(g_side))
@@ -442,6 +443,42 @@ def test_pairs_concentrated_on_few_targets():
     s = np.concatenate([rng.uniform(0.5, 1.0, 7792), rng.uniform(0.0, 0.5, 400)]).astype(np.float32)
     p = rng.permutation(len(s))
     _check_single(b[p], s[p], 0.5)
+
+
+def _clusters(n, k, jitter, seed, wh=(20.0, 40.0), span=3000.0):
+    rng = np.random.default_rng(seed)
+    centres = rng.uniform(0, span, (k, 2))
+    c = centres[rng.integers(0, k, n)] + rng.normal(0, jitter, (n, 2))
+    size = rng.uniform(wh[0], wh[1], (n, 2))
+    b = np.concatenate([c - size / 2, c + size / 2], 1).astype(np.float32)
+    return b, rng.uniform(0, 1, n).astype(np.float32)
+
+
+@pytest.mark.parametrize("n,k,jitter,thr", [(8192, 100, 2.0, 0.5), (12000, 300, 6.0, 0.5),
+                                            (16384, 600, 6.0, 0.5), (4000, 20, 10.0, 0.3),
+                                            (4000, 4, 6.0, 0.3), (4000, 2, 6.0, 0.3)])
+def test_lists_beyond_one_cta_up_to_16384_boxes(n, k, jitter, thr):
+    """Clustered boxes whose pair list exceeds one CTA's shared memory (43 K
+    to 49 K pairs) at no more than 16384 boxes: 67 K, 69 K, 151 K, 272 K and
+    1.4 M pairs, where the first passes run over the list in global memory,
+    compacting it in place, and the rest in shared memory once the
+    survivors fit; and about 4 M pairs at 4000 boxes in two clusters, more
+    than the list holds (1.57 M), where the walk decides.  Also with
+    max_out, whose first stage must leave the list intact for the second."""
+    b, s = _clusters(n, k, jitter, seed=n + k)
+    _check_single(b, s, thr)
+    _check_single(b, s, thr, max_out=n // 3)
+    _check_single(b, s, thr, max_out=50)
+
+
+def test_deep_chains_beyond_one_cta():
+    """40 chains of 400 unit boxes sliding by 0.1 at threshold 0.3: five
+    pairs a box (80 K pairs, more than one CTA holds) and well over a
+    hundred passes, so the passes from global memory give up and the walk
+    decides over the mask (which the in-place compaction leaves intact)."""
+    b, s = _parallel_chains(40, 400, step=0.1)
+    _check_single(b, s, 0.3)
+    _check_single(b, s, 0.5)
 
 
 @pytest.mark.parametrize("max_out,score_thr", [(100, None), (40, 0.3), (1, None), (3000, None)])

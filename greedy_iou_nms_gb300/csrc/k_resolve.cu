@@ -13,7 +13,9 @@
 // links even when the walk below would take thousands of steps.  One CTA
 // keeps a byte per box (the last pass that blocked it), a removed byte per
 // box and the live pairs in shared memory; a round is one pass over the pairs
-// whose source is still open and one barrier (graph_resolve).  Up to 16384
+// whose source is still open and one barrier (graph_resolve).  Launched as
+// a cluster, four CTAs share passes 0 and 1 and CTA 0 goes on alone
+// (graph_cluster_prologue).  Up to 16384
 // boxes, the first passes over a longer list run from global memory
 // (global_passes) until the rest fits; passes 0 and 1, which need no barrier
 // inside, can also run on every SM first (graph_pass0_kernel,
@@ -286,6 +288,11 @@ constexpr int GR_GRID_MIN_N = 16384;
 // the first passes over a longer list than one CTA holds run from global
 // memory.
 constexpr unsigned GR_LIST_X = 32;
+// The resolve of the box path is launched as a cluster of GR_CLUSTER CTAs,
+// which share passes 0 and 1 of lists of GR_CLUSTER_MIN_PAIRS pairs or more
+// (graph_cluster_prologue).
+constexpr int GR_CLUSTER = 4;
+constexpr unsigned GR_CLUSTER_MIN_PAIRS = 2048;
 constexpr unsigned GR_GRID_MAX_PAIRS = 1u << 24;
 constexpr int GG_THREADS = 1024;
 
@@ -334,6 +341,60 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
             smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(b))
         : "memory");
+}
+
+// Thread-block cluster: this CTA's rank and the cluster's size, a shared
+// address of the CTA of rank r (mapa), stores and an add into it, and the
+// cluster barrier as its two halves (arrive with release, wait with acquire;
+// every thread of every CTA takes both).
+__device__ __forceinline__ unsigned cluster_rank()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_size()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ unsigned cluster_map(const void* p, unsigned rank)
+{
+    unsigned r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_u8(unsigned addr, unsigned v)
+{
+    asm volatile("st.shared::cluster.u8 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(unsigned addr, unsigned v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;\n" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint4 ld_cluster_v4(unsigned addr)
+{
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned atom_cluster_add(unsigned addr, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;\n" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ void cluster_arrive()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
 // Kept bits of 32-box word w (lane l: box 32w + l) once the rounds are over.
@@ -473,6 +534,85 @@ __device__ __forceinline__ int global_passes(uint32_t* __restrict__ gedges, unsi
     return -1;
 }
 
+// Passes 0 and 1 of graph_resolve shared by the C CTAs of a cluster, each
+// over its own staged pairs Es[0, Eloc) in warp shares as in the rounds.
+// Neither pass needs a barrier inside (pass 0 keeps exactly the sources
+// without a source; in pass 1 every byte is 0 or 2, so it keeps nothing), so
+// a cluster barrier after each is enough.  Pass 0 stores its removals into
+// this CTA's plane; after the barrier each CTA ORs the other CTAs' planes
+// into its own (16-byte loads of their shared memory; a plane read while its
+// owner merges holds at least the owner's removals, and every bit is a
+// removal of pass 0, so the merged planes are all the same).  Pass 1 reads
+// the full plane, blocks its targets in CTA 0 and gathers the pairs left at
+// CTA 0's Es2 (one reservation per CTA on the count at word 36 of CTA 0).  gave_up: this
+// CTA's copy did not arrive (word 37 of CTA 0 is raised).  Every CTA takes
+// the three cluster barriers (the first arrived at by the caller).  Returns
+// whether this is CTA 0, which goes on with the rounds from pass 2.
+__device__ __forceinline__ bool graph_cluster_prologue(uint32_t* Es, unsigned Eloc, bool gave_up, uint8_t* FL,
+                                                       uint8_t* RMb, int NWp, uint32_t* Es2, uint32_t* sm,
+                                                       unsigned C, unsigned crank)
+{
+    const int tid = threadIdx.x;
+    const unsigned l = lane_id();
+    const int warp = tid >> 5;
+    const uint32_t lt = (1u << l) - 1u;
+    int* scratch = reinterpret_cast<int*>(sm);
+    cluster_wait();  // barrier 0: every CTA's planes and CTA 0's counts are set up
+    if (gave_up && tid == 0) st_cluster_u32(cluster_map(sm + 37, 0), 1u);
+    const unsigned chunk = (Eloc + 32u * RV_WARPS - 1) / (32u * RV_WARPS) * 32u;
+    const unsigned wbeg = min(Eloc, static_cast<unsigned>(warp) * chunk);
+    unsigned cnt = min(Eloc, wbeg + chunk) - wbeg;
+    uint32_t* Ew = Es + wbeg;
+    unsigned out = 0;
+    for (unsigned k = 0; k < cnt; k += 32) {
+        const bool have = k + l < cnt;
+        const uint32_t e = have ? Ew[k + l] : 0u;
+        const bool kept = have && FL[e >> 16] == 0;
+        if (kept) RMb[e & 0xffffu] = 1;
+        const bool stay = have && !kept;
+        const uint32_t b = __ballot_sync(FULL, stay);  // every lane has read its pair
+        if (stay) Ew[out + __popc(b & lt)] = e;
+        out += __popc(b);
+    }
+    cnt = out;
+    cluster_arrive();
+    cluster_wait();  // barrier 1: every CTA's removals of pass 0 are in its plane
+    uint4* R4 = reinterpret_cast<uint4*>(RMb);
+    for (int w = tid; w < 2 * NWp; w += RV_THREADS) {
+        uint4 v = R4[w];
+        for (unsigned q = 1; q < C; ++q) {
+            const uint4 o = ld_cluster_v4(cluster_map(R4 + w, (crank + q) % C));
+            v = make_uint4(v.x | o.x, v.y | o.y, v.z | o.z, v.w | o.w);
+        }
+        R4[w] = v;
+    }
+    __syncthreads();
+    const unsigned fl0 = cluster_map(FL, 0);
+    out = 0;
+    for (unsigned k = 0; k < cnt; k += 32) {
+        const bool have = k + l < cnt;
+        const uint32_t e = have ? Ew[k + l] : 0u;
+        const bool stay = have && RMb[e >> 16] == 0;
+        if (stay) st_cluster_u8(fl0 + (e & 0xffffu), 3u);  // blocked in pass 1
+        const uint32_t b = __ballot_sync(FULL, stay);
+        if (stay) Ew[out + __popc(b & lt)] = e;
+        out += __popc(b);
+    }
+    cnt = out;
+    if (l == 0) scratch[warp] = static_cast<int>(cnt);
+    __syncthreads();
+    const int wc = scratch[l];
+    const int total = __reduce_add_sync(FULL, wc);
+    const int before = __reduce_add_sync(FULL, static_cast<int>(l) < warp ? wc : 0);
+    if (tid == 0) sm[38] = total ? atom_cluster_add(cluster_map(sm + 36, 0), static_cast<unsigned>(total)) : 0u;
+    __syncthreads();
+    const unsigned dst = cluster_map(Es2, 0) + 4u * (sm[38] + static_cast<unsigned>(before));
+    for (unsigned k = l; k < cnt; k += 32) st_cluster_u32(dst + 4u * k, Ew[k]);
+    cluster_arrive();
+    cluster_wait();  // barrier 2: CTA 0 holds every pair left and every block of pass 1
+    return crank == 0;
+}
+
 // Rounds over the pair list gedges[0..E) of n sorted boxes (haspred: bit j
 // set iff box j has a pair).  Returns false, with nothing written, when the
 // rounds outnumber the walk's tiles plus 16 (a long chain of dependencies:
@@ -505,9 +645,11 @@ __device__ __forceinline__ int global_passes(uint32_t* __restrict__ gedges, unsi
 // survivors fit.  kPre: passes 0 and 1 were done over all SMs
 // (graph_pass0_kernel, graph_pass1_kernel): gedges holds the pairs left
 // after them, pre->removed the removed bytes and pre->blocked a 3 for each
-// box blocked in pass 1; the rounds start at pass 2.  Separate instances
-// keep the common one's code as it is.
-template <bool kLong, bool kPre>
+// box blocked in pass 1; the rounds start at pass 2.  kCluster: the CTAs of
+// this thread-block cluster share passes 0 and 1 (graph_cluster_prologue
+// below), and CTA 0 goes on alone.  Separate instances keep the common one's
+// code as it is.
+template <bool kLong, bool kPre, bool kCluster = false>
 __device__ __forceinline__ bool graph_resolve(uint32_t* __restrict__ gedges, unsigned E, unsigned cap_words,
                               const uint32_t* __restrict__ haspred, int n, int NWp,
                               const int* __restrict__ perm, int max_out, int64_t* __restrict__ keep,
@@ -517,6 +659,7 @@ __device__ __forceinline__ bool graph_resolve(uint32_t* __restrict__ gedges, uns
 {
     int* scratch = reinterpret_cast<int*>(sm);
     unsigned long long* bar = reinterpret_cast<unsigned long long*>(sm + 32);
+    unsigned long long* pbar = reinterpret_cast<unsigned long long*>(sm + 34);  // kCluster: the permutation
     uint8_t* FL = reinterpret_cast<uint8_t*>(sm + GR_HEAD);
     uint8_t* RMb = FL + 32 * NWp;
     uint32_t* Es = sm + GR_HEAD + 16 * NWp;
@@ -529,29 +672,47 @@ __device__ __forceinline__ bool graph_resolve(uint32_t* __restrict__ gedges, uns
     // to a multiple of 4 pairs) while the bitmaps are set up; the sort
     // permutation follows it when both fit (the output then maps positions
     // from shared memory).
-    const unsigned bytes = kLong ? 0u : 16u * ((E + 3) / 4);
+    //
+    // kCluster: CTA crank of C stages pairs [my0, my0 + Eloc) of the list
+    // (shares of S pairs, a multiple of 4); CTA 0 also stages the permutation
+    // after its share, when its share, the permutation and all E pairs fit
+    // (the pairs left after pass 1 gather after them, at Es2), on a barrier
+    // of its own that only the output waits for.
+    const unsigned C = kCluster ? cluster_size() : 1u;
+    const unsigned crank = kCluster ? cluster_rank() : 0u;
+    const unsigned S = kCluster ? (((E + C - 1) / C + 3) & ~3u) : E;
+    const unsigned my0 = kCluster ? min(E, crank * S) : 0u;
+    const unsigned Eloc = kCluster ? min(E, my0 + S) - my0 : E;
+    const unsigned bytes = kLong ? 0u : 16u * ((Eloc + 3) / 4);
     const unsigned ncopy = (bytes + GR_COPY - 1) / GR_COPY;
     const unsigned pbytes = 16u * ((static_cast<unsigned>(n) + 3) / 4);
-    const bool perm_here = !kLong && perm && (bytes + pbytes) / 4 <= cap_words;
-    const int* perm_s = perm_here ? reinterpret_cast<const int*>(reinterpret_cast<const char*>(Es) + bytes) : nullptr;
+    const bool perm0 = kCluster && perm && S + pbytes / 4 + E <= cap_words;
+    uint32_t* Es2 = Es + S + (perm0 ? pbytes / 4 : 0u);
+    const bool perm_here =
+        kCluster ? perm0 && crank == 0 : !kLong && perm && (bytes + pbytes) / 4 <= cap_words;
+    const unsigned pofs = kCluster ? 4u * S : bytes;  // byte offset of the permutation
+    const int* perm_s = perm_here ? reinterpret_cast<const int*>(reinterpret_cast<const char*>(Es) + pofs) : nullptr;
     const unsigned pcopy = perm_here ? (pbytes + GR_COPY - 1) / GR_COPY : 0u;
     if (tid == 0) {
         mbar_init(bar, 1);
+        if (kCluster) mbar_init(pbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     __syncthreads();
-    const unsigned tx = bytes + (perm_here ? pbytes : 0u);  // bytes the barrier waits for
+    const unsigned tx = bytes + (perm_here && !kCluster ? pbytes : 0u);  // bytes the barrier waits for
     if (tid == 0 && tx) mbar_expect_tx(bar, tx);
+    if (kCluster && tid == 0 && perm_here) mbar_expect_tx(pbar, pbytes);
     __syncwarp();
     if (warp == 0 && l < ncopy) {
         const unsigned off = l * GR_COPY;
         const unsigned len = min(static_cast<unsigned>(GR_COPY), bytes - off);
-        bulk_g2s(reinterpret_cast<char*>(Es) + off, reinterpret_cast<const char*>(gedges) + off, len, bar);
+        bulk_g2s(reinterpret_cast<char*>(Es) + off, reinterpret_cast<const char*>(gedges + my0) + off, len, bar);
     }
     if (warp == 1 && l < pcopy) {
         const unsigned off = l * GR_COPY;
         const unsigned len = min(static_cast<unsigned>(GR_COPY), pbytes - off);
-        bulk_g2s(reinterpret_cast<char*>(Es) + bytes + off, reinterpret_cast<const char*>(perm) + off, len, bar);
+        bulk_g2s(reinterpret_cast<char*>(Es) + pofs + off, reinterpret_cast<const char*>(perm) + off, len,
+                 kCluster ? pbar : bar);
     }
     for (int w = tid; w < NW; w += RV_THREADS) {
         const uint32_t hp = haspred[w];  // a box with a source starts blocked in pass 0
@@ -575,6 +736,13 @@ __device__ __forceinline__ bool graph_resolve(uint32_t* __restrict__ gedges, uns
             rq[1] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
+    if (kCluster) {
+        if (tid == 0) {
+            sm[36] = 0u;  // CTA 0: pairs gathered at Es2
+            sm[37] = 0u;  // CTA 0: some CTA's copy gave up
+        }
+        cluster_arrive();  // this CTA's planes are set up (barrier 0, waited for below)
+    }
     bool copied = true;
     if (tx) {
         long long tries = 0;
@@ -585,15 +753,48 @@ __device__ __forceinline__ bool graph_resolve(uint32_t* __restrict__ gedges, uns
     }
     const bool all_copied = __syncthreads_and(copied);
     if (tid == 0) asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(smem_addr(bar)) : "memory");
-    if (!all_copied) {
+    if (!kCluster && !all_copied) {
         if (tid == 0) {
             if (status) set_status(status, NMS_ERR_TIMEOUT);
             counts[0] = 0;
         }
         return true;
     }
+    // kCluster, CTA 0: waits for the permutation's copy; on giving up raises
+    // the status, writes a zero count and returns false.
+    auto perm_ready = [&]() -> bool {
+        bool got = true;
+        long long tries = 0;
+        while (!mbar_try_wait(pbar, 0)) {
+            if (++tries > RV_WAIT_LIMIT) { got = false; break; }
+            __nanosleep(64);
+        }
+        const bool all_got = __syncthreads_and(got);
+        if (tid == 0) asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(smem_addr(pbar)) : "memory");
+        if (!all_got && tid == 0) {
+            if (status) set_status(status, NMS_ERR_TIMEOUT);
+            counts[0] = 0;
+        }
+        return all_got;
+    };
     const int max_rounds = (n + 63) / 64 + 16;
     int round0 = kPre ? 2 : 0;  // the first pass over the list in shared memory
+    uint32_t* Eb = Es;          // the list the rounds run over
+    if (kCluster) {
+        if (!graph_cluster_prologue(Es, all_copied ? Eloc : 0u, !all_copied, FL, RMb, NWp, Es2, sm, C, crank))
+            return true;  // CTAs 1 .. C-1 are done
+        if (sm[37]) {     // a copy gave up: nothing is decided
+            if (perm_here) perm_ready();  // no copy into this CTA stays in flight
+            if (tid == 0) {
+                if (status) set_status(status, NMS_ERR_TIMEOUT);
+                counts[0] = 0;
+            }
+            return true;
+        }
+        E = sm[36];
+        Eb = Es2;
+        round0 = 2;
+    }
     if (kLong) {
         unsigned left = 0;
         round0 = global_passes(gedges, E, cap_words, FL, RMb, Es, scratch, round0, max_rounds, &left);
@@ -612,7 +813,7 @@ __device__ __forceinline__ bool graph_resolve(uint32_t* __restrict__ gedges, uns
     const unsigned chunk = (E + 32u * RV_WARPS - 1) / (32u * RV_WARPS) * 32u;
     const unsigned wbeg = min(E, static_cast<unsigned>(warp) * chunk);
     unsigned cnt = min(E, wbeg + chunk) - wbeg;
-    uint32_t* Ew = Es + wbeg;
+    uint32_t* Ew = Eb + wbeg;
     const uint32_t lt = (1u << l) - 1u;
     // Pass 0: a source without a source of its own (byte 0) is kept and
     // removes its target; every other pair stays.
@@ -633,7 +834,12 @@ __device__ __forceinline__ bool graph_resolve(uint32_t* __restrict__ gedges, uns
         any = __syncthreads_or(cnt > 0u);
     }
     for (int round = round0 > 0 ? round0 : 1; any; ++round) {
-        if (round == max_rounds) return false;
+        if (round == max_rounds) {
+            // kCluster: the walk reuses the shared memory the permutation's
+            // copy may still be writing.
+            if (kCluster && perm_here && !perm_ready()) return true;
+            return false;
+        }
         const uint32_t kept_f = static_cast<uint32_t>(round) & 0xffu;
         const uint8_t blk_f = static_cast<uint8_t>(round + 2);
         unsigned out = 0;
@@ -654,6 +860,7 @@ __device__ __forceinline__ bool graph_resolve(uint32_t* __restrict__ gedges, uns
         cnt = out;
         any = __syncthreads_or(cnt > 0u);
     }
+    if (kCluster && perm_here && !perm_ready()) return true;
     // Output: warp w owns 32-box words [w*wpw, (w+1)*wpw); a block-wide
     // prefix of the warps' kept counts places them, and within a word lane l
     // writes box 32w+l, so loads of perm and stores of keep are coalesced.
@@ -710,7 +917,10 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
     if (grid_done && *grid_done) return;  // graph_grid_kernel resolved this stage
     const int n_all = m_dev ? *m_dev : m_bound;
     const int n = min(n_all, limit);
-    if (done_out && threadIdx.x == 0) *done_out = n >= n_all;  // raised below on max_out
+    // Launched as a cluster, CTAs 1 .. C-1 only help with passes 0 and 1 of
+    // the graph path; everything else is CTA 0's.
+    const unsigned crank = cluster_rank();
+    if (done_out && threadIdx.x == 0 && crank == 0) *done_out = n >= n_all;  // raised below on max_out
     if (edges) {
         // A list beyond shared memory is compacted in place by the first
         // passes: only the last stage may do that, and only when no all-SM
@@ -718,7 +928,17 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
         const unsigned E = *ecount;
         uint32_t* sm = reinterpret_cast<uint32_t*>(smem);
         const int NWp = graph_words(m_bound);
-        if (E <= ecap) {
+        const unsigned C = cluster_size();
+        const bool shared = !kPre && C > 1 && E >= GR_CLUSTER_MIN_PAIRS && E <= ecap &&
+                            (((E + C - 1) / C + 3) & ~3u) + E <= ecap;
+        if (shared) {
+            // Only CTA 0 comes back, when the rounds outnumber the limit.
+            if (graph_resolve<false, false, true>(edges, E, ecap, haspred, n, NWp, perm, max_out, keep, counts,
+                                                  status, sm, done_out))
+                return;
+        } else if (crank != 0) {
+            return;
+        } else if (E <= ecap) {
             if (graph_resolve<false, false>(edges, E, ecap, haspred, n, NWp, perm, max_out, keep, counts, status,
                                             sm, done_out))
                 return;
@@ -741,6 +961,7 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
         }
         __syncthreads();  // the walk reuses the shared memory
     }
+    if (crank != 0) return;
     const int T = (n + 63) / 64;              // tiles
     const int T256 = (n + 255) / 256;         // 256-column chunks
     const ResolveLayout LY = resolve_layout(m_bound, NB);
@@ -1347,13 +1568,21 @@ void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* ro
                             : reinterpret_cast<const void*>(resolve_single_kernel<false>),
                         smem);
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(1);
+    // The box path with a pair list: a cluster of GR_CLUSTER CTAs (passes 0
+    // and 1 shared; CTA 0 does the rest).
+    const unsigned csize = edges && !pre ? GR_CLUSTER : 1u;
+    cfg.gridDim = dim3(csize);
     cfg.blockDim = dim3(RV_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg.attrs = attr;
-    cfg.numAttrs = pdl_attr_count();
+    cfg.numAttrs = 1u + static_cast<unsigned>(pdl_attr_count());
     const uint32_t* hp = reinterpret_cast<const uint32_t*>(haspred);
     const unsigned lc = edges ? lcap : 0u;
     if (pre)

@@ -434,9 +434,8 @@ __device__ __forceinline__ void write_kept(const uint8_t* RMb, int w0, int w1, i
 }
 
 // Passes start, start + 1, ... of graph_resolve over a list too long for
-// shared memory,
-// straight from global memory (the per-box bytes FL and RMb stay in shared
-// memory).  Thread t owns the 16-byte quads t, t + RV_THREADS, ... of gedges
+// shared memory, straight from global memory (the per-box bytes FL and RMb
+// stay in shared memory).  Thread t owns the 16-byte quads t, t + RV_THREADS, ... of gedges
 // and packs its survivors in place into the pair slots of those quads (slot
 // s: quad t + RV_THREADS * (s / 4), element s % 4).  Four quads, sixteen
 // pairs, are taken a step, and the next step's quads are loaded before this
@@ -651,7 +650,7 @@ __device__ __forceinline__ bool graph_cluster_prologue(uint32_t* Es, unsigned El
 // code as it is.
 template <bool kLong, bool kPre, bool kCluster = false>
 __device__ __forceinline__ bool graph_resolve(uint32_t* __restrict__ gedges, unsigned E, unsigned cap_words,
-                              const uint32_t* __restrict__ haspred, int n, int NWp,
+                              const uint32_t* __restrict__ haspred, int n, int NWp, uint32_t hp_tid,
                               const int* __restrict__ perm, int max_out, int64_t* __restrict__ keep,
                               int64_t* __restrict__ counts, int32_t* status, uint32_t* sm,
                               int* done_out, const uint8_t* __restrict__ pre_rm = nullptr,
@@ -715,7 +714,9 @@ __device__ __forceinline__ bool graph_resolve(uint32_t* __restrict__ gedges, uns
                  kCluster ? pbar : bar);
     }
     for (int w = tid; w < NW; w += RV_THREADS) {
-        const uint32_t hp = haspred[w];  // a box with a source starts blocked in pass 0
+        // A box with a source starts blocked in pass 0 (word tid was loaded
+        // with the pair count).
+        const uint32_t hp = w == tid ? hp_tid : haspred[w];
         uint32_t bx[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) bx[q] = (((hp >> (4 * q)) & 0xfu) * 0x00204081u & 0x01010101u) << 1;  // bits -> 0/2
@@ -926,6 +927,9 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
         // passes: only the last stage may do that, and only when no all-SM
         // pass ran over it before.
         const unsigned E = *ecount;
+        // The neighbour bitmap's word of this thread, loaded with the count.
+        const uint32_t hp_tid =
+            haspred && static_cast<int>(threadIdx.x) < (m_bound + 31) / 32 ? haspred[threadIdx.x] : 0u;
         uint32_t* sm = reinterpret_cast<uint32_t*>(smem);
         const int NWp = graph_words(m_bound);
         const unsigned C = cluster_size();
@@ -933,30 +937,30 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
                             (((E + C - 1) / C + 3) & ~3u) + E <= ecap;
         if (shared) {
             // Only CTA 0 comes back, when the rounds outnumber the limit.
-            if (graph_resolve<false, false, true>(edges, E, ecap, haspred, n, NWp, perm, max_out, keep, counts,
-                                                  status, sm, done_out))
+            if (graph_resolve<false, false, true>(edges, E, ecap, haspred, n, NWp, hp_tid, perm, max_out, keep,
+                                                  counts, status, sm, done_out))
                 return;
         } else if (crank != 0) {
             return;
         } else if (E <= ecap) {
-            if (graph_resolve<false, false>(edges, E, ecap, haspred, n, NWp, perm, max_out, keep, counts, status,
-                                            sm, done_out))
+            if (graph_resolve<false, false>(edges, E, ecap, haspred, n, NWp, hp_tid, perm, max_out, keep, counts,
+                                            status, sm, done_out))
                 return;
         } else if (kPre && E <= lcap) {
             // The pairs left after passes 0 and 1 (the list was complete).
             const unsigned E2 = *pre.ecount;
             if (E2 <= ecap) {
-                if (graph_resolve<false, true>(pre.edges, E2, ecap, haspred, n, NWp, perm, max_out, keep, counts,
-                                               status, sm, done_out, pre.removed, pre.blocked))
+                if (graph_resolve<false, true>(pre.edges, E2, ecap, haspred, n, NWp, hp_tid, perm, max_out, keep,
+                                               counts, status, sm, done_out, pre.removed, pre.blocked))
                     return;
             } else if (E2 <= pre.cap) {
-                if (graph_resolve<true, true>(pre.edges, E2, ecap, haspred, n, NWp, perm, max_out, keep, counts,
-                                              status, sm, done_out, pre.removed, pre.blocked))
+                if (graph_resolve<true, true>(pre.edges, E2, ecap, haspred, n, NWp, hp_tid, perm, max_out, keep,
+                                              counts, status, sm, done_out, pre.removed, pre.blocked))
                     return;
             }
         } else if (!kPre && E <= lcap && !grid_done && n >= n_all) {
-            if (graph_resolve<true, false>(edges, E, ecap, haspred, n, NWp, perm, max_out, keep, counts, status,
-                                           sm, done_out))
+            if (graph_resolve<true, false>(edges, E, ecap, haspred, n, NWp, hp_tid, perm, max_out, keep, counts,
+                                           status, sm, done_out))
                 return;
         }
         __syncthreads();  // the walk reuses the shared memory

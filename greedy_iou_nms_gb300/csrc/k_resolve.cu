@@ -913,10 +913,19 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
     extern __shared__ __align__(128) uint64_t smem[];
     __shared__ ResolveShared S;
 
-    pdl_wait();                           // the mask (or an earlier kernel) has finished
-    if (done_in && *done_in) return;      // an earlier stage already finished
-    if (grid_done && *grid_done) return;  // graph_grid_kernel resolved this stage
+    pdl_wait();  // the mask (or an earlier kernel) has finished
+    // Everything read from the earlier kernels, loaded together before any
+    // store: the stage flags, the box and pair counts, and the neighbour
+    // bitmap's word of this thread.
+    const int was_done = done_in ? *done_in : 0;
+    const int grid_did = grid_done ? *grid_done : 0;
     const int n_all = m_dev ? *m_dev : m_bound;
+    const unsigned E = edges ? *ecount : 0u;
+    const unsigned E2 = kPre && edges ? *pre.ecount : 0u;
+    const uint32_t hp_tid =
+        edges && haspred && static_cast<int>(threadIdx.x) < (m_bound + 31) / 32 ? haspred[threadIdx.x] : 0u;
+    if (was_done) return;  // an earlier stage already finished
+    if (grid_did) return;  // graph_grid_kernel resolved this stage
     const int n = min(n_all, limit);
     // Launched as a cluster, CTAs 1 .. C-1 only help with passes 0 and 1 of
     // the graph path; everything else is CTA 0's.
@@ -926,10 +935,6 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
         // A list beyond shared memory is compacted in place by the first
         // passes: only the last stage may do that, and only when no all-SM
         // pass ran over it before.
-        const unsigned E = *ecount;
-        // The neighbour bitmap's word of this thread, loaded with the count.
-        const uint32_t hp_tid =
-            haspred && static_cast<int>(threadIdx.x) < (m_bound + 31) / 32 ? haspred[threadIdx.x] : 0u;
         uint32_t* sm = reinterpret_cast<uint32_t*>(smem);
         const int NWp = graph_words(m_bound);
         const unsigned C = cluster_size();
@@ -948,7 +953,6 @@ resolve_single_kernel(const uint64_t* __restrict__ mask, int64_t ldw,
                 return;
         } else if (kPre && E <= lcap) {
             // The pairs left after passes 0 and 1 (the list was complete).
-            const unsigned E2 = *pre.ecount;
             if (E2 <= ecap) {
                 if (graph_resolve<false, true>(pre.edges, E2, ecap, haspred, n, NWp, hp_tid, perm, max_out, keep,
                                                counts, status, sm, done_out, pre.removed, pre.blocked))

@@ -16,11 +16,13 @@
 //           cover, its row span, and a flag for a lane with a non-finite x
 //           in a covered row; 32 lanes a CTA, transposed through shared
 //           memory;
-//   mask:   one CTA of 256 threads per 64 x 64 tile of the upper triangle;
-//           thread (q, r) holds row lane r's 72 x in registers and takes 16
-//           of the tile's 64 column lanes (staged in shared memory, negated,
-//           row by row) -- per row one add, one max and one add:
-//             acc += max(|x_r + (-x_c)|, 0)
+//   mask:   one CTA of 256 threads per run of 64 x 64 tiles along a row of
+//           tiles of the upper triangle; thread (q, r) holds row lane r's 72
+//           x in registers and takes 16 of each tile's 64 column lanes
+//           (staged in shared memory row by row, the next tile by cp.async
+//           while this one is compared) -- per row one subtraction, one max
+//           and one add:
+//             acc += max(|x_r - x_c|, 0)
 //           max(NaN, 0) is 0, so a row either lane does not cover adds +0,
 //           which leaves a non-negative sum unchanged: the sum is the
 //           definition's sum over the common rows in row order.  Pairs with
@@ -32,6 +34,7 @@
 //           rounds run on all SMs first (launch_graph_prepass), then
 //           launch_resolve_single (rounds over the pairs they leave, or the
 //           walk).
+#include <algorithm>
 #include <cstdint>
 
 #include "common.cuh"
@@ -144,27 +147,49 @@ lane_gather_kernel(const float* __restrict__ props, const int* __restrict__ perm
     }
 }
 
-// Linear tile index -> (row tile a, column tile c), a <= c, column by column.
-__device__ __forceinline__ void lane_tile(int u, int& a, int& c)
+// Row tile a and column tiles [c0, c1) of CTA b: each row of tiles of the
+// upper triangle (column tiles a .. T-1) is cut into runs of K tiles, rows in
+// order.
+__device__ __forceinline__ void lane_run(int b, int T, int K, int& a, int& c0, int& c1)
 {
-    int cc = static_cast<int>((sqrtf(8.0f * static_cast<float>(u) + 1.0f) - 1.0f) * 0.5f);
-    if (cc < 0) cc = 0;
-    while ((cc + 1) * (cc + 2) / 2 <= u) ++cc;
-    while (cc > 0 && cc * (cc + 1) / 2 > u) --cc;
-    c = cc;
-    a = u - cc * (cc + 1) / 2;
+    int left = b;
+    for (a = 0; a < T - 1; ++a) {
+        const int m = (T - a + K - 1) / K;
+        if (left < m) break;
+        left -= m;
+    }
+    c0 = a + left * K;
+    c1 = min(T, c0 + K);
 }
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(
+                     static_cast<unsigned>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// One CTA per run of K column tiles of one row tile: the row lanes' x stay
+// in registers for the run, and the next column tile (its 72 x 64 x, spans
+// and flags) is copied into the other half of a double buffer by 16-byte
+// cp.async while the current one is compared.
 __global__ void __launch_bounds__(LN_THREADS, 2)
 lane_mask_kernel(const float* __restrict__ xs, const uint32_t* __restrict__ span,
                  const uint32_t* __restrict__ flag, const float* __restrict__ props, const int* __restrict__ perm,
-                 int n, int ld, float thr, uint64_t* __restrict__ mask, int64_t ldw,
+                 int n, int ld, int K, float thr, uint64_t* __restrict__ mask, int64_t ldw,
                  unsigned long long* __restrict__ rowbits, int NB, uint32_t* __restrict__ edges,
                  unsigned* __restrict__ ecount, unsigned ecap, unsigned long long* __restrict__ haspred)
 {
-    __shared__ __align__(16) float s_nx[LN_ROWS][LN_TILE];  // -x of the column lanes, row by row
-    __shared__ uint32_t s_span[LN_TILE];
-    __shared__ uint32_t s_flag[LN_TILE];
+    __shared__ __align__(16) float s_x[2][LN_ROWS][LN_TILE];  // x of the column lanes, row by row
+    __shared__ __align__(16) uint32_t s_span[2][LN_TILE];
+    __shared__ __align__(16) uint32_t s_flag[2][LN_TILE];
     __shared__ uint16_t s_piece[LN_TILE][LN_THREADS / LN_TILE];
     __shared__ unsigned long long s_or[2];
     __shared__ int s_cnt[2];
@@ -173,119 +198,136 @@ lane_mask_kernel(const float* __restrict__ xs, const uint32_t* __restrict__ span
 
     pdl_wait();  // the gather has finished
     pdl_release();
-    int ta, tc;
-    lane_tile(blockIdx.x, ta, tc);
-    const int rbase = ta * LN_TILE, cbase = tc * LN_TILE;
+    const int T = ld / LN_TILE;
+    int ta, cA, cB;
+    lane_run(blockIdx.x, T, K, ta, cA, cB);
     const int t = threadIdx.x;
     const int r = t & (LN_TILE - 1), q = t / LN_TILE;
-    // Stage the column lanes (negated; NaN stays NaN).
-    for (int e = t; e < LN_ROWS * LN_TILE; e += LN_THREADS) {
-        const int k = e / LN_TILE, c = e % LN_TILE;
-        s_nx[k][c] = -xs[static_cast<int64_t>(k) * ld + cbase + c];
-    }
-    if (t < LN_TILE) {
-        s_span[t] = span[cbase + t];
-        s_flag[t] = flag[cbase + t];
-    }
+    const int rbase = ta * LN_TILE;
+    // Column tile c into half h of the buffer (one commit group).
+    auto stage = [&](int h, int c) {
+        const int cb = c * LN_TILE;
+        for (int e = t; e < LN_ROWS * (LN_TILE / 4); e += LN_THREADS) {
+            const int k = e / (LN_TILE / 4), v = 4 * (e % (LN_TILE / 4));
+            cp_async16(&s_x[h][k][v], xs + static_cast<int64_t>(k) * ld + cb + v);
+        }
+        if (t < LN_TILE / 4)
+            cp_async16(&s_span[h][4 * t], span + cb + 4 * t);
+        else if (t < LN_TILE / 2)
+            cp_async16(&s_flag[h][4 * t - LN_TILE], flag + cb + 4 * t - LN_TILE);
+        cp_async_commit();
+    };
+    if (cA < cB) stage(0, cA);
     const int i = rbase + r;
     float xr[LN_ROWS];
 #pragma unroll
     for (int k = 0; k < LN_ROWS; ++k) xr[k] = xs[static_cast<int64_t>(k) * ld + i];
     const uint32_t sr = span[i];
     const uint32_t fr = flag[i];
-    __syncthreads();
-
-    uint32_t bits = 0u;
-    const int c0 = q * LN_QCOLS;
 #pragma unroll 1
-    for (int g = 0; g < LN_QCOLS; g += 4) {
-        float acc0 = 0.0f, acc1 = 0.0f, acc2 = 0.0f, acc3 = 0.0f;
-#pragma unroll
-        for (int k = 0; k < LN_ROWS; ++k) {
-            const float4 nc = *reinterpret_cast<const float4*>(&s_nx[k][c0 + g]);
-            acc0 = __fadd_rn(acc0, fmaxf(fabsf(__fadd_rn(xr[k], nc.x)), 0.0f));
-            acc1 = __fadd_rn(acc1, fmaxf(fabsf(__fadd_rn(xr[k], nc.y)), 0.0f));
-            acc2 = __fadd_rn(acc2, fmaxf(fabsf(__fadd_rn(xr[k], nc.z)), 0.0f));
-            acc3 = __fadd_rn(acc3, fmaxf(fabsf(__fadd_rn(xr[k], nc.w)), 0.0f));
+    for (int tc = cA; tc < cB; ++tc) {
+        const int h = (tc - cA) & 1;
+        if (tc + 1 < cB) {
+            stage(h ^ 1, tc + 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
         }
-        const float acc[4] = {acc0, acc1, acc2, acc3};
+        __syncthreads();
+        const int cbase = tc * LN_TILE;
+        uint32_t bits = 0u;
+        const int c0 = q * LN_QCOLS;
+#pragma unroll 1
+        for (int g = 0; g < LN_QCOLS; g += 4) {
+            float acc0 = 0.0f, acc1 = 0.0f, acc2 = 0.0f, acc3 = 0.0f;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int cl = c0 + g + u, j = cbase + cl;
-            if (j <= i || j >= n || i >= n) continue;  // the upper triangle only
-            const uint32_t sc = s_span[cl];
-            const int lo = max(static_cast<int>(sr & 255u), static_cast<int>(sc & 255u));
-            const int hi = min(static_cast<int>(sr >> 8), static_cast<int>(sc >> 8));
-            if (hi <= lo) continue;  // no common row: +inf, never below the threshold
-            float d;
-            if (fr | s_flag[cl])
-                d = lane_distance_exact(props + static_cast<int64_t>(perm[i]) * LN_VALUES,
-                                        props + static_cast<int64_t>(perm[j]) * LN_VALUES, sr, sc);
-            else
-                d = __fdiv_rn(acc[u], static_cast<float>(hi - lo));
-            if (d < thr) bits |= 1u << (g + u);
-        }
-    }
-    s_piece[r][q] = static_cast<uint16_t>(bits);
-    __syncthreads();
-    // Threads 0..63 own the tile's rows: word, chunk bit, pair count.
-    uint64_t w = 0;
-    int cnt = 0;
-    if (t < LN_TILE) {
+            for (int k = 0; k < LN_ROWS; ++k) {
+                const float4 xc = *reinterpret_cast<const float4*>(&s_x[h][k][c0 + g]);
+                acc0 = __fadd_rn(acc0, fmaxf(fabsf(__fsub_rn(xr[k], xc.x)), 0.0f));
+                acc1 = __fadd_rn(acc1, fmaxf(fabsf(__fsub_rn(xr[k], xc.y)), 0.0f));
+                acc2 = __fadd_rn(acc2, fmaxf(fabsf(__fsub_rn(xr[k], xc.z)), 0.0f));
+                acc3 = __fadd_rn(acc3, fmaxf(fabsf(__fsub_rn(xr[k], xc.w)), 0.0f));
+            }
+            const float acc[4] = {acc0, acc1, acc2, acc3};
 #pragma unroll
-        for (int k = 0; k < LN_THREADS / LN_TILE; ++k)
-            w |= static_cast<uint64_t>(s_piece[t][k]) << (LN_QCOLS * k);
-        const int row = rbase + t;
-        if (row < n) {
-            mask[static_cast<int64_t>(row) * ldw + tc] = w;
-            if (w && rowbits) {
-                const int chunk = cbase >> 8;
-                atomicOr(rowbits + static_cast<int64_t>(row) * NB + (chunk >> 6), 1ull << (chunk & 63));
+            for (int u = 0; u < 4; ++u) {
+                const int cl = c0 + g + u, j = cbase + cl;
+                if (j <= i || j >= n || i >= n) continue;  // the upper triangle only
+                const uint32_t sc = s_span[h][cl];
+                const int lo = max(static_cast<int>(sr & 255u), static_cast<int>(sc & 255u));
+                const int hi = min(static_cast<int>(sr >> 8), static_cast<int>(sc >> 8));
+                if (hi <= lo) continue;  // no common row: +inf, never below the threshold
+                float d;
+                if (fr | s_flag[h][cl])
+                    d = lane_distance_exact(props + static_cast<int64_t>(perm[i]) * LN_VALUES,
+                                            props + static_cast<int64_t>(perm[j]) * LN_VALUES, sr, sc);
+                else
+                    d = __fdiv_rn(acc[u], static_cast<float>(hi - lo));
+                if (d < thr) bits |= 1u << (g + u);
             }
         }
-        cnt = __popcll(w);
-        // Inclusive prefix of the counts within the warp.
-        const unsigned l = lane_id();
-        int x = cnt;
+        s_piece[r][q] = static_cast<uint16_t>(bits);
+        __syncthreads();
+        // Threads 0..63 own the tile's rows: word, chunk bit, pair count.
+        uint64_t w = 0;
+        int cnt = 0;
+        if (t < LN_TILE) {
 #pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(FULL, x, d);
-            if (static_cast<int>(l) >= d) x += y;
+            for (int k = 0; k < LN_THREADS / LN_TILE; ++k)
+                w |= static_cast<uint64_t>(s_piece[t][k]) << (LN_QCOLS * k);
+            const int row = rbase + t;
+            if (row < n) {
+                mask[static_cast<int64_t>(row) * ldw + tc] = w;
+                if (w && rowbits) {
+                    const int chunk = cbase >> 8;
+                    atomicOr(rowbits + static_cast<int64_t>(row) * NB + (chunk >> 6), 1ull << (chunk & 63));
+                }
+            }
+            cnt = __popcll(w);
+            // Inclusive prefix of the counts within the warp.
+            const unsigned l = lane_id();
+            int x = cnt;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(FULL, x, d);
+                if (static_cast<int>(l) >= d) x += y;
+            }
+            const unsigned long long o = __reduce_or_sync(FULL, static_cast<unsigned>(w)) |
+                                         (static_cast<unsigned long long>(__reduce_or_sync(FULL,
+                                              static_cast<unsigned>(w >> 32))) << 32);
+            if (l == 31) {
+                s_cnt[t >> 5] = x;
+                s_or[t >> 5] = o;
+            }
+            cnt = x - cnt;  // exclusive prefix within the warp
         }
-        const unsigned long long o = __reduce_or_sync(FULL, static_cast<unsigned>(w)) |
-                                     (static_cast<unsigned long long>(__reduce_or_sync(FULL,
-                                          static_cast<unsigned>(w >> 32))) << 32);
-        if (l == 31) {
-            s_cnt[t >> 5] = x;
-            s_or[t >> 5] = o;
+        __syncthreads();
+        if (t == 0) {
+            const unsigned long long o = s_or[0] | s_or[1];
+            if (o && haspred) atomicOr(haspred + tc, o);
+            const int total = s_cnt[0] + s_cnt[1];
+            s_base = total && edges ? atomicAdd(ecount, static_cast<unsigned>(total)) : 0u;
+            s_total = total;
         }
-        cnt = x - cnt;  // exclusive prefix within the warp
-    }
-    __syncthreads();
-    if (t == 0) {
-        const unsigned long long o = s_or[0] | s_or[1];
-        if (o && haspred) atomicOr(haspred + tc, o);
-        const int total = s_cnt[0] + s_cnt[1];
-        s_base = total && edges ? atomicAdd(ecount, static_cast<unsigned>(total)) : 0u;
-        s_total = total;
-    }
-    __syncthreads();
-    // The pair list: the tile's pairs land contiguously, row by row.  Past
-    // the capacity the count still grows (the resolve then takes the walk)
-    // and nothing is written.
-    if (t < LN_TILE && edges && w) {
-        const unsigned total = static_cast<unsigned>(s_total);
-        const unsigned base = s_base;
-        if (base <= ecap && total <= ecap - base) {
-            uint32_t* dst = edges + base + cnt + (t >= 32 ? s_cnt[0] : 0);
-            const uint32_t row = static_cast<uint32_t>(rbase + t);
-            uint64_t x = w;
-            while (x) {
-                const int b = __ffsll(static_cast<long long>(x)) - 1;
-                x &= x - 1;
-                *dst++ = (row << 16) | static_cast<uint32_t>(cbase + b);
+        __syncthreads();
+        // The pair list: the tile's pairs land contiguously, row by row.  Past
+        // the capacity the count still grows (the resolve then takes the walk)
+        // and nothing is written.
+        if (t < LN_TILE && edges && w) {
+            const unsigned total = static_cast<unsigned>(s_total);
+            const unsigned base = s_base;
+            if (base <= ecap && total <= ecap - base) {
+                uint32_t* dst = edges + base + cnt + (t >= 32 ? s_cnt[0] : 0);
+                const uint32_t row = static_cast<uint32_t>(rbase + t);
+                uint64_t x = w;
+                while (x) {
+                    const int b = __ffsll(static_cast<long long>(x)) - 1;
+                    x &= x - 1;
+                    *dst++ = (row << 16) | static_cast<uint32_t>(cbase + b);
+                }
             }
         }
+        __syncthreads();  // the buffer half and the tile's scratch are written again
     }
 }
 
@@ -304,9 +346,18 @@ void launch_lane_mask(const float* props, const int* perm, int n, float thr, flo
     const int ld = lane_ld(n);
     launch_pdl(lane_gather_kernel, dim3(ld / LG_LANES), dim3(LG_THREADS), 0, st, props, perm, n, ld, xs, span, flag,
                static_cast<uint4*>(zero), zero ? static_cast<int>(zero_bytes / 16) : 0, zcount);
+    // Runs of K column tiles: about one wave of 2 CTAs per SM, K at most 8.
     const int T = ld / LN_TILE;
-    launch_pdl(lane_mask_kernel, dim3(T * (T + 1) / 2), dim3(LN_THREADS), 0, st, xs,
-               static_cast<const uint32_t*>(span), static_cast<const uint32_t*>(flag), props, perm, n, ld, thr, mask,
+    const long long tiles = static_cast<long long>(T) * (T + 1) / 2;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long slots = 2ll * (sms > 0 ? sms : 1);
+    const int K = static_cast<int>(std::min<long long>(8, std::max<long long>(1, (tiles + slots - 1) / slots)));
+    int runs = 0;
+    for (int a = 0; a < T; ++a) runs += (T - a + K - 1) / K;
+    launch_pdl(lane_mask_kernel, dim3(runs), dim3(LN_THREADS), 0, st, xs,
+               static_cast<const uint32_t*>(span), static_cast<const uint32_t*>(flag), props, perm, n, ld, K, thr, mask,
                ldw, reinterpret_cast<unsigned long long*>(rowbits), NB, edges, ecount, ecap,
                reinterpret_cast<unsigned long long*>(haspred));
 }

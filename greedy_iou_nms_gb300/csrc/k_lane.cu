@@ -20,9 +20,11 @@
 //           tiles of the upper triangle; thread (q, r) holds row lane r's 72
 //           x in registers and takes 16 of each tile's 64 column lanes
 //           (staged in shared memory row by row, the next tile by cp.async
-//           while this one is compared) -- per row one subtraction, one max
-//           and one add:
-//             acc += max(|x_r - x_c|, 0)
+//           while this one is compared) -- per row and pair of columns one
+//           packed add, two maxes and one packed add:
+//             acc += max(|x_c + (-x_r)|, 0)
+//           (|x_c - x_r| = |x_r - x_c| exactly: binary32 subtraction is
+//           antisymmetric)
 //           max(NaN, 0) is 0, so a row either lane does not cover adds +0,
 //           which leaves a non-negative sum unchanged: the sum is the
 //           definition's sum over the common rows in row order.  Pairs with
@@ -219,9 +221,9 @@ lane_mask_kernel(const float* __restrict__ xs, const uint32_t* __restrict__ span
     };
     if (cA < cB) stage(0, cA);
     const int i = rbase + r;
-    float xr[LN_ROWS];
+    float nxr[LN_ROWS];  // the row lane's x, negated (NaN stays NaN)
 #pragma unroll
-    for (int k = 0; k < LN_ROWS; ++k) xr[k] = xs[static_cast<int64_t>(k) * ld + i];
+    for (int k = 0; k < LN_ROWS; ++k) nxr[k] = -xs[static_cast<int64_t>(k) * ld + i];
     const uint32_t sr = span[i];
     const uint32_t fr = flag[i];
 #pragma unroll 1
@@ -239,16 +241,17 @@ lane_mask_kernel(const float* __restrict__ xs, const uint32_t* __restrict__ span
         const int c0 = q * LN_QCOLS;
 #pragma unroll 1
         for (int g = 0; g < LN_QCOLS; g += 4) {
-            float acc0 = 0.0f, acc1 = 0.0f, acc2 = 0.0f, acc3 = 0.0f;
+            float2 a01 = make_float2(0.0f, 0.0f), a23 = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int k = 0; k < LN_ROWS; ++k) {
                 const float4 xc = *reinterpret_cast<const float4*>(&s_x[h][k][c0 + g]);
-                acc0 = __fadd_rn(acc0, fmaxf(fabsf(__fsub_rn(xr[k], xc.x)), 0.0f));
-                acc1 = __fadd_rn(acc1, fmaxf(fabsf(__fsub_rn(xr[k], xc.y)), 0.0f));
-                acc2 = __fadd_rn(acc2, fmaxf(fabsf(__fsub_rn(xr[k], xc.z)), 0.0f));
-                acc3 = __fadd_rn(acc3, fmaxf(fabsf(__fsub_rn(xr[k], xc.w)), 0.0f));
+                const float2 nr = make_float2(nxr[k], nxr[k]);
+                const float2 d01 = __fadd2_rn(make_float2(xc.x, xc.y), nr);  // x_c - x_r, two lanes
+                const float2 d23 = __fadd2_rn(make_float2(xc.z, xc.w), nr);
+                a01 = __fadd2_rn(a01, make_float2(fmaxf(fabsf(d01.x), 0.0f), fmaxf(fabsf(d01.y), 0.0f)));
+                a23 = __fadd2_rn(a23, make_float2(fmaxf(fabsf(d23.x), 0.0f), fmaxf(fabsf(d23.y), 0.0f)));
             }
-            const float acc[4] = {acc0, acc1, acc2, acc3};
+            const float acc[4] = {a01.x, a01.y, a23.x, a23.y};
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int cl = c0 + g + u, j = cbase + cl;

@@ -169,6 +169,23 @@ def test_resolve_entries_reject_misaligned_pointers(lib):
     assert g.nms_resolve_mask_noalloc(FAKE + 8, 100, 0, 0, FAKE, FAKE, 0) == g.NMS_ERR_INVALID_ARG
 
 
+def test_workspace_sizes_grow_with_n(lib):
+    """A workspace sized for n serves every smaller call: the sizes never
+    shrink as n grows (the pair list's capacity, one CTA's pairs times a
+    factor up to 16384 boxes and the all-SM path's above, included), and
+    the lane workspace holds the prepass's planes and second list besides
+    the single-image regions."""
+    sizes = [1, 63, 64, 65, 1000, 3000, 8192, 8193, 16384, 16385, 32768, 65536]
+    for f, top in ((g.nms_workspace_size, 1 << 18), (g.nms_lane_workspace_size, g.NMS_LANE_MAX_N)):
+        prev = 0
+        for n in [x for x in sizes if x <= top]:
+            b = f(n)
+            assert b >= prev, (f.__name__, n)
+            prev = b
+    for n in (1000, 3000, 16384):
+        assert g.nms_lane_workspace_size(n) > g.nms_workspace_size(n)
+
+
 def test_lane_entry_validation(lib):
     ws = 1 << 20
     big = 1 << 40

@@ -62,6 +62,9 @@
 // the whole CTA after the walk.
 #include <climits>
 #include <cstddef>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "internal.h"
@@ -1561,6 +1564,38 @@ void launch_graph_prepass(const uint32_t* edges, const unsigned* ecount, unsigne
 
 size_t resolve_smem_bytes(int m_bound, int NB) { return resolve_layout(m_bound, NB).total; }
 
+// GR_CLUSTER when a cluster of that many resolve CTAs with `smem` bytes each
+// can be resident on the current device at all, else 1 (the kernel then runs
+// passes 0 and 1 in one CTA).  Asked once per device and size.
+unsigned resolve_cluster_size(size_t smem)
+{
+    static std::mutex mu;
+    static std::map<std::pair<int, size_t>, unsigned> known;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1u;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto it = known.find({dev, smem});
+    if (it != known.end()) return it->second;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(GR_CLUSTER);
+    cfg.blockDim = dim3(RV_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = GR_CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    const bool fits =
+        cudaOccupancyMaxActiveClusters(&clusters, resolve_single_kernel<false>, &cfg) == cudaSuccess && clusters >= 1;
+    cudaGetLastError();  // a refused query leaves no error behind
+    const unsigned c = fits ? static_cast<unsigned>(GR_CLUSTER) : 1u;
+    known[{dev, smem}] = c;
+    return c;
+}
+
 void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* rowbits, int NB,
                            uint32_t* edges, const unsigned* ecount, unsigned lcap,
                            const uint64_t* haspred, const int* m_dev, int m_bound, const int* perm,
@@ -1577,8 +1612,8 @@ void launch_resolve_single(const uint64_t* mask, int64_t ldw, const uint64_t* ro
                         smem);
     cudaLaunchConfig_t cfg{};
     // The box path with a pair list: a cluster of GR_CLUSTER CTAs (passes 0
-    // and 1 shared; CTA 0 does the rest).
-    const unsigned csize = edges && !pre ? GR_CLUSTER : 1u;
+    // and 1 shared; CTA 0 does the rest) where the device can hold one.
+    const unsigned csize = edges && !pre ? resolve_cluster_size(smem) : 1u;
     cfg.gridDim = dim3(csize);
     cfg.blockDim = dim3(RV_THREADS);
     cfg.dynamicSmemBytes = smem;

@@ -276,7 +276,7 @@ __host__ __device__ __forceinline__ ResolveLayout resolve_layout(int m_bound, in
 // ---------------------------------------------------------------- graph path
 constexpr int GR_SMEM = 200 * 1024;   // shared bytes the graph path may take
 constexpr int GR_MAX_N = 65536;       // a pair packs two 16-bit sorted positions
-constexpr int GR_HEAD = 64;           // words: block-prefix scratch [0,32), copy barrier at 32
+constexpr int GR_HEAD = 64;           // words: block-prefix scratch [0,32), barriers at 32 and 34, counts 36..38
 constexpr int GR_COPY = 32 * 1024;    // bytes per bulk copy of the pair list
 
 // 32-bit bitmap words for m_bound boxes, rounded up to a multiple of 4 so the
@@ -546,10 +546,11 @@ __device__ __forceinline__ int global_passes(uint32_t* __restrict__ gedges, unsi
 // owner merges holds at least the owner's removals, and every bit is a
 // removal of pass 0, so the merged planes are all the same).  Pass 1 reads
 // the full plane, blocks its targets in CTA 0 and gathers the pairs left at
-// CTA 0's Es2 (one reservation per CTA on the count at word 36 of CTA 0).  gave_up: this
-// CTA's copy did not arrive (word 37 of CTA 0 is raised).  Every CTA takes
-// the three cluster barriers (the first arrived at by the caller).  Returns
-// whether this is CTA 0, which goes on with the rounds from pass 2.
+// CTA 0's Es2 (one reservation per CTA on the count at word 36 of CTA 0).
+// gave_up: this CTA's copy did not arrive (word 37 of CTA 0 is raised).
+// Every CTA takes the three cluster barriers (the first arrived at by the
+// caller).  Returns whether this is CTA 0, which goes on with the rounds
+// from pass 2.
 __device__ __forceinline__ bool graph_cluster_prologue(uint32_t* Es, unsigned Eloc, bool gave_up, uint8_t* FL,
                                                        uint8_t* RMb, int NWp, uint32_t* Es2, uint32_t* sm,
                                                        unsigned C, unsigned crank)
@@ -620,9 +621,11 @@ __device__ __forceinline__ bool graph_cluster_prologue(uint32_t* Es, unsigned El
 // rounds outnumber the walk's tiles plus 16 (a long chain of dependencies:
 // the walk is then the faster way).
 //
-// Shared layout: scratch and the copy barrier (GR_HEAD words), then one byte
-// per box holding the last pass that blocked it (plus 2, mod 256), then one
-// "removed" byte per box, then the live pairs.  Byte planes keep a warp's
+// Shared layout: the head of GR_HEAD words (block-prefix scratch at [0, 32),
+// the copy barrier at 32, the permutation's own barrier at 34 and the
+// cluster's counts at 36..38), then one byte per box holding the last pass
+// that blocked it (plus 2, mod 256), then one "removed" byte per box, then
+// the live pairs.  Byte planes keep a warp's
 // stores conflict-free: its pairs come from one 128-column tile of the mask,
 // so their targets are 128 consecutive bytes.  Each warp owns an equal
 // contiguous share of the list and compacts it in place.
